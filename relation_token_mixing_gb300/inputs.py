@@ -1,0 +1,77 @@
+"""Seeded synthetic inputs shared by the oracle-side and GPU-side tests and the benchmark.
+
+This module holds no arithmetic of the Relation operator: it only draws
+Gaussian tensors from a fixed seed, scales them, and rounds them to the
+requested storage dtype.  Both sides of a parity check get the same rounded
+tensors (the oracle upcasts them exactly to float64).
+
+Recipe (workloads of the paper's models: head width 48-128, T 128-16384,
+B*H independent heads): tensors are [B, H, T, d], drawn in float32 on the CPU
+with ``torch.Generator().manual_seed(seed)`` and ``torch.randn``, multiplied by
+``scale``, then rounded to nearest-even bf16 when dtype is bf16.  Default seeds
+42/43/44/45 for P1/P2/V/dY (42 is the first of the paper's paired seeds).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import torch
+
+SEEDS = {"P1": 42, "P2": 43, "V": 44, "dY": 45}
+
+
+@dataclass(frozen=True)
+class Workload:
+    """One synthetic workload: shapes, dtype, Self temperature, count coefficient."""
+
+    name: str
+    B: int
+    H: int
+    T: int
+    d: int
+    dtype: torch.dtype
+    tau_S: float
+    lam: float
+    causal: bool = True
+    p_scale: float = 1.0  # multiplies P1 and P2
+    backward: bool = False
+    seeds: dict = field(default_factory=lambda: dict(SEEDS))
+
+
+def gaussian(shape, seed: int, scale: float = 1.0, dtype: torch.dtype = torch.float32) -> torch.Tensor:
+    g = torch.Generator().manual_seed(int(seed))
+    x = torch.randn(*shape, generator=g, dtype=torch.float32)
+    if scale != 1.0:
+        x = x * scale
+    return x.to(dtype)
+
+
+def make(w: Workload, with_dy: bool | None = None) -> dict:
+    """CPU tensors P1, P2, V (and dY when backward) for workload ``w``."""
+    shape = (w.B, w.H, w.T, w.d)
+    out = {
+        "P1": gaussian(shape, w.seeds["P1"], w.p_scale, w.dtype),
+        "P2": gaussian(shape, w.seeds["P2"], w.p_scale, w.dtype),
+        "V": gaussian(shape, w.seeds["V"], 1.0, w.dtype),
+    }
+    if with_dy if with_dy is not None else w.backward:
+        out["dY"] = gaussian(shape, w.seeds["dY"], 1.0, w.dtype)
+    return out
+
+
+# The five workloads: single-head fp32 (T=128, d=64); the 10M-decoder forward
+# (B8 H8 T1024 d64); the large-|U| forward (P1,P2 ~ N(0,1) * 3 / d^(1/4), tau 0.5);
+# forward+backward at B8 H12 T2048 d64; long context B1 H32 T16384 d128.
+# lambda = 0.5 is the paper's initial value of the per-layer count coefficient.
+WORKLOADS = {
+    "single_head_fp32": Workload("single_head_fp32", 1, 1, 128, 64, torch.float32, 1.0, 0.5),
+    "mhr_fwd_T1024": Workload("mhr_fwd_T1024", 8, 8, 1024, 64, torch.bfloat16, 1.0, 0.5),
+    "mhr_fwd_T4096_large_u": Workload("mhr_fwd_T4096_large_u", 4, 16, 4096, 64, torch.bfloat16, 0.5, 0.5,
+                                      p_scale=3.0 / 64 ** 0.25),
+    "mhr_fwd_bwd_T2048": Workload("mhr_fwd_bwd_T2048", 8, 12, 2048, 64, torch.bfloat16, 1.0, 0.5, backward=True),
+    "mhr_fwd_bwd_T16384_d128": Workload("mhr_fwd_bwd_T16384_d128", 1, 32, 16384, 128, torch.bfloat16, 1.0, 0.5,
+                                        backward=True),
+    # The headline shape: the large-|U| forward workload run forward+backward.
+    "mhr_fwd_bwd_T4096": Workload("mhr_fwd_bwd_T4096", 4, 16, 4096, 64, torch.bfloat16, 0.5, 0.5,
+                                  p_scale=3.0 / 64 ** 0.25, backward=True),
+}
