@@ -1,0 +1,384 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused Full Relation forward + backward on GB300.
+
+One step = relation_fwd + relation_bwd (prepare, main, finish) over one batch
+of seeded synthetic bf16 inputs already resident in HBM.  Default workload:
+causal, B=4, H=16, T=4096, d_h=64, tau_S=0.5, lambda=0.5, P1/P2 ~ N(0,1)*3/d^(1/4),
+V, dY ~ N(0,1).  Throughput counts algorithmic work: 4*d flops per visible
+pair forward, 8*d backward (the U recompute of the backward is not counted).
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the float64 CPU
+oracle instead on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="mhr_fwd_bwd_T4096")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def pairs(T: int, causal: bool) -> int:
+    return T * (T + 1) // 2 if causal else T * T
+
+
+def flops(w, per_pair: int) -> float:
+    return float(per_pair) * w.d * pairs(w.T, w.causal) * w.B * w.H
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["bf16_tflops"]), float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])), "measured"
+    return 1900.0, 1700.0, "fallback"
+
+
+def kernel_source_hash(names) -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "relation_token_mixing_gb300", "csrc")
+    for n in names:
+        with open(os.path.join(csrc, n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, source_hash: str):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the current source."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    e = rec.get(kernel)
+    if not e or e.get("source_hash") != source_hash:
+        return None
+    return e.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for k, n in enumerate(names):
+                if parts[5 + k].lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(w, target_s: float = 12.0):
+    """The float64 oracle (as it stands) on a bounded sample of the workload: a few heads, same T and d."""
+    import oracle
+    from relation_token_mixing_gb300 import inputs as rin
+
+    threads = oracle.threads()
+    heads = max(1, threads)
+    ws = rin.Workload(w.name, 1, heads, w.T, w.d, w.dtype, w.tau_S, w.lam, w.causal, w.p_scale, backward=True)
+    x = rin.make(ws)
+    t0 = time.perf_counter()
+    oracle.fwd(x["P1"], x["P2"], x["V"], ws.tau_S, ws.lam, ws.causal)
+    oracle.bwd(x["P1"], x["P2"], x["V"], x["dY"], ws.tau_S, ws.lam, ws.causal)
+    dt = time.perf_counter() - t0
+    value = flops(ws, 12) / dt / 1e12
+    return {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"fwd+bwd of B=1 H={heads} (of {w.B * w.H} heads) at T={w.T} d={w.d}, float64, {dt:.1f} s"}
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    from relation_token_mixing_gb300 import inputs as rin
+
+    threads = oracle.threads()
+    heads = max(1, threads)
+    ws = rin.Workload(w.name, 1, heads, w.T, w.d, w.dtype, w.tau_S, w.lam, w.causal, w.p_scale, backward=True)
+    x = rin.make(ws)
+
+    def step():
+        oracle.fwd(x["P1"], x["P2"], x["V"], ws.tau_S, ws.lam, ws.causal)
+        oracle.bwd(x["P1"], x["P2"], x["V"], x["dY"], ws.tau_S, ws.lam, ws.causal)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = flops(ws, 12) / dt / 1e12
+    sample = f"each step: fwd+bwd of B=1 H={heads} (of {w.B * w.H} heads) at T={w.T} d={w.d}, float64"
+    print(json.dumps({
+        "impl": "reference", "metric": "Relation fwd+bwd TFLOP/s (bf16, causal) and % of GB300 dense bf16 peak",
+        "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded Gaussian, bf16-rounded then upcast)",
+        "config": {"workload": w.name, "B": 1, "H": heads, "T": w.T, "d_h": w.d, "causal": w.causal,
+                   "tau_S": w.tau_S, "lambda": w.lam},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+    return 0
+
+
+def main():
+    args = parse()
+    from relation_token_mixing_gb300 import inputs as rin
+
+    w = rin.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    import torch
+    import torch.distributed as dist
+
+    from relation_token_mixing_gb300 import binding as rb
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    rb.load()
+
+    # Inputs: every rank processes its own copy of the workload (independent heads; weak scaling).
+    x_cpu = rin.make(w, with_dy=True)
+    x = {k: v.to(dev) for k, v in x_cpu.items()}
+    P1, P2, V, dY = x["P1"], x["P2"], x["V"], x["dY"]
+    prob = rb.problem_for(P1, w.tau_S, w.lam, w.causal)
+    Y = torch.empty_like(V)
+    L = torch.empty(P1.shape[:3], dtype=torch.float32, device=dev)
+    dP1, dP2, dV = torch.empty_like(P1), torch.empty_like(P2), torch.empty_like(V)
+    dlam = torch.empty(1, dtype=torch.float32, device=dev)
+    ws = torch.empty((rb.relation_bwd_workspace_bytes(prob) + 3) // 4, dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    launches = [0]
+
+    def step(events=None):
+        if events:
+            events[0].record(stream)
+        rb.relation_fwd(prob, P1, P2, V, Y, L, stream)
+        launches[0] += rb.relation_last_launch_count()
+        if events:
+            events[1].record(stream)
+        args_b = (prob, P1, P2, V, Y, L, dY, dP1, dP2, dV, dlam, ws, stream)
+        rb.relation_bwd_prepare(*args_b)
+        launches[0] += rb.relation_last_launch_count()
+        if events:
+            events[2].record(stream)
+        rb.relation_bwd_main(*args_b)
+        launches[0] += rb.relation_last_launch_count()
+        if events:
+            events[3].record(stream)
+        rb.relation_bwd_finish(*args_b)
+        launches[0] += rb.relation_last_launch_count()
+        if events:
+            events[4].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if rb.relation_check_device_status() != 0:
+        raise RuntimeError("device-side wait expired during warm-up")
+
+    ev_sets = [[ev() for _ in range(5)] for _ in range(args.steps)]
+    launches[0] = 0
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        for k in range(args.steps):
+            flush.zero_()  # evict L2 between timed steps (outside the events)
+            step(ev_sets[k])
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    if rb.relation_check_device_status() != 0:
+        raise RuntimeError("device-side wait expired during the timed region")
+    timed_launches = launches[0]
+
+    t_step = [e[0].elapsed_time(e[4]) for e in ev_sets]
+    t_fwd = [e[0].elapsed_time(e[1]) for e in ev_sets]
+    t_prep = [e[1].elapsed_time(e[2]) for e in ev_sets]
+    t_main = [e[2].elapsed_time(e[3]) for e in ev_sets]
+    t_fin = [e[3].elapsed_time(e[4]) for e in ev_sets]
+    total_ms = sum(t_step)
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / args.steps
+    f_fwd, f_bwd = flops(w, 4), flops(w, 8)
+    value = world * (f_fwd + f_bwd) * args.steps / (total_ms * 1e-3) / 1e12
+    executed = world * flops(w, 14) * args.steps / (total_ms * 1e-3) / 1e12
+
+    # e2e: same step through the C ABI with host buffers (pinned), copies inside the timed region.
+    e2e = None
+    if not args.no_e2e:
+        h_in = {k: v.pin_memory() for k, v in x_cpu.items()}
+        h_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in (("Y", Y), ("dP1", dP1),
+                                                                                     ("dP2", dP2), ("dV", dV))}
+        h_lam = torch.empty(1, dtype=torch.float32).pin_memory()
+
+        def e2e_step():
+            P1.copy_(h_in["P1"], non_blocking=True)
+            P2.copy_(h_in["P2"], non_blocking=True)
+            V.copy_(h_in["V"], non_blocking=True)
+            dY.copy_(h_in["dY"], non_blocking=True)
+            step()
+            h_out["Y"].copy_(Y, non_blocking=True)
+            h_out["dP1"].copy_(dP1, non_blocking=True)
+            h_out["dP2"].copy_(dP2, non_blocking=True)
+            h_out["dV"].copy_(dV, non_blocking=True)
+            h_lam.copy_(dlam, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e_ms = 0.0
+        for _ in range(args.steps):
+            flush.zero_()
+            a, b = ev(), ev()
+            a.record(stream)
+            e2e_step()
+            b.record(stream)
+            b.synchronize()
+            e_ms += a.elapsed_time(b)
+        if world > 1:
+            tt = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e_ms = float(tt.item())
+        h2d = sum(v.numel() * v.element_size() for v in h_in.values())
+        d2h = sum(v.numel() * v.element_size() for v in h_out.values()) + 4
+        e2e = {"value": world * (f_fwd + f_bwd) * args.steps / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    peak_burst, peak_sust, peak_src = load_peaks()
+    mean_fwd, mean_main = statistics.mean(t_fwd), statistics.mean(t_main)
+    if mean_main >= mean_fwd:
+        dom, dom_ms, dom_flops, srcs = "relation_bwd_tc_kernel", mean_main, f_bwd, ["bwd_tc.cu", "ptx_sm100.cuh"]
+    else:
+        dom, dom_ms, dom_flops, srcs = "relation_fwd_tc_kernel", mean_fwd, f_fwd, ["fwd_tc.cu", "ptx_sm100.cuh"]
+    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
+    line = {
+        "metric": "Relation fwd+bwd TFLOP/s (bf16, causal) and % of GB300 dense bf16 peak",
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": max(3, args.warmup),
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded Gaussian inputs, resident in HBM)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d_h": w.d, "causal": w.causal,
+                   "tau_S": w.tau_S, "lambda": w.lam, "p_scale": round(w.p_scale, 6),
+                   "parallelism": f"independent heads, {world} replica(s)", "l2": "flushed between timed steps"},
+        "frac_of_peak": {"value": value / peak_burst, "peak_tflops": peak_burst, "source": peak_src,
+                         "sustained_frac": value / peak_sust},
+        "executed_tflops": executed,
+        "breakdown_ms": {"fwd": mean_fwd, "bwd_prepare": statistics.mean(t_prep), "bwd_main": mean_main,
+                         "bwd_finish": statistics.mean(t_fin)},
+        "roofline": {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak_burst, "unit": "TFLOP/s",
+                     "frac": achieved / peak_burst, "peak_source": f"{peak_src} bf16 burst",
+                     "traffic": recorded_traffic(dom, kernel_source_hash(srcs))},
+        "gpu_launches": timed_launches,
+        "e2e": e2e,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline and world == 1:
+        try:
+            line["cpu_baseline"] = cpu_baseline(w)
+        except Exception as exc:  # the baseline is context only; keep the GPU line
+            line["cpu_baseline"] = {"value": None, "unit": "TFLOP/s", "cores": None, "kind": "oracle",
+                                    "sample": f"failed: {exc}"}
+    print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,143 @@
+/*
+ * relation.h -- C ABI of the Full Relation operator on NVIDIA GB300 (sm_103a).
+ *
+ * The operator ("Ask Self, Ask Others: Relation Is All You Need",
+ * arXiv:2608.20172, Sec. 3.1 eq.(1)-(3), Appendix A.1.1), per head with
+ * P1, P2, V in R^{T x d_h} and one-based row index i:
+ *
+ *   U_ij = p1_i . p2_j / sqrt(d_h)                               eq.(1)
+ *   R_ii = sigmoid(U_ii / tau_S)                       (Self)     eq.(2)
+ *   R_ij = SiLU(U_ij) - lambda * log(c_i),  j != i     (Exchange) eq.(2)
+ *   R_ij = -inf for j > i when causal                  (mask)     eq.(2)
+ *   F_i  = Softmax(R_i),   Y_i = sum_j F_ij V_j                   eq.(3)
+ *
+ * c_i = i when causal (the paper's count correction "-lambda_l log i",
+ * Sec. 3.1 and Appendix A.1.5); c_i = T when non-causal (the paper defines
+ * only the causal operator; non-causal uses the visible-candidate count).
+ * V is the information state after Givens head mixing (I~ of eq.(4)-(5));
+ * P1 and P2 arrive already rotated by RoPE (Appendix B.3).
+ *
+ * Conventions shared by every entry point:
+ *  - Tensors are contiguous [B, H, T, d_h] (d_h innermost) in the problem's
+ *    dtype; L and the workspace are float32.  All tensor pointers are device
+ *    pointers owned by the caller; the library keeps no reference after a call
+ *    returns and allocates no device memory per call.
+ *  - Every tensor pointer must be 16-byte aligned (RELATION_ERR_MISALIGNED).
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and nothing synchronises.  Argument errors are reported before any
+ *    work is enqueued; launch failures return RELATION_ERR_CUDA.
+ *  - Device-side waits are bounded: if one expires the kernel records the
+ *    event in a library-owned device word and returns early;
+ *    relation_check_device_status() reports it after the caller synchronises.
+ *  - Supported: d_h in {64, 128}; dtype RELATION_BF16 (tensor-core path,
+ *    fp32 accumulation) or RELATION_F32 (fp32 CUDA-core path); any T >= 1;
+ *    causal or not.  Other sizes return RELATION_ERR_UNSUPPORTED.
+ *  - No entry point throws, aborts, or falls back to the CPU.
+ */
+#ifndef RELATION_GB300_RELATION_H_
+#define RELATION_GB300_RELATION_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define RELATION_ABI_VERSION 1
+
+typedef enum {
+    RELATION_OK = 0,
+    RELATION_ERR_INVALID_ARGUMENT = 1, /* bad size, NULL pointer, tau_S <= 0, aliasing */
+    RELATION_ERR_UNSUPPORTED = 2,      /* d_h or dtype this build has no kernel for */
+    RELATION_ERR_MISALIGNED = 3,       /* a tensor pointer is not 16-byte aligned */
+    RELATION_ERR_WORKSPACE_TOO_SMALL = 4,
+    RELATION_ERR_CUDA = 5,             /* a CUDA runtime call or launch failed */
+    RELATION_ERR_DEVICE_TIMEOUT = 6    /* a bounded device-side wait expired */
+} relation_status_t;
+
+typedef enum { RELATION_F32 = 0, RELATION_BF16 = 1 } relation_dtype_t;
+
+/* One operator invocation: B*H independent heads of length T and width d_h. */
+typedef struct {
+    int64_t B, H, T, d_h;
+    int32_t dtype;  /* relation_dtype_t */
+    float tau_S;    /* Self temperature, > 0 (eq.(2); the paper fixes 2) */
+    float lambda;   /* count-correction coefficient lambda_l (eq.(2); init 0.5); 0 disables it */
+    int32_t causal; /* nonzero: mask j > i as in eq.(2) */
+} relation_problem_t;
+
+/*
+ * Forward, eq.(1)-(3).  Reads P1, P2, V; writes Y [B,H,T,d_h] (dtype) and,
+ * when L is not NULL, L [B,H,T] float32 with L_i = log sum_j exp(R_ij) in the
+ * paper's convention (correction included).  The backward needs L.
+ * Y and L must not overlap any input.
+ */
+relation_status_t relation_fwd(const relation_problem_t* p, const void* P1, const void* P2,
+                               const void* V, void* Y, float* L, void* stream);
+
+/* Bytes of float32 workspace relation_bwd needs for problem p (0 if p is invalid). */
+size_t relation_bwd_workspace_bytes(const relation_problem_t* p);
+
+/*
+ * Backward of the forward above (the paper gives no backward; it is the chain
+ * rule of eq.(1)-(3)):
+ *   D_i = dY_i . Y_i,  dR_ij = F_ij (dY_i . V_j - D_i),
+ *   dU_ii = dR_ii S_i (1 - S_i) / tau_S,  dU_ij = dR_ij SiLU'(U_ij)  (j != i),
+ *   dP1 = dU P2 / sqrt(d_h),  dP2 = dU^T P1 / sqrt(d_h),  dV = F^T dY,
+ *   dlambda = -sum_i log(c_i) sum_{j != i} dR_ij.
+ * Inputs: P1, P2, V, the forward's Y and L, upstream dY.  Outputs dP1, dP2,
+ * dV [B,H,T,d_h] (dtype) are fully overwritten.  dlambda (device float, may
+ * be NULL) is overwritten with the gradient summed over all heads.
+ * workspace: device memory of at least relation_bwd_workspace_bytes(p) bytes,
+ * 16-byte aligned, owned by the caller, contents ignored on entry.  Outputs
+ * and workspace must not overlap each other or any input.
+ */
+relation_status_t relation_bwd(const relation_problem_t* p, const void* P1, const void* P2,
+                               const void* V, const void* Y, const float* L, const void* dY,
+                               void* dP1, void* dP2, void* dV, float* dlambda, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+/*
+ * The three stages relation_bwd runs in order, with the same arguments, for
+ * callers that time or schedule them separately.  prepare: D_i, dlambda and
+ * the dP1 accumulator reset.  main: the tensor-core (or fp32) pass producing
+ * dP2, dV and the dP1 partial sums.  finish: dP1 accumulator to dtype.
+ */
+relation_status_t relation_bwd_prepare(const relation_problem_t* p, const void* P1, const void* P2,
+                                       const void* V, const void* Y, const float* L,
+                                       const void* dY, void* dP1, void* dP2, void* dV,
+                                       float* dlambda, void* workspace, size_t workspace_bytes,
+                                       void* stream);
+relation_status_t relation_bwd_main(const relation_problem_t* p, const void* P1, const void* P2,
+                                    const void* V, const void* Y, const float* L, const void* dY,
+                                    void* dP1, void* dP2, void* dV, float* dlambda, void* workspace,
+                                    size_t workspace_bytes, void* stream);
+relation_status_t relation_bwd_finish(const relation_problem_t* p, const void* P1, const void* P2,
+                                      const void* V, const void* Y, const float* L,
+                                      const void* dY, void* dP1, void* dP2, void* dV,
+                                      float* dlambda, void* workspace, size_t workspace_bytes,
+                                      void* stream);
+
+/*
+ * Reads and clears the device status word of the current device.  Call after
+ * synchronising the streams used.  Returns RELATION_OK or
+ * RELATION_ERR_DEVICE_TIMEOUT (a bounded wait expired; outputs of the calls
+ * since the last check are invalid) or RELATION_ERR_CUDA.
+ */
+relation_status_t relation_check_device_status(void);
+
+/* Number of kernel launches the last successful call on this thread enqueued. */
+int relation_last_launch_count(void);
+
+/* Static description of a status code; never NULL. */
+const char* relation_status_string(relation_status_t s);
+
+/* RELATION_ABI_VERSION of the loaded library. */
+int relation_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RELATION_GB300_RELATION_H_ */

@@ -1,0 +1,210 @@
+"""Thin Python binding of the Relation C ABI (include/relation.h).
+
+The functions named like the C entry points (``relation_fwd``,
+``relation_bwd``, ...) marshal torch CUDA tensors into pointers and call the
+library; every step of the computation runs in the library's CUDA kernels.
+PyTorch provides device memory and streams only.  There is no fallback: if the
+library is missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+from . import build as _build
+
+RELATION_F32 = 0
+RELATION_BF16 = 1
+
+STATUS = {
+    0: "RELATION_OK",
+    1: "RELATION_ERR_INVALID_ARGUMENT",
+    2: "RELATION_ERR_UNSUPPORTED",
+    3: "RELATION_ERR_MISALIGNED",
+    4: "RELATION_ERR_WORKSPACE_TOO_SMALL",
+    5: "RELATION_ERR_CUDA",
+    6: "RELATION_ERR_DEVICE_TIMEOUT",
+}
+
+
+class RelationError(RuntimeError):
+    def __init__(self, code: int, what: str, message: str):
+        super().__init__(f"{what}: {STATUS.get(code, code)} ({message})")
+        self.code = code
+
+
+class Problem(ctypes.Structure):
+    """Mirror of relation_problem_t."""
+
+    _fields_ = [
+        ("B", ctypes.c_int64),
+        ("H", ctypes.c_int64),
+        ("T", ctypes.c_int64),
+        ("d_h", ctypes.c_int64),
+        ("dtype", ctypes.c_int32),
+        ("tau_S", ctypes.c_float),
+        ("lam", ctypes.c_float),
+        ("causal", ctypes.c_int32),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+
+_VP = ctypes.c_void_p
+_BWD_ARGTYPES = [ctypes.POINTER(Problem), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_size_t, _VP]
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Loads the in-tree library (building it first when missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if build_if_missing and not _build.up_to_date():
+            _build.build()
+        if not os.path.exists(_build.LIB):
+            raise RuntimeError(f"Relation CUDA library not built at {_build.LIB}")
+        lib = ctypes.CDLL(_build.LIB)
+        lib.relation_fwd.argtypes = [ctypes.POINTER(Problem), _VP, _VP, _VP, _VP, _VP, _VP]
+        lib.relation_fwd.restype = ctypes.c_int
+        for name in ("relation_bwd", "relation_bwd_prepare", "relation_bwd_main", "relation_bwd_finish"):
+            getattr(lib, name).argtypes = _BWD_ARGTYPES
+            getattr(lib, name).restype = ctypes.c_int
+        lib.relation_bwd_workspace_bytes.argtypes = [ctypes.POINTER(Problem)]
+        lib.relation_bwd_workspace_bytes.restype = ctypes.c_size_t
+        lib.relation_check_device_status.argtypes = []
+        lib.relation_check_device_status.restype = ctypes.c_int
+        lib.relation_last_launch_count.argtypes = []
+        lib.relation_last_launch_count.restype = ctypes.c_int
+        lib.relation_status_string.argtypes = [ctypes.c_int]
+        lib.relation_status_string.restype = ctypes.c_char_p
+        lib.relation_abi_version.argtypes = []
+        lib.relation_abi_version.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def declared_symbols() -> list[str]:
+    """Entry points declared in include/*.h."""
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    names = []
+    for fn in sorted(os.listdir(inc)):
+        if fn.endswith(".h"):
+            text = open(os.path.join(inc, fn)).read()
+            names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(relation_[a-z0-9_]+)\s*\(", text, re.M)
+    return sorted(set(names))
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("Relation tensors must be CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("Relation tensors must be contiguous [B, H, T, d_h]")
+    return t.data_ptr()
+
+
+def _stream_ptr(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream or None
+
+
+def _check(code: int, what: str) -> None:
+    if code != 0:
+        msg = load().relation_status_string(code).decode()
+        raise RelationError(code, what, msg)
+
+
+def problem_for(t: torch.Tensor, tau_S: float, lam: float, causal: bool) -> Problem:
+    if t.dim() != 4:
+        raise ValueError("expected [B, H, T, d_h] tensors")
+    if t.dtype == torch.bfloat16:
+        dt = RELATION_BF16
+    elif t.dtype == torch.float32:
+        dt = RELATION_F32
+    else:
+        raise ValueError(f"unsupported dtype {t.dtype}")
+    B, H, T, d = t.shape
+    return Problem(B, H, T, d, dt, float(tau_S), float(lam), 1 if causal else 0)
+
+
+# ------------------------------------------------------------------ C-ABI calls
+def relation_fwd(prob: Problem, P1, P2, V, Y, L=None, stream=None) -> None:
+    _check(load().relation_fwd(ctypes.byref(prob), _ptr(P1), _ptr(P2), _ptr(V), _ptr(Y), _ptr(L),
+                               _stream_ptr(stream)), "relation_fwd")
+
+
+def relation_bwd_workspace_bytes(prob: Problem) -> int:
+    return int(load().relation_bwd_workspace_bytes(ctypes.byref(prob)))
+
+
+def _bwd_call(name, prob, P1, P2, V, Y, L, dY, dP1, dP2, dV, dlambda, workspace, stream):
+    fn = getattr(load(), name)
+    _check(fn(ctypes.byref(prob), _ptr(P1), _ptr(P2), _ptr(V), _ptr(Y), _ptr(L), _ptr(dY), _ptr(dP1), _ptr(dP2),
+              _ptr(dV), _ptr(dlambda), _ptr(workspace), workspace.numel() * workspace.element_size(),
+              _stream_ptr(stream)), name)
+
+
+def relation_bwd(prob, P1, P2, V, Y, L, dY, dP1, dP2, dV, dlambda, workspace, stream=None) -> None:
+    _bwd_call("relation_bwd", prob, P1, P2, V, Y, L, dY, dP1, dP2, dV, dlambda, workspace, stream)
+
+
+def relation_bwd_prepare(prob, P1, P2, V, Y, L, dY, dP1, dP2, dV, dlambda, workspace, stream=None) -> None:
+    _bwd_call("relation_bwd_prepare", prob, P1, P2, V, Y, L, dY, dP1, dP2, dV, dlambda, workspace, stream)
+
+
+def relation_bwd_main(prob, P1, P2, V, Y, L, dY, dP1, dP2, dV, dlambda, workspace, stream=None) -> None:
+    _bwd_call("relation_bwd_main", prob, P1, P2, V, Y, L, dY, dP1, dP2, dV, dlambda, workspace, stream)
+
+
+def relation_bwd_finish(prob, P1, P2, V, Y, L, dY, dP1, dP2, dV, dlambda, workspace, stream=None) -> None:
+    _bwd_call("relation_bwd_finish", prob, P1, P2, V, Y, L, dY, dP1, dP2, dV, dlambda, workspace, stream)
+
+
+def relation_check_device_status() -> int:
+    return int(load().relation_check_device_status())
+
+
+def relation_last_launch_count() -> int:
+    return int(load().relation_last_launch_count())
+
+
+def relation_status_string(code: int) -> str:
+    return load().relation_status_string(code).decode()
+
+
+def relation_abi_version() -> int:
+    return int(load().relation_abi_version())
+
+
+# ------------------------------------------------------- tensor-level helpers
+def fwd(P1, P2, V, tau_S: float, lam: float, causal: bool = True, stream=None, want_L: bool = True):
+    """Allocates Y (and L) and runs relation_fwd; returns (Y, L)."""
+    prob = problem_for(P1, tau_S, lam, causal)
+    Y = torch.empty_like(V)
+    L = torch.empty(P1.shape[:3], dtype=torch.float32, device=P1.device) if want_L else None
+    relation_fwd(prob, P1, P2, V, Y, L, stream)
+    return Y, L
+
+
+def bwd(P1, P2, V, Y, L, dY, tau_S: float, lam: float, causal: bool = True, stream=None, workspace=None):
+    """Allocates the gradients and workspace and runs relation_bwd; returns (dP1, dP2, dV, dlambda)."""
+    prob = problem_for(P1, tau_S, lam, causal)
+    dP1, dP2, dV = torch.empty_like(P1), torch.empty_like(P2), torch.empty_like(V)
+    dlam = torch.empty(1, dtype=torch.float32, device=P1.device)
+    if workspace is None:
+        nbytes = relation_bwd_workspace_bytes(prob)
+        workspace = torch.empty((nbytes + 3) // 4, dtype=torch.float32, device=P1.device)
+    relation_bwd(prob, P1, P2, V, Y, L, dY, dP1, dP2, dV, dlam, workspace, stream)
+    return dP1, dP2, dV, dlam

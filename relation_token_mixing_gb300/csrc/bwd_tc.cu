@@ -1,0 +1,448 @@
+// Fused Full Relation backward on the sm_103a tensor cores (bf16 in, fp32 accumulate).
+//
+// The paper ("Ask Self, Ask Others: Relation Is All You Need") gives no
+// backward; this is the chain rule of Sec. 3.1 eq.(1)-(3), with the forward's
+// row log-normaliser L_i used to rebuild F_ij = exp(R_ij - L_i) block by block:
+//   dF_ij = dY_i . V_j,  dR_ij = F_ij (dF_ij - D_i),  D_i = dY_i . Y_i,
+//   dU_ii = dR_ii S_i (1 - S_i) / tau_S,  dU_ij = dR_ij SiLU'(U_ij),
+//   dP1 = dU P2 / sqrt(d),  dP2 = dU^T P1 / sqrt(d),  dV = F^T dY.
+//
+// One CTA = one head x one 128-row key tile j (rows of P2 and V); it walks the
+// query tiles i that can see it (i >= j when causal).
+//   warp 0      loader: P2_j, V_j once (TMA); per query tile P1_i, dY_i (TMA)
+//               and the per-query constants (L_i folded with lambda log c_i, D_i)
+//   warp 1      MMA issuer and TMEM owner
+//   warps 2-5   elementwise stage, one thread per key row
+//   warps 6-9   dP1 reduction: tensor memory -> fp32 accumulator in global memory
+// Per query tile, with everything transposed so that key rows sit on TMEM lanes:
+//   S^T  = P2_j P1_i^T          (SS)      dP^T = V_j dY_i^T    (SS)
+//   elementwise: P^T, dS^T = dU^T / sqrt(d) -> TMEM (bf16) and dS^T -> smem
+//   dV  += P^T dY_i             (TS)      dP2 += dS^T P1_i     (TS)
+//   dP1_i (partial) = dS P2_j   (SS, dS read MN-major from smem) -> fp32 atomics
+// TMEM: S^T [0,128) | dP^T [128,256) | dV | dP2 | dP1 partial (d = 64) — for
+// d = 128 the dP1 partial reuses the S^T columns.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "ptx_sm100.cuh"
+#include "tmap.h"
+
+namespace relation {
+namespace {
+
+constexpr int kTile = 128;
+constexpr int kThreads = 320;
+constexpr int kPanelBytes = 128 * 128;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BwdCfg {
+    static constexpr int kPanels = D / 64;
+    static constexpr int kTileBytes = kTile * D * 2;
+    static constexpr int kStages = (D == 64) ? 2 : 1;
+    static constexpr int kDsBytes = kTile * kTile * 2;
+    // TMEM column map.
+    static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+    static constexpr uint32_t kColDQ = (D == 64) ? 256 + 2 * D : 0;
+    static constexpr bool kDqAliasesS = (D != 64);
+    // alignment slack, tiles, dS^T, per-query constants, barriers, 16 KB guard band
+    static constexpr int kSmemBytes =
+        1024 + 2 * kTileBytes + kStages * 2 * kTileBytes + kDsBytes + kStages * 2 * kTile * 4 + 256 + 16384;
+};
+
+struct BwdBarriers {
+    uint64_t kv_full;
+    uint64_t q_full[2];
+    uint64_t q_empty[2];
+    uint64_t s_full;
+    uint64_t p_full;
+    uint64_t dq_full;
+    uint64_t dq_free;
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+__device__ __forceinline__ float as_f(uint32_t u) { return __uint_as_float(u); }
+
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+    const uint64_t t0 = global_ns();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        if (global_ns() - t0 > RELATION_WAIT_LIMIT_NS) return;
+    }
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    relation_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_p1, const __grid_constant__ CUtensorMap tm_p2,
+                           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_dy,
+                           const KernelProblem kp, const float* __restrict__ L, const float* __restrict__ Dw,
+                           float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dP2,
+                           __nv_bfloat16* __restrict__ dV, unsigned int* status) {
+    using C = BwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sK = smem;                              // P2_j
+    uint8_t* sV = sK + C::kTileBytes;                // V_j
+    uint8_t* sQ = sV + C::kTileBytes;                // P1_i per stage
+    uint8_t* sG = sQ + C::kStages * C::kTileBytes;   // dY_i per stage
+    uint8_t* sDS = sG + C::kStages * C::kTileBytes;  // dS^T (bf16), [key row][query], MN-major for dS
+    float* sLt = reinterpret_cast<float*>(sDS + C::kDsBytes);  // per stage: 128 folded log2 normalisers
+    float* sDd = sLt + C::kStages * kTile;                      // per stage: 128 values of D
+    BwdBarriers* bars = reinterpret_cast<BwdBarriers*>(sDd + C::kStages * kTile);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.x;
+    const int jt = blockIdx.y;  // key tile; low tiles see the most query tiles
+    const int T = kp.T;
+    const int kv0 = jt * kTile;
+    const int nq_all = (T + kTile - 1) / kTile;
+    const int i_first = kp.causal ? jt : 0;
+    const int n_q = nq_all - i_first;
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(&bars->kv_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            ptx::mbar_init(&bars->q_full[s], 32);
+            ptx::mbar_init(&bars->q_empty[s], 1);
+        }
+        ptx::mbar_init(&bars->s_full, 1);
+        ptx::mbar_init(&bars->p_full, 128);
+        ptx::mbar_init(&bars->dq_full, 1);
+        ptx::mbar_init(&bars->dq_free, 128);
+        ptx::mbar_init(&bars->mma_done, 1);
+        bars->abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(&bars->tmem_base, 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+    volatile int* abort_flag = &bars->abort_flag;
+
+    if (warp == 0) {
+        // -------------------------------------------------------------- loader
+        if (lane == 0) {
+            ptx::tma_prefetch_desc(&tm_p1);
+            ptx::tma_prefetch_desc(&tm_p2);
+            ptx::tma_prefetch_desc(&tm_v);
+            ptx::tma_prefetch_desc(&tm_dy);
+            ptx::mbar_arrive_expect_tx(&bars->kv_full, 2 * C::kTileBytes);
+            for (int p = 0; p < C::kPanels; ++p) {
+                ptx::tma_load_3d(sK + p * kPanelBytes, &tm_p2, &bars->kv_full, p * 64, kv0, bh);
+                ptx::tma_load_3d(sV + p * kPanelBytes, &tm_v, &bars->kv_full, p * 64, kv0, bh);
+            }
+        }
+        int it = 0;
+        for (; it < n_q; ++it) {
+            const int s = it % C::kStages;
+            const int i = i_first + it;
+            if (it >= C::kStages &&
+                !ptx::mbar_wait_warp(&bars->q_empty[s], ((it / C::kStages) - 1) & 1, abort_flag, status,
+                                     kDevTimeoutEmpty))
+                break;
+            for (int c = lane; c < kTile; c += 32) {
+                const int q = i * kTile + c;
+                float lt = 0.f, dd = 0.f;
+                if (q < T) {
+                    const int count = kp.causal ? (q + 1) : T;
+                    lt = (L[(size_t)bh * T + q] + kp.lambda * logf((float)count)) * kLog2e;
+                    dd = Dw[(size_t)bh * T + q];
+                }
+                sLt[s * kTile + c] = lt;
+                sDd[s * kTile + c] = dd;
+            }
+            if (lane == 0) {
+                ptx::mbar_arrive_expect_tx(&bars->q_full[s], 2 * C::kTileBytes);
+                for (int p = 0; p < C::kPanels; ++p) {
+                    ptx::tma_load_3d(sQ + s * C::kTileBytes + p * kPanelBytes, &tm_p1, &bars->q_full[s], p * 64,
+                                     i * kTile, bh);
+                    ptx::tma_load_3d(sG + s * C::kTileBytes + p * kPanelBytes, &tm_dy, &bars->q_full[s], p * 64,
+                                     i * kTile, bh);
+                }
+            } else {
+                ptx::mbar_arrive(&bars->q_full[s]);
+            }
+        }
+        if (lane == 0 && *abort_flag) {
+            drain_wait(&bars->kv_full, 0);
+            for (int jj = max(0, it - C::kStages); jj < it; ++jj)
+                drain_wait(&bars->q_full[jj % C::kStages], (jj / C::kStages) & 1);
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t id_nn = ptx::idesc_bf16(kTile, kTile, false, false);  // S^T, dP^T
+            const uint32_t id_tb = ptx::idesc_bf16(kTile, D, false, true);       // dV, dP2 (B MN-major)
+            const uint32_t id_dq = ptx::idesc_bf16(kTile, D, true, true);        // dP1 (A, B MN-major)
+            const uint32_t ka = ptx::smem_u32(sK), va = ptx::smem_u32(sV), dsa = ptx::smem_u32(sDS);
+            bool ok = ptx::mbar_wait(&bars->kv_full, 0, abort_flag, status, kDevTimeoutFull);
+            for (int it = 0; ok && it < n_q; ++it) {
+                const int s = it % C::kStages;
+                const uint32_t qa = ptx::smem_u32(sQ + s * C::kTileBytes);
+                const uint32_t ga = ptx::smem_u32(sG + s * C::kTileBytes);
+                if (!ptx::mbar_wait(&bars->q_full[s], (it / C::kStages) & 1, abort_flag, status, kDevTimeoutFull)) {
+                    ok = false;
+                    break;
+                }
+                if (C::kDqAliasesS && it > 0 &&
+                    !ptx::mbar_wait(&bars->dq_free, (it - 1) & 1, abort_flag, status, kDevTimeoutMma)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks / 4) * kPanelBytes + (ks % 4) * 32;
+                    ptx::mma_ss(tmem + C::kColS, ptx::smem_desc(ka + off, 16, 1024, ptx::kSwizzle128B),
+                                ptx::smem_desc(qa + off, 16, 1024, ptx::kSwizzle128B), id_nn, ks > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks / 4) * kPanelBytes + (ks % 4) * 32;
+                    ptx::mma_ss(tmem + C::kColDP, ptx::smem_desc(va + off, 16, 1024, ptx::kSwizzle128B),
+                                ptx::smem_desc(ga + off, 16, 1024, ptx::kSwizzle128B), id_nn, ks > 0 ? 1u : 0u);
+                }
+                ptx::mma_commit(&bars->s_full);
+                if (!ptx::mbar_wait(&bars->p_full, it & 1, abort_flag, status, kDevTimeoutFull)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < kTile / 16; ++ks) {
+                    const uint64_t gdesc = ptx::smem_desc(ga + ks * 2048, kPanelBytes, 1024, ptx::kSwizzle128B);
+                    ptx::mma_ts(tmem + C::kColDV, tmem + C::kColS + ks * 8, gdesc, id_tb,
+                                (it > 0 || ks > 0) ? 1u : 0u);
+                }
+#pragma unroll
+                for (int ks = 0; ks < kTile / 16; ++ks) {
+                    const uint64_t qdesc = ptx::smem_desc(qa + ks * 2048, kPanelBytes, 1024, ptx::kSwizzle128B);
+                    ptx::mma_ts(tmem + C::kColDK, tmem + C::kColDP + ks * 8, qdesc, id_tb,
+                                (it > 0 || ks > 0) ? 1u : 0u);
+                }
+                if (!C::kDqAliasesS && it > 0 &&
+                    !ptx::mbar_wait(&bars->dq_free, (it - 1) & 1, abort_flag, status, kDevTimeoutMma)) {
+                    ok = false;
+                    break;
+                }
+#pragma unroll
+                for (int ks = 0; ks < kTile / 16; ++ks) {
+                    const uint64_t adesc = ptx::smem_desc(dsa + ks * 2048, kPanelBytes, 1024, ptx::kSwizzle128B);
+                    const uint64_t bdesc = ptx::smem_desc(ka + ks * 2048, kPanelBytes, 1024, ptx::kSwizzle128B);
+                    ptx::mma_ss(tmem + C::kColDQ, adesc, bdesc, id_dq, ks > 0 ? 1u : 0u);
+                }
+                ptx::mma_commit(&bars->dq_full);
+                ptx::mma_commit(&bars->q_empty[s]);
+            }
+            ptx::mma_commit(&bars->mma_done);
+            drain_wait(&bars->mma_done, 0);
+        }
+    } else if (warp < 6) {
+        // --------------------------------------------------- elementwise stage
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;  // key row within the tile
+        const int kv = kv0 + r;
+        const bool row_valid = kv < T;
+        const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+        const float c_half = 0.5f * kp.inv_sqrt_d;
+        const float c_diag = 0.5f * kp.inv_sqrt_d / kp.tau_S;
+        const float inv_tau = 1.f / kp.tau_S;
+        const float diag_corr = kp.lambda * logf((float)(kp.causal ? (kv + 1) : T));
+        bool ok = true;
+        for (int it = 0; ok && it < n_q; ++it) {
+            const int s = it % C::kStages;
+            const int i = i_first + it;
+            if (!ptx::mbar_wait_warp(&bars->s_full, it & 1, abort_flag, status, kDevTimeoutMma)) {
+                ok = false;
+                break;
+            }
+            // q_full of this stage has completed (the MMA waited on it before S^T).
+            ptx::tc_fence_after();
+            const float* lt = sLt + s * kTile;
+            const float* dd = sDd + s * kTile;
+            const bool diag_tile = (i == jt);
+            const int qlimit = T - i * kTile;  // query columns c < qlimit exist
+            const bool special = diag_tile || qlimit < kTile || !row_valid;
+            uint8_t* ds_row = sDS + r * 128;
+#pragma unroll
+            for (int qq = 0; qq < 8; ++qq) {
+                uint32_t sv[16], gv[16];
+                tmem_ld16(lane_addr + C::kColS + 16 * qq, sv);
+                tmem_ld16(lane_addr + C::kColDP + 16 * qq, gv);
+                ptx::tmem_ld_wait();
+                ptx::pin_regs(sv);
+                ptx::pin_regs(gv);
+                uint32_t pp[8], dp[8];
+#pragma unroll
+                for (int k2 = 0; k2 < 8; ++k2) {
+                    float pv[2], dv[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int c = 16 * qq + 2 * k2 + h;
+                        const float a = as_f(sv[2 * k2 + h]);
+                        float x, slope;
+                        if (special && diag_tile && c == r) {
+                            const float sg = 0.5f + 0.5f * ptx::tanh_approx(a * c_diag);
+                            x = (sg + diag_corr) * kLog2e;
+                            slope = sg * (1.f - sg) * inv_tau;
+                        } else {
+                            const float hh = a * c_half;
+                            const float sg = 0.5f + 0.5f * ptx::tanh_approx(hh);
+                            const float u = 2.f * hh;
+                            x = u * sg * kLog2e;
+                            slope = fmaf(u * sg, 1.f - sg, sg);
+                        }
+                        float p = ptx::ex2_approx(x - lt[c]);
+                        if (special && (c >= qlimit || (kp.causal && diag_tile && c < r) || !row_valid)) p = 0.f;
+                        const float dR = p * (as_f(gv[2 * k2 + h]) - dd[c]);
+                        pv[h] = p;
+                        dv[h] = dR * slope * kp.inv_sqrt_d;
+                    }
+                    pp[k2] = ptx::pack_bf16x2(pv[0], pv[1]);
+                    dp[k2] = ptx::pack_bf16x2(dv[0], dv[1]);
+                }
+                // P^T -> TMEM over S^T columns [8qq, 8qq+8) (already read), dS^T likewise over dP^T.
+                asm volatile(
+                    "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
+                        lane_addr + C::kColS + 8 * qq),
+                    "r"(pp[0]), "r"(pp[1]), "r"(pp[2]), "r"(pp[3]), "r"(pp[4]), "r"(pp[5]), "r"(pp[6]), "r"(pp[7])
+                    : "memory");
+                asm volatile(
+                    "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
+                        lane_addr + C::kColDP + 8 * qq),
+                    "r"(dp[0]), "r"(dp[1]), "r"(dp[2]), "r"(dp[3]), "r"(dp[4]), "r"(dp[5]), "r"(dp[6]), "r"(dp[7])
+                    : "memory");
+                // dS^T row r, queries 16qq..16qq+15: two 16-byte chunks of the
+                // 128-byte swizzled row in panel qq/4.
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int chunk = (2 * qq + h) & 7;
+                    const int panel = (2 * qq + h) >> 3;
+                    uint4* dst = reinterpret_cast<uint4*>(ds_row + panel * kPanelBytes + ((chunk ^ (r & 7)) << 4));
+                    *dst = make_uint4(dp[4 * h], dp[4 * h + 1], dp[4 * h + 2], dp[4 * h + 3]);
+                }
+            }
+            ptx::tmem_st_wait();
+            fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&bars->p_full);
+        }
+        // Epilogue: dV and dP2 rows of this key tile.
+        if (ok && ptx::mbar_wait_warp(&bars->mma_done, 0, abort_flag, status, kDevTimeoutMma)) {
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                __nv_bfloat16* dst_row = (which == 0 ? dV : dP2) + ((size_t)bh * T + kv) * D;
+                const uint32_t col = which == 0 ? C::kColDV : C::kColDK;
+#pragma unroll
+                for (int c0 = 0; c0 < D / 32; ++c0) {
+                    uint32_t ov[32];
+                    ptx::tmem_ld32(lane_addr + col + 32 * c0, ov);
+                    ptx::tmem_ld_wait();
+                    ptx::pin_regs(ov);
+                    if (row_valid) {
+                        uint4* dst = reinterpret_cast<uint4*>(dst_row + 32 * c0);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            dst[k] = make_uint4(ptx::pack_bf16x2(as_f(ov[8 * k + 0]), as_f(ov[8 * k + 1])),
+                                                ptx::pack_bf16x2(as_f(ov[8 * k + 2]), as_f(ov[8 * k + 3])),
+                                                ptx::pack_bf16x2(as_f(ov[8 * k + 4]), as_f(ov[8 * k + 5])),
+                                                ptx::pack_bf16x2(as_f(ov[8 * k + 6]), as_f(ov[8 * k + 7])));
+                    }
+                }
+            }
+        }
+    } else {
+        // -------------------------------------------------- dP1 partial reduce
+        const int quarter = warp & 3;
+        const int rq = quarter * 32 + lane;  // query row within the tile
+        const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+        for (int it = 0; it < n_q; ++it) {
+            const int i = i_first + it;
+            if (!ptx::mbar_wait_warp(&bars->dq_full, it & 1, abort_flag, status, kDevTimeoutMma)) break;
+            ptx::tc_fence_after();
+            const int q = i * kTile + rq;
+            float4* dst = reinterpret_cast<float4*>(dq_acc + ((size_t)bh * T + q) * D);
+#pragma unroll
+            for (int c0 = 0; c0 < D / 32; ++c0) {
+                uint32_t ov[32];
+                ptx::tmem_ld32(lane_addr + C::kColDQ + 32 * c0, ov);
+                ptx::tmem_ld_wait();
+                ptx::pin_regs(ov);
+                if (q < T) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        atomicAdd(dst + 8 * c0 + k,
+                                  make_float4(as_f(ov[4 * k]), as_f(ov[4 * k + 1]), as_f(ov[4 * k + 2]),
+                                              as_f(ov[4 * k + 3])));
+                }
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&bars->dq_free);
+        }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int D>
+cudaError_t launch_bwd_tc_d(const KernelProblem& kp, const void* P1, const void* P2, const void* V, const float* L,
+                            const float* Dw, const void* dY, float* dq_acc, void* dP2, void* dV, const TcLaunch& tl,
+                            cudaStream_t s) {
+    using C = BwdCfg<D>;
+    static_assert(C::kSmemBytes <= 232448, "shared memory budget");
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(relation_bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        C::kSmemBytes);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    CUtensorMap m1, m2, mv, mg;
+    const void* bases[4] = {P1, P2, V, dY};
+    CUtensorMap* maps[4] = {&m1, &m2, &mv, &mg};
+    for (int k = 0; k < 4; ++k) {
+        cudaError_t e = make_tensor_map_3d(maps[k], bases[k], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, kp.T, kp.BH,
+                                           64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (e != cudaSuccess) return e;
+    }
+    dim3 grid((unsigned)kp.BH, (unsigned)((kp.T + kTile - 1) / kTile));
+    relation_bwd_tc_kernel<D><<<grid, kThreads, C::kSmemBytes, s>>>(m1, m2, mv, mg, kp, L, Dw, dq_acc,
+                                                                     (__nv_bfloat16*)dP2, (__nv_bfloat16*)dV,
+                                                                     tl.status);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_tc(const KernelProblem& kp, const void* P1, const void* P2, const void* V, const float* L,
+                          const float* Dw, const void* dY, float* dq_acc, void* dP2, void* dV, const TcLaunch& tl,
+                          cudaStream_t s) {
+    if (kp.d == 64) return launch_bwd_tc_d<64>(kp, P1, P2, V, L, Dw, dY, dq_acc, dP2, dV, tl, s);
+    if (kp.d == 128) return launch_bwd_tc_d<128>(kp, P1, P2, V, L, Dw, dY, dq_acc, dP2, dV, tl, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace relation

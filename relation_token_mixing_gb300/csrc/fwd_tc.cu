@@ -1,0 +1,423 @@
+// Fused Full Relation forward on the sm_103a tensor cores (bf16 in, fp32 accumulate).
+//
+// Operator: "Ask Self, Ask Others: Relation Is All You Need", Sec. 3.1
+// eq.(1)-(3): U = P1 P2^T / sqrt(d), Self S_i = sigmoid(U_ii / tau_S) on the
+// diagonal, Exchange E_ij = SiLU(U_ij) - lambda log c_i off it, -inf above it
+// (causal), F = Softmax(R), Y = F V.  U, R and F are never stored: each
+// 128 x 128 block of U lives in tensor memory for one step of an online
+// softmax (the running max / sum scan of Sec. 5.1 eq.(12), applied to whole
+// rows of R rather than to the Exchange part only).
+//
+// Count correction: every off-diagonal entry of row i carries -lambda log c_i
+// and softmax is invariant to a per-row shift (Appendix A.1.5), so the kernel
+// adds +lambda log c_i to the diagonal entry instead and leaves off-diagonal
+// blocks as plain SiLU.  L is reported in the paper's convention.
+//
+// One CTA = one head x two 128-row query tiles (rows q_base .. q_base+255).
+//   warp 0      TMA producer: both Q tiles once, then K/V tiles through a ring
+//   warp 1      MMA issuer (one thread) and TMEM owner
+//   warps 2-5   softmax of query tile 0 (one thread per row)
+//   warps 6-9   softmax of query tile 1
+// TMEM (512 columns): S0 | S1 (128 fp32 columns each; P overwrites the first
+// 64 columns as packed bf16) | O0 | O1 (d columns each).
+// Per key tile j, per query tile t:  S_t = Q_t K_j^T (SS MMA) -> softmax ->
+// P_t -> O_t += P_t V_j (TS MMA, P read from TMEM).  The two query tiles
+// alternate so the tensor core works on one while the other is in softmax.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "ptx_sm100.cuh"
+#include "tmap.h"
+
+namespace relation {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBN = 128;
+constexpr int kThreads = 320;
+constexpr int kPanelBytes = 128 * 128;  // 128 rows x 64 bf16 (one 128-byte swizzle span)
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+// The running max is raised only when a block's max exceeds it by more than
+// this many powers of two; exact, since numerator and denominator share it.
+constexpr float kRescaleThreshold = 8.0f;
+
+template <int D>
+struct FwdCfg {
+    static constexpr int kPanels = D / 64;
+    static constexpr int kTileBytes = kBM * D * 2;
+    static constexpr int kStages = (D == 64) ? 4 : 2;
+    // 1 KB for 1024-byte alignment of the swizzled tiles, the tiles, the
+    // barriers, and a 16 KB guard band that keeps any descriptor walk past a
+    // tile's end inside the CTA's allocation.
+    static constexpr int kSmemBytes = 1024 + (2 + 2 * kStages) * kTileBytes + 256 + 16384;
+};
+
+struct FwdBarriers {
+    uint64_t q_full[2];
+    uint64_t k_full[4];
+    uint64_t v_full[4];
+    uint64_t kv_empty[4];
+    uint64_t s_full[2];
+    uint64_t p_full[2];
+    uint64_t o_done[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+__device__ __forceinline__ float as_f(uint32_t u) { return __uint_as_float(u); }
+__device__ __forceinline__ uint32_t as_u(float f) { return __float_as_uint(f); }
+
+// Bounded wait that ignores the abort flag; used only to drain in-flight work.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+    const uint64_t t0 = global_ns();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        if (global_ns() - t0 > RELATION_WAIT_LIMIT_NS) return;
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    relation_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_p1, const __grid_constant__ CUtensorMap tm_p2,
+                           const __grid_constant__ CUtensorMap tm_v, const KernelProblem kp,
+                           __nv_bfloat16* __restrict__ Y, float* __restrict__ L, unsigned int* status) {
+    using C = FwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sQ = smem;
+    uint8_t* sK = sQ + 2 * C::kTileBytes;
+    uint8_t* sV = sK + C::kStages * C::kTileBytes;
+    FwdBarriers* bars = reinterpret_cast<FwdBarriers*>(sV + C::kStages * C::kTileBytes);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.x;
+    const int pair = (int)gridDim.y - 1 - (int)blockIdx.y;  // heaviest (latest) query rows first
+    const int T = kp.T;
+    const int q_base = pair * 2 * kBM;
+    const int n_kv_all = (T + kBN - 1) / kBN;
+    int n_t[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int row0 = q_base + t * kBM;
+        n_t[t] = (row0 >= T) ? 0 : (kp.causal ? (row0 / kBN + 1) : n_kv_all);
+    }
+    const int n_max = max(n_t[0], n_t[1]);
+
+    if (threadIdx.x == 0) {
+        for (int t = 0; t < 2; ++t) {
+            ptx::mbar_init(&bars->q_full[t], 1);
+            ptx::mbar_init(&bars->s_full[t], 1);
+            ptx::mbar_init(&bars->p_full[t], 128);
+            ptx::mbar_init(&bars->o_done[t], 1);
+        }
+        for (int s = 0; s < C::kStages; ++s) {
+            ptx::mbar_init(&bars->k_full[s], 1);
+            ptx::mbar_init(&bars->v_full[s], 1);
+            ptx::mbar_init(&bars->kv_empty[s], 1);
+        }
+        ptx::mbar_init(&bars->drain, 1);
+        bars->abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(&bars->tmem_base, 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+    volatile int* abort_flag = &bars->abort_flag;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            ptx::tma_prefetch_desc(&tm_p1);
+            ptx::tma_prefetch_desc(&tm_p2);
+            ptx::tma_prefetch_desc(&tm_v);
+            for (int t = 0; t < 2; ++t) {
+                if (n_t[t] == 0) continue;
+                ptx::mbar_arrive_expect_tx(&bars->q_full[t], C::kTileBytes);
+                for (int p = 0; p < C::kPanels; ++p)
+                    ptx::tma_load_3d(sQ + t * C::kTileBytes + p * kPanelBytes, &tm_p1, &bars->q_full[t], p * 64,
+                                     q_base + t * kBM, bh);
+            }
+            int j = 0;
+            for (; j < n_max; ++j) {
+                const int s = j % C::kStages;
+                if (j >= C::kStages &&
+                    !ptx::mbar_wait(&bars->kv_empty[s], ((j / C::kStages) - 1) & 1, abort_flag, status,
+                                    kDevTimeoutEmpty))
+                    break;
+                ptx::mbar_arrive_expect_tx(&bars->k_full[s], C::kTileBytes);
+                for (int p = 0; p < C::kPanels; ++p)
+                    ptx::tma_load_3d(sK + s * C::kTileBytes + p * kPanelBytes, &tm_p2, &bars->k_full[s], p * 64,
+                                     j * kBN, bh);
+                ptx::mbar_arrive_expect_tx(&bars->v_full[s], C::kTileBytes);
+                for (int p = 0; p < C::kPanels; ++p)
+                    ptx::tma_load_3d(sV + s * C::kTileBytes + p * kPanelBytes, &tm_v, &bars->v_full[s], p * 64,
+                                     j * kBN, bh);
+            }
+            if (*abort_flag) {
+                // Let the copies already issued land before the CTA exits.
+                for (int jj = max(0, j - C::kStages); jj < j; ++jj) {
+                    const int s = jj % C::kStages;
+                    drain_wait(&bars->k_full[s], (jj / C::kStages) & 1);
+                    drain_wait(&bars->v_full[s], (jj / C::kStages) & 1);
+                }
+                for (int t = 0; t < 2; ++t)
+                    if (n_t[t] > 0) drain_wait(&bars->q_full[t], 0);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t id_s = ptx::idesc_bf16(kBM, kBN, false, false);
+            const uint32_t id_o = ptx::idesc_bf16(kBM, D, false, true);
+            auto issue_s = [&](int t, int s) {
+                const uint32_t qa = ptx::smem_u32(sQ + t * C::kTileBytes);
+                const uint32_t ka = ptx::smem_u32(sK + s * C::kTileBytes);
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks / 4) * kPanelBytes + (ks % 4) * 32;
+                    ptx::mma_ss(tmem + t * 128, ptx::smem_desc(qa + off, 16, 1024, ptx::kSwizzle128B),
+                                ptx::smem_desc(ka + off, 16, 1024, ptx::kSwizzle128B), id_s, ks > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_pv = [&](int t, int s, bool accumulate) {
+                const uint32_t va = ptx::smem_u32(sV + s * C::kTileBytes);
+#pragma unroll
+                for (int ks = 0; ks < kBN / 16; ++ks) {
+                    ptx::mma_ts(tmem + 256 + t * D, tmem + t * 128 + ks * 8,
+                                ptx::smem_desc(va + ks * 2048, kPanelBytes, 1024, ptx::kSwizzle128B), id_o,
+                                (accumulate || ks > 0) ? 1u : 0u);
+                }
+            };
+            bool ok = true;
+            for (int t = 0; t < 2 && ok; ++t)
+                if (n_t[t] > 0) ok = ptx::mbar_wait(&bars->q_full[t], 0, abort_flag, status, kDevTimeoutFull);
+            if (ok && n_max > 0) ok = ptx::mbar_wait(&bars->k_full[0], 0, abort_flag, status, kDevTimeoutFull);
+            if (ok) {
+                ptx::tc_fence_after();
+                for (int t = 0; t < 2; ++t) {
+                    if (n_t[t] == 0) continue;
+                    issue_s(t, 0);
+                    ptx::mma_commit(&bars->s_full[t]);
+                }
+            }
+            for (int j = 0; ok && j < n_max; ++j) {
+                const int s = j % C::kStages;
+                const int s1 = (j + 1) % C::kStages;
+                bool v_ready = false, k_next_ready = false;
+                for (int t = 0; t < 2; ++t) {
+                    if (j >= n_t[t]) continue;
+                    if (!ptx::mbar_wait(&bars->p_full[t], j & 1, abort_flag, status, kDevTimeoutFull)) {
+                        ok = false;
+                        break;
+                    }
+                    if (!v_ready) {
+                        if (!ptx::mbar_wait(&bars->v_full[s], (j / C::kStages) & 1, abort_flag, status,
+                                            kDevTimeoutFull)) {
+                            ok = false;
+                            break;
+                        }
+                        v_ready = true;
+                    }
+                    ptx::tc_fence_after();
+                    issue_pv(t, s, j > 0);
+                    ptx::mma_commit(&bars->o_done[t]);
+                    if (j + 1 < n_t[t]) {
+                        if (!k_next_ready) {
+                            if (!ptx::mbar_wait(&bars->k_full[s1], ((j + 1) / C::kStages) & 1, abort_flag, status,
+                                                kDevTimeoutFull)) {
+                                ok = false;
+                                break;
+                            }
+                            k_next_ready = true;
+                            ptx::tc_fence_after();
+                        }
+                        issue_s(t, s1);
+                        ptx::mma_commit(&bars->s_full[t]);
+                    }
+                }
+                if (ok) ptx::mma_commit(&bars->kv_empty[s]);
+            }
+            ptx::mma_commit(&bars->drain);
+            drain_wait(&bars->drain, 0);
+        }
+    } else {
+        // ------------------------------------------------------------- softmax
+        const int t = (warp - 2) >> 2;
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        const int i = q_base + t * kBM + r;
+        const int nt = n_t[t];
+        const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+        const uint32_t s_col = t * 128, o_col = 256 + t * D;
+        const float c_half = 0.5f * kp.inv_sqrt_d;         // U/2 per raw dot product
+        const float c_half_l2 = c_half * kLog2e;
+        const float c_diag = 0.5f * kp.inv_sqrt_d / kp.tau_S;  // U/(2 tau_S)
+        const int count = kp.causal ? (i + 1) : T;
+        const float corr = kp.lambda * logf((float)count);    // lambda log c_i
+        const int diag_tile = (q_base + t * kBM) / kBN;
+        const int tail_cols = T - (n_kv_all - 1) * kBN;
+        float m = -INFINITY, l = 0.f;
+        bool ok = nt > 0;
+        for (int j = 0; ok && j < nt; ++j) {
+            if (!ptx::mbar_wait_warp(&bars->s_full[t], j & 1, abort_flag, status, kDevTimeoutMma)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            uint32_t sv[128];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                ptx::tmem_ld32(lane_addr + s_col + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * c));
+            ptx::tmem_ld_wait();
+            ptx::pin_regs(sv);
+            // sv[c] becomes x_c = R'_ic * log2(e) in place (R' = R + lambda log c_i).
+            const bool is_diag = (j == diag_tile);
+            const int climit = (j == n_kv_all - 1) ? tail_cols : kBN;
+            if (!is_diag && climit == kBN) {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) {
+                    const float a = as_f(sv[c]);
+                    const float th = ptx::tanh_approx(a * c_half);
+                    const float hx = a * c_half_l2;
+                    sv[c] = as_u(fmaf(hx, th, hx));  // SiLU(U) * log2(e)
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) {
+                    const float a = as_f(sv[c]);
+                    float v;
+                    if (is_diag && c == r) {
+                        v = (0.5f + 0.5f * ptx::tanh_approx(a * c_diag) + corr) * kLog2e;
+                    } else if (c >= climit || (kp.causal && is_diag && c > r)) {
+                        v = -INFINITY;
+                    } else {
+                        const float th = ptx::tanh_approx(a * c_half);
+                        const float hx = a * c_half_l2;
+                        v = fmaf(hx, th, hx);
+                    }
+                    sv[c] = as_u(v);
+                }
+            }
+            float mt = as_f(sv[0]);
+#pragma unroll
+            for (int c = 1; c + 1 < 128; c += 2) mt = ptx::max3(mt, as_f(sv[c]), as_f(sv[c + 1]));
+            mt = fmaxf(mt, as_f(sv[127]));
+            const float m_new = fmaxf(m, mt);
+            const bool rescale = __any_sync(0xffffffffu, m_new > m + kRescaleThreshold);
+            float scale = 1.f;
+            if (rescale) {
+                scale = ptx::ex2_approx(m - m_new);  // 0 when m = -inf
+                l *= scale;
+                m = m_new;
+            }
+            uint32_t pk[2][32];
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                const float p0 = ptx::ex2_approx(as_f(sv[2 * c]) - m);
+                const float p1 = ptx::ex2_approx(as_f(sv[2 * c + 1]) - m);
+                l += p0 + p1;
+                pk[c >> 5][c & 31] = ptx::pack_bf16x2(p0, p1);
+            }
+            ptx::tmem_st32(lane_addr + s_col, pk[0]);
+            ptx::tmem_st32(lane_addr + s_col + 32, pk[1]);
+            if (rescale && j > 0) {
+                // O holds the sums of key blocks 0..j-1; rescale it once the
+                // transport MMA of block j-1 has landed.  Block j's MMA waits
+                // for p_full, which is signalled only after this.
+                if (!ptx::mbar_wait_warp(&bars->o_done[t], (j - 1) & 1, abort_flag, status, kDevTimeoutMma)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+#pragma unroll
+                for (int c0 = 0; c0 < D / 32; ++c0) {
+                    uint32_t ov[32];
+                    ptx::tmem_ld32(lane_addr + o_col + 32 * c0, ov);
+                    ptx::tmem_ld_wait();
+                    ptx::pin_regs(ov);
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) ov[k] = as_u(as_f(ov[k]) * scale);
+                    ptx::tmem_st32(lane_addr + o_col + 32 * c0, ov);
+                }
+            }
+            ptx::tmem_st_wait();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&bars->p_full[t]);
+        }
+        if (ok && nt > 0 && ptx::mbar_wait_warp(&bars->o_done[t], (nt - 1) & 1, abort_flag, status, kDevTimeoutMma)) {
+            ptx::tc_fence_after();
+            const float inv_l = 1.f / l;
+            __nv_bfloat16* yrow = Y + ((size_t)bh * T + i) * D;
+#pragma unroll
+            for (int c0 = 0; c0 < D / 32; ++c0) {
+                uint32_t ov[32];
+                ptx::tmem_ld32(lane_addr + o_col + 32 * c0, ov);
+                ptx::tmem_ld_wait();
+                ptx::pin_regs(ov);
+                if (i < T) {
+                    uint32_t pkd[16];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k)
+                        pkd[k] = ptx::pack_bf16x2(as_f(ov[2 * k]) * inv_l, as_f(ov[2 * k + 1]) * inv_l);
+                    uint4* dst = reinterpret_cast<uint4*>(yrow + 32 * c0);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        dst[k] = make_uint4(pkd[4 * k], pkd[4 * k + 1], pkd[4 * k + 2], pkd[4 * k + 3]);
+                }
+            }
+            if (L != nullptr && i < T) L[(size_t)bh * T + i] = (m + __log2f(l)) * kLn2 - corr;
+        }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int D>
+cudaError_t launch_fwd_tc_d(const KernelProblem& kp, const void* P1, const void* P2, const void* V, void* Y,
+                            float* L, const TcLaunch& tl, cudaStream_t s) {
+    using C = FwdCfg<D>;
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(relation_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        C::kSmemBytes);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    CUtensorMap m1, m2, mv;
+    cudaError_t e;
+    if ((e = make_tensor_map_3d(&m1, P1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, kp.T, kp.BH, 64, 128,
+                                CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+        return e;
+    if ((e = make_tensor_map_3d(&m2, P2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, kp.T, kp.BH, 64, 128,
+                                CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+        return e;
+    if ((e = make_tensor_map_3d(&mv, V, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, kp.T, kp.BH, 64, 128,
+                                CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+        return e;
+    const unsigned pairs = (unsigned)((kp.T + 2 * kBM - 1) / (2 * kBM));
+    dim3 grid((unsigned)kp.BH, pairs);
+    relation_fwd_tc_kernel<D><<<grid, kThreads, C::kSmemBytes, s>>>(m1, m2, mv, kp, (__nv_bfloat16*)Y, L, tl.status);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_tc(const KernelProblem& kp, const void* P1, const void* P2, const void* V, void* Y, float* L,
+                          const TcLaunch& tl, cudaStream_t s) {
+    if (kp.BH > 2147483647LL) return cudaErrorInvalidValue;
+    if (kp.d == 64) return launch_fwd_tc_d<64>(kp, P1, P2, V, Y, L, tl, s);
+    if (kp.d == 128) return launch_fwd_tc_d<128>(kp, P1, P2, V, Y, L, tl, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace relation

@@ -1,0 +1,35 @@
+// Internal launch functions of the Relation library (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace relation {
+
+// float32 CUDA-core path (also instantiated for bf16 storage).
+cudaError_t launch_fwd_simt(const KernelProblem& kp, bool bf16, const void* P1, const void* P2, const void* V,
+                            void* Y, float* L, cudaStream_t s);
+cudaError_t launch_bwd_simt(const KernelProblem& kp, bool bf16, const void* P1, const void* P2, const void* V,
+                            const float* L, const float* Dw, const void* dY, void* dP1, void* dP2, void* dV,
+                            cudaStream_t s);
+
+// Shared backward stages.
+cudaError_t launch_bwd_prepare(const KernelProblem& kp, bool bf16, const void* P1, const void* P2, const void* V,
+                               const void* Y, const float* L, const void* dY, float* Dw, float* dq_acc,
+                               float* dlambda, cudaStream_t s);
+cudaError_t launch_convert(const float* src, void* dst, bool bf16, int64_t n, int num_sms, cudaStream_t s);
+
+// Tensor-core (tcgen05) bf16 path.
+struct TcLaunch {
+    int num_sms;
+    unsigned int* status;
+};
+cudaError_t launch_fwd_tc(const KernelProblem& kp, const void* P1, const void* P2, const void* V, void* Y, float* L,
+                          const TcLaunch& tl, cudaStream_t s);
+cudaError_t launch_bwd_tc(const KernelProblem& kp, const void* P1, const void* P2, const void* V, const float* L,
+                          const float* Dw, const void* dY, float* dq_acc, void* dP2, void* dV, const TcLaunch& tl,
+                          cudaStream_t s);
+
+}  // namespace relation

@@ -1,0 +1,321 @@
+// Host side of the Relation C ABI (include/relation.h): argument checks,
+// kernel selection by dtype, launch bookkeeping and the device status word.
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/relation.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace relation {
+
+// One status word per device; kernels write it through a pointer obtained by
+// cudaGetSymbolAddress (the host-side symbol is not a device address).
+__device__ unsigned int g_device_status = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+unsigned int* g_status_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+thread_local int t_last_launches = 0;
+
+struct DeviceInfo {
+    unsigned int* status;
+    int num_sms;
+};
+
+relation_status_t device_info(DeviceInfo* out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RELATION_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_status_ptr[dev] == nullptr) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_device_status) != cudaSuccess) return RELATION_ERR_CUDA;
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return RELATION_ERR_CUDA;
+        g_status_ptr[dev] = static_cast<unsigned int*>(ptr);
+        g_num_sms[dev] = sms;
+    }
+    out->status = g_status_ptr[dev];
+    out->num_sms = g_num_sms[dev];
+    return RELATION_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t elem_bytes(const relation_problem_t* p) { return p->dtype == RELATION_BF16 ? 2 : 4; }
+
+size_t tensor_bytes(const relation_problem_t* p) {
+    return (size_t)p->B * (size_t)p->H * (size_t)p->T * (size_t)p->d_h * elem_bytes(p);
+}
+
+size_t rows_of(const relation_problem_t* p) { return (size_t)p->B * (size_t)p->H * (size_t)p->T; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    if (a == nullptr || b == nullptr || na == 0 || nb == 0) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+// Problem checks shared by every entry point.
+relation_status_t check_problem(const relation_problem_t* p) {
+    if (p == nullptr) return RELATION_ERR_INVALID_ARGUMENT;
+    if (p->B < 1 || p->H < 1 || p->T < 1 || p->d_h < 1) return RELATION_ERR_INVALID_ARGUMENT;
+    if (p->T > (int64_t)INT32_MAX || p->B > (int64_t)INT32_MAX || p->H > (int64_t)INT32_MAX)
+        return RELATION_ERR_INVALID_ARGUMENT;
+    const double elems = (double)p->B * (double)p->H * (double)p->T * (double)p->d_h;
+    if (elems > 1.0e12) return RELATION_ERR_INVALID_ARGUMENT;
+    if (p->dtype != RELATION_F32 && p->dtype != RELATION_BF16) return RELATION_ERR_INVALID_ARGUMENT;
+    if (!(p->tau_S > 0.f) || !isfinite(p->tau_S) || !isfinite(p->lambda)) return RELATION_ERR_INVALID_ARGUMENT;
+    if (p->d_h != 64 && p->d_h != 128) return RELATION_ERR_UNSUPPORTED;
+    return RELATION_OK;
+}
+
+KernelProblem kernel_problem(const relation_problem_t* p) {
+    KernelProblem kp;
+    kp.BH = p->B * p->H;
+    kp.T = (int)p->T;
+    kp.d = (int)p->d_h;
+    kp.tau_S = p->tau_S;
+    kp.lambda = p->lambda;
+    kp.causal = p->causal ? 1 : 0;
+    kp.inv_sqrt_d = (float)(1.0 / sqrt((double)p->d_h));
+    return kp;
+}
+
+size_t workspace_layout(const relation_problem_t* p, size_t* dq_offset) {
+    const size_t d_bytes = round_up(rows_of(p) * sizeof(float), 256);
+    const size_t dq_bytes = p->dtype == RELATION_BF16 ? rows_of(p) * (size_t)p->d_h * sizeof(float) : 0;
+    if (dq_offset) *dq_offset = d_bytes;
+    return d_bytes + dq_bytes;
+}
+
+// The tensor-core path serves every bf16 problem.
+bool use_tensor_cores(const relation_problem_t* p) { return p->dtype == RELATION_BF16; }
+
+struct BwdArgs {
+    const relation_problem_t* p;
+    const void *P1, *P2, *V, *Y;
+    const float* L;
+    const void* dY;
+    void *dP1, *dP2, *dV;
+    float* dlambda;
+    void* workspace;
+    size_t workspace_bytes;
+    cudaStream_t stream;
+};
+
+relation_status_t check_bwd(const BwdArgs& a) {
+    relation_status_t st = check_problem(a.p);
+    if (st != RELATION_OK) return st;
+    const void* ins[] = {a.P1, a.P2, a.V, a.Y, a.L, a.dY};
+    void* outs[] = {a.dP1, a.dP2, a.dV};
+    for (const void* x : ins)
+        if (x == nullptr) return RELATION_ERR_INVALID_ARGUMENT;
+    for (void* x : outs)
+        if (x == nullptr) return RELATION_ERR_INVALID_ARGUMENT;
+    if (a.workspace == nullptr) return RELATION_ERR_INVALID_ARGUMENT;
+    for (const void* x : ins)
+        if (!aligned16(x)) return RELATION_ERR_MISALIGNED;
+    for (void* x : outs)
+        if (!aligned16(x)) return RELATION_ERR_MISALIGNED;
+    if (!aligned16(a.workspace)) return RELATION_ERR_MISALIGNED;
+    if (a.dlambda != nullptr && (reinterpret_cast<uintptr_t>(a.dlambda) & 3u)) return RELATION_ERR_MISALIGNED;
+    const size_t need = workspace_layout(a.p, nullptr);
+    if (a.workspace_bytes < need) return RELATION_ERR_WORKSPACE_TOO_SMALL;
+    const size_t tb = tensor_bytes(a.p), lb = rows_of(a.p) * sizeof(float);
+    const void* in_ptr[] = {a.P1, a.P2, a.V, a.Y, a.L, a.dY};
+    const size_t in_len[] = {tb, tb, tb, tb, lb, tb};
+    const void* out_ptr[] = {a.dP1, a.dP2, a.dV, a.workspace, a.dlambda};
+    const size_t out_len[] = {tb, tb, tb, need, a.dlambda ? sizeof(float) : 0};
+    for (int o = 0; o < 5; ++o) {
+        for (int i = 0; i < 6; ++i)
+            if (overlaps(out_ptr[o], out_len[o], in_ptr[i], in_len[i])) return RELATION_ERR_INVALID_ARGUMENT;
+        for (int o2 = o + 1; o2 < 5; ++o2)
+            if (overlaps(out_ptr[o], out_len[o], out_ptr[o2], out_len[o2])) return RELATION_ERR_INVALID_ARGUMENT;
+    }
+    return RELATION_OK;
+}
+
+relation_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? RELATION_OK : RELATION_ERR_CUDA; }
+
+relation_status_t run_prepare(const BwdArgs& a, int* launches) {
+    size_t dq_off = 0;
+    workspace_layout(a.p, &dq_off);
+    float* Dw = static_cast<float*>(a.workspace);
+    float* dq = use_tensor_cores(a.p) ? reinterpret_cast<float*>(static_cast<char*>(a.workspace) + dq_off) : nullptr;
+    if (a.dlambda != nullptr) {
+        if (cudaMemsetAsync(a.dlambda, 0, sizeof(float), a.stream) != cudaSuccess) return RELATION_ERR_CUDA;
+    }
+    const KernelProblem kp = kernel_problem(a.p);
+    relation_status_t st = from_cuda(launch_bwd_prepare(kp, a.p->dtype == RELATION_BF16, a.P1, a.P2, a.V, a.Y, a.L,
+                                                        a.dY, Dw, dq, a.dlambda, a.stream));
+    if (st == RELATION_OK) *launches += 1;
+    return st;
+}
+
+relation_status_t run_main(const BwdArgs& a, int* launches) {
+    size_t dq_off = 0;
+    workspace_layout(a.p, &dq_off);
+    const float* Dw = static_cast<const float*>(a.workspace);
+    const KernelProblem kp = kernel_problem(a.p);
+    if (use_tensor_cores(a.p)) {
+        DeviceInfo di;
+        relation_status_t st = device_info(&di);
+        if (st != RELATION_OK) return st;
+        float* dq = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + dq_off);
+        TcLaunch tl{di.num_sms, di.status};
+        st = from_cuda(launch_bwd_tc(kp, a.P1, a.P2, a.V, a.L, Dw, a.dY, dq, a.dP2, a.dV, tl, a.stream));
+        if (st == RELATION_OK) *launches += 1;
+        return st;
+    }
+    relation_status_t st = from_cuda(launch_bwd_simt(kp, false, a.P1, a.P2, a.V, a.L, Dw, a.dY, a.dP1, a.dP2, a.dV,
+                                                     a.stream));
+    if (st == RELATION_OK) *launches += 2;
+    return st;
+}
+
+relation_status_t run_finish(const BwdArgs& a, int* launches) {
+    if (!use_tensor_cores(a.p)) return RELATION_OK;  // the fp32 path writes dP1 directly
+    size_t dq_off = 0;
+    workspace_layout(a.p, &dq_off);
+    DeviceInfo di;
+    relation_status_t st = device_info(&di);
+    if (st != RELATION_OK) return st;
+    const float* dq = reinterpret_cast<const float*>(static_cast<const char*>(a.workspace) + dq_off);
+    st = from_cuda(launch_convert(dq, a.dP1, true, (int64_t)(rows_of(a.p) * (size_t)a.p->d_h), di.num_sms,
+                                  a.stream));
+    if (st == RELATION_OK) *launches += 1;
+    return st;
+}
+
+}  // namespace
+}  // namespace relation
+
+using namespace relation;
+
+extern "C" {
+
+relation_status_t relation_fwd(const relation_problem_t* p, const void* P1, const void* P2, const void* V, void* Y,
+                               float* L, void* stream) {
+    relation_status_t st = check_problem(p);
+    if (st != RELATION_OK) return st;
+    if (!P1 || !P2 || !V || !Y) return RELATION_ERR_INVALID_ARGUMENT;
+    if (!aligned16(P1) || !aligned16(P2) || !aligned16(V) || !aligned16(Y) || (L && !aligned16(L)))
+        return RELATION_ERR_MISALIGNED;
+    const size_t tb = tensor_bytes(p), lb = rows_of(p) * sizeof(float);
+    const void* ins[] = {P1, P2, V};
+    for (const void* x : ins) {
+        if (overlaps(Y, tb, x, tb)) return RELATION_ERR_INVALID_ARGUMENT;
+        if (L && overlaps(L, lb, x, tb)) return RELATION_ERR_INVALID_ARGUMENT;
+    }
+    if (L && overlaps(L, lb, Y, tb)) return RELATION_ERR_INVALID_ARGUMENT;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const KernelProblem kp = kernel_problem(p);
+    if (use_tensor_cores(p)) {
+        DeviceInfo di;
+        st = device_info(&di);
+        if (st != RELATION_OK) return st;
+        TcLaunch tl{di.num_sms, di.status};
+        st = from_cuda(launch_fwd_tc(kp, P1, P2, V, Y, L, tl, s));
+    } else {
+        st = from_cuda(launch_fwd_simt(kp, false, P1, P2, V, Y, L, s));
+    }
+    if (st == RELATION_OK) t_last_launches = 1;
+    return st;
+}
+
+size_t relation_bwd_workspace_bytes(const relation_problem_t* p) {
+    if (check_problem(p) != RELATION_OK) return 0;
+    return workspace_layout(p, nullptr);
+}
+
+#define RELATION_BWD_ARGS                                                                                     \
+    const relation_problem_t *p, const void *P1, const void *P2, const void *V, const void *Y, const float *L, \
+        const void *dY, void *dP1, void *dP2, void *dV, float *dlambda, void *workspace, size_t workspace_bytes, \
+        void *stream
+#define RELATION_BWD_PACK \
+    BwdArgs a{p, P1, P2, V, Y, L, dY, dP1, dP2, dV, dlambda, workspace, workspace_bytes, static_cast<cudaStream_t>(stream)}
+
+relation_status_t relation_bwd(RELATION_BWD_ARGS) {
+    RELATION_BWD_PACK;
+    relation_status_t st = check_bwd(a);
+    if (st != RELATION_OK) return st;
+    int launches = 0;
+    if ((st = run_prepare(a, &launches)) != RELATION_OK) return st;
+    if ((st = run_main(a, &launches)) != RELATION_OK) return st;
+    if ((st = run_finish(a, &launches)) != RELATION_OK) return st;
+    t_last_launches = launches;
+    return RELATION_OK;
+}
+
+relation_status_t relation_bwd_prepare(RELATION_BWD_ARGS) {
+    RELATION_BWD_PACK;
+    relation_status_t st = check_bwd(a);
+    if (st != RELATION_OK) return st;
+    int launches = 0;
+    st = run_prepare(a, &launches);
+    if (st == RELATION_OK) t_last_launches = launches;
+    return st;
+}
+
+relation_status_t relation_bwd_main(RELATION_BWD_ARGS) {
+    RELATION_BWD_PACK;
+    relation_status_t st = check_bwd(a);
+    if (st != RELATION_OK) return st;
+    int launches = 0;
+    st = run_main(a, &launches);
+    if (st == RELATION_OK) t_last_launches = launches;
+    return st;
+}
+
+relation_status_t relation_bwd_finish(RELATION_BWD_ARGS) {
+    RELATION_BWD_PACK;
+    relation_status_t st = check_bwd(a);
+    if (st != RELATION_OK) return st;
+    int launches = 0;
+    st = run_finish(a, &launches);
+    if (st == RELATION_OK) t_last_launches = launches;
+    return st;
+}
+
+relation_status_t relation_check_device_status(void) {
+    DeviceInfo di;
+    relation_status_t st = device_info(&di);
+    if (st != RELATION_OK) return st;
+    unsigned int word = 0;
+    if (cudaMemcpy(&word, di.status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return RELATION_ERR_CUDA;
+    if (word != 0) {
+        const unsigned int zero = 0;
+        if (cudaMemcpy(di.status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+            return RELATION_ERR_CUDA;
+        return RELATION_ERR_DEVICE_TIMEOUT;
+    }
+    return RELATION_OK;
+}
+
+int relation_last_launch_count(void) { return t_last_launches; }
+
+const char* relation_status_string(relation_status_t s) {
+    switch (s) {
+        case RELATION_OK: return "ok";
+        case RELATION_ERR_INVALID_ARGUMENT: return "invalid argument";
+        case RELATION_ERR_UNSUPPORTED: return "unsupported problem (d_h must be 64 or 128)";
+        case RELATION_ERR_MISALIGNED: return "tensor pointer not 16-byte aligned";
+        case RELATION_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than relation_bwd_workspace_bytes()";
+        case RELATION_ERR_CUDA: return "CUDA runtime error";
+        case RELATION_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait expired";
+    }
+    return "unknown status";
+}
+
+int relation_abi_version(void) { return RELATION_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,409 @@
+// CUDA-core kernels of the Relation library:
+//  - the float32 forward and backward (exact expf/logf arithmetic, fp32
+//    accumulation), used for RELATION_F32 problems;
+//  - the backward preparation (D_i, dlambda, dP1 accumulator reset) and the
+//    dP1 accumulator conversion, shared by both dtypes.
+//
+// Operator: "Ask Self, Ask Others: Relation Is All You Need", Sec. 3.1
+// eq.(1)-(3) (forward, with the -lambda log i count correction of eq.(2)); the
+// backward is the chain rule of those equations.  The forward uses the
+// online-softmax scan of Sec. 5.1 eq.(12) over every visible entry (Self
+// included), so U, R and F are never stored.
+//
+// Layout: four threads share one row; thread `part` owns columns
+// part, part+4, part+8, ... of d, so the four threads of a quad read four
+// distinct shared-memory banks when they all read one K/V row.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace relation {
+namespace {
+
+constexpr int kRows = 32;     // rows (queries or keys) per block
+constexpr int kTile = 32;     // rows of the streamed operand per shared-memory tile
+constexpr int kThreads = 128; // kRows * 4
+
+__device__ __forceinline__ float sigmoid_exact(float x) {
+    if (x >= 0.f) return 1.f / (1.f + expf(-x));
+    float e = expf(x);
+    return e / (1.f + e);
+}
+
+__device__ __forceinline__ float quad_sum(float v) {
+    v += __shfl_xor_sync(0xffffffffu, v, 1);
+    v += __shfl_xor_sync(0xffffffffu, v, 2);
+    return v;
+}
+
+// Count-correction term lambda * log(c_i) for zero-based row i.
+__device__ __forceinline__ float count_correction(const KernelProblem& kp, int i) {
+    const int c = kp.causal ? (i + 1) : kp.T;
+    return kp.lambda * logf((float)c);
+}
+
+template <typename Tin, int D>
+__device__ __forceinline__ void load_tile(float (*dst)[D], const Tin* src_head, int row0, int T) {
+    for (int e = threadIdx.x; e < kTile * D; e += kThreads) {
+        const int rr = e / D, cc = e % D;
+        const int row = row0 + rr;
+        dst[rr][cc] = (row < T) ? load_as_float(src_head + (int64_t)row * D + cc) : 0.f;
+    }
+}
+
+// ------------------------------------------------------------------ forward
+template <typename Tin, int D>
+__global__ void __launch_bounds__(kThreads) fwd_simt_kernel(KernelProblem kp, const Tin* __restrict__ P1,
+                                                            const Tin* __restrict__ P2,
+                                                            const Tin* __restrict__ V, Tin* __restrict__ Y,
+                                                            float* __restrict__ L) {
+    constexpr int S = D / 4;
+    __shared__ float sK[kTile][D];
+    __shared__ float sV[kTile][D];
+    const int64_t bh = blockIdx.y;
+    const int T = kp.T;
+    const int q0 = blockIdx.x * kRows;
+    const int r = threadIdx.x >> 2, part = threadIdx.x & 3;
+    const int i = q0 + r;
+    const bool valid = i < T;
+    const size_t head = (size_t)bh * T * D;
+
+    float q[S], acc[S];
+#pragma unroll
+    for (int k = 0; k < S; ++k) {
+        q[k] = valid ? load_as_float(P1 + head + (size_t)i * D + part + 4 * k) : 0.f;
+        acc[k] = 0.f;
+    }
+    float m = -INFINITY, l = 0.f;
+    const float corr = count_correction(kp, i);
+    const int kv_end = kp.causal ? min(T, q0 + kRows) : T;
+
+    for (int j0 = 0; j0 < kv_end; j0 += kTile) {
+        __syncthreads();
+        load_tile<Tin, D>(sK, P2 + head, j0, T);
+        load_tile<Tin, D>(sV, V + head, j0, T);
+        __syncthreads();
+        for (int jj = 0; jj < kTile; ++jj) {
+            const int j = j0 + jj;
+            if (j >= kv_end) break;
+            float dot = 0.f;
+#pragma unroll
+            for (int k = 0; k < S; ++k) dot = fmaf(q[k], sK[jj][part + 4 * k], dot);
+            dot = quad_sum(dot);
+            const bool visible = valid && (!kp.causal || j <= i);
+            if (visible) {
+                const float u = dot * kp.inv_sqrt_d;
+                const float x = (j == i) ? sigmoid_exact(u / kp.tau_S) : u * sigmoid_exact(u) - corr;
+                const float m_new = fmaxf(m, x);
+                const float sc = expf(m - m_new);  // 0 on the first visible entry
+                const float p = expf(x - m_new);
+                l = l * sc + p;
+#pragma unroll
+                for (int k = 0; k < S; ++k) acc[k] = fmaf(p, sV[jj][part + 4 * k], acc[k] * sc);
+                m = m_new;
+            }
+        }
+    }
+    if (valid) {
+        const float inv_l = 1.f / l;
+#pragma unroll
+        for (int k = 0; k < S; ++k) store_from_float(Y + head + (size_t)i * D + part + 4 * k, acc[k] * inv_l);
+        if (L != nullptr && part == 0) L[bh * T + i] = m + logf(l);
+    }
+}
+
+// ------------------------------------------------- backward: D_i and dlambda
+// One warp per row.  D_i = dY_i . Y_i.  dlambda = sum_i log(c_i) dR_ii, which
+// equals -sum_i log(c_i) sum_{j!=i} dR_ij because every row of dR sums to 0.
+// Also clears the row of the float32 dP1 accumulator when one is given.
+template <typename Tin>
+__global__ void __launch_bounds__(256) bwd_prepare_kernel(KernelProblem kp, const Tin* __restrict__ P1,
+                                                          const Tin* __restrict__ P2,
+                                                          const Tin* __restrict__ V,
+                                                          const Tin* __restrict__ Yf,
+                                                          const float* __restrict__ L,
+                                                          const Tin* __restrict__ dY,
+                                                          float* __restrict__ Dout, float* __restrict__ dq_acc,
+                                                          float* __restrict__ dlambda) {
+    __shared__ float s_part[8];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * 8 + warp;  // flattened (bh, i)
+    const int64_t rows = kp.BH * kp.T;
+    const int d = kp.d;
+    float contrib = 0.f;
+    if (row < rows) {
+        const int i = (int)(row % kp.T);
+        const size_t off = (size_t)row * d;
+        float dy_y = 0.f, p1p2 = 0.f, dy_v = 0.f;
+        for (int c = lane; c < d; c += 32) {
+            const float g = load_as_float(dY + off + c);
+            dy_y = fmaf(g, load_as_float(Yf + off + c), dy_y);
+            dy_v = fmaf(g, load_as_float(V + off + c), dy_v);
+            p1p2 = fmaf(load_as_float(P1 + off + c), load_as_float(P2 + off + c), p1p2);
+            if (dq_acc != nullptr) dq_acc[off + c] = 0.f;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            dy_y += __shfl_xor_sync(0xffffffffu, dy_y, o);
+            dy_v += __shfl_xor_sync(0xffffffffu, dy_v, o);
+            p1p2 += __shfl_xor_sync(0xffffffffu, p1p2, o);
+        }
+        if (lane == 0) {
+            Dout[row] = dy_y;
+            const float u = p1p2 * kp.inv_sqrt_d;
+            const float S = sigmoid_exact(u / kp.tau_S);
+            const float Fii = expf(S - L[row]);
+            const float dRii = Fii * (dy_v - dy_y);
+            const int c = kp.causal ? (i + 1) : kp.T;
+            contrib = logf((float)c) * dRii;
+        }
+    }
+    if (dlambda == nullptr) return;
+    if (lane == 0) s_part[warp] = contrib;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) s += s_part[w];
+        atomicAdd(dlambda, s);
+    }
+}
+
+// Relation entry r_ij and its slope dr/du for zero-based (i, j), j visible.
+__device__ __forceinline__ void relation_entry(const KernelProblem& kp, int i, int j, float u, float corr,
+                                               float* r, float* slope) {
+    if (j == i) {
+        const float sg = sigmoid_exact(u / kp.tau_S);
+        *r = sg;
+        *slope = sg * (1.f - sg) / kp.tau_S;
+    } else {
+        const float sg = sigmoid_exact(u);
+        *r = u * sg - corr;
+        *slope = sg * (1.f + u * (1.f - sg));
+    }
+}
+
+// --------------------------------------- backward: key-stationary dP2 and dV
+template <typename Tin, int D>
+__global__ void __launch_bounds__(kThreads) bwd_kv_simt_kernel(KernelProblem kp, const Tin* __restrict__ P1,
+                                                               const Tin* __restrict__ P2,
+                                                               const Tin* __restrict__ V,
+                                                               const float* __restrict__ L,
+                                                               const float* __restrict__ Dw,
+                                                               const Tin* __restrict__ dY, Tin* __restrict__ dP2,
+                                                               Tin* __restrict__ dV) {
+    constexpr int S = D / 4;
+    __shared__ float sQ[kTile][D];
+    __shared__ float sG[kTile][D];
+    __shared__ float sL[kTile], sD[kTile], sC[kTile];
+    const int64_t bh = blockIdx.y;
+    const int T = kp.T;
+    const int j0 = blockIdx.x * kRows;
+    const int r = threadIdx.x >> 2, part = threadIdx.x & 3;
+    const int j = j0 + r;
+    const bool valid = j < T;
+    const size_t head = (size_t)bh * T * D;
+    float kreg[S], vreg[S], adv[S], adk[S];
+#pragma unroll
+    for (int k = 0; k < S; ++k) {
+        kreg[k] = valid ? load_as_float(P2 + head + (size_t)j * D + part + 4 * k) : 0.f;
+        vreg[k] = valid ? load_as_float(V + head + (size_t)j * D + part + 4 * k) : 0.f;
+        adv[k] = adk[k] = 0.f;
+    }
+    const int i_begin = kp.causal ? j0 : 0;
+    for (int i0 = i_begin; i0 < T; i0 += kTile) {
+        __syncthreads();
+        load_tile<Tin, D>(sQ, P1 + head, i0, T);
+        load_tile<Tin, D>(sG, dY + head, i0, T);
+        if (threadIdx.x < kTile) {
+            const int i = i0 + threadIdx.x;
+            sL[threadIdx.x] = i < T ? L[bh * T + i] : 0.f;
+            sD[threadIdx.x] = i < T ? Dw[bh * T + i] : 0.f;
+            sC[threadIdx.x] = count_correction(kp, i);
+        }
+        __syncthreads();
+        for (int ii = 0; ii < kTile; ++ii) {
+            const int i = i0 + ii;
+            if (i >= T) break;
+            float du = 0.f, df = 0.f;
+#pragma unroll
+            for (int k = 0; k < S; ++k) {
+                du = fmaf(kreg[k], sQ[ii][part + 4 * k], du);
+                df = fmaf(vreg[k], sG[ii][part + 4 * k], df);
+            }
+            du = quad_sum(du);
+            df = quad_sum(df);
+            if (valid && (!kp.causal || j <= i)) {
+                const float u = du * kp.inv_sqrt_d;
+                float rr, slope;
+                relation_entry(kp, i, j, u, sC[ii], &rr, &slope);
+                const float F = expf(rr - sL[ii]);
+                const float dU = F * (df - sD[ii]) * slope * kp.inv_sqrt_d;
+#pragma unroll
+                for (int k = 0; k < S; ++k) {
+                    adv[k] = fmaf(F, sG[ii][part + 4 * k], adv[k]);
+                    adk[k] = fmaf(dU, sQ[ii][part + 4 * k], adk[k]);
+                }
+            }
+        }
+    }
+    if (valid) {
+#pragma unroll
+        for (int k = 0; k < S; ++k) {
+            store_from_float(dP2 + head + (size_t)j * D + part + 4 * k, adk[k]);
+            store_from_float(dV + head + (size_t)j * D + part + 4 * k, adv[k]);
+        }
+    }
+}
+
+// ----------------------------------------------- backward: query-stationary dP1
+template <typename Tin, int D>
+__global__ void __launch_bounds__(kThreads) bwd_q_simt_kernel(KernelProblem kp, const Tin* __restrict__ P1,
+                                                              const Tin* __restrict__ P2,
+                                                              const Tin* __restrict__ V,
+                                                              const float* __restrict__ L,
+                                                              const float* __restrict__ Dw,
+                                                              const Tin* __restrict__ dY, Tin* __restrict__ dP1) {
+    constexpr int S = D / 4;
+    __shared__ float sK[kTile][D];
+    __shared__ float sV[kTile][D];
+    const int64_t bh = blockIdx.y;
+    const int T = kp.T;
+    const int q0 = blockIdx.x * kRows;
+    const int r = threadIdx.x >> 2, part = threadIdx.x & 3;
+    const int i = q0 + r;
+    const bool valid = i < T;
+    const size_t head = (size_t)bh * T * D;
+    float qreg[S], greg[S], acc[S];
+#pragma unroll
+    for (int k = 0; k < S; ++k) {
+        qreg[k] = valid ? load_as_float(P1 + head + (size_t)i * D + part + 4 * k) : 0.f;
+        greg[k] = valid ? load_as_float(dY + head + (size_t)i * D + part + 4 * k) : 0.f;
+        acc[k] = 0.f;
+    }
+    const float Li = valid ? L[bh * T + i] : 0.f;
+    const float Di = valid ? Dw[bh * T + i] : 0.f;
+    const float corr = count_correction(kp, i);
+    const int kv_end = kp.causal ? min(T, q0 + kRows) : T;
+    for (int j0 = 0; j0 < kv_end; j0 += kTile) {
+        __syncthreads();
+        load_tile<Tin, D>(sK, P2 + head, j0, T);
+        load_tile<Tin, D>(sV, V + head, j0, T);
+        __syncthreads();
+        for (int jj = 0; jj < kTile; ++jj) {
+            const int j = j0 + jj;
+            if (j >= kv_end) break;
+            float du = 0.f, df = 0.f;
+#pragma unroll
+            for (int k = 0; k < S; ++k) {
+                du = fmaf(qreg[k], sK[jj][part + 4 * k], du);
+                df = fmaf(greg[k], sV[jj][part + 4 * k], df);
+            }
+            du = quad_sum(du);
+            df = quad_sum(df);
+            if (valid && (!kp.causal || j <= i)) {
+                const float u = du * kp.inv_sqrt_d;
+                float rr, slope;
+                relation_entry(kp, i, j, u, corr, &rr, &slope);
+                const float F = expf(rr - Li);
+                const float dU = F * (df - Di) * slope * kp.inv_sqrt_d;
+#pragma unroll
+                for (int k = 0; k < S; ++k) acc[k] = fmaf(dU, sK[jj][part + 4 * k], acc[k]);
+            }
+        }
+    }
+    if (valid) {
+#pragma unroll
+        for (int k = 0; k < S; ++k) store_from_float(dP1 + head + (size_t)i * D + part + 4 * k, acc[k]);
+    }
+}
+
+// ------------------------------------------- dP1 accumulator (fp32) -> dtype
+template <typename Tout>
+__global__ void __launch_bounds__(256) convert_kernel(const float* __restrict__ src, Tout* __restrict__ dst,
+                                                      int64_t n4) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < n4; k += stride) {
+        const float4 v = reinterpret_cast<const float4*>(src)[k];
+        store_from_float(dst + 4 * k + 0, v.x);
+        store_from_float(dst + 4 * k + 1, v.y);
+        store_from_float(dst + 4 * k + 2, v.z);
+        store_from_float(dst + 4 * k + 3, v.w);
+    }
+}
+
+template <typename Tin>
+cudaError_t launch_fwd_simt_t(const KernelProblem& kp, const void* P1, const void* P2, const void* V, void* Y,
+                              float* L, cudaStream_t s) {
+    dim3 grid((kp.T + kRows - 1) / kRows, (unsigned)kp.BH);
+    if (kp.d == 64)
+        fwd_simt_kernel<Tin, 64><<<grid, kThreads, 0, s>>>(kp, (const Tin*)P1, (const Tin*)P2, (const Tin*)V,
+                                                           (Tin*)Y, L);
+    else
+        fwd_simt_kernel<Tin, 128><<<grid, kThreads, 0, s>>>(kp, (const Tin*)P1, (const Tin*)P2, (const Tin*)V,
+                                                            (Tin*)Y, L);
+    return cudaGetLastError();
+}
+
+template <typename Tin>
+cudaError_t launch_bwd_simt_t(const KernelProblem& kp, const void* P1, const void* P2, const void* V,
+                              const float* L, const float* Dw, const void* dY, void* dP1, void* dP2, void* dV,
+                              cudaStream_t s) {
+    dim3 grid((kp.T + kRows - 1) / kRows, (unsigned)kp.BH);
+    if (kp.d == 64) {
+        bwd_kv_simt_kernel<Tin, 64><<<grid, kThreads, 0, s>>>(kp, (const Tin*)P1, (const Tin*)P2, (const Tin*)V, L,
+                                                              Dw, (const Tin*)dY, (Tin*)dP2, (Tin*)dV);
+        bwd_q_simt_kernel<Tin, 64><<<grid, kThreads, 0, s>>>(kp, (const Tin*)P1, (const Tin*)P2, (const Tin*)V, L,
+                                                             Dw, (const Tin*)dY, (Tin*)dP1);
+    } else {
+        bwd_kv_simt_kernel<Tin, 128><<<grid, kThreads, 0, s>>>(kp, (const Tin*)P1, (const Tin*)P2, (const Tin*)V,
+                                                               L, Dw, (const Tin*)dY, (Tin*)dP2, (Tin*)dV);
+        bwd_q_simt_kernel<Tin, 128><<<grid, kThreads, 0, s>>>(kp, (const Tin*)P1, (const Tin*)P2, (const Tin*)V, L,
+                                                              Dw, (const Tin*)dY, (Tin*)dP1);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_simt(const KernelProblem& kp, bool bf16, const void* P1, const void* P2, const void* V,
+                            void* Y, float* L, cudaStream_t s) {
+    return bf16 ? launch_fwd_simt_t<__nv_bfloat16>(kp, P1, P2, V, Y, L, s)
+                : launch_fwd_simt_t<float>(kp, P1, P2, V, Y, L, s);
+}
+
+cudaError_t launch_bwd_simt(const KernelProblem& kp, bool bf16, const void* P1, const void* P2, const void* V,
+                            const float* L, const float* Dw, const void* dY, void* dP1, void* dP2, void* dV,
+                            cudaStream_t s) {
+    return bf16 ? launch_bwd_simt_t<__nv_bfloat16>(kp, P1, P2, V, L, Dw, dY, dP1, dP2, dV, s)
+                : launch_bwd_simt_t<float>(kp, P1, P2, V, L, Dw, dY, dP1, dP2, dV, s);
+}
+
+cudaError_t launch_bwd_prepare(const KernelProblem& kp, bool bf16, const void* P1, const void* P2, const void* V,
+                               const void* Y, const float* L, const void* dY, float* Dw, float* dq_acc,
+                               float* dlambda, cudaStream_t s) {
+    const int64_t rows = kp.BH * kp.T;
+    const unsigned blocks = (unsigned)((rows + 7) / 8);
+    if (bf16)
+        bwd_prepare_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
+            kp, (const __nv_bfloat16*)P1, (const __nv_bfloat16*)P2, (const __nv_bfloat16*)V,
+            (const __nv_bfloat16*)Y, L, (const __nv_bfloat16*)dY, Dw, dq_acc, dlambda);
+    else
+        bwd_prepare_kernel<float><<<blocks, 256, 0, s>>>(kp, (const float*)P1, (const float*)P2, (const float*)V,
+                                                         (const float*)Y, L, (const float*)dY, Dw, dq_acc, dlambda);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_convert(const float* src, void* dst, bool bf16, int64_t n, int num_sms, cudaStream_t s) {
+    const int64_t n4 = n / 4;  // n is a multiple of d (64 or 128)
+    int64_t blocks = (n4 + 255) / 256;
+    const int64_t cap = (int64_t)num_sms * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    if (bf16)
+        convert_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(src, (__nv_bfloat16*)dst, n4);
+    else
+        convert_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(src, (float*)dst, n4);
+    return cudaGetLastError();
+}
+
+}  // namespace relation

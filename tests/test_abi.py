@@ -1,0 +1,91 @@
+"""Host-side checks of the C ABI: the library builds and loads, exports every
+symbol include/relation.h declares, and rejects bad arguments before touching
+the GPU (so these run without one)."""
+import ctypes
+import subprocess
+
+import pytest
+
+from relation_token_mixing_gb300 import binding as rb
+from relation_token_mixing_gb300 import build as rbuild
+
+A = 0x10000  # fake, 16-byte aligned addresses: validation fails before any use
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return rb.load()
+
+
+def test_library_exports_every_declared_symbol(lib):
+    declared = rb.declared_symbols()
+    assert "relation_fwd" in declared and "relation_bwd" in declared
+    out = subprocess.run(["nm", "-D", "--defined-only", rbuild.LIB], capture_output=True, text=True, check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    missing = [s for s in declared if s not in exported]
+    assert not missing, missing
+    for s in declared:
+        getattr(lib, s)
+
+
+def test_version_and_status_strings(lib):
+    assert rb.relation_abi_version() == 1
+    for code in range(7):
+        assert rb.relation_status_string(code)
+    assert rb.relation_status_string(99) == "unknown status"
+
+
+def _prob(**kw):
+    base = dict(B=2, H=3, T=100, d_h=64, dtype=rb.RELATION_BF16, tau_S=1.0, lam=0.5, causal=1)
+    base.update(kw)
+    return rb.Problem(base["B"], base["H"], base["T"], base["d_h"], base["dtype"], base["tau_S"], base["lam"],
+                      base["causal"])
+
+
+def _fwd(lib, prob, P1=A, P2=2 * A, V=3 * A, Y=4 * A, L=5 * A):
+    return lib.relation_fwd(ctypes.byref(prob), P1, P2, V, Y, L, None)
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(H=-1), dict(T=0), dict(tau_S=0.0), dict(tau_S=-1.0),
+                                dict(tau_S=float("inf")), dict(lam=float("nan")), dict(dtype=7)])
+def test_invalid_problem_rejected(lib, kw):
+    assert _fwd(lib, _prob(**kw)) == 1
+
+
+@pytest.mark.parametrize("d", [32, 48, 80, 256])
+def test_unsupported_head_width(lib, d):
+    assert _fwd(lib, _prob(d_h=d)) == 2
+    assert rb.relation_bwd_workspace_bytes(_prob(d_h=d)) == 0
+
+
+def test_null_and_misaligned_pointers(lib):
+    p = _prob()
+    assert _fwd(lib, p, P1=None) == 1
+    assert _fwd(lib, p, Y=None) == 1
+    assert _fwd(lib, p, V=3 * A + 8) == 3
+
+
+def test_overlapping_output_rejected(lib):
+    p = _prob(B=1, H=1, T=128, d_h=64)
+    nbytes = 128 * 64 * 2
+    assert _fwd(lib, p, P1=A, P2=A + nbytes, V=A + 2 * nbytes, Y=A + nbytes // 2) == 1
+    assert _fwd(lib, p, Y=8 * A, L=8 * A + 16) == 1
+
+
+def test_workspace_size_and_backward_checks(lib):
+    p = _prob(B=2, H=3, T=100, d_h=64)
+    need = rb.relation_bwd_workspace_bytes(p)
+    rows = 2 * 3 * 100
+    assert need >= rows * 4 + rows * 64 * 4  # D_i plus the fp32 dP1 accumulator
+    pf = _prob(B=2, H=3, T=100, d_h=64, dtype=rb.RELATION_F32)
+    assert rb.relation_bwd_workspace_bytes(pf) >= rows * 4
+    args = [A * k for k in range(1, 11)]  # P1 P2 V Y L dY dP1 dP2 dV dlambda
+    ws = 64 * A
+    for name in ("relation_bwd", "relation_bwd_prepare", "relation_bwd_main", "relation_bwd_finish"):
+        fn = getattr(lib, name)
+        assert fn(ctypes.byref(p), *args, ws, need - 4, None) == 4
+        assert fn(ctypes.byref(p), *args[:6], args[0], *args[7:], ws, need, None) == 1  # dP1 aliases P1
+        bad = list(args)
+        bad[7] += 4
+        assert fn(ctypes.byref(p), *bad, ws, need, None) == 3
+        assert fn(ctypes.byref(p), *args, None, need, None) == 1
