@@ -9,7 +9,9 @@ Tolerances (from the arithmetic):
 Inputs come from the seeded generator (relation_token_mixing_gb300.inputs); the
 oracle upcasts the same rounded tensors to float64.
 """
+import json
 import math
+import os
 
 import numpy as np
 import pytest
@@ -24,6 +26,17 @@ pytestmark = pytest.mark.gpu
 Y_TOL = {torch.float32: 1e-5, torch.bfloat16: 1e-2}
 L_TOL = {torch.float32: 1e-5, torch.bfloat16: 1e-2}
 G_TOL = {torch.float32: 1e-4, torch.bfloat16: 2e-2}
+
+
+_MARGIN_LOG = os.environ.get("RELATION_PARITY_LOG")
+
+
+def _record(what, err, tol):
+    """Appends (test, quantity, error, tolerance) to RELATION_PARITY_LOG when set."""
+    if _MARGIN_LOG:
+        test = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+        with open(_MARGIN_LOG, "a") as f:
+            f.write(json.dumps({"test": test, "what": what, "err": err, "tol": tol}) + "\n")
 
 
 def _dev(x):
@@ -59,6 +72,8 @@ def _check_fwd_full(w, x_cpu):
     Yr, Lr = oracle.fwd(x_cpu["P1"], x_cpu["P2"], x_cpu["V"], w.tau_S, w.lam, w.causal)
     vmax = float(np.max(np.abs(_np(x_cpu["V"]))))
     ey, el = _maxerr(_np(Y), Yr), _maxerr(_np(L), Lr)
+    _record("Y", ey, Y_TOL[w.dtype] * vmax)
+    _record("L", el, L_TOL[w.dtype])
     assert ey <= Y_TOL[w.dtype] * vmax, (ey, vmax)
     assert el <= L_TOL[w.dtype], el
     return Y, L
@@ -68,12 +83,20 @@ def _check_bwd_full(w, x_cpu, Y, L):
     x = _dev(x_cpu)
     dP1, dP2, dV, dlam = _gpu_bwd(x, w, Y, L)
     ref = oracle.bwd(x_cpu["P1"], x_cpu["P2"], x_cpu["V"], x_cpu["dY"], w.tau_S, w.lam, w.causal)
+    # A tensor whose reference is identically zero (dP1, dP2 at T = 1) is held to
+    # the scale of the other gradients instead.
+    floor = max(float(np.max(np.abs(e))) for e in ref[:3])
     for got, exp, name in zip((dP1, dP2, dV), ref[:3], ("dP1", "dP2", "dV")):
         gmax = float(np.max(np.abs(exp)))
+        if gmax == 0.0:
+            gmax = floor
         err = _maxerr(_np(got), exp)
+        _record(name, err, G_TOL[w.dtype] * gmax)
         assert err <= G_TOL[w.dtype] * gmax, (name, err, gmax)
     scale = max(1.0, abs(ref[3]))
-    assert abs(float(dlam.item()) - ref[3]) <= 50 * G_TOL[w.dtype] * scale, (float(dlam.item()), ref[3])
+    derr = abs(float(dlam.item()) - ref[3])
+    _record("dlambda", derr, 5 * G_TOL[w.dtype] * scale)
+    assert derr <= 5 * G_TOL[w.dtype] * scale, (float(dlam.item()), ref[3])
 
 
 # --------------------------------------------------------------- small cases
@@ -122,6 +145,7 @@ def test_zero_evidence_closed_form(lam):
     P2 = rin.gaussian((B, H, T, d), 43, 1.0, torch.bfloat16)
     V = rin.gaussian((B, H, T, d), 44, 1.0, torch.bfloat16)
     Y, _ = rb.fwd(P1.cuda(), P2.cuda(), V.cuda(), 1.0, lam, True)
+    torch.cuda.synchronize()
     Vn = _np(V)
     i = np.arange(1, T + 1, dtype=np.float64)
     f = math.exp(0.5) / (math.exp(0.5) + (i - 1) * i ** (-lam))
@@ -129,6 +153,7 @@ def test_zero_evidence_closed_form(lam):
     hist = np.zeros_like(Vn)
     hist[:, :, 1:] = csum[:, :, :-1] / (i[1:, None] - 1)
     expect = f[None, None, :, None] * Vn + (1 - f)[None, None, :, None] * hist
+    _record("Y(closed form)", _maxerr(_np(Y), expect), 1e-2 * np.max(np.abs(Vn)))
     assert _maxerr(_np(Y), expect) <= 1e-2 * np.max(np.abs(Vn))
 
 
@@ -222,6 +247,8 @@ def _check_fwd_sampled(w, x_cpu, Y, L, n=200, seed=0):
     Yg = _np(Y).reshape(BH, w.T, w.d)[heads, rows]
     Lg = _np(L).reshape(BH, w.T)[heads, rows]
     vmax = float(np.max(np.abs(_np(x_cpu["V"]))))
+    _record("Y(sampled)", _maxerr(Yg, Yr), Y_TOL[w.dtype] * vmax)
+    _record("L(sampled)", _maxerr(Lg, Lr), L_TOL[w.dtype])
     assert _maxerr(Yg, Yr) <= Y_TOL[w.dtype] * vmax
     assert _maxerr(Lg, Lr) <= L_TOL[w.dtype]
 
@@ -241,6 +268,7 @@ def _check_bwd_sampled(w, x_cpu, grads, heads=(0,), ncols=24, seed=1):
             gg = _np(got).reshape(BH, T, w.d)[h, cols]
             # per-tensor scale: the largest reference magnitude among the sampled rows
             gmax = float(np.max(np.abs(exp)))
+            _record(name + "(sampled)", _maxerr(gg, exp), G_TOL[w.dtype] * gmax)
             assert _maxerr(gg, exp) <= G_TOL[w.dtype] * gmax, (name, h, _maxerr(gg, exp), gmax)
 
 
