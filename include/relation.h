@@ -120,6 +120,29 @@ relation_status_t relation_bwd_finish(const relation_problem_t* p, const void* P
                                       void* stream);
 
 /*
+ * relation_bwd for callers that cannot allocate device memory (the paper has
+ * no counterpart; this is an interface for the library's users).  Such callers
+ * include code whose device memory all belongs to a host framework's own
+ * allocator that a C caller cannot reach, and serving loops that must not
+ * allocate after start-up because cudaMalloc can synchronise the device.
+ * Same arguments and results as relation_bwd without workspace and
+ * workspace_bytes: the workspace is a fixed device array inside the library of
+ * RELATION_NOALLOC_SCRATCH_BYTES (32 MiB), held on every GPU that loads the
+ * library until the process exits.  Problems whose
+ * relation_bwd_workspace_bytes() exceeds it return
+ * RELATION_ERR_WORKSPACE_TOO_SMALL before any work is enqueued.  The function
+ * calls no allocator.  The first call on each device looks up the array's
+ * device address (cudaGetSymbolAddress, with that device current): make it
+ * before any stream capture.  All calls share the array and overwrite what
+ * they need, so calls whose work overlaps on the GPU race and must not run
+ * concurrently.
+ */
+#define RELATION_NOALLOC_SCRATCH_BYTES (32u << 20)
+relation_status_t relation_bwd_noalloc(const relation_problem_t* p, const void* P1, const void* P2,
+                                       const void* V, const void* Y, const float* L, const void* dY,
+                                       void* dP1, void* dP2, void* dV, float* dlambda, void* stream);
+
+/*
  * Reads and clears the device status word of the current device.  Call after
  * synchronising the streams used.  Returns RELATION_OK or
  * RELATION_ERR_DEVICE_TIMEOUT (a bounded wait expired; outputs of the calls

@@ -79,6 +79,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         for name in ("relation_bwd", "relation_bwd_prepare", "relation_bwd_main", "relation_bwd_finish"):
             getattr(lib, name).argtypes = _BWD_ARGTYPES
             getattr(lib, name).restype = ctypes.c_int
+        lib.relation_bwd_noalloc.argtypes = [ctypes.POINTER(Problem), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                             _VP]
+        lib.relation_bwd_noalloc.restype = ctypes.c_int
         lib.relation_bwd_workspace_bytes.argtypes = [ctypes.POINTER(Problem)]
         lib.relation_bwd_workspace_bytes.restype = ctypes.c_size_t
         lib.relation_check_device_status.argtypes = []
@@ -170,6 +173,13 @@ def relation_bwd_main(prob, P1, P2, V, Y, L, dY, dP1, dP2, dV, dlambda, workspac
 
 def relation_bwd_finish(prob, P1, P2, V, Y, L, dY, dP1, dP2, dV, dlambda, workspace, stream=None) -> None:
     _bwd_call("relation_bwd_finish", prob, P1, P2, V, Y, L, dY, dP1, dP2, dV, dlambda, workspace, stream)
+
+
+def relation_bwd_noalloc(prob, P1, P2, V, Y, L, dY, dP1, dP2, dV, dlambda, stream=None) -> None:
+    """relation_bwd with the library's built-in scratch array as workspace (no allocation)."""
+    _check(load().relation_bwd_noalloc(ctypes.byref(prob), _ptr(P1), _ptr(P2), _ptr(V), _ptr(Y), _ptr(L), _ptr(dY),
+                                       _ptr(dP1), _ptr(dP2), _ptr(dV), _ptr(dlambda), _stream_ptr(stream)),
+           "relation_bwd_noalloc")
 
 
 def relation_check_device_status() -> int:
