@@ -336,9 +336,13 @@ def main():
     peak_burst, peak_sust, peak_src = load_peaks()
     mean_fwd, mean_main = statistics.mean(t_fwd), statistics.mean(t_main)
     if mean_main >= mean_fwd:
-        dom, dom_ms, dom_flops, srcs = "relation_bwd_tc_kernel", mean_main, f_bwd, ["bwd_tc.cu", "ptx_sm100.cuh"]
+        if w.d == 64:
+            dom, srcs = "relation_bwd_tc64_kernel", ["bwd_tc64.cu", "ptx_sm100.cuh"]
+        else:
+            dom, srcs = f"relation_bwd_tc_kernel<{w.d}>", ["bwd_tc.cu", "ptx_sm100.cuh"]
+        dom_ms, dom_flops = mean_main, f_bwd
     else:
-        dom, dom_ms, dom_flops, srcs = "relation_fwd_tc_kernel", mean_fwd, f_fwd, ["fwd_tc.cu", "ptx_sm100.cuh"]
+        dom, dom_ms, dom_flops, srcs = f"relation_fwd_tc_kernel<{w.d}>", mean_fwd, f_fwd, ["fwd_tc.cu", "ptx_sm100.cuh"]
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
     line = {
         "metric": "Relation fwd+bwd TFLOP/s (bf16, causal) and % of GB300 dense bf16 peak",

@@ -72,19 +72,6 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
     }
 }
 
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-}
-
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     relation_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_p1, const __grid_constant__ CUtensorMap tm_p2,
@@ -285,8 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int qq = 0; qq < 8; ++qq) {
                 uint32_t sv[16], gv[16];
-                tmem_ld16(lane_addr + C::kColS + 16 * qq, sv);
-                tmem_ld16(lane_addr + C::kColDP + 16 * qq, gv);
+                ptx::tmem_ld16(lane_addr + C::kColS + 16 * qq, sv);
+                ptx::tmem_ld16(lane_addr + C::kColDP + 16 * qq, gv);
                 ptx::tmem_ld_wait();
                 ptx::pin_regs(sv);
                 ptx::pin_regs(gv);
@@ -341,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             ptx::tmem_st_wait();
-            fence_proxy_async_smem();
+            ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
             ptx::mbar_arrive(&bars->p_full);
         }
@@ -438,9 +425,9 @@ cudaError_t launch_bwd_tc_d(const KernelProblem& kp, const void* P1, const void*
 }  // namespace
 
 cudaError_t launch_bwd_tc(const KernelProblem& kp, const void* P1, const void* P2, const void* V, const float* L,
-                          const float* Dw, const void* dY, float* dq_acc, void* dP2, void* dV, const TcLaunch& tl,
-                          cudaStream_t s) {
-    if (kp.d == 64) return launch_bwd_tc_d<64>(kp, P1, P2, V, L, Dw, dY, dq_acc, dP2, dV, tl, s);
+                          const float* Dw, const void* dY, float* dq_acc, void* dP2, void* dV, float* dlambda,
+                          const TcLaunch& tl, cudaStream_t s) {
+    if (kp.d == 64) return launch_bwd_tc64(kp, P1, P2, V, L, Dw, dY, dq_acc, dP2, dV, dlambda, tl, s);
     if (kp.d == 128) return launch_bwd_tc_d<128>(kp, P1, P2, V, L, Dw, dY, dq_acc, dP2, dV, tl, s);
     return cudaErrorInvalidValue;
 }

@@ -16,8 +16,9 @@
 // One CTA = one head x two 128-row query tiles (rows q_base .. q_base+255).
 //   warp 0      TMA producer: both Q tiles once, then K/V tiles through a ring
 //   warp 1      MMA issuer (one thread) and TMEM owner
-//   warps 2-5   softmax of query tile 0 (one thread per row)
-//   warps 6-9   softmax of query tile 1
+//   warps 2-3   idle (they complete the first warpgroup for register reallocation)
+//   warps 4-7   softmax of query tile 0 (one thread per row)
+//   warps 8-11  softmax of query tile 1
 // TMEM (512 columns): S0 | S1 (128 fp32 columns each; P overwrites the first
 // 64 columns as packed bf16) | O0 | O1 (d columns each).
 // Per key tile j, per query tile t:  S_t = Q_t K_j^T (SS MMA) -> softmax ->
@@ -34,13 +35,17 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBN = 128;
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
+// Register split (per thread) after launch at 168: the load/MMA warpgroup
+// gives back, the two softmax warpgroups take: 128*56 + 256*224 = 64512 <= 384*168.
+constexpr uint32_t kRegsControl = 56, kRegsSoftmax = 224;
 constexpr int kPanelBytes = 128 * 128;  // 128 rows x 64 bf16 (one 128-byte swizzle span)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-// The running max is raised only when a block's max exceeds it by more than
-// this many powers of two; exact, since numerator and denominator share it.
-constexpr float kRescaleThreshold = 8.0f;
+// The running max (natural units) is raised only when a block's max exceeds
+// it by more than 8 ln 2 (a factor 256); exact, since numerator and
+// denominator share whatever max is used.
+constexpr float kRescaleThreshold = 8.0f * 0.6931471805599453f;
 
 template <int D>
 struct FwdCfg {
@@ -75,6 +80,31 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
     while (!ptx::mbar_try_wait(bar, parity)) {
         if (global_ns() - t0 > RELATION_WAIT_LIMIT_NS) return;
     }
+}
+
+// Dot product of row r of two staged tiles (D/64 swizzled panels of 128 rows x
+// 128 bytes; 16-byte chunk k of row r sits at chunk k ^ (r % 8)).
+template <int kPanels>
+__device__ __forceinline__ float row_dot(const uint8_t* a_tile, const uint8_t* b_tile, int r) {
+    float acc = 0.f;
+#pragma unroll
+    for (int p = 0; p < kPanels; ++p) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int off = p * kPanelBytes + r * 128 + ((k ^ (r & 7)) << 4);
+            const uint4 x = *reinterpret_cast<const uint4*>(a_tile + off);
+            const uint4 y = *reinterpret_cast<const uint4*>(b_tile + off);
+            const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xs[w]));
+                const float2 yf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ys[w]));
+                acc = fmaf(xf.x, yf.x, acc);
+                acc = fmaf(xf.y, yf.y, acc);
+            }
+        }
+    }
+    return acc;
 }
 
 template <int D>
@@ -129,9 +159,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
     volatile int* abort_flag = &bars->abort_flag;
-
     if (warp == 0) {
         // ------------------------------------------------------------ producer
+        ptx::regs_dec<kRegsControl>();
         if (lane == 0) {
             ptx::tma_prefetch_desc(&tm_p1);
             ptx::tma_prefetch_desc(&tm_p2);
@@ -172,6 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
+        ptx::regs_dec<kRegsControl>();
         if (lane == 0) {
             const uint32_t id_s = ptx::idesc_bf16(kBM, kBN, false, false);
             const uint32_t id_o = ptx::idesc_bf16(kBM, D, false, true);
@@ -246,9 +277,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mma_commit(&bars->drain);
             drain_wait(&bars->drain, 0);
         }
+    } else if (warp < 4) {
+        ptx::regs_dec<kRegsControl>();
     } else {
         // ------------------------------------------------------------- softmax
-        const int t = (warp - 2) >> 2;
+        ptx::regs_inc<kRegsSoftmax>();
+        const int t = (warp - 4) >> 2;
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;
         const int i = q_base + t * kBM + r;
@@ -256,7 +290,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
         const uint32_t s_col = t * 128, o_col = 256 + t * D;
         const float c_half = 0.5f * kp.inv_sqrt_d;         // U/2 per raw dot product
-        const float c_half_l2 = c_half * kLog2e;
         const float c_diag = 0.5f * kp.inv_sqrt_d / kp.tau_S;  // U/(2 tau_S)
         const int count = kp.causal ? (i + 1) : T;
         const float corr = kp.lambda * logf((float)count);    // lambda log c_i
@@ -276,53 +309,64 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tmem_ld32(lane_addr + s_col + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * c));
             ptx::tmem_ld_wait();
             ptx::pin_regs(sv);
-            // sv[c] becomes x_c = R'_ic * log2(e) in place (R' = R + lambda log c_i).
+            // sv[c] becomes R'_ic (natural units) in place, R' = R + lambda log c_i.
             const bool is_diag = (j == diag_tile);
             const int climit = (j == n_kv_all - 1) ? tail_cols : kBN;
-            if (!is_diag && climit == kBN) {
+            const float2 ch2 = make_float2(c_half, c_half);
 #pragma unroll
-                for (int c = 0; c < 128; ++c) {
-                    const float a = as_f(sv[c]);
-                    const float th = ptx::tanh_approx(a * c_half);
-                    const float hx = a * c_half_l2;
-                    sv[c] = as_u(fmaf(hx, th, hx));  // SiLU(U) * log2(e)
+            for (int e = 0; e < 64; ++e) {
+                const float2 h = ptx::mul2(make_float2(as_f(sv[2 * e]), as_f(sv[2 * e + 1])), ch2);
+                const float2 th = make_float2(ptx::tanh_approx(h.x), ptx::tanh_approx(h.y));
+                const float2 E = ptx::fma2(h, th, h);  // SiLU(U) = (U/2)(1 + tanh(U/2))
+                sv[2 * e] = as_u(E.x);
+                sv[2 * e + 1] = as_u(E.y);
+            }
+            if (is_diag || climit < kBN) {
+                // Self entry sigmoid(U_ii/tau_S) = (1 + tanh(U_ii/(2 tau_S)))/2 plus the folded
+                // count correction; U_ii is recomputed from the staged P1 and P2 rows.
+                // Masked entries (future keys, keys past T) become -inf.
+                float s_diag = 0.f;
+                if (is_diag) {
+                    const float a_diag = row_dot<C::kPanels>(sQ + t * C::kTileBytes, sK + (j % C::kStages) * C::kTileBytes, r);
+                    s_diag = fmaf(0.5f, ptx::tanh_approx(a_diag * c_diag), 0.5f) + corr;
                 }
-            } else {
+                const int cmax = (kp.causal && is_diag) ? min(r, climit - 1) : climit - 1;  // last visible column
 #pragma unroll
                 for (int c = 0; c < 128; ++c) {
-                    const float a = as_f(sv[c]);
-                    float v;
-                    if (is_diag && c == r) {
-                        v = (0.5f + 0.5f * ptx::tanh_approx(a * c_diag) + corr) * kLog2e;
-                    } else if (c >= climit || (kp.causal && is_diag && c > r)) {
-                        v = -INFINITY;
-                    } else {
-                        const float th = ptx::tanh_approx(a * c_half);
-                        const float hx = a * c_half_l2;
-                        v = fmaf(hx, th, hx);
-                    }
-                    sv[c] = as_u(v);
+                    float v = (c > cmax) ? -INFINITY : as_f(sv[c]);
+                    sv[c] = as_u((is_diag && c == r) ? s_diag : v);
                 }
             }
-            float mt = as_f(sv[0]);
+            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int c = 1; c + 1 < 128; c += 2) mt = ptx::max3(mt, as_f(sv[c]), as_f(sv[c + 1]));
-            mt = fmaxf(mt, as_f(sv[127]));
+            for (int c = 0; c < 128; c += 8) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) mx[k] = ptx::max3(mx[k], as_f(sv[c + 2 * k]), as_f(sv[c + 2 * k + 1]));
+            }
+            const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
             const float m_new = fmaxf(m, mt);
             const bool rescale = __any_sync(0xffffffffu, m_new > m + kRescaleThreshold);
             float scale = 1.f;
             if (rescale) {
-                scale = ptx::ex2_approx(m - m_new);  // 0 when m = -inf
+                scale = ptx::ex2_approx((m - m_new) * kLog2e);  // 0 when m = -inf
                 l *= scale;
                 m = m_new;
             }
+            const float2 l2e2 = make_float2(kLog2e, kLog2e);
+            const float2 nm2 = make_float2(-m * kLog2e, -m * kLog2e);
+            float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
             uint32_t pk[2][32];
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
-                const float p0 = ptx::ex2_approx(as_f(sv[2 * c]) - m);
-                const float p1 = ptx::ex2_approx(as_f(sv[2 * c + 1]) - m);
-                l += p0 + p1;
-                pk[c >> 5][c & 31] = ptx::pack_bf16x2(p0, p1);
+                const float2 y = ptx::fma2(make_float2(as_f(sv[2 * c]), as_f(sv[2 * c + 1])), l2e2, nm2);
+                const float2 p = make_float2(ptx::ex2_approx(y.x), ptx::ex2_approx(y.y));
+                ls[c & 3] = ptx::add2(ls[c & 3], p);
+                pk[c >> 5][c & 31] = ptx::pack_bf16x2(p.x, p.y);
+            }
+            {
+                const float2 s01 = ptx::add2(ls[0], ls[1]), s23 = ptx::add2(ls[2], ls[3]);
+                const float2 st = ptx::add2(s01, s23);
+                l += st.x + st.y;
             }
             ptx::tmem_st32(lane_addr + s_col, pk[0]);
             ptx::tmem_st32(lane_addr + s_col + 32, pk[1]);
@@ -371,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         dst[k] = make_uint4(pkd[4 * k], pkd[4 * k + 1], pkd[4 * k + 2], pkd[4 * k + 3]);
                 }
             }
-            if (L != nullptr && i < T) L[(size_t)bh * T + i] = (m + __log2f(l)) * kLn2 - corr;
+            if (L != nullptr && i < T) L[(size_t)bh * T + i] = m + __log2f(l) * kLn2 - corr;
         }
     }
     ptx::tc_fence_before();

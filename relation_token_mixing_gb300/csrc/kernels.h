@@ -28,8 +28,13 @@ struct TcLaunch {
 };
 cudaError_t launch_fwd_tc(const KernelProblem& kp, const void* P1, const void* P2, const void* V, void* Y, float* L,
                           const TcLaunch& tl, cudaStream_t s);
+// Whether the tensor-core backward kernel for this head width also sums dlambda.
+inline bool bwd_tc_sums_dlambda(int d) { return d == 64; }
 cudaError_t launch_bwd_tc(const KernelProblem& kp, const void* P1, const void* P2, const void* V, const float* L,
-                          const float* Dw, const void* dY, float* dq_acc, void* dP2, void* dV, const TcLaunch& tl,
-                          cudaStream_t s);
+                          const float* Dw, const void* dY, float* dq_acc, void* dP2, void* dV, float* dlambda,
+                          const TcLaunch& tl, cudaStream_t s);
+cudaError_t launch_bwd_tc64(const KernelProblem& kp, const void* P1, const void* P2, const void* V, const float* L,
+                            const float* Dw, const void* dY, float* dq_acc, void* dP2, void* dV, float* dlambda,
+                            const TcLaunch& tl, cudaStream_t s);
 
 }  // namespace relation

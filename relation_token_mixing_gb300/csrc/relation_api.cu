@@ -155,8 +155,10 @@ relation_status_t run_prepare(const BwdArgs& a, int* launches) {
         if (cudaMemsetAsync(a.dlambda, 0, sizeof(float), a.stream) != cudaSuccess) return RELATION_ERR_CUDA;
     }
     const KernelProblem kp = kernel_problem(a.p);
+    // dlambda is summed by the main pass where that kernel does it, else here.
+    float* dlam_here = (use_tensor_cores(a.p) && bwd_tc_sums_dlambda(kp.d)) ? nullptr : a.dlambda;
     relation_status_t st = from_cuda(launch_bwd_prepare(kp, a.p->dtype == RELATION_BF16, a.P1, a.P2, a.V, a.Y, a.L,
-                                                        a.dY, Dw, dq, a.dlambda, a.stream));
+                                                        a.dY, Dw, dq, dlam_here, a.stream));
     if (st == RELATION_OK) *launches += 1;
     return st;
 }
@@ -172,7 +174,8 @@ relation_status_t run_main(const BwdArgs& a, int* launches) {
         if (st != RELATION_OK) return st;
         float* dq = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + dq_off);
         TcLaunch tl{di.num_sms, di.status};
-        st = from_cuda(launch_bwd_tc(kp, a.P1, a.P2, a.V, a.L, Dw, a.dY, dq, a.dP2, a.dV, tl, a.stream));
+        float* dlam_main = bwd_tc_sums_dlambda(kp.d) ? a.dlambda : nullptr;
+        st = from_cuda(launch_bwd_tc(kp, a.P1, a.P2, a.V, a.L, Dw, a.dY, dq, a.dP2, a.dV, dlam_main, tl, a.stream));
         if (st == RELATION_OK) *launches += 1;
         return st;
     }
