@@ -1,5 +1,6 @@
-// Fused Full Relation backward for head width 64 on the sm_103a tensor cores:
-// the pipelined variant of the key-stationary backward (bf16 in, fp32 accumulate).
+// Fused Full Relation backward for head width 64 on the sm_103a tensor cores
+// (bf16 in, fp32 accumulate): key-stationary, with the tensor core and the
+// elementwise stage overlapped across query tiles.
 //
 // Mathematics: the chain rule of "Ask Self, Ask Others: Relation Is All You
 // Need", Sec. 3.1 eq.(1)-(3) (the paper gives no backward), with
@@ -11,19 +12,21 @@
 // so one MUFU tanh serves both SiLU (forward value) and its slope.
 //
 // One CTA = one head x one 128-row key tile; it walks the query tiles i that
-// see it.  Each query tile is processed as two 64-column halves so that the
-// two elementwise warpgroups and the tensor core ping-pong:
-//   tensor core:  S_lo dP_lo | S_hi dP_hi | dV,dP2 += lo | S_lo dP_lo (i+1) | dV,dP2 += hi, dP1(i) | S_hi dP_hi (i+1)
-//   WG lo:                   |  lo(i)                     |                  lo(i+1) ...
-//   WG hi:                                 |  hi(i)                          |  hi(i+1) ...
+// see it.  Per query tile (everything transposed so key rows sit on TMEM lanes):
+//   S^T = P2_j P1_i^T, dP^T = V_j dY_i^T        (SS, N = 128)
+//   elementwise: P^T -> TMEM (bf16), dS^T = dU^T/8 -> shared memory (bf16)
+//   dV  += P^T dY_i     (TS)
+//   dP2 += dS^T P1_i    (SS, dS^T read K-major from shared memory)
+//   dP1_i = dS P2_j     (SS, dS read MN-major from the same bytes) -> fp32 atomics
+// As soon as every elementwise warp has copied S^T(i) and dP^T(i) into
+// registers, the MMA warp issues S^T(i+1) and dP^T(i+1), so the tensor core
+// works on tile i+1 (and on the accumulations of tile i) while the
+// elementwise warps work on tile i.
 // Warps: 0 loader (TMA + per-query constants), 1 MMA issuer / TMEM owner,
-// 2-3 idle (complete the first warpgroup), 4-7 elementwise for query columns
-// 0-63, 8-11 for columns 64-127, 12-15 dP1 reduction (TMEM -> fp32
-// accumulator in global memory, atomics).
-// TMEM: S^T [0,128) | dP^T [128,256) | dV [256,320) | dP2 [320,384) | dP1 part [384,448).
-// P^T and dS^T (bf16) overwrite the first half of each S^T / dP^T half they came from.
-// dS^T also goes to shared memory (double-buffered) as the MN-major A operand
-// of dP1 = dS P2.
+// 2-3 idle (complete the first warpgroup), 4-19 elementwise: four warpgroups,
+// one per 32 query columns, 20-23 dP1 reduction (TMEM -> fp32 accumulator in
+// global memory, atomics).
+// TMEM: S^T [0,128) | dP^T [128,256) | P^T [256,320) | dV [320,384) | dP2 [384,448) | dP1 part [448,512).
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -35,29 +38,31 @@ namespace {
 
 constexpr int kD = 64;
 constexpr int kTile = 128;
-constexpr int kThreads = 512;
-// Register split after launch at 128 per thread: load/MMA warpgroup 56, the two
-// elementwise warpgroups 176, the dP1-reduce warpgroup 88:
-// 128*56 + 256*176 + 128*88 = 63488 <= 512*128.
-constexpr uint32_t kRegsControl = 56, kRegsElementwise = 176, kRegsReduce = 88;
+constexpr int kThreads = 768;
+constexpr int kElemWarps = 16;
+// Register split after launch at 80 per thread (six warps per SM sub-partition):
+// load/MMA warpgroup 56, the four elementwise warpgroups 96, the dP1-reduce
+// warpgroup 40:  128*56 + 512*96 + 128*40 = 61440 <= 768*80.
+constexpr uint32_t kRegsControl = 56, kRegsElementwise = 96, kRegsReduce = 40;
 constexpr int kTileBytes = kTile * kD * 2;  // 16 KB: one 128-row x 128-byte swizzled panel
-constexpr int kHalfBytes = kTileBytes / 2;  // 64 rows
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kColDQ = 384;
+constexpr uint32_t kColS = 0, kColDP = 128, kColP = 256, kColDV = 320, kColDK = 384, kColDQ = 448;
 
 struct Smem {
-    uint8_t k[kTileBytes];        // P2_j
-    uint8_t v[kTileBytes];        // V_j
-    uint8_t q[2][kTileBytes];     // P1_i, two stages
-    uint8_t g[2][kTileBytes];     // dY_i, two stages
+    uint8_t k[kTileBytes];          // P2_j
+    uint8_t v[kTileBytes];          // V_j
+    uint8_t q[2][kTileBytes];       // P1_i, two stages
+    uint8_t g[2][kTileBytes];       // dY_i, two stages
     uint8_t ds[2][2 * kTileBytes];  // dS^T, two buffers of two 64-query panels
-    float neg_lt[2][kTile];       // -(L_q + lambda log c_q) * log2(e)
-    float neg_dk[2][kTile];       // -D_q * (1/2) / sqrt(d)
+    float neg_lt[2][kTile];         // -(L_q + lambda log c_q) * log2(e)
+    float neg_dk[2][kTile];         // -D_q * (1/2) / sqrt(d)
     uint64_t kv_full;
     uint64_t q_full[2];
     uint64_t q_empty[2];
-    uint64_t s_full[2];
-    uint64_t p_full[2];
+    uint64_t s_full;
+    uint64_t s_free;
+    uint64_t p_full;
+    uint64_t pv_done;
     uint64_t ds_free[2];
     uint64_t dq_full;
     uint64_t dq_free;
@@ -78,6 +83,8 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
     }
 }
 
+// Descriptors are built once per operand; a byte offset `off` within the
+// operand is added as off >> 4 to the start-address field.
 __device__ __forceinline__ uint64_t kdesc(uint32_t addr) {  // K-major, 128-byte swizzle
     return ptx::smem_desc(addr, 16, 1024, ptx::kSwizzle128B);
 }
@@ -92,65 +99,55 @@ struct ElemConst {
     bool row_valid, causal;
 };
 
-// Elementwise stage for one 64-column half of a query tile, one key row per
-// thread: P^T and dS^T (scaled by 1/sqrt(d)) to TMEM over the consumed
-// columns, dS^T to the shared-memory row.  kMasked selects the variant with
-// the diagonal Self entry and masking; the plain variant has no branches so
-// that the 32 independent element pairs of a chunk interleave.
+// Elementwise arithmetic for 16 columns (8 pairs) of one key row: P (to pp,
+// packed bf16) and dS^T / sqrt(d) (to dd, packed bf16).  kMasked selects the
+// variant with the diagonal Self entry and masking; the plain variant has no
+// branches so that the element pairs interleave.
 template <bool kMasked>
-__device__ __forceinline__ void elementwise_half(const uint32_t (&sv)[64], const uint32_t (&gv)[64],
-                                                 const float* nlt, const float* ndk, uint32_t lane_addr, int h,
-                                                 int r, uint8_t* ds_row, const ElemConst& ec, bool diag_tile,
-                                                 int qlimit, float* dlam) {
+__device__ __forceinline__ void elementwise16(const uint32_t* sv, const uint32_t* gv, const float* nlt,
+                                              const float* ndk, int col0, int r, const ElemConst& ec,
+                                              bool diag_tile, int qlimit, float* dlam, uint32_t (&pp)[8],
+                                              uint32_t (&dd)[8]) {
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
-        uint32_t pp[16], dd[16];
+    for (int e = 0; e < 8; ++e) {
+        const float2 a = make_float2(as_f(sv[2 * e]), as_f(sv[2 * e + 1]));
+        const float2 g = make_float2(as_f(gv[2 * e]), as_f(gv[2 * e + 1]));
+        const float2 nh = ptx::mul2(a, ec.c_nh);
+        const float2 nt = make_float2(ptx::tanh_approx(nh.x), ptx::tanh_approx(nh.y));
+        const float2 tp1 = ptx::fma2(nt, ec.mone, ec.one);
+        const float2 hl = ptx::mul2(a, ec.c_hl);
+        const float2 x = ptx::fma2(hl, tp1, *reinterpret_cast<const float2*>(nlt + 2 * e));
+        float2 p = make_float2(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
+        const float2 nq = ptx::fma2(nt, nt, ec.mone);
+        float2 s2 = ptx::fma2(nh, nq, tp1);
+        const float2 gk = ptx::fma2(g, ec.k2, *reinterpret_cast<const float2*>(ndk + 2 * e));
+        if (kMasked) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const int cc0 = 32 * c + 2 * e;  // column within the half
-            const float2 a = make_float2(as_f(sv[cc0]), as_f(sv[cc0 + 1]));
-            const float2 g = make_float2(as_f(gv[cc0]), as_f(gv[cc0 + 1]));
-            const float2 nh = ptx::mul2(a, ec.c_nh);
-            const float2 nt = make_float2(ptx::tanh_approx(nh.x), ptx::tanh_approx(nh.y));
-            const float2 tp1 = ptx::fma2(nt, ec.mone, ec.one);
-            const float2 hl = ptx::mul2(a, ec.c_hl);
-            const float2 x = ptx::fma2(hl, tp1, *reinterpret_cast<const float2*>(nlt + cc0));
-            float2 p = make_float2(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
-            const float2 nq = ptx::fma2(nt, nt, ec.mone);
-            float2 s2 = ptx::fma2(nh, nq, tp1);
-            const float2 gk = ptx::fma2(g, ec.k2, *reinterpret_cast<const float2*>(ndk + cc0));
-            if (kMasked) {
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int cc = cc0 + u;
-                    const int col = 64 * h + cc;  // column within the query tile
-                    float& pu = u ? p.y : p.x;
-                    float& su = u ? s2.y : s2.x;
-                    if (diag_tile && col == r && ec.row_valid) {
-                        const float aa = u ? a.y : a.x;
-                        const float td = ptx::tanh_approx(aa * ec.c_diag);
-                        pu = ptx::ex2_approx(fmaf(0.5f * kLog2e, td, ec.diag_off + nlt[cc]));
-                        su = fmaf(-td, td, 1.f) * ec.half_inv_tau;  // 2 S(1-S)/tau_S
-                        *dlam += ec.log_count * pu * (u ? gk.y : gk.x);
-                    }
-                    if (cc >= qlimit || !ec.row_valid || (ec.causal && diag_tile && col < r)) pu = 0.f;
+            for (int u = 0; u < 2; ++u) {
+                const int col = col0 + 2 * e + u;  // column within the query tile
+                float& pu = u ? p.y : p.x;
+                float& su = u ? s2.y : s2.x;
+                if (diag_tile && col == r && ec.row_valid) {
+                    const float aa = u ? a.y : a.x;
+                    const float td = ptx::tanh_approx(aa * ec.c_diag);
+                    pu = ptx::ex2_approx(fmaf(0.5f * kLog2e, td, ec.diag_off + nlt[2 * e + u]));
+                    su = fmaf(-td, td, 1.f) * ec.half_inv_tau;  // 2 S(1-S)/tau_S
+                    *dlam += ec.log_count * pu * (u ? gk.y : gk.x);
                 }
+                if (col >= qlimit || !ec.row_valid || (ec.causal && diag_tile && col < r)) pu = 0.f;
             }
-            const float2 dr = ptx::mul2(p, gk);
-            const float2 ds = ptx::mul2(dr, s2);
-            pp[e] = ptx::pack_bf16x2(p.x, p.y);
-            dd[e] = ptx::pack_bf16x2(ds.x, ds.y);
         }
-        // P^T and dS^T over already-read columns of this half.
-        ptx::tmem_st16(lane_addr + kColS + 64 * h + 16 * c, pp);
-        ptx::tmem_st16(lane_addr + kColDP + 64 * h + 16 * c, dd);
-#pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-            const int chunk = 4 * c + k4;
-            *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (r & 7)) << 4)) =
-                make_uint4(dd[4 * k4], dd[4 * k4 + 1], dd[4 * k4 + 2], dd[4 * k4 + 3]);
-        }
+        const float2 dr = ptx::mul2(p, gk);
+        const float2 ds = ptx::mul2(dr, s2);
+        pp[e] = ptx::pack_bf16x2(p.x, p.y);
+        dd[e] = ptx::pack_bf16x2(ds.x, ds.y);
     }
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -177,10 +174,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < 2; ++s) {
             ptx::mbar_init(&sm.q_full[s], 32);
             ptx::mbar_init(&sm.q_empty[s], 1);
-            ptx::mbar_init(&sm.s_full[s], 1);
-            ptx::mbar_init(&sm.p_full[s], 128);
             ptx::mbar_init(&sm.ds_free[s], 1);
         }
+        ptx::mbar_init(&sm.s_full, 1);
+        ptx::mbar_init(&sm.s_free, kElemWarps);
+        ptx::mbar_init(&sm.p_full, kElemWarps);
+        ptx::mbar_init(&sm.pv_done, 1);
         ptx::mbar_init(&sm.dq_full, 1);
         ptx::mbar_init(&sm.dq_free, 128);
         ptx::mbar_init(&sm.mma_done, 1);
@@ -250,80 +249,77 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------- MMA issuer
         ptx::regs_dec<kRegsControl>();
         if (lane == 0) {
-            const uint32_t id_half = ptx::idesc_bf16(kTile, 64, false, false);  // S^T, dP^T halves (N = 64)
-            const uint32_t id_acc = ptx::idesc_bf16(kTile, kD, false, true);    // dV, dP2 (B MN-major)
+            const uint32_t id_s = ptx::idesc_bf16(kTile, kTile, false, false);  // S^T, dP^T (N = 128)
+            const uint32_t id_dv = ptx::idesc_bf16(kTile, kD, false, true);     // dV (B MN-major)
+            const uint32_t id_dk = ptx::idesc_bf16(kTile, kD, false, true);     // dP2 (A K-major, B MN-major)
             const uint32_t id_dq = ptx::idesc_bf16(kTile, kD, true, true);      // dP1 (A, B MN-major)
-            const uint32_t ka = ptx::smem_u32(sm.k), va = ptx::smem_u32(sm.v);
-            auto issue_s_dp = [&](int it, int h) {
-                const int s = it & 1;
-                const uint32_t qa = ptx::smem_u32(sm.q[s]) + h * kHalfBytes;
-                const uint32_t ga = ptx::smem_u32(sm.g[s]) + h * kHalfBytes;
+            const uint64_t dK = kdesc(ptx::smem_u32(sm.k)), dVv = kdesc(ptx::smem_u32(sm.v));
+            const uint64_t dKm = mdesc(ptx::smem_u32(sm.k));
+            // Stage s of a double buffer sits s * (buffer bytes) further on: its
+            // descriptors are the stage-0 ones plus s * (bytes >> 4).
+            const uint64_t dQk0 = kdesc(ptx::smem_u32(sm.q[0])), dGk0 = kdesc(ptx::smem_u32(sm.g[0]));
+            const uint64_t dQm0 = mdesc(ptx::smem_u32(sm.q[0])), dGm0 = mdesc(ptx::smem_u32(sm.g[0]));
+            const uint64_t dSk0 = kdesc(ptx::smem_u32(sm.ds[0])), dSm0 = mdesc(ptx::smem_u32(sm.ds[0]));
+            constexpr uint64_t kStageQ = kTileBytes >> 4, kStageS = (2 * kTileBytes) >> 4;
+            auto issue_s_dp = [&](int s) {
+                // K-step ks: 32-byte step inside the 128-byte swizzled rows.
 #pragma unroll
                 for (int ks = 0; ks < kD / 16; ++ks)
-                    ptx::mma_ss(tmem + kColS + 64 * h, kdesc(ka + ks * 32), kdesc(qa + ks * 32), id_half,
-                                ks > 0 ? 1u : 0u);
+                    ptx::mma_ss(tmem + kColS, dK + 2 * ks, dQk0 + s * kStageQ + 2 * ks, id_s, ks > 0 ? 1u : 0u);
 #pragma unroll
                 for (int ks = 0; ks < kD / 16; ++ks)
-                    ptx::mma_ss(tmem + kColDP + 64 * h, kdesc(va + ks * 32), kdesc(ga + ks * 32), id_half,
-                                ks > 0 ? 1u : 0u);
-                ptx::mma_commit(&sm.s_full[h]);
-            };
-            auto issue_acc = [&](int it, int h) {
-                const int s = it & 1;
-                const uint32_t qa = ptx::smem_u32(sm.q[s]) + h * kHalfBytes;
-                const uint32_t ga = ptx::smem_u32(sm.g[s]) + h * kHalfBytes;
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    ptx::mma_ts(tmem + kColDV, tmem + kColS + 64 * h + 8 * ks, mdesc(ga + ks * 2048), id_acc,
-                                (it > 0 || h > 0 || ks > 0) ? 1u : 0u);
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    ptx::mma_ts(tmem + kColDK, tmem + kColDP + 64 * h + 8 * ks, mdesc(qa + ks * 2048), id_acc,
-                                (it > 0 || h > 0 || ks > 0) ? 1u : 0u);
+                    ptx::mma_ss(tmem + kColDP, dVv + 2 * ks, dGk0 + s * kStageQ + 2 * ks, id_s, ks > 0 ? 1u : 0u);
+                ptx::mma_commit(&sm.s_full);
             };
             bool ok = ptx::mbar_wait(&sm.kv_full, 0, abort_flag, status, kDevTimeoutFull);
             if (ok && n_q > 0) ok = ptx::mbar_wait(&sm.q_full[0], 0, abort_flag, status, kDevTimeoutFull);
             if (ok && n_q > 0) {
                 ptx::tc_fence_after();
-                issue_s_dp(0, 0);
-                issue_s_dp(0, 1);
+                issue_s_dp(0);
             }
             for (int it = 0; ok && it < n_q; ++it) {
-                const bool more = it + 1 < n_q;
-                // low half of query tile it
-                if (!ptx::mbar_wait(&sm.p_full[0], it & 1, abort_flag, status, kDevTimeoutFull)) break;
-                ptx::tc_fence_after();
-                issue_acc(it, 0);
-                if (more) {
-                    if (!ptx::mbar_wait(&sm.q_full[(it + 1) & 1], ((it + 1) >> 1) & 1, abort_flag, status,
+                const int s = it & 1;
+                if (it + 1 < n_q) {
+                    // S^T(i+1), dP^T(i+1) once tile i's values are out of TMEM.
+                    if (!ptx::mbar_wait(&sm.s_free, it & 1, abort_flag, status, kDevTimeoutFull) ||
+                        !ptx::mbar_wait(&sm.q_full[s ^ 1], ((it + 1) >> 1) & 1, abort_flag, status,
                                         kDevTimeoutFull))
                         break;
                     ptx::tc_fence_after();
-                    issue_s_dp(it + 1, 0);
+                    issue_s_dp(s ^ 1);
                 }
-                // high half, then dP1 for the whole tile
-                if (!ptx::mbar_wait(&sm.p_full[1], it & 1, abort_flag, status, kDevTimeoutFull)) break;
+                if (!ptx::mbar_wait(&sm.p_full, it & 1, abort_flag, status, kDevTimeoutFull)) break;
                 ptx::tc_fence_after();
-                issue_acc(it, 1);
-                if (it > 0 && !ptx::mbar_wait(&sm.dq_free, (it - 1) & 1, abort_flag, status, kDevTimeoutMma)) break;
-                const uint32_t dsa = ptx::smem_u32(sm.ds[it & 1]);
+                // dV += P^T dY_i: K-step ks covers queries 16ks..16ks+15 (8 packed TMEM
+                // columns; 16 dY rows = 2048 bytes of the MN-major tile).
 #pragma unroll
                 for (int ks = 0; ks < kTile / 16; ++ks)
-                    ptx::mma_ss(tmem + kColDQ, mdesc(dsa + ks * 2048), mdesc(ka + ks * 2048), id_dq, ks > 0 ? 1u : 0u);
+                    ptx::mma_ts(tmem + kColDV, tmem + kColP + 8 * ks, dGm0 + s * kStageQ + 128 * ks, id_dv,
+                                (it > 0 || ks > 0) ? 1u : 0u);
+                ptx::mma_commit(&sm.pv_done);
+                // dP2 += dS^T P1_i: A K-major over the two 64-query panels of dS^T.
+#pragma unroll
+                for (int ks = 0; ks < kTile / 16; ++ks)
+                    ptx::mma_ss(tmem + kColDK, dSk0 + s * kStageS + (ks >> 2) * kStageQ + 2 * (ks & 3),
+                                dQm0 + s * kStageQ + 128 * ks, id_dk, (it > 0 || ks > 0) ? 1u : 0u);
+                if (it > 0 && !ptx::mbar_wait(&sm.dq_free, (it - 1) & 1, abort_flag, status, kDevTimeoutMma)) break;
+                // dP1_i = dS P2_j: A = dS (MN-major view of the same bytes), K over key rows.
+#pragma unroll
+                for (int ks = 0; ks < kTile / 16; ++ks)
+                    ptx::mma_ss(tmem + kColDQ, dSm0 + s * kStageS + 128 * ks, dKm + 128 * ks, id_dq, ks > 0 ? 1u : 0u);
                 ptx::mma_commit(&sm.dq_full);
-                ptx::mma_commit(&sm.ds_free[it & 1]);
-                ptx::mma_commit(&sm.q_empty[it & 1]);
-                if (more) issue_s_dp(it + 1, 1);
+                ptx::mma_commit(&sm.ds_free[s]);
+                ptx::mma_commit(&sm.q_empty[s]);
             }
             ptx::mma_commit(&sm.mma_done);
             drain_wait(&sm.mma_done, 0);
         }
     } else if (warp < 4) {
         ptx::regs_dec<kRegsControl>();
-    } else if (warp < 12) {
-        // --------------------------------------------------- elementwise halves
+    } else if (warp < 4 + kElemWarps) {
+        // ------------------------------------------------- elementwise blocks
         ptx::regs_inc<kRegsElementwise>();
-        const int h = (warp - 4) >> 2;  // query columns 64h .. 64h+63
+        const int blk = (warp - 4) >> 2;  // query columns 32*blk .. 32*blk+31
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;  // key row within the tile
         const int kv = kv0 + r;
@@ -349,39 +345,70 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int it = 0; ok && it < n_q; ++it) {
             const int s = it & 1;
             const int i = i_first + it;
-            if (!ptx::mbar_wait_warp(&sm.s_full[h], it & 1, abort_flag, status, kDevTimeoutMma) ||
-                !ptx::mbar_wait_warp(&sm.q_full[s], (it >> 1) & 1, abort_flag, status, kDevTimeoutFull) ||
-                (it >= 2 &&
-                 !ptx::mbar_wait_warp(&sm.ds_free[s], ((it >> 1) - 1) & 1, abort_flag, status, kDevTimeoutMma))) {
+            if (!ptx::mbar_wait_warp(&sm.s_full, it & 1, abort_flag, status, kDevTimeoutMma)) {
                 ok = false;
                 break;
             }
             ptx::tc_fence_after();
-            uint32_t sv[64], gv[64];
-            ptx::tmem_ld32(lane_addr + kColS + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(sv));
-            ptx::tmem_ld32(lane_addr + kColS + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
-            ptx::tmem_ld32(lane_addr + kColDP + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(gv));
-            ptx::tmem_ld32(lane_addr + kColDP + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(gv + 32));
+            uint32_t sv[32], gv[32];
+            ptx::tmem_ld16(lane_addr + kColS + 32 * blk, *reinterpret_cast<uint32_t(*)[16]>(sv));
+            ptx::tmem_ld16(lane_addr + kColS + 32 * blk + 16, *reinterpret_cast<uint32_t(*)[16]>(sv + 16));
+            ptx::tmem_ld16(lane_addr + kColDP + 32 * blk, *reinterpret_cast<uint32_t(*)[16]>(gv));
+            ptx::tmem_ld16(lane_addr + kColDP + 32 * blk + 16, *reinterpret_cast<uint32_t(*)[16]>(gv + 16));
             ptx::tmem_ld_wait();
             ptx::pin_regs(sv);
             ptx::pin_regs(gv);
-            const float* nlt = sm.neg_lt[s] + 64 * h;
-            const float* ndk = sm.neg_dk[s] + 64 * h;
+            // This warp's part of S^T(i) and dP^T(i) is in registers: the next tile's
+            // products may overwrite those TMEM columns.
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&sm.s_free);
+            if (!ptx::mbar_wait_warp(&sm.q_full[s], (it >> 1) & 1, abort_flag, status, kDevTimeoutFull)) {
+                ok = false;
+                break;
+            }
+            const float* nlt = sm.neg_lt[s] + 32 * blk;
+            const float* ndk = sm.neg_dk[s] + 32 * blk;
             const bool diag_tile = (i == jt);
-            const int qlimit = T - i * kTile - 64 * h;  // columns cc < qlimit hold queries < T
-            // The two bodies contain warp-collective TMEM stores, so the choice must be
-            // warp-uniform: a warp takes the masked body if any of its rows needs it.
-            const bool special = __any_sync(0xffffffffu, diag_tile || qlimit < 64 || !row_valid);
-            uint8_t* ds_row = sm.ds[s] + h * kTileBytes + r * 128;
-            if (!special) {
-                elementwise_half<false>(sv, gv, nlt, ndk, lane_addr, h, r, ds_row, ec, false, 0, &dlam);
-            } else {
-                elementwise_half<true>(sv, gv, nlt, ndk, lane_addr, h, r, ds_row, ec, diag_tile, qlimit, &dlam);
+            const int qlimit = T - i * kTile;  // columns col < qlimit hold queries < T
+            // The masked variant is chosen per warp (uniformly) if any of its rows needs it.
+            const bool special = __any_sync(0xffffffffu, diag_tile || qlimit < 32 * blk + 32 || !row_valid);
+            uint32_t pp[2][8], dd[2][8];
+#pragma unroll
+            for (int sc = 0; sc < 2; ++sc) {
+                if (!special)
+                    elementwise16<false>(sv + 16 * sc, gv + 16 * sc, nlt + 16 * sc, ndk + 16 * sc, 32 * blk + 16 * sc,
+                                         r, ec, false, 0, &dlam, pp[sc], dd[sc]);
+                else
+                    elementwise16<true>(sv + 16 * sc, gv + 16 * sc, nlt + 16 * sc, ndk + 16 * sc, 32 * blk + 16 * sc,
+                                        r, ec, diag_tile, qlimit, &dlam, pp[sc], dd[sc]);
+            }
+            // P^T(i) may overwrite P^T(i-1) once dV(i-1) has read it.
+            if (it > 0 && !ptx::mbar_wait_warp(&sm.pv_done, (it - 1) & 1, abort_flag, status, kDevTimeoutMma)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            tmem_st8(lane_addr + kColP + 16 * blk, pp[0]);
+            tmem_st8(lane_addr + kColP + 16 * blk + 8, pp[1]);
+            // dS^T(i) into buffer s once the products of tile i-2 have read it.
+            if (it >= 2 &&
+                !ptx::mbar_wait_warp(&sm.ds_free[s], ((it >> 1) - 1) & 1, abort_flag, status, kDevTimeoutMma)) {
+                ok = false;
+                break;
+            }
+            uint8_t* ds_row = sm.ds[s] + (blk >> 1) * kTileBytes + r * 128;
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {
+                const int chunk = 4 * (blk & 1) + k4;
+                const uint32_t* src = dd[k4 >> 1] + 4 * (k4 & 1);
+                *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (r & 7)) << 4)) = make_uint4(src[0], src[1], src[2], src[3]);
             }
             ptx::tmem_st_wait();
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(&sm.p_full[h]);
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&sm.p_full);
         }
         if (dlambda != nullptr) {
             // dR_ii = p (g - D) = dr / k_scale; sum log(c_i) dR_ii.
@@ -389,26 +416,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int o = 16; o > 0; o >>= 1) dlam += __shfl_xor_sync(0xffffffffu, dlam, o);
             if (lane == 0 && dlam != 0.f) atomicAdd(dlambda, dlam / k_scale);
         }
-        // Epilogue: warpgroup 0 writes dV rows, warpgroup 1 writes dP2 rows.
+        // Epilogue: blocks 0-1 write dV, blocks 2-3 write dP2, 32 columns each.
         if (ok && ptx::mbar_wait_warp(&sm.mma_done, 0, abort_flag, status, kDevTimeoutMma)) {
             ptx::tc_fence_after();
-            __nv_bfloat16* dst_row = (h == 0 ? dV : dP2) + ((size_t)bh * T + kv) * kD;
-            const uint32_t col = h == 0 ? kColDV : kColDK;
+            const int c0 = blk & 1;
+            __nv_bfloat16* dst_row = (blk < 2 ? dV : dP2) + ((size_t)bh * T + kv) * kD + 32 * c0;
+            const uint32_t col = (blk < 2 ? kColDV : kColDK) + 32 * c0;
+            uint32_t ov[32];
+            ptx::tmem_ld32(lane_addr + col, ov);
+            ptx::tmem_ld_wait();
+            ptx::pin_regs(ov);
+            if (row_valid) {
+                uint4* dst = reinterpret_cast<uint4*>(dst_row);
 #pragma unroll
-            for (int c0 = 0; c0 < kD / 32; ++c0) {
-                uint32_t ov[32];
-                ptx::tmem_ld32(lane_addr + col + 32 * c0, ov);
-                ptx::tmem_ld_wait();
-                ptx::pin_regs(ov);
-                if (row_valid) {
-                    uint4* dst = reinterpret_cast<uint4*>(dst_row + 32 * c0);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        dst[k] = make_uint4(ptx::pack_bf16x2(as_f(ov[8 * k + 0]), as_f(ov[8 * k + 1])),
-                                            ptx::pack_bf16x2(as_f(ov[8 * k + 2]), as_f(ov[8 * k + 3])),
-                                            ptx::pack_bf16x2(as_f(ov[8 * k + 4]), as_f(ov[8 * k + 5])),
-                                            ptx::pack_bf16x2(as_f(ov[8 * k + 6]), as_f(ov[8 * k + 7])));
-                }
+                for (int k = 0; k < 4; ++k)
+                    dst[k] = make_uint4(ptx::pack_bf16x2(as_f(ov[8 * k + 0]), as_f(ov[8 * k + 1])),
+                                        ptx::pack_bf16x2(as_f(ov[8 * k + 2]), as_f(ov[8 * k + 3])),
+                                        ptx::pack_bf16x2(as_f(ov[8 * k + 4]), as_f(ov[8 * k + 5])),
+                                        ptx::pack_bf16x2(as_f(ov[8 * k + 6]), as_f(ov[8 * k + 7])));
             }
         }
     } else {
@@ -422,22 +447,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ptx::mbar_wait_warp(&sm.dq_full, it & 1, abort_flag, status, kDevTimeoutMma)) break;
             ptx::tc_fence_after();
             const int q = i * kTile + rq;
-            uint32_t ov[2][32];
-            ptx::tmem_ld32(lane_addr + kColDQ, ov[0]);
-            ptx::tmem_ld32(lane_addr + kColDQ + 32, ov[1]);
-            ptx::tmem_ld_wait();
-            ptx::pin_regs(ov[0]);
-            ptx::pin_regs(ov[1]);
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(&sm.dq_free);  // TMEM copy is in registers; the next dP1 MMA may start
-            if (q < T) {
-                float4* dst = reinterpret_cast<float4*>(dq_acc + ((size_t)bh * T + q) * kD);
+            float4* dst = reinterpret_cast<float4*>(dq_acc + ((size_t)bh * T + q) * kD);
 #pragma unroll
-                for (int c0 = 0; c0 < 2; ++c0)
+            for (int c0 = 0; c0 < 2; ++c0) {
+                uint32_t ov[32];
+                ptx::tmem_ld32(lane_addr + kColDQ + 32 * c0, ov);
+                ptx::tmem_ld_wait();
+                ptx::pin_regs(ov);
+                if (c0 == 1) {
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(&sm.dq_free);  // both halves are in registers
+                }
+                if (q < T) {
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
-                        atomicAdd(dst + 8 * c0 + k, make_float4(as_f(ov[c0][4 * k]), as_f(ov[c0][4 * k + 1]),
-                                                                as_f(ov[c0][4 * k + 2]), as_f(ov[c0][4 * k + 3])));
+                        atomicAdd(dst + 8 * c0 + k, make_float4(as_f(ov[4 * k]), as_f(ov[4 * k + 1]),
+                                                                as_f(ov[4 * k + 2]), as_f(ov[4 * k + 3])));
+                }
             }
         }
     }

@@ -206,22 +206,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             const uint32_t id_s = ptx::idesc_bf16(kBM, kBN, false, false);
             const uint32_t id_o = ptx::idesc_bf16(kBM, D, false, true);
+            // Descriptors are built once; a byte offset is added as offset >> 4.
+            const uint64_t dq0 = ptx::smem_desc(ptx::smem_u32(sQ), 16, 1024, ptx::kSwizzle128B);
+            const uint64_t dk0 = ptx::smem_desc(ptx::smem_u32(sK), 16, 1024, ptx::kSwizzle128B);
+            const uint64_t dv0 = ptx::smem_desc(ptx::smem_u32(sV), kPanelBytes, 1024, ptx::kSwizzle128B);
+            constexpr uint64_t kTileStep = C::kTileBytes >> 4, kPanelStep = kPanelBytes >> 4;
             auto issue_s = [&](int t, int s) {
-                const uint32_t qa = ptx::smem_u32(sQ + t * C::kTileBytes);
-                const uint32_t ka = ptx::smem_u32(sK + s * C::kTileBytes);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks / 4) * kPanelBytes + (ks % 4) * 32;
-                    ptx::mma_ss(tmem + t * 128, ptx::smem_desc(qa + off, 16, 1024, ptx::kSwizzle128B),
-                                ptx::smem_desc(ka + off, 16, 1024, ptx::kSwizzle128B), id_s, ks > 0 ? 1u : 0u);
+                    const uint64_t off = (ks / 4) * kPanelStep + (ks % 4) * 2;  // 32 bytes per K-step
+                    ptx::mma_ss(tmem + t * 128, dq0 + t * kTileStep + off, dk0 + s * kTileStep + off, id_s,
+                                ks > 0 ? 1u : 0u);
                 }
             };
             auto issue_pv = [&](int t, int s, bool accumulate) {
-                const uint32_t va = ptx::smem_u32(sV + s * C::kTileBytes);
 #pragma unroll
                 for (int ks = 0; ks < kBN / 16; ++ks) {
-                    ptx::mma_ts(tmem + 256 + t * D, tmem + t * 128 + ks * 8,
-                                ptx::smem_desc(va + ks * 2048, kPanelBytes, 1024, ptx::kSwizzle128B), id_o,
+                    // 16 key rows of V per K-step: 2048 bytes of the MN-major tile.
+                    ptx::mma_ts(tmem + 256 + t * D, tmem + t * 128 + ks * 8, dv0 + s * kTileStep + ks * 128, id_o,
                                 (accumulate || ks > 0) ? 1u : 0u);
                 }
             };
