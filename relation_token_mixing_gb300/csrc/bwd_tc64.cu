@@ -17,15 +17,16 @@
 //   elementwise: P^T -> TMEM (bf16), dS^T = dU^T/8 -> shared memory (bf16)
 //   dV  += P^T dY_i     (TS)
 //   dP2 += dS^T P1_i    (SS, dS^T read K-major from shared memory)
-//   dP1_i = dS P2_j     (SS, dS read MN-major from the same bytes) -> fp32 atomics
+//   dP1_i = dS P2_j     (SS, dS read MN-major from the same bytes), then added
+//                       to an fp32 accumulator in global memory by TMA bulk reduce
 // As soon as every elementwise warp has copied S^T(i) and dP^T(i) into
 // registers, the MMA warp issues S^T(i+1) and dP^T(i+1), so the tensor core
 // works on tile i+1 (and on the accumulations of tile i) while the
 // elementwise warps work on tile i.
 // Warps: 0 loader (TMA + per-query constants), 1 MMA issuer / TMEM owner,
 // 2-3 idle (complete the first warpgroup), 4-19 elementwise: four warpgroups,
-// one per 32 query columns, 20-23 dP1 reduction (TMEM -> fp32 accumulator in
-// global memory, atomics).
+// one per 32 query columns, 20-23 dP1 reduction (TMEM -> swizzled shared
+// staging -> TMA reduce-add).
 // TMEM: S^T [0,128) | dP^T [128,256) | P^T [256,320) | dV [320,384) | dP2 [384,448) | dP1 part [448,512).
 #include <cuda_bf16.h>
 
@@ -41,24 +42,27 @@ constexpr int kTile = 128;
 constexpr int kThreads = 768;
 constexpr int kElemWarps = 16;
 // Register split after launch at 80 per thread (six warps per SM sub-partition):
-// load/MMA warpgroup 56, the four elementwise warpgroups 96, the dP1-reduce
-// warpgroup 40:  128*56 + 512*96 + 128*40 = 61440 <= 768*80.
-constexpr uint32_t kRegsControl = 56, kRegsElementwise = 96, kRegsReduce = 40;
+// load/MMA warpgroup 56, the four elementwise warpgroups 88, the dP1-reduce
+// warpgroup 56:  128*56 + 512*88 + 128*56 = 59392 <= 768*80.
+constexpr uint32_t kRegsControl = 56, kRegsElementwise = 88, kRegsReduce = 56;
 constexpr int kTileBytes = kTile * kD * 2;  // 16 KB: one 128-row x 128-byte swizzled panel
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kColS = 0, kColDP = 128, kColP = 256, kColDV = 320, kColDK = 384, kColDQ = 448;
+// Depth of the P1/dY ring: loads for tile i+2 are in flight while tile i is processed.
+constexpr int kQStages = 3;
 
 struct Smem {
-    uint8_t k[kTileBytes];          // P2_j
-    uint8_t v[kTileBytes];          // V_j
-    uint8_t q[2][kTileBytes];       // P1_i, two stages
-    uint8_t g[2][kTileBytes];       // dY_i, two stages
-    uint8_t ds[2][2 * kTileBytes];  // dS^T, two buffers of two 64-query panels
-    float neg_lt[2][kTile];         // -(L_q + lambda log c_q) * log2(e)
-    float neg_dk[2][kTile];         // -D_q * (1/2) / sqrt(d)
+    uint8_t k[kTileBytes];            // P2_j
+    uint8_t v[kTileBytes];            // V_j
+    uint8_t q[kQStages][kTileBytes];  // P1_i ring
+    uint8_t g[kQStages][kTileBytes];  // dY_i ring
+    uint8_t ds[2][2 * kTileBytes];    // dS^T, two buffers of two 64-query panels
+    uint8_t dq_stage[kTileBytes];     // one 32-column panel of the dP1 partial, fp32 [128][32], swizzled
+    float neg_lt[kQStages][kTile];    // -(L_q + lambda log c_q) * log2(e)
+    float neg_dk[kQStages][kTile];    // -D_q * (1/2) / sqrt(d)
     uint64_t kv_full;
-    uint64_t q_full[2];
-    uint64_t q_empty[2];
+    uint64_t q_full[kQStages];
+    uint64_t q_empty[kQStages];
     uint64_t s_full;
     uint64_t s_free;
     uint64_t p_full;
@@ -70,8 +74,8 @@ struct Smem {
     uint32_t tmem_base;
     int abort_flag;
 };
-// Alignment slack and a 16 KB guard band after the tiles.
-constexpr int kSmemBytes = (int)sizeof(Smem) + 1024 + 16384;
+// Alignment slack.
+constexpr int kSmemBytes = (int)sizeof(Smem) + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 __device__ __forceinline__ float as_f(uint32_t u) { return __uint_as_float(u); }
@@ -83,8 +87,6 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
     }
 }
 
-// Descriptors are built once per operand; a byte offset `off` within the
-// operand is added as off >> 4 to the start-address field.
 __device__ __forceinline__ uint64_t kdesc(uint32_t addr) {  // K-major, 128-byte swizzle
     return ptx::smem_desc(addr, 16, 1024, ptx::kSwizzle128B);
 }
@@ -102,12 +104,13 @@ struct ElemConst {
 // Elementwise arithmetic for 16 columns (8 pairs) of one key row: P (to pp,
 // packed bf16) and dS^T / sqrt(d) (to dd, packed bf16).  kMasked selects the
 // variant with the diagonal Self entry and masking; the plain variant has no
-// branches so that the element pairs interleave.
+// branches so that the element pairs interleave.  Returns this block's
+// contribution log(c_i) * dR_ii * k_scale to dlambda.
 template <bool kMasked>
-__device__ __forceinline__ void elementwise16(const uint32_t* sv, const uint32_t* gv, const float* nlt,
-                                              const float* ndk, int col0, int r, const ElemConst& ec,
-                                              bool diag_tile, int qlimit, float* dlam, uint32_t (&pp)[8],
-                                              uint32_t (&dd)[8]) {
+__device__ __forceinline__ float elementwise16(const uint32_t* sv, const uint32_t* gv, const float* nlt,
+                                               const float* ndk, int col0, int r, const ElemConst& ec,
+                                               bool diag_tile, int qlimit, uint32_t (&pp)[8], uint32_t (&dd)[8]) {
+    float dlam = 0.f;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
         const float2 a = make_float2(as_f(sv[2 * e]), as_f(sv[2 * e + 1]));
@@ -132,7 +135,7 @@ __device__ __forceinline__ void elementwise16(const uint32_t* sv, const uint32_t
                     const float td = ptx::tanh_approx(aa * ec.c_diag);
                     pu = ptx::ex2_approx(fmaf(0.5f * kLog2e, td, ec.diag_off + nlt[2 * e + u]));
                     su = fmaf(-td, td, 1.f) * ec.half_inv_tau;  // 2 S(1-S)/tau_S
-                    *dlam += ec.log_count * pu * (u ? gk.y : gk.x);
+                    dlam += ec.log_count * pu * (u ? gk.y : gk.x);
                 }
                 if (col >= qlimit || !ec.row_valid || (ec.causal && diag_tile && col < r)) pu = 0.f;
             }
@@ -142,6 +145,7 @@ __device__ __forceinline__ void elementwise16(const uint32_t* sv, const uint32_t
         pp[e] = ptx::pack_bf16x2(p.x, p.y);
         dd[e] = ptx::pack_bf16x2(ds.x, ds.y);
     }
+    return dlam;
 }
 
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
@@ -153,8 +157,8 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
 __global__ void __launch_bounds__(kThreads, 1)
     relation_bwd_tc64_kernel(const __grid_constant__ CUtensorMap tm_p1, const __grid_constant__ CUtensorMap tm_p2,
                              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_dy,
-                             const KernelProblem kp, const float* __restrict__ L, const float* __restrict__ Dw,
-                             float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dP2,
+                             const __grid_constant__ CUtensorMap tm_dq, const KernelProblem kp,
+                             const float* __restrict__ L, const float* __restrict__ Dw, __nv_bfloat16* __restrict__ dP2,
                              __nv_bfloat16* __restrict__ dV, float* __restrict__ dlambda, unsigned int* status) {
     extern __shared__ uint8_t smem_raw[];
     Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -171,11 +175,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         ptx::mbar_init(&sm.kv_full, 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kQStages; ++s) {
             ptx::mbar_init(&sm.q_full[s], 32);
             ptx::mbar_init(&sm.q_empty[s], 1);
-            ptx::mbar_init(&sm.ds_free[s], 1);
         }
+        for (int s = 0; s < 2; ++s) ptx::mbar_init(&sm.ds_free[s], 1);
         ptx::mbar_init(&sm.s_full, 1);
         ptx::mbar_init(&sm.s_free, kElemWarps);
         ptx::mbar_init(&sm.p_full, kElemWarps);
@@ -204,13 +208,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tma_prefetch_desc(&tm_p2);
             ptx::tma_prefetch_desc(&tm_v);
             ptx::tma_prefetch_desc(&tm_dy);
+            ptx::tma_prefetch_desc(&tm_dq);
             ptx::mbar_arrive_expect_tx(&sm.kv_full, 2 * kTileBytes);
             ptx::tma_load_3d(sm.k, &tm_p2, &sm.kv_full, 0, kv0, bh);
             ptx::tma_load_3d(sm.v, &tm_v, &sm.kv_full, 0, kv0, bh);
         }
         int it = 0;
         for (; it < n_q; ++it) {
-            const int s = it & 1;
+            const int s = it % kQStages;
             const int i = i_first + it;
             // Global loads first: they do not depend on the stage being free.
             float nlt[4], ndk[4];
@@ -225,8 +230,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ndk[k] = -Dw[(size_t)bh * T + q] * k_scale;
                 }
             }
-            if (it >= 2 &&
-                !ptx::mbar_wait_warp(&sm.q_empty[s], ((it >> 1) - 1) & 1, abort_flag, status, kDevTimeoutEmpty))
+            if (it >= kQStages &&
+                !ptx::mbar_wait_warp(&sm.q_empty[s], ((it / kQStages) - 1) & 1, abort_flag, status, kDevTimeoutEmpty))
                 break;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -243,7 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (lane == 0 && *abort_flag) {
             drain_wait(&sm.kv_full, 0);
-            for (int jj = max(0, it - 2); jj < it; ++jj) drain_wait(&sm.q_full[jj & 1], (jj >> 1) & 1);
+            for (int jj = max(0, it - kQStages); jj < it; ++jj)
+                drain_wait(&sm.q_full[jj % kQStages], (jj / kQStages) & 1);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
@@ -253,22 +259,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t id_dv = ptx::idesc_bf16(kTile, kD, false, true);     // dV (B MN-major)
             const uint32_t id_dk = ptx::idesc_bf16(kTile, kD, false, true);     // dP2 (A K-major, B MN-major)
             const uint32_t id_dq = ptx::idesc_bf16(kTile, kD, true, true);      // dP1 (A, B MN-major)
-            const uint64_t dK = kdesc(ptx::smem_u32(sm.k)), dVv = kdesc(ptx::smem_u32(sm.v));
-            const uint64_t dKm = mdesc(ptx::smem_u32(sm.k));
-            // Stage s of a double buffer sits s * (buffer bytes) further on: its
-            // descriptors are the stage-0 ones plus s * (bytes >> 4).
-            const uint64_t dQk0 = kdesc(ptx::smem_u32(sm.q[0])), dGk0 = kdesc(ptx::smem_u32(sm.g[0]));
-            const uint64_t dQm0 = mdesc(ptx::smem_u32(sm.q[0])), dGm0 = mdesc(ptx::smem_u32(sm.g[0]));
-            const uint64_t dSk0 = kdesc(ptx::smem_u32(sm.ds[0])), dSm0 = mdesc(ptx::smem_u32(sm.ds[0]));
-            constexpr uint64_t kStageQ = kTileBytes >> 4, kStageS = (2 * kTileBytes) >> 4;
-            auto issue_s_dp = [&](int s) {
+            // Descriptor words: the high word depends only on the layout (K-major or
+            // MN-major); the low word is the start address >> 4 plus the leading byte
+            // offset field, advanced by (byte offset >> 4) per K-step.
+            const uint32_t hi_k = ptx::desc_hi(kdesc(ptx::smem_u32(sm.k)));
+            const uint32_t hi_m = ptx::desc_hi(mdesc(ptx::smem_u32(sm.k)));
+            const uint32_t k_lo = ptx::desc_lo(kdesc(ptx::smem_u32(sm.k)));
+            const uint32_t v_lo = ptx::desc_lo(kdesc(ptx::smem_u32(sm.v)));
+            const uint32_t km_lo = ptx::desc_lo(mdesc(ptx::smem_u32(sm.k)));
+            const uint32_t q_lo0 = ptx::desc_lo(kdesc(ptx::smem_u32(sm.q[0])));
+            const uint32_t g_lo0 = ptx::desc_lo(kdesc(ptx::smem_u32(sm.g[0])));
+            const uint32_t qm_lo0 = ptx::desc_lo(mdesc(ptx::smem_u32(sm.q[0])));
+            const uint32_t gm_lo0 = ptx::desc_lo(mdesc(ptx::smem_u32(sm.g[0])));
+            const uint32_t sk_lo0 = ptx::desc_lo(kdesc(ptx::smem_u32(sm.ds[0])));
+            const uint32_t sm_lo0 = ptx::desc_lo(mdesc(ptx::smem_u32(sm.ds[0])));
+            constexpr uint32_t kStageQ = kTileBytes >> 4, kStageS = (2 * kTileBytes) >> 4;
+            auto issue_s_dp = [&](int qs) {
+                const uint32_t q_lo = q_lo0 + qs * kStageQ, g_lo = g_lo0 + qs * kStageQ;
                 // K-step ks: 32-byte step inside the 128-byte swizzled rows.
 #pragma unroll
                 for (int ks = 0; ks < kD / 16; ++ks)
-                    ptx::mma_ss(tmem + kColS, dK + 2 * ks, dQk0 + s * kStageQ + 2 * ks, id_s, ks > 0 ? 1u : 0u);
+                    ptx::mma_ss_lh(tmem + kColS, k_lo + 2 * ks, hi_k, q_lo + 2 * ks, hi_k, id_s, ks > 0 ? 1u : 0u);
 #pragma unroll
                 for (int ks = 0; ks < kD / 16; ++ks)
-                    ptx::mma_ss(tmem + kColDP, dVv + 2 * ks, dGk0 + s * kStageQ + 2 * ks, id_s, ks > 0 ? 1u : 0u);
+                    ptx::mma_ss_lh(tmem + kColDP, v_lo + 2 * ks, hi_k, g_lo + 2 * ks, hi_k, id_s, ks > 0 ? 1u : 0u);
                 ptx::mma_commit(&sm.s_full);
             };
             bool ok = ptx::mbar_wait(&sm.kv_full, 0, abort_flag, status, kDevTimeoutFull);
@@ -278,38 +292,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                 issue_s_dp(0);
             }
             for (int it = 0; ok && it < n_q; ++it) {
-                const int s = it & 1;
+                const int s = it & 1;          // dS buffer
+                const int qs = it % kQStages;  // P1/dY stage
                 if (it + 1 < n_q) {
                     // S^T(i+1), dP^T(i+1) once tile i's values are out of TMEM.
+                    const int qn = (it + 1) % kQStages;
                     if (!ptx::mbar_wait(&sm.s_free, it & 1, abort_flag, status, kDevTimeoutFull) ||
-                        !ptx::mbar_wait(&sm.q_full[s ^ 1], ((it + 1) >> 1) & 1, abort_flag, status,
+                        !ptx::mbar_wait(&sm.q_full[qn], ((it + 1) / kQStages) & 1, abort_flag, status,
                                         kDevTimeoutFull))
                         break;
                     ptx::tc_fence_after();
-                    issue_s_dp(s ^ 1);
+                    issue_s_dp(qn);
                 }
                 if (!ptx::mbar_wait(&sm.p_full, it & 1, abort_flag, status, kDevTimeoutFull)) break;
                 ptx::tc_fence_after();
                 // dV += P^T dY_i: K-step ks covers queries 16ks..16ks+15 (8 packed TMEM
                 // columns; 16 dY rows = 2048 bytes of the MN-major tile).
+                const uint32_t gm_lo = gm_lo0 + qs * kStageQ, qm_lo = qm_lo0 + qs * kStageQ;
+                const uint32_t sk_lo = sk_lo0 + (s ? kStageS : 0u), sm_lo = sm_lo0 + (s ? kStageS : 0u);
+                const uint32_t acc0 = it > 0 ? 1u : 0u;
 #pragma unroll
                 for (int ks = 0; ks < kTile / 16; ++ks)
-                    ptx::mma_ts(tmem + kColDV, tmem + kColP + 8 * ks, dGm0 + s * kStageQ + 128 * ks, id_dv,
-                                (it > 0 || ks > 0) ? 1u : 0u);
+                    ptx::mma_ts_lh(tmem + kColDV, tmem + kColP + 8 * ks, gm_lo + 128 * ks, hi_m, id_dv,
+                                   ks > 0 ? 1u : acc0);
                 ptx::mma_commit(&sm.pv_done);
                 // dP2 += dS^T P1_i: A K-major over the two 64-query panels of dS^T.
 #pragma unroll
                 for (int ks = 0; ks < kTile / 16; ++ks)
-                    ptx::mma_ss(tmem + kColDK, dSk0 + s * kStageS + (ks >> 2) * kStageQ + 2 * (ks & 3),
-                                dQm0 + s * kStageQ + 128 * ks, id_dk, (it > 0 || ks > 0) ? 1u : 0u);
+                    ptx::mma_ss_lh(tmem + kColDK, sk_lo + (ks >> 2) * kStageQ + 2 * (ks & 3), hi_k, qm_lo + 128 * ks,
+                                   hi_m, id_dk, ks > 0 ? 1u : acc0);
+                ptx::mma_commit(&sm.q_empty[qs]);  // P1_i and dY_i are no longer read
                 if (it > 0 && !ptx::mbar_wait(&sm.dq_free, (it - 1) & 1, abort_flag, status, kDevTimeoutMma)) break;
                 // dP1_i = dS P2_j: A = dS (MN-major view of the same bytes), K over key rows.
 #pragma unroll
                 for (int ks = 0; ks < kTile / 16; ++ks)
-                    ptx::mma_ss(tmem + kColDQ, dSm0 + s * kStageS + 128 * ks, dKm + 128 * ks, id_dq, ks > 0 ? 1u : 0u);
+                    ptx::mma_ss_lh(tmem + kColDQ, sm_lo + 128 * ks, hi_m, km_lo + 128 * ks, hi_m, id_dq,
+                                   ks > 0 ? 1u : 0u);
                 ptx::mma_commit(&sm.dq_full);
                 ptx::mma_commit(&sm.ds_free[s]);
-                ptx::mma_commit(&sm.q_empty[s]);
             }
             ptx::mma_commit(&sm.mma_done);
             drain_wait(&sm.mma_done, 0);
@@ -349,61 +369,63 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = false;
                 break;
             }
-            ptx::tc_fence_after();
-            uint32_t sv[32], gv[32];
-            ptx::tmem_ld16(lane_addr + kColS + 32 * blk, *reinterpret_cast<uint32_t(*)[16]>(sv));
-            ptx::tmem_ld16(lane_addr + kColS + 32 * blk + 16, *reinterpret_cast<uint32_t(*)[16]>(sv + 16));
-            ptx::tmem_ld16(lane_addr + kColDP + 32 * blk, *reinterpret_cast<uint32_t(*)[16]>(gv));
-            ptx::tmem_ld16(lane_addr + kColDP + 32 * blk + 16, *reinterpret_cast<uint32_t(*)[16]>(gv + 16));
-            ptx::tmem_ld_wait();
-            ptx::pin_regs(sv);
-            ptx::pin_regs(gv);
-            // This warp's part of S^T(i) and dP^T(i) is in registers: the next tile's
-            // products may overwrite those TMEM columns.
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&sm.s_free);
-            if (!ptx::mbar_wait_warp(&sm.q_full[s], (it >> 1) & 1, abort_flag, status, kDevTimeoutFull)) {
+            // Per-query constants of this tile (loaded with P1_i and dY_i).
+            const int qs = it % kQStages;
+            if (!ptx::mbar_wait_warp(&sm.q_full[qs], (it / kQStages) & 1, abort_flag, status, kDevTimeoutFull)) {
                 ok = false;
                 break;
             }
-            const float* nlt = sm.neg_lt[s] + 32 * blk;
-            const float* ndk = sm.neg_dk[s] + 32 * blk;
+            ptx::tc_fence_after();
+            const float* nlt = sm.neg_lt[qs] + 32 * blk;
+            const float* ndk = sm.neg_dk[qs] + 32 * blk;
             const bool diag_tile = (i == jt);
             const int qlimit = T - i * kTile;  // columns col < qlimit hold queries < T
             // The masked variant is chosen per warp (uniformly) if any of its rows needs it.
             const bool special = __any_sync(0xffffffffu, diag_tile || qlimit < 32 * blk + 32 || !row_valid);
-            uint32_t pp[2][8], dd[2][8];
-#pragma unroll
-            for (int sc = 0; sc < 2; ++sc) {
-                if (!special)
-                    elementwise16<false>(sv + 16 * sc, gv + 16 * sc, nlt + 16 * sc, ndk + 16 * sc, 32 * blk + 16 * sc,
-                                         r, ec, false, 0, &dlam, pp[sc], dd[sc]);
-                else
-                    elementwise16<true>(sv + 16 * sc, gv + 16 * sc, nlt + 16 * sc, ndk + 16 * sc, 32 * blk + 16 * sc,
-                                        r, ec, diag_tile, qlimit, &dlam, pp[sc], dd[sc]);
-            }
-            // P^T(i) may overwrite P^T(i-1) once dV(i-1) has read it.
-            if (it > 0 && !ptx::mbar_wait_warp(&sm.pv_done, (it - 1) & 1, abort_flag, status, kDevTimeoutMma)) {
-                ok = false;
-                break;
-            }
-            ptx::tc_fence_after();
-            tmem_st8(lane_addr + kColP + 16 * blk, pp[0]);
-            tmem_st8(lane_addr + kColP + 16 * blk + 8, pp[1]);
-            // dS^T(i) into buffer s once the products of tile i-2 have read it.
-            if (it >= 2 &&
-                !ptx::mbar_wait_warp(&sm.ds_free[s], ((it >> 1) - 1) & 1, abort_flag, status, kDevTimeoutMma)) {
-                ok = false;
-                break;
-            }
             uint8_t* ds_row = sm.ds[s] + (blk >> 1) * kTileBytes + r * 128;
 #pragma unroll
-            for (int k4 = 0; k4 < 4; ++k4) {
-                const int chunk = 4 * (blk & 1) + k4;
-                const uint32_t* src = dd[k4 >> 1] + 4 * (k4 & 1);
-                *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (r & 7)) << 4)) = make_uint4(src[0], src[1], src[2], src[3]);
+            for (int sc = 0; sc < 2; ++sc) {  // two 16-column sub-chunks, outputs stored at once
+                uint32_t sv[16], gv[16];
+                ptx::tmem_ld16(lane_addr + kColS + 32 * blk + 16 * sc, sv);
+                ptx::tmem_ld16(lane_addr + kColDP + 32 * blk + 16 * sc, gv);
+                ptx::tmem_ld_wait();
+                ptx::pin_regs(sv);
+                ptx::pin_regs(gv);
+                if (sc == 1) {
+                    // This warp's part of S^T(i) and dP^T(i) is in registers: the next
+                    // tile's products may overwrite those TMEM columns.
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(&sm.s_free);
+                }
+                uint32_t pp[8], dd[8];
+                if (!special)
+                    elementwise16<false>(sv, gv, nlt + 16 * sc, ndk + 16 * sc, 32 * blk + 16 * sc, r, ec, false, 0, pp,
+                                         dd);
+                else
+                    dlam += elementwise16<true>(sv, gv, nlt + 16 * sc, ndk + 16 * sc, 32 * blk + 16 * sc, r, ec,
+                                                diag_tile, qlimit, pp, dd);
+                if (sc == 0) {
+                    // Before the first store: P^T(i-1) must have been read by dV(i-1), and
+                    // dS buffer s by the products of tile i-2 (normally long done).
+                    if ((it > 0 &&
+                         !ptx::mbar_wait_warp(&sm.pv_done, (it - 1) & 1, abort_flag, status, kDevTimeoutMma)) ||
+                        (it >= 2 && !ptx::mbar_wait_warp(&sm.ds_free[s], ((it >> 1) - 1) & 1, abort_flag, status,
+                                                         kDevTimeoutMma))) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                }
+                tmem_st8(lane_addr + kColP + 16 * blk + 8 * sc, pp);
+#pragma unroll
+                for (int k2 = 0; k2 < 2; ++k2) {
+                    const int chunk = 4 * (blk & 1) + 2 * sc + k2;
+                    *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (r & 7)) << 4)) =
+                        make_uint4(dd[4 * k2], dd[4 * k2 + 1], dd[4 * k2 + 2], dd[4 * k2 + 3]);
+                }
             }
+            if (!ok) break;
             ptx::tmem_st_wait();
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
@@ -438,16 +460,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // -------------------------------------------------- dP1 partial reduce
+        // TMEM -> swizzled shared staging -> one TMA bulk reduce-add (fp32) per
+        // 32-column panel into the accumulator; rows past T are dropped by TMA.
         ptx::regs_dec<kRegsReduce>();
         const int quarter = warp & 3;
         const int rq = quarter * 32 + lane;
         const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+        const bool leader = (warp == 4 + kElemWarps) && lane == 0;
         for (int it = 0; it < n_q; ++it) {
             const int i = i_first + it;
             if (!ptx::mbar_wait_warp(&sm.dq_full, it & 1, abort_flag, status, kDevTimeoutMma)) break;
             ptx::tc_fence_after();
-            const int q = i * kTile + rq;
-            float4* dst = reinterpret_cast<float4*>(dq_acc + ((size_t)bh * T + q) * kD);
 #pragma unroll
             for (int c0 = 0; c0 < 2; ++c0) {
                 uint32_t ov[32];
@@ -456,16 +479,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::pin_regs(ov);
                 if (c0 == 1) {
                     ptx::tc_fence_before();
-                    ptx::mbar_arrive(&sm.dq_free);  // both halves are in registers
+                    ptx::mbar_arrive(&sm.dq_free);  // both halves have left TMEM
                 }
-                if (q < T) {
+                // The previous bulk reduce must have finished reading the staging panel.
+                if (leader) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                uint8_t* row = sm.dq_stage + rq * 128;
 #pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        atomicAdd(dst + 8 * c0 + k, make_float4(as_f(ov[4 * k]), as_f(ov[4 * k + 1]),
-                                                                as_f(ov[4 * k + 2]), as_f(ov[4 * k + 3])));
+                for (int k = 0; k < 8; ++k)
+                    *reinterpret_cast<uint4*>(row + ((k ^ (rq & 7)) << 4)) =
+                        make_uint4(ov[4 * k], ov[4 * k + 1], ov[4 * k + 2], ov[4 * k + 3]);
+                ptx::fence_proxy_async_smem();
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                if (leader) {
+                    asm volatile(
+                        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2, %3}], "
+                        "[%4];" ::"l"(reinterpret_cast<uint64_t>(&tm_dq)),
+                        "r"(32 * c0), "r"(i * kTile), "r"(bh), "r"(ptx::smem_u32(sm.dq_stage))
+                        : "memory");
+                    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
                 }
             }
         }
+        if (leader) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -487,7 +523,7 @@ cudaError_t launch_bwd_tc64(const KernelProblem& kp, const void* P1, const void*
                                         kSmemBytes);
     });
     if (attr_err != cudaSuccess) return attr_err;
-    CUtensorMap m1, m2, mv, mg;
+    CUtensorMap m1, m2, mv, mg, mq;
     const void* bases[4] = {P1, P2, V, dY};
     CUtensorMap* maps[4] = {&m1, &m2, &mv, &mg};
     for (int k = 0; k < 4; ++k) {
@@ -495,10 +531,13 @@ cudaError_t launch_bwd_tc64(const KernelProblem& kp, const void* P1, const void*
                                            64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
         if (e != cudaSuccess) return e;
     }
+    // dP1 accumulator: fp32 [BH, T, 64], reduced in 32-column (128-byte) swizzled boxes.
+    cudaError_t e = make_tensor_map_3d(&mq, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kD, kp.T, kp.BH, 32, 128,
+                                       CU_TENSOR_MAP_SWIZZLE_128B);
+    if (e != cudaSuccess) return e;
     dim3 grid((unsigned)kp.BH, (unsigned)((kp.T + kTile - 1) / kTile));
-    relation_bwd_tc64_kernel<<<grid, kThreads, kSmemBytes, s>>>(m1, m2, mv, mg, kp, L, Dw, dq_acc,
-                                                                (__nv_bfloat16*)dP2, (__nv_bfloat16*)dV, dlambda,
-                                                                tl.status);
+    relation_bwd_tc64_kernel<<<grid, kThreads, kSmemBytes, s>>>(m1, m2, mv, mg, mq, kp, L, Dw, (__nv_bfloat16*)dP2,
+                                                                (__nv_bfloat16*)dV, dlambda, tl.status);
     return cudaGetLastError();
 }
 
