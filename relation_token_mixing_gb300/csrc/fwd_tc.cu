@@ -49,6 +49,11 @@ constexpr float kRescaleThreshold = 8.0f * 0.6931471805599453f;
 
 template <int D>
 struct FwdCfg {
+    // d = 64 leaves 128 TMEM columns free: P gets its own region per tile, so the
+    // next S can be issued while the softmax still works on the current one.
+    // d = 128 fills TMEM with S and O, and P overwrites S.
+    static constexpr bool kSepP = (D == 64);
+    static constexpr uint32_t kColP = 384;
     static constexpr int kPanels = D / 64;
     static constexpr int kTileBytes = kBM * D * 2;
     static constexpr int kStages = (D == 64) ? 4 : 2;
@@ -64,6 +69,7 @@ struct FwdBarriers {
     uint64_t v_full[4];
     uint64_t kv_empty[4];
     uint64_t s_full[2];
+    uint64_t s_free[2];
     uint64_t p_full[2];
     uint64_t o_done[2];
     uint64_t drain;
@@ -138,6 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < 2; ++t) {
             ptx::mbar_init(&bars->q_full[t], 1);
             ptx::mbar_init(&bars->s_full[t], 1);
+            ptx::mbar_init(&bars->s_free[t], 128);
             ptx::mbar_init(&bars->p_full[t], 128);
             ptx::mbar_init(&bars->o_done[t], 1);
         }
@@ -223,7 +230,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int ks = 0; ks < kBN / 16; ++ks) {
                     // 16 key rows of V per K-step: 2048 bytes of the MN-major tile.
-                    ptx::mma_ts(tmem + 256 + t * D, tmem + t * 128 + ks * 8, dv0 + s * kTileStep + ks * 128, id_o,
+                    const uint32_t p_col = C::kSepP ? C::kColP + 64 * t : 128 * t;
+                    ptx::mma_ts(tmem + 256 + t * D, tmem + p_col + ks * 8, dv0 + s * kTileStep + ks * 128, id_o,
                                 (accumulate || ks > 0) ? 1u : 0u);
                 }
             };
@@ -243,24 +251,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int s = j % C::kStages;
                 const int s1 = (j + 1) % C::kStages;
                 bool v_ready = false, k_next_ready = false;
-                for (int t = 0; t < 2; ++t) {
-                    if (j >= n_t[t]) continue;
-                    if (!ptx::mbar_wait(&bars->p_full[t], j & 1, abort_flag, status, kDevTimeoutFull)) {
-                        ok = false;
-                        break;
-                    }
-                    if (!v_ready) {
-                        if (!ptx::mbar_wait(&bars->v_full[s], (j / C::kStages) & 1, abort_flag, status,
-                                            kDevTimeoutFull)) {
+                if constexpr (C::kSepP) {
+                    // Next S of each tile as soon as its softmax has S(j) in registers.
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        if (j + 1 >= n_t[t]) continue;
+                        if (!ptx::mbar_wait(&bars->s_free[t], j & 1, abort_flag, status, kDevTimeoutFull)) {
                             ok = false;
                             break;
                         }
-                        v_ready = true;
-                    }
-                    ptx::tc_fence_after();
-                    issue_pv(t, s, j > 0);
-                    ptx::mma_commit(&bars->o_done[t]);
-                    if (j + 1 < n_t[t]) {
                         if (!k_next_ready) {
                             if (!ptx::mbar_wait(&bars->k_full[s1], ((j + 1) / C::kStages) & 1, abort_flag, status,
                                                 kDevTimeoutFull)) {
@@ -268,10 +266,60 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 break;
                             }
                             k_next_ready = true;
-                            ptx::tc_fence_after();
                         }
+                        ptx::tc_fence_after();
                         issue_s(t, s1);
                         ptx::mma_commit(&bars->s_full[t]);
+                    }
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        if (j >= n_t[t]) continue;
+                        if (!ptx::mbar_wait(&bars->p_full[t], j & 1, abort_flag, status, kDevTimeoutFull)) {
+                            ok = false;
+                            break;
+                        }
+                        if (!v_ready) {
+                            if (!ptx::mbar_wait(&bars->v_full[s], (j / C::kStages) & 1, abort_flag, status,
+                                                kDevTimeoutFull)) {
+                                ok = false;
+                                break;
+                            }
+                            v_ready = true;
+                        }
+                        ptx::tc_fence_after();
+                        issue_pv(t, s, j > 0);
+                        ptx::mma_commit(&bars->o_done[t]);
+                    }
+                } else {
+                    for (int t = 0; t < 2; ++t) {
+                        if (j >= n_t[t]) continue;
+                        if (!ptx::mbar_wait(&bars->p_full[t], j & 1, abort_flag, status, kDevTimeoutFull)) {
+                            ok = false;
+                            break;
+                        }
+                        if (!v_ready) {
+                            if (!ptx::mbar_wait(&bars->v_full[s], (j / C::kStages) & 1, abort_flag, status,
+                                                kDevTimeoutFull)) {
+                                ok = false;
+                                break;
+                            }
+                            v_ready = true;
+                        }
+                        ptx::tc_fence_after();
+                        issue_pv(t, s, j > 0);
+                        ptx::mma_commit(&bars->o_done[t]);
+                        if (j + 1 < n_t[t]) {
+                            if (!k_next_ready) {
+                                if (!ptx::mbar_wait(&bars->k_full[s1], ((j + 1) / C::kStages) & 1, abort_flag,
+                                                    status, kDevTimeoutFull)) {
+                                    ok = false;
+                                    break;
+                                }
+                                k_next_ready = true;
+                                ptx::tc_fence_after();
+                            }
+                            issue_s(t, s1);
+                            ptx::mma_commit(&bars->s_full[t]);
+                        }
                     }
                 }
                 if (ok) ptx::mma_commit(&bars->kv_empty[s]);
@@ -311,6 +359,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tmem_ld32(lane_addr + s_col + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * c));
             ptx::tmem_ld_wait();
             ptx::pin_regs(sv);
+            if constexpr (C::kSepP) {
+                // S(j) is in registers: the next S of this tile may overwrite it.
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(&bars->s_free[t]);
+            }
             // sv[c] becomes R'_ic (natural units) in place, R' = R + lambda log c_i.
             const bool is_diag = (j == diag_tile);
             const int climit = (j == n_kv_all - 1) ? tail_cols : kBN;
@@ -370,17 +423,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float2 st = ptx::add2(s01, s23);
                 l += st.x + st.y;
             }
-            ptx::tmem_st32(lane_addr + s_col, pk[0]);
-            ptx::tmem_st32(lane_addr + s_col + 32, pk[1]);
+            if constexpr (C::kSepP) {
+                // P(j) replaces P(j-1) once the transport of block j-1 has read it (that
+                // also makes O final for a rescale).
+                if (j > 0) {
+                    if (!ptx::mbar_wait_warp(&bars->o_done[t], (j - 1) & 1, abort_flag, status, kDevTimeoutMma)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                }
+                ptx::tmem_st32(lane_addr + C::kColP + 64 * t, pk[0]);
+                ptx::tmem_st32(lane_addr + C::kColP + 64 * t + 32, pk[1]);
+            } else {
+                ptx::tmem_st32(lane_addr + s_col, pk[0]);
+                ptx::tmem_st32(lane_addr + s_col + 32, pk[1]);
+            }
             if (rescale && j > 0) {
                 // O holds the sums of key blocks 0..j-1; rescale it once the
-                // transport MMA of block j-1 has landed.  Block j's MMA waits
-                // for p_full, which is signalled only after this.
-                if (!ptx::mbar_wait_warp(&bars->o_done[t], (j - 1) & 1, abort_flag, status, kDevTimeoutMma)) {
-                    ok = false;
-                    break;
+                // transport MMA of block j-1 has landed (already awaited above when P
+                // has its own region).  Block j's MMA waits for p_full, which is
+                // signalled only after this.
+                if (!C::kSepP) {
+                    if (!ptx::mbar_wait_warp(&bars->o_done[t], (j - 1) & 1, abort_flag, status, kDevTimeoutMma)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
                 }
-                ptx::tc_fence_after();
 #pragma unroll
                 for (int c0 = 0; c0 < D / 32; ++c0) {
                     uint32_t ov[32];

@@ -168,6 +168,37 @@ __global__ void __launch_bounds__(256) bwd_prepare_kernel(KernelProblem kp, cons
     }
 }
 
+// Vectorised D_i = dY_i . Y_i for bf16 rows of width D plus the reset of the
+// row's fp32 dP1 accumulator; used when dlambda is summed elsewhere.  D/8
+// threads per row, each owning 16 bytes of dY and Y and D/(D/8)*4 bytes of the
+// accumulator.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_prepare_bf16_kernel(int64_t rows, const uint4* __restrict__ Yv,
+                                                               const uint4* __restrict__ dYv,
+                                                               float* __restrict__ Dout, float4* __restrict__ dq4) {
+    constexpr int kTpr = D / 8;  // threads per row
+    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t row = t / kTpr;
+    const int part = (int)(t % kTpr);
+    float acc = 0.f;
+    if (row < rows) {
+        const uint4 y = Yv[row * kTpr + part], g = dYv[row * kTpr + part];
+        const uint32_t ys[4] = {y.x, y.y, y.z, y.w}, gs[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 yf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ys[k]));
+            const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gs[k]));
+            acc = fmaf(yf.x, gf.x, acc);
+            acc = fmaf(yf.y, gf.y, acc);
+        }
+        dq4[row * (D / 4) + 2 * part] = make_float4(0.f, 0.f, 0.f, 0.f);
+        dq4[row * (D / 4) + 2 * part + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int o = kTpr / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (row < rows && part == 0) Dout[row] = acc;
+}
+
 // Relation entry r_ij and its slope dr/du for zero-based (i, j), j visible.
 __device__ __forceinline__ void relation_entry(const KernelProblem& kp, int i, int j, float u, float corr,
                                                float* r, float* slope) {
@@ -382,6 +413,17 @@ cudaError_t launch_bwd_prepare(const KernelProblem& kp, bool bf16, const void* P
                                const void* Y, const float* L, const void* dY, float* Dw, float* dq_acc,
                                float* dlambda, cudaStream_t s) {
     const int64_t rows = kp.BH * kp.T;
+    if (bf16 && dlambda == nullptr && dq_acc != nullptr) {
+        const int64_t threads = rows * (kp.d / 8);
+        const unsigned blocks = (unsigned)((threads + 255) / 256);
+        if (kp.d == 64)
+            bwd_prepare_bf16_kernel<64><<<blocks, 256, 0, s>>>(rows, (const uint4*)Y, (const uint4*)dY, Dw,
+                                                               (float4*)dq_acc);
+        else
+            bwd_prepare_bf16_kernel<128><<<blocks, 256, 0, s>>>(rows, (const uint4*)Y, (const uint4*)dY, Dw,
+                                                                (float4*)dq_acc);
+        return cudaGetLastError();
+    }
     const unsigned blocks = (unsigned)((rows + 7) / 8);
     if (bf16)
         bwd_prepare_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
