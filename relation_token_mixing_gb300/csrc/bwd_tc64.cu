@@ -58,8 +58,9 @@ struct Smem {
     uint8_t g[kQStages][kTileBytes];  // dY_i ring
     uint8_t ds[2][2 * kTileBytes];    // dS^T, two buffers of two 64-query panels
     uint8_t dq_stage[kTileBytes];     // one 32-column panel of the dP1 partial, fp32 [128][32], swizzled
-    float neg_lt[kQStages][kTile];    // -(L_q + lambda log c_q) * log2(e)
-    float neg_dk[kQStages][kTile];    // -D_q * (1/2) / sqrt(d)
+    // Per-query constants, interleaved per column pair (2c, 2c+1):
+    // { -(L + lambda log c) log2(e) [2c], [2c+1],  -D (1/2)/sqrt(d) [2c], [2c+1] }
+    float4 qconst[kQStages][kTile / 2];
     uint64_t kv_full;
     uint64_t q_full[kQStages];
     uint64_t q_empty[kQStages];
@@ -107,23 +108,25 @@ struct ElemConst {
 // branches so that the element pairs interleave.  Returns this block's
 // contribution log(c_i) * dR_ii * k_scale to dlambda.
 template <bool kMasked>
-__device__ __forceinline__ float elementwise16(const uint32_t* sv, const uint32_t* gv, const float* nlt,
-                                               const float* ndk, int col0, int r, const ElemConst& ec,
-                                               bool diag_tile, int qlimit, uint32_t (&pp)[8], uint32_t (&dd)[8]) {
+__device__ __forceinline__ float elementwise16(const uint32_t* sv, const uint32_t* gv, const float4* qc, int col0,
+                                               int r, const ElemConst& ec, bool diag_tile, int qlimit,
+                                               uint32_t (&pp)[8], uint32_t (&dd)[8]) {
     float dlam = 0.f;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
         const float2 a = make_float2(as_f(sv[2 * e]), as_f(sv[2 * e + 1]));
         const float2 g = make_float2(as_f(gv[2 * e]), as_f(gv[2 * e + 1]));
+        const float4 c4 = qc[e];  // one broadcast 16-byte load per column pair
+        const float2 nlt2 = make_float2(c4.x, c4.y), ndk2 = make_float2(c4.z, c4.w);
         const float2 nh = ptx::mul2(a, ec.c_nh);
         const float2 nt = make_float2(ptx::tanh_approx(nh.x), ptx::tanh_approx(nh.y));
         const float2 tp1 = ptx::fma2(nt, ec.mone, ec.one);
         const float2 hl = ptx::mul2(a, ec.c_hl);
-        const float2 x = ptx::fma2(hl, tp1, *reinterpret_cast<const float2*>(nlt + 2 * e));
+        const float2 x = ptx::fma2(hl, tp1, nlt2);
         float2 p = make_float2(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
         const float2 nq = ptx::fma2(nt, nt, ec.mone);
         float2 s2 = ptx::fma2(nh, nq, tp1);
-        const float2 gk = ptx::fma2(g, ec.k2, *reinterpret_cast<const float2*>(ndk + 2 * e));
+        const float2 gk = ptx::fma2(g, ec.k2, ndk2);
         if (kMasked) {
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
@@ -133,7 +136,7 @@ __device__ __forceinline__ float elementwise16(const uint32_t* sv, const uint32_
                 if (diag_tile && col == r && ec.row_valid) {
                     const float aa = u ? a.y : a.x;
                     const float td = ptx::tanh_approx(aa * ec.c_diag);
-                    pu = ptx::ex2_approx(fmaf(0.5f * kLog2e, td, ec.diag_off + nlt[2 * e + u]));
+                    pu = ptx::ex2_approx(fmaf(0.5f * kLog2e, td, ec.diag_off + (u ? nlt2.y : nlt2.x)));
                     su = fmaf(-td, td, 1.f) * ec.half_inv_tau;  // 2 S(1-S)/tau_S
                     dlam += ec.log_count * pu * (u ? gk.y : gk.x);
                 }
@@ -233,10 +236,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (it >= kQStages &&
                 !ptx::mbar_wait_warp(&sm.q_empty[s], ((it / kQStages) - 1) & 1, abort_flag, status, kDevTimeoutEmpty))
                 break;
+            // Lane pairs (2c, 2c+1) of each 32-column group build one float4.
+            float* qc = reinterpret_cast<float*>(sm.qconst[s]);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                sm.neg_lt[s][lane + 32 * k] = nlt[k];
-                sm.neg_dk[s][lane + 32 * k] = ndk[k];
+                const int col = lane + 32 * k;
+                qc[(col >> 1) * 4 + (col & 1)] = nlt[k];
+                qc[(col >> 1) * 4 + 2 + (col & 1)] = ndk[k];
             }
             if (lane == 0) {
                 ptx::mbar_arrive_expect_tx(&sm.q_full[s], 2 * kTileBytes);
@@ -376,8 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             ptx::tc_fence_after();
-            const float* nlt = sm.neg_lt[qs] + 32 * blk;
-            const float* ndk = sm.neg_dk[qs] + 32 * blk;
+            const float4* qc = sm.qconst[qs] + 16 * blk;
             const bool diag_tile = (i == jt);
             const int qlimit = T - i * kTile;  // columns col < qlimit hold queries < T
             // The masked variant is chosen per warp (uniformly) if any of its rows needs it.
@@ -400,11 +405,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 uint32_t pp[8], dd[8];
                 if (!special)
-                    elementwise16<false>(sv, gv, nlt + 16 * sc, ndk + 16 * sc, 32 * blk + 16 * sc, r, ec, false, 0, pp,
-                                         dd);
+                    elementwise16<false>(sv, gv, qc + 8 * sc, 32 * blk + 16 * sc, r, ec, false, 0, pp, dd);
                 else
-                    dlam += elementwise16<true>(sv, gv, nlt + 16 * sc, ndk + 16 * sc, 32 * blk + 16 * sc, r, ec,
-                                                diag_tile, qlimit, pp, dd);
+                    dlam += elementwise16<true>(sv, gv, qc + 8 * sc, 32 * blk + 16 * sc, r, ec, diag_tile, qlimit, pp,
+                                                dd);
                 if (sc == 0) {
                     // Before the first store: P^T(i-1) must have been read by dV(i-1), and
                     // dS buffer s by the products of tile i-2 (normally long done).
