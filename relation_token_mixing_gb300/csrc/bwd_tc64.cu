@@ -13,20 +13,21 @@
 //
 // One CTA = one head x one 128-row key tile; it walks the query tiles i that
 // see it.  Per query tile (everything transposed so key rows sit on TMEM lanes):
-//   S^T = P2_j P1_i^T, dP^T = V_j dY_i^T        (SS, N = 128)
+//   S^T = P2_j P1_i^T, dP^T = V_j dY_i^T        (SS, two N = 64 halves each)
 //   elementwise: P^T -> TMEM (bf16), dS^T = dU^T/8 -> shared memory (bf16)
 //   dV  += P^T dY_i     (TS)
 //   dP2 += dS^T P1_i    (SS, dS^T read K-major from shared memory)
 //   dP1_i = dS P2_j     (SS, dS read MN-major from the same bytes), then added
 //                       to an fp32 accumulator in global memory by TMA bulk reduce
-// As soon as every elementwise warp has copied S^T(i) and dP^T(i) into
-// registers, the MMA warp issues S^T(i+1) and dP^T(i+1), so the tensor core
-// works on tile i+1 (and on the accumulations of tile i) while the
-// elementwise warps work on tile i.
+// S^T and dP^T are produced and consumed in two halves of 64 queries with their
+// own full/free barriers.  Every elementwise warp copies its part of a half to
+// registers before working on it, so the MMA warp issues that half of tile i+1
+// right away: the products of tile i+1 run while tile i is still being worked
+// on, and the accumulations of tile i run while tile i+1 is.
 // Warps: 0 loader (TMA + per-query constants), 1 MMA issuer / TMEM owner,
 // 2-3 idle (complete the first warpgroup), 4-19 elementwise: four warpgroups,
-// one per 32 query columns, 20-23 dP1 reduction (TMEM -> swizzled shared
-// staging -> TMA reduce-add).
+// one per 16 query columns of each half, 20-23 dP1 reduction (TMEM -> swizzled
+// shared staging -> TMA reduce-add).
 // TMEM: S^T [0,128) | dP^T [128,256) | P^T [256,320) | dV [320,384) | dP2 [384,448) | dP1 part [448,512).
 #include <cuda_bf16.h>
 
@@ -64,8 +65,8 @@ struct Smem {
     uint64_t kv_full;
     uint64_t q_full[kQStages];
     uint64_t q_empty[kQStages];
-    uint64_t s_full;
-    uint64_t s_free;
+    uint64_t s_full[2];  // S^T / dP^T of query half h (columns 64h..64h+63) computed
+    uint64_t s_free[2];  // ... and read by every elementwise warp
     uint64_t p_full;
     uint64_t pv_done;
     uint64_t ds_free[2];
@@ -183,8 +184,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(&sm.q_empty[s], 1);
         }
         for (int s = 0; s < 2; ++s) ptx::mbar_init(&sm.ds_free[s], 1);
-        ptx::mbar_init(&sm.s_full, 1);
-        ptx::mbar_init(&sm.s_free, kElemWarps);
+        for (int h = 0; h < 2; ++h) {
+            ptx::mbar_init(&sm.s_full[h], 1);
+            ptx::mbar_init(&sm.s_free[h], kElemWarps);
+        }
         ptx::mbar_init(&sm.p_full, kElemWarps);
         ptx::mbar_init(&sm.pv_done, 1);
         ptx::mbar_init(&sm.dq_full, 1);
@@ -259,9 +262,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
+        // The whole warp runs the issue loop; one elected lane issues each MMA.
         ptx::regs_dec<kRegsControl>();
-        if (lane == 0) {
-            const uint32_t id_s = ptx::idesc_bf16(kTile, kTile, false, false);  // S^T, dP^T (N = 128)
+        {
+            const uint32_t id_s = ptx::idesc_bf16(kTile, kTile / 2, false, false);  // S^T, dP^T halves (N = 64)
             const uint32_t id_dv = ptx::idesc_bf16(kTile, kD, false, true);     // dV (B MN-major)
             const uint32_t id_dk = ptx::idesc_bf16(kTile, kD, false, true);     // dP2 (A K-major, B MN-major)
             const uint32_t id_dq = ptx::idesc_bf16(kTile, kD, true, true);      // dP1 (A, B MN-major)
@@ -279,38 +283,47 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t gm_lo0 = ptx::desc_lo(mdesc(ptx::smem_u32(sm.g[0])));
             const uint32_t sk_lo0 = ptx::desc_lo(kdesc(ptx::smem_u32(sm.ds[0])));
             const uint32_t sm_lo0 = ptx::desc_lo(mdesc(ptx::smem_u32(sm.ds[0])));
-            constexpr uint32_t kStageQ = kTileBytes >> 4, kStageS = (2 * kTileBytes) >> 4;
-            auto issue_s_dp = [&](int qs) {
-                const uint32_t q_lo = q_lo0 + qs * kStageQ, g_lo = g_lo0 + qs * kStageQ;
+            constexpr uint32_t kStageQ = kTileBytes >> 4, kStageS = (2 * kTileBytes) >> 4, kHalfQ = (kTileBytes / 2) >> 4;
+            // S^T and dP^T of query half h (64 queries): N = 64 products into columns
+            // 64h..64h+63 of their regions; B starts 64 rows (8 KB) into the tile.
+            auto issue_s_dp = [&](int qs, int h) {
+                const uint32_t q_lo = q_lo0 + qs * kStageQ + h * kHalfQ, g_lo = g_lo0 + qs * kStageQ + h * kHalfQ;
                 // K-step ks: 32-byte step inside the 128-byte swizzled rows.
 #pragma unroll
                 for (int ks = 0; ks < kD / 16; ++ks)
-                    ptx::mma_ss_lh(tmem + kColS, k_lo + 2 * ks, hi_k, q_lo + 2 * ks, hi_k, id_s, ks > 0 ? 1u : 0u);
+                    ptx::mma_ss_elect(tmem + kColS + 64 * h, k_lo + 2 * ks, hi_k, q_lo + 2 * ks, hi_k, id_s,
+                                      ks > 0 ? 1u : 0u);
 #pragma unroll
                 for (int ks = 0; ks < kD / 16; ++ks)
-                    ptx::mma_ss_lh(tmem + kColDP, v_lo + 2 * ks, hi_k, g_lo + 2 * ks, hi_k, id_s, ks > 0 ? 1u : 0u);
-                ptx::mma_commit(&sm.s_full);
+                    ptx::mma_ss_elect(tmem + kColDP + 64 * h, v_lo + 2 * ks, hi_k, g_lo + 2 * ks, hi_k, id_s,
+                                      ks > 0 ? 1u : 0u);
+                ptx::mma_commit_elect(&sm.s_full[h]);
             };
-            bool ok = ptx::mbar_wait(&sm.kv_full, 0, abort_flag, status, kDevTimeoutFull);
-            if (ok && n_q > 0) ok = ptx::mbar_wait(&sm.q_full[0], 0, abort_flag, status, kDevTimeoutFull);
+            bool ok = ptx::mbar_wait_warp(&sm.kv_full, 0, abort_flag, status, kDevTimeoutFull);
+            if (ok && n_q > 0) ok = ptx::mbar_wait_warp(&sm.q_full[0], 0, abort_flag, status, kDevTimeoutFull);
             if (ok && n_q > 0) {
                 ptx::tc_fence_after();
-                issue_s_dp(0);
+                issue_s_dp(0, 0);
+                issue_s_dp(0, 1);
             }
             for (int it = 0; ok && it < n_q; ++it) {
                 const int s = it & 1;          // dS buffer
                 const int qs = it % kQStages;  // P1/dY stage
                 if (it + 1 < n_q) {
-                    // S^T(i+1), dP^T(i+1) once tile i's values are out of TMEM.
+                    // Each half of S^T(i+1), dP^T(i+1) as soon as every elementwise warp
+                    // has that half of tile i in registers.
                     const int qn = (it + 1) % kQStages;
-                    if (!ptx::mbar_wait(&sm.s_free, it & 1, abort_flag, status, kDevTimeoutFull) ||
-                        !ptx::mbar_wait(&sm.q_full[qn], ((it + 1) / kQStages) & 1, abort_flag, status,
-                                        kDevTimeoutFull))
+                    if (!ptx::mbar_wait_warp(&sm.s_free[0], it & 1, abort_flag, status, kDevTimeoutFull) ||
+                        !ptx::mbar_wait_warp(&sm.q_full[qn], ((it + 1) / kQStages) & 1, abort_flag, status,
+                                             kDevTimeoutFull))
                         break;
                     ptx::tc_fence_after();
-                    issue_s_dp(qn);
+                    issue_s_dp(qn, 0);
+                    if (!ptx::mbar_wait_warp(&sm.s_free[1], it & 1, abort_flag, status, kDevTimeoutFull)) break;
+                    ptx::tc_fence_after();
+                    issue_s_dp(qn, 1);
                 }
-                if (!ptx::mbar_wait(&sm.p_full, it & 1, abort_flag, status, kDevTimeoutFull)) break;
+                if (!ptx::mbar_wait_warp(&sm.p_full, it & 1, abort_flag, status, kDevTimeoutFull)) break;
                 ptx::tc_fence_after();
                 // dV += P^T dY_i: K-step ks covers queries 16ks..16ks+15 (8 packed TMEM
                 // columns; 16 dY rows = 2048 bytes of the MN-major tile).
@@ -319,25 +332,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t acc0 = it > 0 ? 1u : 0u;
 #pragma unroll
                 for (int ks = 0; ks < kTile / 16; ++ks)
-                    ptx::mma_ts_lh(tmem + kColDV, tmem + kColP + 8 * ks, gm_lo + 128 * ks, hi_m, id_dv,
+                    ptx::mma_ts_elect(tmem + kColDV, tmem + kColP + 8 * ks, gm_lo + 128 * ks, hi_m, id_dv,
                                    ks > 0 ? 1u : acc0);
-                ptx::mma_commit(&sm.pv_done);
+                ptx::mma_commit_elect(&sm.pv_done);
                 // dP2 += dS^T P1_i: A K-major over the two 64-query panels of dS^T.
 #pragma unroll
                 for (int ks = 0; ks < kTile / 16; ++ks)
-                    ptx::mma_ss_lh(tmem + kColDK, sk_lo + (ks >> 2) * kStageQ + 2 * (ks & 3), hi_k, qm_lo + 128 * ks,
+                    ptx::mma_ss_elect(tmem + kColDK, sk_lo + (ks >> 2) * kStageQ + 2 * (ks & 3), hi_k, qm_lo + 128 * ks,
                                    hi_m, id_dk, ks > 0 ? 1u : acc0);
-                ptx::mma_commit(&sm.q_empty[qs]);  // P1_i and dY_i are no longer read
-                if (it > 0 && !ptx::mbar_wait(&sm.dq_free, (it - 1) & 1, abort_flag, status, kDevTimeoutMma)) break;
+                ptx::mma_commit_elect(&sm.q_empty[qs]);  // P1_i and dY_i are no longer read
+                if (it > 0 && !ptx::mbar_wait_warp(&sm.dq_free, (it - 1) & 1, abort_flag, status, kDevTimeoutMma)) break;
                 // dP1_i = dS P2_j: A = dS (MN-major view of the same bytes), K over key rows.
 #pragma unroll
                 for (int ks = 0; ks < kTile / 16; ++ks)
-                    ptx::mma_ss_lh(tmem + kColDQ, sm_lo + 128 * ks, hi_m, km_lo + 128 * ks, hi_m, id_dq,
+                    ptx::mma_ss_elect(tmem + kColDQ, sm_lo + 128 * ks, hi_m, km_lo + 128 * ks, hi_m, id_dq,
                                    ks > 0 ? 1u : 0u);
-                ptx::mma_commit(&sm.dq_full);
-                ptx::mma_commit(&sm.ds_free[s]);
+                ptx::mma_commit_elect(&sm.dq_full);
+                ptx::mma_commit_elect(&sm.ds_free[s]);
             }
-            ptx::mma_commit(&sm.mma_done);
+            ptx::mma_commit_elect(&sm.mma_done);
             drain_wait(&sm.mma_done, 0);
         }
     } else if (warp < 4) {
@@ -345,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp < 4 + kElemWarps) {
         // ------------------------------------------------- elementwise blocks
         ptx::regs_inc<kRegsElementwise>();
-        const int blk = (warp - 4) >> 2;  // query columns 32*blk .. 32*blk+31
+        const int blk = (warp - 4) >> 2;  // query columns 64h + 16*blk .. +15 of each half h
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;  // key row within the tile
         const int kv = kv0 + r;
@@ -371,45 +384,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int it = 0; ok && it < n_q; ++it) {
             const int s = it & 1;
             const int i = i_first + it;
-            if (!ptx::mbar_wait_warp(&sm.s_full, it & 1, abort_flag, status, kDevTimeoutMma)) {
-                ok = false;
-                break;
-            }
-            // Per-query constants of this tile (loaded with P1_i and dY_i).
             const int qs = it % kQStages;
-            if (!ptx::mbar_wait_warp(&sm.q_full[qs], (it / kQStages) & 1, abort_flag, status, kDevTimeoutFull)) {
-                ok = false;
-                break;
-            }
-            ptx::tc_fence_after();
-            const float4* qc = sm.qconst[qs] + 16 * blk;
             const bool diag_tile = (i == jt);
             const int qlimit = T - i * kTile;  // columns col < qlimit hold queries < T
-            // The masked variant is chosen per warp (uniformly) if any of its rows needs it.
-            const bool special = __any_sync(0xffffffffu, diag_tile || qlimit < 32 * blk + 32 || !row_valid);
-            uint8_t* ds_row = sm.ds[s] + (blk >> 1) * kTileBytes + r * 128;
 #pragma unroll
-            for (int sc = 0; sc < 2; ++sc) {  // two 16-column sub-chunks, outputs stored at once
+            for (int h = 0; h < 2; ++h) {  // query half: columns 64h + 16blk .. +15 of this warp
+                const int col0 = 64 * h + 16 * blk;
+                if (!ptx::mbar_wait_warp(&sm.s_full[h], it & 1, abort_flag, status, kDevTimeoutMma) ||
+                    // Per-query constants of this tile (loaded with P1_i and dY_i).
+                    (h == 0 && !ptx::mbar_wait_warp(&sm.q_full[qs], (it / kQStages) & 1, abort_flag, status,
+                                                    kDevTimeoutFull))) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
                 uint32_t sv[16], gv[16];
-                ptx::tmem_ld16(lane_addr + kColS + 32 * blk + 16 * sc, sv);
-                ptx::tmem_ld16(lane_addr + kColDP + 32 * blk + 16 * sc, gv);
+                ptx::tmem_ld16(lane_addr + kColS + col0, sv);
+                ptx::tmem_ld16(lane_addr + kColDP + col0, gv);
                 ptx::tmem_ld_wait();
                 ptx::pin_regs(sv);
                 ptx::pin_regs(gv);
-                if (sc == 1) {
-                    // This warp's part of S^T(i) and dP^T(i) is in registers: the next
-                    // tile's products may overwrite those TMEM columns.
-                    ptx::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(&sm.s_free);
-                }
+                // This warp's part of half h is in registers: the next tile's products
+                // may overwrite those TMEM columns.
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&sm.s_free[h]);
+                const float4* qc = sm.qconst[qs] + col0 / 2;
+                // The masked variant is chosen per warp (uniformly) if any of its rows needs it.
+                const bool special = __any_sync(0xffffffffu, diag_tile || qlimit < col0 + 16 || !row_valid);
                 uint32_t pp[8], dd[8];
                 if (!special)
-                    elementwise16<false>(sv, gv, qc + 8 * sc, 32 * blk + 16 * sc, r, ec, false, 0, pp, dd);
+                    elementwise16<false>(sv, gv, qc, col0, r, ec, false, 0, pp, dd);
                 else
-                    dlam += elementwise16<true>(sv, gv, qc + 8 * sc, 32 * blk + 16 * sc, r, ec, diag_tile, qlimit, pp,
-                                                dd);
-                if (sc == 0) {
+                    dlam += elementwise16<true>(sv, gv, qc, col0, r, ec, diag_tile, qlimit, pp, dd);
+                if (h == 0) {
                     // Before the first store: P^T(i-1) must have been read by dV(i-1), and
                     // dS buffer s by the products of tile i-2 (normally long done).
                     if ((it > 0 &&
@@ -421,10 +429,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     ptx::tc_fence_after();
                 }
-                tmem_st8(lane_addr + kColP + 16 * blk + 8 * sc, pp);
+                // P^T packs query pairs: query column c lives in TMEM column c/2.
+                tmem_st8(lane_addr + kColP + col0 / 2, pp);
+                // dS^T: panel h (64 queries), 16-byte chunks 2blk, 2blk+1 of the 128-byte row.
+                uint8_t* ds_row = sm.ds[s] + h * kTileBytes + r * 128;
 #pragma unroll
                 for (int k2 = 0; k2 < 2; ++k2) {
-                    const int chunk = 4 * (blk & 1) + 2 * sc + k2;
+                    const int chunk = 2 * blk + k2;
                     *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (r & 7)) << 4)) =
                         make_uint4(dd[4 * k2], dd[4 * k2 + 1], dd[4 * k2 + 2], dd[4 * k2 + 3]);
                 }

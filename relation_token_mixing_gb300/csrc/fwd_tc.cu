@@ -209,8 +209,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
+        // The whole warp runs the issue loop; one elected lane issues each MMA.
         ptx::regs_dec<kRegsControl>();
-        if (lane == 0) {
+        {
             const uint32_t id_s = ptx::idesc_bf16(kBM, kBN, false, false);
             const uint32_t id_o = ptx::idesc_bf16(kBM, D, false, true);
             // Descriptors are built once; a byte offset is added as offset >> 4.
@@ -222,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint64_t off = (ks / 4) * kPanelStep + (ks % 4) * 2;  // 32 bytes per K-step
-                    ptx::mma_ss(tmem + t * 128, dq0 + t * kTileStep + off, dk0 + s * kTileStep + off, id_s,
+                    ptx::mma_ss_elect(tmem + t * 128, dq0 + t * kTileStep + off, dk0 + s * kTileStep + off, id_s,
                                 ks > 0 ? 1u : 0u);
                 }
             };
@@ -231,20 +232,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int ks = 0; ks < kBN / 16; ++ks) {
                     // 16 key rows of V per K-step: 2048 bytes of the MN-major tile.
                     const uint32_t p_col = C::kSepP ? C::kColP + 64 * t : 128 * t;
-                    ptx::mma_ts(tmem + 256 + t * D, tmem + p_col + ks * 8, dv0 + s * kTileStep + ks * 128, id_o,
+                    ptx::mma_ts_elect(tmem + 256 + t * D, tmem + p_col + ks * 8, dv0 + s * kTileStep + ks * 128, id_o,
                                 (accumulate || ks > 0) ? 1u : 0u);
                 }
             };
             bool ok = true;
             for (int t = 0; t < 2 && ok; ++t)
-                if (n_t[t] > 0) ok = ptx::mbar_wait(&bars->q_full[t], 0, abort_flag, status, kDevTimeoutFull);
-            if (ok && n_max > 0) ok = ptx::mbar_wait(&bars->k_full[0], 0, abort_flag, status, kDevTimeoutFull);
+                if (n_t[t] > 0) ok = ptx::mbar_wait_warp(&bars->q_full[t], 0, abort_flag, status, kDevTimeoutFull);
+            if (ok && n_max > 0) ok = ptx::mbar_wait_warp(&bars->k_full[0], 0, abort_flag, status, kDevTimeoutFull);
             if (ok) {
                 ptx::tc_fence_after();
                 for (int t = 0; t < 2; ++t) {
                     if (n_t[t] == 0) continue;
                     issue_s(t, 0);
-                    ptx::mma_commit(&bars->s_full[t]);
+                    ptx::mma_commit_elect(&bars->s_full[t]);
                 }
             }
             for (int j = 0; ok && j < n_max; ++j) {
@@ -255,12 +256,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // Next S of each tile as soon as its softmax has S(j) in registers.
                     for (int t = 0; t < 2 && ok; ++t) {
                         if (j + 1 >= n_t[t]) continue;
-                        if (!ptx::mbar_wait(&bars->s_free[t], j & 1, abort_flag, status, kDevTimeoutFull)) {
+                        if (!ptx::mbar_wait_warp(&bars->s_free[t], j & 1, abort_flag, status, kDevTimeoutFull)) {
                             ok = false;
                             break;
                         }
                         if (!k_next_ready) {
-                            if (!ptx::mbar_wait(&bars->k_full[s1], ((j + 1) / C::kStages) & 1, abort_flag, status,
+                            if (!ptx::mbar_wait_warp(&bars->k_full[s1], ((j + 1) / C::kStages) & 1, abort_flag, status,
                                                 kDevTimeoutFull)) {
                                 ok = false;
                                 break;
@@ -269,16 +270,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         ptx::tc_fence_after();
                         issue_s(t, s1);
-                        ptx::mma_commit(&bars->s_full[t]);
+                        ptx::mma_commit_elect(&bars->s_full[t]);
                     }
                     for (int t = 0; t < 2 && ok; ++t) {
                         if (j >= n_t[t]) continue;
-                        if (!ptx::mbar_wait(&bars->p_full[t], j & 1, abort_flag, status, kDevTimeoutFull)) {
+                        if (!ptx::mbar_wait_warp(&bars->p_full[t], j & 1, abort_flag, status, kDevTimeoutFull)) {
                             ok = false;
                             break;
                         }
                         if (!v_ready) {
-                            if (!ptx::mbar_wait(&bars->v_full[s], (j / C::kStages) & 1, abort_flag, status,
+                            if (!ptx::mbar_wait_warp(&bars->v_full[s], (j / C::kStages) & 1, abort_flag, status,
                                                 kDevTimeoutFull)) {
                                 ok = false;
                                 break;
@@ -287,17 +288,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         ptx::tc_fence_after();
                         issue_pv(t, s, j > 0);
-                        ptx::mma_commit(&bars->o_done[t]);
+                        ptx::mma_commit_elect(&bars->o_done[t]);
                     }
                 } else {
                     for (int t = 0; t < 2; ++t) {
                         if (j >= n_t[t]) continue;
-                        if (!ptx::mbar_wait(&bars->p_full[t], j & 1, abort_flag, status, kDevTimeoutFull)) {
+                        if (!ptx::mbar_wait_warp(&bars->p_full[t], j & 1, abort_flag, status, kDevTimeoutFull)) {
                             ok = false;
                             break;
                         }
                         if (!v_ready) {
-                            if (!ptx::mbar_wait(&bars->v_full[s], (j / C::kStages) & 1, abort_flag, status,
+                            if (!ptx::mbar_wait_warp(&bars->v_full[s], (j / C::kStages) & 1, abort_flag, status,
                                                 kDevTimeoutFull)) {
                                 ok = false;
                                 break;
@@ -306,10 +307,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         ptx::tc_fence_after();
                         issue_pv(t, s, j > 0);
-                        ptx::mma_commit(&bars->o_done[t]);
+                        ptx::mma_commit_elect(&bars->o_done[t]);
                         if (j + 1 < n_t[t]) {
                             if (!k_next_ready) {
-                                if (!ptx::mbar_wait(&bars->k_full[s1], ((j + 1) / C::kStages) & 1, abort_flag,
+                                if (!ptx::mbar_wait_warp(&bars->k_full[s1], ((j + 1) / C::kStages) & 1, abort_flag,
                                                     status, kDevTimeoutFull)) {
                                     ok = false;
                                     break;
@@ -318,13 +319,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 ptx::tc_fence_after();
                             }
                             issue_s(t, s1);
-                            ptx::mma_commit(&bars->s_full[t]);
+                            ptx::mma_commit_elect(&bars->s_full[t]);
                         }
                     }
                 }
-                if (ok) ptx::mma_commit(&bars->kv_empty[s]);
+                if (ok) ptx::mma_commit_elect(&bars->kv_empty[s]);
             }
-            ptx::mma_commit(&bars->drain);
+            ptx::mma_commit_elect(&bars->drain);
             drain_wait(&bars->drain, 0);
         }
     } else if (warp < 4) {
