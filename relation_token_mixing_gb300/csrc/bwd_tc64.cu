@@ -163,18 +163,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_dy,
                              const __grid_constant__ CUtensorMap tm_dq, const KernelProblem kp,
                              const float* __restrict__ L, const float* __restrict__ Dw, __nv_bfloat16* __restrict__ dP2,
-                             __nv_bfloat16* __restrict__ dV, float* __restrict__ dlambda, unsigned int* status) {
+                             __nv_bfloat16* __restrict__ dV, float* __restrict__ dlambda, unsigned int* status,
+                             int head_group) {
     extern __shared__ uint8_t smem_raw[];
     Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.x;
-    const int jt = blockIdx.y;
     const int T = kp.T;
+    const int nt_all = (T + kTile - 1) / kTile;
+    int bh, jt;  // key tile jt of head bh; causal: low jt (most query tiles) first
+    grouped_tile_order(blockIdx.x, kp.BH, nt_all, head_group, bh, jt);
     const int kv0 = jt * kTile;
-    const int nq_all = (T + kTile - 1) / kTile;
     const int i_first = kp.causal ? jt : 0;
-    const int n_q = nq_all - i_first;
+    const int n_q = nt_all - i_first;
     const float k_scale = 0.5f * kp.inv_sqrt_d;
 
     if (threadIdx.x == 0) {
@@ -306,11 +307,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 issue_s_dp(0, 0);
                 issue_s_dp(0, 1);
             }
+            // dP1_t = dS_t P2_j: A = dS_t (MN-major view of dS^T buffer t&1), K over key
+            // rows.  Issued one tile late, early in tile t+1: dS_t is complete and the
+            // reduce warps have had a whole tile to drain dP1_{t-1} from TMEM, so the
+            // products of the next tiles never queue behind the reduction.
+            auto issue_dq = [&](int t) -> bool {
+                if (t > 0 && !ptx::mbar_wait_warp(&sm.dq_free, (t - 1) & 1, abort_flag, status, kDevTimeoutMma))
+                    return false;
+                ptx::tc_fence_after();
+                const uint32_t sm_lo = sm_lo0 + ((t & 1) ? kStageS : 0u);
+#pragma unroll
+                for (int ks = 0; ks < kTile / 16; ++ks)
+                    ptx::mma_ss_elect(tmem + kColDQ, sm_lo + 128 * ks, hi_m, km_lo + 128 * ks, hi_m, id_dq,
+                                      ks > 0 ? 1u : 0u);
+                ptx::mma_commit_elect(&sm.dq_full);
+                ptx::mma_commit_elect(&sm.ds_free[t & 1]);
+                return true;
+            };
             for (int it = 0; ok && it < n_q; ++it) {
                 const int s = it & 1;          // dS buffer
                 const int qs = it % kQStages;  // P1/dY stage
                 if (it + 1 < n_q) {
-                    // Each half of S^T(i+1), dP^T(i+1) as soon as every elementwise warp
+                    // First half of S^T(i+1), dP^T(i+1) as soon as every elementwise warp
                     // has that half of tile i in registers.
                     const int qn = (it + 1) % kQStages;
                     if (!ptx::mbar_wait_warp(&sm.s_free[0], it & 1, abort_flag, status, kDevTimeoutFull) ||
@@ -319,6 +337,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     ptx::tc_fence_after();
                     issue_s_dp(qn, 0);
+                }
+                if (it > 0 && !issue_dq(it - 1)) break;
+                if (it + 1 < n_q) {
+                    const int qn = (it + 1) % kQStages;
                     if (!ptx::mbar_wait_warp(&sm.s_free[1], it & 1, abort_flag, status, kDevTimeoutFull)) break;
                     ptx::tc_fence_after();
                     issue_s_dp(qn, 1);
@@ -328,27 +350,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // dV += P^T dY_i: K-step ks covers queries 16ks..16ks+15 (8 packed TMEM
                 // columns; 16 dY rows = 2048 bytes of the MN-major tile).
                 const uint32_t gm_lo = gm_lo0 + qs * kStageQ, qm_lo = qm_lo0 + qs * kStageQ;
-                const uint32_t sk_lo = sk_lo0 + (s ? kStageS : 0u), sm_lo = sm_lo0 + (s ? kStageS : 0u);
+                const uint32_t sk_lo = sk_lo0 + (s ? kStageS : 0u);
                 const uint32_t acc0 = it > 0 ? 1u : 0u;
 #pragma unroll
                 for (int ks = 0; ks < kTile / 16; ++ks)
                     ptx::mma_ts_elect(tmem + kColDV, tmem + kColP + 8 * ks, gm_lo + 128 * ks, hi_m, id_dv,
-                                   ks > 0 ? 1u : acc0);
+                                      ks > 0 ? 1u : acc0);
                 ptx::mma_commit_elect(&sm.pv_done);
                 // dP2 += dS^T P1_i: A K-major over the two 64-query panels of dS^T.
 #pragma unroll
                 for (int ks = 0; ks < kTile / 16; ++ks)
-                    ptx::mma_ss_elect(tmem + kColDK, sk_lo + (ks >> 2) * kStageQ + 2 * (ks & 3), hi_k, qm_lo + 128 * ks,
-                                   hi_m, id_dk, ks > 0 ? 1u : acc0);
+                    ptx::mma_ss_elect(tmem + kColDK, sk_lo + (ks >> 2) * kStageQ + 2 * (ks & 3), hi_k,
+                                      qm_lo + 128 * ks, hi_m, id_dk, ks > 0 ? 1u : acc0);
                 ptx::mma_commit_elect(&sm.q_empty[qs]);  // P1_i and dY_i are no longer read
-                if (it > 0 && !ptx::mbar_wait_warp(&sm.dq_free, (it - 1) & 1, abort_flag, status, kDevTimeoutMma)) break;
-                // dP1_i = dS P2_j: A = dS (MN-major view of the same bytes), K over key rows.
-#pragma unroll
-                for (int ks = 0; ks < kTile / 16; ++ks)
-                    ptx::mma_ss_elect(tmem + kColDQ, sm_lo + 128 * ks, hi_m, km_lo + 128 * ks, hi_m, id_dq,
-                                   ks > 0 ? 1u : 0u);
-                ptx::mma_commit_elect(&sm.dq_full);
-                ptx::mma_commit_elect(&sm.ds_free[s]);
+                if (it + 1 == n_q && !issue_dq(it)) break;
             }
             ptx::mma_commit_elect(&sm.mma_done);
             drain_wait(&sm.mma_done, 0);
@@ -550,9 +565,23 @@ cudaError_t launch_bwd_tc64(const KernelProblem& kp, const void* P1, const void*
     cudaError_t e = make_tensor_map_3d(&mq, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kD, kp.T, kp.BH, 32, 128,
                                        CU_TENSOR_MAP_SWIZZLE_128B);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)kp.BH, (unsigned)((kp.T + kTile - 1) / kTile));
+    const int64_t ctas = kp.BH * ((kp.T + kTile - 1) / kTile);
+    if (ctas > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    // Heads in flight: as many as fit in three quarters of L2 with P1, P2, V, dY
+    // (bf16) and the fp32 dP1 accumulator of each, i.e. 12 T d bytes per head.
+    static std::once_flag l2_once;
+    static int l2_bytes = 0;
+    std::call_once(l2_once, [] {
+        int dev = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&l2_bytes, cudaDevAttrL2CacheSize, dev);
+    });
+    const int64_t per_head = 12 * (int64_t)kp.T * kD;
+    int64_t group = (l2_bytes > 0 ? (int64_t)l2_bytes * 3 / 4 : (int64_t)96 << 20) / per_head;
+    group = group < 1 ? 1 : (group > kp.BH ? kp.BH : group);
+    dim3 grid((unsigned)ctas);
     relation_bwd_tc64_kernel<<<grid, kThreads, kSmemBytes, s>>>(m1, m2, mv, mg, mq, kp, L, Dw, (__nv_bfloat16*)dP2,
-                                                                (__nv_bfloat16*)dV, dlambda, tl.status);
+                                                                (__nv_bfloat16*)dV, dlambda, tl.status,
+                                                                (int)group);
     return cudaGetLastError();
 }
 

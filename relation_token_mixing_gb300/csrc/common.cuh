@@ -29,6 +29,21 @@ struct KernelProblem {
     float inv_sqrt_d;
 };
 
+// CTA launch order of the key-stationary backward: the linear block index
+// walks groups of `group` heads; inside a group it walks tile index 0 of all
+// those heads, then tile 1, and so on (heaviest first for causal masks), so the
+// causal tail stays short while the heads in flight at any time stay few enough
+// for their inputs and fp32 accumulators to remain in L2.
+__device__ __forceinline__ void grouped_tile_order(unsigned idx, int64_t BH, int n_tiles, int group, int& bh,
+                                                   int& tile) {
+    const unsigned per_group = (unsigned)group * (unsigned)n_tiles;
+    const int64_t g = idx / per_group;
+    const int r = (int)(idx - g * per_group);
+    const int heads = (int)((BH - g * group) < group ? (BH - g * group) : group);
+    tile = r / heads;
+    bh = (int)(g * group) + (r - tile * heads);
+}
+
 // Records the first failure in the status word; never traps.
 __device__ __forceinline__ void record_status(unsigned int* status, unsigned int code) {
     if (status != nullptr) atomicCAS(status, 0u, code);
