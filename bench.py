@@ -337,7 +337,7 @@ def main():
     mean_fwd, mean_main = statistics.mean(t_fwd), statistics.mean(t_main)
     if mean_main >= mean_fwd:
         if w.d == 64:
-            dom, srcs = "relation_bwd_tc64_kernel", ["bwd_tc64.cu", "ptx_sm100.cuh", "common.cuh"]
+            dom, srcs = "relation_bwd_tc64_kernel<true>", ["bwd_tc64.cu", "ptx_sm100.cuh", "common.cuh"]
         else:
             dom, srcs = f"relation_bwd_tc_kernel<{w.d}>", ["bwd_tc.cu", "ptx_sm100.cuh"]
         dom_ms, dom_flops = mean_main, f_bwd

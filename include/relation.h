@@ -18,10 +18,13 @@
  * P1 and P2 arrive already rotated by RoPE (Appendix B.3).
  *
  * Conventions shared by every entry point:
- *  - Tensors are contiguous [B, H, T, d_h] (d_h innermost) in the problem's
- *    dtype; L and the workspace are float32.  All tensor pointers are device
- *    pointers owned by the caller; the library keeps no reference after a call
- *    returns and allocates no device memory per call.
+ *  - Operand tensors (P1, P2, V, Y, dY, dP1, dP2, dV) are contiguous in the
+ *    problem's dtype and layout: [B, H, T, d_h] (RELATION_LAYOUT_BHTD) or
+ *    [B, T, H, d_h] (RELATION_LAYOUT_BTHD, the heads of a [B, T, H*d_h]
+ *    projection output used in place); d_h is innermost in both.  L is always
+ *    [B, H, T] float32; the workspace is float32.  All tensor pointers are
+ *    device pointers owned by the caller; the library keeps no reference after
+ *    a call returns and allocates no device memory per call.
  *  - Every tensor pointer must be 16-byte aligned (RELATION_ERR_MISALIGNED).
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *    stream) and nothing synchronises.  Argument errors are reported before any
@@ -29,9 +32,12 @@
  *  - Device-side waits are bounded: if one expires the kernel records the
  *    event in a library-owned device word and returns early;
  *    relation_check_device_status() reports it after the caller synchronises.
- *  - Supported: d_h in {64, 128}; dtype RELATION_BF16 (tensor-core path,
- *    fp32 accumulation) or RELATION_F32 (fp32 CUDA-core path); any T >= 1;
- *    causal or not.  Other sizes return RELATION_ERR_UNSUPPORTED.
+ *  - Supported: d_h in {48, 60, 64, 80, 128} (the paper's model widths,
+ *    Table 2 and Appendix F.1, plus 128); dtype RELATION_BF16 (tensor-core
+ *    path with fp32 accumulation; d_h = 60, whose 120-byte rows the tensor
+ *    memory accelerator cannot address, runs on the CUDA-core kernels) or
+ *    RELATION_F32 (fp32 CUDA-core path); any T >= 1; causal or not; either
+ *    layout.  Other widths return RELATION_ERR_UNSUPPORTED.
  *  - No entry point throws, aborts, or falls back to the CPU.
  */
 #ifndef RELATION_GB300_RELATION_H_
@@ -44,7 +50,8 @@
 extern "C" {
 #endif
 
-#define RELATION_ABI_VERSION 1
+/* 2: relation_problem_t gained `layout`. */
+#define RELATION_ABI_VERSION 2
 
 typedef enum {
     RELATION_OK = 0,
@@ -58,6 +65,9 @@ typedef enum {
 
 typedef enum { RELATION_F32 = 0, RELATION_BF16 = 1 } relation_dtype_t;
 
+/* Memory order of the operand tensors (see the conventions above). */
+typedef enum { RELATION_LAYOUT_BHTD = 0, RELATION_LAYOUT_BTHD = 1 } relation_layout_t;
+
 /* One operator invocation: B*H independent heads of length T and width d_h. */
 typedef struct {
     int64_t B, H, T, d_h;
@@ -65,6 +75,7 @@ typedef struct {
     float tau_S;    /* Self temperature, > 0 (eq.(2); the paper fixes 2) */
     float lambda;   /* count-correction coefficient lambda_l (eq.(2); init 0.5); 0 disables it */
     int32_t causal; /* nonzero: mask j > i as in eq.(2) */
+    int32_t layout; /* relation_layout_t of P1, P2, V, Y, dY, dP1, dP2, dV; L stays [B, H, T] */
 } relation_problem_t;
 
 /*

@@ -19,6 +19,8 @@ from . import build as _build
 
 RELATION_F32 = 0
 RELATION_BF16 = 1
+RELATION_LAYOUT_BHTD = 0  # operands [B, H, T, d_h]
+RELATION_LAYOUT_BTHD = 1  # operands [B, T, H, d_h]
 
 STATUS = {
     0: "RELATION_OK",
@@ -49,6 +51,7 @@ class Problem(ctypes.Structure):
         ("tau_S", ctypes.c_float),
         ("lam", ctypes.c_float),
         ("causal", ctypes.c_int32),
+        ("layout", ctypes.c_int32),
     ]
 
 
@@ -129,17 +132,23 @@ def _check(code: int, what: str) -> None:
         raise RelationError(code, what, msg)
 
 
-def problem_for(t: torch.Tensor, tau_S: float, lam: float, causal: bool) -> Problem:
+def problem_for(t: torch.Tensor, tau_S: float, lam: float, causal: bool, layout: int = RELATION_LAYOUT_BHTD) -> Problem:
+    """Problem for operand tensors shaped [B, H, T, d_h] (BHTD) or [B, T, H, d_h] (BTHD)."""
     if t.dim() != 4:
-        raise ValueError("expected [B, H, T, d_h] tensors")
+        raise ValueError("expected 4-D operand tensors")
     if t.dtype == torch.bfloat16:
         dt = RELATION_BF16
     elif t.dtype == torch.float32:
         dt = RELATION_F32
     else:
         raise ValueError(f"unsupported dtype {t.dtype}")
-    B, H, T, d = t.shape
-    return Problem(B, H, T, d, dt, float(tau_S), float(lam), 1 if causal else 0)
+    if layout == RELATION_LAYOUT_BHTD:
+        B, H, T, d = t.shape
+    elif layout == RELATION_LAYOUT_BTHD:
+        B, T, H, d = t.shape
+    else:
+        raise ValueError(f"unknown layout {layout}")
+    return Problem(B, H, T, d, dt, float(tau_S), float(lam), 1 if causal else 0, int(layout))
 
 
 # ------------------------------------------------------------------ C-ABI calls
@@ -199,18 +208,20 @@ def relation_abi_version() -> int:
 
 
 # ------------------------------------------------------- tensor-level helpers
-def fwd(P1, P2, V, tau_S: float, lam: float, causal: bool = True, stream=None, want_L: bool = True):
-    """Allocates Y (and L) and runs relation_fwd; returns (Y, L)."""
-    prob = problem_for(P1, tau_S, lam, causal)
+def fwd(P1, P2, V, tau_S: float, lam: float, causal: bool = True, stream=None, want_L: bool = True,
+        layout: int = RELATION_LAYOUT_BHTD):
+    """Allocates Y (and L [B, H, T]) and runs relation_fwd; returns (Y, L)."""
+    prob = problem_for(P1, tau_S, lam, causal, layout)
     Y = torch.empty_like(V)
-    L = torch.empty(P1.shape[:3], dtype=torch.float32, device=P1.device) if want_L else None
+    L = torch.empty((prob.B, prob.H, prob.T), dtype=torch.float32, device=P1.device) if want_L else None
     relation_fwd(prob, P1, P2, V, Y, L, stream)
     return Y, L
 
 
-def bwd(P1, P2, V, Y, L, dY, tau_S: float, lam: float, causal: bool = True, stream=None, workspace=None):
+def bwd(P1, P2, V, Y, L, dY, tau_S: float, lam: float, causal: bool = True, stream=None, workspace=None,
+        layout: int = RELATION_LAYOUT_BHTD):
     """Allocates the gradients and workspace and runs relation_bwd; returns (dP1, dP2, dV, dlambda)."""
-    prob = problem_for(P1, tau_S, lam, causal)
+    prob = problem_for(P1, tau_S, lam, causal, layout)
     dP1, dP2, dV = torch.empty_like(P1), torch.empty_like(P2), torch.empty_like(V)
     dlam = torch.empty(1, dtype=torch.float32, device=P1.device)
     if workspace is None:

@@ -93,6 +93,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bh = blockIdx.x;
+    const int batch = bh / kp.H, head = bh - batch * kp.H;
     const int jt = blockIdx.y;  // key tile; low tiles see the most query tiles
     const int T = kp.T;
     const int kv0 = jt * kTile;
@@ -133,8 +134,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tma_prefetch_desc(&tm_dy);
             ptx::mbar_arrive_expect_tx(&bars->kv_full, 2 * C::kTileBytes);
             for (int p = 0; p < C::kPanels; ++p) {
-                ptx::tma_load_3d(sK + p * kPanelBytes, &tm_p2, &bars->kv_full, p * 64, kv0, bh);
-                ptx::tma_load_3d(sV + p * kPanelBytes, &tm_v, &bars->kv_full, p * 64, kv0, bh);
+                ptx::tma_load_operand(sK + p * kPanelBytes, &tm_p2, &bars->kv_full, p * 64, kv0, bh, head, batch,
+                                      kp.layout == 0);
+                ptx::tma_load_operand(sV + p * kPanelBytes, &tm_v, &bars->kv_full, p * 64, kv0, bh, head, batch,
+                                      kp.layout == 0);
             }
         }
         int it = 0;
@@ -159,10 +162,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) {
                 ptx::mbar_arrive_expect_tx(&bars->q_full[s], 2 * C::kTileBytes);
                 for (int p = 0; p < C::kPanels; ++p) {
-                    ptx::tma_load_3d(sQ + s * C::kTileBytes + p * kPanelBytes, &tm_p1, &bars->q_full[s], p * 64,
-                                     i * kTile, bh);
-                    ptx::tma_load_3d(sG + s * C::kTileBytes + p * kPanelBytes, &tm_dy, &bars->q_full[s], p * 64,
-                                     i * kTile, bh);
+                    ptx::tma_load_operand(sQ + s * C::kTileBytes + p * kPanelBytes, &tm_p1, &bars->q_full[s], p * 64,
+                                     i * kTile, bh, head, batch, kp.layout == 0);
+                    ptx::tma_load_operand(sG + s * C::kTileBytes + p * kPanelBytes, &tm_dy, &bars->q_full[s], p * 64,
+                                     i * kTile, bh, head, batch, kp.layout == 0);
                 }
             } else {
                 ptx::mbar_arrive(&bars->q_full[s]);
@@ -337,22 +340,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_after();
 #pragma unroll
             for (int which = 0; which < 2; ++which) {
-                __nv_bfloat16* dst_row = (which == 0 ? dV : dP2) + ((size_t)bh * T + kv) * D;
+                __nv_bfloat16* dst_row = (which == 0 ? dV : dP2) + row_offset(kp, bh, row_valid ? kv : 0);
                 const uint32_t col = which == 0 ? C::kColDV : C::kColDK;
 #pragma unroll
                 for (int c0 = 0; c0 < D / 32; ++c0) {
+                    if (32 * c0 >= kp.d) break;  // zero-padding columns of a narrower head
                     uint32_t ov[32];
                     ptx::tmem_ld32(lane_addr + col + 32 * c0, ov);
                     ptx::tmem_ld_wait();
                     ptx::pin_regs(ov);
                     if (row_valid) {
-                        uint4* dst = reinterpret_cast<uint4*>(dst_row + 32 * c0);
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
-                            dst[k] = make_uint4(ptx::pack_bf16x2(as_f(ov[8 * k + 0]), as_f(ov[8 * k + 1])),
-                                                ptx::pack_bf16x2(as_f(ov[8 * k + 2]), as_f(ov[8 * k + 3])),
-                                                ptx::pack_bf16x2(as_f(ov[8 * k + 4]), as_f(ov[8 * k + 5])),
-                                                ptx::pack_bf16x2(as_f(ov[8 * k + 6]), as_f(ov[8 * k + 7])));
+                            store_bf16x8(dst_row, 32 * c0 + 8 * k, kp.d,
+                                         ptx::pack_bf16x2(as_f(ov[8 * k + 0]), as_f(ov[8 * k + 1])),
+                                         ptx::pack_bf16x2(as_f(ov[8 * k + 2]), as_f(ov[8 * k + 3])),
+                                         ptx::pack_bf16x2(as_f(ov[8 * k + 4]), as_f(ov[8 * k + 5])),
+                                         ptx::pack_bf16x2(as_f(ov[8 * k + 6]), as_f(ov[8 * k + 7])));
                     }
                 }
             }
@@ -407,12 +411,14 @@ cudaError_t launch_bwd_tc_d(const KernelProblem& kp, const void* P1, const void*
                                         C::kSmemBytes);
     });
     if (attr_err != cudaSuccess) return attr_err;
+    // Operands in the problem's layout; heads narrower than D read as D-wide tiles
+    // with zero columns.
     CUtensorMap m1, m2, mv, mg;
     const void* bases[4] = {P1, P2, V, dY};
     CUtensorMap* maps[4] = {&m1, &m2, &mv, &mg};
     for (int k = 0; k < 4; ++k) {
-        cudaError_t e = make_tensor_map_3d(maps[k], bases[k], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, kp.T, kp.BH,
-                                           64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+        cudaError_t e =
+            make_operand_map(maps[k], bases[k], kp.BH / kp.H, kp.H, kp.T, kp.d, kp.layout, 64, 128, true);
         if (e != cudaSuccess) return e;
     }
     dim3 grid((unsigned)kp.BH, (unsigned)((kp.T + kTile - 1) / kTile));
@@ -427,8 +433,8 @@ cudaError_t launch_bwd_tc_d(const KernelProblem& kp, const void* P1, const void*
 cudaError_t launch_bwd_tc(const KernelProblem& kp, const void* P1, const void* P2, const void* V, const float* L,
                           const float* Dw, const void* dY, float* dq_acc, void* dP2, void* dV, float* dlambda,
                           const TcLaunch& tl, cudaStream_t s) {
-    if (kp.d == 64) return launch_bwd_tc64(kp, P1, P2, V, L, Dw, dY, dq_acc, dP2, dV, dlambda, tl, s);
-    if (kp.d == 128) return launch_bwd_tc_d<128>(kp, P1, P2, V, L, Dw, dY, dq_acc, dP2, dV, tl, s);
+    if (kp.d == 48 || kp.d == 64) return launch_bwd_tc64(kp, P1, P2, V, L, Dw, dY, dq_acc, dP2, dV, dlambda, tl, s);
+    if (kp.d == 80 || kp.d == 128) return launch_bwd_tc_d<128>(kp, P1, P2, V, L, Dw, dY, dq_acc, dP2, dV, tl, s);
     return cudaErrorInvalidValue;
 }
 

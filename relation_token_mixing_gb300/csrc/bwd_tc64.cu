@@ -158,6 +158,8 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
                  : "memory");
 }
 
+// kRank3: operands through 3-D maps ([B, H, T, d] layout), else 4-D maps.
+template <bool kRank3>
 __global__ void __launch_bounds__(kThreads, 1)
     relation_bwd_tc64_kernel(const __grid_constant__ CUtensorMap tm_p1, const __grid_constant__ CUtensorMap tm_p2,
                              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_dy,
@@ -173,6 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nt_all = (T + kTile - 1) / kTile;
     int bh, jt;  // key tile jt of head bh; causal: low jt (most query tiles) first
     grouped_tile_order(blockIdx.x, kp.BH, nt_all, head_group, bh, jt);
+    const int batch = bh / kp.H, head = bh - batch * kp.H;
     const int kv0 = jt * kTile;
     const int i_first = kp.causal ? jt : 0;
     const int n_q = nt_all - i_first;
@@ -217,8 +220,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tma_prefetch_desc(&tm_dy);
             ptx::tma_prefetch_desc(&tm_dq);
             ptx::mbar_arrive_expect_tx(&sm.kv_full, 2 * kTileBytes);
-            ptx::tma_load_3d(sm.k, &tm_p2, &sm.kv_full, 0, kv0, bh);
-            ptx::tma_load_3d(sm.v, &tm_v, &sm.kv_full, 0, kv0, bh);
+            ptx::tma_load_operand(sm.k, &tm_p2, &sm.kv_full, 0, kv0, bh, head, batch, kRank3);
+            ptx::tma_load_operand(sm.v, &tm_v, &sm.kv_full, 0, kv0, bh, head, batch, kRank3);
         }
         int it = 0;
         for (; it < n_q; ++it) {
@@ -250,8 +253,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (lane == 0) {
                 ptx::mbar_arrive_expect_tx(&sm.q_full[s], 2 * kTileBytes);
-                ptx::tma_load_3d(sm.q[s], &tm_p1, &sm.q_full[s], 0, i * kTile, bh);
-                ptx::tma_load_3d(sm.g[s], &tm_dy, &sm.q_full[s], 0, i * kTile, bh);
+                ptx::tma_load_operand(sm.q[s], &tm_p1, &sm.q_full[s], 0, i * kTile, bh, head, batch,
+                                      kRank3);
+                ptx::tma_load_operand(sm.g[s], &tm_dy, &sm.q_full[s], 0, i * kTile, bh, head, batch,
+                                      kRank3);
             } else {
                 ptx::mbar_arrive(&sm.q_full[s]);
             }
@@ -472,20 +477,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok && ptx::mbar_wait_warp(&sm.mma_done, 0, abort_flag, status, kDevTimeoutMma)) {
             ptx::tc_fence_after();
             const int c0 = blk & 1;
-            __nv_bfloat16* dst_row = (blk < 2 ? dV : dP2) + ((size_t)bh * T + kv) * kD + 32 * c0;
+            __nv_bfloat16* dst_row = (blk < 2 ? dV : dP2) + row_offset(kp, bh, row_valid ? kv : 0);
             const uint32_t col = (blk < 2 ? kColDV : kColDK) + 32 * c0;
             uint32_t ov[32];
             ptx::tmem_ld32(lane_addr + col, ov);
             ptx::tmem_ld_wait();
             ptx::pin_regs(ov);
             if (row_valid) {
-                uint4* dst = reinterpret_cast<uint4*>(dst_row);
+                // Columns past the head width (zero padding of the tiles) are not written.
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    dst[k] = make_uint4(ptx::pack_bf16x2(as_f(ov[8 * k + 0]), as_f(ov[8 * k + 1])),
-                                        ptx::pack_bf16x2(as_f(ov[8 * k + 2]), as_f(ov[8 * k + 3])),
-                                        ptx::pack_bf16x2(as_f(ov[8 * k + 4]), as_f(ov[8 * k + 5])),
-                                        ptx::pack_bf16x2(as_f(ov[8 * k + 6]), as_f(ov[8 * k + 7])));
+                    store_bf16x8(dst_row, 32 * c0 + 8 * k, kp.d, ptx::pack_bf16x2(as_f(ov[8 * k + 0]), as_f(ov[8 * k + 1])),
+                                 ptx::pack_bf16x2(as_f(ov[8 * k + 2]), as_f(ov[8 * k + 3])),
+                                 ptx::pack_bf16x2(as_f(ov[8 * k + 4]), as_f(ov[8 * k + 5])),
+                                 ptx::pack_bf16x2(as_f(ov[8 * k + 6]), as_f(ov[8 * k + 7])));
             }
         }
     } else {
@@ -549,19 +554,25 @@ cudaError_t launch_bwd_tc64(const KernelProblem& kp, const void* P1, const void*
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(relation_bwd_tc64_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr_err = cudaFuncSetAttribute(relation_bwd_tc64_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         kSmemBytes);
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(relation_bwd_tc64_kernel<false>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     });
     if (attr_err != cudaSuccess) return attr_err;
+    // Operands in the problem's layout; heads narrower than 64 read as 64-wide
+    // tiles whose extra columns are zero (so they add nothing to any product).
     CUtensorMap m1, m2, mv, mg, mq;
     const void* bases[4] = {P1, P2, V, dY};
     CUtensorMap* maps[4] = {&m1, &m2, &mv, &mg};
     for (int k = 0; k < 4; ++k) {
-        cudaError_t e = make_tensor_map_3d(maps[k], bases[k], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kD, kp.T, kp.BH,
-                                           64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+        cudaError_t e =
+            make_operand_map(maps[k], bases[k], kp.BH / kp.H, kp.H, kp.T, kp.d, kp.layout, 64, 128, true);
         if (e != cudaSuccess) return e;
     }
-    // dP1 accumulator: fp32 [BH, T, 64], reduced in 32-column (128-byte) swizzled boxes.
+    // dP1 accumulator: fp32 [BH, T, 64] (its own padded layout), reduced in
+    // 32-column (128-byte) swizzled boxes.
     cudaError_t e = make_tensor_map_3d(&mq, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kD, kp.T, kp.BH, 32, 128,
                                        CU_TENSOR_MAP_SWIZZLE_128B);
     if (e != cudaSuccess) return e;
@@ -579,9 +590,12 @@ cudaError_t launch_bwd_tc64(const KernelProblem& kp, const void* P1, const void*
     int64_t group = (l2_bytes > 0 ? (int64_t)l2_bytes * 3 / 4 : (int64_t)96 << 20) / per_head;
     group = group < 1 ? 1 : (group > kp.BH ? kp.BH : group);
     dim3 grid((unsigned)ctas);
-    relation_bwd_tc64_kernel<<<grid, kThreads, kSmemBytes, s>>>(m1, m2, mv, mg, mq, kp, L, Dw, (__nv_bfloat16*)dP2,
-                                                                (__nv_bfloat16*)dV, dlambda, tl.status,
-                                                                (int)group);
+    if (kp.layout == 0)
+        relation_bwd_tc64_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(
+            m1, m2, mv, mg, mq, kp, L, Dw, (__nv_bfloat16*)dP2, (__nv_bfloat16*)dV, dlambda, tl.status, (int)group);
+    else
+        relation_bwd_tc64_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(
+            m1, m2, mv, mg, mq, kp, L, Dw, (__nv_bfloat16*)dP2, (__nv_bfloat16*)dV, dlambda, tl.status, (int)group);
     return cudaGetLastError();
 }
 

@@ -17,8 +17,9 @@ enum DeviceStatus : unsigned int {
     kDevBadLaunch = 4,      // a kernel saw a launch shape it was not built for
 };
 
-// Kernel-side view of one problem.  Strides are in elements of the tensors;
-// all tensors are contiguous [B*H, T, d].
+// Kernel-side view of one problem.  Operand tensors (P1, P2, V, Y, dY, dP1,
+// dP2, dV) are contiguous [B, H, T, d] (layout 0) or [B, T, H, d] (layout 1);
+// L, D and the dP1 accumulator are always [B*H, T(, d_pad)].
 struct KernelProblem {
     int64_t BH;
     int T;
@@ -27,7 +28,30 @@ struct KernelProblem {
     float lambda;
     int causal;
     float inv_sqrt_d;
+    int H;
+    int layout;
 };
+
+// Element offset of row t of head bh (= b*H + h) in an operand tensor.
+__host__ __device__ __forceinline__ size_t row_offset(const KernelProblem& kp, int64_t bh, int64_t t) {
+    if (kp.layout == 0) return ((size_t)bh * (size_t)kp.T + (size_t)t) * (size_t)kp.d;
+    const int64_t b = bh / kp.H, h = bh - b * kp.H;
+    return (((size_t)b * (size_t)kp.T + (size_t)t) * (size_t)kp.H + (size_t)h) * (size_t)kp.d;
+}
+
+// Stores columns c..c+7 (four packed bf16 pairs) of one row of width d (d a
+// multiple of 4, c a multiple of 8): one 16-byte store when the whole group is
+// inside the row and rows are 16-byte aligned (d % 8 == 0), else 8-byte halves;
+// columns >= d are not written.
+__device__ __forceinline__ void store_bf16x8(__nv_bfloat16* row, int c, int d, uint32_t w0, uint32_t w1, uint32_t w2,
+                                             uint32_t w3) {
+    if (c + 8 <= d && (d & 7) == 0) {
+        *reinterpret_cast<uint4*>(row + c) = make_uint4(w0, w1, w2, w3);
+        return;
+    }
+    if (c + 4 <= d) *reinterpret_cast<uint2*>(row + c) = make_uint2(w0, w1);
+    if (c + 8 <= d) *reinterpret_cast<uint2*>(row + c + 4) = make_uint2(w2, w3);
+}
 
 // CTA launch order of the key-stationary backward: the linear block index
 // walks groups of `group` heads; inside a group it walks tile index 0 of all

@@ -128,6 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bh = blockIdx.x;
+    const int batch = bh / kp.H, head = bh - batch * kp.H;
     const int pair = (int)gridDim.y - 1 - (int)blockIdx.y;  // heaviest (latest) query rows first
     const int T = kp.T;
     const int q_base = pair * 2 * kBM;
@@ -177,8 +178,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (n_t[t] == 0) continue;
                 ptx::mbar_arrive_expect_tx(&bars->q_full[t], C::kTileBytes);
                 for (int p = 0; p < C::kPanels; ++p)
-                    ptx::tma_load_3d(sQ + t * C::kTileBytes + p * kPanelBytes, &tm_p1, &bars->q_full[t], p * 64,
-                                     q_base + t * kBM, bh);
+                    ptx::tma_load_4d(sQ + t * C::kTileBytes + p * kPanelBytes, &tm_p1, &bars->q_full[t], p * 64,
+                                     q_base + t * kBM, head, batch);
             }
             int j = 0;
             for (; j < n_max; ++j) {
@@ -189,12 +190,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 ptx::mbar_arrive_expect_tx(&bars->k_full[s], C::kTileBytes);
                 for (int p = 0; p < C::kPanels; ++p)
-                    ptx::tma_load_3d(sK + s * C::kTileBytes + p * kPanelBytes, &tm_p2, &bars->k_full[s], p * 64,
-                                     j * kBN, bh);
+                    ptx::tma_load_4d(sK + s * C::kTileBytes + p * kPanelBytes, &tm_p2, &bars->k_full[s], p * 64,
+                                     j * kBN, head, batch);
                 ptx::mbar_arrive_expect_tx(&bars->v_full[s], C::kTileBytes);
                 for (int p = 0; p < C::kPanels; ++p)
-                    ptx::tma_load_3d(sV + s * C::kTileBytes + p * kPanelBytes, &tm_v, &bars->v_full[s], p * 64,
-                                     j * kBN, bh);
+                    ptx::tma_load_4d(sV + s * C::kTileBytes + p * kPanelBytes, &tm_v, &bars->v_full[s], p * 64,
+                                     j * kBN, head, batch);
             }
             if (*abort_flag) {
                 // Let the copies already issued land before the CTA exits.
@@ -470,9 +471,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok && nt > 0 && ptx::mbar_wait_warp(&bars->o_done[t], (nt - 1) & 1, abort_flag, status, kDevTimeoutMma)) {
             ptx::tc_fence_after();
             const float inv_l = 1.f / l;
-            __nv_bfloat16* yrow = Y + ((size_t)bh * T + i) * D;
+            __nv_bfloat16* yrow = Y + row_offset(kp, bh, i < T ? i : 0);
 #pragma unroll
             for (int c0 = 0; c0 < D / 32; ++c0) {
+                if (32 * c0 >= kp.d) break;  // columns past the head width are zero padding
                 uint32_t ov[32];
                 ptx::tmem_ld32(lane_addr + o_col + 32 * c0, ov);
                 ptx::tmem_ld_wait();
@@ -482,10 +484,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int k = 0; k < 16; ++k)
                         pkd[k] = ptx::pack_bf16x2(as_f(ov[2 * k]) * inv_l, as_f(ov[2 * k + 1]) * inv_l);
-                    uint4* dst = reinterpret_cast<uint4*>(yrow + 32 * c0);
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        dst[k] = make_uint4(pkd[4 * k], pkd[4 * k + 1], pkd[4 * k + 2], pkd[4 * k + 3]);
+                        store_bf16x8(yrow, 32 * c0 + 8 * k, kp.d, pkd[4 * k], pkd[4 * k + 1], pkd[4 * k + 2],
+                                     pkd[4 * k + 3]);
                 }
             }
             if (L != nullptr && i < T) L[(size_t)bh * T + i] = m + __log2f(l) * kLn2 - corr;
@@ -510,17 +512,13 @@ cudaError_t launch_fwd_tc_d(const KernelProblem& kp, const void* P1, const void*
                                         C::kSmemBytes);
     });
     if (attr_err != cudaSuccess) return attr_err;
+    // Heads narrower than D read as D-wide tiles whose extra columns are zero.
     CUtensorMap m1, m2, mv;
     cudaError_t e;
-    if ((e = make_tensor_map_3d(&m1, P1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, kp.T, kp.BH, 64, 128,
-                                CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
-        return e;
-    if ((e = make_tensor_map_3d(&m2, P2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, kp.T, kp.BH, 64, 128,
-                                CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
-        return e;
-    if ((e = make_tensor_map_3d(&mv, V, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, kp.T, kp.BH, 64, 128,
-                                CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
-        return e;
+    const int64_t B = kp.BH / kp.H;
+    if ((e = make_operand_map(&m1, P1, B, kp.H, kp.T, kp.d, kp.layout, 64, 128, false)) != cudaSuccess) return e;
+    if ((e = make_operand_map(&m2, P2, B, kp.H, kp.T, kp.d, kp.layout, 64, 128, false)) != cudaSuccess) return e;
+    if ((e = make_operand_map(&mv, V, B, kp.H, kp.T, kp.d, kp.layout, 64, 128, false)) != cudaSuccess) return e;
     const unsigned pairs = (unsigned)((kp.T + 2 * kBM - 1) / (2 * kBM));
     dim3 grid((unsigned)kp.BH, pairs);
     relation_fwd_tc_kernel<D><<<grid, kThreads, C::kSmemBytes, s>>>(m1, m2, mv, kp, (__nv_bfloat16*)Y, L, tl.status);
@@ -532,8 +530,8 @@ cudaError_t launch_fwd_tc_d(const KernelProblem& kp, const void* P1, const void*
 cudaError_t launch_fwd_tc(const KernelProblem& kp, const void* P1, const void* P2, const void* V, void* Y, float* L,
                           const TcLaunch& tl, cudaStream_t s) {
     if (kp.BH > 2147483647LL) return cudaErrorInvalidValue;
-    if (kp.d == 64) return launch_fwd_tc_d<64>(kp, P1, P2, V, Y, L, tl, s);
-    if (kp.d == 128) return launch_fwd_tc_d<128>(kp, P1, P2, V, Y, L, tl, s);
+    if (kp.d == 48 || kp.d == 64) return launch_fwd_tc_d<64>(kp, P1, P2, V, Y, L, tl, s);
+    if (kp.d == 80 || kp.d == 128) return launch_fwd_tc_d<128>(kp, P1, P2, V, Y, L, tl, s);
     return cudaErrorInvalidValue;
 }
 

@@ -16,10 +16,13 @@ cudaError_t launch_bwd_simt(const KernelProblem& kp, bool bf16, const void* P1, 
                             cudaStream_t s);
 
 // Shared backward stages.
+// dq_acc (optional) is the fp32 dP1 accumulator [BH, T, dq_w]; it is zeroed.
 cudaError_t launch_bwd_prepare(const KernelProblem& kp, bool bf16, const void* P1, const void* P2, const void* V,
-                               const void* Y, const float* L, const void* dY, float* Dw, float* dq_acc,
+                               const void* Y, const float* L, const void* dY, float* Dw, float* dq_acc, int dq_w,
                                float* dlambda, cudaStream_t s);
-cudaError_t launch_convert(const float* src, void* dst, bool bf16, int64_t n, int num_sms, cudaStream_t s);
+// dP1 accumulator [BH, T, dq_w] -> dP1 in the problem's layout and width.
+cudaError_t launch_convert(const KernelProblem& kp, const float* src, int dq_w, void* dst, bool bf16, int num_sms,
+                           cudaStream_t s);
 
 // Tensor-core (tcgen05) bf16 path.
 struct TcLaunch {
@@ -29,7 +32,7 @@ struct TcLaunch {
 cudaError_t launch_fwd_tc(const KernelProblem& kp, const void* P1, const void* P2, const void* V, void* Y, float* L,
                           const TcLaunch& tl, cudaStream_t s);
 // Whether the tensor-core backward kernel for this head width also sums dlambda.
-inline bool bwd_tc_sums_dlambda(int d) { return d == 64; }
+inline bool bwd_tc_sums_dlambda(int d) { return d == 48 || d == 64; }  // the d = 64 kernel serves both
 cudaError_t launch_bwd_tc(const KernelProblem& kp, const void* P1, const void* P2, const void* V, const float* L,
                           const float* Dw, const void* dY, float* dq_acc, void* dP2, void* dV, float* dlambda,
                           const TcLaunch& tl, cudaStream_t s);

@@ -96,6 +96,27 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
         : "memory");
 }
 
+// 4-D tiled load (x, y, z, w), completion signalled on `bar` (tx bytes).
+__device__ __forceinline__ void tma_load_4d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
+                                            int z, int w) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w)
+        : "memory");
+}
+
+// Tile of an operand tensor through a map made by make_operand_map (rank3:
+// the 3-D form): rows row..row+box_y-1 of head bh = batch*H + head, columns
+// x..x+box_x-1.
+__device__ __forceinline__ void tma_load_operand(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x,
+                                                 int row, int bh, int head, int batch, bool rank3) {
+    if (rank3)
+        tma_load_3d(smem_dst, map, bar, x, row, bh);
+    else
+        tma_load_4d(smem_dst, map, bar, x, row, head, batch);
+}
+
 // ------------------------------------------------------------------- tcgen05
 // TMEM allocation; executed by one full warp.  Writes the base address to smem.
 __device__ __forceinline__ void tmem_alloc(uint32_t* smem_dst, uint32_t ncols) {

@@ -74,7 +74,8 @@ relation_status_t check_problem(const relation_problem_t* p) {
     if (elems > 1.0e12) return RELATION_ERR_INVALID_ARGUMENT;
     if (p->dtype != RELATION_F32 && p->dtype != RELATION_BF16) return RELATION_ERR_INVALID_ARGUMENT;
     if (!(p->tau_S > 0.f) || !isfinite(p->tau_S) || !isfinite(p->lambda)) return RELATION_ERR_INVALID_ARGUMENT;
-    if (p->d_h != 64 && p->d_h != 128) return RELATION_ERR_UNSUPPORTED;
+    if (p->layout != RELATION_LAYOUT_BHTD && p->layout != RELATION_LAYOUT_BTHD) return RELATION_ERR_INVALID_ARGUMENT;
+    if (p->d_h != 48 && p->d_h != 60 && p->d_h != 64 && p->d_h != 80 && p->d_h != 128) return RELATION_ERR_UNSUPPORTED;
     return RELATION_OK;
 }
 
@@ -87,18 +88,27 @@ KernelProblem kernel_problem(const relation_problem_t* p) {
     kp.lambda = p->lambda;
     kp.causal = p->causal ? 1 : 0;
     kp.inv_sqrt_d = (float)(1.0 / sqrt((double)p->d_h));
+    kp.H = (int)p->H;
+    kp.layout = (int)p->layout;
     return kp;
 }
 
+// The tensor-core kernels read operands with TMA, which needs 16-byte strides
+// (d_h * 2 % 16 == 0): every supported bf16 width except 60, which runs on the
+// CUDA-core kernels.
+bool use_tensor_cores(const relation_problem_t* p) { return p->dtype == RELATION_BF16 && p->d_h != 60; }
+
+// Width of the fp32 dP1 accumulator rows: the tensor-core tile width that the
+// head width is padded to.
+int dq_width(const relation_problem_t* p) { return p->d_h <= 64 ? 64 : 128; }
+
 size_t workspace_layout(const relation_problem_t* p, size_t* dq_offset) {
     const size_t d_bytes = round_up(rows_of(p) * sizeof(float), 256);
-    const size_t dq_bytes = p->dtype == RELATION_BF16 ? rows_of(p) * (size_t)p->d_h * sizeof(float) : 0;
+    const size_t dq_bytes = use_tensor_cores(p) ? rows_of(p) * (size_t)dq_width(p) * sizeof(float) : 0;
     if (dq_offset) *dq_offset = d_bytes;
     return d_bytes + dq_bytes;
 }
 
-// The tensor-core path serves every bf16 problem.
-bool use_tensor_cores(const relation_problem_t* p) { return p->dtype == RELATION_BF16; }
 
 struct BwdArgs {
     const relation_problem_t* p;
@@ -158,7 +168,7 @@ relation_status_t run_prepare(const BwdArgs& a, int* launches) {
     // dlambda is summed by the main pass where that kernel does it, else here.
     float* dlam_here = (use_tensor_cores(a.p) && bwd_tc_sums_dlambda(kp.d)) ? nullptr : a.dlambda;
     relation_status_t st = from_cuda(launch_bwd_prepare(kp, a.p->dtype == RELATION_BF16, a.P1, a.P2, a.V, a.Y, a.L,
-                                                        a.dY, Dw, dq, dlam_here, a.stream));
+                                                        a.dY, Dw, dq, dq_width(a.p), dlam_here, a.stream));
     if (st == RELATION_OK) *launches += 1;
     return st;
 }
@@ -179,22 +189,21 @@ relation_status_t run_main(const BwdArgs& a, int* launches) {
         if (st == RELATION_OK) *launches += 1;
         return st;
     }
-    relation_status_t st = from_cuda(launch_bwd_simt(kp, false, a.P1, a.P2, a.V, a.L, Dw, a.dY, a.dP1, a.dP2, a.dV,
-                                                     a.stream));
+    relation_status_t st = from_cuda(launch_bwd_simt(kp, a.p->dtype == RELATION_BF16, a.P1, a.P2, a.V, a.L, Dw,
+                                                     a.dY, a.dP1, a.dP2, a.dV, a.stream));
     if (st == RELATION_OK) *launches += 2;
     return st;
 }
 
 relation_status_t run_finish(const BwdArgs& a, int* launches) {
-    if (!use_tensor_cores(a.p)) return RELATION_OK;  // the fp32 path writes dP1 directly
+    if (!use_tensor_cores(a.p)) return RELATION_OK;  // the CUDA-core path writes dP1 directly
     size_t dq_off = 0;
     workspace_layout(a.p, &dq_off);
     DeviceInfo di;
     relation_status_t st = device_info(&di);
     if (st != RELATION_OK) return st;
     const float* dq = reinterpret_cast<const float*>(static_cast<const char*>(a.workspace) + dq_off);
-    st = from_cuda(launch_convert(dq, a.dP1, true, (int64_t)(rows_of(a.p) * (size_t)a.p->d_h), di.num_sms,
-                                  a.stream));
+    st = from_cuda(launch_convert(kernel_problem(a.p), dq, dq_width(a.p), a.dP1, true, di.num_sms, a.stream));
     if (st == RELATION_OK) *launches += 1;
     return st;
 }
@@ -229,7 +238,7 @@ relation_status_t relation_fwd(const relation_problem_t* p, const void* P1, cons
         TcLaunch tl{di.num_sms, di.status};
         st = from_cuda(launch_fwd_tc(kp, P1, P2, V, Y, L, tl, s));
     } else {
-        st = from_cuda(launch_fwd_simt(kp, false, P1, P2, V, Y, L, s));
+        st = from_cuda(launch_fwd_simt(kp, p->dtype == RELATION_BF16, P1, P2, V, Y, L, s));
     }
     if (st == RELATION_OK) t_last_launches = 1;
     return st;
@@ -310,7 +319,7 @@ const char* relation_status_string(relation_status_t s) {
     switch (s) {
         case RELATION_OK: return "ok";
         case RELATION_ERR_INVALID_ARGUMENT: return "invalid argument";
-        case RELATION_ERR_UNSUPPORTED: return "unsupported problem (d_h must be 64 or 128)";
+        case RELATION_ERR_UNSUPPORTED: return "unsupported problem (d_h must be 48, 60, 64, 80 or 128)";
         case RELATION_ERR_MISALIGNED: return "tensor pointer not 16-byte aligned";
         case RELATION_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than relation_bwd_workspace_bytes()";
         case RELATION_ERR_CUDA: return "CUDA runtime error";

@@ -41,12 +41,14 @@ __device__ __forceinline__ float count_correction(const KernelProblem& kp, int i
     return kp.lambda * logf((float)c);
 }
 
+// Rows row0 .. row0+kTile-1 of head bh of an operand tensor (any layout) as fp32.
 template <typename Tin, int D>
-__device__ __forceinline__ void load_tile(float (*dst)[D], const Tin* src_head, int row0, int T) {
+__device__ __forceinline__ void load_tile(float (*dst)[D], const Tin* src, const KernelProblem& kp, int64_t bh,
+                                          int row0) {
     for (int e = threadIdx.x; e < kTile * D; e += kThreads) {
         const int rr = e / D, cc = e % D;
         const int row = row0 + rr;
-        dst[rr][cc] = (row < T) ? load_as_float(src_head + (int64_t)row * D + cc) : 0.f;
+        dst[rr][cc] = (row < kp.T) ? load_as_float(src + row_offset(kp, bh, row) + cc) : 0.f;
     }
 }
 
@@ -65,12 +67,12 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(KernelProblem kp, co
     const int r = threadIdx.x >> 2, part = threadIdx.x & 3;
     const int i = q0 + r;
     const bool valid = i < T;
-    const size_t head = (size_t)bh * T * D;
+    const size_t off_i = row_offset(kp, bh, valid ? i : 0);
 
     float q[S], acc[S];
 #pragma unroll
     for (int k = 0; k < S; ++k) {
-        q[k] = valid ? load_as_float(P1 + head + (size_t)i * D + part + 4 * k) : 0.f;
+        q[k] = valid ? load_as_float(P1 + off_i + part + 4 * k) : 0.f;
         acc[k] = 0.f;
     }
     float m = -INFINITY, l = 0.f;
@@ -79,8 +81,8 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(KernelProblem kp, co
 
     for (int j0 = 0; j0 < kv_end; j0 += kTile) {
         __syncthreads();
-        load_tile<Tin, D>(sK, P2 + head, j0, T);
-        load_tile<Tin, D>(sV, V + head, j0, T);
+        load_tile<Tin, D>(sK, P2, kp, bh, j0);
+        load_tile<Tin, D>(sV, V, kp, bh, j0);
         __syncthreads();
         for (int jj = 0; jj < kTile; ++jj) {
             const int j = j0 + jj;
@@ -106,7 +108,7 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(KernelProblem kp, co
     if (valid) {
         const float inv_l = 1.f / l;
 #pragma unroll
-        for (int k = 0; k < S; ++k) store_from_float(Y + head + (size_t)i * D + part + 4 * k, acc[k] * inv_l);
+        for (int k = 0; k < S; ++k) store_from_float(Y + off_i + part + 4 * k, acc[k] * inv_l);
         if (L != nullptr && part == 0) L[bh * T + i] = m + logf(l);
     }
 }
@@ -123,7 +125,7 @@ __global__ void __launch_bounds__(256) bwd_prepare_kernel(KernelProblem kp, cons
                                                           const float* __restrict__ L,
                                                           const Tin* __restrict__ dY,
                                                           float* __restrict__ Dout, float* __restrict__ dq_acc,
-                                                          float* __restrict__ dlambda) {
+                                                          int dq_w, float* __restrict__ dlambda) {
     __shared__ float s_part[8];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * 8 + warp;  // flattened (bh, i)
@@ -132,15 +134,16 @@ __global__ void __launch_bounds__(256) bwd_prepare_kernel(KernelProblem kp, cons
     float contrib = 0.f;
     if (row < rows) {
         const int i = (int)(row % kp.T);
-        const size_t off = (size_t)row * d;
+        const size_t off = row_offset(kp, row / kp.T, i);
         float dy_y = 0.f, p1p2 = 0.f, dy_v = 0.f;
         for (int c = lane; c < d; c += 32) {
             const float g = load_as_float(dY + off + c);
             dy_y = fmaf(g, load_as_float(Yf + off + c), dy_y);
             dy_v = fmaf(g, load_as_float(V + off + c), dy_v);
             p1p2 = fmaf(load_as_float(P1 + off + c), load_as_float(P2 + off + c), p1p2);
-            if (dq_acc != nullptr) dq_acc[off + c] = 0.f;
         }
+        if (dq_acc != nullptr)
+            for (int c = lane; c < dq_w; c += 32) dq_acc[(size_t)row * dq_w + c] = 0.f;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             dy_y += __shfl_xor_sync(0xffffffffu, dy_y, o);
@@ -232,19 +235,19 @@ __global__ void __launch_bounds__(kThreads) bwd_kv_simt_kernel(KernelProblem kp,
     const int r = threadIdx.x >> 2, part = threadIdx.x & 3;
     const int j = j0 + r;
     const bool valid = j < T;
-    const size_t head = (size_t)bh * T * D;
+    const size_t off_j = row_offset(kp, bh, valid ? j : 0);
     float kreg[S], vreg[S], adv[S], adk[S];
 #pragma unroll
     for (int k = 0; k < S; ++k) {
-        kreg[k] = valid ? load_as_float(P2 + head + (size_t)j * D + part + 4 * k) : 0.f;
-        vreg[k] = valid ? load_as_float(V + head + (size_t)j * D + part + 4 * k) : 0.f;
+        kreg[k] = valid ? load_as_float(P2 + off_j + part + 4 * k) : 0.f;
+        vreg[k] = valid ? load_as_float(V + off_j + part + 4 * k) : 0.f;
         adv[k] = adk[k] = 0.f;
     }
     const int i_begin = kp.causal ? j0 : 0;
     for (int i0 = i_begin; i0 < T; i0 += kTile) {
         __syncthreads();
-        load_tile<Tin, D>(sQ, P1 + head, i0, T);
-        load_tile<Tin, D>(sG, dY + head, i0, T);
+        load_tile<Tin, D>(sQ, P1, kp, bh, i0);
+        load_tile<Tin, D>(sG, dY, kp, bh, i0);
         if (threadIdx.x < kTile) {
             const int i = i0 + threadIdx.x;
             sL[threadIdx.x] = i < T ? L[bh * T + i] : 0.f;
@@ -280,8 +283,8 @@ __global__ void __launch_bounds__(kThreads) bwd_kv_simt_kernel(KernelProblem kp,
     if (valid) {
 #pragma unroll
         for (int k = 0; k < S; ++k) {
-            store_from_float(dP2 + head + (size_t)j * D + part + 4 * k, adk[k]);
-            store_from_float(dV + head + (size_t)j * D + part + 4 * k, adv[k]);
+            store_from_float(dP2 + off_j + part + 4 * k, adk[k]);
+            store_from_float(dV + off_j + part + 4 * k, adv[k]);
         }
     }
 }
@@ -303,12 +306,12 @@ __global__ void __launch_bounds__(kThreads) bwd_q_simt_kernel(KernelProblem kp, 
     const int r = threadIdx.x >> 2, part = threadIdx.x & 3;
     const int i = q0 + r;
     const bool valid = i < T;
-    const size_t head = (size_t)bh * T * D;
+    const size_t off_i = row_offset(kp, bh, valid ? i : 0);
     float qreg[S], greg[S], acc[S];
 #pragma unroll
     for (int k = 0; k < S; ++k) {
-        qreg[k] = valid ? load_as_float(P1 + head + (size_t)i * D + part + 4 * k) : 0.f;
-        greg[k] = valid ? load_as_float(dY + head + (size_t)i * D + part + 4 * k) : 0.f;
+        qreg[k] = valid ? load_as_float(P1 + off_i + part + 4 * k) : 0.f;
+        greg[k] = valid ? load_as_float(dY + off_i + part + 4 * k) : 0.f;
         acc[k] = 0.f;
     }
     const float Li = valid ? L[bh * T + i] : 0.f;
@@ -317,8 +320,8 @@ __global__ void __launch_bounds__(kThreads) bwd_q_simt_kernel(KernelProblem kp, 
     const int kv_end = kp.causal ? min(T, q0 + kRows) : T;
     for (int j0 = 0; j0 < kv_end; j0 += kTile) {
         __syncthreads();
-        load_tile<Tin, D>(sK, P2 + head, j0, T);
-        load_tile<Tin, D>(sV, V + head, j0, T);
+        load_tile<Tin, D>(sK, P2, kp, bh, j0);
+        load_tile<Tin, D>(sV, V, kp, bh, j0);
         __syncthreads();
         for (int jj = 0; jj < kTile; ++jj) {
             const int j = j0 + jj;
@@ -344,7 +347,7 @@ __global__ void __launch_bounds__(kThreads) bwd_q_simt_kernel(KernelProblem kp, 
     }
     if (valid) {
 #pragma unroll
-        for (int k = 0; k < S; ++k) store_from_float(dP1 + head + (size_t)i * D + part + 4 * k, acc[k]);
+        for (int k = 0; k < S; ++k) store_from_float(dP1 + off_i + part + 4 * k, acc[k]);
     }
 }
 
@@ -362,16 +365,41 @@ __global__ void __launch_bounds__(256) convert_kernel(const float* __restrict__ 
     }
 }
 
+// dP1 accumulator [BH, T, dq_w] fp32 -> dP1 in the problem's layout and width;
+// one thread per 4 columns of a row.
+template <typename Tout>
+__global__ void __launch_bounds__(256) convert_rows_kernel(KernelProblem kp, const float* __restrict__ src, int dq_w,
+                                                           Tout* __restrict__ dst, int64_t n4) {
+    const int q4 = kp.d / 4;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < n4; k += stride) {
+        const int64_t row = k / q4;
+        const int c = (int)(k - row * q4) * 4;
+        const float4 v = *reinterpret_cast<const float4*>(src + (size_t)row * dq_w + c);
+        Tout* o = dst + row_offset(kp, row / kp.T, row % kp.T) + c;
+        store_from_float(o + 0, v.x);
+        store_from_float(o + 1, v.y);
+        store_from_float(o + 2, v.z);
+        store_from_float(o + 3, v.w);
+    }
+}
+
 template <typename Tin>
 cudaError_t launch_fwd_simt_t(const KernelProblem& kp, const void* P1, const void* P2, const void* V, void* Y,
                               float* L, cudaStream_t s) {
     dim3 grid((kp.T + kRows - 1) / kRows, (unsigned)kp.BH);
-    if (kp.d == 64)
-        fwd_simt_kernel<Tin, 64><<<grid, kThreads, 0, s>>>(kp, (const Tin*)P1, (const Tin*)P2, (const Tin*)V,
-                                                           (Tin*)Y, L);
-    else
-        fwd_simt_kernel<Tin, 128><<<grid, kThreads, 0, s>>>(kp, (const Tin*)P1, (const Tin*)P2, (const Tin*)V,
-                                                            (Tin*)Y, L);
+#define RELATION_FWD_SIMT(DD)                                                                               \
+    fwd_simt_kernel<Tin, DD><<<grid, kThreads, 0, s>>>(kp, (const Tin*)P1, (const Tin*)P2, (const Tin*)V, \
+                                                       (Tin*)Y, L)
+    switch (kp.d) {
+        case 48: RELATION_FWD_SIMT(48); break;
+        case 60: RELATION_FWD_SIMT(60); break;
+        case 64: RELATION_FWD_SIMT(64); break;
+        case 80: RELATION_FWD_SIMT(80); break;
+        case 128: RELATION_FWD_SIMT(128); break;
+        default: return cudaErrorInvalidValue;
+    }
+#undef RELATION_FWD_SIMT
     return cudaGetLastError();
 }
 
@@ -380,17 +408,20 @@ cudaError_t launch_bwd_simt_t(const KernelProblem& kp, const void* P1, const voi
                               const float* L, const float* Dw, const void* dY, void* dP1, void* dP2, void* dV,
                               cudaStream_t s) {
     dim3 grid((kp.T + kRows - 1) / kRows, (unsigned)kp.BH);
-    if (kp.d == 64) {
-        bwd_kv_simt_kernel<Tin, 64><<<grid, kThreads, 0, s>>>(kp, (const Tin*)P1, (const Tin*)P2, (const Tin*)V, L,
-                                                              Dw, (const Tin*)dY, (Tin*)dP2, (Tin*)dV);
-        bwd_q_simt_kernel<Tin, 64><<<grid, kThreads, 0, s>>>(kp, (const Tin*)P1, (const Tin*)P2, (const Tin*)V, L,
-                                                             Dw, (const Tin*)dY, (Tin*)dP1);
-    } else {
-        bwd_kv_simt_kernel<Tin, 128><<<grid, kThreads, 0, s>>>(kp, (const Tin*)P1, (const Tin*)P2, (const Tin*)V,
-                                                               L, Dw, (const Tin*)dY, (Tin*)dP2, (Tin*)dV);
-        bwd_q_simt_kernel<Tin, 128><<<grid, kThreads, 0, s>>>(kp, (const Tin*)P1, (const Tin*)P2, (const Tin*)V, L,
-                                                              Dw, (const Tin*)dY, (Tin*)dP1);
+#define RELATION_BWD_SIMT(DD)                                                                                     \
+    bwd_kv_simt_kernel<Tin, DD><<<grid, kThreads, 0, s>>>(kp, (const Tin*)P1, (const Tin*)P2, (const Tin*)V, L, Dw, \
+                                                          (const Tin*)dY, (Tin*)dP2, (Tin*)dV);                    \
+    bwd_q_simt_kernel<Tin, DD><<<grid, kThreads, 0, s>>>(kp, (const Tin*)P1, (const Tin*)P2, (const Tin*)V, L, Dw,  \
+                                                         (const Tin*)dY, (Tin*)dP1)
+    switch (kp.d) {
+        case 48: RELATION_BWD_SIMT(48); break;
+        case 60: RELATION_BWD_SIMT(60); break;
+        case 64: RELATION_BWD_SIMT(64); break;
+        case 80: RELATION_BWD_SIMT(80); break;
+        case 128: RELATION_BWD_SIMT(128); break;
+        default: return cudaErrorInvalidValue;
     }
+#undef RELATION_BWD_SIMT
     return cudaGetLastError();
 }
 
@@ -410,10 +441,12 @@ cudaError_t launch_bwd_simt(const KernelProblem& kp, bool bf16, const void* P1, 
 }
 
 cudaError_t launch_bwd_prepare(const KernelProblem& kp, bool bf16, const void* P1, const void* P2, const void* V,
-                               const void* Y, const float* L, const void* dY, float* Dw, float* dq_acc,
+                               const void* Y, const float* L, const void* dY, float* Dw, float* dq_acc, int dq_w,
                                float* dlambda, cudaStream_t s) {
     const int64_t rows = kp.BH * kp.T;
-    if (bf16 && dlambda == nullptr && dq_acc != nullptr) {
+    // Vector path: contiguous [B, H, T, d] rows whose width is the accumulator's.
+    if (bf16 && dlambda == nullptr && dq_acc != nullptr && kp.layout == 0 && kp.d == dq_w &&
+        (kp.d == 64 || kp.d == 128)) {
         const int64_t threads = rows * (kp.d / 8);
         const unsigned blocks = (unsigned)((threads + 255) / 256);
         if (kp.d == 64)
@@ -428,23 +461,31 @@ cudaError_t launch_bwd_prepare(const KernelProblem& kp, bool bf16, const void* P
     if (bf16)
         bwd_prepare_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
             kp, (const __nv_bfloat16*)P1, (const __nv_bfloat16*)P2, (const __nv_bfloat16*)V,
-            (const __nv_bfloat16*)Y, L, (const __nv_bfloat16*)dY, Dw, dq_acc, dlambda);
+            (const __nv_bfloat16*)Y, L, (const __nv_bfloat16*)dY, Dw, dq_acc, dq_w, dlambda);
     else
         bwd_prepare_kernel<float><<<blocks, 256, 0, s>>>(kp, (const float*)P1, (const float*)P2, (const float*)V,
-                                                         (const float*)Y, L, (const float*)dY, Dw, dq_acc, dlambda);
+                                                         (const float*)Y, L, (const float*)dY, Dw, dq_acc, dq_w,
+                                                         dlambda);
     return cudaGetLastError();
 }
 
-cudaError_t launch_convert(const float* src, void* dst, bool bf16, int64_t n, int num_sms, cudaStream_t s) {
-    const int64_t n4 = n / 4;  // n is a multiple of d (64 or 128)
+cudaError_t launch_convert(const KernelProblem& kp, const float* src, int dq_w, void* dst, bool bf16, int num_sms,
+                           cudaStream_t s) {
+    const int64_t n4 = kp.BH * (int64_t)kp.T * (kp.d / 4);  // d is a multiple of 4
     int64_t blocks = (n4 + 255) / 256;
     const int64_t cap = (int64_t)num_sms * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    if (bf16)
-        convert_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(src, (__nv_bfloat16*)dst, n4);
-    else
-        convert_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(src, (float*)dst, n4);
+    if (kp.layout == 0 && kp.d == dq_w) {  // same layout on both sides: a flat conversion
+        if (bf16)
+            convert_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(src, (__nv_bfloat16*)dst, n4);
+        else
+            convert_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(src, (float*)dst, n4);
+    } else if (bf16) {
+        convert_rows_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(kp, src, dq_w, (__nv_bfloat16*)dst, n4);
+    } else {
+        convert_rows_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(kp, src, dq_w, (float*)dst, n4);
+    }
     return cudaGetLastError();
 }
 

@@ -29,17 +29,18 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert rb.relation_abi_version() == 1
+    assert rb.relation_abi_version() == 2
     for code in range(7):
         assert rb.relation_status_string(code)
     assert rb.relation_status_string(99) == "unknown status"
 
 
 def _prob(**kw):
-    base = dict(B=2, H=3, T=100, d_h=64, dtype=rb.RELATION_BF16, tau_S=1.0, lam=0.5, causal=1)
+    base = dict(B=2, H=3, T=100, d_h=64, dtype=rb.RELATION_BF16, tau_S=1.0, lam=0.5, causal=1,
+                layout=rb.RELATION_LAYOUT_BHTD)
     base.update(kw)
     return rb.Problem(base["B"], base["H"], base["T"], base["d_h"], base["dtype"], base["tau_S"], base["lam"],
-                      base["causal"])
+                      base["causal"], base["layout"])
 
 
 def _fwd(lib, prob, P1=A, P2=2 * A, V=3 * A, Y=4 * A, L=5 * A):
@@ -47,15 +48,34 @@ def _fwd(lib, prob, P1=A, P2=2 * A, V=3 * A, Y=4 * A, L=5 * A):
 
 
 @pytest.mark.parametrize("kw", [dict(B=0), dict(H=-1), dict(T=0), dict(tau_S=0.0), dict(tau_S=-1.0),
-                                dict(tau_S=float("inf")), dict(lam=float("nan")), dict(dtype=7)])
+                                dict(tau_S=float("inf")), dict(lam=float("nan")), dict(dtype=7), dict(layout=2),
+                                dict(layout=-1)])
 def test_invalid_problem_rejected(lib, kw):
     assert _fwd(lib, _prob(**kw)) == 1
 
 
-@pytest.mark.parametrize("d", [32, 48, 80, 256])
+@pytest.mark.parametrize("d", [16, 32, 50, 96, 256])
 def test_unsupported_head_width(lib, d):
     assert _fwd(lib, _prob(d_h=d)) == 2
     assert rb.relation_bwd_workspace_bytes(_prob(d_h=d)) == 0
+
+
+@pytest.mark.parametrize("layout", [rb.RELATION_LAYOUT_BHTD, rb.RELATION_LAYOUT_BTHD])
+@pytest.mark.parametrize("d,acc", [(48, 64), (60, 0), (64, 64), (80, 128), (128, 128)])
+def test_workspace_for_every_width(lib, d, acc, layout):
+    """bf16 workspace: D_i, then the fp32 dP1 accumulator padded to the tensor-core tile width
+    (none for d_h = 60, which runs on the CUDA-core kernels and writes dP1 directly)."""
+    rows = 2 * 3 * 100
+    need = rb.relation_bwd_workspace_bytes(_prob(d_h=d, layout=layout))
+    assert need >= rows * 4 + rows * acc * 4
+    assert need < rows * 4 + 256 + rows * acc * 4 + 1
+
+
+def test_problem_struct_matches_header():
+    """The ctypes mirror has the header's field order and size (ABI 2 added `layout`)."""
+    names = [f[0] for f in rb.Problem._fields_]
+    assert names == ["B", "H", "T", "d_h", "dtype", "tau_S", "lam", "causal", "layout"]
+    assert ctypes.sizeof(rb.Problem) == 4 * 8 + 5 * 4 + 4  # 52 bytes of fields, padded to 8
 
 
 def test_null_and_misaligned_pointers(lib):
