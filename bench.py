@@ -335,14 +335,20 @@ def main():
 
     peak_burst, peak_sust, peak_src = load_peaks()
     mean_fwd, mean_main = statistics.mean(t_fwd), statistics.mean(t_main)
-    if mean_main >= mean_fwd:
-        if w.d == 64:
-            dom, srcs = "relation_bwd_tc64_kernel<true>", ["bwd_tc64.cu", "ptx_sm100.cuh", "common.cuh"]
-        else:
-            dom, srcs = f"relation_bwd_tc_kernel<{w.d}>", ["bwd_tc.cu", "ptx_sm100.cuh"]
-        dom_ms, dom_flops = mean_main, f_bwd
+    # Kernels by head width: 48, 60 and 64 run the 64-wide tensor-core kernels, 80 and
+    # 128 the 128-wide ones (zero-padded tiles); 60 loads its tiles with cp.async.
+    tile, cp = (64 if w.d <= 64 else 128), w.d == 60
+    srcs_common = ["ptx_sm100.cuh", "common.cuh"] + (["tile_copy.cuh"] if cp else [])
+    fwd_k = f"relation_fwd_tc_kernel<{tile}, {'true' if cp else 'false'}>"
+    fwd_src = ["fwd_tc.cu"] + srcs_common
+    if tile == 64:
+        bwd_k, bwd_src = f"relation_bwd_tc64_kernel<{2 if cp else 0}>", ["bwd_tc64.cu"] + srcs_common
     else:
-        dom, dom_ms, dom_flops, srcs = f"relation_fwd_tc_kernel<{w.d}>", mean_fwd, f_fwd, ["fwd_tc.cu", "ptx_sm100.cuh"]
+        bwd_k, bwd_src = "relation_bwd_tc_kernel<128>", ["bwd_tc.cu"] + srcs_common
+    if mean_main >= mean_fwd:
+        dom, srcs, dom_ms, dom_flops = bwd_k, bwd_src, mean_main, f_bwd
+    else:
+        dom, srcs, dom_ms, dom_flops = fwd_k, fwd_src, mean_fwd, f_fwd
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
     line = {
         "metric": "Relation fwd+bwd TFLOP/s (bf16, causal) and % of GB300 dense bf16 peak",

@@ -34,10 +34,10 @@
  *    relation_check_device_status() reports it after the caller synchronises.
  *  - Supported: d_h in {48, 60, 64, 80, 128} (the paper's model widths,
  *    Table 2 and Appendix F.1, plus 128); dtype RELATION_BF16 (tensor-core
- *    path with fp32 accumulation; d_h = 60, whose 120-byte rows the tensor
- *    memory accelerator cannot address, runs on the CUDA-core kernels) or
- *    RELATION_F32 (fp32 CUDA-core path); any T >= 1; causal or not; either
- *    layout.  Other widths return RELATION_ERR_UNSUPPORTED.
+ *    path with fp32 accumulation; widths below 64 / 128 run as zero-padded
+ *    64- / 128-wide tiles) or RELATION_F32 (fp32 CUDA-core path); any T >= 1;
+ *    causal or not; either layout.  Other widths return
+ *    RELATION_ERR_UNSUPPORTED.
  *  - No entry point throws, aborts, or falls back to the CPU.
  */
 #ifndef RELATION_GB300_RELATION_H_

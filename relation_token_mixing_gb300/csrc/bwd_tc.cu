@@ -432,8 +432,9 @@ cudaError_t launch_bwd_tc_d(const KernelProblem& kp, const void* P1, const void*
 
 cudaError_t launch_bwd_tc(const KernelProblem& kp, const void* P1, const void* P2, const void* V, const float* L,
                           const float* Dw, const void* dY, float* dq_acc, void* dP2, void* dV, float* dlambda,
-                          const TcLaunch& tl, cudaStream_t s) {
-    if (kp.d == 48 || kp.d == 64) return launch_bwd_tc64(kp, P1, P2, V, L, Dw, dY, dq_acc, dP2, dV, dlambda, tl, s);
+                          const TcLaunch& tl, cudaStream_t s, bool padded64) {
+    if (kp.d == 48 || kp.d == 60 || kp.d == 64)
+        return launch_bwd_tc64(kp, P1, P2, V, L, Dw, dY, dq_acc, dP2, dV, dlambda, tl, s, padded64);
     if (kp.d == 80 || kp.d == 128) return launch_bwd_tc_d<128>(kp, P1, P2, V, L, Dw, dY, dq_acc, dP2, dV, tl, s);
     return cudaErrorInvalidValue;
 }

@@ -27,6 +27,7 @@
 #include <cuda_bf16.h>
 
 #include "kernels.h"
+#include "tile_copy.cuh"
 #include "ptx_sm100.cuh"
 #include "tmap.h"
 
@@ -113,11 +114,16 @@ __device__ __forceinline__ float row_dot(const uint8_t* a_tile, const uint8_t* b
     return acc;
 }
 
-template <int D>
+// kCp: operand tiles copied by the producer warp with cp.async from the raw
+// pointers (head widths whose rows TMA cannot address; D = 64 only), else TMA.
+template <int D, bool kCp>
 __global__ void __launch_bounds__(kThreads, 1)
     relation_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_p1, const __grid_constant__ CUtensorMap tm_p2,
                            const __grid_constant__ CUtensorMap tm_v, const KernelProblem kp,
-                           __nv_bfloat16* __restrict__ Y, float* __restrict__ L, unsigned int* status) {
+                           const __nv_bfloat16* __restrict__ P1, const __nv_bfloat16* __restrict__ P2,
+                           const __nv_bfloat16* __restrict__ V, __nv_bfloat16* __restrict__ Y,
+                           float* __restrict__ L, unsigned int* status) {
+    static_assert(!kCp || D == 64, "cp.async tiles are 64 columns wide");
     using C = FwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -170,7 +176,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         ptx::regs_dec<kRegsControl>();
-        if (lane == 0) {
+        if constexpr (kCp) {
+            // The whole warp copies the two query tiles, then streams the K/V stages.
+            for (int t = 0; t < 2; ++t)
+                if (n_t[t] > 0) cp_async_tile64(sQ + t * C::kTileBytes, P1, kp, bh, q_base + t * kBM, lane);
+            cp_async_commit();
+            cp_async_publish<0>();
+            if (lane == 0)
+                for (int t = 0; t < 2; ++t)
+                    if (n_t[t] > 0) ptx::mbar_arrive(&bars->q_full[t]);
+            // Stage j is issued, then stage j - kAhead is published (kAhead < kStages, so
+            // the wait for a free stage never waits on a stage still unpublished).
+            constexpr int kAhead = 2;
+            static_assert(kAhead < C::kStages, "lookahead must leave a stage");
+            int j = 0;
+            for (; j < n_max; ++j) {
+                const int s = j % C::kStages;
+                if (j >= C::kStages && !ptx::mbar_wait_warp(&bars->kv_empty[s], ((j / C::kStages) - 1) & 1,
+                                                            abort_flag, status, kDevTimeoutEmpty))
+                    break;
+                cp_async_tile64(sK + s * C::kTileBytes, P2, kp, bh, j * kBN, lane);
+                cp_async_commit();
+                cp_async_tile64(sV + s * C::kTileBytes, V, kp, bh, j * kBN, lane);
+                cp_async_commit();
+                if (j >= kAhead) {
+                    cp_async_publish<2 * kAhead>();  // stage j - kAhead has landed
+                    if (lane == 0) {
+                        const int sp = (j - kAhead) % C::kStages;
+                        ptx::mbar_arrive(&bars->k_full[sp]);
+                        ptx::mbar_arrive(&bars->v_full[sp]);
+                    }
+                }
+            }
+            cp_async_publish<0>();  // every copy has landed before the warp moves on
+            if (j == n_max && lane == 0)
+                for (int jj = max(0, n_max - kAhead); jj < n_max; ++jj) {
+                    ptx::mbar_arrive(&bars->k_full[jj % C::kStages]);
+                    ptx::mbar_arrive(&bars->v_full[jj % C::kStages]);
+                }
+        } else if (lane == 0) {
             ptx::tma_prefetch_desc(&tm_p1);
             ptx::tma_prefetch_desc(&tm_p2);
             ptx::tma_prefetch_desc(&tm_v);
@@ -501,27 +545,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D>
+template <int D, bool kCp>
 cudaError_t launch_fwd_tc_d(const KernelProblem& kp, const void* P1, const void* P2, const void* V, void* Y,
                             float* L, const TcLaunch& tl, cudaStream_t s) {
     using C = FwdCfg<D>;
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(relation_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr_err = cudaFuncSetAttribute(relation_fwd_tc_kernel<D, kCp>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         C::kSmemBytes);
     });
     if (attr_err != cudaSuccess) return attr_err;
     // Heads narrower than D read as D-wide tiles whose extra columns are zero.
-    CUtensorMap m1, m2, mv;
-    cudaError_t e;
-    const int64_t B = kp.BH / kp.H;
-    if ((e = make_operand_map(&m1, P1, B, kp.H, kp.T, kp.d, kp.layout, 64, 128, false)) != cudaSuccess) return e;
-    if ((e = make_operand_map(&m2, P2, B, kp.H, kp.T, kp.d, kp.layout, 64, 128, false)) != cudaSuccess) return e;
-    if ((e = make_operand_map(&mv, V, B, kp.H, kp.T, kp.d, kp.layout, 64, 128, false)) != cudaSuccess) return e;
+    CUtensorMap m1{}, m2{}, mv{};  // unused by the cp.async producer
+    if (!kCp) {
+        cudaError_t e;
+        const int64_t B = kp.BH / kp.H;
+        if ((e = make_operand_map(&m1, P1, B, kp.H, kp.T, kp.d, kp.layout, 64, 128, false)) != cudaSuccess) return e;
+        if ((e = make_operand_map(&m2, P2, B, kp.H, kp.T, kp.d, kp.layout, 64, 128, false)) != cudaSuccess) return e;
+        if ((e = make_operand_map(&mv, V, B, kp.H, kp.T, kp.d, kp.layout, 64, 128, false)) != cudaSuccess) return e;
+    }
     const unsigned pairs = (unsigned)((kp.T + 2 * kBM - 1) / (2 * kBM));
     dim3 grid((unsigned)kp.BH, pairs);
-    relation_fwd_tc_kernel<D><<<grid, kThreads, C::kSmemBytes, s>>>(m1, m2, mv, kp, (__nv_bfloat16*)Y, L, tl.status);
+    relation_fwd_tc_kernel<D, kCp><<<grid, kThreads, C::kSmemBytes, s>>>(
+        m1, m2, mv, kp, (const __nv_bfloat16*)P1, (const __nv_bfloat16*)P2, (const __nv_bfloat16*)V, (__nv_bfloat16*)Y,
+        L, tl.status);
     return cudaGetLastError();
 }
 
@@ -530,8 +578,9 @@ cudaError_t launch_fwd_tc_d(const KernelProblem& kp, const void* P1, const void*
 cudaError_t launch_fwd_tc(const KernelProblem& kp, const void* P1, const void* P2, const void* V, void* Y, float* L,
                           const TcLaunch& tl, cudaStream_t s) {
     if (kp.BH > 2147483647LL) return cudaErrorInvalidValue;
-    if (kp.d == 48 || kp.d == 64) return launch_fwd_tc_d<64>(kp, P1, P2, V, Y, L, tl, s);
-    if (kp.d == 80 || kp.d == 128) return launch_fwd_tc_d<128>(kp, P1, P2, V, Y, L, tl, s);
+    if (kp.d == 48 || kp.d == 64) return launch_fwd_tc_d<64, false>(kp, P1, P2, V, Y, L, tl, s);
+    if (kp.d == 60) return launch_fwd_tc_d<64, true>(kp, P1, P2, V, Y, L, tl, s);  // 120-byte rows: no TMA
+    if (kp.d == 80 || kp.d == 128) return launch_fwd_tc_d<128, false>(kp, P1, P2, V, Y, L, tl, s);
     return cudaErrorInvalidValue;
 }
 

@@ -20,6 +20,10 @@ cudaError_t launch_bwd_simt(const KernelProblem& kp, bool bf16, const void* P1, 
 cudaError_t launch_bwd_prepare(const KernelProblem& kp, bool bf16, const void* P1, const void* P2, const void* V,
                                const void* Y, const float* L, const void* dY, float* Dw, float* dq_acc, int dq_w,
                                float* dlambda, cudaStream_t s);
+// n (<= 4) bf16 operand tensors of width kp.d <= 64 (any layout) -> zero-padded
+// contiguous [BH, T, 64] copies.
+cudaError_t launch_pad_operands(const KernelProblem& kp, const void* const* src, void* const* dst, int n,
+                                int num_sms, cudaStream_t s);
 // dP1 accumulator [BH, T, dq_w] -> dP1 in the problem's layout and width.
 cudaError_t launch_convert(const KernelProblem& kp, const float* src, int dq_w, void* dst, bool bf16, int num_sms,
                            cudaStream_t s);
@@ -32,12 +36,15 @@ struct TcLaunch {
 cudaError_t launch_fwd_tc(const KernelProblem& kp, const void* P1, const void* P2, const void* V, void* Y, float* L,
                           const TcLaunch& tl, cudaStream_t s);
 // Whether the tensor-core backward kernel for this head width also sums dlambda.
-inline bool bwd_tc_sums_dlambda(int d) { return d == 48 || d == 64; }  // the d = 64 kernel serves both
+inline bool bwd_tc_sums_dlambda(int d) { return d <= 64; }  // the 64-wide kernel serves d = 48, 60, 64
+// padded64: P1, P2, V, dY point to zero-padded contiguous [BH, T, 64] copies
+// (made by launch_pad_operands) instead of the caller's tensors; dP2 and dV are
+// still written in the problem's layout and width.
 cudaError_t launch_bwd_tc(const KernelProblem& kp, const void* P1, const void* P2, const void* V, const float* L,
                           const float* Dw, const void* dY, float* dq_acc, void* dP2, void* dV, float* dlambda,
-                          const TcLaunch& tl, cudaStream_t s);
+                          const TcLaunch& tl, cudaStream_t s, bool padded64 = false);
 cudaError_t launch_bwd_tc64(const KernelProblem& kp, const void* P1, const void* P2, const void* V, const float* L,
                             const float* Dw, const void* dY, float* dq_acc, void* dP2, void* dV, float* dlambda,
-                            const TcLaunch& tl, cudaStream_t s);
+                            const TcLaunch& tl, cudaStream_t s, bool padded64 = false);
 
 }  // namespace relation

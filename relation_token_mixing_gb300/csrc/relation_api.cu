@@ -93,20 +93,35 @@ KernelProblem kernel_problem(const relation_problem_t* p) {
     return kp;
 }
 
-// The tensor-core kernels read operands with TMA, which needs 16-byte strides
-// (d_h * 2 % 16 == 0): every supported bf16 width except 60, which runs on the
-// CUDA-core kernels.
-bool use_tensor_cores(const relation_problem_t* p) { return p->dtype == RELATION_BF16 && p->d_h != 60; }
+// Every bf16 problem runs on the tensor cores (d_h = 60, whose 120-byte rows TMA
+// cannot step through, loads its tiles with cp.async instead).
+bool use_tensor_cores(const relation_problem_t* p) { return p->dtype == RELATION_BF16; }
 
 // Width of the fp32 dP1 accumulator rows: the tensor-core tile width that the
 // head width is padded to.
 int dq_width(const relation_problem_t* p) { return p->d_h <= 64 ? 64 : 128; }
 
-size_t workspace_layout(const relation_problem_t* p, size_t* dq_offset) {
+// bf16 operands whose rows TMA cannot step through (d_h = 60) are copied once,
+// zero-padded to 64 columns, into the workspace by the preparation stage.
+bool pads_operands(const relation_problem_t* p) { return use_tensor_cores(p) && (p->d_h * 2) % 16 != 0; }
+
+// Workspace: D [rows] fp32 | dP1 accumulator [rows, dq_width] fp32 | (d_h = 60)
+// padded copies of P1, P2, V, dY [rows, 64] bf16; each part 256-byte aligned.
+size_t workspace_layout(const relation_problem_t* p, size_t* dq_offset, size_t* pad_offset = nullptr) {
     const size_t d_bytes = round_up(rows_of(p) * sizeof(float), 256);
-    const size_t dq_bytes = use_tensor_cores(p) ? rows_of(p) * (size_t)dq_width(p) * sizeof(float) : 0;
+    const size_t dq_bytes = use_tensor_cores(p) ? round_up(rows_of(p) * (size_t)dq_width(p) * sizeof(float), 256) : 0;
+    const size_t pad_bytes = pads_operands(p) ? 4 * round_up(rows_of(p) * 64 * 2, 256) : 0;
     if (dq_offset) *dq_offset = d_bytes;
-    return d_bytes + dq_bytes;
+    if (pad_offset) *pad_offset = d_bytes + dq_bytes;
+    return d_bytes + dq_bytes + pad_bytes;
+}
+
+// The four padded operand copies inside the workspace (P1, P2, V, dY).
+void padded_operands(const relation_problem_t* p, void* workspace, void* out[4]) {
+    size_t pad_off = 0;
+    workspace_layout(p, nullptr, &pad_off);
+    const size_t each = round_up(rows_of(p) * 64 * 2, 256);
+    for (int k = 0; k < 4; ++k) out[k] = static_cast<char*>(workspace) + pad_off + k * each;
 }
 
 
@@ -170,6 +185,15 @@ relation_status_t run_prepare(const BwdArgs& a, int* launches) {
     relation_status_t st = from_cuda(launch_bwd_prepare(kp, a.p->dtype == RELATION_BF16, a.P1, a.P2, a.V, a.Y, a.L,
                                                         a.dY, Dw, dq, dq_width(a.p), dlam_here, a.stream));
     if (st == RELATION_OK) *launches += 1;
+    if (st == RELATION_OK && pads_operands(a.p)) {
+        DeviceInfo di;
+        if ((st = device_info(&di)) != RELATION_OK) return st;
+        const void* src[4] = {a.P1, a.P2, a.V, a.dY};
+        void* dst[4];
+        padded_operands(a.p, a.workspace, dst);
+        st = from_cuda(launch_pad_operands(kp, src, dst, 4, di.num_sms, a.stream));
+        if (st == RELATION_OK) *launches += 1;
+    }
     return st;
 }
 
@@ -185,7 +209,15 @@ relation_status_t run_main(const BwdArgs& a, int* launches) {
         float* dq = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + dq_off);
         TcLaunch tl{di.num_sms, di.status};
         float* dlam_main = bwd_tc_sums_dlambda(kp.d) ? a.dlambda : nullptr;
-        st = from_cuda(launch_bwd_tc(kp, a.P1, a.P2, a.V, a.L, Dw, a.dY, dq, a.dP2, a.dV, dlam_main, tl, a.stream));
+        if (pads_operands(a.p)) {
+            void* pad[4];
+            padded_operands(a.p, a.workspace, pad);
+            st = from_cuda(launch_bwd_tc(kp, pad[0], pad[1], pad[2], a.L, Dw, pad[3], dq, a.dP2, a.dV, dlam_main, tl,
+                                         a.stream, true));
+        } else {
+            st = from_cuda(launch_bwd_tc(kp, a.P1, a.P2, a.V, a.L, Dw, a.dY, dq, a.dP2, a.dV, dlam_main, tl,
+                                         a.stream));
+        }
         if (st == RELATION_OK) *launches += 1;
         return st;
     }

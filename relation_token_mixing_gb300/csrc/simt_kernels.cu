@@ -384,6 +384,26 @@ __global__ void __launch_bounds__(256) convert_rows_kernel(KernelProblem kp, con
     }
 }
 
+// Operand rows of width d (any layout) -> zero-padded contiguous [BH, T, 64]
+// bf16 copies (operand blockIdx.y of the four), one thread per 8-byte unit.
+struct PadArgs {
+    const uint2* src[4];
+    uint2* dst[4];
+};
+__global__ void __launch_bounds__(256) pad_operands_kernel(KernelProblem kp, PadArgs a, int64_t units) {
+    const uint2* __restrict__ src = a.src[blockIdx.y];
+    uint2* __restrict__ dst = a.dst[blockIdx.y];
+    const int src_units = kp.d / 4;  // d is a multiple of 4
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < units; k += stride) {
+        const int64_t row = k >> 4;
+        const int u = (int)(k & 15);
+        uint2 v = make_uint2(0u, 0u);
+        if (u < src_units) v = src[row_offset(kp, row / kp.T, row % kp.T) / 4 + u];
+        dst[k] = v;
+    }
+}
+
 template <typename Tin>
 cudaError_t launch_fwd_simt_t(const KernelProblem& kp, const void* P1, const void* P2, const void* V, void* Y,
                               float* L, cudaStream_t s) {
@@ -466,6 +486,23 @@ cudaError_t launch_bwd_prepare(const KernelProblem& kp, bool bf16, const void* P
         bwd_prepare_kernel<float><<<blocks, 256, 0, s>>>(kp, (const float*)P1, (const float*)P2, (const float*)V,
                                                          (const float*)Y, L, (const float*)dY, Dw, dq_acc, dq_w,
                                                          dlambda);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pad_operands(const KernelProblem& kp, const void* const* src, void* const* dst, int n,
+                                int num_sms, cudaStream_t s) {
+    if (n < 1 || n > 4 || kp.d > 64 || (kp.d & 3)) return cudaErrorInvalidValue;
+    PadArgs a{};
+    for (int k = 0; k < n; ++k) {
+        a.src[k] = static_cast<const uint2*>(src[k]);
+        a.dst[k] = static_cast<uint2*>(dst[k]);
+    }
+    const int64_t units = kp.BH * (int64_t)kp.T * 16;
+    int64_t blocks = (units + 255) / 256;
+    const int64_t cap = (int64_t)num_sms * 4;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    pad_operands_kernel<<<dim3((unsigned)blocks, (unsigned)n), 256, 0, s>>>(kp, a, units);
     return cudaGetLastError();
 }
 

@@ -71,6 +71,12 @@ WORKLOADS = {
     "mhr_fwd_bwd_T2048": Workload("mhr_fwd_bwd_T2048", 8, 12, 2048, 64, torch.bfloat16, 1.0, 0.5, backward=True),
     "mhr_fwd_bwd_T16384_d128": Workload("mhr_fwd_bwd_T16384_d128", 1, 32, 16384, 128, torch.bfloat16, 1.0, 0.5,
                                         backward=True),
+    # The paper's other model widths ("Ask Self, Ask Others", Table 2: 8 heads of 48 at
+    # T=1024, 8 of 80 at T=4096; Appendix F.1: the Hybrid model's 8 heads of 60 at
+    # T=2048), forward+backward with the paper's tau_S = 2 and lambda = 0.5.
+    "paper_d48_T1024": Workload("paper_d48_T1024", 16, 8, 1024, 48, torch.bfloat16, 2.0, 0.5, backward=True),
+    "paper_d60_T2048": Workload("paper_d60_T2048", 16, 8, 2048, 60, torch.bfloat16, 2.0, 0.5, backward=True),
+    "paper_d80_T4096": Workload("paper_d80_T4096", 4, 8, 4096, 80, torch.bfloat16, 2.0, 0.5, backward=True),
     # The headline shape: the large-|U| forward workload run forward+backward.
     "mhr_fwd_bwd_T4096": Workload("mhr_fwd_bwd_T4096", 4, 16, 4096, 64, torch.bfloat16, 0.5, 0.5,
                                   p_scale=3.0 / 64 ** 0.25, backward=True),
