@@ -37,6 +37,8 @@ def parse():
     ap.add_argument("--workload", default="mhr_fwd_bwd_T4096")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode", action="store_true",
+                    help="time one Relation Cache decode step (full caches of the workload's T) instead")
     return ap.parse_args()
 
 
@@ -153,6 +155,78 @@ def cpu_baseline(w, target_s: float = 12.0):
             "sample": f"fwd+bwd of B=1 H={heads} (of {w.B * w.H} heads) at T={w.T} d={w.d}, float64, {dt:.1f} s"}
 
 
+def run_decode(args, w):
+    """One Relation Cache step per timed iteration: every sequence has T-1 cached tokens
+    (full caches of capacity T) and decodes token T; caches are not appended, so every
+    step reads the same state.  HBM-bound: value = cache bytes read / time."""
+    import torch
+
+    from relation_token_mixing_gb300 import binding as rb
+    from relation_token_mixing_gb300 import inputs as rin
+
+    rb.load()
+    dev = torch.device("cuda", 0)
+    x = {k: v.to(dev) for k, v in rin.make(w).items()}
+    t = w.T - 1
+    P1n, P2n, Vn = (x[k][:, :, t].contiguous() for k in ("P1", "P2", "V"))
+    P2c, Vc = x["P2"], x["V"]
+    pos = torch.full((w.B,), t, dtype=torch.int32, device=dev)
+    prob = rb.Problem(w.B, w.H, w.T, w.d, rb.RELATION_BF16, w.tau_S, w.lam, 1, rb.RELATION_LAYOUT_BHTD)
+    ws = torch.empty((rb.relation_decode_workspace_bytes(prob) + 3) // 4, dtype=torch.float32, device=dev)
+    Y = torch.empty_like(P1n)
+    L = torch.empty(w.B, w.H, dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    e = 2  # bf16
+    bytes_step = w.B * w.H * (2 * t * w.d * e + 3 * w.d * e + w.d * e + 4)  # caches, new rows, Y, L
+    times = []
+    with ClockSampler(0) as clk:
+        for k in range(args.warmup + args.steps):
+            flush.zero_()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            ev[0].record()
+            rb.relation_decode(prob, P1n, P2n, Vn, P2c, Vc, pos, 0, Y, L, ws)
+            ev[1].record()
+            torch.cuda.synchronize()
+            if k >= args.warmup:
+                times.append(ev[0].elapsed_time(ev[1]))
+    assert rb.relation_check_device_status() == 0
+    ms = statistics.mean(times)
+    hbm = load_peaks_hbm()
+    line = {
+        "metric": "Relation Cache decode: cache bytes read per second (bf16)",
+        "value": bytes_step / (ms * 1e-3) / 1e9, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32 arithmetic on bf16", "data": "synthetic (seeded Gaussian caches, resident in HBM)",
+        "config": {"workload": f"decode_{w.name}", "B": w.B, "H": w.H, "cache_tokens": t, "d_h": w.d,
+                   "tau_S": w.tau_S, "lambda": w.lam, "l2": "flushed between timed steps"},
+        "tokens_per_s": w.B / (ms * 1e-3),
+        "roofline": {"kernel": "decode_partial_kernel + decode_combine_kernel", "bound": "hbm",
+                     "achieved": bytes_step / (ms * 1e-3) / 1e9, "peak": hbm[0], "unit": "GB/s",
+                     "frac": bytes_step / (ms * 1e-3) / 1e9 / hbm[0], "peak_source": hbm[1], "traffic": None},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        heads = list(range(min(8, w.B * w.H)))
+        t0 = time.perf_counter()
+        oracle.fwd_rows(x["P1"].cpu(), x["P2"].cpu(), x["V"].cpu(), w.tau_S, w.lam, True, heads, [t] * len(heads))
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": bytes_step * len(heads) / (w.B * w.H) / dt / 1e9, "unit": "GB/s",
+                                "cores": oracle.threads(), "kind": "oracle",
+                                "sample": f"row {t} of {len(heads)} heads, float64, {dt:.2f} s"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def load_peaks_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured copy"
+    return 6800.0, "fallback"
+
+
 def run_reference(args, w):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -197,6 +271,8 @@ def main():
     w = rin.WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.decode:
+        return run_decode(args, w)
 
     import torch
     import torch.distributed as dist

@@ -154,10 +154,45 @@ relation_status_t relation_bwd_noalloc(const relation_problem_t* p, const void* 
                                        void* dP1, void* dP2, void* dV, float* dlambda, void* stream);
 
 /*
+ * Relation Cache decoding (Sec. 5.3 eq.(18); Appendix A.5): one autoregressive
+ * step for B*H heads.  The cache of a head holds the P2 rows and information
+ * states I~ of the tokens already processed; only the new Relation row is
+ * formed:
+ *   U_j = p1_new . p2_j / sqrt(d_h) for j = 1..t (cached) and j = t+1 (p2_new),
+ *   R_{t+1} = sigmoid(U_{t+1} / tau_S) (Self),
+ *   R_j = SiLU(U_j) - lambda log(t+1) for j <= t (Exchange, c = t+1),
+ *   Y = sum_j Softmax(R)_j I~_j,
+ * i.e. exactly row t+1 of the causal relation_fwd over the t+1 tokens.
+ *
+ * p: B, H, d_h, dtype, tau_S, lambda, layout as for relation_fwd; p->T is the
+ *    cache capacity (rows per head); p->causal is ignored (decoding is causal).
+ * P1_new, P2_new, V_new: [B, H, d_h] (dtype), the new token's states.
+ * P2_cache, V_cache: [B, H, T, d_h] or [B, T, H, d_h] per p->layout (dtype);
+ *    rows 0 .. positions[b]-1 of batch b hold the history.
+ * positions: device int32 [B], t = number of cached tokens of batch b
+ *    (0 <= t < T; t = 0 is the first token, whose output is V_new exactly).
+ *    A position outside [0, T) is reported by relation_check_device_status()
+ *    as RELATION_ERR_INVALID_ARGUMENT and that batch's outputs are not written.
+ * append: nonzero also stores P2_new and V_new at row t of the caches (the
+ *    cache update of Appendix A.5.3), after which positions[b] + 1 is the next
+ *    step's position; the library does not change `positions`.
+ * Y: [B, H, d_h] (dtype).  L: optional [B, H] float32 log-normaliser of the row.
+ * workspace: at least relation_decode_workspace_bytes(p) bytes, float32
+ *    partial results.  Outputs must not overlap inputs or caches.
+ * Two kernel launches (per-chunk partials, then one merge per head).
+ */
+size_t relation_decode_workspace_bytes(const relation_problem_t* p);
+relation_status_t relation_decode(const relation_problem_t* p, const void* P1_new, const void* P2_new,
+                                  const void* V_new, void* P2_cache, void* V_cache, const int32_t* positions,
+                                  int append, void* Y, float* L, void* workspace, size_t workspace_bytes,
+                                  void* stream);
+
+/*
  * Reads and clears the device status word of the current device.  Call after
- * synchronising the streams used.  Returns RELATION_OK or
+ * synchronising the streams used.  Returns RELATION_OK,
  * RELATION_ERR_DEVICE_TIMEOUT (a bounded wait expired; outputs of the calls
- * since the last check are invalid) or RELATION_ERR_CUDA.
+ * since the last check are invalid), RELATION_ERR_INVALID_ARGUMENT (a decode
+ * position outside its cache) or RELATION_ERR_CUDA.
  */
 relation_status_t relation_check_device_status(void);
 

@@ -87,6 +87,11 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.relation_bwd_noalloc.restype = ctypes.c_int
         lib.relation_bwd_workspace_bytes.argtypes = [ctypes.POINTER(Problem)]
         lib.relation_bwd_workspace_bytes.restype = ctypes.c_size_t
+        lib.relation_decode_workspace_bytes.argtypes = [ctypes.POINTER(Problem)]
+        lib.relation_decode_workspace_bytes.restype = ctypes.c_size_t
+        lib.relation_decode.argtypes = [ctypes.POINTER(Problem), _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_int, _VP, _VP,
+                                        _VP, ctypes.c_size_t, _VP]
+        lib.relation_decode.restype = ctypes.c_int
         lib.relation_check_device_status.argtypes = []
         lib.relation_check_device_status.restype = ctypes.c_int
         lib.relation_last_launch_count.argtypes = []
@@ -191,6 +196,18 @@ def relation_bwd_noalloc(prob, P1, P2, V, Y, L, dY, dP1, dP2, dV, dlambda, strea
            "relation_bwd_noalloc")
 
 
+def relation_decode_workspace_bytes(prob: Problem) -> int:
+    return int(load().relation_decode_workspace_bytes(ctypes.byref(prob)))
+
+
+def relation_decode(prob, P1_new, P2_new, V_new, P2_cache, V_cache, positions, append, Y, L, workspace,
+                    stream=None) -> None:
+    _check(load().relation_decode(ctypes.byref(prob), _ptr(P1_new), _ptr(P2_new), _ptr(V_new), _ptr(P2_cache),
+                                  _ptr(V_cache), _ptr(positions), int(append), _ptr(Y), _ptr(L), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream_ptr(stream)),
+           "relation_decode")
+
+
 def relation_check_device_status() -> int:
     return int(load().relation_check_device_status())
 
@@ -215,6 +232,22 @@ def fwd(P1, P2, V, tau_S: float, lam: float, causal: bool = True, stream=None, w
     Y = torch.empty_like(V)
     L = torch.empty((prob.B, prob.H, prob.T), dtype=torch.float32, device=P1.device) if want_L else None
     relation_fwd(prob, P1, P2, V, Y, L, stream)
+    return Y, L
+
+
+def decode(P1_new, P2_new, V_new, P2_cache, V_cache, positions, tau_S: float, lam: float, append: bool = True,
+           layout: int = RELATION_LAYOUT_BHTD, stream=None, workspace=None):
+    """One Relation Cache step; allocates Y [B, H, d_h] and L [B, H]; returns (Y, L)."""
+    B, H, d = P1_new.shape
+    T = P2_cache.shape[2] if layout == RELATION_LAYOUT_BHTD else P2_cache.shape[1]
+    dt = RELATION_BF16 if P1_new.dtype == torch.bfloat16 else RELATION_F32
+    prob = Problem(B, H, T, d, dt, float(tau_S), float(lam), 1, int(layout))
+    Y = torch.empty_like(P1_new)
+    L = torch.empty((B, H), dtype=torch.float32, device=P1_new.device)
+    if workspace is None:
+        workspace = torch.empty((relation_decode_workspace_bytes(prob) + 3) // 4, dtype=torch.float32,
+                                device=P1_new.device)
+    relation_decode(prob, P1_new, P2_new, V_new, P2_cache, V_cache, positions, append, Y, L, workspace, stream)
     return Y, L
 
 

@@ -15,6 +15,7 @@ enum DeviceStatus : unsigned int {
     kDevTimeoutEmpty = 2,   // a producer gave up waiting for a free buffer
     kDevTimeoutMma = 3,     // a wait on tensor-core completion expired
     kDevBadLaunch = 4,      // a kernel saw a launch shape it was not built for
+    kDevBadPosition = 5,    // a decode position outside the cache (the head was skipped)
 };
 
 // Kernel-side view of one problem.  Operand tensors (P1, P2, V, Y, dY, dP1,

@@ -1,0 +1,277 @@
+// Relation Cache decoding ("Ask Self, Ask Others: Relation Is All You Need",
+// Sec. 5.3 eq.(18) and Appendix A.5): at autoregressive position t+1 (one
+// based) only the new Relation row is formed, from the new p1 against the
+// cached P2_{1:t} and the new p2 (the Self entry), and it transports the cached
+// information states I~_{1:t} and the new one:
+//   U_j = p1 . p2_j / sqrt(d),  R_{t+1} = sigmoid(U_{t+1} / tau_S),
+//   R_j = SiLU(U_j) - lambda log(t+1) (j <= t),  Y = sum_j softmax(R)_j I~_j.
+// The cache update appends p2_{t+1} and I~_{t+1} (Appendix A.5.3).
+//
+// The pass is HBM-bound (it reads 2 t d values per head), so it runs on CUDA
+// cores in fp32: split over key chunks (each CTA streams its chunk once with a
+// running softmax per group of lanes), then one CTA per head merges the chunks.
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace relation {
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ float sigmoid_exact(float x) {
+    if (x >= 0.f) return 1.f / (1.f + expf(-x));
+    const float e = expf(x);
+    return e / (1.f + e);
+}
+
+__device__ __forceinline__ float block_reduce(float v, float* red, bool is_max) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float w = __shfl_xor_sync(0xffffffffu, v, o);
+        v = is_max ? fmaxf(v, w) : v + w;
+    }
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    v = red[0];
+    for (int w = 1; w < kThreads / 32; ++w) v = is_max ? fmaxf(v, red[w]) : v + red[w];
+    return v;
+}
+
+// Vector of VEC consecutive elements as fp32 (16-byte or 8-byte loads).
+template <typename Tin, int VEC>
+__device__ __forceinline__ void load_vec(const Tin* p, float (&v)[VEC]) {
+    if constexpr (sizeof(Tin) == 2 && VEC == 8) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+            v[2 * k] = f.x;
+            v[2 * k + 1] = f.y;
+        }
+    } else if constexpr (sizeof(Tin) == 2 && VEC == 4) {
+        const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+        const uint32_t w[2] = {u.x, u.y};
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+            v[2 * k] = f.x;
+            v[2 * k + 1] = f.y;
+        }
+    } else {
+        static_assert(sizeof(Tin) == 4 && VEC == 4, "fp32 rows are read 16 bytes at a time");
+        const float4 u = __ldg(reinterpret_cast<const float4*>(p));
+        v[0] = u.x;
+        v[1] = u.y;
+        v[2] = u.z;
+        v[3] = u.w;
+    }
+}
+
+// Partial pass: CTA (bh, chunk) handles keys [chunk*C, min(chunk*C + C, t+1));
+// key t is the new token (read from the new-row tensors).  A group of G lanes
+// reads one key row, VEC elements per lane (lane li owns columns li*VEC ..),
+// so one warp instruction covers 32/G whole rows.  Writes (m, l, o[d]) of the
+// chunk to part[bh][chunk].
+template <typename Tin, int VEC, int G>
+__global__ void __launch_bounds__(kThreads) decode_partial_kernel(
+    KernelProblem kp, const Tin* __restrict__ P1n, const Tin* __restrict__ P2n, const Tin* __restrict__ Vn,
+    Tin* __restrict__ P2c, Tin* __restrict__ Vc, const int* __restrict__ pos, int append, int chunk,
+    float* __restrict__ part, unsigned int* status) {
+    constexpr int kGroups = kThreads / G;  // key rows in flight per CTA step
+    extern __shared__ float sm[];
+    float* sr = sm;           // chunk scores
+    float* red = sr + chunk;  // per-warp reductions (8)
+    float* oacc = red + 8;    // kGroups x d partial outputs
+    const int64_t bh = blockIdx.x;
+    const int b = (int)(bh / kp.H);
+    const int d = kp.d;
+    const int t = pos[b];
+    float* out = part + ((size_t)bh * gridDim.y + blockIdx.y) * (size_t)(d + 2);
+    if (t < 0 || t >= kp.T) {  // position outside the cache: reported, head skipped
+        if (threadIdx.x == 0) {
+            record_status(status, kDevBadPosition);
+            out[0] = -INFINITY;
+            out[1] = 0.f;
+        }
+        return;
+    }
+    const int n = t + 1;  // keys visible to the new row
+    const int j0 = blockIdx.y * chunk, j1 = min(n, j0 + chunk);
+    const size_t new_off = (size_t)bh * d;  // [B, H, d] new-row tensors
+    if (append && blockIdx.y == 0)          // the new row goes to cache row t, which no CTA reads
+        for (int c = threadIdx.x; c < d; c += kThreads) {
+            P2c[row_offset(kp, bh, t) + c] = P2n[new_off + c];
+            Vc[row_offset(kp, bh, t) + c] = Vn[new_off + c];
+        }
+    if (j0 >= j1) {
+        if (threadIdx.x == 0) {
+            out[0] = -INFINITY;
+            out[1] = 0.f;
+        }
+        return;
+    }
+    const int grp = threadIdx.x / G, li = threadIdx.x % G;
+    const int col = li * VEC;
+    const bool active = col < d;
+    float q[VEC];
+#pragma unroll
+    for (int k = 0; k < VEC; ++k) q[k] = 0.f;
+    if (active) load_vec<Tin, VEC>(P1n + new_off + col, q);
+    const float corr = kp.lambda * logf((float)n);  // lambda log c, c = t+1
+    // Pass 1: scores.  The loop bounds are the same for every thread (the shuffles
+    // need the whole warp); a group past the chunk end only idles.
+    float mloc = -INFINITY;
+    for (int base = j0; base < j1; base += kGroups) {
+        const int j = base + grp;
+        float dot = 0.f;
+        if (j < j1 && active) {
+            float kv[VEC];
+            load_vec<Tin, VEC>(((j == t) ? P2n + new_off : P2c + row_offset(kp, bh, j)) + col, kv);
+#pragma unroll
+            for (int k = 0; k < VEC; ++k) dot = fmaf(q[k], kv[k], dot);
+        }
+#pragma unroll
+        for (int o = G / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+        if (j < j1) {
+            const float u = dot * kp.inv_sqrt_d;
+            const float r = (j == t) ? sigmoid_exact(u / kp.tau_S) : u * sigmoid_exact(u) - corr;
+            if (li == 0) sr[j - j0] = r;
+            mloc = fmaxf(mloc, r);
+        }
+    }
+    const float m = block_reduce(mloc, red, true);  // also orders the score stores
+    // Pass 2: weights and the weighted sum of the information states.
+    float o[VEC];
+#pragma unroll
+    for (int k = 0; k < VEC; ++k) o[k] = 0.f;
+    float lloc = 0.f;
+    for (int j = j0 + grp; j < j1; j += kGroups) {  // no shuffles here
+        const float p = expf(sr[j - j0] - m);
+        if (li == 0) lloc += p;
+        if (active) {
+            float vv[VEC];
+            load_vec<Tin, VEC>(((j == t) ? Vn + new_off : Vc + row_offset(kp, bh, j)) + col, vv);
+#pragma unroll
+            for (int k = 0; k < VEC; ++k) o[k] = fmaf(p, vv[k], o[k]);
+        }
+    }
+    const float l = block_reduce(lloc, red, false);
+    if (active) {
+        float* dst = oacc + (size_t)grp * d + col;
+#pragma unroll
+        for (int k = 0; k < VEC; ++k) dst[k] = o[k];
+    }
+    __syncthreads();
+    for (int c = threadIdx.x; c < d; c += kThreads) {
+        float acc = 0.f;
+        for (int g = 0; g < kGroups; ++g) acc += oacc[(size_t)g * d + c];
+        out[2 + c] = acc;
+    }
+    if (threadIdx.x == 0) {
+        out[0] = m;
+        out[1] = l;
+    }
+}
+
+// Merge of the chunks of one head: Y = sum_c e^{m_c - M} o_c / sum_c e^{m_c - M} l_c,
+// L = M + log(sum_c e^{m_c - M} l_c) (the paper's convention, correction included).
+template <typename Tin>
+__global__ void __launch_bounds__(128) decode_combine_kernel(KernelProblem kp, const float* __restrict__ part,
+                                                              int n_chunks, Tin* __restrict__ Y,
+                                                              float* __restrict__ L) {
+    extern __shared__ float w[];  // per chunk: e^{m_c - M}, then the denominator at w[n_chunks]
+    __shared__ float red[4];
+    const int64_t bh = blockIdx.x;
+    const int d = kp.d;
+    const float* ph = part + (size_t)bh * n_chunks * (d + 2);
+    float mloc = -INFINITY;
+    for (int c = threadIdx.x; c < n_chunks; c += blockDim.x) {
+        const float mc = ph[(size_t)c * (d + 2)];
+        w[c] = mc;
+        mloc = fmaxf(mloc, mc);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mloc;
+    __syncthreads();
+    const float M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    if (M == -INFINITY) return;  // a position outside the cache (reported by the partial pass)
+    float dloc = 0.f;
+    for (int c = threadIdx.x; c < n_chunks; c += blockDim.x) {
+        const float e = (w[c] == -INFINITY) ? 0.f : expf(w[c] - M);
+        w[c] = e;
+        dloc = fmaf(e, ph[(size_t)c * (d + 2) + 1], dloc);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dloc += __shfl_xor_sync(0xffffffffu, dloc, o);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = dloc;
+    __syncthreads();
+    const float den = red[0] + red[1] + red[2] + red[3];
+    for (int col = threadIdx.x; col < d; col += blockDim.x) {
+        float num = 0.f;
+        for (int c = 0; c < n_chunks; ++c)
+            if (w[c] != 0.f) num = fmaf(w[c], ph[(size_t)c * (d + 2) + 2 + col], num);
+        store_from_float(Y + (size_t)bh * d + col, num / den);
+    }
+    if (L != nullptr && threadIdx.x == 0) L[bh] = M + logf(den);
+}
+
+template <typename Tin, int VEC, int G>
+cudaError_t launch_decode_t(const KernelProblem& kp, const void* P1n, const void* P2n, const void* Vn, void* P2c,
+                            void* Vc, const int* pos, int append, void* Y, float* L, float* part, int chunk,
+                            int n_chunks, unsigned int* status, cudaStream_t s) {
+    const size_t smem = sizeof(float) * ((size_t)chunk + 8 + (size_t)(kThreads / G) * kp.d);
+    dim3 grid((unsigned)kp.BH, (unsigned)n_chunks);
+    decode_partial_kernel<Tin, VEC, G><<<grid, kThreads, smem, s>>>(kp, (const Tin*)P1n, (const Tin*)P2n,
+                                                                    (const Tin*)Vn, (Tin*)P2c, (Tin*)Vc, pos, append,
+                                                                    chunk, part, status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    decode_combine_kernel<Tin><<<(unsigned)kp.BH, 128, sizeof(float) * n_chunks, s>>>(kp, part, n_chunks, (Tin*)Y, L);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int decode_chunk() { return 512; }
+
+int decode_chunks(const KernelProblem& kp) { return (kp.T + decode_chunk() - 1) / decode_chunk(); }
+
+cudaError_t launch_decode(const KernelProblem& kp, bool bf16, const void* P1n, const void* P2n, const void* Vn,
+                          void* P2c, void* Vc, const int* pos, int append, void* Y, float* L, float* part,
+                          unsigned int* status, cudaStream_t s) {
+    // Chunk statistics of a head fit in 32 KB of shared memory in the merge (T <= 4M).
+    if (kp.BH > 2147483647LL || decode_chunks(kp) > 8192) return cudaErrorInvalidValue;
+    // Vector width and lanes per key row by (dtype, d): rows are read 16 bytes per
+    // lane where the row pitch allows it (8 bytes for bf16 d = 60).
+#define RELATION_DECODE(T_, VEC, G)                                                                              \
+    return launch_decode_t<T_, VEC, G>(kp, P1n, P2n, Vn, P2c, Vc, pos, append, Y, L, part, decode_chunk(), \
+                                       decode_chunks(kp), status, s)
+    if (bf16) {
+        switch (kp.d) {
+            case 48: RELATION_DECODE(__nv_bfloat16, 8, 8);
+            case 60: RELATION_DECODE(__nv_bfloat16, 4, 16);
+            case 64: RELATION_DECODE(__nv_bfloat16, 8, 8);
+            case 80: RELATION_DECODE(__nv_bfloat16, 8, 16);
+            case 128: RELATION_DECODE(__nv_bfloat16, 8, 16);
+            default: return cudaErrorInvalidValue;
+        }
+    }
+    switch (kp.d) {
+        case 48: RELATION_DECODE(float, 4, 16);
+        case 60: RELATION_DECODE(float, 4, 16);
+        case 64: RELATION_DECODE(float, 4, 16);
+        case 80: RELATION_DECODE(float, 4, 32);
+        case 128: RELATION_DECODE(float, 4, 32);
+        default: return cudaErrorInvalidValue;
+    }
+#undef RELATION_DECODE
+}
+
+}  // namespace relation

@@ -20,6 +20,12 @@ cudaError_t launch_bwd_simt(const KernelProblem& kp, bool bf16, const void* P1, 
 cudaError_t launch_bwd_prepare(const KernelProblem& kp, bool bf16, const void* P1, const void* P2, const void* V,
                                const void* Y, const float* L, const void* dY, float* Dw, float* dq_acc, int dq_w,
                                float* dlambda, cudaStream_t s);
+// Relation Cache decode: kp.T is the cache capacity (rows per head of the caches,
+// stored in kp.layout); part holds decode_chunks(kp) x (d + 2) floats per head.
+int decode_chunks(const KernelProblem& kp);
+cudaError_t launch_decode(const KernelProblem& kp, bool bf16, const void* P1n, const void* P2n, const void* Vn,
+                          void* P2c, void* Vc, const int* pos, int append, void* Y, float* L, float* part,
+                          unsigned int* status, cudaStream_t s);
 // n (<= 4) bf16 operand tensors of width kp.d <= 64 (any layout) -> zero-padded
 // contiguous [BH, T, 64] copies.
 cudaError_t launch_pad_operands(const KernelProblem& kp, const void* const* src, void* const* dst, int n,

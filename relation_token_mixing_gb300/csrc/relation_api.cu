@@ -340,9 +340,51 @@ relation_status_t relation_check_device_status(void) {
         const unsigned int zero = 0;
         if (cudaMemcpy(di.status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
             return RELATION_ERR_CUDA;
-        return RELATION_ERR_DEVICE_TIMEOUT;
+        return word == kDevBadPosition ? RELATION_ERR_INVALID_ARGUMENT : RELATION_ERR_DEVICE_TIMEOUT;
     }
     return RELATION_OK;
+}
+
+size_t relation_decode_workspace_bytes(const relation_problem_t* p) {
+    if (check_problem(p) != RELATION_OK) return 0;
+    const KernelProblem kp = kernel_problem(p);
+    return (size_t)kp.BH * (size_t)decode_chunks(kp) * (size_t)(p->d_h + 2) * sizeof(float);
+}
+
+relation_status_t relation_decode(const relation_problem_t* p, const void* P1_new, const void* P2_new,
+                                  const void* V_new, void* P2_cache, void* V_cache, const int32_t* positions,
+                                  int append, void* Y, float* L, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+    relation_status_t st = check_problem(p);
+    if (st != RELATION_OK) return st;
+    const void* ptrs[] = {P1_new, P2_new, V_new, P2_cache, V_cache, positions, Y, workspace};
+    for (const void* x : ptrs)
+        if (x == nullptr) return RELATION_ERR_INVALID_ARGUMENT;
+    for (const void* x : ptrs)
+        if (!aligned16(x)) return RELATION_ERR_MISALIGNED;
+    if (L != nullptr && !aligned16(L)) return RELATION_ERR_MISALIGNED;
+    const size_t need = relation_decode_workspace_bytes(p);
+    if (workspace_bytes < need) return RELATION_ERR_WORKSPACE_TOO_SMALL;
+    const size_t rows = (size_t)p->B * (size_t)p->H, eb = elem_bytes(p);
+    const size_t nb = rows * (size_t)p->d_h * eb, cb = tensor_bytes(p);
+    const void* in_ptr[] = {P1_new, P2_new, V_new, P2_cache, V_cache, positions};
+    const size_t in_len[] = {nb, nb, nb, cb, cb, (size_t)p->B * sizeof(int32_t)};
+    const void* out_ptr[] = {Y, L, workspace};
+    const size_t out_len[] = {nb, L ? rows * sizeof(float) : 0, need};
+    for (int o = 0; o < 3; ++o) {
+        for (int i = 0; i < 6; ++i)
+            if (overlaps(out_ptr[o], out_len[o], in_ptr[i], in_len[i])) return RELATION_ERR_INVALID_ARGUMENT;
+        for (int o2 = o + 1; o2 < 3; ++o2)
+            if (overlaps(out_ptr[o], out_len[o], out_ptr[o2], out_len[o2])) return RELATION_ERR_INVALID_ARGUMENT;
+    }
+    if (overlaps(P2_cache, cb, V_cache, cb)) return RELATION_ERR_INVALID_ARGUMENT;
+    DeviceInfo di;
+    if ((st = device_info(&di)) != RELATION_OK) return st;
+    st = from_cuda(launch_decode(kernel_problem(p), p->dtype == RELATION_BF16, P1_new, P2_new, V_new, P2_cache,
+                                 V_cache, positions, append, Y, L, static_cast<float*>(workspace), di.status,
+                                 static_cast<cudaStream_t>(stream)));
+    if (st == RELATION_OK) t_last_launches = 2;
+    return st;
 }
 
 int relation_last_launch_count(void) { return t_last_launches; }
