@@ -188,6 +188,36 @@ relation_status_t relation_decode(const relation_problem_t* p, const void* P1_ne
                                   void* stream);
 
 /*
+ * Input prologue of the operator and its backward.
+ *  - RoPE on the relation coordinates (Sec. 3.1 below eq.(1); Appendix B.3: full
+ *    head width, base 10^4 in the paper; the information states stay
+ *    unrotated): coordinate c < d_h/2 turns together with c + d_h/2 by the
+ *    angle pos * rope_base^(-2c/d_h), pos = pos0[b] + t the zero-based token
+ *    position (the pages do not fix the pairing of coordinates; this is the
+ *    half-split form).  rope_base <= 0 disables the rotation (a copy).
+ *  - Givens mixing of the information states of adjacent head pairs (Sec. 3.2
+ *    eq.(4); Appendix A.2.2-A.2.3): for pair k = (a, b) with angle theta[k],
+ *      I~a = cos(theta) Ia - sin(theta) Ib,  I~b = sin(theta) Ia + cos(theta) Ib,
+ *    pairing 0: (1,2), (3,4), ..., (H-1,H); pairing 1: (2,3), ..., (H,1)
+ *    (one-based heads, alternating between layers).  H must be even.
+ * relation_prologue_fwd: X1, X2, I (unrotated / unmixed, [B,H,T,d_h] per
+ *   p->layout, dtype) -> P1, P2, I_mixed (the operator's P1, P2, V).
+ * relation_prologue_bwd: the operator's dP1, dP2, dV (= dI_mixed) and the
+ *   forward's I_mixed -> dX1, dX2, dI and, when dtheta is not NULL, dtheta
+ *   [H/2] float32 (overwritten; dtheta_k = sum dI~b . I~a - dI~a . I~b).
+ * theta: device float32 [H/2].  pos0: optional device int32 [B] (NULL: 0),
+ * e.g. the decode position.  Outputs must not overlap inputs.  Two kernel
+ * launches each (HBM-bound elementwise passes).
+ */
+relation_status_t relation_prologue_fwd(const relation_problem_t* p, const void* X1, const void* X2, const void* I,
+                                        const float* theta, int pairing, float rope_base, const int32_t* pos0,
+                                        void* P1, void* P2, void* I_mixed, void* stream);
+relation_status_t relation_prologue_bwd(const relation_problem_t* p, const void* dP1, const void* dP2,
+                                        const void* dI_mixed, const void* I_mixed, const float* theta, int pairing,
+                                        float rope_base, const int32_t* pos0, void* dX1, void* dX2, void* dI,
+                                        float* dtheta, void* stream);
+
+/*
  * Reads and clears the device status word of the current device.  Call after
  * synchronising the streams used.  Returns RELATION_OK,
  * RELATION_ERR_DEVICE_TIMEOUT (a bounded wait expired; outputs of the calls

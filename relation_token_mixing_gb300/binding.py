@@ -87,6 +87,12 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.relation_bwd_noalloc.restype = ctypes.c_int
         lib.relation_bwd_workspace_bytes.argtypes = [ctypes.POINTER(Problem)]
         lib.relation_bwd_workspace_bytes.restype = ctypes.c_size_t
+        lib.relation_prologue_fwd.argtypes = [ctypes.POINTER(Problem), _VP, _VP, _VP, _VP, ctypes.c_int,
+                                              ctypes.c_float, _VP, _VP, _VP, _VP, _VP]
+        lib.relation_prologue_fwd.restype = ctypes.c_int
+        lib.relation_prologue_bwd.argtypes = [ctypes.POINTER(Problem), _VP, _VP, _VP, _VP, _VP, ctypes.c_int,
+                                              ctypes.c_float, _VP, _VP, _VP, _VP, _VP, _VP]
+        lib.relation_prologue_bwd.restype = ctypes.c_int
         lib.relation_decode_workspace_bytes.argtypes = [ctypes.POINTER(Problem)]
         lib.relation_decode_workspace_bytes.restype = ctypes.c_size_t
         lib.relation_decode.argtypes = [ctypes.POINTER(Problem), _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_int, _VP, _VP,
@@ -206,6 +212,20 @@ def relation_decode(prob, P1_new, P2_new, V_new, P2_cache, V_cache, positions, a
                                   _ptr(V_cache), _ptr(positions), int(append), _ptr(Y), _ptr(L), _ptr(workspace),
                                   workspace.numel() * workspace.element_size(), _stream_ptr(stream)),
            "relation_decode")
+
+
+def relation_prologue_fwd(prob, X1, X2, I, theta, pairing, rope_base, pos0, P1, P2, I_mixed, stream=None) -> None:
+    _check(load().relation_prologue_fwd(ctypes.byref(prob), _ptr(X1), _ptr(X2), _ptr(I), _ptr(theta), int(pairing),
+                                        float(rope_base), _ptr(pos0), _ptr(P1), _ptr(P2), _ptr(I_mixed),
+                                        _stream_ptr(stream)), "relation_prologue_fwd")
+
+
+def relation_prologue_bwd(prob, dP1, dP2, dI_mixed, I_mixed, theta, pairing, rope_base, pos0, dX1, dX2, dI, dtheta,
+                          stream=None) -> None:
+    _check(load().relation_prologue_bwd(ctypes.byref(prob), _ptr(dP1), _ptr(dP2), _ptr(dI_mixed), _ptr(I_mixed),
+                                        _ptr(theta), int(pairing), float(rope_base), _ptr(pos0), _ptr(dX1),
+                                        _ptr(dX2), _ptr(dI), _ptr(dtheta), _stream_ptr(stream)),
+           "relation_prologue_bwd")
 
 
 def relation_check_device_status() -> int:

@@ -20,6 +20,21 @@ cudaError_t launch_bwd_simt(const KernelProblem& kp, bool bf16, const void* P1, 
 cudaError_t launch_bwd_prepare(const KernelProblem& kp, bool bf16, const void* P1, const void* P2, const void* V,
                                const void* Y, const float* L, const void* dY, float* Dw, float* dq_acc, int dq_w,
                                float* dlambda, cudaStream_t s);
+// Input prologue.  RoPE frequencies base^(-2c/d) / (2 pi), c < d/2, as float
+// pairs hi + lo (enabled = 0: no rotation, a copy).
+struct RopeTable {
+    int enabled;
+    float hi[64];
+    float lo[64];
+};
+// RoPE of two operand tensors (x0 -> y0, x1 -> y1); transpose: the backward.
+cudaError_t launch_rope(const KernelProblem& kp, bool bf16, const void* x0, const void* x1, void* y0, void* y1,
+                        const int* pos0, const RopeTable& tab, bool transpose, int num_sms, cudaStream_t s);
+// Givens head-pair mixing x -> y; transpose: the backward, with d theta (+=)
+// accumulated from the mixed states Im when dtheta is not NULL.
+cudaError_t launch_givens(const KernelProblem& kp, bool bf16, const void* x, const void* Im, void* y,
+                          const float* theta, int pairing, bool transpose, float* dtheta, int num_sms,
+                          cudaStream_t s);
 // Relation Cache decode: kp.T is the cache capacity (rows per head of the caches,
 // stored in kp.layout); part holds decode_chunks(kp) x (d + 2) floats per head.
 int decode_chunks(const KernelProblem& kp);

@@ -345,6 +345,90 @@ relation_status_t relation_check_device_status(void) {
     return RELATION_OK;
 }
 
+namespace relation {
+namespace {
+// RoPE frequencies base^(-2c/d) / (2 pi) for c < d/2 as float pairs (computed in double).
+RopeTable rope_table(int d, float base) {
+    RopeTable tab{};
+    tab.enabled = base > 0.f ? 1 : 0;
+    for (int c = 0; c < d / 2 && tab.enabled; ++c) {
+        const double f = pow((double)base, -2.0 * c / d) / (2.0 * 3.14159265358979323846);
+        tab.hi[c] = (float)f;
+        tab.lo[c] = (float)(f - (double)tab.hi[c]);
+    }
+    return tab;
+}
+
+relation_status_t check_prologue(const relation_problem_t* p, const void* const* in, int n_in, const void* const* out,
+                                 int n_out, const float* theta, int pairing, float rope_base) {
+    relation_status_t st = check_problem(p);
+    if (st != RELATION_OK) return st;
+    if (p->H % 2 != 0 || (pairing != 0 && pairing != 1) || !isfinite(rope_base) || theta == nullptr)
+        return RELATION_ERR_INVALID_ARGUMENT;
+    for (int k = 0; k < n_in; ++k)
+        if (in[k] == nullptr) return RELATION_ERR_INVALID_ARGUMENT;
+    for (int k = 0; k < n_out; ++k)
+        if (out[k] == nullptr) return RELATION_ERR_INVALID_ARGUMENT;
+    for (int k = 0; k < n_in; ++k)
+        if (!aligned16(in[k])) return RELATION_ERR_MISALIGNED;
+    for (int k = 0; k < n_out; ++k)
+        if (!aligned16(out[k])) return RELATION_ERR_MISALIGNED;
+    const size_t tb = tensor_bytes(p);
+    for (int o = 0; o < n_out; ++o) {
+        for (int i = 0; i < n_in; ++i)
+            if (overlaps(out[o], tb, in[i], tb)) return RELATION_ERR_INVALID_ARGUMENT;
+        for (int o2 = o + 1; o2 < n_out; ++o2)
+            if (overlaps(out[o], tb, out[o2], tb)) return RELATION_ERR_INVALID_ARGUMENT;
+    }
+    return RELATION_OK;
+}
+}  // namespace
+}  // namespace relation
+
+relation_status_t relation_prologue_fwd(const relation_problem_t* p, const void* X1, const void* X2, const void* I,
+                                        const float* theta, int pairing, float rope_base, const int32_t* pos0,
+                                        void* P1, void* P2, void* I_mixed, void* stream) {
+    const void* in[] = {X1, X2, I};
+    const void* out[] = {P1, P2, I_mixed};
+    relation_status_t st = check_prologue(p, in, 3, out, 3, theta, pairing, rope_base);
+    if (st != RELATION_OK) return st;
+    DeviceInfo di;
+    if ((st = device_info(&di)) != RELATION_OK) return st;
+    const KernelProblem kp = kernel_problem(p);
+    const bool bf16 = p->dtype == RELATION_BF16;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    st = from_cuda(launch_rope(kp, bf16, X1, X2, P1, P2, pos0, rope_table((int)p->d_h, rope_base), false,
+                               di.num_sms, s));
+    if (st != RELATION_OK) return st;
+    st = from_cuda(launch_givens(kp, bf16, I, nullptr, I_mixed, theta, pairing, false, nullptr, di.num_sms, s));
+    if (st == RELATION_OK) t_last_launches = 2;
+    return st;
+}
+
+relation_status_t relation_prologue_bwd(const relation_problem_t* p, const void* dP1, const void* dP2,
+                                        const void* dI_mixed, const void* I_mixed, const float* theta, int pairing,
+                                        float rope_base, const int32_t* pos0, void* dX1, void* dX2, void* dI,
+                                        float* dtheta, void* stream) {
+    const void* in[] = {dP1, dP2, dI_mixed, I_mixed};
+    const void* out[] = {dX1, dX2, dI};
+    relation_status_t st = check_prologue(p, in, 4, out, 3, theta, pairing, rope_base);
+    if (st != RELATION_OK) return st;
+    if (dtheta != nullptr && (reinterpret_cast<uintptr_t>(dtheta) & 3u)) return RELATION_ERR_MISALIGNED;
+    DeviceInfo di;
+    if ((st = device_info(&di)) != RELATION_OK) return st;
+    const KernelProblem kp = kernel_problem(p);
+    const bool bf16 = p->dtype == RELATION_BF16;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtheta != nullptr && cudaMemsetAsync(dtheta, 0, sizeof(float) * (size_t)(p->H / 2), s) != cudaSuccess)
+        return RELATION_ERR_CUDA;
+    st = from_cuda(launch_rope(kp, bf16, dP1, dP2, dX1, dX2, pos0, rope_table((int)p->d_h, rope_base), true,
+                               di.num_sms, s));
+    if (st != RELATION_OK) return st;
+    st = from_cuda(launch_givens(kp, bf16, dI_mixed, I_mixed, dI, theta, pairing, true, dtheta, di.num_sms, s));
+    if (st == RELATION_OK) t_last_launches = 2;
+    return st;
+}
+
 size_t relation_decode_workspace_bytes(const relation_problem_t* p) {
     if (check_problem(p) != RELATION_OK) return 0;
     const KernelProblem kp = kernel_problem(p);
