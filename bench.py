@@ -39,6 +39,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode", action="store_true",
                     help="time one Relation Cache decode step (full caches of the workload's T) instead")
+    ap.add_argument("--prologue", action="store_true",
+                    help="time the input prologue (RoPE + Givens) forward and backward of the workload instead")
     return ap.parse_args()
 
 
@@ -219,6 +221,60 @@ def run_decode(args, w):
     return 0
 
 
+def run_prologue(args, w):
+    """Prologue forward (RoPE of P1, P2; Givens mixing of V) plus backward (transposed
+    rotations and d theta) of the workload's tensors, inputs larger than L2.  HBM-bound:
+    value = bytes read and written / time."""
+    import torch
+
+    from relation_token_mixing_gb300 import binding as rb
+    from relation_token_mixing_gb300 import inputs as rin
+
+    rb.load()
+    dev = torch.device("cuda", 0)
+    x = {k: v.to(dev) for k, v in rin.make(w, with_dy=True).items()}
+    prob = rb.problem_for(x["P1"], w.tau_S, w.lam, True)
+    theta = torch.linspace(-1.0, 1.0, w.H // 2, device=dev)
+    outs = [torch.empty_like(x["P1"]) for _ in range(3)]
+    grads = [torch.empty_like(x["P1"]) for _ in range(3)]
+    dth = torch.empty(w.H // 2, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    tb = x["P1"].numel() * x["P1"].element_size()
+    bytes_step = (3 + 3) * tb + (4 + 3) * tb  # fwd: 3 in, 3 out; bwd: 4 in, 3 out
+    tf, tbw = [], []
+    with ClockSampler(0) as clk:
+        for k in range(args.warmup + args.steps):
+            flush.zero_()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            ev[0].record()
+            rb.relation_prologue_fwd(prob, x["P1"], x["P2"], x["V"], theta, 1, 1e4, None, *outs)
+            ev[1].record()
+            rb.relation_prologue_bwd(prob, x["dY"], x["dY"], x["dY"], outs[2], theta, 1, 1e4, None, *grads, dth)
+            ev[2].record()
+            torch.cuda.synchronize()
+            if k >= args.warmup:
+                tf.append(ev[0].elapsed_time(ev[1]))
+                tbw.append(ev[1].elapsed_time(ev[2]))
+    ms = statistics.mean(tf) + statistics.mean(tbw)
+    hbm = load_peaks_hbm()
+    gbs = bytes_step / (ms * 1e-3) / 1e9
+    line = {
+        "metric": "Relation input prologue (RoPE + Givens) fwd+bwd bytes per second (bf16)",
+        "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32 arithmetic on bf16",
+        "data": "synthetic (seeded Gaussian tensors, resident in HBM)",
+        "config": {"workload": f"prologue_{w.name}", "B": w.B, "H": w.H, "T": w.T, "d_h": w.d, "pairing": "B",
+                   "rope_base": 1e4, "l2": "flushed between timed steps"},
+        "breakdown_ms": {"fwd": statistics.mean(tf), "bwd": statistics.mean(tbw)},
+        "roofline": {"kernel": "rope_kernel + givens_kernel", "bound": "hbm", "achieved": gbs, "peak": hbm[0],
+                     "unit": "GB/s", "frac": gbs / hbm[0], "peak_source": hbm[1], "traffic": None},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def load_peaks_hbm():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -273,6 +329,8 @@ def main():
         return run_reference(args, w)
     if args.decode:
         return run_decode(args, w)
+    if args.prologue:
+        return run_prologue(args, w)
 
     import torch
     import torch.distributed as dist

@@ -31,92 +31,165 @@ __device__ __forceinline__ void rope_sincos(float pos, float hi, float lo, float
     sincospif(2.f * frac, s, c);
 }
 
-template <typename T>
-__device__ __forceinline__ void load2(const T* p, float& a, float& b) {
-    a = load_as_float(p);
-    b = load_as_float(p + 1);
+// VC consecutive elements as fp32 (8-byte loads for bf16 VC = 4, 4-byte VC = 2;
+// 16- / 8-byte for fp32).
+template <typename T, int VC>
+__device__ __forceinline__ void loadv(const T* p, float (&v)[VC]) {
+    if constexpr (sizeof(T) == 2) {
+        uint32_t w[VC / 2];
+        if constexpr (VC == 4) {
+            const uint2 u = *reinterpret_cast<const uint2*>(p);
+            w[0] = u.x;
+            w[1] = u.y;
+        } else {
+            w[0] = *reinterpret_cast<const uint32_t*>(p);
+        }
+#pragma unroll
+        for (int k = 0; k < VC / 2; ++k) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+            v[2 * k] = f.x;
+            v[2 * k + 1] = f.y;
+        }
+    } else if constexpr (VC == 4) {
+        const float4 u = *reinterpret_cast<const float4*>(p);
+        v[0] = u.x, v[1] = u.y, v[2] = u.z, v[3] = u.w;
+    } else {
+        const float2 u = *reinterpret_cast<const float2*>(p);
+        v[0] = u.x, v[1] = u.y;
+    }
 }
-template <typename T>
-__device__ __forceinline__ void store2(T* p, float a, float b) {
-    store_from_float(p, a);
-    store_from_float(p + 1, b);
+template <typename T, int VC>
+__device__ __forceinline__ void storev(T* p, const float (&v)[VC]) {
+    if constexpr (sizeof(T) == 2) {
+        uint32_t w[VC / 2];
+#pragma unroll
+        for (int k = 0; k < VC / 2; ++k) {
+            const __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+            w[k] = *reinterpret_cast<const uint32_t*>(&b);
+        }
+        if constexpr (VC == 4)
+            *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
+        else
+            *reinterpret_cast<uint32_t*>(p) = w[0];
+    } else if constexpr (VC == 4) {
+        *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+    } else {
+        *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
+    }
 }
 
-// RoPE of operand blockIdx.y (0: P1, 1: P2), forward (sign = +1) or transposed
-// (sign = -1, the backward).  One thread per (row, column pair c, c+1) of the
-// first half; base <= 0 copies.
-template <typename T>
+// RoPE of P1 and P2 (x0 -> y0, x1 -> y1), forward (sign = +1) or transposed
+// (sign = -1, the backward).  The angle depends on (batch, token, column) only,
+// so one thread takes VC columns c.. of the first half (and their partners
+// c + d/2) of one (batch, token) and applies them to every kRopeHeadSplit-th
+// head of both tensors (the split gives the loads enough threads in flight).
+constexpr int kRopeHeadSplit = 4;
+// Idx: the flat index type (32-bit whenever the index space fits: its divisions
+// are several times cheaper than 64-bit ones).
+template <typename T, int VC, typename Idx>
 __global__ void __launch_bounds__(kThreads) rope_kernel(KernelProblem kp, const T* __restrict__ x0,
                                                         const T* __restrict__ x1, T* __restrict__ y0,
                                                         T* __restrict__ y1, const int* __restrict__ pos0,
-                                                        RopeTable tab, float sign, int64_t units) {
-    const T* __restrict__ x = blockIdx.y == 0 ? x0 : x1;
-    T* __restrict__ y = blockIdx.y == 0 ? y0 : y1;
-    const int half = kp.d / 2, per_row = half / 2;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < units; k += stride) {
-        const int64_t row = k / per_row;
-        const int c = (int)(k - row * per_row) * 2;
-        const int64_t bh = row / kp.T;
-        const int t = (int)(row - bh * kp.T);
-        const size_t off = row_offset(kp, bh, t);
-        float a0, a1, b0, b1;  // columns c, c+1 and their partners c+d/2, c+1+d/2
-        load2(x + off + c, a0, a1);
-        load2(x + off + c + half, b0, b1);
+                                                        RopeTable tab, float sign, Idx units) {
+    const int half = kp.d / 2;
+    const int hsplit = kp.H < kRopeHeadSplit ? kp.H : kRopeHeadSplit;
+    const Idx per_row = (Idx)(half / VC) * hsplit, Tn = (Idx)kp.T;
+    const Idx stride = (Idx)gridDim.x * blockDim.x;
+    for (Idx k = (Idx)blockIdx.x * blockDim.x + threadIdx.x; k < units; k += stride) {
+        const Idx bt = k / per_row;
+        const int w = (int)(k - bt * per_row);
+        const int hg = w % hsplit;  // this thread's heads: hg, hg + hsplit, ...
+        const int c = (w / hsplit) * VC;
+        const Idx b = bt / Tn;
+        const int t = (int)(bt - b * Tn);
+        float sn[VC], cs[VC];
         if (tab.enabled) {
-            const float pos = (float)((pos0 != nullptr ? pos0[bh / kp.H] : 0) + t);
-            float s0, c0, s1, c1;
-            rope_sincos(pos, tab.hi[c], tab.lo[c], &s0, &c0);
-            rope_sincos(pos, tab.hi[c + 1], tab.lo[c + 1], &s1, &c1);
-            s0 *= sign;
-            s1 *= sign;
-            const float r0 = c0 * a0 - s0 * b0, q0 = s0 * a0 + c0 * b0;
-            const float r1 = c1 * a1 - s1 * b1, q1 = s1 * a1 + c1 * b1;
-            a0 = r0, b0 = q0, a1 = r1, b1 = q1;
+            const float pos = (float)((pos0 != nullptr ? pos0[b] : 0) + t);
+#pragma unroll
+            for (int v = 0; v < VC; ++v) {
+                rope_sincos(pos, tab.hi[c + v], tab.lo[c + v], &sn[v], &cs[v]);
+                sn[v] *= sign;
+            }
+        } else {
+#pragma unroll
+            for (int v = 0; v < VC; ++v) sn[v] = 0.f, cs[v] = 1.f;
         }
-        store2(y + off + c, a0, a1);
-        store2(y + off + c + half, b0, b1);
+        for (int h = hg; h < kp.H; h += hsplit) {
+            const size_t off = row_offset(kp, (int64_t)b * kp.H + h, t) + c;
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                const T* x = which ? x1 : x0;
+                T* y = which ? y1 : y0;
+                float a[VC], q[VC], ra[VC], rq[VC];
+                loadv<T, VC>(x + off, a);
+                loadv<T, VC>(x + off + half, q);
+#pragma unroll
+                for (int v = 0; v < VC; ++v) {
+                    ra[v] = cs[v] * a[v] - sn[v] * q[v];
+                    rq[v] = sn[v] * a[v] + cs[v] * q[v];
+                }
+                storev<T, VC>(y + off, ra);
+                storev<T, VC>(y + off + half, rq);
+            }
+        }
     }
 }
 
 // Givens mixing of the information states, forward (I -> I~) or backward
 // (dI~ -> dI, plus d theta from the mixed states Im = I~ when dtheta != NULL).
-// One warp per (batch, token, head pair); lanes cover column pairs.
-template <typename T>
+// One warp per (batch, token, head pair); each lane takes one VC-column group
+// (d <= 32 VC for every supported width).
+template <typename T, int VC, typename Idx>
 __global__ void __launch_bounds__(kThreads) givens_kernel(KernelProblem kp, const T* __restrict__ x,
                                                           const T* __restrict__ Im, T* __restrict__ y,
                                                           const float* __restrict__ theta, int pairing, float sign,
-                                                          float* __restrict__ dtheta, int64_t rows) {
-    extern __shared__ float acc[];  // per-block partial d theta, H/2 entries
+                                                          float* __restrict__ dtheta, Idx rows) {
+    extern __shared__ float sh[];  // cos, sin, partial d theta: 3 x H/2
     const int P = kp.H / 2;
-    const int lane = threadIdx.x & 31;
-    if (dtheta != nullptr)
-        for (int k = threadIdx.x; k < P; k += blockDim.x) acc[k] = 0.f;
+    float* scos = sh;
+    float* ssin = sh + P;
+    float* acc = sh + 2 * P;
+    for (int k = threadIdx.x; k < P; k += blockDim.x) {
+        float sn, cs;
+        sincosf(theta[k], &sn, &cs);
+        scos[k] = cs;
+        ssin[k] = sign * sn;  // -1: the transposed rotation
+        acc[k] = 0.f;
+    }
     __syncthreads();
-    const int64_t wstride = (int64_t)gridDim.x * (blockDim.x / 32);
-    for (int64_t r = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); r < rows; r += wstride) {
-        const int pr = (int)(r % P);
-        const int64_t bt = r / P;
-        const int t = (int)(bt % kp.T);
-        const int64_t b = bt / kp.T;
+    const int lane = threadIdx.x & 31;
+    const int c = VC * lane;
+    const bool on = c < kp.d;
+    const Idx Pn = (Idx)P, Tn = (Idx)kp.T;
+    const Idx wstride = (Idx)gridDim.x * (blockDim.x / 32);
+    for (Idx r = (Idx)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); r < rows; r += wstride) {
+        const Idx bt = r / Pn;
+        const int pr = (int)(r - bt * Pn);
+        const Idx b = bt / Tn;
+        const int t = (int)(bt - b * Tn);
         const int ha = pairing == 0 ? 2 * pr : 2 * pr + 1;
         const int hb = pairing == 0 ? 2 * pr + 1 : (2 * pr + 2) % kp.H;
-        const size_t oa = row_offset(kp, b * kp.H + ha, t), ob = row_offset(kp, b * kp.H + hb, t);
-        float sn, cs;
-        sincosf(theta[pr], &sn, &cs);
-        sn *= sign;  // -1: the transposed rotation
+        const size_t oa = row_offset(kp, (int64_t)b * kp.H + ha, t) + c;
+        const size_t ob = row_offset(kp, (int64_t)b * kp.H + hb, t) + c;
+        const float cs = scos[pr], sn = ssin[pr];
         float part = 0.f;
-        for (int c = 2 * lane; c < kp.d; c += 64) {
-            float a0, a1, b0, b1;
-            load2(x + oa + c, a0, a1);
-            load2(x + ob + c, b0, b1);
-            store2(y + oa + c, cs * a0 - sn * b0, cs * a1 - sn * b1);
-            store2(y + ob + c, sn * a0 + cs * b0, sn * a1 + cs * b1);
+        if (on) {
+            float a[VC], q[VC], ya[VC], yb[VC];
+            loadv<T, VC>(x + oa, a);
+            loadv<T, VC>(x + ob, q);
+#pragma unroll
+            for (int v = 0; v < VC; ++v) {
+                ya[v] = cs * a[v] - sn * q[v];
+                yb[v] = sn * a[v] + cs * q[v];
+            }
+            storev<T, VC>(y + oa, ya);
+            storev<T, VC>(y + ob, yb);
             if (dtheta != nullptr) {  // x = dI~: dI~b . I~a - dI~a . I~b
-                float ma0, ma1, mb0, mb1;
-                load2(Im + oa + c, ma0, ma1);
-                load2(Im + ob + c, mb0, mb1);
-                part += b0 * ma0 + b1 * ma1 - a0 * mb0 - a1 * mb1;
+                float ma[VC], mb[VC];
+                loadv<T, VC>(Im + oa, ma);
+                loadv<T, VC>(Im + ob, mb);
+#pragma unroll
+                for (int v = 0; v < VC; ++v) part += q[v] * ma[v] - a[v] * mb[v];
             }
         }
         if (dtheta != nullptr) {
@@ -137,22 +210,33 @@ int64_t blocks_for(int64_t units, int num_sms) {
     return b < 1 ? 1 : (b > cap ? cap : b);
 }
 
-template <typename T>
+template <typename T, int VC>
 cudaError_t launch_rope_t(const KernelProblem& kp, const void* x0, const void* x1, void* y0, void* y1,
                           const int* pos0, const RopeTable& tab, float sign, int num_sms, cudaStream_t s) {
-    const int64_t units = kp.BH * (int64_t)kp.T * (kp.d / 4);
-    rope_kernel<T><<<dim3((unsigned)blocks_for(units, num_sms), 2), kThreads, 0, s>>>(
-        kp, (const T*)x0, (const T*)x1, (T*)y0, (T*)y1, pos0, tab, sign, units);
+    const int hsplit = kp.H < kRopeHeadSplit ? kp.H : kRopeHeadSplit;
+    const int64_t units = (kp.BH / kp.H) * (int64_t)kp.T * (kp.d / 2 / VC) * hsplit;  // (batch, token, cols, heads)
+    const unsigned blocks = (unsigned)blocks_for(units, num_sms);
+    if (units + (int64_t)blocks * kThreads < (int64_t)UINT32_MAX)
+        rope_kernel<T, VC, uint32_t><<<blocks, kThreads, 0, s>>>(kp, (const T*)x0, (const T*)x1, (T*)y0, (T*)y1,
+                                                                 pos0, tab, sign, (uint32_t)units);
+    else
+        rope_kernel<T, VC, uint64_t><<<blocks, kThreads, 0, s>>>(kp, (const T*)x0, (const T*)x1, (T*)y0, (T*)y1,
+                                                                 pos0, tab, sign, (uint64_t)units);
     return cudaGetLastError();
 }
 
-template <typename T>
+template <typename T, int VC>
 cudaError_t launch_givens_t(const KernelProblem& kp, const void* x, const void* Im, void* y, const float* theta,
                             int pairing, float sign, float* dtheta, int num_sms, cudaStream_t s) {
     const int64_t rows = (kp.BH / 2) * (int64_t)kp.T;  // (batch, token, head pair)
-    const size_t smem = dtheta != nullptr ? sizeof(float) * (size_t)(kp.H / 2) : 0;
-    givens_kernel<T><<<(unsigned)blocks_for(rows * 32, num_sms), kThreads, smem, s>>>(
-        kp, (const T*)x, (const T*)Im, (T*)y, theta, pairing, sign, dtheta, rows);
+    const size_t smem = sizeof(float) * 3 * (size_t)(kp.H / 2);
+    const unsigned blocks = (unsigned)blocks_for(rows * 32, num_sms);
+    if (rows + (int64_t)blocks * (kThreads / 32) < (int64_t)UINT32_MAX)
+        givens_kernel<T, VC, uint32_t><<<blocks, kThreads, smem, s>>>(kp, (const T*)x, (const T*)Im, (T*)y, theta,
+                                                                      pairing, sign, dtheta, (uint32_t)rows);
+    else
+        givens_kernel<T, VC, uint64_t><<<blocks, kThreads, smem, s>>>(kp, (const T*)x, (const T*)Im, (T*)y, theta,
+                                                                      pairing, sign, dtheta, (uint64_t)rows);
     return cudaGetLastError();
 }
 
@@ -161,16 +245,25 @@ cudaError_t launch_givens_t(const KernelProblem& kp, const void* x, const void* 
 cudaError_t launch_rope(const KernelProblem& kp, bool bf16, const void* x0, const void* x1, void* y0, void* y1,
                         const int* pos0, const RopeTable& tab, bool transpose, int num_sms, cudaStream_t s) {
     const float sign = transpose ? -1.f : 1.f;
-    return bf16 ? launch_rope_t<__nv_bfloat16>(kp, x0, x1, y0, y1, pos0, tab, sign, num_sms, s)
-                : launch_rope_t<float>(kp, x0, x1, y0, y1, pos0, tab, sign, num_sms, s);
+    // Four columns per thread where d/2 allows it (8-byte bf16 / 16-byte fp32 accesses), else two.
+    const bool four = (kp.d / 2) % 4 == 0;
+    if (bf16)
+        return four ? launch_rope_t<__nv_bfloat16, 4>(kp, x0, x1, y0, y1, pos0, tab, sign, num_sms, s)
+                    : launch_rope_t<__nv_bfloat16, 2>(kp, x0, x1, y0, y1, pos0, tab, sign, num_sms, s);
+    return four ? launch_rope_t<float, 4>(kp, x0, x1, y0, y1, pos0, tab, sign, num_sms, s)
+                : launch_rope_t<float, 2>(kp, x0, x1, y0, y1, pos0, tab, sign, num_sms, s);
 }
 
 cudaError_t launch_givens(const KernelProblem& kp, bool bf16, const void* x, const void* Im, void* y,
                           const float* theta, int pairing, bool transpose, float* dtheta, int num_sms,
                           cudaStream_t s) {
     const float sign = transpose ? -1.f : 1.f;
-    return bf16 ? launch_givens_t<__nv_bfloat16>(kp, x, Im, y, theta, pairing, sign, dtheta, num_sms, s)
-                : launch_givens_t<float>(kp, x, Im, y, theta, pairing, sign, dtheta, num_sms, s);
+    const bool four = kp.d % 4 == 0 && (kp.d * (bf16 ? 2 : 4)) % 16 == 0;  // rows aligned for 4-column accesses
+    if (bf16)
+        return four ? launch_givens_t<__nv_bfloat16, 4>(kp, x, Im, y, theta, pairing, sign, dtheta, num_sms, s)
+                    : launch_givens_t<__nv_bfloat16, 2>(kp, x, Im, y, theta, pairing, sign, dtheta, num_sms, s);
+    return four ? launch_givens_t<float, 4>(kp, x, Im, y, theta, pairing, sign, dtheta, num_sms, s)
+                : launch_givens_t<float, 2>(kp, x, Im, y, theta, pairing, sign, dtheta, num_sms, s);
 }
 
 }  // namespace relation
