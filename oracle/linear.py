@@ -5,7 +5,7 @@ Appendix A.4, per head with P1, P2 (after RoPE), information states I~ and the
 channel-wise log-retention g (alpha = exp(g) in (0, 1], Sec. 5.2 eq.(16); the
 projection that produces g from the token is outside the operator):
     S_t  = sigmoid(p1_t . p2_t / (tau_S sqrt(d)))                          (15)
-    p^1_t = p1_t / ||p1_t||,  p^2_t = p2_t / ||p2_t||
+    p^1_t = p1_t / ||p1_t||,  p^2_t = p2_t / ||p2_t||   (a zero vector maps to zero)
     C-_t = Diag(alpha_t) C_{t-1},   C_0 = 0 (or a given initial state)
     E_t  = S_t (C-_t)^T p^1_t,  Y_t = I~_t + E_t,  C_t = C-_t + S_t p^2_t I~_t^T   (17)
 The backward is the chain rule of this recurrence, run backwards in time with
@@ -21,7 +21,10 @@ def _prep(p1, p2, tau):
     n1, n2 = np.linalg.norm(p1), np.linalg.norm(p2)
     z = float(p1 @ p2) / (tau * np.sqrt(d))
     S = 1.0 / (1.0 + np.exp(-z))
-    return S, p1 / n1, p2 / n2, n1, n2
+    # A zero coordinate vector normalises to zero (the pages leave 0/0 open).
+    q = p1 / n1 if n1 > 0 else np.zeros_like(p1)
+    k = p2 / n2 if n2 > 0 else np.zeros_like(p2)
+    return S, q, k, n1, n2
 
 
 def fwd(P1, P2, I, G, tau: float, C0=None):
@@ -99,6 +102,6 @@ def bwd(P1, P2, I, G, tau: float, dY):
                 # S = sigmoid(p1.p2 / (tau sqrt d)); p^ = p / ||p||
                 dz = dS * S * (1.0 - S) / (tau * sq)
                 p1, p2 = P1[b, h, t], P2[b, h, t]
-                dP1[b, h, t] = (dq - q * float(q @ dq)) / n1 + dz * p2
-                dP2[b, h, t] = (dk - k * float(k @ dk)) / n2 + dz * p1
+                dP1[b, h, t] = dz * p2 + ((dq - q * float(q @ dq)) / n1 if n1 > 0 else 0.0)
+                dP2[b, h, t] = dz * p1 + ((dk - k * float(k @ dk)) / n2 if n2 > 0 else 0.0)
     return dP1, dP2, dI, dG

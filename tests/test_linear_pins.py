@@ -114,6 +114,20 @@ def test_write_stores_information_not_answer():
     assert np.allclose(Y[0, 0, 2], I[0, 0, 2] + E3, rtol=1e-13)
 
 
+def test_zero_coordinates_neither_read_nor_write():
+    """A token whose p1 is zero reads nothing (E_t = 0); one whose p2 is zero writes
+    nothing, so the later tokens see the same history as with that token's I~ zeroed."""
+    P1, P2, I, G = _inputs(1, 1, 6, 4, seed=10)
+    P1[0, 0, 2] = 0.0
+    P2[0, 0, 3] = 0.0
+    Y, _ = lo.fwd(P1, P2, I, G, 1.0)
+    assert np.array_equal(Y[0, 0, 2], I[0, 0, 2])
+    I0 = I.copy()
+    I0[0, 0, 3] = 0.0
+    Y0, _ = lo.fwd(P1, P2, I0, G, 1.0)
+    assert np.allclose((Y - I)[0, 0, 4:], (Y0 - I0)[0, 0, 4:], rtol=0, atol=1e-15)
+
+
 def test_split_sequence_carries_the_state():
     P1, P2, I, G = _inputs(2, 2, 20, 6, seed=7)
     Y, CT = lo.fwd(P1, P2, I, G, 1.3)
