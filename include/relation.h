@@ -218,6 +218,38 @@ relation_status_t relation_prologue_bwd(const relation_problem_t* p, const void*
                                         float* dtheta, void* stream);
 
 /*
+ * Linear Relation ("Ask Self, Ask Others", Sec. 5.2 eq.(15)-(17); Appendix
+ * A.4): per head a d_h x d_h relational state C with C_0 = 0 and channel-wise
+ * retention alpha_t = exp(G_t) (Sec. 5.2 eq.(16); the projection producing G
+ * from the token is the caller's), read before it is written:
+ *
+ *   S_t  = sigmoid(p1_t . p2_t / (tau_S sqrt(d_h)))                  eq.(15)
+ *   p^_t = p_t / ||p_t||   (a zero vector stays zero)
+ *   C-_t = Diag(alpha_t) C_{t-1},  E_t = S_t (C-_t)^T p^1_t,  Y_t = I~_t + E_t,
+ *   C_t  = C-_t + S_t p^2_t I~_t^T                                    eq.(17)
+ *
+ * P1, P2 (after RoPE), I (= I~) and Y: [B,H,T,d_h] or [B,T,H,d_h] per
+ * p->layout, bfloat16.  G: log-retention (<= 0 for alpha in (0, 1]; any
+ * finite value is accepted), float32, same layout.  p->lambda and p->causal
+ * are ignored (the recurrence is causal by construction).  Supported: d_h in
+ * {48, 60, 64}, dtype RELATION_BF16 (fp32 state and accumulation); others
+ * return RELATION_ERR_UNSUPPORTED.
+ *
+ * relation_linear_fwd: Y and, when `state` is not NULL, the final state C_T
+ *   per head, float32 [B, H, d_h, d_h] (row = key channel, column = value
+ *   channel).  1 to 3 kernel launches (segment state pass and scan only when
+ *   B*H is too small to fill the GPU).
+ * relation_linear_workspace_bytes: the float32 workspace both directions need
+ *   (16-byte aligned, caller-owned, contents need not be preserved between
+ *   calls); 0 on invalid arguments.
+ * Outputs must not overlap inputs.
+ */
+size_t relation_linear_workspace_bytes(const relation_problem_t* p);
+relation_status_t relation_linear_fwd(const relation_problem_t* p, const void* P1, const void* P2, const void* I,
+                                      const float* G, void* Y, float* state, void* workspace,
+                                      size_t workspace_bytes, void* stream);
+
+/*
  * Reads and clears the device status word of the current device.  Call after
  * synchronising the streams used.  Returns RELATION_OK,
  * RELATION_ERR_DEVICE_TIMEOUT (a bounded wait expired; outputs of the calls

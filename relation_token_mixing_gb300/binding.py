@@ -98,6 +98,11 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.relation_decode.argtypes = [ctypes.POINTER(Problem), _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_int, _VP, _VP,
                                         _VP, ctypes.c_size_t, _VP]
         lib.relation_decode.restype = ctypes.c_int
+        lib.relation_linear_workspace_bytes.argtypes = [ctypes.POINTER(Problem)]
+        lib.relation_linear_workspace_bytes.restype = ctypes.c_size_t
+        lib.relation_linear_fwd.argtypes = [ctypes.POINTER(Problem), _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                            ctypes.c_size_t, _VP]
+        lib.relation_linear_fwd.restype = ctypes.c_int
         lib.relation_check_device_status.argtypes = []
         lib.relation_check_device_status.restype = ctypes.c_int
         lib.relation_last_launch_count.argtypes = []
@@ -228,6 +233,16 @@ def relation_prologue_bwd(prob, dP1, dP2, dI_mixed, I_mixed, theta, pairing, rop
            "relation_prologue_bwd")
 
 
+def relation_linear_workspace_bytes(prob: Problem) -> int:
+    return int(load().relation_linear_workspace_bytes(ctypes.byref(prob)))
+
+
+def relation_linear_fwd(prob, P1, P2, I, G, Y, state, workspace, stream=None) -> None:
+    _check(load().relation_linear_fwd(ctypes.byref(prob), _ptr(P1), _ptr(P2), _ptr(I), _ptr(G), _ptr(Y),
+                                      _ptr(state), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                      _stream_ptr(stream)), "relation_linear_fwd")
+
+
 def relation_check_device_status() -> int:
     return int(load().relation_check_device_status())
 
@@ -253,6 +268,25 @@ def fwd(P1, P2, V, tau_S: float, lam: float, causal: bool = True, stream=None, w
     L = torch.empty((prob.B, prob.H, prob.T), dtype=torch.float32, device=P1.device) if want_L else None
     relation_fwd(prob, P1, P2, V, Y, L, stream)
     return Y, L
+
+
+def linear_workspace(prob: Problem, device) -> torch.Tensor:
+    """Workspace tensor for relation_linear_fwd / relation_linear_bwd."""
+    n = relation_linear_workspace_bytes(prob)
+    return torch.empty(max(1, (n + 3) // 4), dtype=torch.float32, device=device)
+
+
+def linear_fwd(P1, P2, I, G, tau_S: float, layout: int = RELATION_LAYOUT_BHTD, want_state: bool = False,
+               stream=None, workspace=None):
+    """Linear Relation forward; allocates Y (and the final state [B, H, d, d]); returns (Y, state)."""
+    prob = problem_for(P1, tau_S, 0.0, True, layout)
+    Y = torch.empty_like(I)
+    state = (torch.empty((prob.B, prob.H, prob.d_h, prob.d_h), dtype=torch.float32, device=P1.device)
+             if want_state else None)
+    if workspace is None:
+        workspace = linear_workspace(prob, P1.device)
+    relation_linear_fwd(prob, P1, P2, I, G, Y, state, workspace, stream)
+    return Y, state
 
 
 def decode(P1_new, P2_new, V_new, P2_cache, V_cache, positions, tau_S: float, lam: float, append: bool = True,

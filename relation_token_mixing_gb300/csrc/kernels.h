@@ -49,6 +49,12 @@ cudaError_t launch_pad_operands(const KernelProblem& kp, const void* const* src,
 cudaError_t launch_convert(const KernelProblem& kp, const float* src, int dq_w, void* dst, bool bf16, int num_sms,
                            cudaStream_t s);
 
+// Linear Relation (bf16 operands, fp32 log-retention G, d <= 64).  The
+// workspace holds BH * nseg * (64 * 64 + 64) floats for the segment states.
+int linear_segments(const KernelProblem& kp, int num_sms, int* seg_len);
+cudaError_t launch_linear_fwd(const KernelProblem& kp, const void* P1, const void* P2, const void* V, const float* G,
+                              void* Y, float* state_out, float* ws, int num_sms, cudaStream_t s);
+
 // Tensor-core (tcgen05) bf16 path.
 struct TcLaunch {
     int num_sms;

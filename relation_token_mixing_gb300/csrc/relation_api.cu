@@ -429,6 +429,61 @@ relation_status_t relation_prologue_bwd(const relation_problem_t* p, const void*
     return st;
 }
 
+namespace relation {
+namespace {
+relation_status_t check_linear(const relation_problem_t* p) {
+    relation_status_t st = check_problem(p);
+    if (st != RELATION_OK) return st;
+    if (p->dtype != RELATION_BF16) return RELATION_ERR_UNSUPPORTED;
+    if (p->d_h != 48 && p->d_h != 60 && p->d_h != 64) return RELATION_ERR_UNSUPPORTED;
+    return RELATION_OK;
+}
+// Floats of the segment-state workspace of one direction.
+size_t linear_ws_floats(const relation_problem_t* p, int num_sms) {
+    int len = 0;
+    const int nseg = linear_segments(kernel_problem(p), num_sms, &len);
+    return (size_t)p->B * (size_t)p->H * (size_t)nseg * (64 * 64 + 64);
+}
+}  // namespace
+}  // namespace relation
+
+size_t relation_linear_workspace_bytes(const relation_problem_t* p) {
+    if (check_linear(p) != RELATION_OK) return 0;
+    DeviceInfo di;
+    if (device_info(&di) != RELATION_OK) return 0;
+    return linear_ws_floats(p, di.num_sms) * sizeof(float);
+}
+
+relation_status_t relation_linear_fwd(const relation_problem_t* p, const void* P1, const void* P2, const void* I,
+                                      const float* G, void* Y, float* state, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+    relation_status_t st = check_linear(p);
+    if (st != RELATION_OK) return st;
+    if (!P1 || !P2 || !I || !G || !Y || !workspace) return RELATION_ERR_INVALID_ARGUMENT;
+    if (!aligned16(P1) || !aligned16(P2) || !aligned16(I) || !aligned16(G) || !aligned16(Y) ||
+        !aligned16(workspace) || (state && !aligned16(state)))
+        return RELATION_ERR_MISALIGNED;
+    DeviceInfo di;
+    if ((st = device_info(&di)) != RELATION_OK) return st;
+    if (workspace_bytes < linear_ws_floats(p, di.num_sms) * sizeof(float)) return RELATION_ERR_WORKSPACE_TOO_SMALL;
+    const size_t tb = tensor_bytes(p), gb = rows_of(p) * (size_t)p->d_h * sizeof(float);
+    const size_t sb = (size_t)p->B * p->H * p->d_h * p->d_h * sizeof(float);
+    const void* ins[] = {P1, P2, I};
+    for (const void* x : ins) {
+        if (overlaps(Y, tb, x, tb)) return RELATION_ERR_INVALID_ARGUMENT;
+        if (state && overlaps(state, sb, x, tb)) return RELATION_ERR_INVALID_ARGUMENT;
+    }
+    if (overlaps(Y, tb, G, gb) || (state && (overlaps(state, sb, G, gb) || overlaps(state, sb, Y, tb))))
+        return RELATION_ERR_INVALID_ARGUMENT;
+    const KernelProblem kp = kernel_problem(p);
+    int len = 0;
+    const int nseg = linear_segments(kp, di.num_sms, &len);
+    st = from_cuda(launch_linear_fwd(kp, P1, P2, I, G, Y, state, static_cast<float*>(workspace), di.num_sms,
+                                     static_cast<cudaStream_t>(stream)));
+    if (st == RELATION_OK) t_last_launches = nseg > 1 ? 3 : 1;
+    return st;
+}
+
 size_t relation_decode_workspace_bytes(const relation_problem_t* p) {
     if (check_problem(p) != RELATION_OK) return 0;
     const KernelProblem kp = kernel_problem(p);

@@ -81,3 +81,58 @@ WORKLOADS = {
     "mhr_fwd_bwd_T4096": Workload("mhr_fwd_bwd_T4096", 4, 16, 4096, 64, torch.bfloat16, 0.5, 0.5,
                                   p_scale=3.0 / 64 ** 0.25, backward=True),
 }
+
+
+# ---------------------------------------------------------------- Linear Relation
+# Inputs of Linear Relation ("Ask Self, Ask Others", Sec. 5.2): P1, P2, I~ as above
+# (bf16) plus the float32 log-retention G <= 0.  G is drawn with the statistics of its
+# parameterisation at initialisation (eq.(16), the caller's projection, not part of the
+# operator): g = -a * softplus(0.5 z + b) with a ~ U(1, 16) per (head, channel),
+# softplus(b) log-uniform in [1e-3, 1e-1] per (head, channel), z ~ N(0, 1) per entry;
+# ``g_scale`` multiplies the result (strong or weak retention cases).
+LINEAR_G_SEED = 46
+
+
+@dataclass(frozen=True)
+class LinearWorkload:
+    name: str
+    B: int
+    H: int
+    T: int
+    d: int
+    tau_S: float = 2.0
+    g_scale: float = 1.0
+    backward: bool = False
+
+
+def linear_retention(B: int, H: int, T: int, d: int, seed: int = LINEAR_G_SEED, g_scale: float = 1.0) -> torch.Tensor:
+    g = torch.Generator().manual_seed(int(seed))
+    a = 1.0 + 15.0 * torch.rand(1, H, 1, d, generator=g)
+    sp_b = torch.exp(torch.empty(1, H, 1, d).uniform_(float(torch.log(torch.tensor(1e-3))),
+                                                     float(torch.log(torch.tensor(1e-1))), generator=g))
+    b = torch.log(torch.expm1(sp_b))  # inverse softplus
+    z = torch.randn(B, H, T, d, generator=g)
+    return (-g_scale * a * torch.nn.functional.softplus(0.5 * z + b)).to(torch.float32)
+
+
+def make_linear(w: LinearWorkload) -> dict:
+    """CPU tensors P1, P2, I (bf16), G (float32) and, when backward, dY (bf16); [B, H, T, d]."""
+    shape = (w.B, w.H, w.T, w.d)
+    out = {
+        "P1": gaussian(shape, SEEDS["P1"], 1.0, torch.bfloat16),
+        "P2": gaussian(shape, SEEDS["P2"], 1.0, torch.bfloat16),
+        "I": gaussian(shape, SEEDS["V"], 1.0, torch.bfloat16),
+        "G": linear_retention(w.B, w.H, w.T, w.d, g_scale=w.g_scale),
+    }
+    if w.backward:
+        out["dY"] = gaussian(shape, SEEDS["dY"], 1.0, torch.bfloat16)
+    return out
+
+
+# The Hybrid model's Linear Relation layers (Appendix F.1: 8 heads of width 60, T = 2048,
+# micro-batch 16) and the longest context its long-context runs pass (Appendix I.2,
+# Table 28: T = 32768, micro-batch 1).
+LINEAR_WORKLOADS = {
+    "linear_d60_T2048": LinearWorkload("linear_d60_T2048", 16, 8, 2048, 60, backward=True),
+    "linear_d60_T32768": LinearWorkload("linear_d60_T32768", 1, 8, 32768, 60, backward=True),
+}

@@ -1,0 +1,110 @@
+"""GPU parity of Linear Relation ("Ask Self, Ask Others", Sec. 5.2 eq.(15)-(17),
+Appendix A.4) against the float64 recurrent oracle, through the C ABI.
+
+Tolerance (bf16 operands, fp32 state and accumulation): the state enters every chunk
+as a bf16 tensor-core operand and the chunk operands (q . F, k . B, the intra-chunk
+matrix) are rounded to bf16 (relative 2^-9 each), and Y is rounded to bf16 once, so
+    max |Y - Y_ref| <= 1e-2 * max |Y_ref|;
+the final fp32 state sums bf16-rounded products: max |C - C_ref| <= 1e-2 * max |C_ref|.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import linear as lo
+from relation_token_mixing_gb300 import binding as rb
+from relation_token_mixing_gb300 import inputs as rin
+
+pytestmark = pytest.mark.gpu
+
+BHTD, BTHD = rb.RELATION_LAYOUT_BHTD, rb.RELATION_LAYOUT_BTHD
+TOL = 1e-2
+
+
+def _np(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def _to(t, layout):
+    return t.permute(0, 2, 1, 3).contiguous() if layout == BTHD else t.contiguous()
+
+
+def _back(t, layout):
+    return t.permute(0, 2, 1, 3) if layout == BTHD else t
+
+
+def _run_fwd(x, tau, layout, want_state=True):
+    dev = {k: _to(v, layout).cuda() for k, v in x.items()}
+    Y, C = rb.linear_fwd(dev["P1"], dev["P2"], dev["I"], dev["G"], tau, layout=layout, want_state=want_state)
+    torch.cuda.synchronize()
+    assert rb.relation_check_device_status() == 0
+    return _np(_back(Y, layout)), (None if C is None else _np(C))
+
+
+def _err(a, b):
+    return float(np.max(np.abs(np.asarray(a) - np.asarray(b))))
+
+
+# name, B, H, T, d, layout, g_scale, tau
+CASES = [
+    ("d64_ragged", 2, 3, 100, 64, BHTD, 1.0, 2.0),
+    ("d64_segments", 1, 2, 700, 64, BHTD, 1.0, 1.0),
+    ("d60_bthd_segments", 1, 4, 333, 60, BTHD, 1.0, 2.0),
+    ("d48", 2, 2, 150, 48, BHTD, 1.0, 0.5),
+    ("d64_strong_decay", 1, 2, 200, 64, BHTD, 8.0, 2.0),
+    ("d64_full_retention", 1, 2, 300, 64, BHTD, 0.0, 2.0),
+    ("d64_T1", 2, 2, 1, 64, BHTD, 1.0, 2.0),
+    ("d60_T17", 1, 3, 17, 60, BTHD, 1.0, 2.0),
+]
+
+
+@pytest.mark.parametrize("name,B,H,T,d,layout,gs,tau", CASES, ids=[c[0] for c in CASES])
+def test_linear_forward_matches_oracle(name, B, H, T, d, layout, gs, tau):
+    x = rin.make_linear(rin.LinearWorkload(name, B, H, T, d, tau, gs))
+    Y, C = _run_fwd(x, tau, layout)
+    xs = {k: _np(v) for k, v in x.items()}
+    Yr, Cr = lo.fwd(xs["P1"], xs["P2"], xs["I"], xs["G"], tau)
+    assert _err(Y, Yr) <= TOL * float(np.max(np.abs(Yr))), name
+    assert _err(C, Cr) <= TOL * max(float(np.max(np.abs(Cr))), 1e-6), name
+
+
+def test_linear_forward_first_token_is_its_information():
+    """Strict historical support (Appendix A.4.3): Y_1 = I~_1 exactly."""
+    x = rin.make_linear(rin.LinearWorkload("first", 2, 4, 40, 64))
+    Y, _ = _run_fwd(x, 2.0, BHTD, want_state=False)
+    assert np.array_equal(Y[:, :, 0], _np(x["I"])[:, :, 0])
+
+
+def test_linear_forward_many_heads_sampled():
+    """B*H large enough for one segment per head (the single-pass path); sampled heads."""
+    B, H, T, d, tau = 48, 8, 96, 64, 2.0
+    x = rin.make_linear(rin.LinearWorkload("many", B, H, T, d, tau))
+    Y, C = _run_fwd(x, tau, BHTD)
+    for b, h in [(0, 0), (17, 5), (47, 7)]:
+        xs = {k: _np(v[b:b + 1, h:h + 1]) for k, v in x.items()}
+        Yr, Cr = lo.fwd(xs["P1"], xs["P2"], xs["I"], xs["G"], tau)
+        assert _err(Y[b:b + 1, h:h + 1], Yr) <= TOL * float(np.max(np.abs(Yr)))
+        assert _err(C[b:b + 1, h:h + 1], Cr) <= TOL * float(np.max(np.abs(Cr)))
+
+
+def test_linear_forward_zero_coordinates():
+    x = rin.make_linear(rin.LinearWorkload("zero", 1, 2, 48, 64))
+    x["P1"][0, 0, 5] = 0
+    x["P2"][0, 1, 20:24] = 0
+    Y, C = _run_fwd(x, 2.0, BHTD)
+    xs = {k: _np(v) for k, v in x.items()}
+    Yr, Cr = lo.fwd(xs["P1"], xs["P2"], xs["I"], xs["G"], 2.0)
+    assert np.array_equal(Y[0, 0, 5], xs["I"][0, 0, 5])
+    assert _err(Y, Yr) <= TOL * float(np.max(np.abs(Yr)))
+
+
+def test_linear_rejects_unsupported():
+    x = torch.zeros(1, 1, 8, 80, dtype=torch.bfloat16, device="cuda")
+    g = torch.zeros(1, 1, 8, 80, dtype=torch.float32, device="cuda")
+    with pytest.raises(rb.RelationError) as e:
+        rb.linear_fwd(x, x, x, g, 1.0)
+    assert e.value.code == 2
+    xf = torch.zeros(1, 1, 8, 64, dtype=torch.float32, device="cuda")
+    with pytest.raises(rb.RelationError) as e:
+        rb.linear_fwd(xf, xf, xf, xf, 1.0)
+    assert e.value.code == 2
