@@ -5,14 +5,17 @@
 //     C_t  = C-_t + S_t p^2_t I~_t^T,  S_t = sigmoid(p1_t . p2_t / (tau_S sqrt d)),
 // p^ = p / ||p|| (a zero vector stays zero).
 //
-// Execution.  One warp owns one (head, segment) pair and walks the segment in
-// chunks of 16 tokens, with q = S p^1 and k = S p^2:
-//   * the state enters a chunk through two warp-level bf16 tensor-core products
-//     (E += (q . F) C and C <- Diag(a) C + (k . B)^T I~, F / B the retention
+// Execution.  One CTA of 4 warps owns one (head, segment) pair and walks the
+// segment in chunks of 16 tokens, with q = S p^1 and k = S p^2:
+//   * the state enters a chunk through warp-level bf16 tensor-core products,
+//     E += (q . F) C and C <- Diag(a) C + (k . B)^T I~ (F / B the retention
 //     products from the chunk start to t / from t to the chunk end, a = F_15);
-//   * pairs inside the chunk use the exact retention product of every pair,
-//     prod_{u=j+1..i} alpha_u, formed by running multiplications on the fp32
-//     pipes, so no factor ever exceeds 1 and any g <= 0 is exact;
+//     warp w owns the value channels [16w, 16w+16) of C and of E;
+//   * pairs inside the chunk: split at the highest bit in which the two token
+//     indices differ, every pair (i, j) has a boundary r with j < r <= i, and
+//     prod_{u=j+1..i} alpha_u = prod_{u=r..i} alpha_u * prod_{u=j+1..r-1} alpha_u;
+//     the four bit levels are four small tensor-core products whose operands
+//     carry these factors, all <= 1, so any g <= 0 is exact;
 //   * long sequences with few heads are split into segments: a state pass gives
 //     each segment's own contribution and retention, a scan over segments gives
 //     every segment's entering state, and the output pass runs from it.
@@ -32,7 +35,6 @@ namespace lin {
 
 constexpr int kC = 16;          // tokens per chunk
 constexpr int kDp = 64;         // head width the kernels work in (narrower heads are zero-padded)
-constexpr int kWarpsPerCta = 3;
 
 // ---------------------------------------------------------------- PTX helpers
 __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -92,22 +94,47 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
 }
 constexpr int kArow = 48;  // bytes per row of the 16 x 16 bf16 intra-chunk matrix
 
-// --------------------------------------------------------------- per-warp smem
+// ldmatrix lane addresses (PTX fragment layouts of m16n8k16).
+// A operand 16 x 16 from a row-major [m][k] swizzled tile at column k0.
+__device__ __forceinline__ uint32_t addr_a(const uint8_t* tile, int k0, int lane) {
+    const int m = lane >> 3, r = (lane & 7) + 8 * (m & 1), c = k0 + 8 * (m >> 1);
+    return ptx::smem_u32(tile) + swz(r, c);
+}
+// B fragments of two 8-wide column blocks n0, n0+8 from a [k][n] tile (.trans).
+__device__ __forceinline__ uint32_t addr_bt(const uint8_t* tile, int n0, int lane) {
+    const int m = lane >> 3, r = (lane & 7) + 8 * (m & 1), c = n0 + 8 * (m >> 1);
+    return ptx::smem_u32(tile) + swz(r, c);
+}
+// A operand from a [k][m] tile (.trans): a0..a3 = (m0-7,k0-7), (m8-15,k0-7),
+// (m0-7,k8-15), (m8-15,k8-15).
+__device__ __forceinline__ uint32_t addr_at(const uint8_t* tile, int m0, int lane) {
+    const int m = lane >> 3, r = (lane & 7) + 8 * (m >> 1), c = m0 + 8 * (m & 1);
+    return ptx::smem_u32(tile) + swz(r, c);
+}
+
+
+// ------------------------------------------------------------- group smem
+// One group of 4 warps (one CTA) owns a (head, segment) pair.  Warp w owns the
+// value channels v in [16w, 16w+16) of the state and of the outputs.
+constexpr int kWarps = 4;
+constexpr int kThreads = 32 * kWarps;
+
 struct Stage {
     uint8_t p1[kC * 128];  // bf16, swizzled
     uint8_t p2[kC * 128];
     uint8_t v[kC * 128];
-    float g[kC * kDp];  // fp32 rows of 64; overwritten in place by alpha = exp(g)
+    float g[kC * kDp];  // fp32 rows of 64
 };
-struct WarpSmem {
+struct GroupSmem {
     Stage st[2];
-    uint8_t qt[kC * 128];  // q . F        (bf16, swizzled)
-    uint8_t kb[kC * 128];  // k . B        (bf16, swizzled)
-    float qf[kC * kDp];    // q (fp32)
-    float kf[kC * kDp];    // k (fp32)
-    uint8_t amat[kC * kArow];
-    float2 rs[kC];    // (S / ||p1||, S / ||p2||) per token
-    float avec[kDp];  // retention over the whole chunk
+    uint8_t qt[kC * 128];     // q . F   (F: retention from the chunk start to t)
+    uint8_t kb[kC * 128];     // k . B   (B: retention from t to the chunk end)
+    uint8_t ql[4][kC * 128];  // level query operands (rows that are queries at that level)
+    uint8_t kl[4][8 * 128];   // level key operands, the 8 key rows of each level compacted
+    uint8_t amat[kC * kArow]; // intra-chunk matrix (bf16)
+    float2 rs[kC];            // (S / ||p1||, S / ||p2||)
+    float avec[kDp];          // retention over the chunk
+    float tot[4][kDp];        // retention over each quarter (4 tokens) of the chunk
 };
 
 struct Args {
@@ -125,420 +152,430 @@ struct Args {
     int seg_len;  // tokens per segment, a multiple of kC
 };
 
-// Issues the copies of chunk rows t0 .. t0+15 into a stage (rows >= T and the
-// columns >= d of the fp32 tile are zero / unused; the bf16 tiles' columns >= d
-// are zeroed once at kernel start and never written).
+// Element offset of row 0 of head bh and the distance between rows.
+struct RowMap {
+    size_t base;
+    size_t stride;
+};
+__device__ __forceinline__ RowMap row_map(const KernelProblem& kp, int64_t bh) {
+    return RowMap{row_offset(kp, bh, 0), kp.layout == 0 ? (size_t)kp.d : (size_t)kp.H * kp.d};
+}
+
+// Warp w issues the copies of tensor w (P1, P2, I~, G) for chunk rows
+// t0 .. t0+15 (rows >= T zero; bf16 columns >= d stay zero from the start).
 template <bool kVec16>
-__device__ __forceinline__ void load_chunk(Stage& s, const Args& a, int64_t bh, int t0, int lane) {
+__device__ __forceinline__ void load_chunk(Stage& s, const Args& a, const RowMap& rm, int t0, int warp, int lane) {
     const KernelProblem& kp = a.kp;
-    const __nv_bfloat16* src[3] = {a.P1, a.P2, a.V};
-    uint8_t* dst[3] = {s.p1, s.p2, s.v};
-#pragma unroll
-    for (int m = 0; m < 3; ++m) {
-        const uint32_t base = ptx::smem_u32(dst[m]);
+    if (warp < 3) {
+        const __nv_bfloat16* src = (warp == 0 ? a.P1 : (warp == 1 ? a.P2 : a.V)) + rm.base + (size_t)t0 * rm.stride;
+        const uint32_t base = ptx::smem_u32(warp == 0 ? s.p1 : (warp == 1 ? s.p2 : s.v));
         if (kVec16) {
+            const int q = lane & 7, col = 8 * q;
+            if (col < kp.d) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int idx = lane + 32 * k, r = idx >> 3, q = idx & 7, col = 8 * q;
-                if (col >= kp.d) continue;
-                const uint32_t d = base + r * 128 + (((q ^ r) & 7) << 4);
-                if (t0 + r < kp.T)
-                    cp_async_16(d, src[m] + row_offset(kp, bh, t0 + r) + col);
-                else
-                    st_zero16(d);
+                for (int k = 0; k < 4; ++k) {
+                    const int r = (lane >> 3) + 4 * k;
+                    const uint32_t dst = base + r * 128 + (((q ^ r) & 7) << 4);
+                    if (t0 + r < kp.T)
+                        cp_async_16(dst, src + (size_t)r * rm.stride + col);
+                    else
+                        st_zero16(dst);
+                }
             }
         } else {
+            const int q = lane & 15, col = 4 * q;
+            if (col < kp.d) {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int idx = lane + 32 * k, r = idx >> 4, q = idx & 15, col = 4 * q;
-                if (col >= kp.d) continue;
-                const uint32_t d = base + r * 128 + ((((q >> 1) ^ r) & 7) << 4) + ((q & 1) << 3);
-                if (t0 + r < kp.T)
-                    cp_async_8(d, src[m] + row_offset(kp, bh, t0 + r) + col);
-                else
-                    st_shared_zero8(d);
+                for (int k = 0; k < 8; ++k) {
+                    const int r = (lane >> 4) + 2 * k;
+                    const uint32_t dst = base + r * 128 + ((((q >> 1) ^ r) & 7) << 4) + ((q & 1) << 3);
+                    if (t0 + r < kp.T)
+                        cp_async_8(dst, src + (size_t)r * rm.stride + col);
+                    else
+                        st_shared_zero8(dst);
+                }
             }
         }
-    }
-    const uint32_t gb = ptx::smem_u32(s.g);
+    } else {
+        const float* src = a.G + rm.base + (size_t)t0 * rm.stride;
+        const int q = lane & 15, col = 4 * q;
+        const uint32_t gb = ptx::smem_u32(s.g);
+        if (col < kp.d) {
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const int idx = lane + 32 * k, r = idx >> 4, q = idx & 15, col = 4 * q;
-        if (col >= kp.d) continue;
-        const uint32_t d = gb + (r * kDp + col) * 4;
-        if (t0 + r < kp.T)
-            cp_async_16(d, a.G + row_offset(kp, bh, t0 + r) + col);
-        else
-            st_zero16(d);
+            for (int k = 0; k < 8; ++k) {
+                const int r = (lane >> 4) + 2 * k;
+                const uint32_t dst = gb + (r * kDp + col) * 4;
+                if (t0 + r < kp.T)
+                    cp_async_16(dst, src + (size_t)r * rm.stride + col);
+                else
+                    st_zero16(dst);
+            }
+        }
     }
     cp_async_commit();
 }
 
-// Lanes (token i = lane & 15, channel half lane >> 4): S, then s1 = S/||p1||,
-// s2 = S/||p2|| into ws.rs.
-__device__ __forceinline__ void row_scalars(WarpSmem& ws, const Stage& s, float zscale, int lane) {
-    const int i = lane & 15, h = lane >> 4;
+// Warp w, lanes (token 4w + lane/8, channels 8*(lane%8) .. +7): S, then
+// s1 = S/||p1||, s2 = S/||p2|| into gs.rs.
+__device__ __forceinline__ void row_scalars(GroupSmem& gs, const Stage& s, float zscale, int warp, int lane) {
+    const int i = 4 * warp + (lane >> 3), col = 8 * (lane & 7);
+    const uint4 x = *reinterpret_cast<const uint4*>(s.p1 + swz(i, col));
+    const uint4 y = *reinterpret_cast<const uint4*>(s.p2 + swz(i, col));
+    const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
     float n1 = 0.f, n2 = 0.f, dt = 0.f;
 #pragma unroll
-    for (int c8 = 0; c8 < 4; ++c8) {
-        const int col = 32 * h + 8 * c8;
-        const uint4 x = *reinterpret_cast<const uint4*>(s.p1 + swz(i, col));
-        const uint4 y = *reinterpret_cast<const uint4*>(s.p2 + swz(i, col));
-        const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            const float a0 = lo_f(xs[w]), a1 = hi_f(xs[w]), b0 = lo_f(ys[w]), b1 = hi_f(ys[w]);
-            n1 = fmaf(a0, a0, fmaf(a1, a1, n1));
-            n2 = fmaf(b0, b0, fmaf(b1, b1, n2));
-            dt = fmaf(a0, b0, fmaf(a1, b1, dt));
-        }
+    for (int w = 0; w < 4; ++w) {
+        const float a0 = lo_f(xs[w]), a1 = hi_f(xs[w]), b0 = lo_f(ys[w]), b1 = hi_f(ys[w]);
+        n1 = fmaf(a0, a0, fmaf(a1, a1, n1));
+        n2 = fmaf(b0, b0, fmaf(b1, b1, n2));
+        dt = fmaf(a0, b0, fmaf(a1, b1, dt));
     }
-    n1 += __shfl_xor_sync(0xffffffffu, n1, 16);
-    n2 += __shfl_xor_sync(0xffffffffu, n2, 16);
-    dt += __shfl_xor_sync(0xffffffffu, dt, 16);
-    const float S = 1.f / (1.f + __expf(-dt * zscale));
-    if (h == 0) ws.rs[i] = make_float2(n1 > 0.f ? S * rsqrtf(n1) : 0.f, n2 > 0.f ? S * rsqrtf(n2) : 0.f);
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+        n1 += __shfl_xor_sync(0xffffffffu, n1, o);
+        n2 += __shfl_xor_sync(0xffffffffu, n2, o);
+        dt += __shfl_xor_sync(0xffffffffu, dt, o);
+    }
+    if ((lane & 7) == 0) {
+        const float S = 1.f / (1.f + __expf(-dt * zscale));
+        gs.rs[i] = make_float2(n1 > 0.f ? S * rsqrtf(n1) : 0.f, n2 > 0.f ? S * rsqrtf(n2) : 0.f);
+    }
 }
 
-// Lane l owns channels c = 2l, 2l+1 of all 16 tokens: alpha (in place of g),
-// q, k (fp32), q . F and k . B (bf16 operands) and the chunk retention a = F_15.
-// kQ = false skips the query side (state passes).
-template <bool kQ>
-__device__ __forceinline__ void channel_pass(WarpSmem& ws, Stage& s, int d, int lane) {
+// Compacted row of key token i among the 8 keys of level bit b.
+__device__ __forceinline__ int key_row(int i, int b) { return ((i >> (b + 1)) << b) | (i & ((1 << b) - 1)); }
+
+// Channel pass.  Warp w owns the tokens 4w .. 4w+3 (a quarter of the chunk),
+// lane l the channels c = 2l, 2l+1, so every branch below is warp-uniform.
+// Phase A: alpha = exp(g) and the products inside the quarter, f (from the
+// quarter start to t) and b (from t+1 to the quarter end); the quarter totals go
+// to gs.tot.  Phase B (after a barrier) writes q . F, k . B, the level operands
+// and the chunk retention.  Every factor is a product of retentions over a run
+// of tokens lying between the two tokens of the pairs it serves, so all factors
+// are <= 1.  Levels (bit b of the token index): pairs (i, j), j < i, that first
+// differ in bit b meet at the boundary r = i with bits < b cleared: query factor
+// prod_{u=r..i} alpha_u, key factor prod_{u=j+1..r-1} alpha_u.
+struct Quarter {
+    float2 al[4], f[4], b[4];
+};
+
+__device__ __forceinline__ void channel_phase_a(Quarter& Q, GroupSmem& gs, const Stage& s, int d, int warp, int lane) {
     const int c = 2 * lane;
     const bool valid = c < d;
-    float2 F = make_float2(1.f, 1.f);
-    float2 al[kC], kk[kC];
+    float2 prod = make_float2(1.f, 1.f);
 #pragma unroll
-    for (int i = 0; i < kC; ++i) {
-        float2* gp = reinterpret_cast<float2*>(s.g + i * kDp + c);
-        const float2 g = *gp;
-        al[i] = valid ? make_float2(__expf(g.x), __expf(g.y)) : make_float2(1.f, 1.f);
-        *gp = al[i];
-        F = mul2(F, al[i]);
-        const float2 r = ws.rs[i];
-        const uint32_t w2 = *reinterpret_cast<const uint32_t*>(s.p2 + swz(i, c));
-        kk[i] = make_float2(lo_f(w2) * r.y, hi_f(w2) * r.y);
-        if (kQ) {
-            const uint32_t w1 = *reinterpret_cast<const uint32_t*>(s.p1 + swz(i, c));
-            const float2 q = make_float2(lo_f(w1) * r.x, hi_f(w1) * r.x);
-            *reinterpret_cast<float2*>(ws.qf + i * kDp + c) = q;
-            *reinterpret_cast<float2*>(ws.kf + i * kDp + c) = kk[i];
-            const float2 qF = mul2(q, F);
-            *reinterpret_cast<uint32_t*>(ws.qt + swz(i, c)) = pack2(qF.x, qF.y);
+    for (int r = 0; r < 4; ++r) {
+        const float2 g = *reinterpret_cast<const float2*>(s.g + (4 * warp + r) * kDp + c);
+        Q.al[r] = valid ? make_float2(__expf(g.x), __expf(g.y)) : make_float2(1.f, 1.f);
+        prod = mul2(prod, Q.al[r]);
+        Q.f[r] = prod;
+    }
+    float2 back = make_float2(1.f, 1.f);
+#pragma unroll
+    for (int r = 3; r >= 0; --r) {
+        Q.b[r] = back;
+        back = mul2(back, Q.al[r]);
+    }
+    *reinterpret_cast<float2*>(&gs.tot[warp][c]) = prod;
+}
+
+template <bool kQ>
+__device__ __forceinline__ void channel_phase_b(const Quarter& Q, GroupSmem& gs, const Stage& s, int warp, int lane) {
+    const int c = 2 * lane;
+    float2 P[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) P[k] = *reinterpret_cast<const float2*>(&gs.tot[k][c]);
+    float2 pre = make_float2(1.f, 1.f), suf = make_float2(1.f, 1.f);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        if (k < warp) pre = mul2(pre, P[k]);
+        if (k > warp) suf = mul2(suf, P[k]);
+    }
+    if (warp == 0) *reinterpret_cast<float2*>(gs.avec + c) = mul2(mul2(P[0], P[1]), mul2(P[2], P[3]));
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int i = 4 * warp + r;
+        const uint32_t sw = swz(i, c);
+        const float2 rr = gs.rs[i];
+        const uint32_t w2 = *reinterpret_cast<const uint32_t*>(s.p2 + sw);
+        const float2 k = make_float2(lo_f(w2) * rr.y, hi_f(w2) * rr.y);
+        const float2 kB = mul2(k, mul2(Q.b[r], suf));
+        *reinterpret_cast<uint32_t*>(gs.kb + sw) = pack2(kB.x, kB.y);
+        if (!kQ) continue;
+        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(s.p1 + sw);
+        const float2 q = make_float2(lo_f(w1) * rr.x, hi_f(w1) * rr.x);
+        const float2 qF = mul2(q, mul2(pre, Q.f[r]));
+        *reinterpret_cast<uint32_t*>(gs.qt + sw) = pack2(qF.x, qF.y);
+        float2 x;
+        // level bit 3 (boundary 8)
+        if (warp >= 2) {
+            x = mul2(q, warp == 3 ? mul2(P[2], Q.f[r]) : Q.f[r]);
+            *reinterpret_cast<uint32_t*>(gs.ql[0] + sw) = pack2(x.x, x.y);
+        } else {
+            x = mul2(k, warp == 0 ? mul2(Q.b[r], P[1]) : Q.b[r]);
+            *reinterpret_cast<uint32_t*>(gs.kl[0] + swz(key_row(i, 3), c)) = pack2(x.x, x.y);
+        }
+        // level bit 2 (boundary at the quarter start)
+        if (warp & 1) {
+            x = mul2(q, Q.f[r]);
+            *reinterpret_cast<uint32_t*>(gs.ql[1] + sw) = pack2(x.x, x.y);
+        } else {
+            x = mul2(k, Q.b[r]);
+            *reinterpret_cast<uint32_t*>(gs.kl[1] + swz(key_row(i, 2), c)) = pack2(x.x, x.y);
+        }
+        // level bit 1 (boundary at token 2 of the quarter)
+        if (r >= 2) {
+            x = mul2(q, r == 2 ? Q.al[2] : mul2(Q.al[2], Q.al[3]));
+            *reinterpret_cast<uint32_t*>(gs.ql[2] + sw) = pack2(x.x, x.y);
+        } else {
+            x = r == 0 ? mul2(k, Q.al[1]) : k;
+            *reinterpret_cast<uint32_t*>(gs.kl[2] + swz(key_row(i, 1), c)) = pack2(x.x, x.y);
+        }
+        // level bit 0 (adjacent pairs)
+        if (r & 1) {
+            x = mul2(q, Q.al[r]);
+            *reinterpret_cast<uint32_t*>(gs.ql[3] + sw) = pack2(x.x, x.y);
+        } else {
+            *reinterpret_cast<uint32_t*>(gs.kl[3] + swz(key_row(i, 0), c)) = pack2(k.x, k.y);
         }
     }
-    *reinterpret_cast<float2*>(ws.avec + c) = F;
-    float2 Bk = make_float2(1.f, 1.f);
+}
+
+// Warp w computes level bit b = 3 - w of the intra-chunk matrix: the 16 x 8
+// product of its query and key operands, and writes the entries (i, j) whose
+// first differing bit is b into gs.amat (zeroed beforehand).
+__device__ __forceinline__ void level_matrix(GroupSmem& gs, int warp, int lane) {
+    const int lvl = warp, b = 3 - warp;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int i = kC - 1; i >= 0; --i) {
-        const float2 kB = mul2(kk[i], Bk);
-        *reinterpret_cast<uint32_t*>(ws.kb + swz(i, c)) = pack2(kB.x, kB.y);
-        Bk = mul2(Bk, al[i]);
+    for (int ks = 0; ks < 4; ++ks) {
+        uint32_t af[4], bf[4];
+        ldsm4(af, addr_a(gs.ql[lvl], 16 * ks, lane));
+        // B from the [n][k] key tile (8 rows): matrices (k 0-7), (k 8-15) for n 0-7.
+        const int m = lane >> 3;
+        ldsm4(bf, ptx::smem_u32(gs.kl[lvl]) + swz(lane & 7, 16 * ks + 8 * (m & 1)));
+        mma16816(acc, af, bf[0], bf[1]);
+    }
+    const int g = lane >> 2, t = lane & 3;
+    __nv_bfloat16* A = reinterpret_cast<__nv_bfloat16*>(gs.amat);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const int i = g + 8 * (e >> 1), n = 2 * t + (e & 1);
+        const int j = ((n >> b) << (b + 1)) | (n & ((1 << b) - 1));
+        if (((i >> b) & 1) && (i >> (b + 1)) == (j >> (b + 1))) A[i * (kArow / 2) + j] = __float2bfloat16_rn(acc[e]);
     }
 }
 
-// Intra-chunk matrix A[i][j] = sum_c q_ic k_jc prod_{u=j+1..i} alpha_uc (j < i,
-// zero elsewhere) into ws.amat (bf16).  Lane = (key j = lane & 15, channel half
-// lane >> 4); W = k_j . prod alpha is carried down the rows.
-__device__ __forceinline__ void intra_matrix(WarpSmem& ws, const Stage& s, int lane) {
-    const int j = lane & 15, h = lane >> 4, c0 = 32 * h;
-    float2 W[16];
-#pragma unroll
-    for (int m = 0; m < 16; ++m) W[m] = *reinterpret_cast<const float2*>(ws.kf + j * kDp + c0 + 2 * m);
-    __nv_bfloat16* A = reinterpret_cast<__nv_bfloat16*>(ws.amat);
-    if (h == 0) A[j] = __float2bfloat16_rn(0.f);  // row 0
-#pragma unroll 1
-    for (int i = 1; i < kC; ++i) {
-        const float2* al = reinterpret_cast<const float2*>(s.g + i * kDp + c0);
-        const float2* q = reinterpret_cast<const float2*>(ws.qf + i * kDp + c0);
-        if (i > j) {
-#pragma unroll
-            for (int m = 0; m < 16; ++m) W[m] = mul2(W[m], al[m]);
-        }
-        float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int m = 0; m < 16; ++m) acc = fma2(W[m], q[m], acc);
-        float dot = acc.x + acc.y;
-        dot += __shfl_xor_sync(0xffffffffu, dot, 16);
-        if (h == 0) A[i * (kArow / 2) + j] = __float2bfloat16_rn(i > j ? dot : 0.f);
-    }
-}
-
-// ldmatrix lane addresses (see the PTX fragment layouts of m16n8k16).
-// A operand 16 x 16 from a row-major [m][k] swizzled tile at column k0.
-__device__ __forceinline__ uint32_t addr_a(const uint8_t* tile, int k0, int lane) {
-    const int m = lane >> 3, r = (lane & 7) + 8 * (m & 1), c = k0 + 8 * (m >> 1);
-    return ptx::smem_u32(tile) + swz(r, c);
-}
-// Operand fragments from a [k][n] (or [k][m]) tile with .trans: two 8-wide
-// column blocks n0, n0+8, rows k = 0..15.
-__device__ __forceinline__ uint32_t addr_bt(const uint8_t* tile, int n0, int lane) {
-    const int m = lane >> 3, r = (lane & 7) + 8 * (m & 1), c = n0 + 8 * (m >> 1);
-    return ptx::smem_u32(tile) + swz(r, c);
-}
-// Same for the A operand from a [k][m] tile (.trans): a0..a3 = (m0-7,k0-7),
-// (m8-15,k0-7), (m0-7,k8-15), (m8-15,k8-15).
-__device__ __forceinline__ uint32_t addr_at(const uint8_t* tile, int m0, int lane) {
-    const int m = lane >> 3, r = (lane & 7) + 8 * (m >> 1), c = m0 + 8 * (m & 1);
-    return ptx::smem_u32(tile) + swz(r, c);
-}
-
-// State C^T as mma accumulators: hT[mt][nt][r] = C^T[v][c], v = 16 mt + g (+8
-// for r >= 2), c = 8 nt + 2 t + (r & 1), g = lane / 4, t = lane % 4.
+// The warp's slice of the state C^T: rows v = 16w + g (+8 for r >= 2), columns
+// c = 8 nt + 2t + (r & 1) (mma accumulator layout, g = lane/4, t = lane%4).
 struct State {
-    float x[4][8][4];
+    float x[8][4];
 };
 
 __device__ __forceinline__ void state_zero(State& S) {
 #pragma unroll
-    for (int mt = 0; mt < 4; ++mt)
+    for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-            for (int r = 0; r < 4; ++r) S.x[mt][nt][r] = 0.f;
+        for (int r = 0; r < 4; ++r) S.x[nt][r] = 0.f;
 }
 // C [64][64] (row = key channel c, column = value channel v) <-> registers.
-__device__ __forceinline__ void state_load(State& S, const float* C, int lane) {
+__device__ __forceinline__ void state_load(State& S, const float* C, int warp, int lane) {
     const int g = lane >> 2, t = lane & 3;
 #pragma unroll
-    for (int mt = 0; mt < 4; ++mt)
+    for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int v = 16 * mt + g + 8 * (r >> 1), c = 8 * nt + 2 * t + (r & 1);
-                S.x[mt][nt][r] = C[c * kDp + v];
-            }
+        for (int r = 0; r < 4; ++r) {
+            const int v = 16 * warp + g + 8 * (r >> 1), c = 8 * nt + 2 * t + (r & 1);
+            S.x[nt][r] = C[c * kDp + v];
+        }
 }
-__device__ __forceinline__ void state_store(const State& S, float* C, int ld, int d, int lane) {
+__device__ __forceinline__ void state_store(const State& S, float* C, int ld, int d, int warp, int lane) {
     const int g = lane >> 2, t = lane & 3;
 #pragma unroll
-    for (int mt = 0; mt < 4; ++mt)
+    for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int v = 16 * mt + g + 8 * (r >> 1), c = 8 * nt + 2 * t + (r & 1);
-                if (v < d && c < d) C[c * ld + v] = S.x[mt][nt][r];
-            }
+        for (int r = 0; r < 4; ++r) {
+            const int v = 16 * warp + g + 8 * (r >> 1), c = 8 * nt + 2 * t + (r & 1);
+            if (v < d && c < d) C[c * ld + v] = S.x[nt][r];
+        }
 }
 
-// C <- Diag(a) C + (k . B)^T I~ for the chunk in ws / s.
-__device__ __forceinline__ void state_update(State& S, const WarpSmem& ws, const Stage& s, int lane) {
+// C <- Diag(a) C + (k . B)^T I~ on the warp's slice.
+__device__ __forceinline__ void state_update(State& S, const GroupSmem& gs, const Stage& s, int warp, int lane) {
     const int t = lane & 3;
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
-        const float2 a = *reinterpret_cast<const float2*>(ws.avec + 8 * nt + 2 * t);
-#pragma unroll
-        for (int mt = 0; mt < 4; ++mt) {
-            S.x[mt][nt][0] *= a.x;
-            S.x[mt][nt][1] *= a.y;
-            S.x[mt][nt][2] *= a.x;
-            S.x[mt][nt][3] *= a.y;
-        }
+        const float2 a = *reinterpret_cast<const float2*>(gs.avec + 8 * nt + 2 * t);
+        S.x[nt][0] *= a.x;
+        S.x[nt][1] *= a.y;
+        S.x[nt][2] *= a.x;
+        S.x[nt][3] *= a.y;
     }
-    uint32_t b[8][2];
+    uint32_t af[4];
+    ldsm4t(af, addr_at(s.v, 16 * warp, lane));
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
         uint32_t r[4];
-        ldsm4t(r, addr_bt(ws.kb, 16 * p, lane));
-        b[2 * p][0] = r[0];
-        b[2 * p][1] = r[1];
-        b[2 * p + 1][0] = r[2];
-        b[2 * p + 1][1] = r[3];
-    }
-#pragma unroll
-    for (int mt = 0; mt < 4; ++mt) {
-        uint32_t af[4];
-        ldsm4t(af, addr_at(s.v, 16 * mt, lane));
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt) mma16816(S.x[mt][nt], af, b[nt][0], b[nt][1]);
+        ldsm4t(r, addr_bt(gs.kb, 16 * p, lane));
+        mma16816(S.x[2 * p], af, r[0], r[1]);
+        mma16816(S.x[2 * p + 1], af, r[2], r[3]);
     }
 }
 
-// E = (q . F) C + A I~ as mma accumulators E[nv][r]: token g (+8), v = 8 nv + 2t (+1).
-__device__ __forceinline__ void chunk_output(float (&E)[8][4], const State& S, const WarpSmem& ws, const Stage& s,
-                                             int lane) {
+// E = (q . F) C + A I~ on the warp's value channels: E[s][r], token g (+8 for
+// r >= 2), v = 16w + 8s + 2t (+1).
+__device__ __forceinline__ void chunk_output(float (&E)[2][4], const State& S, const GroupSmem& gs, const Stage& s,
+                                             int warp, int lane) {
 #pragma unroll
-    for (int nv = 0; nv < 8; ++nv)
+    for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int r = 0; r < 4; ++r) E[nv][r] = 0.f;
+        for (int r = 0; r < 4; ++r) E[h][r] = 0.f;
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {
         uint32_t af[4];
-        ldsm4(af, addr_a(ws.qt, 16 * ks, lane));
+        ldsm4(af, addr_a(gs.qt, 16 * ks, lane));
 #pragma unroll
-        for (int nv = 0; nv < 8; ++nv) {
-            const int mt = nv >> 1, rr = (nv & 1) * 2;
-            const uint32_t b0 = pack2(S.x[mt][2 * ks][rr], S.x[mt][2 * ks][rr + 1]);
-            const uint32_t b1 = pack2(S.x[mt][2 * ks + 1][rr], S.x[mt][2 * ks + 1][rr + 1]);
-            mma16816(E[nv], af, b0, b1);
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t b0 = pack2(S.x[2 * ks][2 * h], S.x[2 * ks][2 * h + 1]);
+            const uint32_t b1 = pack2(S.x[2 * ks + 1][2 * h], S.x[2 * ks + 1][2 * h + 1]);
+            mma16816(E[h], af, b0, b1);
         }
     }
     uint32_t af[4];
     {
         const int m = lane >> 3, r = (lane & 7) + 8 * (m & 1), cb = 16 * (m >> 1);
-        ldsm4(af, ptx::smem_u32(ws.amat) + r * kArow + cb);
+        ldsm4(af, ptx::smem_u32(gs.amat) + r * kArow + cb);
     }
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-        uint32_t r[4];
-        ldsm4t(r, addr_bt(s.v, 16 * p, lane));
-        mma16816(E[2 * p], af, r[0], r[1]);
-        mma16816(E[2 * p + 1], af, r[2], r[3]);
-    }
+    uint32_t r[4];
+    ldsm4t(r, addr_bt(s.v, 16 * warp, lane));
+    mma16816(E[0], af, r[0], r[1]);
+    mma16816(E[1], af, r[2], r[3]);
 }
 
-__device__ __forceinline__ void zero_warp_smem(WarpSmem& ws, int lane) {
-    uint4* p = reinterpret_cast<uint4*>(&ws);
-    const int n = (int)(sizeof(WarpSmem) / 16);
-    for (int k = lane; k < n; k += 32) p[k] = make_uint4(0, 0, 0, 0);
-    __syncwarp();
+__device__ __forceinline__ void zero_group_smem(GroupSmem& gs) {
+    uint4* p = reinterpret_cast<uint4*>(&gs);
+    const int n = (int)(sizeof(GroupSmem) / 16);
+    for (int k = threadIdx.x; k < n; k += kThreads) p[k] = make_uint4(0, 0, 0, 0);
+    __syncthreads();
 }
 
 // ------------------------------------------------------------------- kernels
-// Work item w = bh * nseg + segment; one warp per item.
-template <bool kVec16>
-__global__ void __launch_bounds__(32 * kWarpsPerCta) linear_state_kernel(Args a) {
+// One CTA (4 warps) per work item bh * nseg + segment.
+template <bool kVec16, bool kOut>
+__device__ __forceinline__ void segment_pass(const Args& a) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
+    GroupSmem& gs = *reinterpret_cast<GroupSmem*>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    WarpSmem& ws = reinterpret_cast<WarpSmem*>(smem_raw)[warp];
-    const int64_t item = (int64_t)blockIdx.x * kWarpsPerCta + warp;
-    if (item >= a.kp.BH * a.nseg) return;
+    const int64_t item = blockIdx.x;
     const int64_t bh = item / a.nseg;
     const int seg = (int)(item - bh * a.nseg);
-    const int t_begin = seg * a.seg_len, t_end = min(a.kp.T, t_begin + a.seg_len);
-    const int nchunks = (t_end - t_begin + kC - 1) / kC;
-    zero_warp_smem(ws, lane);
-
-    State S;
-    state_zero(S);
-    float2 aseg = make_float2(1.f, 1.f);
-    load_chunk<kVec16>(ws.st[0], a, bh, t_begin, lane);
-    for (int n = 0; n < nchunks; ++n) {
-        Stage& s = ws.st[n & 1];
-        if (n + 1 < nchunks) {
-            load_chunk<kVec16>(ws.st[(n + 1) & 1], a, bh, t_begin + (n + 1) * kC, lane);
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
-        }
-        __syncwarp();
-        row_scalars(ws, s, a.zscale, lane);
-        __syncwarp();
-        channel_pass<false>(ws, s, a.kp.d, lane);
-        aseg = mul2(aseg, *reinterpret_cast<const float2*>(ws.avec + 2 * lane));
-        __syncwarp();
-        state_update(S, ws, s, lane);
-        __syncwarp();
-    }
-    float* H = a.hseg + (size_t)item * kDp * kDp;
-    state_store(S, H, kDp, kDp, lane);
-    *reinterpret_cast<float2*>(a.aseg + (size_t)item * kDp + 2 * lane) = aseg;
-}
-
-// One block per head: entering state of every segment (in place of its own
-// contribution) and the final state.
-__global__ void __launch_bounds__(256) linear_scan_kernel(float* hseg, const float* aseg, int nseg, float* state_out,
-                                                          int d) {
-    const int64_t bh = blockIdx.x;
-    const int c = threadIdx.x >> 2, v0 = (threadIdx.x & 3) * 16;
-    float h[16];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) h[k] = 0.f;
-    for (int s = 0; s < nseg; ++s) {
-        float4* p = reinterpret_cast<float4*>(hseg + ((size_t)(bh * nseg + s) * kDp + c) * kDp + v0);
-        const float al = aseg[(size_t)(bh * nseg + s) * kDp + c];
-        float4 dh[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) dh[k] = p[k];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) p[k] = make_float4(h[4 * k], h[4 * k + 1], h[4 * k + 2], h[4 * k + 3]);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            h[4 * k] = fmaf(al, h[4 * k], dh[k].x);
-            h[4 * k + 1] = fmaf(al, h[4 * k + 1], dh[k].y);
-            h[4 * k + 2] = fmaf(al, h[4 * k + 2], dh[k].z);
-            h[4 * k + 3] = fmaf(al, h[4 * k + 3], dh[k].w);
-        }
-    }
-    if (state_out != nullptr && c < d) {
-        float* o = state_out + ((size_t)bh * d + c) * d;
-#pragma unroll
-        for (int k = 0; k < 16; ++k)
-            if (v0 + k < d) o[v0 + k] = h[k];
-    }
-}
-
-template <bool kVec16>
-__global__ void __launch_bounds__(32 * kWarpsPerCta) linear_fwd_kernel(Args a) {
-    extern __shared__ __align__(128) uint8_t smem_raw[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    WarpSmem& ws = reinterpret_cast<WarpSmem*>(smem_raw)[warp];
-    const int64_t item = (int64_t)blockIdx.x * kWarpsPerCta + warp;
-    if (item >= a.kp.BH * a.nseg) return;
-    const int64_t bh = item / a.nseg;
-    const int seg = (int)(item - bh * a.nseg);
-    const int t_begin = seg * a.seg_len, t_end = min(a.kp.T, t_begin + a.seg_len);
-    const int nchunks = (t_end - t_begin + kC - 1) / kC;
     const KernelProblem& kp = a.kp;
-    zero_warp_smem(ws, lane);
+    const int t_begin = seg * a.seg_len, t_end = min(kp.T, t_begin + a.seg_len);
+    const int nchunks = (t_end - t_begin + kC - 1) / kC;
+    zero_group_smem(gs);
 
     State S;
-    if (a.nseg > 1)
-        state_load(S, a.hseg + (size_t)item * kDp * kDp, lane);
+    if (kOut && a.nseg > 1)
+        state_load(S, a.hseg + (size_t)item * kDp * kDp, warp, lane);
     else
         state_zero(S);
+    float2 aseg = make_float2(1.f, 1.f);
     const int g = lane >> 2, t = lane & 3;
-    load_chunk<kVec16>(ws.st[0], a, bh, t_begin, lane);
+    const RowMap rm = row_map(kp, bh);
+    load_chunk<kVec16>(gs.st[0], a, rm, t_begin, warp, lane);
     for (int n = 0; n < nchunks; ++n) {
-        Stage& s = ws.st[n & 1];
+        Stage& s = gs.st[n & 1];
         const int t0 = t_begin + n * kC;
-        if (n + 1 < nchunks) {
-            load_chunk<kVec16>(ws.st[(n + 1) & 1], a, bh, t0 + kC, lane);
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
+        cp_async_wait<0>();
+        __syncthreads();  // chunk n visible; every warp is done with chunk n-1
+        if (n + 1 < nchunks) load_chunk<kVec16>(gs.st[(n + 1) & 1], a, rm, t0 + kC, warp, lane);
+        row_scalars(gs, s, a.zscale, warp, lane);
+        Quarter Q;
+        channel_phase_a(Q, gs, s, kp.d, warp, lane);
+        if (kOut && warp == 0) {
+            uint4* A = reinterpret_cast<uint4*>(gs.amat);
+            for (int k = lane; k < (int)(sizeof(gs.amat) / 16); k += 32) A[k] = make_uint4(0, 0, 0, 0);
         }
-        __syncwarp();
-        row_scalars(ws, s, a.zscale, lane);
-        __syncwarp();
-        channel_pass<true>(ws, s, kp.d, lane);
-        __syncwarp();
-        intra_matrix(ws, s, lane);
-        __syncwarp();
-        float E[8][4];
-        chunk_output(E, S, ws, s, lane);
-        // Y = I~ + E
+        __syncthreads();
+        channel_phase_b<kOut>(Q, gs, s, warp, lane);
+        __syncthreads();
+        if (kOut) {
+            level_matrix(gs, warp, lane);
+            __syncthreads();
+            float E[2][4];
+            chunk_output(E, S, gs, s, warp, lane);
+            const size_t yrow0 = rm.base + (size_t)t0 * rm.stride;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const int r = g + 8 * half, tok = t0 + r;
-            if (tok < kp.T) {
-                __nv_bfloat16* yrow = a.Y + row_offset(kp, bh, tok);
+            for (int half = 0; half < 2; ++half) {
+                const int r = g + 8 * half;
+                if (t0 + r < kp.T) {
+                    __nv_bfloat16* yrow = a.Y + yrow0 + (size_t)r * rm.stride;
 #pragma unroll
-                for (int nv = 0; nv < 8; ++nv) {
-                    const int v = 8 * nv + 2 * t;
-                    if (v < kp.d) {
-                        const uint32_t iw = *reinterpret_cast<const uint32_t*>(s.v + swz(r, v));
-                        *reinterpret_cast<uint32_t*>(yrow + v) =
-                            pack2(lo_f(iw) + E[nv][2 * half], hi_f(iw) + E[nv][2 * half + 1]);
+                    for (int h = 0; h < 2; ++h) {
+                        const int v = 16 * warp + 8 * h + 2 * t;
+                        if (v < kp.d) {
+                            const uint32_t iw = *reinterpret_cast<const uint32_t*>(s.v + swz(r, v));
+                            *reinterpret_cast<uint32_t*>(yrow + v) =
+                                pack2(lo_f(iw) + E[h][2 * half], hi_f(iw) + E[h][2 * half + 1]);
+                        }
                     }
                 }
             }
+        } else if (warp == 0) {
+            aseg = mul2(aseg, *reinterpret_cast<const float2*>(gs.avec + 2 * lane));
         }
-        state_update(S, ws, s, lane);
-        __syncwarp();
+        state_update(S, gs, s, warp, lane);
     }
-    if (a.nseg == 1 && a.state_out != nullptr) state_store(S, a.state_out + (size_t)bh * kp.d * kp.d, kp.d, kp.d, lane);
+    if (kOut) {
+        if (a.nseg == 1 && a.state_out != nullptr)
+            state_store(S, a.state_out + (size_t)bh * kp.d * kp.d, kp.d, kp.d, warp, lane);
+    } else {
+        state_store(S, a.hseg + (size_t)item * kDp * kDp, kDp, kDp, warp, lane);
+        if (warp == 0) *reinterpret_cast<float2*>(a.aseg + (size_t)item * kDp + 2 * lane) = aseg;
+    }
+}
+
+template <bool kVec16>
+__global__ void __launch_bounds__(kThreads, 4) linear_state_kernel(Args a) {
+    segment_pass<kVec16, false>(a);
+}
+template <bool kVec16>
+__global__ void __launch_bounds__(kThreads, 4) linear_fwd_kernel(Args a) {
+    segment_pass<kVec16, true>(a);
+}
+
+// Entering state of every segment (in place of its own contribution) and the
+// final state.  One thread per state entry (c, v); 16 blocks per head.
+__global__ void __launch_bounds__(256) linear_scan_kernel(float* hseg, const float* aseg, int nseg, float* state_out,
+                                                          int d) {
+    const int64_t bh = blockIdx.x >> 4;
+    const int e = ((blockIdx.x & 15) << 8) | threadIdx.x, c = e >> 6, v = e & 63;
+    float* H = hseg + (size_t)bh * nseg * kDp * kDp + e;
+    const float* A = aseg + (size_t)bh * nseg * kDp + c;
+    float h = 0.f;
+    for (int s0 = 0; s0 < nseg; s0 += 16) {
+        float dh[16], al[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const bool ok = s0 + k < nseg;
+            dh[k] = ok ? H[(size_t)(s0 + k) * kDp * kDp] : 0.f;
+            al[k] = ok ? A[(size_t)(s0 + k) * kDp] : 1.f;
+        }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            if (s0 + k < nseg) H[(size_t)(s0 + k) * kDp * kDp] = h;
+            h = fmaf(al[k], h, dh[k]);
+        }
+    }
+    if (state_out != nullptr && c < d && v < d) state_out[((size_t)bh * d + c) * d + v] = h;
 }
 
 }  // namespace lin
 
 // ------------------------------------------------------------------ launchers
 int linear_segments(const KernelProblem& kp, int num_sms, int* seg_len) {
-    // Enough warps to fill the GPU about twice over; segments of at least 128 tokens.
-    const int64_t want = (int64_t)num_sms * 2 * 2 * lin::kWarpsPerCta;
+    // Enough groups for about four per SM; segments of at least 128 tokens.
+    const int64_t want = (int64_t)num_sms * 4;
     int nseg = 1;
     if (kp.BH < want) nseg = (int)((want + kp.BH - 1) / kp.BH);
     const int max_seg = (kp.T + 127) / 128;
@@ -550,8 +587,6 @@ int linear_segments(const KernelProblem& kp, int num_sms, int* seg_len) {
     *seg_len = len;
     return nseg;
 }
-
-size_t linear_smem_bytes() { return sizeof(lin::WarpSmem) * lin::kWarpsPerCta; }
 
 cudaError_t launch_linear_fwd(const KernelProblem& kp, const void* P1, const void* P2, const void* V, const float* G,
                               void* Y, float* state_out, float* ws, int num_sms, cudaStream_t s) {
@@ -567,7 +602,7 @@ cudaError_t launch_linear_fwd(const KernelProblem& kp, const void* P1, const voi
     a.nseg = linear_segments(kp, num_sms, &a.seg_len);
     a.hseg = ws;
     a.aseg = ws + (size_t)kp.BH * a.nseg * lin::kDp * lin::kDp;
-    const size_t smem = linear_smem_bytes();
+    const size_t smem = sizeof(lin::GroupSmem);
     const bool vec16 = (kp.d % 8) == 0;
     static bool attr_done = false;
     if (!attr_done) {
@@ -578,15 +613,14 @@ cudaError_t launch_linear_fwd(const KernelProblem& kp, const void* P1, const voi
                              (int)smem);
         attr_done = true;
     }
-    const int64_t items = kp.BH * a.nseg;
-    const unsigned grid = (unsigned)((items + lin::kWarpsPerCta - 1) / lin::kWarpsPerCta);
-    const dim3 block(32 * lin::kWarpsPerCta);
+    const unsigned grid = (unsigned)(kp.BH * a.nseg);
+    const dim3 block(lin::kThreads);
     if (a.nseg > 1) {
         if (vec16)
             lin::linear_state_kernel<true><<<grid, block, smem, s>>>(a);
         else
             lin::linear_state_kernel<false><<<grid, block, smem, s>>>(a);
-        lin::linear_scan_kernel<<<(unsigned)kp.BH, 256, 0, s>>>(a.hseg, a.aseg, a.nseg, state_out, kp.d);
+        lin::linear_scan_kernel<<<(unsigned)kp.BH * 16, 256, 0, s>>>(a.hseg, a.aseg, a.nseg, state_out, kp.d);
     }
     if (vec16)
         lin::linear_fwd_kernel<true><<<grid, block, smem, s>>>(a);
