@@ -239,15 +239,22 @@ relation_status_t relation_prologue_bwd(const relation_problem_t* p, const void*
  *   per head, float32 [B, H, d_h, d_h] (row = key channel, column = value
  *   channel).  1 to 3 kernel launches (segment state pass and scan only when
  *   B*H is too small to fill the GPU).
+ * relation_linear_bwd: from dY (bf16, like Y): dP1, dP2, dI (bf16) and dG
+ *   (float32), all fully overwritten (gradients of sum(Y * dY) with C_0 = 0).
+ *   2 to 6 kernel launches (the forward and reverse segment state passes and
+ *   scans only when B*H is too small to fill the GPU).
  * relation_linear_workspace_bytes: the float32 workspace both directions need
  *   (16-byte aligned, caller-owned, contents need not be preserved between
  *   calls); 0 on invalid arguments.
- * Outputs must not overlap inputs.
+ * Outputs must not overlap inputs or each other.
  */
 size_t relation_linear_workspace_bytes(const relation_problem_t* p);
 relation_status_t relation_linear_fwd(const relation_problem_t* p, const void* P1, const void* P2, const void* I,
                                       const float* G, void* Y, float* state, void* workspace,
                                       size_t workspace_bytes, void* stream);
+relation_status_t relation_linear_bwd(const relation_problem_t* p, const void* P1, const void* P2, const void* I,
+                                      const float* G, const void* dY, void* dP1, void* dP2, void* dI, float* dG,
+                                      void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Reads and clears the device status word of the current device.  Call after

@@ -103,6 +103,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.relation_linear_fwd.argtypes = [ctypes.POINTER(Problem), _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                             ctypes.c_size_t, _VP]
         lib.relation_linear_fwd.restype = ctypes.c_int
+        lib.relation_linear_bwd.argtypes = [ctypes.POINTER(Problem), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                            ctypes.c_size_t, _VP]
+        lib.relation_linear_bwd.restype = ctypes.c_int
         lib.relation_check_device_status.argtypes = []
         lib.relation_check_device_status.restype = ctypes.c_int
         lib.relation_last_launch_count.argtypes = []
@@ -243,6 +246,13 @@ def relation_linear_fwd(prob, P1, P2, I, G, Y, state, workspace, stream=None) ->
                                       _stream_ptr(stream)), "relation_linear_fwd")
 
 
+def relation_linear_bwd(prob, P1, P2, I, G, dY, dP1, dP2, dI, dG, workspace, stream=None) -> None:
+    _check(load().relation_linear_bwd(ctypes.byref(prob), _ptr(P1), _ptr(P2), _ptr(I), _ptr(G), _ptr(dY), _ptr(dP1),
+                                      _ptr(dP2), _ptr(dI), _ptr(dG), _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(), _stream_ptr(stream)),
+           "relation_linear_bwd")
+
+
 def relation_check_device_status() -> int:
     return int(load().relation_check_device_status())
 
@@ -287,6 +297,16 @@ def linear_fwd(P1, P2, I, G, tau_S: float, layout: int = RELATION_LAYOUT_BHTD, w
         workspace = linear_workspace(prob, P1.device)
     relation_linear_fwd(prob, P1, P2, I, G, Y, state, workspace, stream)
     return Y, state
+
+
+def linear_bwd(P1, P2, I, G, dY, tau_S: float, layout: int = RELATION_LAYOUT_BHTD, stream=None, workspace=None):
+    """Linear Relation backward; allocates and returns (dP1, dP2, dI, dG)."""
+    prob = problem_for(P1, tau_S, 0.0, True, layout)
+    dP1, dP2, dI, dG = torch.empty_like(P1), torch.empty_like(P2), torch.empty_like(I), torch.empty_like(G)
+    if workspace is None:
+        workspace = linear_workspace(prob, P1.device)
+    relation_linear_bwd(prob, P1, P2, I, G, dY, dP1, dP2, dI, dG, workspace, stream)
+    return dP1, dP2, dI, dG
 
 
 def decode(P1_new, P2_new, V_new, P2_cache, V_cache, positions, tau_S: float, lam: float, append: bool = True,

@@ -49,11 +49,16 @@ cudaError_t launch_pad_operands(const KernelProblem& kp, const void* const* src,
 cudaError_t launch_convert(const KernelProblem& kp, const float* src, int dq_w, void* dst, bool bf16, int num_sms,
                            cudaStream_t s);
 
-// Linear Relation (bf16 operands, fp32 log-retention G, d <= 64).  The
+// Linear Relation (bf16 operands, fp32 log-retention G, d <= 64).  The forward's
 // workspace holds BH * nseg * (64 * 64 + 64) floats for the segment states.
 int linear_segments(const KernelProblem& kp, int num_sms, int* seg_len);
 cudaError_t launch_linear_fwd(const KernelProblem& kp, const void* P1, const void* P2, const void* V, const float* G,
                               void* Y, float* state_out, float* ws, int num_sms, cudaStream_t s);
+// The backward's workspace adds BH * nseg * 64 * 64 floats (reverse segment states)
+// and BH * T floats (p^1 . dq per token).
+cudaError_t launch_linear_bwd(const KernelProblem& kp, const void* P1, const void* P2, const void* V, const float* G,
+                              const void* dY, void* dP1, void* dP2, void* dV, float* dG, float* ws, int num_sms,
+                              cudaStream_t s);
 
 // Tensor-core (tcgen05) bf16 path.
 struct TcLaunch {

@@ -126,6 +126,7 @@ struct Stage {
     float g[kC * kDp];  // fp32 rows of 64
 };
 struct GroupSmem {
+    static constexpr bool kNorms = false;
     Stage st[2];
     uint8_t qt[kC * 128];     // q . F   (F: retention from the chunk start to t)
     uint8_t kb[kC * 128];     // k . B   (B: retention from t to the chunk end)
@@ -217,7 +218,8 @@ __device__ __forceinline__ void load_chunk(Stage& s, const Args& a, const RowMap
 
 // Warp w, lanes (token 4w + lane/8, channels 8*(lane%8) .. +7): S, then
 // s1 = S/||p1||, s2 = S/||p2|| into gs.rs.
-__device__ __forceinline__ void row_scalars(GroupSmem& gs, const Stage& s, float zscale, int warp, int lane) {
+template <class GS, class ST>
+__device__ __forceinline__ void row_scalars(GS& gs, const ST& s, float zscale, int warp, int lane) {
     const int i = 4 * warp + (lane >> 3), col = 8 * (lane & 7);
     const uint4 x = *reinterpret_cast<const uint4*>(s.p1 + swz(i, col));
     const uint4 y = *reinterpret_cast<const uint4*>(s.p2 + swz(i, col));
@@ -238,7 +240,9 @@ __device__ __forceinline__ void row_scalars(GroupSmem& gs, const Stage& s, float
     }
     if ((lane & 7) == 0) {
         const float S = 1.f / (1.f + __expf(-dt * zscale));
-        gs.rs[i] = make_float2(n1 > 0.f ? S * rsqrtf(n1) : 0.f, n2 > 0.f ? S * rsqrtf(n2) : 0.f);
+        const float i1 = n1 > 0.f ? rsqrtf(n1) : 0.f, i2 = n2 > 0.f ? rsqrtf(n2) : 0.f;
+        gs.rs[i] = make_float2(S * i1, S * i2);
+        if constexpr (GS::kNorms) gs.rn[i] = make_float4(i1, i2, S, 0.f);
     }
 }
 
@@ -259,7 +263,8 @@ struct Quarter {
     float2 al[4], f[4], b[4];
 };
 
-__device__ __forceinline__ void channel_phase_a(Quarter& Q, GroupSmem& gs, const Stage& s, int d, int warp, int lane) {
+template <class GS, class ST>
+__device__ __forceinline__ void channel_phase_a(Quarter& Q, GS& gs, const ST& s, int d, int warp, int lane) {
     const int c = 2 * lane;
     const bool valid = c < d;
     float2 prod = make_float2(1.f, 1.f);
@@ -279,64 +284,81 @@ __device__ __forceinline__ void channel_phase_a(Quarter& Q, GroupSmem& gs, const
     *reinterpret_cast<float2*>(&gs.tot[warp][c]) = prod;
 }
 
-template <bool kQ>
-__device__ __forceinline__ void channel_phase_b(const Quarter& Q, GroupSmem& gs, const Stage& s, int warp, int lane) {
+// Products shared by every token of the quarter (read after the barrier).
+struct QuarterTotals {
+    float2 P[4], pre, suf;
+};
+template <class GS>
+__device__ __forceinline__ QuarterTotals quarter_totals(GS& gs, int warp, int lane) {
     const int c = 2 * lane;
-    float2 P[4];
+    QuarterTotals T;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) P[k] = *reinterpret_cast<const float2*>(&gs.tot[k][c]);
-    float2 pre = make_float2(1.f, 1.f), suf = make_float2(1.f, 1.f);
+    for (int k = 0; k < 4; ++k) T.P[k] = *reinterpret_cast<const float2*>(&gs.tot[k][c]);
+    T.pre = make_float2(1.f, 1.f);
+    T.suf = make_float2(1.f, 1.f);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        if (k < warp) pre = mul2(pre, P[k]);
-        if (k > warp) suf = mul2(suf, P[k]);
+        if (k < warp) T.pre = mul2(T.pre, T.P[k]);
+        if (k > warp) T.suf = mul2(T.suf, T.P[k]);
     }
-    if (warp == 0) *reinterpret_cast<float2*>(gs.avec + c) = mul2(mul2(P[0], P[1]), mul2(P[2], P[3]));
+    return T;
+}
+// Factor of token r of quarter `warp` at level bit b (query side / key side).
+__device__ __forceinline__ float2 query_factor(const Quarter& Q, const QuarterTotals& T, int warp, int r, int b) {
+    if (b == 3) return warp == 3 ? mul2(T.P[2], Q.f[r]) : Q.f[r];
+    if (b == 2) return Q.f[r];
+    if (b == 1) return r == 2 ? Q.al[2] : mul2(Q.al[2], Q.al[3]);
+    return Q.al[r];
+}
+__device__ __forceinline__ float2 key_factor(const Quarter& Q, const QuarterTotals& T, int warp, int r, int b) {
+    if (b == 3) return warp == 0 ? mul2(Q.b[r], T.P[1]) : Q.b[r];
+    if (b == 2) return Q.b[r];
+    if (b == 1) return r == 0 ? Q.al[1] : make_float2(1.f, 1.f);
+    return make_float2(1.f, 1.f);
+}
+__device__ __forceinline__ bool is_query(int i, int b) { return (i >> b) & 1; }
+
+// Writes the operands of the chunk: q . F (kQT), k . B (kKB), the level query
+// (kLQ) and key (kLK) operands; warp 0 writes the chunk retention.
+template <bool kQT, bool kKB, bool kLQ, bool kLK, class GS, class ST>
+__device__ __forceinline__ void channel_phase_b(const Quarter& Q, const QuarterTotals& T, GS& gs, const ST& s,
+                                                int warp, int lane) {
+    const int c = 2 * lane;
+    if (warp == 0) *reinterpret_cast<float2*>(gs.avec + c) = mul2(mul2(T.P[0], T.P[1]), mul2(T.P[2], T.P[3]));
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
         const int i = 4 * warp + r;
         const uint32_t sw = swz(i, c);
         const float2 rr = gs.rs[i];
-        const uint32_t w2 = *reinterpret_cast<const uint32_t*>(s.p2 + sw);
-        const float2 k = make_float2(lo_f(w2) * rr.y, hi_f(w2) * rr.y);
-        const float2 kB = mul2(k, mul2(Q.b[r], suf));
-        *reinterpret_cast<uint32_t*>(gs.kb + sw) = pack2(kB.x, kB.y);
-        if (!kQ) continue;
-        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(s.p1 + sw);
-        const float2 q = make_float2(lo_f(w1) * rr.x, hi_f(w1) * rr.x);
-        const float2 qF = mul2(q, mul2(pre, Q.f[r]));
-        *reinterpret_cast<uint32_t*>(gs.qt + sw) = pack2(qF.x, qF.y);
-        float2 x;
-        // level bit 3 (boundary 8)
-        if (warp >= 2) {
-            x = mul2(q, warp == 3 ? mul2(P[2], Q.f[r]) : Q.f[r]);
-            *reinterpret_cast<uint32_t*>(gs.ql[0] + sw) = pack2(x.x, x.y);
-        } else {
-            x = mul2(k, warp == 0 ? mul2(Q.b[r], P[1]) : Q.b[r]);
-            *reinterpret_cast<uint32_t*>(gs.kl[0] + swz(key_row(i, 3), c)) = pack2(x.x, x.y);
+        float2 k = make_float2(0.f, 0.f), q = make_float2(0.f, 0.f);
+        if (kKB || kLK) {
+            const uint32_t w2 = *reinterpret_cast<const uint32_t*>(s.p2 + sw);
+            k = make_float2(lo_f(w2) * rr.y, hi_f(w2) * rr.y);
         }
-        // level bit 2 (boundary at the quarter start)
-        if (warp & 1) {
-            x = mul2(q, Q.f[r]);
-            *reinterpret_cast<uint32_t*>(gs.ql[1] + sw) = pack2(x.x, x.y);
-        } else {
-            x = mul2(k, Q.b[r]);
-            *reinterpret_cast<uint32_t*>(gs.kl[1] + swz(key_row(i, 2), c)) = pack2(x.x, x.y);
+        if (kQT || kLQ) {
+            const uint32_t w1 = *reinterpret_cast<const uint32_t*>(s.p1 + sw);
+            q = make_float2(lo_f(w1) * rr.x, hi_f(w1) * rr.x);
         }
-        // level bit 1 (boundary at token 2 of the quarter)
-        if (r >= 2) {
-            x = mul2(q, r == 2 ? Q.al[2] : mul2(Q.al[2], Q.al[3]));
-            *reinterpret_cast<uint32_t*>(gs.ql[2] + sw) = pack2(x.x, x.y);
-        } else {
-            x = r == 0 ? mul2(k, Q.al[1]) : k;
-            *reinterpret_cast<uint32_t*>(gs.kl[2] + swz(key_row(i, 1), c)) = pack2(x.x, x.y);
+        if (kKB) {
+            const float2 x = mul2(k, mul2(Q.b[r], T.suf));
+            *reinterpret_cast<uint32_t*>(gs.kb + sw) = pack2(x.x, x.y);
         }
-        // level bit 0 (adjacent pairs)
-        if (r & 1) {
-            x = mul2(q, Q.al[r]);
-            *reinterpret_cast<uint32_t*>(gs.ql[3] + sw) = pack2(x.x, x.y);
-        } else {
-            *reinterpret_cast<uint32_t*>(gs.kl[3] + swz(key_row(i, 0), c)) = pack2(k.x, k.y);
+        if (kQT) {
+            const float2 x = mul2(q, mul2(T.pre, Q.f[r]));
+            *reinterpret_cast<uint32_t*>(gs.qt + sw) = pack2(x.x, x.y);
+        }
+#pragma unroll
+        for (int lvl = 0; lvl < 4; ++lvl) {
+            const int b = 3 - lvl;
+            if (is_query(i, b)) {
+                if (kLQ) {
+                    const float2 x = mul2(q, query_factor(Q, T, warp, r, b));
+                    *reinterpret_cast<uint32_t*>(gs.ql[lvl] + sw) = pack2(x.x, x.y);
+                }
+            } else if (kLK) {
+                const float2 x = mul2(k, key_factor(Q, T, warp, r, b));
+                *reinterpret_cast<uint32_t*>(gs.kl[lvl] + swz(key_row(i, b), c)) = pack2(x.x, x.y);
+            }
         }
     }
 }
@@ -344,7 +366,8 @@ __device__ __forceinline__ void channel_phase_b(const Quarter& Q, GroupSmem& gs,
 // Warp w computes level bit b = 3 - w of the intra-chunk matrix: the 16 x 8
 // product of its query and key operands, and writes the entries (i, j) whose
 // first differing bit is b into gs.amat (zeroed beforehand).
-__device__ __forceinline__ void level_matrix(GroupSmem& gs, int warp, int lane) {
+template <class GS>
+__device__ __forceinline__ void level_matrix(GS& gs, int warp, int lane) {
     const int lvl = warp, b = 3 - warp;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -401,7 +424,8 @@ __device__ __forceinline__ void state_store(const State& S, float* C, int ld, in
 }
 
 // C <- Diag(a) C + (k . B)^T I~ on the warp's slice.
-__device__ __forceinline__ void state_update(State& S, const GroupSmem& gs, const Stage& s, int warp, int lane) {
+template <class GS, class ST>
+__device__ __forceinline__ void state_update(State& S, const GS& gs, const ST& s, int warp, int lane) {
     const int t = lane & 3;
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
@@ -497,7 +521,10 @@ __device__ __forceinline__ void segment_pass(const Args& a) {
             for (int k = lane; k < (int)(sizeof(gs.amat) / 16); k += 32) A[k] = make_uint4(0, 0, 0, 0);
         }
         __syncthreads();
-        channel_phase_b<kOut>(Q, gs, s, warp, lane);
+        {
+            const QuarterTotals T = quarter_totals(gs, warp, lane);
+            channel_phase_b<kOut, true, kOut, kOut>(Q, T, gs, s, warp, lane);
+        }
         __syncthreads();
         if (kOut) {
             level_matrix(gs, warp, lane);
@@ -570,6 +597,625 @@ __global__ void __launch_bounds__(256) linear_scan_kernel(float* hseg, const flo
     if (state_out != nullptr && c < d && v < d) state_out[((size_t)bh * d + c) * d + v] = h;
 }
 
+// ================================================================= backward
+// With q = S p^1, k = S p^2, the chunk products give (dE = dY):
+//   dq_i = F_i . (C dE_i) + sum_{j<i} dA_ij k_j . P(j, i),   dA_ij = dE_i . I~_j,
+//   dk_j = B_j . (dC v_j) + sum_{i>j} dA_ij q_i . P(j, i),   dv_j = dC^T (k_j . B_j)
+//          + sum_{i>j} A_ij dE_i + dY_j,
+// with C the state entering the chunk (forward in time) and dC the gradient of the
+// state leaving it (backward in time: dC <- Diag(a) dC + (q . F)^T dE).  The
+// retention gradient uses dg_u = sum_{t >= u} (q_t . dq_t - k_t . dk_t), the sum
+// running to the end of the sequence; from a segment end on it equals the row
+// sums of C_end . dC_end.  Sweep A (forward) writes q . dq into dG as scratch,
+// the normalisation part of dP1 into dP1 and p^1 . dq per token; sweep B
+// (backward) finishes dG, dP1, dP2 and dI~.
+struct BStage {
+    uint8_t p1[kC * 128];
+    uint8_t p2[kC * 128];
+    uint8_t v[kC * 128];
+    uint8_t dy[kC * 128];
+    float g[kC * kDp];
+};
+struct BwdSmem {
+    static constexpr bool kNorms = true;
+    BStage st[2];
+    uint8_t qt[kC * 128];
+    uint8_t kb[kC * 128];
+    uint8_t ql[4][kC * 128];
+    uint8_t kl[4][8 * 128];
+    uint8_t amat[kC * kArow];
+    uint8_t dal[4][kC * kArow];  // dA on the pairs of each level, keys compacted (columns 8..15 zero)
+    float xq[kC * kDp];          // dQ~ (sweep A) or dK~ (sweep B), fp32 [row][channel]
+    float xl[4][kC * kDp];       // per level: dQ_L [token][c] (sweep A) or dK_L [key row][c] (sweep B)
+    float2 rs[kC];               // (S / ||p1||, S / ||p2||)
+    float4 rn[kC];               // (1 / ||p1||, 1 / ||p2||, S, -)
+    float avec[kDp];
+    float tot[4][kDp];
+    float zt[4][kDp];   // quarter sums of q . dq - k . dk
+    float bnd[kDp];     // row sums of C_end . dC_end at the segment end
+};
+
+struct BArgs {
+    const __nv_bfloat16* P1;
+    const __nv_bfloat16* P2;
+    const __nv_bfloat16* V;
+    const float* G;
+    const __nv_bfloat16* dY;
+    __nv_bfloat16* dP1;
+    __nv_bfloat16* dP2;
+    __nv_bfloat16* dV;
+    float* dG;
+    float* hseg;   // entering states of the segments (after the forward scan)
+    float* aseg;   // retention over each segment
+    float* dcseg;  // gradient of the state at each segment end (after the reverse scan)
+    float* pdq;    // [BH, T]: p^1 . dq per token
+    KernelProblem kp;
+    float zscale;
+    int nseg;
+    int seg_len;
+};
+
+// Copies of chunk rows t0..t0+15: warps 0-2 take P1, P2, I~; warp 3 takes G and dY.
+template <bool kVec16>
+__device__ __forceinline__ void copy_bf16_rows(uint8_t* tile, const __nv_bfloat16* src, const RowMap& rm, int t0,
+                                               int T, int d, int lane) {
+    const uint32_t base = ptx::smem_u32(tile);
+    if (kVec16) {
+        const int q = lane & 7, col = 8 * q;
+        if (col < d) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int r = (lane >> 3) + 4 * k;
+                const uint32_t dst = base + r * 128 + (((q ^ r) & 7) << 4);
+                if (t0 + r < T)
+                    cp_async_16(dst, src + (size_t)r * rm.stride + col);
+                else
+                    st_zero16(dst);
+            }
+        }
+    } else {
+        const int q = lane & 15, col = 4 * q;
+        if (col < d) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int r = (lane >> 4) + 2 * k;
+                const uint32_t dst = base + r * 128 + ((((q >> 1) ^ r) & 7) << 4) + ((q & 1) << 3);
+                if (t0 + r < T)
+                    cp_async_8(dst, src + (size_t)r * rm.stride + col);
+                else
+                    st_shared_zero8(dst);
+            }
+        }
+    }
+}
+template <bool kVec16>
+__device__ __forceinline__ void load_chunk_b(BStage& s, const BArgs& a, const RowMap& rm, int t0, int warp, int lane,
+                                             bool need_v) {
+    const KernelProblem& kp = a.kp;
+    const size_t off = rm.base + (size_t)t0 * rm.stride;
+    if (warp == 0) copy_bf16_rows<kVec16>(s.p1, a.P1 + off, rm, t0, kp.T, kp.d, lane);
+    if (warp == 1) copy_bf16_rows<kVec16>(s.p2, a.P2 + off, rm, t0, kp.T, kp.d, lane);
+    if (warp == 2) {
+        if (need_v) copy_bf16_rows<kVec16>(s.v, a.V + off, rm, t0, kp.T, kp.d, lane);
+        copy_bf16_rows<kVec16>(s.dy, a.dY + off, rm, t0, kp.T, kp.d, lane);
+    }
+    if (warp == 3) {
+        const float* src = a.G + off;
+        const int q = lane & 15, col = 4 * q;
+        const uint32_t gb = ptx::smem_u32(s.g);
+        if (col < kp.d) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int r = (lane >> 4) + 2 * k;
+                const uint32_t dst = gb + (r * kDp + col) * 4;
+                if (t0 + r < kp.T)
+                    cp_async_16(dst, src + (size_t)r * rm.stride + col);
+                else
+                    st_zero16(dst);
+            }
+        }
+    }
+    cp_async_commit();
+}
+
+// B fragments of two 8-row blocks n0.., n0+8.. from an [n][k] tile (no .trans):
+// r0 = b0 (n 0-7), r1 = b1 (n 0-7), r2 = b0 (n 8-15), r3 = b1 (n 8-15).
+__device__ __forceinline__ uint32_t addr_b(const uint8_t* tile, int k0, int lane) {
+    const int m = lane >> 3, r = (lane & 7) + 8 * (m >> 1), c = k0 + 8 * (m & 1);
+    return ptx::smem_u32(tile) + swz(r, c);
+}
+// A operand from a [k][m] 16 x 16 tile with 48-byte rows (.trans).
+__device__ __forceinline__ uint32_t addr_at48(const uint8_t* tile, int lane) {
+    const int m = lane >> 3, r = (lane & 7) + 8 * (m >> 1), c = 8 * (m & 1);
+    return ptx::smem_u32(tile) + r * kArow + 2 * c;
+}
+// A operand from a row-major [m][k] 16 x 16 tile with 48-byte rows.
+__device__ __forceinline__ uint32_t addr_a48(const uint8_t* tile, int lane) {
+    const int m = lane >> 3, r = (lane & 7) + 8 * (m & 1), c = 8 * (m >> 1);
+    return ptx::smem_u32(tile) + r * kArow + 2 * c;
+}
+__device__ __forceinline__ void ldsm2t(uint32_t& r0, uint32_t& r1, uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+
+// dA = dE I~^T (16 x 16) and the level-w tile of it (keys compacted, zero elsewhere).
+__device__ __forceinline__ void level_dA(BwdSmem& gs, const BStage& s, int warp, int lane) {
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+        uint32_t af[4], bf[4];
+        ldsm4(af, addr_a(s.dy, 16 * ks, lane));
+        ldsm4(bf, addr_b(s.v, 16 * ks, lane));
+        mma16816(acc[0], af, bf[0], bf[1]);
+        mma16816(acc[1], af, bf[2], bf[3]);
+    }
+    uint8_t* tile = gs.dal[warp];
+    {
+        uint4* z = reinterpret_cast<uint4*>(tile);
+        for (int k = lane; k < (int)(kC * kArow / 16); k += 32) z[k] = make_uint4(0, 0, 0, 0);
+    }
+    __syncwarp();
+    const int b = 3 - warp, g = lane >> 2, t = lane & 3;
+    __nv_bfloat16* D = reinterpret_cast<__nv_bfloat16*>(tile);
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int i = g + 8 * (e >> 1), j = 8 * h + 2 * t + (e & 1);
+            if (is_query(i, b) && !is_query(j, b) && (i >> (b + 1)) == (j >> (b + 1)))
+                D[i * (kArow / 2) + key_row(j, b)] = __float2bfloat16_rn(acc[h][e]);
+        }
+}
+
+// ---- state passes of the backward (segment contributions of the reverse state)
+template <bool kVec16>
+__global__ void __launch_bounds__(kThreads, 3) linear_bstate_kernel(BArgs a) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    BwdSmem& gs = *reinterpret_cast<BwdSmem*>(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t item = blockIdx.x, bh = item / a.nseg;
+    const int seg = (int)(item - bh * a.nseg);
+    const KernelProblem& kp = a.kp;
+    const int t_begin = seg * a.seg_len, t_end = min(kp.T, t_begin + a.seg_len);
+    const int nchunks = (t_end - t_begin + kC - 1) / kC;
+    {
+        uint4* p = reinterpret_cast<uint4*>(&gs);
+        for (int k = threadIdx.x; k < (int)(sizeof(BwdSmem) / 16); k += kThreads) p[k] = make_uint4(0, 0, 0, 0);
+        __syncthreads();
+    }
+    State D;  // dC rows c = 16w + g (+8), columns v
+    state_zero(D);
+    const RowMap rm = row_map(kp, bh);
+    load_chunk_b<kVec16>(gs.st[(nchunks - 1) & 1], a, rm, t_begin + (nchunks - 1) * kC, warp, lane, false);
+    for (int n = nchunks - 1; n >= 0; --n) {
+        BStage& s = gs.st[n & 1];
+        cp_async_wait<0>();
+        __syncthreads();
+        if (n > 0) load_chunk_b<kVec16>(gs.st[(n - 1) & 1], a, rm, t_begin + (n - 1) * kC, warp, lane, false);
+        row_scalars(gs, s, a.zscale, warp, lane);
+        Quarter Q;
+        channel_phase_a(Q, gs, s, kp.d, warp, lane);
+        __syncthreads();
+        {
+            const QuarterTotals T = quarter_totals(gs, warp, lane);
+            channel_phase_b<true, false, false, false>(Q, T, gs, s, warp, lane);
+        }
+        __syncthreads();
+        // dC <- Diag(a) dC + (q . F)^T dE on rows c of this warp
+        const int g = lane >> 2;
+        const float a0 = gs.avec[16 * warp + g], a1 = gs.avec[16 * warp + 8 + g];
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+            D.x[nt][0] *= a0;
+            D.x[nt][1] *= a0;
+            D.x[nt][2] *= a1;
+            D.x[nt][3] *= a1;
+        }
+        uint32_t af[4];
+        ldsm4t(af, addr_at(gs.qt, 16 * warp, lane));
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            uint32_t r[4];
+            ldsm4t(r, addr_bt(s.dy, 16 * p, lane));
+            mma16816(D.x[2 * p], af, r[0], r[1]);
+            mma16816(D.x[2 * p + 1], af, r[2], r[3]);
+        }
+    }
+    // store rows c of dC as [c][v]
+    const int g = lane >> 2, t = lane & 3;
+    float* out = a.dcseg + (size_t)item * kDp * kDp;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) out[(16 * warp + g + 8 * (r >> 1)) * kDp + 8 * nt + 2 * t + (r & 1)] = D.x[nt][r];
+}
+
+// Gradient of the state at every segment end (in place of the segment's own
+// contribution); zero after the last segment.
+__global__ void __launch_bounds__(256) linear_bscan_kernel(float* dcseg, const float* aseg, int nseg) {
+    const int64_t bh = blockIdx.x >> 4;
+    const int e = ((blockIdx.x & 15) << 8) | threadIdx.x, c = e >> 6;
+    float* H = dcseg + (size_t)bh * nseg * kDp * kDp + e;
+    const float* A = aseg + (size_t)bh * nseg * kDp + c;
+    float h = 0.f;
+    for (int s1 = nseg - 1; s1 >= 0; s1 -= 16) {
+        float dh[16], al[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const bool ok = s1 - k >= 0;
+            dh[k] = ok ? H[(size_t)(s1 - k) * kDp * kDp] : 0.f;
+            al[k] = ok ? A[(size_t)(s1 - k) * kDp] : 1.f;
+        }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            if (s1 - k >= 0) H[(size_t)(s1 - k) * kDp * kDp] = h;
+            h = fmaf(al[k], h, dh[k]);
+        }
+    }
+}
+
+// ---- sweep A: forward in time, dq
+template <bool kVec16>
+__global__ void __launch_bounds__(kThreads, 3) linear_bwd_a_kernel(BArgs a) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    BwdSmem& gs = *reinterpret_cast<BwdSmem*>(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t item = blockIdx.x, bh = item / a.nseg;
+    const int seg = (int)(item - bh * a.nseg);
+    const KernelProblem& kp = a.kp;
+    const int t_begin = seg * a.seg_len, t_end = min(kp.T, t_begin + a.seg_len);
+    const int nchunks = (t_end - t_begin + kC - 1) / kC;
+    {
+        uint4* p = reinterpret_cast<uint4*>(&gs);
+        for (int k = threadIdx.x; k < (int)(sizeof(BwdSmem) / 16); k += kThreads) p[k] = make_uint4(0, 0, 0, 0);
+        __syncthreads();
+    }
+    const int g = lane >> 2, t = lane & 3, c = 2 * lane;
+    // Entering state C, rows c = 16w + g (+8), columns v.
+    State H;
+    if (a.nseg > 1) {
+        const float* src = a.hseg + (size_t)item * kDp * kDp;
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                H.x[nt][r] = src[(16 * warp + g + 8 * (r >> 1)) * kDp + 8 * nt + 2 * t + (r & 1)];
+    } else {
+        state_zero(H);
+    }
+    const RowMap rm = row_map(kp, bh);
+    load_chunk_b<kVec16>(gs.st[0], a, rm, t_begin, warp, lane, true);
+    for (int n = 0; n < nchunks; ++n) {
+        BStage& s = gs.st[n & 1];
+        const int t0 = t_begin + n * kC;
+        cp_async_wait<0>();
+        __syncthreads();  // B1
+        if (n + 1 < nchunks) load_chunk_b<kVec16>(gs.st[(n + 1) & 1], a, rm, t0 + kC, warp, lane, true);
+        row_scalars(gs, s, a.zscale, warp, lane);
+        Quarter Q;
+        channel_phase_a(Q, gs, s, kp.d, warp, lane);
+        __syncthreads();  // B2
+        const QuarterTotals T = quarter_totals(gs, warp, lane);
+        channel_phase_b<false, true, false, true>(Q, T, gs, s, warp, lane);
+        level_dA(gs, s, warp, lane);
+        __syncthreads();  // B3
+        {
+            // dQ~ = dE C^T and dQ_L = dA_L K_L on channels [16w, 16w+16)
+            float dq[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                uint32_t af[4];
+                ldsm4(af, addr_a(s.dy, 16 * ks, lane));
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t b0 = pack2(H.x[2 * ks][2 * h], H.x[2 * ks][2 * h + 1]);
+                    const uint32_t b1 = pack2(H.x[2 * ks + 1][2 * h], H.x[2 * ks + 1][2 * h + 1]);
+                    mma16816(dq[h], af, b0, b1);
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int col = 16 * warp + 8 * h + 2 * t;
+                *reinterpret_cast<float2*>(gs.xq + g * kDp + col) = make_float2(dq[h][0], dq[h][1]);
+                *reinterpret_cast<float2*>(gs.xq + (g + 8) * kDp + col) = make_float2(dq[h][2], dq[h][3]);
+            }
+#pragma unroll
+            for (int lvl = 0; lvl < 4; ++lvl) {
+                uint32_t af[4], b0a, b0b;
+                ldsm4(af, addr_a48(gs.dal[lvl], lane));
+                ldsm2t(b0a, b0b, ptx::smem_u32(gs.kl[lvl]) + swz(lane & 7, 16 * warp + 8 * ((lane >> 3) & 1)));
+                float o[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                mma16816(o[0], af, b0a, 0u);
+                mma16816(o[1], af, b0b, 0u);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int col = 16 * warp + 8 * h + 2 * t;
+                    *reinterpret_cast<float2*>(gs.xl[lvl] + g * kDp + col) = make_float2(o[h][0], o[h][1]);
+                    *reinterpret_cast<float2*>(gs.xl[lvl] + (g + 8) * kDp + col) = make_float2(o[h][2], o[h][3]);
+                }
+            }
+            // C <- Diag(a) C + (k . B)^T I~ on rows c of this warp
+            const float a0 = gs.avec[16 * warp + g], a1 = gs.avec[16 * warp + 8 + g];
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) {
+                H.x[nt][0] *= a0;
+                H.x[nt][1] *= a0;
+                H.x[nt][2] *= a1;
+                H.x[nt][3] *= a1;
+            }
+            uint32_t af[4];
+            ldsm4t(af, addr_at(gs.kb, 16 * warp, lane));
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                uint32_t r[4];
+                ldsm4t(r, addr_bt(s.v, 16 * p, lane));
+                mma16816(H.x[2 * p], af, r[0], r[1]);
+                mma16816(H.x[2 * p + 1], af, r[2], r[3]);
+            }
+        }
+        __syncthreads();  // B4
+        // Channel layout: warp = token quarter, lane = channels c, c+1.
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int i = 4 * warp + r, tok = t0 + i;
+            float2 dq = mul2(mul2(T.pre, Q.f[r]), *reinterpret_cast<const float2*>(gs.xq + i * kDp + c));
+#pragma unroll
+            for (int lvl = 0; lvl < 4; ++lvl) {
+                const int b = 3 - lvl;
+                if (is_query(i, b))
+                    dq = fma2(query_factor(Q, T, warp, r, b), *reinterpret_cast<const float2*>(gs.xl[lvl] + i * kDp + c),
+                              dq);
+            }
+            const float4 rn = gs.rn[i];
+            const float s1 = gs.rs[i].x;
+            const uint32_t w1 = *reinterpret_cast<const uint32_t*>(s.p1 + swz(i, c));
+            const float2 p1 = make_float2(lo_f(w1), hi_f(w1));
+            const float2 ph = make_float2(p1.x * rn.x, p1.y * rn.x);
+            float pd = ph.x * dq.x + ph.y * dq.y;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) pd += __shfl_xor_sync(0xffffffffu, pd, o);
+            if (tok < kp.T) {
+                const size_t off = rm.base + (size_t)tok * rm.stride;
+                if (c < kp.d) {
+                    const float2 q = make_float2(p1.x * s1, p1.y * s1);
+                    *reinterpret_cast<float2*>(a.dG + off + c) = mul2(q, dq);
+                    *reinterpret_cast<uint32_t*>(a.dP1 + off + c) =
+                        pack2(s1 * (dq.x - ph.x * pd), s1 * (dq.y - ph.y * pd));
+                }
+                if (lane == 0) a.pdq[(size_t)bh * kp.T + tok] = pd;
+            }
+        }
+    }
+}
+
+// ---- sweep B: backward in time, dk, dv and the outputs
+template <bool kVec16>
+__global__ void __launch_bounds__(kThreads, 3) linear_bwd_b_kernel(BArgs a) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    BwdSmem& gs = *reinterpret_cast<BwdSmem*>(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t item = blockIdx.x, bh = item / a.nseg;
+    const int seg = (int)(item - bh * a.nseg);
+    const KernelProblem& kp = a.kp;
+    const int t_begin = seg * a.seg_len, t_end = min(kp.T, t_begin + a.seg_len);
+    const int nchunks = (t_end - t_begin + kC - 1) / kC;
+    {
+        uint4* p = reinterpret_cast<uint4*>(&gs);
+        for (int k = threadIdx.x; k < (int)(sizeof(BwdSmem) / 16); k += kThreads) p[k] = make_uint4(0, 0, 0, 0);
+        __syncthreads();
+    }
+    const int g = lane >> 2, t = lane & 3, c = 2 * lane;
+    // Gradient of the state leaving the segment: DC rows c = 16w + g (+8), columns v;
+    // DT the same matrix with rows v = 16w + g (+8), columns c.
+    State DC, DT;
+    const bool has_end = a.nseg > 1 && seg + 1 < a.nseg;
+    if (has_end) {
+        const float* src = a.dcseg + (size_t)item * kDp * kDp;
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int rr = 16 * warp + g + 8 * (r >> 1), cc = 8 * nt + 2 * t + (r & 1);
+                DC.x[nt][r] = src[rr * kDp + cc];
+                DT.x[nt][r] = src[cc * kDp + rr];
+            }
+        // bnd_c = sum_v C_end[c][v] dC_end[c][v], C_end = entering state of the next segment
+        const float* hn = a.hseg + (size_t)(item + 1) * kDp * kDp;
+        const int cc = threadIdx.x >> 1, v0 = (threadIdx.x & 1) * 32;
+        float acc = 0.f;
+        for (int v = 0; v < 32; ++v) acc = fmaf(hn[cc * kDp + v0 + v], src[cc * kDp + v0 + v], acc);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+        if ((threadIdx.x & 1) == 0) gs.bnd[cc] = acc;
+    } else {
+        state_zero(DC);
+        state_zero(DT);
+    }
+    __syncthreads();
+    float2 carry = *reinterpret_cast<const float2*>(gs.bnd + c);  // sum of z over the later tokens (+ boundary)
+    const RowMap rm = row_map(kp, bh);
+    load_chunk_b<kVec16>(gs.st[(nchunks - 1) & 1], a, rm, t_begin + (nchunks - 1) * kC, warp, lane, true);
+    for (int n = nchunks - 1; n >= 0; --n) {
+        BStage& s = gs.st[n & 1];
+        const int t0 = t_begin + n * kC;
+        cp_async_wait<0>();
+        __syncthreads();  // B1
+        if (n > 0) load_chunk_b<kVec16>(gs.st[(n - 1) & 1], a, rm, t0 - kC, warp, lane, true);
+        row_scalars(gs, s, a.zscale, warp, lane);
+        Quarter Q;
+        channel_phase_a(Q, gs, s, kp.d, warp, lane);
+        if (warp == 0) {
+            uint4* A = reinterpret_cast<uint4*>(gs.amat);
+            for (int k = lane; k < (int)(sizeof(gs.amat) / 16); k += 32) A[k] = make_uint4(0, 0, 0, 0);
+        }
+        __syncthreads();  // B2
+        const QuarterTotals T = quarter_totals(gs, warp, lane);
+        channel_phase_b<true, true, true, true>(Q, T, gs, s, warp, lane);
+        __syncthreads();  // B3
+        level_matrix(gs, warp, lane);
+        level_dA(gs, s, warp, lane);
+        __syncthreads();  // B4
+        {
+            // dK~ = I~ dC^T on channels [16w, 16w+16)
+            float dk[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                uint32_t af[4];
+                ldsm4(af, addr_a(s.v, 16 * ks, lane));
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t b0 = pack2(DC.x[2 * ks][2 * h], DC.x[2 * ks][2 * h + 1]);
+                    const uint32_t b1 = pack2(DC.x[2 * ks + 1][2 * h], DC.x[2 * ks + 1][2 * h + 1]);
+                    mma16816(dk[h], af, b0, b1);
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int col = 16 * warp + 8 * h + 2 * t;
+                *reinterpret_cast<float2*>(gs.xq + g * kDp + col) = make_float2(dk[h][0], dk[h][1]);
+                *reinterpret_cast<float2*>(gs.xq + (g + 8) * kDp + col) = make_float2(dk[h][2], dk[h][3]);
+            }
+            // dK_L = dA_L^T Q_L (rows: compacted keys 0..7)
+#pragma unroll
+            for (int lvl = 0; lvl < 4; ++lvl) {
+                uint32_t af[4], r4[4];
+                ldsm4t(af, addr_at48(gs.dal[lvl], lane));
+                ldsm4t(r4, addr_bt(gs.ql[lvl], 16 * warp, lane));
+                float o[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                mma16816(o[0], af, r4[0], r4[1]);
+                mma16816(o[1], af, r4[2], r4[3]);
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    *reinterpret_cast<float2*>(gs.xl[lvl] + g * kDp + 16 * warp + 8 * h + 2 * t) =
+                        make_float2(o[h][0], o[h][1]);
+            }
+            // dI~ = (k . B) dC + A^T dE + dY on value channels [16w, 16w+16)
+            float dv[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                uint32_t af[4];
+                ldsm4(af, addr_a(gs.kb, 16 * ks, lane));
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t b0 = pack2(DT.x[2 * ks][2 * h], DT.x[2 * ks][2 * h + 1]);
+                    const uint32_t b1 = pack2(DT.x[2 * ks + 1][2 * h], DT.x[2 * ks + 1][2 * h + 1]);
+                    mma16816(dv[h], af, b0, b1);
+                }
+            }
+            {
+                uint32_t af[4], r4[4];
+                ldsm4t(af, addr_at48(gs.amat, lane));
+                ldsm4t(r4, addr_bt(s.dy, 16 * warp, lane));
+                mma16816(dv[0], af, r4[0], r4[1]);
+                mma16816(dv[1], af, r4[2], r4[3]);
+            }
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int r = g + 8 * half, tok = t0 + r;
+                if (tok < kp.T) {
+                    __nv_bfloat16* row = a.dV + rm.base + (size_t)tok * rm.stride;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int v = 16 * warp + 8 * h + 2 * t;
+                        if (v < kp.d) {
+                            const uint32_t yw = *reinterpret_cast<const uint32_t*>(s.dy + swz(r, v));
+                            *reinterpret_cast<uint32_t*>(row + v) =
+                                pack2(lo_f(yw) + dv[h][2 * half], hi_f(yw) + dv[h][2 * half + 1]);
+                        }
+                    }
+                }
+            }
+            // dC <- Diag(a) dC + (q . F)^T dE, in both layouts
+            const float a0 = gs.avec[16 * warp + g], a1 = gs.avec[16 * warp + 8 + g];
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) {
+                DC.x[nt][0] *= a0;
+                DC.x[nt][1] *= a0;
+                DC.x[nt][2] *= a1;
+                DC.x[nt][3] *= a1;
+                const float2 ac = *reinterpret_cast<const float2*>(gs.avec + 8 * nt + 2 * t);
+                DT.x[nt][0] *= ac.x;
+                DT.x[nt][1] *= ac.y;
+                DT.x[nt][2] *= ac.x;
+                DT.x[nt][3] *= ac.y;
+            }
+            uint32_t aq[4], ad[4];
+            ldsm4t(aq, addr_at(gs.qt, 16 * warp, lane));
+            ldsm4t(ad, addr_at(s.dy, 16 * warp, lane));
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                uint32_t r4[4];
+                ldsm4t(r4, addr_bt(s.dy, 16 * p, lane));
+                mma16816(DC.x[2 * p], aq, r4[0], r4[1]);
+                mma16816(DC.x[2 * p + 1], aq, r4[2], r4[3]);
+                ldsm4t(r4, addr_bt(gs.qt, 16 * p, lane));
+                mma16816(DT.x[2 * p], ad, r4[0], r4[1]);
+                mma16816(DT.x[2 * p + 1], ad, r4[2], r4[3]);
+            }
+        }
+        __syncthreads();  // B5
+        // Channel layout: dk, then z = q . dq - k . dk and its suffix sums.
+        float2 dkv[4], zs[4];
+        float2 zq = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int i = 4 * warp + r, tok = t0 + i;
+            float2 dk = mul2(mul2(Q.b[r], T.suf), *reinterpret_cast<const float2*>(gs.xq + i * kDp + c));
+#pragma unroll
+            for (int lvl = 0; lvl < 4; ++lvl) {
+                const int b = 3 - lvl;
+                if (!is_query(i, b))
+                    dk = fma2(key_factor(Q, T, warp, r, b),
+                              *reinterpret_cast<const float2*>(gs.xl[lvl] + key_row(i, b) * kDp + c), dk);
+            }
+            dkv[r] = dk;
+            const float s2 = gs.rs[i].y;
+            const uint32_t w2 = *reinterpret_cast<const uint32_t*>(s.p2 + swz(i, c));
+            const float2 k = make_float2(lo_f(w2) * s2, hi_f(w2) * s2);
+            float2 x = make_float2(0.f, 0.f);
+            if (tok < kp.T && c < kp.d) x = *reinterpret_cast<const float2*>(a.dG + rm.base + (size_t)tok * rm.stride + c);
+            zs[r] = make_float2(x.x - k.x * dk.x, x.y - k.y * dk.y);
+            zq = make_float2(zq.x + zs[r].x, zq.y + zs[r].y);
+        }
+        *reinterpret_cast<float2*>(&gs.zt[warp][c]) = zq;
+        __syncthreads();  // B6
+        float2 later = carry;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 zk = *reinterpret_cast<const float2*>(&gs.zt[k][c]);
+            if (k > warp) later = make_float2(later.x + zk.x, later.y + zk.y);
+            carry = make_float2(carry.x + zk.x, carry.y + zk.y);
+        }
+#pragma unroll
+        for (int r = 3; r >= 0; --r) {
+            const int i = 4 * warp + r, tok = t0 + i;
+            later = make_float2(later.x + zs[r].x, later.y + zs[r].y);
+            const float4 rn = gs.rn[i];
+            const float s2 = gs.rs[i].y;
+            const uint32_t w1 = *reinterpret_cast<const uint32_t*>(s.p1 + swz(i, c));
+            const uint32_t w2 = *reinterpret_cast<const uint32_t*>(s.p2 + swz(i, c));
+            const float2 p1 = make_float2(lo_f(w1), hi_f(w1)), p2 = make_float2(lo_f(w2), hi_f(w2));
+            const float2 ph = make_float2(p2.x * rn.y, p2.y * rn.y);
+            const float2 dk = dkv[r];
+            float pd = ph.x * dk.x + ph.y * dk.y;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) pd += __shfl_xor_sync(0xffffffffu, pd, o);
+            if (tok < kp.T) {
+                const size_t off = rm.base + (size_t)tok * rm.stride;
+                const float S = rn.z;
+                const float dz = (a.pdq[(size_t)bh * kp.T + tok] + pd) * S * (1.f - S) * a.zscale;
+                if (c < kp.d) {
+                    *reinterpret_cast<float2*>(a.dG + off + c) = later;
+                    const uint32_t pw = *reinterpret_cast<const uint32_t*>(a.dP1 + off + c);
+                    *reinterpret_cast<uint32_t*>(a.dP1 + off + c) =
+                        pack2(lo_f(pw) + dz * p2.x, hi_f(pw) + dz * p2.y);
+                    *reinterpret_cast<uint32_t*>(a.dP2 + off + c) =
+                        pack2(s2 * (dk.x - ph.x * pd) + dz * p1.x, s2 * (dk.y - ph.y * pd) + dz * p1.y);
+                }
+            }
+        }
+    }
+}
+
 }  // namespace lin
 
 // ------------------------------------------------------------------ launchers
@@ -626,6 +1272,81 @@ cudaError_t launch_linear_fwd(const KernelProblem& kp, const void* P1, const voi
         lin::linear_fwd_kernel<true><<<grid, block, smem, s>>>(a);
     else
         lin::linear_fwd_kernel<false><<<grid, block, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_linear_bwd(const KernelProblem& kp, const void* P1, const void* P2, const void* V, const float* G,
+                              const void* dY, void* dP1, void* dP2, void* dV, float* dG, float* ws, int num_sms,
+                              cudaStream_t s) {
+    lin::Args fa;
+    fa.P1 = static_cast<const __nv_bfloat16*>(P1);
+    fa.P2 = static_cast<const __nv_bfloat16*>(P2);
+    fa.V = static_cast<const __nv_bfloat16*>(V);
+    fa.G = G;
+    fa.Y = nullptr;
+    fa.state_out = nullptr;
+    fa.kp = kp;
+    fa.zscale = kp.inv_sqrt_d / kp.tau_S;
+    fa.nseg = linear_segments(kp, num_sms, &fa.seg_len);
+    const size_t per_seg = (size_t)kp.BH * fa.nseg;
+    fa.hseg = ws;
+    fa.aseg = ws + per_seg * lin::kDp * lin::kDp;
+    lin::BArgs b;
+    b.P1 = fa.P1;
+    b.P2 = fa.P2;
+    b.V = fa.V;
+    b.G = G;
+    b.dY = static_cast<const __nv_bfloat16*>(dY);
+    b.dP1 = static_cast<__nv_bfloat16*>(dP1);
+    b.dP2 = static_cast<__nv_bfloat16*>(dP2);
+    b.dV = static_cast<__nv_bfloat16*>(dV);
+    b.dG = dG;
+    b.hseg = fa.hseg;
+    b.aseg = fa.aseg;
+    b.dcseg = fa.aseg + per_seg * lin::kDp;
+    b.pdq = b.dcseg + per_seg * lin::kDp * lin::kDp;
+    b.kp = kp;
+    b.zscale = fa.zscale;
+    b.nseg = fa.nseg;
+    b.seg_len = fa.seg_len;
+    const size_t fsmem = sizeof(lin::GroupSmem), bsmem = sizeof(lin::BwdSmem);
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaFuncSetAttribute(lin::linear_state_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsmem);
+        cudaFuncSetAttribute(lin::linear_state_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)fsmem);
+        cudaFuncSetAttribute(lin::linear_bstate_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bsmem);
+        cudaFuncSetAttribute(lin::linear_bstate_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)bsmem);
+        cudaFuncSetAttribute(lin::linear_bwd_a_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bsmem);
+        cudaFuncSetAttribute(lin::linear_bwd_a_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bsmem);
+        cudaFuncSetAttribute(lin::linear_bwd_b_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bsmem);
+        cudaFuncSetAttribute(lin::linear_bwd_b_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bsmem);
+        attr_done = true;
+    }
+    const unsigned grid = (unsigned)per_seg;
+    const dim3 block(lin::kThreads);
+    const bool vec16 = (kp.d % 8) == 0;
+    if (fa.nseg > 1) {
+        if (vec16) {
+            lin::linear_state_kernel<true><<<grid, block, fsmem, s>>>(fa);
+        } else {
+            lin::linear_state_kernel<false><<<grid, block, fsmem, s>>>(fa);
+        }
+        lin::linear_scan_kernel<<<(unsigned)kp.BH * 16, 256, 0, s>>>(fa.hseg, fa.aseg, fa.nseg, nullptr, kp.d);
+        if (vec16)
+            lin::linear_bstate_kernel<true><<<grid, block, bsmem, s>>>(b);
+        else
+            lin::linear_bstate_kernel<false><<<grid, block, bsmem, s>>>(b);
+        lin::linear_bscan_kernel<<<(unsigned)kp.BH * 16, 256, 0, s>>>(b.dcseg, b.aseg, b.nseg);
+    }
+    if (vec16) {
+        lin::linear_bwd_a_kernel<true><<<grid, block, bsmem, s>>>(b);
+        lin::linear_bwd_b_kernel<true><<<grid, block, bsmem, s>>>(b);
+    } else {
+        lin::linear_bwd_a_kernel<false><<<grid, block, bsmem, s>>>(b);
+        lin::linear_bwd_b_kernel<false><<<grid, block, bsmem, s>>>(b);
+    }
     return cudaGetLastError();
 }
 

@@ -438,11 +438,15 @@ relation_status_t check_linear(const relation_problem_t* p) {
     if (p->d_h != 48 && p->d_h != 60 && p->d_h != 64) return RELATION_ERR_UNSUPPORTED;
     return RELATION_OK;
 }
-// Floats of the segment-state workspace of one direction.
-size_t linear_ws_floats(const relation_problem_t* p, int num_sms) {
+// Floats of the workspace: segment states and retentions (forward), plus the
+// reverse segment states and one float per token (backward).
+size_t linear_ws_floats(const relation_problem_t* p, int num_sms, bool backward) {
     int len = 0;
     const int nseg = linear_segments(kernel_problem(p), num_sms, &len);
-    return (size_t)p->B * (size_t)p->H * (size_t)nseg * (64 * 64 + 64);
+    const size_t bh = (size_t)p->B * (size_t)p->H;
+    size_t n = bh * (size_t)nseg * (64 * 64 + 64);
+    if (backward) n += bh * (size_t)nseg * 64 * 64 + bh * (size_t)p->T;
+    return n;
 }
 }  // namespace
 }  // namespace relation
@@ -451,7 +455,7 @@ size_t relation_linear_workspace_bytes(const relation_problem_t* p) {
     if (check_linear(p) != RELATION_OK) return 0;
     DeviceInfo di;
     if (device_info(&di) != RELATION_OK) return 0;
-    return linear_ws_floats(p, di.num_sms) * sizeof(float);
+    return linear_ws_floats(p, di.num_sms, true) * sizeof(float);
 }
 
 relation_status_t relation_linear_fwd(const relation_problem_t* p, const void* P1, const void* P2, const void* I,
@@ -465,7 +469,8 @@ relation_status_t relation_linear_fwd(const relation_problem_t* p, const void* P
         return RELATION_ERR_MISALIGNED;
     DeviceInfo di;
     if ((st = device_info(&di)) != RELATION_OK) return st;
-    if (workspace_bytes < linear_ws_floats(p, di.num_sms) * sizeof(float)) return RELATION_ERR_WORKSPACE_TOO_SMALL;
+    if (workspace_bytes < linear_ws_floats(p, di.num_sms, false) * sizeof(float))
+        return RELATION_ERR_WORKSPACE_TOO_SMALL;
     const size_t tb = tensor_bytes(p), gb = rows_of(p) * (size_t)p->d_h * sizeof(float);
     const size_t sb = (size_t)p->B * p->H * p->d_h * p->d_h * sizeof(float);
     const void* ins[] = {P1, P2, I};
@@ -481,6 +486,44 @@ relation_status_t relation_linear_fwd(const relation_problem_t* p, const void* P
     st = from_cuda(launch_linear_fwd(kp, P1, P2, I, G, Y, state, static_cast<float*>(workspace), di.num_sms,
                                      static_cast<cudaStream_t>(stream)));
     if (st == RELATION_OK) t_last_launches = nseg > 1 ? 3 : 1;
+    return st;
+}
+
+relation_status_t relation_linear_bwd(const relation_problem_t* p, const void* P1, const void* P2, const void* I,
+                                      const float* G, const void* dY, void* dP1, void* dP2, void* dI, float* dG,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+    relation_status_t st = check_linear(p);
+    if (st != RELATION_OK) return st;
+    const void* ins[] = {P1, P2, I, G, dY};
+    void* outs[] = {dP1, dP2, dI, dG};
+    for (const void* x : ins)
+        if (x == nullptr) return RELATION_ERR_INVALID_ARGUMENT;
+    for (const void* x : outs)
+        if (x == nullptr) return RELATION_ERR_INVALID_ARGUMENT;
+    if (workspace == nullptr) return RELATION_ERR_INVALID_ARGUMENT;
+    for (const void* x : ins)
+        if (!aligned16(x)) return RELATION_ERR_MISALIGNED;
+    for (const void* x : outs)
+        if (!aligned16(x)) return RELATION_ERR_MISALIGNED;
+    if (!aligned16(workspace)) return RELATION_ERR_MISALIGNED;
+    DeviceInfo di;
+    if ((st = device_info(&di)) != RELATION_OK) return st;
+    if (workspace_bytes < linear_ws_floats(p, di.num_sms, true) * sizeof(float))
+        return RELATION_ERR_WORKSPACE_TOO_SMALL;
+    const size_t tb = tensor_bytes(p), gb = rows_of(p) * (size_t)p->d_h * sizeof(float);
+    const size_t in_len[] = {tb, tb, tb, gb, tb}, out_len[] = {tb, tb, tb, gb};
+    for (int o = 0; o < 4; ++o) {
+        for (int i = 0; i < 5; ++i)
+            if (overlaps(outs[o], out_len[o], ins[i], in_len[i])) return RELATION_ERR_INVALID_ARGUMENT;
+        for (int o2 = o + 1; o2 < 4; ++o2)
+            if (overlaps(outs[o], out_len[o], outs[o2], out_len[o2])) return RELATION_ERR_INVALID_ARGUMENT;
+    }
+    const KernelProblem kp = kernel_problem(p);
+    int len = 0;
+    const int nseg = linear_segments(kp, di.num_sms, &len);
+    st = from_cuda(launch_linear_bwd(kp, P1, P2, I, G, dY, dP1, dP2, dI, dG, static_cast<float*>(workspace),
+                                     di.num_sms, static_cast<cudaStream_t>(stream)));
+    if (st == RELATION_OK) t_last_launches = nseg > 1 ? 6 : 2;
     return st;
 }
 

@@ -108,3 +108,49 @@ def test_linear_rejects_unsupported():
     with pytest.raises(rb.RelationError) as e:
         rb.linear_fwd(xf, xf, xf, xf, 1.0)
     assert e.value.code == 2
+
+
+# Backward tolerance: every gradient is a sum of products of bf16-rounded operands
+# (chunk operands, the bf16 inputs, the state as a bf16 tensor-core operand) with fp32
+# accumulation, rounded to bf16 once (dG: float32), and dP1 / dP2 pass through one
+# more bf16 rounding (the normalisation part stored, then the Self part added):
+#     max |g - g_ref| <= 2e-2 * max |g_ref|   for g in dP1, dP2, dI, dG.
+GTOL = 2e-2
+
+BWD_CASES = [
+    ("d64_ragged", 2, 3, 100, 64, BHTD, 1.0, 2.0),
+    ("d64_segments", 1, 2, 700, 64, BHTD, 1.0, 1.0),
+    ("d60_bthd_segments", 1, 4, 333, 60, BTHD, 1.0, 2.0),
+    ("d48", 2, 2, 150, 48, BHTD, 1.0, 0.5),
+    ("d64_strong_decay", 1, 2, 200, 64, BHTD, 8.0, 2.0),
+    ("d64_full_retention", 1, 2, 300, 64, BHTD, 0.0, 2.0),
+    ("d64_T1", 2, 2, 1, 64, BHTD, 1.0, 2.0),
+    ("d60_T17", 1, 3, 17, 60, BTHD, 1.0, 2.0),
+    ("d64_T32_even_chunks", 1, 1, 32, 64, BHTD, 1.0, 2.0),
+]
+
+
+@pytest.mark.parametrize("name,B,H,T,d,layout,gs,tau", BWD_CASES, ids=[c[0] for c in BWD_CASES])
+def test_linear_backward_matches_oracle(name, B, H, T, d, layout, gs, tau):
+    x = rin.make_linear(rin.LinearWorkload(name, B, H, T, d, tau, gs, backward=True))
+    dev = {k: _to(v, layout).cuda() for k, v in x.items()}
+    grads = rb.linear_bwd(dev["P1"], dev["P2"], dev["I"], dev["G"], dev["dY"], tau, layout=layout)
+    torch.cuda.synchronize()
+    assert rb.relation_check_device_status() == 0
+    xs = {k: _np(v) for k, v in x.items()}
+    refs = lo.bwd(xs["P1"], xs["P2"], xs["I"], xs["G"], tau, xs["dY"])
+    for got, ref, label in zip(grads, refs, ("dP1", "dP2", "dI", "dG")):
+        err = _err(_np(_back(got, layout)), ref)
+        assert err <= GTOL * max(float(np.max(np.abs(ref))), 1e-6), (name, label, err, float(np.max(np.abs(ref))))
+
+
+def test_linear_backward_many_heads_sampled():
+    B, H, T, d, tau = 48, 8, 80, 64, 2.0
+    x = rin.make_linear(rin.LinearWorkload("many", B, H, T, d, tau, backward=True))
+    dev = {k: v.cuda() for k, v in x.items()}
+    grads = [_np(g) for g in rb.linear_bwd(dev["P1"], dev["P2"], dev["I"], dev["G"], dev["dY"], tau)]
+    for b, h in [(0, 0), (31, 2), (47, 7)]:
+        xs = {k: _np(v[b:b + 1, h:h + 1]) for k, v in x.items()}
+        refs = lo.bwd(xs["P1"], xs["P2"], xs["I"], xs["G"], tau, xs["dY"])
+        for got, ref in zip(grads, refs):
+            assert _err(got[b:b + 1, h:h + 1], ref) <= GTOL * float(np.max(np.abs(ref)))
