@@ -41,6 +41,9 @@ def parse():
                     help="time one Relation Cache decode step (full caches of the workload's T) instead")
     ap.add_argument("--prologue", action="store_true",
                     help="time the input prologue (RoPE + Givens) forward and backward of the workload instead")
+    ap.add_argument("--linear", action="store_true",
+                    help="time Linear Relation forward + backward (workload from the linear set, default "
+                         "linear_d60_T2048) instead")
     return ap.parse_args()
 
 
@@ -275,6 +278,171 @@ def run_prologue(args, w):
     return 0
 
 
+def linear_bytes_per_head_token(d: int) -> int:
+    """Algorithmic HBM bytes of one Linear Relation fwd+bwd per head and token: forward
+    reads P1, P2, I~ (bf16) and G (fp32) and writes Y (bf16): 12 d; backward reads P1,
+    P2, I~, dY (bf16) and G (fp32) and writes dP1, dP2, dI~ (bf16) and dG (fp32): 22 d."""
+    return 34 * d
+
+
+def linear_cpu_sample(w, target_s: float):
+    """The float64 Linear Relation oracle (as it stands) on whole heads of the workload until
+    about target_s seconds of CPU work; returns (head-tokens per second, heads, seconds)."""
+    import numpy as np
+
+    from oracle import linear as lo
+    from relation_token_mixing_gb300 import inputs as rin
+
+    x = rin.make_linear(rin.LinearWorkload(w.name, 1, 1, w.T, w.d, w.tau_S, w.g_scale, backward=True))
+    xs = {k: v.float().numpy().astype(np.float64) for k, v in x.items()}
+    heads, t0 = 0, time.perf_counter()
+    while True:
+        lo.fwd(xs["P1"], xs["P2"], xs["I"], xs["G"], w.tau_S)
+        lo.bwd(xs["P1"], xs["P2"], xs["I"], xs["G"], w.tau_S, xs["dY"])
+        heads += 1
+        dt = time.perf_counter() - t0
+        if dt >= target_s:
+            return heads * w.T / dt, heads, dt
+
+
+def run_linear(args, w):
+    """Linear Relation forward + backward over B*H heads of length T, inputs larger than L2.
+    value = tokens (B*T) per second; the roofline is HBM bytes of the whole step."""
+    import torch
+
+    from relation_token_mixing_gb300 import binding as rb
+    from relation_token_mixing_gb300 import inputs as rin
+
+    rb.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    x_cpu = rin.make_linear(w)
+    x = {k: v.to(dev) for k, v in x_cpu.items()}
+    prob = rb.problem_for(x["P1"], w.tau_S, 0.0, True)
+    ws = rb.linear_workspace(prob, dev)
+    Y = torch.empty_like(x["I"])
+    g = [torch.empty_like(x["P1"]), torch.empty_like(x["P2"]), torch.empty_like(x["I"]), torch.empty_like(x["G"])]
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    launches = [0]
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        rb.relation_linear_fwd(prob, x["P1"], x["P2"], x["I"], x["G"], Y, None, ws, stream)
+        launches[0] += rb.relation_last_launch_count()
+        if evs:
+            evs[1].record(stream)
+        rb.relation_linear_bwd(prob, x["P1"], x["P2"], x["I"], x["G"], x["dY"], *g, ws, stream)
+        launches[0] += rb.relation_last_launch_count()
+        if evs:
+            evs[2].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if rb.relation_check_device_status() != 0:
+        raise RuntimeError("device-side wait expired during warm-up")
+    evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    launches[0] = 0
+    with ClockSampler(0) as clk:
+        for k in range(args.steps):
+            flush.zero_()
+            step(evsets[k])
+        torch.cuda.synchronize()
+    if rb.relation_check_device_status() != 0:
+        raise RuntimeError("device-side wait expired during the timed region")
+    tf = [e[0].elapsed_time(e[1]) for e in evsets]
+    tb = [e[1].elapsed_time(e[2]) for e in evsets]
+    ms = statistics.mean(tf) + statistics.mean(tb)
+    tokens = w.B * w.T
+    value = tokens / (ms * 1e-3)
+    step_bytes = linear_bytes_per_head_token(w.d) * w.B * w.H * w.T
+    gbs = step_bytes / (ms * 1e-3) / 1e9
+    hbm = load_peaks_hbm()
+
+    e2e = None
+    if not args.no_e2e:
+        h_in = {k: v.pin_memory() for k, v in x_cpu.items()}
+        h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in [Y] + g]
+
+        def e2e_step():
+            for k in ("P1", "P2", "I", "G", "dY"):
+                x[k].copy_(h_in[k], non_blocking=True)
+            step()
+            for h, t in zip(h_out, [Y] + g):
+                h.copy_(t, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e_ms = 0.0
+        for _ in range(args.steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            e2e_step()
+            b.record(stream)
+            b.synchronize()
+            e_ms += a.elapsed_time(b)
+        e2e = {"value": tokens * args.steps / (e_ms * 1e-3), "unit": "tok/s",
+               "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in h_in.values()),
+               "d2h_bytes_per_step": sum(v.numel() * v.element_size() for v in h_out)}
+
+    line = {
+        "metric": "Linear Relation fwd+bwd tokens per second (bf16 operands, fp32 state)",
+        "value": value, "unit": "tok/s", "n_gpus": 1, "steps": args.steps, "warmup": max(3, args.warmup),
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 operands, f32 state and accumulation",
+        "data": "synthetic (seeded Gaussian P1, P2, I~, dY; log-retention G with the statistics of its "
+                "initialisation), resident in HBM",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d_h": w.d, "tau_S": w.tau_S,
+                   "g_scale": w.g_scale, "l2": "flushed between timed steps"},
+        "breakdown_ms": {"fwd": statistics.mean(tf), "bwd": statistics.mean(tb)},
+        "roofline": {"kernel": "relation_linear_fwd + relation_linear_bwd (all launches)", "bound": "hbm",
+                     "achieved": gbs, "peak": hbm[0], "unit": "GB/s", "frac": gbs / hbm[0],
+                     "peak_source": hbm[1], "traffic": None,
+                     "algorithmic_bytes_per_head_token": linear_bytes_per_head_token(w.d)},
+        "gpu_launches": launches[0],
+        "e2e": e2e,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        try:
+            rate, heads, dt = linear_cpu_sample(w, 10.0)
+            line["cpu_baseline"] = {"value": rate / w.H, "unit": "tok/s", "cores": 1, "kind": "oracle",
+                                    "sample": f"fwd+bwd of {heads} whole head(s) at T={w.T} d={w.d}, float64, "
+                                              f"{dt:.1f} s; tok/s = head-tokens/s divided by H={w.H}"}
+        except Exception as exc:
+            line["cpu_baseline"] = {"value": None, "unit": "tok/s", "cores": None, "kind": "oracle",
+                                    "sample": f"failed: {exc}"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_linear_reference(args, w):
+    if int(os.environ.get("RANK", "0")) != 0:
+        return 0
+    rate = []
+    for _ in range(args.warmup):
+        linear_cpu_sample(w, 0.0)
+    for _ in range(args.steps):
+        r, heads, dt = linear_cpu_sample(w, 0.0)
+        rate.append(r / w.H)
+    value = statistics.mean(rate)
+    sample = f"each step: fwd+bwd of 1 whole head (of {w.B * w.H}) at T={w.T} d={w.d}, float64"
+    print(json.dumps({
+        "impl": "reference", "metric": "Linear Relation fwd+bwd tokens per second (bf16 operands, fp32 state)",
+        "value": value, "unit": "tok/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": w.T / w.H / value * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded, bf16-rounded then upcast)",
+        "config": {"workload": w.name, "B": 1, "H": 1, "T": w.T, "d_h": w.d, "tau_S": w.tau_S},
+        "cpu_baseline": {"value": value, "unit": "tok/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+    return 0
+
+
 def load_peaks_hbm():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -324,6 +492,10 @@ def main():
     args = parse()
     from relation_token_mixing_gb300 import inputs as rin
 
+    if args.linear:
+        name = args.workload if args.workload in rin.LINEAR_WORKLOADS else "linear_d60_T2048"
+        lw = rin.LINEAR_WORKLOADS[name]
+        return run_linear_reference(args, lw) if args.impl == "reference" else run_linear(args, lw)
     w = rin.WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)
