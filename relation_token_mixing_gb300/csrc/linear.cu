@@ -1051,6 +1051,26 @@ __global__ void __launch_bounds__(kThreads, 3) linear_bwd_b_kernel(BArgs a) {
         const QuarterTotals T = quarter_totals(gs, warp, lane);
         channel_phase_b<true, true, true, true>(Q, T, gs, s, warp, lane);
         __syncthreads();  // B3
+        // Scratch written by sweep A for this warp's tokens (q . dq, the normalisation
+        // part of dP1, p^1 . dq), loaded now so the latency hides under the products.
+        float2 xs[4];
+        uint32_t p1w[4];
+        float pq[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int tok = t0 + 4 * warp + r;
+            xs[r] = make_float2(0.f, 0.f);
+            p1w[r] = 0u;
+            pq[r] = 0.f;
+            if (tok < kp.T) {
+                const size_t off = rm.base + (size_t)tok * rm.stride + c;
+                if (c < kp.d) {
+                    xs[r] = *reinterpret_cast<const float2*>(a.dG + off);
+                    p1w[r] = *reinterpret_cast<const uint32_t*>(a.dP1 + off);
+                }
+                pq[r] = a.pdq[(size_t)bh * kp.T + tok];
+            }
+        }
         level_matrix(gs, warp, lane);
         level_dA(gs, s, warp, lane);
         __syncthreads();  // B4
@@ -1158,7 +1178,7 @@ __global__ void __launch_bounds__(kThreads, 3) linear_bwd_b_kernel(BArgs a) {
         float2 zq = make_float2(0.f, 0.f);
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-            const int i = 4 * warp + r, tok = t0 + i;
+            const int i = 4 * warp + r;
             float2 dk = mul2(mul2(Q.b[r], T.suf), *reinterpret_cast<const float2*>(gs.xq + i * kDp + c));
 #pragma unroll
             for (int lvl = 0; lvl < 4; ++lvl) {
@@ -1171,9 +1191,7 @@ __global__ void __launch_bounds__(kThreads, 3) linear_bwd_b_kernel(BArgs a) {
             const float s2 = gs.rs[i].y;
             const uint32_t w2 = *reinterpret_cast<const uint32_t*>(s.p2 + swz(i, c));
             const float2 k = make_float2(lo_f(w2) * s2, hi_f(w2) * s2);
-            float2 x = make_float2(0.f, 0.f);
-            if (tok < kp.T && c < kp.d) x = *reinterpret_cast<const float2*>(a.dG + rm.base + (size_t)tok * rm.stride + c);
-            zs[r] = make_float2(x.x - k.x * dk.x, x.y - k.y * dk.y);
+            zs[r] = make_float2(xs[r].x - k.x * dk.x, xs[r].y - k.y * dk.y);
             zq = make_float2(zq.x + zs[r].x, zq.y + zs[r].y);
         }
         *reinterpret_cast<float2*>(&gs.zt[warp][c]) = zq;
@@ -1202,12 +1220,11 @@ __global__ void __launch_bounds__(kThreads, 3) linear_bwd_b_kernel(BArgs a) {
             if (tok < kp.T) {
                 const size_t off = rm.base + (size_t)tok * rm.stride;
                 const float S = rn.z;
-                const float dz = (a.pdq[(size_t)bh * kp.T + tok] + pd) * S * (1.f - S) * a.zscale;
+                const float dz = (pq[r] + pd) * S * (1.f - S) * a.zscale;
                 if (c < kp.d) {
                     *reinterpret_cast<float2*>(a.dG + off + c) = later;
-                    const uint32_t pw = *reinterpret_cast<const uint32_t*>(a.dP1 + off + c);
                     *reinterpret_cast<uint32_t*>(a.dP1 + off + c) =
-                        pack2(lo_f(pw) + dz * p2.x, hi_f(pw) + dz * p2.y);
+                        pack2(lo_f(p1w[r]) + dz * p2.x, hi_f(p1w[r]) + dz * p2.y);
                     *reinterpret_cast<uint32_t*>(a.dP2 + off + c) =
                         pack2(s2 * (dk.x - ph.x * pd) + dz * p1.x, s2 * (dk.y - ph.y * pd) + dz * p1.y);
                 }
@@ -1220,18 +1237,28 @@ __global__ void __launch_bounds__(kThreads, 3) linear_bwd_b_kernel(BArgs a) {
 
 // ------------------------------------------------------------------ launchers
 int linear_segments(const KernelProblem& kp, int num_sms, int* seg_len) {
-    // Enough groups for about four per SM; segments of at least 128 tokens.
-    const int64_t want = (int64_t)num_sms * 4;
-    int nseg = 1;
-    if (kp.BH < want) nseg = (int)((want + kp.BH - 1) / kp.BH);
+    // Segments trade parallelism for an extra state pass over every token (about a
+    // quarter of the output passes' work).  Pick the count that minimises
+    // waves x chunks per segment x (1 + that overhead), with three resident CTAs per
+    // SM and segments of at least 128 tokens.
+    const int64_t slots = (int64_t)num_sms * 3;
     const int max_seg = (kp.T + 127) / 128;
-    if (nseg > max_seg) nseg = max_seg;
-    if (nseg < 1) nseg = 1;
-    int len = (kp.T + nseg - 1) / nseg;
+    int best = 1;
+    double best_cost = 0.0;
+    for (int n = 1; n <= max_seg; ++n) {
+        const int len = ((kp.T + n - 1) / n + lin::kC - 1) / lin::kC * lin::kC;
+        const int nn = (kp.T + len - 1) / len;
+        const double waves = (double)((kp.BH * nn + slots - 1) / slots);
+        const double cost = waves * (double)(len / lin::kC) * (nn > 1 ? 1.25 : 1.0);
+        if (n == 1 || cost < best_cost - 1e-9) {
+            best = nn;
+            best_cost = cost;
+        }
+    }
+    int len = (kp.T + best - 1) / best;
     len = (len + lin::kC - 1) / lin::kC * lin::kC;
-    nseg = (kp.T + len - 1) / len;
     *seg_len = len;
-    return nseg;
+    return (kp.T + len - 1) / len;
 }
 
 cudaError_t launch_linear_fwd(const KernelProblem& kp, const void* P1, const void* P2, const void* V, const float* G,
