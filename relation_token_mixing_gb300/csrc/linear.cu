@@ -616,6 +616,10 @@ struct BStage {
     uint8_t dy[kC * 128];
     float g[kC * kDp];
 };
+// Row stride (floats) of the fp32 exchange tiles: 72 rather than 64 so the 8-byte
+// stores from the accumulator layout (8 rows x 4 column pairs per instruction) take
+// two shared-memory wavefronts instead of eight.
+constexpr int kXs = 72;
 struct BwdSmem {
     static constexpr bool kNorms = true;
     BStage st[2];
@@ -625,8 +629,8 @@ struct BwdSmem {
     uint8_t kl[4][8 * 128];
     uint8_t amat[kC * kArow];
     uint8_t dal[4][kC * kArow];  // dA on the pairs of each level, keys compacted (columns 8..15 zero)
-    float xq[kC * kDp];          // dQ~ (sweep A) or dK~ (sweep B), fp32 [row][channel]
-    float xl[4][kC * kDp];       // per level: dQ_L [token][c] (sweep A) or dK_L [key row][c] (sweep B)
+    float xq[kC * kXs];          // dQ~ (sweep A) or dK~ (sweep B), fp32 [row][channel]
+    float xl[4][kC * kXs];       // per level: dQ_L [token][c] (sweep A) or dK_L [key row][c] (sweep B)
     float2 rs[kC];               // (S / ||p1||, S / ||p2||)
     float4 rn[kC];               // (1 / ||p1||, 1 / ||p2||, S, -)
     float avec[kDp];
@@ -916,8 +920,8 @@ __global__ void __launch_bounds__(kThreads, 3) linear_bwd_a_kernel(BArgs a) {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int col = 16 * warp + 8 * h + 2 * t;
-                *reinterpret_cast<float2*>(gs.xq + g * kDp + col) = make_float2(dq[h][0], dq[h][1]);
-                *reinterpret_cast<float2*>(gs.xq + (g + 8) * kDp + col) = make_float2(dq[h][2], dq[h][3]);
+                *reinterpret_cast<float2*>(gs.xq + g * kXs + col) = make_float2(dq[h][0], dq[h][1]);
+                *reinterpret_cast<float2*>(gs.xq + (g + 8) * kXs + col) = make_float2(dq[h][2], dq[h][3]);
             }
 #pragma unroll
             for (int lvl = 0; lvl < 4; ++lvl) {
@@ -930,8 +934,8 @@ __global__ void __launch_bounds__(kThreads, 3) linear_bwd_a_kernel(BArgs a) {
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int col = 16 * warp + 8 * h + 2 * t;
-                    *reinterpret_cast<float2*>(gs.xl[lvl] + g * kDp + col) = make_float2(o[h][0], o[h][1]);
-                    *reinterpret_cast<float2*>(gs.xl[lvl] + (g + 8) * kDp + col) = make_float2(o[h][2], o[h][3]);
+                    *reinterpret_cast<float2*>(gs.xl[lvl] + g * kXs + col) = make_float2(o[h][0], o[h][1]);
+                    *reinterpret_cast<float2*>(gs.xl[lvl] + (g + 8) * kXs + col) = make_float2(o[h][2], o[h][3]);
                 }
             }
             // C <- Diag(a) C + (k . B)^T I~ on rows c of this warp
@@ -958,12 +962,12 @@ __global__ void __launch_bounds__(kThreads, 3) linear_bwd_a_kernel(BArgs a) {
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const int i = 4 * warp + r, tok = t0 + i;
-            float2 dq = mul2(mul2(T.pre, Q.f[r]), *reinterpret_cast<const float2*>(gs.xq + i * kDp + c));
+            float2 dq = mul2(mul2(T.pre, Q.f[r]), *reinterpret_cast<const float2*>(gs.xq + i * kXs + c));
 #pragma unroll
             for (int lvl = 0; lvl < 4; ++lvl) {
                 const int b = 3 - lvl;
                 if (is_query(i, b))
-                    dq = fma2(query_factor(Q, T, warp, r, b), *reinterpret_cast<const float2*>(gs.xl[lvl] + i * kDp + c),
+                    dq = fma2(query_factor(Q, T, warp, r, b), *reinterpret_cast<const float2*>(gs.xl[lvl] + i * kXs + c),
                               dq);
             }
             const float4 rn = gs.rn[i];
@@ -1091,8 +1095,8 @@ __global__ void __launch_bounds__(kThreads, 3) linear_bwd_b_kernel(BArgs a) {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int col = 16 * warp + 8 * h + 2 * t;
-                *reinterpret_cast<float2*>(gs.xq + g * kDp + col) = make_float2(dk[h][0], dk[h][1]);
-                *reinterpret_cast<float2*>(gs.xq + (g + 8) * kDp + col) = make_float2(dk[h][2], dk[h][3]);
+                *reinterpret_cast<float2*>(gs.xq + g * kXs + col) = make_float2(dk[h][0], dk[h][1]);
+                *reinterpret_cast<float2*>(gs.xq + (g + 8) * kXs + col) = make_float2(dk[h][2], dk[h][3]);
             }
             // dK_L = dA_L^T Q_L (rows: compacted keys 0..7)
 #pragma unroll
@@ -1105,7 +1109,7 @@ __global__ void __launch_bounds__(kThreads, 3) linear_bwd_b_kernel(BArgs a) {
                 mma16816(o[1], af, r4[2], r4[3]);
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
-                    *reinterpret_cast<float2*>(gs.xl[lvl] + g * kDp + 16 * warp + 8 * h + 2 * t) =
+                    *reinterpret_cast<float2*>(gs.xl[lvl] + g * kXs + 16 * warp + 8 * h + 2 * t) =
                         make_float2(o[h][0], o[h][1]);
             }
             // dI~ = (k . B) dC + A^T dE + dY on value channels [16w, 16w+16)
@@ -1179,13 +1183,13 @@ __global__ void __launch_bounds__(kThreads, 3) linear_bwd_b_kernel(BArgs a) {
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const int i = 4 * warp + r;
-            float2 dk = mul2(mul2(Q.b[r], T.suf), *reinterpret_cast<const float2*>(gs.xq + i * kDp + c));
+            float2 dk = mul2(mul2(Q.b[r], T.suf), *reinterpret_cast<const float2*>(gs.xq + i * kXs + c));
 #pragma unroll
             for (int lvl = 0; lvl < 4; ++lvl) {
                 const int b = 3 - lvl;
                 if (!is_query(i, b))
                     dk = fma2(key_factor(Q, T, warp, r, b),
-                              *reinterpret_cast<const float2*>(gs.xl[lvl] + key_row(i, b) * kDp + c), dk);
+                              *reinterpret_cast<const float2*>(gs.xl[lvl] + key_row(i, b) * kXs + c), dk);
             }
             dkv[r] = dk;
             const float s2 = gs.rs[i].y;
