@@ -306,8 +306,9 @@ def linear_cpu_sample(w, target_s: float):
 
 
 def run_linear(args, w):
-    """Linear Relation forward + backward over B*H heads of length T, inputs larger than L2.
-    value = tokens (B*T) per second; the roofline is HBM bytes of the whole step."""
+    """Linear Relation forward + backward over B*H heads of length T, inputs larger than L2, the
+    backward reusing the forward's segment states from the shared workspace (as a training step
+    does).  value = tokens (B*T) per second; the roofline is HBM bytes of the whole step."""
     import torch
 
     from relation_token_mixing_gb300 import binding as rb
@@ -333,7 +334,7 @@ def run_linear(args, w):
         launches[0] += rb.relation_last_launch_count()
         if evs:
             evs[1].record(stream)
-        rb.relation_linear_bwd(prob, x["P1"], x["P2"], x["I"], x["G"], x["dY"], *g, ws, stream)
+        rb.relation_linear_bwd(prob, x["P1"], x["P2"], x["I"], x["G"], x["dY"], *g, 1, ws, stream)
         launches[0] += rb.relation_last_launch_count()
         if evs:
             evs[2].record(stream)

@@ -242,7 +242,11 @@ relation_status_t relation_prologue_bwd(const relation_problem_t* p, const void*
  * relation_linear_bwd: from dY (bf16, like Y): dP1, dP2, dI (bf16) and dG
  *   (float32), all fully overwritten (gradients of sum(Y * dY) with C_0 = 0).
  *   2 to 6 kernel launches (the forward and reverse segment state passes and
- *   scans only when B*H is too small to fill the GPU).
+ *   scans only when B*H is too small to fill the GPU).  states_from_forward
+ *   nonzero: the workspace still holds what relation_linear_fwd left in it for
+ *   the same problem and inputs (as in a training step that keeps the workspace
+ *   from the forward to the backward), and the forward segment states are reused
+ *   instead of recomputed; any other use gives wrong gradients.  0: recompute.
  * relation_linear_workspace_bytes: the float32 workspace both directions need
  *   (16-byte aligned, caller-owned, contents need not be preserved between
  *   calls); 0 on invalid arguments.
@@ -254,7 +258,8 @@ relation_status_t relation_linear_fwd(const relation_problem_t* p, const void* P
                                       size_t workspace_bytes, void* stream);
 relation_status_t relation_linear_bwd(const relation_problem_t* p, const void* P1, const void* P2, const void* I,
                                       const float* G, const void* dY, void* dP1, void* dP2, void* dI, float* dG,
-                                      void* workspace, size_t workspace_bytes, void* stream);
+                                      int states_from_forward, void* workspace, size_t workspace_bytes,
+                                      void* stream);
 
 /*
  * Reads and clears the device status word of the current device.  Call after

@@ -103,8 +103,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.relation_linear_fwd.argtypes = [ctypes.POINTER(Problem), _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                             ctypes.c_size_t, _VP]
         lib.relation_linear_fwd.restype = ctypes.c_int
-        lib.relation_linear_bwd.argtypes = [ctypes.POINTER(Problem), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
-                                            ctypes.c_size_t, _VP]
+        lib.relation_linear_bwd.argtypes = [ctypes.POINTER(Problem), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                            ctypes.c_int, _VP, ctypes.c_size_t, _VP]
         lib.relation_linear_bwd.restype = ctypes.c_int
         lib.relation_check_device_status.argtypes = []
         lib.relation_check_device_status.restype = ctypes.c_int
@@ -246,9 +246,10 @@ def relation_linear_fwd(prob, P1, P2, I, G, Y, state, workspace, stream=None) ->
                                       _stream_ptr(stream)), "relation_linear_fwd")
 
 
-def relation_linear_bwd(prob, P1, P2, I, G, dY, dP1, dP2, dI, dG, workspace, stream=None) -> None:
+def relation_linear_bwd(prob, P1, P2, I, G, dY, dP1, dP2, dI, dG, states_from_forward, workspace,
+                        stream=None) -> None:
     _check(load().relation_linear_bwd(ctypes.byref(prob), _ptr(P1), _ptr(P2), _ptr(I), _ptr(G), _ptr(dY), _ptr(dP1),
-                                      _ptr(dP2), _ptr(dI), _ptr(dG), _ptr(workspace),
+                                      _ptr(dP2), _ptr(dI), _ptr(dG), int(states_from_forward), _ptr(workspace),
                                       workspace.numel() * workspace.element_size(), _stream_ptr(stream)),
            "relation_linear_bwd")
 
@@ -299,13 +300,17 @@ def linear_fwd(P1, P2, I, G, tau_S: float, layout: int = RELATION_LAYOUT_BHTD, w
     return Y, state
 
 
-def linear_bwd(P1, P2, I, G, dY, tau_S: float, layout: int = RELATION_LAYOUT_BHTD, stream=None, workspace=None):
-    """Linear Relation backward; allocates and returns (dP1, dP2, dI, dG)."""
+def linear_bwd(P1, P2, I, G, dY, tau_S: float, layout: int = RELATION_LAYOUT_BHTD, stream=None, workspace=None,
+               states_from_forward: bool = False):
+    """Linear Relation backward; allocates and returns (dP1, dP2, dI, dG).  states_from_forward:
+    ``workspace`` still holds what linear_fwd left in it for the same inputs."""
     prob = problem_for(P1, tau_S, 0.0, True, layout)
     dP1, dP2, dI, dG = torch.empty_like(P1), torch.empty_like(P2), torch.empty_like(I), torch.empty_like(G)
     if workspace is None:
+        if states_from_forward:
+            raise ValueError("states_from_forward needs the forward's workspace")
         workspace = linear_workspace(prob, P1.device)
-    relation_linear_bwd(prob, P1, P2, I, G, dY, dP1, dP2, dI, dG, workspace, stream)
+    relation_linear_bwd(prob, P1, P2, I, G, dY, dP1, dP2, dI, dG, states_from_forward, workspace, stream)
     return dP1, dP2, dI, dG
 
 

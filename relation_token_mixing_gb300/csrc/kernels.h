@@ -56,9 +56,10 @@ cudaError_t launch_linear_fwd(const KernelProblem& kp, const void* P1, const voi
                               void* Y, float* state_out, float* ws, int num_sms, cudaStream_t s);
 // The backward's workspace adds BH * nseg * 64 * 64 floats (reverse segment states)
 // and BH * T floats (p^1 . dq per token).
+// reuse_fwd_states: the workspace already holds the forward's segment states.
 cudaError_t launch_linear_bwd(const KernelProblem& kp, const void* P1, const void* P2, const void* V, const float* G,
-                              const void* dY, void* dP1, void* dP2, void* dV, float* dG, float* ws, int num_sms,
-                              cudaStream_t s);
+                              const void* dY, void* dP1, void* dP2, void* dV, float* dG, bool reuse_fwd_states,
+                              float* ws, int num_sms, cudaStream_t s);
 
 // Tensor-core (tcgen05) bf16 path.
 struct TcLaunch {

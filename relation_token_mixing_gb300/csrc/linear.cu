@@ -1307,8 +1307,8 @@ cudaError_t launch_linear_fwd(const KernelProblem& kp, const void* P1, const voi
 }
 
 cudaError_t launch_linear_bwd(const KernelProblem& kp, const void* P1, const void* P2, const void* V, const float* G,
-                              const void* dY, void* dP1, void* dP2, void* dV, float* dG, float* ws, int num_sms,
-                              cudaStream_t s) {
+                              const void* dY, void* dP1, void* dP2, void* dV, float* dG, bool reuse_fwd_states,
+                              float* ws, int num_sms, cudaStream_t s) {
     lin::Args fa;
     fa.P1 = static_cast<const __nv_bfloat16*>(P1);
     fa.P2 = static_cast<const __nv_bfloat16*>(P2);
@@ -1359,12 +1359,13 @@ cudaError_t launch_linear_bwd(const KernelProblem& kp, const void* P1, const voi
     const dim3 block(lin::kThreads);
     const bool vec16 = (kp.d % 8) == 0;
     if (fa.nseg > 1) {
-        if (vec16) {
-            lin::linear_state_kernel<true><<<grid, block, fsmem, s>>>(fa);
-        } else {
-            lin::linear_state_kernel<false><<<grid, block, fsmem, s>>>(fa);
+        if (!reuse_fwd_states) {
+            if (vec16)
+                lin::linear_state_kernel<true><<<grid, block, fsmem, s>>>(fa);
+            else
+                lin::linear_state_kernel<false><<<grid, block, fsmem, s>>>(fa);
+            lin::linear_scan_kernel<<<(unsigned)kp.BH * 16, 256, 0, s>>>(fa.hseg, fa.aseg, fa.nseg, nullptr, kp.d);
         }
-        lin::linear_scan_kernel<<<(unsigned)kp.BH * 16, 256, 0, s>>>(fa.hseg, fa.aseg, fa.nseg, nullptr, kp.d);
         if (vec16)
             lin::linear_bstate_kernel<true><<<grid, block, bsmem, s>>>(b);
         else

@@ -491,7 +491,8 @@ relation_status_t relation_linear_fwd(const relation_problem_t* p, const void* P
 
 relation_status_t relation_linear_bwd(const relation_problem_t* p, const void* P1, const void* P2, const void* I,
                                       const float* G, const void* dY, void* dP1, void* dP2, void* dI, float* dG,
-                                      void* workspace, size_t workspace_bytes, void* stream) {
+                                      int states_from_forward, void* workspace, size_t workspace_bytes,
+                                      void* stream) {
     relation_status_t st = check_linear(p);
     if (st != RELATION_OK) return st;
     const void* ins[] = {P1, P2, I, G, dY};
@@ -521,9 +522,10 @@ relation_status_t relation_linear_bwd(const relation_problem_t* p, const void* P
     const KernelProblem kp = kernel_problem(p);
     int len = 0;
     const int nseg = linear_segments(kp, di.num_sms, &len);
-    st = from_cuda(launch_linear_bwd(kp, P1, P2, I, G, dY, dP1, dP2, dI, dG, static_cast<float*>(workspace),
+    const bool reuse = states_from_forward != 0;
+    st = from_cuda(launch_linear_bwd(kp, P1, P2, I, G, dY, dP1, dP2, dI, dG, reuse, static_cast<float*>(workspace),
                                      di.num_sms, static_cast<cudaStream_t>(stream)));
-    if (st == RELATION_OK) t_last_launches = nseg > 1 ? 6 : 2;
+    if (st == RELATION_OK) t_last_launches = nseg > 1 ? (reuse ? 4 : 6) : 2;
     return st;
 }
 

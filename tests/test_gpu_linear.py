@@ -154,3 +154,22 @@ def test_linear_backward_many_heads_sampled():
         refs = lo.bwd(xs["P1"], xs["P2"], xs["I"], xs["G"], tau, xs["dY"])
         for got, ref in zip(grads, refs):
             assert _err(got[b:b + 1, h:h + 1], ref) <= GTOL * float(np.max(np.abs(ref)))
+
+
+@pytest.mark.parametrize("T", [700, 64])
+def test_linear_backward_reusing_forward_states(T):
+    """relation_linear_bwd with states_from_forward = 1 after relation_linear_fwd on the same
+    workspace (segment-split path at T = 700, single segment at T = 64) equals the oracle."""
+    B, H, d, tau = 1, 2, 64, 1.0
+    x = rin.make_linear(rin.LinearWorkload("reuse", B, H, T, d, tau, backward=True))
+    dev = {k: v.cuda() for k, v in x.items()}
+    prob = rb.problem_for(dev["P1"], tau, 0.0, True)
+    ws = rb.linear_workspace(prob, "cuda")
+    rb.linear_fwd(dev["P1"], dev["P2"], dev["I"], dev["G"], tau, workspace=ws)
+    grads = rb.linear_bwd(dev["P1"], dev["P2"], dev["I"], dev["G"], dev["dY"], tau, workspace=ws,
+                          states_from_forward=True)
+    torch.cuda.synchronize()
+    xs = {k: _np(v) for k, v in x.items()}
+    refs = lo.bwd(xs["P1"], xs["P2"], xs["I"], xs["G"], tau, xs["dY"])
+    for got, ref in zip(grads, refs):
+        assert _err(_np(got), ref) <= GTOL * float(np.max(np.abs(ref)))
