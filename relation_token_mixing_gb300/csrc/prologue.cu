@@ -31,13 +31,19 @@ __device__ __forceinline__ void rope_sincos(float pos, float hi, float lo, float
     sincospif(2.f * frac, s, c);
 }
 
-// VC consecutive elements as fp32 (8-byte loads for bf16 VC = 4, 4-byte VC = 2;
+// VC consecutive elements as fp32 (16-, 8- or 4-byte loads for bf16 VC = 8, 4, 2;
 // 16- / 8-byte for fp32).
 template <typename T, int VC>
 __device__ __forceinline__ void loadv(const T* p, float (&v)[VC]) {
     if constexpr (sizeof(T) == 2) {
         uint32_t w[VC / 2];
-        if constexpr (VC == 4) {
+        if constexpr (VC == 8) {
+            const uint4 u = *reinterpret_cast<const uint4*>(p);
+            w[0] = u.x;
+            w[1] = u.y;
+            w[2] = u.z;
+            w[3] = u.w;
+        } else if constexpr (VC == 4) {
             const uint2 u = *reinterpret_cast<const uint2*>(p);
             w[0] = u.x;
             w[1] = u.y;
@@ -67,7 +73,9 @@ __device__ __forceinline__ void storev(T* p, const float (&v)[VC]) {
             const __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
             w[k] = *reinterpret_cast<const uint32_t*>(&b);
         }
-        if constexpr (VC == 4)
+        if constexpr (VC == 8)
+            *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+        else if constexpr (VC == 4)
             *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
         else
             *reinterpret_cast<uint32_t*>(p) = w[0];
@@ -137,13 +145,15 @@ __global__ void __launch_bounds__(kThreads) rope_kernel(KernelProblem kp, const 
 
 // Givens mixing of the information states, forward (I -> I~) or backward
 // (dI~ -> dI, plus d theta from the mixed states Im = I~ when dtheta != NULL).
-// One warp per (batch, token, head pair); each lane takes one VC-column group
-// (d <= 32 VC for every supported width).
-template <typename T, int VC, typename Idx>
+// A group of LPR lanes takes one (batch, token, head pair), VC columns per lane
+// (LPR * VC >= d), so a warp covers 32 / LPR pairs per step with 16-byte
+// accesses where the rows allow them.
+template <typename T, int VC, int LPR, typename Idx>
 __global__ void __launch_bounds__(kThreads) givens_kernel(KernelProblem kp, const T* __restrict__ x,
                                                           const T* __restrict__ Im, T* __restrict__ y,
                                                           const float* __restrict__ theta, int pairing, float sign,
                                                           float* __restrict__ dtheta, Idx rows) {
+    constexpr int kRowsPerWarp = 32 / LPR;
     extern __shared__ float sh[];  // cos, sin, partial d theta: 3 x H/2
     const int P = kp.H / 2;
     float* scos = sh;
@@ -158,44 +168,52 @@ __global__ void __launch_bounds__(kThreads) givens_kernel(KernelProblem kp, cons
     }
     __syncthreads();
     const int lane = threadIdx.x & 31;
-    const int c = VC * lane;
+    const int sub = lane / LPR, li = lane % LPR;
+    const int c = VC * li;
     const bool on = c < kp.d;
     const Idx Pn = (Idx)P, Tn = (Idx)kp.T;
-    const Idx wstride = (Idx)gridDim.x * (blockDim.x / 32);
-    for (Idx r = (Idx)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); r < rows; r += wstride) {
-        const Idx bt = r / Pn;
-        const int pr = (int)(r - bt * Pn);
-        const Idx b = bt / Tn;
-        const int t = (int)(bt - b * Tn);
-        const int ha = pairing == 0 ? 2 * pr : 2 * pr + 1;
-        const int hb = pairing == 0 ? 2 * pr + 1 : (2 * pr + 2) % kp.H;
-        const size_t oa = row_offset(kp, (int64_t)b * kp.H + ha, t) + c;
-        const size_t ob = row_offset(kp, (int64_t)b * kp.H + hb, t) + c;
-        const float cs = scos[pr], sn = ssin[pr];
+    const Idx first = ((Idx)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5)) * kRowsPerWarp + sub;
+    const Idx step = (Idx)gridDim.x * (blockDim.x / 32) * kRowsPerWarp;
+    const Idx rows_rounded = (rows + kRowsPerWarp - 1) / kRowsPerWarp * kRowsPerWarp;
+    for (Idx r0 = first; r0 < rows_rounded + sub; r0 += step) {  // same trip count for every lane of the warp
+        const Idx r = r0;
+        const bool valid = r < rows;
         float part = 0.f;
-        if (on) {
-            float a[VC], q[VC], ya[VC], yb[VC];
-            loadv<T, VC>(x + oa, a);
-            loadv<T, VC>(x + ob, q);
+        int pr = 0;
+        if (valid) {
+            const Idx bt = r / Pn;
+            pr = (int)(r - bt * Pn);
+            const Idx b = bt / Tn;
+            const int t = (int)(bt - b * Tn);
+            const int ha = pairing == 0 ? 2 * pr : 2 * pr + 1;
+            const int hb = pairing == 0 ? 2 * pr + 1 : (2 * pr + 2) % kp.H;
+            const size_t oa = row_offset(kp, (int64_t)b * kp.H + ha, t) + c;
+            const size_t ob = row_offset(kp, (int64_t)b * kp.H + hb, t) + c;
+            const float cs = scos[pr], sn = ssin[pr];
+            if (on) {
+                float a[VC], q[VC], ya[VC], yb[VC];
+                loadv<T, VC>(x + oa, a);
+                loadv<T, VC>(x + ob, q);
 #pragma unroll
-            for (int v = 0; v < VC; ++v) {
-                ya[v] = cs * a[v] - sn * q[v];
-                yb[v] = sn * a[v] + cs * q[v];
-            }
-            storev<T, VC>(y + oa, ya);
-            storev<T, VC>(y + ob, yb);
-            if (dtheta != nullptr) {  // x = dI~: dI~b . I~a - dI~a . I~b
-                float ma[VC], mb[VC];
-                loadv<T, VC>(Im + oa, ma);
-                loadv<T, VC>(Im + ob, mb);
+                for (int v = 0; v < VC; ++v) {
+                    ya[v] = cs * a[v] - sn * q[v];
+                    yb[v] = sn * a[v] + cs * q[v];
+                }
+                storev<T, VC>(y + oa, ya);
+                storev<T, VC>(y + ob, yb);
+                if (dtheta != nullptr) {  // x = dI~: dI~b . I~a - dI~a . I~b
+                    float ma[VC], mb[VC];
+                    loadv<T, VC>(Im + oa, ma);
+                    loadv<T, VC>(Im + ob, mb);
 #pragma unroll
-                for (int v = 0; v < VC; ++v) part += q[v] * ma[v] - a[v] * mb[v];
+                    for (int v = 0; v < VC; ++v) part += q[v] * ma[v] - a[v] * mb[v];
+                }
             }
         }
         if (dtheta != nullptr) {
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-            if (lane == 0) atomicAdd(&acc[pr], part);
+            for (int o = LPR / 2; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+            if (valid && li == 0) atomicAdd(&acc[pr], part);
         }
     }
     if (dtheta == nullptr) return;
@@ -225,18 +243,18 @@ cudaError_t launch_rope_t(const KernelProblem& kp, const void* x0, const void* x
     return cudaGetLastError();
 }
 
-template <typename T, int VC>
+template <typename T, int VC, int LPR>
 cudaError_t launch_givens_t(const KernelProblem& kp, const void* x, const void* Im, void* y, const float* theta,
                             int pairing, float sign, float* dtheta, int num_sms, cudaStream_t s) {
     const int64_t rows = (kp.BH / 2) * (int64_t)kp.T;  // (batch, token, head pair)
     const size_t smem = sizeof(float) * 3 * (size_t)(kp.H / 2);
-    const unsigned blocks = (unsigned)blocks_for(rows * 32, num_sms);
-    if (rows + (int64_t)blocks * (kThreads / 32) < (int64_t)UINT32_MAX)
-        givens_kernel<T, VC, uint32_t><<<blocks, kThreads, smem, s>>>(kp, (const T*)x, (const T*)Im, (T*)y, theta,
-                                                                      pairing, sign, dtheta, (uint32_t)rows);
+    const unsigned blocks = (unsigned)blocks_for(rows * LPR, num_sms);
+    if (rows + (int64_t)blocks * kThreads < (int64_t)UINT32_MAX)
+        givens_kernel<T, VC, LPR, uint32_t><<<blocks, kThreads, smem, s>>>(
+            kp, (const T*)x, (const T*)Im, (T*)y, theta, pairing, sign, dtheta, (uint32_t)rows);
     else
-        givens_kernel<T, VC, uint64_t><<<blocks, kThreads, smem, s>>>(kp, (const T*)x, (const T*)Im, (T*)y, theta,
-                                                                      pairing, sign, dtheta, (uint64_t)rows);
+        givens_kernel<T, VC, LPR, uint64_t><<<blocks, kThreads, smem, s>>>(
+            kp, (const T*)x, (const T*)Im, (T*)y, theta, pairing, sign, dtheta, (uint64_t)rows);
     return cudaGetLastError();
 }
 
@@ -245,11 +263,14 @@ cudaError_t launch_givens_t(const KernelProblem& kp, const void* x, const void* 
 cudaError_t launch_rope(const KernelProblem& kp, bool bf16, const void* x0, const void* x1, void* y0, void* y1,
                         const int* pos0, const RopeTable& tab, bool transpose, int num_sms, cudaStream_t s) {
     const float sign = transpose ? -1.f : 1.f;
-    // Four columns per thread where d/2 allows it (8-byte bf16 / 16-byte fp32 accesses), else two.
+    // Eight bf16 / four fp32 columns per thread (16-byte accesses) where d/2 allows it,
+    // else four or two.
     const bool four = (kp.d / 2) % 4 == 0;
-    if (bf16)
+    if (bf16) {
+        if ((kp.d / 2) % 8 == 0) return launch_rope_t<__nv_bfloat16, 8>(kp, x0, x1, y0, y1, pos0, tab, sign, num_sms, s);
         return four ? launch_rope_t<__nv_bfloat16, 4>(kp, x0, x1, y0, y1, pos0, tab, sign, num_sms, s)
                     : launch_rope_t<__nv_bfloat16, 2>(kp, x0, x1, y0, y1, pos0, tab, sign, num_sms, s);
+    }
     return four ? launch_rope_t<float, 4>(kp, x0, x1, y0, y1, pos0, tab, sign, num_sms, s)
                 : launch_rope_t<float, 2>(kp, x0, x1, y0, y1, pos0, tab, sign, num_sms, s);
 }
@@ -258,12 +279,31 @@ cudaError_t launch_givens(const KernelProblem& kp, bool bf16, const void* x, con
                           const float* theta, int pairing, bool transpose, float* dtheta, int num_sms,
                           cudaStream_t s) {
     const float sign = transpose ? -1.f : 1.f;
-    const bool four = kp.d % 4 == 0 && (kp.d * (bf16 ? 2 : 4)) % 16 == 0;  // rows aligned for 4-column accesses
-    if (bf16)
-        return four ? launch_givens_t<__nv_bfloat16, 4>(kp, x, Im, y, theta, pairing, sign, dtheta, num_sms, s)
-                    : launch_givens_t<__nv_bfloat16, 2>(kp, x, Im, y, theta, pairing, sign, dtheta, num_sms, s);
-    return four ? launch_givens_t<float, 4>(kp, x, Im, y, theta, pairing, sign, dtheta, num_sms, s)
-                : launch_givens_t<float, 2>(kp, x, Im, y, theta, pairing, sign, dtheta, num_sms, s);
+    // Widest access the row pitch allows (16 bytes when d * elem is a multiple of 16),
+    // and the fewest lanes (a power of two) that cover a row with it.
+    const int eb = bf16 ? 2 : 4;
+    const int vc = ((kp.d * eb) % 16 == 0) ? 16 / eb : (((kp.d * eb) % 8 == 0) ? 8 / eb : 4 / eb);
+    int lpr = 1;
+    while (lpr * vc < kp.d) lpr <<= 1;
+#define RELATION_GIVENS(T_, VC_, LPR_) \
+    return launch_givens_t<T_, VC_, LPR_>(kp, x, Im, y, theta, pairing, sign, dtheta, num_sms, s)
+    if (bf16) {
+        if (vc == 8) {
+            if (lpr <= 8) RELATION_GIVENS(__nv_bfloat16, 8, 8);
+            RELATION_GIVENS(__nv_bfloat16, 8, 16);
+        }
+        if (vc == 4) {
+            if (lpr <= 16) RELATION_GIVENS(__nv_bfloat16, 4, 16);
+            RELATION_GIVENS(__nv_bfloat16, 4, 32);
+        }
+        RELATION_GIVENS(__nv_bfloat16, 2, 32);
+    }
+    if (vc == 4) {
+        if (lpr <= 16) RELATION_GIVENS(float, 4, 16);
+        RELATION_GIVENS(float, 4, 32);
+    }
+    RELATION_GIVENS(float, 2, 32);
+#undef RELATION_GIVENS
 }
 
 }  // namespace relation
