@@ -577,7 +577,7 @@ const char* relation_status_string(relation_status_t s) {
     switch (s) {
         case RELATION_OK: return "ok";
         case RELATION_ERR_INVALID_ARGUMENT: return "invalid argument";
-        case RELATION_ERR_UNSUPPORTED: return "unsupported problem (d_h must be 48, 60, 64, 80 or 128)";
+        case RELATION_ERR_UNSUPPORTED: return "unsupported problem (no kernel for this head width or dtype)";
         case RELATION_ERR_MISALIGNED: return "tensor pointer not 16-byte aligned";
         case RELATION_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than relation_bwd_workspace_bytes()";
         case RELATION_ERR_CUDA: return "CUDA runtime error";
