@@ -467,10 +467,6 @@ relation_status_t relation_linear_fwd(const relation_problem_t* p, const void* P
     if (!aligned16(P1) || !aligned16(P2) || !aligned16(I) || !aligned16(G) || !aligned16(Y) ||
         !aligned16(workspace) || (state && !aligned16(state)))
         return RELATION_ERR_MISALIGNED;
-    DeviceInfo di;
-    if ((st = device_info(&di)) != RELATION_OK) return st;
-    if (workspace_bytes < linear_ws_floats(p, di.num_sms, false) * sizeof(float))
-        return RELATION_ERR_WORKSPACE_TOO_SMALL;
     const size_t tb = tensor_bytes(p), gb = rows_of(p) * (size_t)p->d_h * sizeof(float);
     const size_t sb = (size_t)p->B * p->H * p->d_h * p->d_h * sizeof(float);
     const void* ins[] = {P1, P2, I};
@@ -480,6 +476,10 @@ relation_status_t relation_linear_fwd(const relation_problem_t* p, const void* P
     }
     if (overlaps(Y, tb, G, gb) || (state && (overlaps(state, sb, G, gb) || overlaps(state, sb, Y, tb))))
         return RELATION_ERR_INVALID_ARGUMENT;
+    DeviceInfo di;
+    if ((st = device_info(&di)) != RELATION_OK) return st;
+    if (workspace_bytes < linear_ws_floats(p, di.num_sms, false) * sizeof(float))
+        return RELATION_ERR_WORKSPACE_TOO_SMALL;
     const KernelProblem kp = kernel_problem(p);
     int len = 0;
     const int nseg = linear_segments(kp, di.num_sms, &len);
@@ -507,10 +507,6 @@ relation_status_t relation_linear_bwd(const relation_problem_t* p, const void* P
     for (const void* x : outs)
         if (!aligned16(x)) return RELATION_ERR_MISALIGNED;
     if (!aligned16(workspace)) return RELATION_ERR_MISALIGNED;
-    DeviceInfo di;
-    if ((st = device_info(&di)) != RELATION_OK) return st;
-    if (workspace_bytes < linear_ws_floats(p, di.num_sms, true) * sizeof(float))
-        return RELATION_ERR_WORKSPACE_TOO_SMALL;
     const size_t tb = tensor_bytes(p), gb = rows_of(p) * (size_t)p->d_h * sizeof(float);
     const size_t in_len[] = {tb, tb, tb, gb, tb}, out_len[] = {tb, tb, tb, gb};
     for (int o = 0; o < 4; ++o) {
@@ -519,6 +515,10 @@ relation_status_t relation_linear_bwd(const relation_problem_t* p, const void* P
         for (int o2 = o + 1; o2 < 4; ++o2)
             if (overlaps(outs[o], out_len[o], outs[o2], out_len[o2])) return RELATION_ERR_INVALID_ARGUMENT;
     }
+    DeviceInfo di;
+    if ((st = device_info(&di)) != RELATION_OK) return st;
+    if (workspace_bytes < linear_ws_floats(p, di.num_sms, true) * sizeof(float))
+        return RELATION_ERR_WORKSPACE_TOO_SMALL;
     const KernelProblem kp = kernel_problem(p);
     int len = 0;
     const int nseg = linear_segments(kp, di.num_sms, &len);

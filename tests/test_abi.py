@@ -110,3 +110,46 @@ def test_workspace_size_and_backward_checks(lib):
         bad[7] += 4
         assert fn(ctypes.byref(p), *bad, ws, need, None) == 3
         assert fn(ctypes.byref(p), *args, None, need, None) == 1
+
+
+def _lfwd(lib, prob, P1=A, P2=2 * A, I=3 * A, G=4 * A, Y=8 * A, state=None, ws=16 * A):
+    return lib.relation_linear_fwd(ctypes.byref(prob), P1, P2, I, G, Y, state, ws, 1 << 30, None)
+
+
+def _lbwd(lib, prob, ptrs=None, ws=32 * A):
+    p = ptrs or [A, 2 * A, 3 * A, 4 * A, 6 * A, 8 * A, 10 * A, 12 * A, 14 * A]  # P1 P2 I G dY dP1 dP2 dI dG
+    return lib.relation_linear_bwd(ctypes.byref(prob), *p, 0, ws, 1 << 30, None)
+
+
+def test_linear_relation_argument_checks(lib):
+    """Linear Relation: bf16 only, d_h in {48, 60, 64}; bad problems, NULL, misaligned and
+    overlapping pointers are refused before the GPU is touched (every call here fails
+    validation: the addresses are fake and nothing may launch)."""
+    small = dict(B=1, H=1, T=16, d_h=64)
+    assert _lfwd(lib, _prob(**small, dtype=rb.RELATION_F32)) == 2
+    assert _lfwd(lib, _prob(B=1, H=1, T=16, d_h=80)) == 2
+    assert _lfwd(lib, _prob(B=1, H=1, T=16, d_h=128)) == 2
+    assert _lfwd(lib, _prob(**small, tau_S=0.0)) == 1
+    assert _lfwd(lib, _prob(**small), P1=None) == 1
+    assert _lfwd(lib, _prob(**small), ws=None) == 1
+    assert _lfwd(lib, _prob(**small), G=4 * A + 4) == 3
+    assert _lfwd(lib, _prob(**small), Y=A + 64) == 1          # Y overlaps P1
+    assert _lfwd(lib, _prob(**small), state=4 * A + 64) == 1  # state overlaps G
+    assert _lbwd(lib, _prob(**small, dtype=rb.RELATION_F32)) == 2
+    bad = [A, 2 * A, 3 * A, 4 * A, 6 * A, 8 * A, 10 * A, 12 * A, 8 * A]  # dG aliases dP1
+    assert _lbwd(lib, _prob(**small), bad) == 1
+    bad = [A, 2 * A, 3 * A, 4 * A, 6 * A, 8 * A + 8, 10 * A, 12 * A, 14 * A]
+    assert _lbwd(lib, _prob(**small), bad) == 3
+    assert _lbwd(lib, _prob(**small), ws=None) == 1
+
+
+def test_prologue_argument_checks(lib):
+    """Every call here is refused by validation (the addresses are fake; nothing may launch)."""
+    p = _prob(B=1, H=4, T=16, d_h=64)
+    f = lib.relation_prologue_fwd
+    assert f(ctypes.byref(_prob(B=1, H=3, T=16, d_h=64)), A, 2 * A, 3 * A, 4 * A, 0, 1e4, None, 8 * A, 9 * A, 10 * A,
+             None) == 1  # odd H: no head pairs
+    assert f(ctypes.byref(p), A, 2 * A, 3 * A, 4 * A, 2, 1e4, None, 8 * A, 9 * A, 10 * A, None) == 1  # pairing 2
+    assert f(ctypes.byref(p), A, 2 * A, 3 * A, None, 0, 1e4, None, 8 * A, 9 * A, 10 * A, None) == 1  # no theta
+    assert f(ctypes.byref(p), A, 2 * A, 3 * A + 8, 4 * A, 0, 1e4, None, 8 * A, 9 * A, 10 * A, None) == 3
+    assert f(ctypes.byref(p), A, 2 * A, 3 * A, 4 * A, 0, 1e4, None, A + 32, 9 * A, 10 * A, None) == 1  # P1 out over X1
