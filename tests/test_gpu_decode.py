@@ -138,3 +138,23 @@ def test_position_outside_cache_is_reported():
     assert torch.all(Y[1] == 3.0)  # the skipped batch is not written
     Yr, _ = _reference(x, [5, 10], 2, 1.0, 0.5)
     assert np.max(np.abs(Y[0].float().cpu().numpy() - Yr[0])) <= 1e-2 * float(x["V"].abs().max())
+
+
+def test_decode_benchmark_workload_every_head():
+    """bench.py --decode at full size: the headline workload's tensors (B4 H16 T4096 d64, large
+    |U|, tau 0.5, lambda 0.5), 4095 cached tokens per sequence, decoding token 4096; every
+    head's row against the oracle."""
+    w = rin.WORKLOADS["mhr_fwd_bwd_T4096"]
+    x = rin.make(w)
+    t = w.T - 1
+    dev = {k: v.cuda() for k, v in x.items()}
+    P1n, P2n, Vn = (dev[k][:, :, t].contiguous() for k in ("P1", "P2", "V"))
+    pos = torch.full((w.B,), t, dtype=torch.int32, device="cuda")
+    Y, L = rb.decode(P1n, P2n, Vn, dev["P2"], dev["V"], pos, w.tau_S, w.lam, append=False)
+    torch.cuda.synchronize()
+    assert rb.relation_check_device_status() == 0
+    heads = list(range(w.B * w.H))
+    Yr, Lr = oracle.fwd_rows(x["P1"], x["P2"], x["V"], w.tau_S, w.lam, True, heads, [t] * len(heads))
+    vmax = float(x["V"].abs().max())
+    assert np.max(np.abs(Y.float().cpu().numpy().reshape(len(heads), -1) - Yr)) <= Y_TOL[torch.bfloat16] * vmax
+    assert np.max(np.abs(L.cpu().numpy().reshape(-1) - Lr.reshape(-1))) <= L_TOL[torch.bfloat16]

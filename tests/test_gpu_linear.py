@@ -173,3 +173,28 @@ def test_linear_backward_reusing_forward_states(T):
     refs = lo.bwd(xs["P1"], xs["P2"], xs["I"], xs["G"], tau, xs["dY"])
     for got, ref in zip(grads, refs):
         assert _err(_np(got), ref) <= GTOL * float(np.max(np.abs(ref)))
+
+
+@pytest.mark.parametrize("wname,heads", [("linear_d60_T2048", [(0, 0), (9, 5), (15, 7)]),
+                                         ("linear_d60_T32768", [(0, 2), (0, 7)])])
+def test_linear_benchmark_workloads_sampled_heads(wname, heads):
+    """The benchmark's workloads at full size, in its launch configuration (forward, then the
+    backward reusing the forward's segment states from the shared workspace); whole heads
+    sampled against the oracle, forward and backward."""
+    w = rin.LINEAR_WORKLOADS[wname]
+    x = rin.make_linear(w)
+    dev = {k: v.cuda() for k, v in x.items()}
+    prob = rb.problem_for(dev["P1"], w.tau_S, 0.0, True)
+    ws = rb.linear_workspace(prob, "cuda")
+    Y, _ = rb.linear_fwd(dev["P1"], dev["P2"], dev["I"], dev["G"], w.tau_S, workspace=ws)
+    grads = rb.linear_bwd(dev["P1"], dev["P2"], dev["I"], dev["G"], dev["dY"], w.tau_S, workspace=ws,
+                          states_from_forward=True)
+    torch.cuda.synchronize()
+    assert rb.relation_check_device_status() == 0
+    for b, h in heads:
+        xs = {k: _np(v[b:b + 1, h:h + 1]) for k, v in x.items()}
+        Yr, _ = lo.fwd(xs["P1"], xs["P2"], xs["I"], xs["G"], w.tau_S)
+        assert _err(_np(Y[b:b + 1, h:h + 1]), Yr) <= TOL * float(np.max(np.abs(Yr)))
+        refs = lo.bwd(xs["P1"], xs["P2"], xs["I"], xs["G"], w.tau_S, xs["dY"])
+        for got, ref in zip(grads, refs):
+            assert _err(_np(got[b:b + 1, h:h + 1]), ref) <= GTOL * float(np.max(np.abs(ref)))

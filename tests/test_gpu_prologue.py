@@ -130,3 +130,32 @@ def test_prologue_operator_chain_matches_composed_oracles():
     for got, ref in ((dX1, rdX1), (dX2, rdX2), (dI, rdI)):
         assert _err(_np(got), ref) <= 2e-2 * float(np.max(np.abs(ref)))
     assert _err(dth.cpu().numpy(), rdth) <= 2e-2 * max(1.0, float(np.max(np.abs(rdth))))
+
+
+def test_prologue_benchmark_workload_in_full():
+    """bench.py --prologue at full size (the headline workload's tensors, B4 H16 T4096 d64, pairing B,
+    theta = linspace(-1, 1, H/2), base 1e4): every output against the oracle."""
+    w = rin.WORKLOADS["mhr_fwd_bwd_T4096"]
+    x = rin.make(w, with_dy=True)
+    dev = {k: v.cuda() for k, v in x.items()}
+    prob = rb.problem_for(dev["P1"], w.tau_S, w.lam, True)
+    theta = torch.linspace(-1.0, 1.0, w.H // 2)
+    th = theta.cuda()
+    outs = [torch.empty_like(dev["P1"]) for _ in range(3)]
+    rb.relation_prologue_fwd(prob, dev["P1"], dev["P2"], dev["V"], th, 1, 1e4, None, *outs)
+    grads = [torch.empty_like(dev["P1"]) for _ in range(3)]
+    dth = torch.empty(w.H // 2, device="cuda")
+    rb.relation_prologue_bwd(prob, dev["dY"], dev["dY"], dev["dY"], outs[2], th, 1, 1e4, None, *grads, dth)
+    torch.cuda.synchronize()
+    xs = {k: _np(v) for k, v in x.items()}
+    scale = max(float(np.max(np.abs(xs[k]))) for k in ("P1", "P2", "V"))
+    assert _err(_np(outs[0]), po.rope(xs["P1"], 1e4)) <= TOL[torch.bfloat16] * scale
+    assert _err(_np(outs[1]), po.rope(xs["P2"], 1e4)) <= TOL[torch.bfloat16] * scale
+    Im = po.givens(xs["V"], theta.double().numpy(), 1)
+    assert _err(_np(outs[2]), Im) <= TOL[torch.bfloat16] * scale
+    gs = xs["dY"]
+    gscale = float(np.max(np.abs(gs)))
+    assert _err(_np(grads[0]), po.rope_bwd(gs, 1e4)) <= TOL[torch.bfloat16] * gscale
+    dI, dthr = po.givens_bwd(gs, _np(outs[2]), theta.double().numpy(), 1)
+    assert _err(_np(grads[2]), dI) <= TOL[torch.bfloat16] * gscale
+    assert _err(dth.cpu().numpy(), dthr) <= DTH_TOL[torch.bfloat16] * max(1.0, float(np.max(np.abs(dthr))))
