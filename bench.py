@@ -402,7 +402,10 @@ def run_linear(args, w):
         "breakdown_ms": {"fwd": statistics.mean(tf), "bwd": statistics.mean(tb)},
         "roofline": {"kernel": "relation_linear_fwd + relation_linear_bwd (all launches)", "bound": "hbm",
                      "achieved": gbs, "peak": hbm[0], "unit": "GB/s", "frac": gbs / hbm[0],
-                     "peak_source": hbm[1], "traffic": None,
+                     "peak_source": hbm[1],
+                     "traffic": recorded_traffic(f"linear fwd+bwd step, {w.name}",
+                                                 kernel_source_hash(["linear.cu", "common.cuh", "ptx_sm100.cuh",
+                                                                     "tile_copy.cuh"])),
                      "algorithmic_bytes_per_head_token": linear_bytes_per_head_token(w.d)},
         "gpu_launches": launches[0],
         "e2e": e2e,
