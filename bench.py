@@ -313,10 +313,13 @@ def run_linear(args, w):
 
     from relation_token_mixing_gb300 import binding as rb
     from relation_token_mixing_gb300 import inputs as rin
+    from relation_token_mixing_gb300 import replicas as rrep
 
-    rb.load()
-    dev = torch.device("cuda", 0)
+    ranks = rrep.from_env()
+    dev = torch.device("cuda", ranks.local)
     torch.cuda.set_device(dev)
+    rrep.init(ranks, "nccl")
+    rb.load()
     x_cpu = rin.make_linear(w)
     x = {k: v.to(dev) for k, v in x_cpu.items()}
     prob = rb.problem_for(x["P1"], w.tau_S, 0.0, True)
@@ -346,20 +349,23 @@ def run_linear(args, w):
         raise RuntimeError("device-side wait expired during warm-up")
     evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     launches[0] = 0
-    with ClockSampler(0) as clk:
+    rrep.barrier(ranks)
+    torch.cuda.synchronize()
+    with ClockSampler(ranks.local) as clk:
         for k in range(args.steps):
             flush.zero_()
             step(evsets[k])
         torch.cuda.synchronize()
+    rrep.barrier(ranks)
     if rb.relation_check_device_status() != 0:
         raise RuntimeError("device-side wait expired during the timed region")
     tf = [e[0].elapsed_time(e[1]) for e in evsets]
     tb = [e[1].elapsed_time(e[2]) for e in evsets]
-    ms = statistics.mean(tf) + statistics.mean(tb)
+    ms = rrep.max_over_ranks(ranks, statistics.mean(tf) + statistics.mean(tb), dev)
     tokens = w.B * w.T
-    value = tokens / (ms * 1e-3)
+    value = rrep.job_rate(ranks, tokens, ms * 1e-3)
     step_bytes = linear_bytes_per_head_token(w.d) * w.B * w.H * w.T
-    gbs = step_bytes / (ms * 1e-3) / 1e9
+    gbs = step_bytes / (ms * 1e-3) / 1e9  # per GPU: the roofline is one device's
     hbm = load_peaks_hbm()
 
     e2e = None
@@ -386,19 +392,24 @@ def run_linear(args, w):
             b.record(stream)
             b.synchronize()
             e_ms += a.elapsed_time(b)
-        e2e = {"value": tokens * args.steps / (e_ms * 1e-3), "unit": "tok/s",
+        e_ms = rrep.max_over_ranks(ranks, e_ms, dev)
+        e2e = {"value": rrep.job_rate(ranks, tokens * args.steps, e_ms * 1e-3), "unit": "tok/s",
                "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in h_in.values()),
                "d2h_bytes_per_step": sum(v.numel() * v.element_size() for v in h_out)}
 
+    if ranks.rank != 0:
+        rrep.finish(ranks)
+        return 0
     line = {
         "metric": "Linear Relation fwd+bwd tokens per second (bf16 operands, fp32 state)",
-        "value": value, "unit": "tok/s", "n_gpus": 1, "steps": args.steps, "warmup": max(3, args.warmup),
+        "value": value, "unit": "tok/s", "n_gpus": ranks.world, "steps": args.steps, "warmup": max(3, args.warmup),
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16 operands, f32 state and accumulation",
         "data": "synthetic (seeded Gaussian P1, P2, I~, dY; log-retention G with the statistics of its "
                 "initialisation), resident in HBM",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d_h": w.d, "tau_S": w.tau_S,
-                   "g_scale": w.g_scale, "l2": "flushed between timed steps"},
+                   "g_scale": w.g_scale, "parallelism": f"independent heads, {ranks.world} replica(s)",
+                   "l2": "flushed between timed steps"},
         "breakdown_ms": {"fwd": statistics.mean(tf), "bwd": statistics.mean(tb)},
         "roofline": {"kernel": "relation_linear_fwd + relation_linear_bwd (all launches)", "bound": "hbm",
                      "achieved": gbs, "peak": hbm[0], "unit": "GB/s", "frac": gbs / hbm[0],
@@ -411,7 +422,7 @@ def run_linear(args, w):
         "e2e": e2e,
         "clocks": clk.summary(),
     }
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and ranks.world == 1:
         try:
             rate, heads, dt = linear_cpu_sample(w, 10.0)
             line["cpu_baseline"] = {"value": rate / w.H, "unit": "tok/s", "cores": 1, "kind": "oracle",
@@ -421,6 +432,7 @@ def run_linear(args, w):
             line["cpu_baseline"] = {"value": None, "unit": "tok/s", "cores": None, "kind": "oracle",
                                     "sample": f"failed: {exc}"}
     print(json.dumps(line), flush=True)
+    rrep.finish(ranks)
     return 0
 
 
@@ -509,16 +521,15 @@ def main():
         return run_prologue(args, w)
 
     import torch
-    import torch.distributed as dist
 
     from relation_token_mixing_gb300 import binding as rb
+    from relation_token_mixing_gb300 import replicas as rrep
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
+    ranks = rrep.from_env()
+    world, rank, local = ranks.world, ranks.rank, ranks.local
+    if ranks.distributed:
         torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+    rrep.init(ranks, "nccl")
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     rb.load()
@@ -568,16 +579,14 @@ def main():
 
     ev_sets = [[ev() for _ in range(5)] for _ in range(args.steps)]
     launches[0] = 0
-    if world > 1:
-        dist.barrier()
+    rrep.barrier(ranks)
     torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device()) as clk:
         for k in range(args.steps):
             flush.zero_()  # evict L2 between timed steps (outside the events)
             step(ev_sets[k])
         torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
+    rrep.barrier(ranks)
     if rb.relation_check_device_status() != 0:
         raise RuntimeError("device-side wait expired during the timed region")
     timed_launches = launches[0]
@@ -587,15 +596,11 @@ def main():
     t_prep = [e[1].elapsed_time(e[2]) for e in ev_sets]
     t_main = [e[2].elapsed_time(e[3]) for e in ev_sets]
     t_fin = [e[3].elapsed_time(e[4]) for e in ev_sets]
-    total_ms = sum(t_step)
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = rrep.max_over_ranks(ranks, sum(t_step), dev)
     ms_per_step = total_ms / args.steps
     f_fwd, f_bwd = flops(w, 4), flops(w, 8)
-    value = world * (f_fwd + f_bwd) * args.steps / (total_ms * 1e-3) / 1e12
-    executed = world * flops(w, 14) * args.steps / (total_ms * 1e-3) / 1e12
+    value = rrep.job_rate(ranks, (f_fwd + f_bwd) * args.steps, total_ms * 1e-3) / 1e12
+    executed = rrep.job_rate(ranks, flops(w, 14) * args.steps, total_ms * 1e-3) / 1e12
 
     # e2e: same step through the C ABI with host buffers (pinned), copies inside the timed region.
     e2e = None
@@ -629,18 +634,14 @@ def main():
             b.record(stream)
             b.synchronize()
             e_ms += a.elapsed_time(b)
-        if world > 1:
-            tt = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e_ms = float(tt.item())
+        e_ms = rrep.max_over_ranks(ranks, e_ms, dev)
         h2d = sum(v.numel() * v.element_size() for v in h_in.values())
         d2h = sum(v.numel() * v.element_size() for v in h_out.values()) + 4
-        e2e = {"value": world * (f_fwd + f_bwd) * args.steps / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": rrep.job_rate(ranks, (f_fwd + f_bwd) * args.steps, e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     if rank != 0:
-        if world > 1:
-            dist.destroy_process_group()
+        rrep.finish(ranks)
         return 0
 
     peak_burst, peak_sust, peak_src = load_peaks()
@@ -695,8 +696,7 @@ def main():
             line["cpu_baseline"] = {"value": None, "unit": "TFLOP/s", "cores": None, "kind": "oracle",
                                     "sample": f"failed: {exc}"}
     print(json.dumps(line))
-    if world > 1:
-        dist.destroy_process_group()
+    rrep.finish(ranks)
     return 0
 
 
