@@ -544,6 +544,7 @@ def main():
     dP1, dP2, dV = torch.empty_like(P1), torch.empty_like(P2), torch.empty_like(V)
     dlam = torch.empty(1, dtype=torch.float32, device=dev)
     ws = torch.empty((rb.relation_bwd_workspace_bytes(prob) + 3) // 4, dtype=torch.float32, device=dev)
+    fws = rb.fwd_workspace(prob, dev)  # None unless the head width needs padded copies (d_h = 60)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -553,7 +554,7 @@ def main():
     def step(events=None):
         if events:
             events[0].record(stream)
-        rb.relation_fwd(prob, P1, P2, V, Y, L, stream)
+        rb.relation_fwd_ws(prob, P1, P2, V, Y, L, fws, stream)
         launches[0] += rb.relation_last_launch_count()
         if events:
             events[1].record(stream)
@@ -647,13 +648,14 @@ def main():
     peak_burst, peak_sust, peak_src = load_peaks()
     mean_fwd, mean_main = statistics.mean(t_fwd), statistics.mean(t_main)
     # Kernels by head width: 48, 60 and 64 run the 64-wide tensor-core kernels, 80 and
-    # 128 the 128-wide ones (zero-padded tiles); 60 loads its tiles with cp.async.
-    tile, cp = (64 if w.d <= 64 else 128), w.d == 60
-    srcs_common = ["ptx_sm100.cuh", "common.cuh"] + (["tile_copy.cuh"] if cp else [])
-    fwd_k = f"relation_fwd_tc_kernel<{tile}, {'true' if cp else 'false'}>"
+    # 128 the 128-wide ones (zero-padded tiles); 60 reads zero-padded copies of its
+    # operands (made by one extra launch in the forward and one in the backward).
+    tile = 64 if w.d <= 64 else 128
+    srcs_common = ["ptx_sm100.cuh", "common.cuh", "tile_copy.cuh"]
+    fwd_k = f"relation_fwd_tc_kernel<{tile}, false>"
     fwd_src = ["fwd_tc.cu"] + srcs_common
     if tile == 64:
-        bwd_k, bwd_src = f"relation_bwd_tc64_kernel<{2 if cp else 0}>", ["bwd_tc64.cu"] + srcs_common
+        bwd_k, bwd_src = "relation_bwd_tc64_kernel<0>", ["bwd_tc64.cu"] + srcs_common
     else:
         bwd_k, bwd_src = "relation_bwd_tc_kernel<128>", ["bwd_tc.cu"] + srcs_common
     if mean_main >= mean_fwd:

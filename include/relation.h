@@ -87,6 +87,25 @@ typedef struct {
 relation_status_t relation_fwd(const relation_problem_t* p, const void* P1, const void* P2,
                                const void* V, void* Y, float* L, void* stream);
 
+/*
+ * The same forward with a caller-owned device workspace, for head widths whose
+ * rows the tensor memory accelerator cannot step through (bf16 d_h = 60: rows
+ * of 120 bytes, not a multiple of 16).  For those, one extra launch first
+ * writes zero-padded contiguous [B*H, T, 64] copies of P1, P2 and V into the
+ * workspace, and the forward reads its tiles from them; Y and L are written
+ * exactly as relation_fwd writes them (the problem's layout and width), and
+ * the results are identical to relation_fwd's.  Every other problem needs no
+ * workspace: then this equals relation_fwd and workspace may be NULL.
+ * relation_fwd_workspace_bytes(p) is the size needed (0 = none, or p invalid).
+ * workspace: 16-byte aligned, contents ignored on entry, must not overlap any
+ * input or output.  Errors as relation_fwd, plus
+ * RELATION_ERR_WORKSPACE_TOO_SMALL.
+ */
+size_t relation_fwd_workspace_bytes(const relation_problem_t* p);
+relation_status_t relation_fwd_ws(const relation_problem_t* p, const void* P1, const void* P2,
+                                  const void* V, void* Y, float* L, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
 /* Bytes of float32 workspace relation_bwd needs for problem p (0 if p is invalid). */
 size_t relation_bwd_workspace_bytes(const relation_problem_t* p);
 

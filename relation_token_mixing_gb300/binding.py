@@ -79,6 +79,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib = ctypes.CDLL(_build.LIB)
         lib.relation_fwd.argtypes = [ctypes.POINTER(Problem), _VP, _VP, _VP, _VP, _VP, _VP]
         lib.relation_fwd.restype = ctypes.c_int
+        lib.relation_fwd_workspace_bytes.argtypes = [ctypes.POINTER(Problem)]
+        lib.relation_fwd_workspace_bytes.restype = ctypes.c_size_t
+        lib.relation_fwd_ws.argtypes = [ctypes.POINTER(Problem), _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_size_t, _VP]
+        lib.relation_fwd_ws.restype = ctypes.c_int
         for name in ("relation_bwd", "relation_bwd_prepare", "relation_bwd_main", "relation_bwd_finish"):
             getattr(lib, name).argtypes = _BWD_ARGTYPES
             getattr(lib, name).restype = ctypes.c_int
@@ -176,6 +180,16 @@ def relation_fwd(prob: Problem, P1, P2, V, Y, L=None, stream=None) -> None:
                                _stream_ptr(stream)), "relation_fwd")
 
 
+def relation_fwd_workspace_bytes(prob: Problem) -> int:
+    return int(load().relation_fwd_workspace_bytes(ctypes.byref(prob)))
+
+
+def relation_fwd_ws(prob: Problem, P1, P2, V, Y, L=None, workspace=None, stream=None) -> None:
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().relation_fwd_ws(ctypes.byref(prob), _ptr(P1), _ptr(P2), _ptr(V), _ptr(Y), _ptr(L), _ptr(workspace),
+                                  nbytes, _stream_ptr(stream)), "relation_fwd_ws")
+
+
 def relation_bwd_workspace_bytes(prob: Problem) -> int:
     return int(load().relation_bwd_workspace_bytes(ctypes.byref(prob)))
 
@@ -271,13 +285,26 @@ def relation_abi_version() -> int:
 
 
 # ------------------------------------------------------- tensor-level helpers
+def fwd_workspace(prob: Problem, device):
+    """Workspace tensor for relation_fwd_ws, or None when the problem needs none."""
+    n = relation_fwd_workspace_bytes(prob)
+    return torch.empty((n + 3) // 4, dtype=torch.float32, device=device) if n else None
+
+
 def fwd(P1, P2, V, tau_S: float, lam: float, causal: bool = True, stream=None, want_L: bool = True,
-        layout: int = RELATION_LAYOUT_BHTD):
-    """Allocates Y (and L [B, H, T]) and runs relation_fwd; returns (Y, L)."""
+        layout: int = RELATION_LAYOUT_BHTD, workspace=None, use_workspace: bool = True):
+    """Allocates Y (and L [B, H, T]) and runs the forward; returns (Y, L).  Head widths that
+    need a workspace (bf16 d_h = 60) get one (allocated here unless given) and run through
+    relation_fwd_ws; use_workspace=False runs relation_fwd instead."""
     prob = problem_for(P1, tau_S, lam, causal, layout)
     Y = torch.empty_like(V)
     L = torch.empty((prob.B, prob.H, prob.T), dtype=torch.float32, device=P1.device) if want_L else None
-    relation_fwd(prob, P1, P2, V, Y, L, stream)
+    if use_workspace and relation_fwd_workspace_bytes(prob):
+        if workspace is None:
+            workspace = fwd_workspace(prob, P1.device)
+        relation_fwd_ws(prob, P1, P2, V, Y, L, workspace, stream)
+    else:
+        relation_fwd(prob, P1, P2, V, Y, L, stream)
     return Y, L
 
 

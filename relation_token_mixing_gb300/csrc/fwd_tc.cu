@@ -547,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, bool kCp>
 cudaError_t launch_fwd_tc_d(const KernelProblem& kp, const void* P1, const void* P2, const void* V, void* Y,
-                            float* L, const TcLaunch& tl, cudaStream_t s) {
+                            float* L, const TcLaunch& tl, cudaStream_t s, bool padded64 = false) {
     using C = FwdCfg<D>;
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
@@ -557,13 +557,17 @@ cudaError_t launch_fwd_tc_d(const KernelProblem& kp, const void* P1, const void*
     });
     if (attr_err != cudaSuccess) return attr_err;
     // Heads narrower than D read as D-wide tiles whose extra columns are zero.
+    // Padded copies are contiguous [B, H, T, 64] whatever the caller's layout;
+    // Y and L are still written in the caller's layout and width.
     CUtensorMap m1{}, m2{}, mv{};  // unused by the cp.async producer
     if (!kCp) {
         cudaError_t e;
         const int64_t B = kp.BH / kp.H;
-        if ((e = make_operand_map(&m1, P1, B, kp.H, kp.T, kp.d, kp.layout, 64, 128, false)) != cudaSuccess) return e;
-        if ((e = make_operand_map(&m2, P2, B, kp.H, kp.T, kp.d, kp.layout, 64, 128, false)) != cudaSuccess) return e;
-        if ((e = make_operand_map(&mv, V, B, kp.H, kp.T, kp.d, kp.layout, 64, 128, false)) != cudaSuccess) return e;
+        const int64_t md = padded64 ? 64 : kp.d;
+        const int ml = padded64 ? 0 : kp.layout;
+        if ((e = make_operand_map(&m1, P1, B, kp.H, kp.T, md, ml, 64, 128, false)) != cudaSuccess) return e;
+        if ((e = make_operand_map(&m2, P2, B, kp.H, kp.T, md, ml, 64, 128, false)) != cudaSuccess) return e;
+        if ((e = make_operand_map(&mv, V, B, kp.H, kp.T, md, ml, 64, 128, false)) != cudaSuccess) return e;
     }
     const unsigned pairs = (unsigned)((kp.T + 2 * kBM - 1) / (2 * kBM));
     dim3 grid((unsigned)kp.BH, pairs);
@@ -576,8 +580,12 @@ cudaError_t launch_fwd_tc_d(const KernelProblem& kp, const void* P1, const void*
 }  // namespace
 
 cudaError_t launch_fwd_tc(const KernelProblem& kp, const void* P1, const void* P2, const void* V, void* Y, float* L,
-                          const TcLaunch& tl, cudaStream_t s) {
+                          const TcLaunch& tl, cudaStream_t s, bool padded64) {
     if (kp.BH > 2147483647LL) return cudaErrorInvalidValue;
+    if (padded64) {
+        if (kp.d > 64) return cudaErrorInvalidValue;
+        return launch_fwd_tc_d<64, false>(kp, P1, P2, V, Y, L, tl, s, true);
+    }
     if (kp.d == 48 || kp.d == 64) return launch_fwd_tc_d<64, false>(kp, P1, P2, V, Y, L, tl, s);
     if (kp.d == 60) return launch_fwd_tc_d<64, true>(kp, P1, P2, V, Y, L, tl, s);  // 120-byte rows: no TMA
     if (kp.d == 80 || kp.d == 128) return launch_fwd_tc_d<128, false>(kp, P1, P2, V, Y, L, tl, s);

@@ -17,9 +17,11 @@ cudaError_t launch_bwd_simt(const KernelProblem& kp, bool bf16, const void* P1, 
 
 // Shared backward stages.
 // dq_acc (optional) is the fp32 dP1 accumulator [BH, T, dq_w]; it is zeroed.
+// pad_dst (bf16, d_h <= 64, dlambda summed elsewhere): also write zero-padded
+// contiguous [BH, T, 64] copies of P1, P2, V, dY to pad_dst[0..3] in the same pass.
 cudaError_t launch_bwd_prepare(const KernelProblem& kp, bool bf16, const void* P1, const void* P2, const void* V,
                                const void* Y, const float* L, const void* dY, float* Dw, float* dq_acc, int dq_w,
-                               float* dlambda, cudaStream_t s);
+                               float* dlambda, cudaStream_t s, void* const* pad_dst = nullptr, int num_sms = 0);
 // Input prologue.  RoPE frequencies base^(-2c/d) / (2 pi), c < d/2, as float
 // pairs hi + lo (enabled = 0: no rotation, a copy).
 struct RopeTable {
@@ -66,8 +68,10 @@ struct TcLaunch {
     int num_sms;
     unsigned int* status;
 };
+// padded64: P1, P2, V point to zero-padded contiguous [BH, T, 64] copies (d <= 64);
+// Y and L are written in the problem's layout and width.
 cudaError_t launch_fwd_tc(const KernelProblem& kp, const void* P1, const void* P2, const void* V, void* Y, float* L,
-                          const TcLaunch& tl, cudaStream_t s);
+                          const TcLaunch& tl, cudaStream_t s, bool padded64 = false);
 // Whether the tensor-core backward kernel for this head width also sums dlambda.
 inline bool bwd_tc_sums_dlambda(int d) { return d <= 64; }  // the 64-wide kernel serves d = 48, 60, 64
 // padded64: P1, P2, V, dY point to zero-padded contiguous [BH, T, 64] copies

@@ -182,18 +182,17 @@ relation_status_t run_prepare(const BwdArgs& a, int* launches) {
     const KernelProblem kp = kernel_problem(a.p);
     // dlambda is summed by the main pass where that kernel does it, else here.
     float* dlam_here = (use_tensor_cores(a.p) && bwd_tc_sums_dlambda(kp.d)) ? nullptr : a.dlambda;
-    relation_status_t st = from_cuda(launch_bwd_prepare(kp, a.p->dtype == RELATION_BF16, a.P1, a.P2, a.V, a.Y, a.L,
-                                                        a.dY, Dw, dq, dq_width(a.p), dlam_here, a.stream));
+    DeviceInfo di;
+    relation_status_t st = device_info(&di);
+    if (st != RELATION_OK) return st;
+    // Widths whose rows TMA cannot step through also get their padded operand
+    // copies here, in the same pass.
+    void* pad[4];
+    if (pads_operands(a.p)) padded_operands(a.p, a.workspace, pad);
+    st = from_cuda(launch_bwd_prepare(kp, a.p->dtype == RELATION_BF16, a.P1, a.P2, a.V, a.Y, a.L, a.dY, Dw, dq,
+                                      dq_width(a.p), dlam_here, a.stream, pads_operands(a.p) ? pad : nullptr,
+                                      di.num_sms));
     if (st == RELATION_OK) *launches += 1;
-    if (st == RELATION_OK && pads_operands(a.p)) {
-        DeviceInfo di;
-        if ((st = device_info(&di)) != RELATION_OK) return st;
-        const void* src[4] = {a.P1, a.P2, a.V, a.dY};
-        void* dst[4];
-        padded_operands(a.p, a.workspace, dst);
-        st = from_cuda(launch_pad_operands(kp, src, dst, 4, di.num_sms, a.stream));
-        if (st == RELATION_OK) *launches += 1;
-    }
     return st;
 }
 
@@ -227,6 +226,62 @@ relation_status_t run_main(const BwdArgs& a, int* launches) {
     return st;
 }
 
+// Forward workspace (relation_fwd_ws): the padded copies of P1, P2, V [rows, 64]
+// bf16, each 256-byte aligned, for widths whose rows TMA cannot step through.
+size_t fwd_workspace_bytes(const relation_problem_t* p) {
+    return pads_operands(p) ? 3 * round_up(rows_of(p) * 64 * 2, 256) : 0;
+}
+
+relation_status_t run_fwd(const relation_problem_t* p, const void* P1, const void* P2, const void* V, void* Y,
+                          float* L, void* workspace, size_t workspace_bytes, bool with_ws, cudaStream_t s) {
+    relation_status_t st = check_problem(p);
+    if (st != RELATION_OK) return st;
+    if (!P1 || !P2 || !V || !Y) return RELATION_ERR_INVALID_ARGUMENT;
+    if (!aligned16(P1) || !aligned16(P2) || !aligned16(V) || !aligned16(Y) || (L && !aligned16(L)))
+        return RELATION_ERR_MISALIGNED;
+    const size_t need = with_ws ? fwd_workspace_bytes(p) : 0;
+    if (need > 0) {
+        if (workspace == nullptr) return RELATION_ERR_INVALID_ARGUMENT;
+        if (!aligned16(workspace)) return RELATION_ERR_MISALIGNED;
+    }
+    const size_t tb = tensor_bytes(p), lb = rows_of(p) * sizeof(float);
+    const void* ins[] = {P1, P2, V};
+    for (const void* x : ins) {
+        if (overlaps(Y, tb, x, tb)) return RELATION_ERR_INVALID_ARGUMENT;
+        if (L && overlaps(L, lb, x, tb)) return RELATION_ERR_INVALID_ARGUMENT;
+        if (need > 0 && overlaps(workspace, need, x, tb)) return RELATION_ERR_INVALID_ARGUMENT;
+    }
+    if (L && overlaps(L, lb, Y, tb)) return RELATION_ERR_INVALID_ARGUMENT;
+    if (need > 0 && (overlaps(workspace, need, Y, tb) || (L && overlaps(workspace, need, L, lb))))
+        return RELATION_ERR_INVALID_ARGUMENT;
+    if (workspace_bytes < need) return RELATION_ERR_WORKSPACE_TOO_SMALL;
+    const KernelProblem kp = kernel_problem(p);
+    int launches = 0;
+    if (use_tensor_cores(p)) {
+        DeviceInfo di;
+        st = device_info(&di);
+        if (st != RELATION_OK) return st;
+        TcLaunch tl{di.num_sms, di.status};
+        if (need > 0) {
+            const void* src[3] = {P1, P2, V};
+            void* dst[3];
+            const size_t each = round_up(rows_of(p) * 64 * 2, 256);
+            for (int k = 0; k < 3; ++k) dst[k] = static_cast<char*>(workspace) + k * each;
+            st = from_cuda(launch_pad_operands(kp, src, dst, 3, di.num_sms, s));
+            if (st == RELATION_OK) {
+                launches += 1;
+                st = from_cuda(launch_fwd_tc(kp, dst[0], dst[1], dst[2], Y, L, tl, s, true));
+            }
+        } else {
+            st = from_cuda(launch_fwd_tc(kp, P1, P2, V, Y, L, tl, s));
+        }
+    } else {
+        st = from_cuda(launch_fwd_simt(kp, p->dtype == RELATION_BF16, P1, P2, V, Y, L, s));
+    }
+    if (st == RELATION_OK) t_last_launches = launches + 1;
+    return st;
+}
+
 relation_status_t run_finish(const BwdArgs& a, int* launches) {
     if (!use_tensor_cores(a.p)) return RELATION_OK;  // the CUDA-core path writes dP1 directly
     size_t dq_off = 0;
@@ -249,31 +304,17 @@ extern "C" {
 
 relation_status_t relation_fwd(const relation_problem_t* p, const void* P1, const void* P2, const void* V, void* Y,
                                float* L, void* stream) {
-    relation_status_t st = check_problem(p);
-    if (st != RELATION_OK) return st;
-    if (!P1 || !P2 || !V || !Y) return RELATION_ERR_INVALID_ARGUMENT;
-    if (!aligned16(P1) || !aligned16(P2) || !aligned16(V) || !aligned16(Y) || (L && !aligned16(L)))
-        return RELATION_ERR_MISALIGNED;
-    const size_t tb = tensor_bytes(p), lb = rows_of(p) * sizeof(float);
-    const void* ins[] = {P1, P2, V};
-    for (const void* x : ins) {
-        if (overlaps(Y, tb, x, tb)) return RELATION_ERR_INVALID_ARGUMENT;
-        if (L && overlaps(L, lb, x, tb)) return RELATION_ERR_INVALID_ARGUMENT;
-    }
-    if (L && overlaps(L, lb, Y, tb)) return RELATION_ERR_INVALID_ARGUMENT;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const KernelProblem kp = kernel_problem(p);
-    if (use_tensor_cores(p)) {
-        DeviceInfo di;
-        st = device_info(&di);
-        if (st != RELATION_OK) return st;
-        TcLaunch tl{di.num_sms, di.status};
-        st = from_cuda(launch_fwd_tc(kp, P1, P2, V, Y, L, tl, s));
-    } else {
-        st = from_cuda(launch_fwd_simt(kp, p->dtype == RELATION_BF16, P1, P2, V, Y, L, s));
-    }
-    if (st == RELATION_OK) t_last_launches = 1;
-    return st;
+    return run_fwd(p, P1, P2, V, Y, L, nullptr, 0, false, static_cast<cudaStream_t>(stream));
+}
+
+size_t relation_fwd_workspace_bytes(const relation_problem_t* p) {
+    if (check_problem(p) != RELATION_OK) return 0;
+    return fwd_workspace_bytes(p);
+}
+
+relation_status_t relation_fwd_ws(const relation_problem_t* p, const void* P1, const void* P2, const void* V, void* Y,
+                                  float* L, void* workspace, size_t workspace_bytes, void* stream) {
+    return run_fwd(p, P1, P2, V, Y, L, workspace, workspace_bytes, true, static_cast<cudaStream_t>(stream));
 }
 
 size_t relation_bwd_workspace_bytes(const relation_problem_t* p) {

@@ -202,6 +202,54 @@ __global__ void __launch_bounds__(256) bwd_prepare_bf16_kernel(int64_t rows, con
     if (row < rows && part == 0) Dout[row] = acc;
 }
 
+// bf16 rows of width d <= 64 (d % 4 == 0), either layout, dlambda summed
+// elsewhere: D_i = dY_i . Y_i, the row's 64-wide fp32 dP1 accumulator zeroed
+// and, when pad.dst[0] is set, the row written zero-padded to 64 columns into
+// contiguous [BH, T, 64] copies of P1, P2, V, dY (in that order) in the same
+// pass.  16 threads per row, thread u owning columns 4u .. 4u+3 (8 bytes); a
+// warp holds two rows, so the reduction stays inside each half-warp.
+struct PrepPad {
+    const uint2* src[3];  // P1, P2, V
+    uint2* dst[4];        // P1, P2, V, dY copies; dst[0] == nullptr: no copies
+};
+__global__ void __launch_bounds__(256) bwd_prepare_narrow_kernel(KernelProblem kp, int64_t rows,
+                                                                 const uint2* __restrict__ Y,
+                                                                 const uint2* __restrict__ dY,
+                                                                 float* __restrict__ Dout, float4* __restrict__ dq4,
+                                                                 PrepPad pad) {
+    const int u = threadIdx.x & 15;
+    const unsigned half = 0xffffu << (threadIdx.x & 16);
+    const int units = kp.d >> 2;
+    const bool copies = pad.dst[0] != nullptr;
+    const uint2 zero = make_uint2(0u, 0u);
+    const int64_t step = (int64_t)gridDim.x * (blockDim.x >> 4);
+    for (int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 4; row < rows; row += step) {
+        // Contiguous rows need no division: row r starts at r * d elements.
+        const size_t base = (kp.layout == 0 ? (size_t)row * (size_t)kp.d : row_offset(kp, row / kp.T, row % kp.T)) / 4;
+        uint2 g = zero;
+        float acc = 0.f;
+        if (u < units) {
+            g = dY[base + u];
+            const uint2 y = Y[base + u];
+            const float2 g0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g.x));
+            const float2 g1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g.y));
+            const float2 y0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&y.x));
+            const float2 y1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&y.y));
+            acc = fmaf(g0.x, y0.x, fmaf(g0.y, y0.y, fmaf(g1.x, y1.x, g1.y * y1.y)));
+        }
+        const int64_t out = row * 16 + u;
+        dq4[out] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (copies) {
+            pad.dst[3][out] = g;
+#pragma unroll
+            for (int k = 0; k < 3; ++k) pad.dst[k][out] = u < units ? pad.src[k][base + u] : zero;
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(half, acc, o);
+        if (u == 0) Dout[row] = acc;
+    }
+}
+
 // Relation entry r_ij and its slope dr/du for zero-based (i, j), j visible.
 __device__ __forceinline__ void relation_entry(const KernelProblem& kp, int i, int j, float u, float corr,
                                                float* r, float* slope) {
@@ -385,22 +433,27 @@ __global__ void __launch_bounds__(256) convert_rows_kernel(KernelProblem kp, con
 }
 
 // Operand rows of width d (any layout) -> zero-padded contiguous [BH, T, 64]
-// bf16 copies (operand blockIdx.y of the four), one thread per 8-byte unit.
+// bf16 copies (operand blockIdx.y of the n), one thread per 16-byte unit of the
+// copy (two 8-byte units of the source row; d is a multiple of 4).
 struct PadArgs {
     const uint2* src[4];
-    uint2* dst[4];
+    uint4* dst[4];
 };
 __global__ void __launch_bounds__(256) pad_operands_kernel(KernelProblem kp, PadArgs a, int64_t units) {
     const uint2* __restrict__ src = a.src[blockIdx.y];
-    uint2* __restrict__ dst = a.dst[blockIdx.y];
-    const int src_units = kp.d / 4;  // d is a multiple of 4
+    uint4* __restrict__ dst = a.dst[blockIdx.y];
+    const int src_units = kp.d / 4;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < units; k += stride) {
-        const int64_t row = k >> 4;
-        const int u = (int)(k & 15);
-        uint2 v = make_uint2(0u, 0u);
-        if (u < src_units) v = src[row_offset(kp, row / kp.T, row % kp.T) / 4 + u];
-        dst[k] = v;
+        const int64_t row = k >> 3;
+        const int u = 2 * (int)(k & 7);
+        // Contiguous rows need no division: row r starts at r * d elements.
+        const uint2* s = src + (kp.layout == 0 ? (size_t)row * (size_t)src_units
+                                               : row_offset(kp, row / kp.T, row % kp.T) / 4);
+        uint2 lo = make_uint2(0u, 0u), hi = make_uint2(0u, 0u);
+        if (u < src_units) lo = s[u];
+        if (u + 1 < src_units) hi = s[u + 1];
+        dst[k] = make_uint4(lo.x, lo.y, hi.x, hi.y);
     }
 }
 
@@ -462,8 +515,28 @@ cudaError_t launch_bwd_simt(const KernelProblem& kp, bool bf16, const void* P1, 
 
 cudaError_t launch_bwd_prepare(const KernelProblem& kp, bool bf16, const void* P1, const void* P2, const void* V,
                                const void* Y, const float* L, const void* dY, float* Dw, float* dq_acc, int dq_w,
-                               float* dlambda, cudaStream_t s) {
+                               float* dlambda, cudaStream_t s, void* const* pad_dst, int num_sms) {
     const int64_t rows = kp.BH * kp.T;
+    // Narrow bf16 rows (and the padded copies, when asked for) in one pass.
+    const bool narrow = bf16 && dlambda == nullptr && dq_acc != nullptr && dq_w == 64 && kp.d <= 64 &&
+                        (kp.d & 3) == 0 && !(kp.layout == 0 && kp.d == 64);
+    if (pad_dst != nullptr && !narrow) return cudaErrorInvalidValue;
+    if (narrow) {
+        PrepPad pad{};
+        if (pad_dst != nullptr) {
+            pad.src[0] = static_cast<const uint2*>(P1);
+            pad.src[1] = static_cast<const uint2*>(P2);
+            pad.src[2] = static_cast<const uint2*>(V);
+            for (int k = 0; k < 4; ++k) pad.dst[k] = static_cast<uint2*>(pad_dst[k]);
+        }
+        int64_t blocks = (rows + 15) / 16;
+        const int64_t cap = (int64_t)(num_sms > 0 ? num_sms : 1) * 16;
+        if (blocks > cap) blocks = cap;
+        if (blocks < 1) blocks = 1;
+        bwd_prepare_narrow_kernel<<<(unsigned)blocks, 256, 0, s>>>(kp, rows, (const uint2*)Y, (const uint2*)dY, Dw,
+                                                                     (float4*)dq_acc, pad);
+        return cudaGetLastError();
+    }
     // Vector path: contiguous [B, H, T, d] rows whose width is the accumulator's.
     if (bf16 && dlambda == nullptr && dq_acc != nullptr && kp.layout == 0 && kp.d == dq_w &&
         (kp.d == 64 || kp.d == 128)) {
@@ -495,11 +568,11 @@ cudaError_t launch_pad_operands(const KernelProblem& kp, const void* const* src,
     PadArgs a{};
     for (int k = 0; k < n; ++k) {
         a.src[k] = static_cast<const uint2*>(src[k]);
-        a.dst[k] = static_cast<uint2*>(dst[k]);
+        a.dst[k] = static_cast<uint4*>(dst[k]);
     }
-    const int64_t units = kp.BH * (int64_t)kp.T * 16;
+    const int64_t units = kp.BH * (int64_t)kp.T * 8;
     int64_t blocks = (units + 255) / 256;
-    const int64_t cap = (int64_t)num_sms * 4;
+    const int64_t cap = (int64_t)num_sms * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     pad_operands_kernel<<<dim3((unsigned)blocks, (unsigned)n), 256, 0, s>>>(kp, a, units);

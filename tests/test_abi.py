@@ -112,6 +112,37 @@ def test_workspace_size_and_backward_checks(lib):
         assert fn(ctypes.byref(p), *args, None, need, None) == 1
 
 
+def test_forward_workspace_size_and_checks(lib):
+    """relation_fwd_ws: only bf16 d_h = 60 needs a workspace (three zero-padded [rows, 64] bf16
+    copies); every call below fails its argument checks before any device call."""
+    rows = 2 * 3 * 100
+    p = _prob(d_h=60)
+    need = rb.relation_fwd_workspace_bytes(p)
+    assert need == 3 * ((rows * 64 * 2 + 255) // 256 * 256)
+    assert rb.relation_fwd_workspace_bytes(_prob(d_h=60, layout=rb.RELATION_LAYOUT_BTHD)) == need
+    for kw in (dict(d_h=48), dict(d_h=64), dict(d_h=80), dict(d_h=128), dict(d_h=60, dtype=rb.RELATION_F32),
+               dict(d_h=60, T=0), dict(d_h=50)):
+        assert rb.relation_fwd_workspace_bytes(_prob(**kw)) == 0
+    M = 1 << 20  # fake, 16-byte aligned addresses 1 MiB apart (each tensor here is 72,000 bytes)
+    P1, P2, V, Y, L, ws = M, 2 * M, 3 * M, 4 * M, 5 * M, 8 * M
+
+    def call(prob, ws=ws, nbytes=need, **kw):
+        a = dict(P1=P1, P2=P2, V=V, Y=Y, L=L)
+        a.update(kw)
+        return lib.relation_fwd_ws(ctypes.byref(prob), a["P1"], a["P2"], a["V"], a["Y"], a["L"], ws, nbytes, None)
+
+    assert call(p, ws=None) == 1                 # needed but missing
+    assert call(p, ws=ws + 8) == 3               # misaligned
+    assert call(p, ws=P1 + 4096) == 1            # overlaps an input
+    assert call(p, ws=Y - 16) == 1               # overlaps the output
+    assert call(p, ws=L - need + 16) == 1        # overlaps L
+    assert call(p, nbytes=need - 16) == 4        # too small
+    assert call(p, Y=None) == 1
+    assert call(p, V=V + 8) == 3
+    assert call(_prob(d_h=60, tau_S=0.0)) == 1
+    assert call(_prob(d_h=50)) == 2
+
+
 def _lfwd(lib, prob, P1=A, P2=2 * A, I=3 * A, G=4 * A, Y=8 * A, state=None, ws=16 * A):
     return lib.relation_linear_fwd(ctypes.byref(prob), P1, P2, I, G, Y, state, ws, 1 << 30, None)
 

@@ -67,7 +67,9 @@ def test_widths_and_layouts_match_oracle(w, layout):
     x_cpu = rin.make(w)
     x = {k: _to_layout(v, layout).cuda() for k, v in x_cpu.items()}
     Y, L = rb.fwd(x["P1"], x["P2"], x["V"], w.tau_S, w.lam, w.causal, layout=layout)
-    assert rb.relation_last_launch_count() == 1
+    prob = rb.problem_for(x["P1"], w.tau_S, w.lam, w.causal, layout)
+    # bf16 d_h = 60 pads its operands into the forward's workspace first (one more launch).
+    assert rb.relation_last_launch_count() == (2 if rb.relation_fwd_workspace_bytes(prob) else 1)
     dP1, dP2, dV, dlam = rb.bwd(x["P1"], x["P2"], x["V"], Y, L, x["dY"], w.tau_S, w.lam, w.causal, layout=layout)
     torch.cuda.synchronize()
     assert rb.relation_check_device_status() == 0
@@ -84,6 +86,45 @@ def test_widths_and_layouts_match_oracle(w, layout):
         err = _maxerr(_np(_from_layout(got, layout)), exp)
         assert err <= G_TOL[w.dtype] * gmax, (name, err, gmax)
     assert abs(float(dlam.item()) - ref[3]) <= 5 * G_TOL[w.dtype] * max(1.0, abs(ref[3]))
+
+
+@pytest.mark.parametrize("layout", [BHTD, BTHD])
+@pytest.mark.parametrize("T,causal", [(1, True), (130, True), (300, True), (257, False)])
+def test_forward_from_padded_copies_equals_direct_forward(T, causal, layout):
+    """d_h = 60: relation_fwd_ws (tiles loaded by TMA from the zero-padded copies in its
+    workspace) and relation_fwd (tiles copied from the caller's 120-byte rows by cp.async)
+    place the same zero-padded tile in shared memory, so Y and L agree bit for bit."""
+    w = rin.Workload("d60_ws", 2, 3, T, 60, torch.bfloat16, 2.0, 0.5, causal, 1.0)
+    x = {k: _to_layout(v, layout).cuda() for k, v in rin.make(w).items()}
+    prob = rb.problem_for(x["P1"], w.tau_S, w.lam, w.causal, layout)
+    Y0, L0 = torch.empty_like(x["V"]), torch.empty(w.B, w.H, w.T, device="cuda")
+    rb.relation_fwd(prob, x["P1"], x["P2"], x["V"], Y0, L0)
+    assert rb.relation_last_launch_count() == 1
+    ws = rb.fwd_workspace(prob, "cuda")
+    assert ws is not None and ws.numel() * 4 >= rb.relation_fwd_workspace_bytes(prob)
+    ws.fill_(float("nan"))  # contents on entry are ignored
+    Y1, L1 = torch.full_like(x["V"], float("nan")), torch.full((w.B, w.H, w.T), float("nan"), device="cuda")
+    rb.relation_fwd_ws(prob, x["P1"], x["P2"], x["V"], Y1, L1, ws)
+    assert rb.relation_last_launch_count() == 2
+    torch.cuda.synchronize()
+    assert rb.relation_check_device_status() == 0
+    assert torch.equal(Y0, Y1) and torch.equal(L0, L1)
+
+
+@pytest.mark.parametrize("d", [48, 64, 80])
+def test_forward_with_workspace_needs_none_elsewhere(d):
+    """Every other width: relation_fwd_ws takes no workspace and is relation_fwd."""
+    w = rin.Workload("nows", 1, 2, 200, d, torch.bfloat16, 1.0, 0.5, True, 1.0)
+    x = {k: v.cuda() for k, v in rin.make(w).items()}
+    prob = rb.problem_for(x["P1"], w.tau_S, w.lam, w.causal)
+    assert rb.relation_fwd_workspace_bytes(prob) == 0 and rb.fwd_workspace(prob, "cuda") is None
+    Y0, L0 = torch.empty_like(x["V"]), torch.empty(w.B, w.H, w.T, device="cuda")
+    Y1, L1 = torch.empty_like(x["V"]), torch.empty(w.B, w.H, w.T, device="cuda")
+    rb.relation_fwd(prob, x["P1"], x["P2"], x["V"], Y0, L0)
+    rb.relation_fwd_ws(prob, x["P1"], x["P2"], x["V"], Y1, L1, None)
+    assert rb.relation_last_launch_count() == 1
+    torch.cuda.synchronize()
+    assert torch.equal(Y0, Y1) and torch.equal(L0, L1)
 
 
 @pytest.mark.parametrize("d,layout", [(48, BHTD), (60, BHTD), (80, BHTD), (48, BTHD), (60, BTHD), (80, BTHD)])
@@ -103,12 +144,22 @@ def test_narrow_heads_write_only_their_tensors(d, layout):
     bY, Y = banded()
     L = torch.empty(w.B, w.H, w.T, device="cuda")
     rb.relation_fwd(prob, x["P1"], x["P2"], x["V"], Y, L)
+    banded_out = [(bY, Y)]
+    nws = rb.relation_fwd_workspace_bytes(prob)
+    if nws:  # the padded-copy forward, its workspace also between NaN guard bands
+        bY2, Y2 = banded()
+        wbuf = torch.full((nws // 4 + 2 * guard,), float("nan"), device="cuda")
+        rb.relation_fwd_ws(prob, x["P1"], x["P2"], x["V"], Y2, L, wbuf[guard:guard + nws // 4])
+        torch.cuda.synchronize()
+        assert torch.isnan(wbuf[:guard]).all() and torch.isnan(wbuf[guard + nws // 4:]).all()
+        assert torch.equal(Y2, Y)
+        banded_out.append((bY2, Y2))
     outs = [banded() for _ in range(3)]
     ws = torch.empty((rb.relation_bwd_workspace_bytes(prob) + 3) // 4, device="cuda")
     dlam = torch.empty(1, device="cuda")
     rb.relation_bwd(prob, x["P1"], x["P2"], x["V"], Y, L, x["dY"], outs[0][1], outs[1][1], outs[2][1], dlam, ws)
     torch.cuda.synchronize()
     assert rb.relation_check_device_status() == 0
-    for buf, inner in [(bY, Y)] + outs:
+    for buf, inner in banded_out + outs:
         assert torch.isnan(buf[:guard].float()).all() and torch.isnan(buf[guard + n:].float()).all()
         assert torch.isfinite(inner.float()).all()
