@@ -26,6 +26,24 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
+L2_CLEAN_BYTES = 256 << 20  # read after the flush, so that no dirty line of it is left to write back
+L2_NOTE = ("flushed between timed steps: 512 MB written, then 256 MB of another buffer read, outside the "
+           "events (the read leaves only clean lines, so no write-back of the flush lands in the timed region)")
+
+
+class L2Flush:
+    """Evicts L2 between timed steps: writes a buffer larger than L2, then reads another one
+    so that the lines left in L2 are clean (the written lines would otherwise be written
+    back to HBM during the next timed kernel)."""
+
+    def __init__(self, device):
+        import torch
+        self.w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.r = torch.ones(L2_CLEAN_BYTES // 4, dtype=torch.float32, device=device)
+
+    def __call__(self):
+        self.w.zero_()
+        return self.r.sum()
 
 
 def parse():
@@ -73,15 +91,16 @@ def kernel_source_hash(names) -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str, source_hash: str):
-    """DRAM bytes per launch from the committed ncu summary, if it matches the current source."""
+def recorded_traffic(kernel: str, source_hash: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this workload and
+    matches the current source."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         rec = json.load(f)
     e = rec.get(kernel)
-    if not e or e.get("source_hash") != source_hash:
+    if not e or e.get("source_hash") != source_hash or e.get("workload") != workload:
         return None
     return e.get("bytes_per_launch")
 
@@ -180,13 +199,13 @@ def run_decode(args, w):
     ws = torch.empty((rb.relation_decode_workspace_bytes(prob) + 3) // 4, dtype=torch.float32, device=dev)
     Y = torch.empty_like(P1n)
     L = torch.empty(w.B, w.H, dtype=torch.float32, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     e = 2  # bf16
     bytes_step = w.B * w.H * (2 * t * w.d * e + 3 * w.d * e + w.d * e + 4)  # caches, new rows, Y, L
     times = []
     with ClockSampler(0) as clk:
         for k in range(args.warmup + args.steps):
-            flush.zero_()
+            flush()
             ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
             ev[0].record()
             rb.relation_decode(prob, P1n, P2n, Vn, P2c, Vc, pos, 0, Y, L, ws)
@@ -203,7 +222,7 @@ def run_decode(args, w):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32 arithmetic on bf16", "data": "synthetic (seeded Gaussian caches, resident in HBM)",
         "config": {"workload": f"decode_{w.name}", "B": w.B, "H": w.H, "cache_tokens": t, "d_h": w.d,
-                   "tau_S": w.tau_S, "lambda": w.lam, "l2": "flushed between timed steps"},
+                   "tau_S": w.tau_S, "lambda": w.lam, "l2": L2_NOTE},
         "tokens_per_s": w.B / (ms * 1e-3),
         "roofline": {"kernel": "decode_partial_kernel + decode_combine_kernel", "bound": "hbm",
                      "achieved": bytes_step / (ms * 1e-3) / 1e9, "peak": hbm[0], "unit": "GB/s",
@@ -241,13 +260,13 @@ def run_prologue(args, w):
     outs = [torch.empty_like(x["P1"]) for _ in range(3)]
     grads = [torch.empty_like(x["P1"]) for _ in range(3)]
     dth = torch.empty(w.H // 2, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     tb = x["P1"].numel() * x["P1"].element_size()
     bytes_step = (3 + 3) * tb + (4 + 3) * tb  # fwd: 3 in, 3 out; bwd: 4 in, 3 out
     tf, tbw = [], []
     with ClockSampler(0) as clk:
         for k in range(args.warmup + args.steps):
-            flush.zero_()
+            flush()
             ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
             ev[0].record()
             rb.relation_prologue_fwd(prob, x["P1"], x["P2"], x["V"], theta, 1, 1e4, None, *outs)
@@ -267,7 +286,7 @@ def run_prologue(args, w):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32 arithmetic on bf16",
         "data": "synthetic (seeded Gaussian tensors, resident in HBM)",
         "config": {"workload": f"prologue_{w.name}", "B": w.B, "H": w.H, "T": w.T, "d_h": w.d, "pairing": "B",
-                   "rope_base": 1e4, "l2": "flushed between timed steps"},
+                   "rope_base": 1e4, "l2": L2_NOTE},
         "breakdown_ms": {"fwd": statistics.mean(tf), "bwd": statistics.mean(tbw)},
         "roofline": {"kernel": "rope_kernel + givens_kernel", "bound": "hbm", "achieved": gbs, "peak": hbm[0],
                      "unit": "GB/s", "frac": gbs / hbm[0], "peak_source": hbm[1], "traffic": None},
@@ -326,7 +345,7 @@ def run_linear(args, w):
     ws = rb.linear_workspace(prob, dev)
     Y = torch.empty_like(x["I"])
     g = [torch.empty_like(x["P1"]), torch.empty_like(x["P2"]), torch.empty_like(x["I"]), torch.empty_like(x["G"])]
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
     launches = [0]
 
@@ -353,7 +372,7 @@ def run_linear(args, w):
     torch.cuda.synchronize()
     with ClockSampler(ranks.local) as clk:
         for k in range(args.steps):
-            flush.zero_()
+            flush()
             step(evsets[k])
         torch.cuda.synchronize()
     rrep.barrier(ranks)
@@ -385,7 +404,7 @@ def run_linear(args, w):
         torch.cuda.synchronize()
         e_ms = 0.0
         for _ in range(args.steps):
-            flush.zero_()
+            flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             e2e_step()
@@ -409,14 +428,14 @@ def run_linear(args, w):
                 "initialisation), resident in HBM",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d_h": w.d, "tau_S": w.tau_S,
                    "g_scale": w.g_scale, "parallelism": f"independent heads, {ranks.world} replica(s)",
-                   "l2": "flushed between timed steps"},
+                   "l2": L2_NOTE},
         "breakdown_ms": {"fwd": statistics.mean(tf), "bwd": statistics.mean(tb)},
         "roofline": {"kernel": "relation_linear_fwd + relation_linear_bwd (all launches)", "bound": "hbm",
                      "achieved": gbs, "peak": hbm[0], "unit": "GB/s", "frac": gbs / hbm[0],
                      "peak_source": hbm[1],
-                     "traffic": recorded_traffic(f"linear fwd+bwd step, {w.name}",
+                     "traffic": recorded_traffic("linear fwd+bwd step",
                                                  kernel_source_hash(["linear.cu", "common.cuh", "ptx_sm100.cuh",
-                                                                     "tile_copy.cuh"])),
+                                                                     "tile_copy.cuh"]), w.name),
                      "algorithmic_bytes_per_head_token": linear_bytes_per_head_token(w.d)},
         "gpu_launches": launches[0],
         "e2e": e2e,
@@ -545,7 +564,7 @@ def main():
     dlam = torch.empty(1, dtype=torch.float32, device=dev)
     ws = torch.empty((rb.relation_bwd_workspace_bytes(prob) + 3) // 4, dtype=torch.float32, device=dev)
     fws = rb.fwd_workspace(prob, dev)  # None unless the head width needs padded copies (d_h = 60)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
 
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
@@ -584,7 +603,7 @@ def main():
     torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device()) as clk:
         for k in range(args.steps):
-            flush.zero_()  # evict L2 between timed steps (outside the events)
+            flush()  # evict L2 between timed steps (outside the events)
             step(ev_sets[k])
         torch.cuda.synchronize()
     rrep.barrier(ranks)
@@ -628,7 +647,7 @@ def main():
         torch.cuda.synchronize()
         e_ms = 0.0
         for _ in range(args.steps):
-            flush.zero_()
+            flush()
             a, b = ev(), ev()
             a.record(stream)
             e2e_step()
@@ -678,7 +697,7 @@ def main():
         "data": "synthetic (seeded Gaussian inputs, resident in HBM)",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d_h": w.d, "causal": w.causal,
                    "tau_S": w.tau_S, "lambda": w.lam, "p_scale": round(w.p_scale, 6),
-                   "parallelism": f"independent heads, {world} replica(s)", "l2": "flushed between timed steps"},
+                   "parallelism": f"independent heads, {world} replica(s)", "l2": L2_NOTE},
         "frac_of_peak": {"value": value / peak_burst, "peak_tflops": peak_burst, "source": peak_src,
                          "sustained_frac": value / peak_sust},
         "executed_tflops": executed,
@@ -686,7 +705,7 @@ def main():
                          "bwd_finish": statistics.mean(t_fin)},
         "roofline": {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak_burst, "unit": "TFLOP/s",
                      "frac": achieved / peak_burst, "peak_source": f"{peak_src} bf16 burst",
-                     "traffic": recorded_traffic(dom, kernel_source_hash(srcs))},
+                     "traffic": recorded_traffic(dom, kernel_source_hash(srcs), w.name)},
         "gpu_launches": timed_launches,
         "e2e": e2e,
         "clocks": clk.summary(),
