@@ -289,6 +289,18 @@ relation_status_t relation_linear_bwd(const relation_problem_t* p, const void* P
  */
 relation_status_t relation_check_device_status(void);
 
+/*
+ * Self-test of the failure-detection path: enqueues one kernel on `stream` in
+ * which a warp waits, through the same bounded wait every kernel uses, on a
+ * barrier that nothing completes.  After limit_ms milliseconds (1..10000) the
+ * wait gives up, records a timeout in the device status word and the kernel
+ * returns; nothing faults or hangs and the context stays usable.  After the
+ * caller synchronises, relation_check_device_status() returns
+ * RELATION_ERR_DEVICE_TIMEOUT (and clears the word).  Returns
+ * RELATION_ERR_INVALID_ARGUMENT for a limit outside 1..10000 ms.
+ */
+relation_status_t relation_selftest_wait_timeout(uint32_t limit_ms, void* stream);
+
 /* Number of kernel launches the last successful call on this thread enqueued. */
 int relation_last_launch_count(void);
 

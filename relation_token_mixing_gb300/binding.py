@@ -110,6 +110,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.relation_linear_bwd.argtypes = [ctypes.POINTER(Problem), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                             ctypes.c_int, _VP, ctypes.c_size_t, _VP]
         lib.relation_linear_bwd.restype = ctypes.c_int
+        lib.relation_selftest_wait_timeout.argtypes = [ctypes.c_uint32, _VP]
+        lib.relation_selftest_wait_timeout.restype = ctypes.c_int
         lib.relation_check_device_status.argtypes = []
         lib.relation_check_device_status.restype = ctypes.c_int
         lib.relation_last_launch_count.argtypes = []
@@ -178,6 +180,10 @@ def problem_for(t: torch.Tensor, tau_S: float, lam: float, causal: bool, layout:
 def relation_fwd(prob: Problem, P1, P2, V, Y, L=None, stream=None) -> None:
     _check(load().relation_fwd(ctypes.byref(prob), _ptr(P1), _ptr(P2), _ptr(V), _ptr(Y), _ptr(L),
                                _stream_ptr(stream)), "relation_fwd")
+
+
+def relation_selftest_wait_timeout(limit_ms: int, stream=None) -> None:
+    _check(load().relation_selftest_wait_timeout(int(limit_ms), _stream_ptr(stream)), "relation_selftest_wait_timeout")
 
 
 def relation_fwd_workspace_bytes(prob: Problem) -> int:

@@ -63,6 +63,10 @@ cudaError_t launch_linear_bwd(const KernelProblem& kp, const void* P1, const voi
                               const void* dY, void* dP1, void* dP2, void* dV, float* dG, bool reuse_fwd_states,
                               float* ws, int num_sms, cudaStream_t s);
 
+// One warp waits on an mbarrier nothing arrives on, through the kernels' bounded
+// wait with a limit of limit_ns; the timeout is recorded in *status.
+cudaError_t launch_wait_selftest(uint64_t limit_ns, unsigned int* status, cudaStream_t s);
+
 // Tensor-core (tcgen05) bf16 path.
 struct TcLaunch {
     int num_sms;

@@ -53,25 +53,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete, at most
-// RELATION_WAIT_LIMIT_NS.  On expiry records `code` in the status word and
-// raises the CTA's abort flag; also returns early once the flag is raised.
-// Returns true when the phase completed.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned int* status, unsigned int code) {
+// Waits for the phase with the given parity to complete, at most limit_ns
+// nanoseconds.  On expiry records `code` in the status word and raises the
+// CTA's abort flag; also returns early once the flag is raised.  Returns true
+// when the phase completed.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              unsigned int* status, unsigned int code, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (uint32_t n = 1;; ++n) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((n & 255u) == 0) {
             if (*abort_flag) return false;
-            if (global_ns() - t0 > RELATION_WAIT_LIMIT_NS) {
+            if (global_ns() - t0 > limit_ns) {
                 record_status(status, code);
                 *abort_flag = 1;
                 return false;
             }
         }
     }
+}
+
+// The kernels' wait: limit RELATION_WAIT_LIMIT_NS.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned int* status, unsigned int code) {
+    return mbar_wait_for(bar, parity, abort_flag, status, code, RELATION_WAIT_LIMIT_NS);
 }
 
 // Warp-uniform bounded wait: every lane waits, the warp agrees on the result.

@@ -371,6 +371,16 @@ relation_status_t relation_bwd_finish(RELATION_BWD_ARGS) {
     return st;
 }
 
+relation_status_t relation_selftest_wait_timeout(uint32_t limit_ms, void* stream) {
+    if (limit_ms < 1 || limit_ms > 10000) return RELATION_ERR_INVALID_ARGUMENT;
+    DeviceInfo di;
+    relation_status_t st = device_info(&di);
+    if (st != RELATION_OK) return st;
+    st = from_cuda(launch_wait_selftest((uint64_t)limit_ms * 1000000ull, di.status, static_cast<cudaStream_t>(stream)));
+    if (st == RELATION_OK) t_last_launches = 1;
+    return st;
+}
+
 relation_status_t relation_check_device_status(void) {
     DeviceInfo di;
     relation_status_t st = device_info(&di);

@@ -143,6 +143,12 @@ def test_forward_workspace_size_and_checks(lib):
     assert call(_prob(d_h=50)) == 2
 
 
+def test_wait_selftest_limit_is_checked(lib):
+    """Limits outside 1..10000 ms are rejected before any device call."""
+    for ms in (0, 10001, 2 ** 31):
+        assert lib.relation_selftest_wait_timeout(ms, None) == 1
+
+
 def _lfwd(lib, prob, P1=A, P2=2 * A, I=3 * A, G=4 * A, Y=8 * A, state=None, ws=16 * A):
     return lib.relation_linear_fwd(ctypes.byref(prob), P1, P2, I, G, Y, state, ws, 1 << 30, None)
 
