@@ -8,19 +8,24 @@
 //   dP1 = dU P2 / sqrt(d),  dP2 = dU^T P1 / sqrt(d),  dV = F^T dY.
 //
 // One CTA = one head x one 128-row key tile j (rows of P2 and V); it walks the
-// query tiles i that can see it (i >= j when causal).
-//   warp 0      loader: P2_j, V_j once (TMA); per query tile P1_i, dY_i (TMA)
-//               and the per-query constants (L_i folded with lambda log c_i, D_i)
-//   warp 1      MMA issuer and TMEM owner
-//   warps 2-5   elementwise stage, one thread per key row
-//   warps 6-9   dP1 reduction: tensor memory -> fp32 accumulator in global memory
+// query tiles i that can see it (i >= j when causal).  Head widths 80 and 128
+// (128-wide tiles; a narrower head reads as a tile with zero columns).
+//   warp 0       loader: P2_j, V_j once (TMA); per query tile P1_i, dY_i (TMA)
+//                and the per-query constants (L_i folded with lambda log c_i, D_i)
+//   warp 1       MMA issuer and TMEM owner
+//   warps 4-19   elementwise stage: warp (quarter q, block b) owns key rows
+//                32q..32q+31 (its TMEM lanes) and query columns 32b..32b+31
+//   warps 20-23  dP1 reduction: TMEM -> swizzled shared staging -> TMA bulk
+//                reduce-add (fp32) into the accumulator in global memory
 // Per query tile, with everything transposed so that key rows sit on TMEM lanes:
 //   S^T  = P2_j P1_i^T          (SS)      dP^T = V_j dY_i^T    (SS)
 //   elementwise: P^T, dS^T = dU^T / sqrt(d) -> TMEM (bf16) and dS^T -> smem
 //   dV  += P^T dY_i             (TS)      dP2 += dS^T P1_i     (TS)
-//   dP1_i (partial) = dS P2_j   (SS, dS read MN-major from smem) -> fp32 atomics
-// TMEM: S^T [0,128) | dP^T [128,256) | dV | dP2 | dP1 partial (d = 64) — for
-// d = 128 the dP1 partial reuses the S^T columns.
+//   dP1_i (partial) = dS P2_j   (SS, dS read MN-major from smem)
+// TMEM: S^T [0,128) | dP^T [128,256) | dV [256,384) | dP2 [384,512); the packed
+// P^T and dS^T overwrite the S^T and dP^T columns their warp has already read
+// (block b stores its 32 queries' pairs in columns 32b..32b+15 of the region),
+// and the dP1 partial reuses the S^T columns once dV has read P^T.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -31,24 +36,31 @@ namespace relation {
 namespace {
 
 constexpr int kTile = 128;
-constexpr int kThreads = 320;
+constexpr int kElemWarps = 16;                     // warps 4 .. 19
+constexpr int kReduceWarp0 = 4 + kElemWarps;       // warps 20 .. 23
+constexpr int kThreads = 32 * (kReduceWarp0 + 4);  // 768
 constexpr int kPanelBytes = 128 * 128;
+constexpr int kStageBytes = kTile * 128;  // one dP1 staging panel: 128 rows x 32 fp32 columns
+constexpr int kStagePanels = 2;           // staging panels in flight
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 struct BwdCfg {
+    static_assert(D == 128, "the 128-wide backward");
     static constexpr int kPanels = D / 64;
     static constexpr int kTileBytes = kTile * D * 2;
-    static constexpr int kStages = (D == 64) ? 2 : 1;
+    static constexpr int kStages = 1;
     static constexpr int kDsBytes = kTile * kTile * 2;
     // TMEM column map.
-    static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
-    static constexpr uint32_t kColDQ = (D == 64) ? 256 + 2 * D : 0;
-    static constexpr bool kDqAliasesS = (D != 64);
-    // alignment slack, tiles, dS^T, per-query constants, barriers, 16 KB guard band
-    static constexpr int kSmemBytes =
-        1024 + 2 * kTileBytes + kStages * 2 * kTileBytes + kDsBytes + kStages * 2 * kTile * 4 + 256 + 16384;
+    static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D, kColDQ = 0;
+    // alignment slack, tiles, dS^T, dP1 staging, per-query constants, barriers, 16 KB guard band
+    static constexpr int kSmemBytes = 1024 + 2 * kTileBytes + kStages * 2 * kTileBytes + kDsBytes +
+                                      kStagePanels * kStageBytes + kStages * 2 * kTile * 4 + 256 + 16384;
 };
+
+// TMEM column (relative to the S^T or dP^T region) of the packed pairs of the
+// 16 queries 16ks..16ks+15: block ks/2 keeps its pairs in its own first 16 columns.
+__host__ __device__ constexpr uint32_t packed_col(int ks) { return 32u * (ks >> 1) + 8u * (ks & 1); }
 
 struct BwdBarriers {
     uint64_t kv_full;
@@ -76,8 +88,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     relation_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_p1, const __grid_constant__ CUtensorMap tm_p2,
                            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_dy,
-                           const KernelProblem kp, const float* __restrict__ L, const float* __restrict__ Dw,
-                           float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dP2,
+                           const __grid_constant__ CUtensorMap tm_dq, const KernelProblem kp,
+                           const float* __restrict__ L, const float* __restrict__ Dw, __nv_bfloat16* __restrict__ dP2,
                            __nv_bfloat16* __restrict__ dV, unsigned int* status) {
     using C = BwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -87,7 +99,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sQ = sV + C::kTileBytes;                // P1_i per stage
     uint8_t* sG = sQ + C::kStages * C::kTileBytes;   // dY_i per stage
     uint8_t* sDS = sG + C::kStages * C::kTileBytes;  // dS^T (bf16), [key row][query], MN-major for dS
-    float* sLt = reinterpret_cast<float*>(sDS + C::kDsBytes);  // per stage: 128 folded log2 normalisers
+    uint8_t* sDQ = sDS + C::kDsBytes;                 // dP1 staging panels (fp32, 128-byte swizzled rows)
+    float* sLt = reinterpret_cast<float*>(sDQ + kStagePanels * kStageBytes);  // per stage: 128 folded log2 normalisers
     float* sDd = sLt + C::kStages * kTile;                      // per stage: 128 values of D
     BwdBarriers* bars = reinterpret_cast<BwdBarriers*>(sDd + C::kStages * kTile);
 
@@ -108,7 +121,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(&bars->q_empty[s], 1);
         }
         ptx::mbar_init(&bars->s_full, 1);
-        ptx::mbar_init(&bars->p_full, 128);
+        ptx::mbar_init(&bars->p_full, kElemWarps);
         ptx::mbar_init(&bars->dq_full, 1);
         ptx::mbar_init(&bars->dq_free, 128);
         ptx::mbar_init(&bars->mma_done, 1);
@@ -132,6 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tma_prefetch_desc(&tm_p2);
             ptx::tma_prefetch_desc(&tm_v);
             ptx::tma_prefetch_desc(&tm_dy);
+            ptx::tma_prefetch_desc(&tm_dq);
             ptx::mbar_arrive_expect_tx(&bars->kv_full, 2 * C::kTileBytes);
             for (int p = 0; p < C::kPanels; ++p) {
                 ptx::tma_load_operand(sK + p * kPanelBytes, &tm_p2, &bars->kv_full, p * 64, kv0, bh, head, batch,
@@ -192,8 +206,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                if (C::kDqAliasesS && it > 0 &&
-                    !ptx::mbar_wait(&bars->dq_free, (it - 1) & 1, abort_flag, status, kDevTimeoutMma)) {
+                ptx::tc_fence_after();
+                // dP^T first: its columns held the previous tile's dS^T, which dP2 has
+                // read (issued earlier), so it runs while the previous dP1 partial drains.
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks / 4) * kPanelBytes + (ks % 4) * 32;
+                    ptx::mma_ss(tmem + C::kColDP, ptx::smem_desc(va + off, 16, 1024, ptx::kSwizzle128B),
+                                ptx::smem_desc(ga + off, 16, 1024, ptx::kSwizzle128B), id_nn, ks > 0 ? 1u : 0u);
+                }
+                // S^T reuses the columns of the previous tile's dP1 partial.
+                if (it > 0 && !ptx::mbar_wait(&bars->dq_free, (it - 1) & 1, abort_flag, status, kDevTimeoutMma)) {
                     ok = false;
                     break;
                 }
@@ -204,12 +227,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mma_ss(tmem + C::kColS, ptx::smem_desc(ka + off, 16, 1024, ptx::kSwizzle128B),
                                 ptx::smem_desc(qa + off, 16, 1024, ptx::kSwizzle128B), id_nn, ks > 0 ? 1u : 0u);
                 }
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks / 4) * kPanelBytes + (ks % 4) * 32;
-                    ptx::mma_ss(tmem + C::kColDP, ptx::smem_desc(va + off, 16, 1024, ptx::kSwizzle128B),
-                                ptx::smem_desc(ga + off, 16, 1024, ptx::kSwizzle128B), id_nn, ks > 0 ? 1u : 0u);
-                }
                 ptx::mma_commit(&bars->s_full);
                 if (!ptx::mbar_wait(&bars->p_full, it & 1, abort_flag, status, kDevTimeoutFull)) {
                     ok = false;
@@ -219,19 +236,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int ks = 0; ks < kTile / 16; ++ks) {
                     const uint64_t gdesc = ptx::smem_desc(ga + ks * 2048, kPanelBytes, 1024, ptx::kSwizzle128B);
-                    ptx::mma_ts(tmem + C::kColDV, tmem + C::kColS + ks * 8, gdesc, id_tb,
+                    ptx::mma_ts(tmem + C::kColDV, tmem + C::kColS + packed_col(ks), gdesc, id_tb,
                                 (it > 0 || ks > 0) ? 1u : 0u);
                 }
 #pragma unroll
                 for (int ks = 0; ks < kTile / 16; ++ks) {
                     const uint64_t qdesc = ptx::smem_desc(qa + ks * 2048, kPanelBytes, 1024, ptx::kSwizzle128B);
-                    ptx::mma_ts(tmem + C::kColDK, tmem + C::kColDP + ks * 8, qdesc, id_tb,
+                    ptx::mma_ts(tmem + C::kColDK, tmem + C::kColDP + packed_col(ks), qdesc, id_tb,
                                 (it > 0 || ks > 0) ? 1u : 0u);
-                }
-                if (!C::kDqAliasesS && it > 0 &&
-                    !ptx::mbar_wait(&bars->dq_free, (it - 1) & 1, abort_flag, status, kDevTimeoutMma)) {
-                    ok = false;
-                    break;
                 }
 #pragma unroll
                 for (int ks = 0; ks < kTile / 16; ++ks) {
@@ -245,9 +257,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mma_commit(&bars->mma_done);
             drain_wait(&bars->mma_done, 0);
         }
-    } else if (warp < 6) {
+    } else if (warp < 4) {
+        // warps 2-3: no role (they complete the first warpgroup)
+    } else if (warp < kReduceWarp0) {
         // --------------------------------------------------- elementwise stage
         const int quarter = warp & 3;
+        const int blk = (warp - 4) >> 2;    // query columns 32blk .. 32blk+31
         const int r = quarter * 32 + lane;  // key row within the tile
         const int kv = kv0 + r;
         const bool row_valid = kv < T;
@@ -273,10 +288,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool special = diag_tile || qlimit < kTile || !row_valid;
             uint8_t* ds_row = sDS + r * 128;
 #pragma unroll
-            for (int qq = 0; qq < 8; ++qq) {
+            for (int half = 0; half < 2; ++half) {
+                const int ks = 2 * blk + half;  // 16 queries 16ks .. 16ks+15
                 uint32_t sv[16], gv[16];
-                ptx::tmem_ld16(lane_addr + C::kColS + 16 * qq, sv);
-                ptx::tmem_ld16(lane_addr + C::kColDP + 16 * qq, gv);
+                ptx::tmem_ld16(lane_addr + C::kColS + 16 * ks, sv);
+                ptx::tmem_ld16(lane_addr + C::kColDP + 16 * ks, gv);
                 ptx::tmem_ld_wait();
                 ptx::pin_regs(sv);
                 ptx::pin_regs(gv);
@@ -286,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float pv[2], dv[2];
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        const int c = 16 * qq + 2 * k2 + h;
+                        const int c = 16 * ks + 2 * k2 + h;
                         const float a = as_f(sv[2 * k2 + h]);
                         float x, slope;
                         if (special && diag_tile && c == r) {
@@ -309,23 +325,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pp[k2] = ptx::pack_bf16x2(pv[0], pv[1]);
                     dp[k2] = ptx::pack_bf16x2(dv[0], dv[1]);
                 }
-                // P^T -> TMEM over S^T columns [8qq, 8qq+8) (already read), dS^T likewise over dP^T.
+                // P^T and dS^T pairs -> TMEM columns this warp has already read.
+                const uint32_t pc = packed_col(ks);
                 asm volatile(
                     "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
-                        lane_addr + C::kColS + 8 * qq),
+                        lane_addr + C::kColS + pc),
                     "r"(pp[0]), "r"(pp[1]), "r"(pp[2]), "r"(pp[3]), "r"(pp[4]), "r"(pp[5]), "r"(pp[6]), "r"(pp[7])
                     : "memory");
                 asm volatile(
                     "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
-                        lane_addr + C::kColDP + 8 * qq),
+                        lane_addr + C::kColDP + pc),
                     "r"(dp[0]), "r"(dp[1]), "r"(dp[2]), "r"(dp[3]), "r"(dp[4]), "r"(dp[5]), "r"(dp[6]), "r"(dp[7])
                     : "memory");
-                // dS^T row r, queries 16qq..16qq+15: two 16-byte chunks of the
-                // 128-byte swizzled row in panel qq/4.
+                // dS^T row r, queries 16ks..16ks+15: two 16-byte chunks of the
+                // 128-byte swizzled row in panel ks/4.
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const int chunk = (2 * qq + h) & 7;
-                    const int panel = (2 * qq + h) >> 3;
+                    const int chunk = (2 * ks + h) & 7;
+                    const int panel = (2 * ks + h) >> 3;
                     uint4* dst = reinterpret_cast<uint4*>(ds_row + panel * kPanelBytes + ((chunk ^ (r & 7)) << 4));
                     *dst = make_uint4(dp[4 * h], dp[4 * h + 1], dp[4 * h + 2], dp[4 * h + 3]);
                 }
@@ -333,62 +350,77 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tmem_st_wait();
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(&bars->p_full);
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&bars->p_full);
         }
-        // Epilogue: dV and dP2 rows of this key tile.
-        if (ok && ptx::mbar_wait_warp(&bars->mma_done, 0, abort_flag, status, kDevTimeoutMma)) {
+        // Epilogue: block b writes columns 32b .. 32b+31 of the dV and dP2 rows of this key tile.
+        if (ok && ptx::mbar_wait_warp(&bars->mma_done, 0, abort_flag, status, kDevTimeoutMma) && 32 * blk < kp.d) {
             ptx::tc_fence_after();
 #pragma unroll
             for (int which = 0; which < 2; ++which) {
                 __nv_bfloat16* dst_row = (which == 0 ? dV : dP2) + row_offset(kp, bh, row_valid ? kv : 0);
-                const uint32_t col = which == 0 ? C::kColDV : C::kColDK;
+                const uint32_t col = (which == 0 ? C::kColDV : C::kColDK) + 32 * blk;
+                uint32_t ov[32];
+                ptx::tmem_ld32(lane_addr + col, ov);
+                ptx::tmem_ld_wait();
+                ptx::pin_regs(ov);
+                if (row_valid) {
 #pragma unroll
-                for (int c0 = 0; c0 < D / 32; ++c0) {
-                    if (32 * c0 >= kp.d) break;  // zero-padding columns of a narrower head
-                    uint32_t ov[32];
-                    ptx::tmem_ld32(lane_addr + col + 32 * c0, ov);
-                    ptx::tmem_ld_wait();
-                    ptx::pin_regs(ov);
-                    if (row_valid) {
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            store_bf16x8(dst_row, 32 * c0 + 8 * k, kp.d,
-                                         ptx::pack_bf16x2(as_f(ov[8 * k + 0]), as_f(ov[8 * k + 1])),
-                                         ptx::pack_bf16x2(as_f(ov[8 * k + 2]), as_f(ov[8 * k + 3])),
-                                         ptx::pack_bf16x2(as_f(ov[8 * k + 4]), as_f(ov[8 * k + 5])),
-                                         ptx::pack_bf16x2(as_f(ov[8 * k + 6]), as_f(ov[8 * k + 7])));
-                    }
+                    for (int k = 0; k < 4; ++k)
+                        store_bf16x8(dst_row, 32 * blk + 8 * k, kp.d,
+                                     ptx::pack_bf16x2(as_f(ov[8 * k + 0]), as_f(ov[8 * k + 1])),
+                                     ptx::pack_bf16x2(as_f(ov[8 * k + 2]), as_f(ov[8 * k + 3])),
+                                     ptx::pack_bf16x2(as_f(ov[8 * k + 4]), as_f(ov[8 * k + 5])),
+                                     ptx::pack_bf16x2(as_f(ov[8 * k + 6]), as_f(ov[8 * k + 7])));
                 }
             }
         }
     } else {
         // -------------------------------------------------- dP1 partial reduce
+        // Per query tile, four 32-column panels: TMEM -> swizzled shared staging
+        // -> one TMA bulk reduce-add (fp32) into the accumulator; rows past T are
+        // dropped by TMA.  TMEM is released once the last panel is in registers.
         const int quarter = warp & 3;
         const int rq = quarter * 32 + lane;  // query row within the tile
         const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+        const bool leader = (warp == kReduceWarp0) && lane == 0;
         for (int it = 0; it < n_q; ++it) {
             const int i = i_first + it;
             if (!ptx::mbar_wait_warp(&bars->dq_full, it & 1, abort_flag, status, kDevTimeoutMma)) break;
             ptx::tc_fence_after();
-            const int q = i * kTile + rq;
-            float4* dst = reinterpret_cast<float4*>(dq_acc + ((size_t)bh * T + q) * D);
-#pragma unroll
+#pragma unroll 1
             for (int c0 = 0; c0 < D / 32; ++c0) {
                 uint32_t ov[32];
                 ptx::tmem_ld32(lane_addr + C::kColDQ + 32 * c0, ov);
                 ptx::tmem_ld_wait();
                 ptx::pin_regs(ov);
-                if (q < T) {
+                if (c0 == D / 32 - 1) {
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(&bars->dq_free);  // every panel has left TMEM
+                }
+                // The bulk reduce issued two panels ago (same staging buffer) must have
+                // finished reading it; bulk groups complete in order.
+                if (leader) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                uint8_t* stage = sDQ + (c0 & 1) * kStageBytes;
+                uint8_t* row = stage + rq * 128;
 #pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        atomicAdd(dst + 8 * c0 + k,
-                                  make_float4(as_f(ov[4 * k]), as_f(ov[4 * k + 1]), as_f(ov[4 * k + 2]),
-                                              as_f(ov[4 * k + 3])));
+                for (int k = 0; k < 8; ++k)
+                    *reinterpret_cast<uint4*>(row + ((k ^ (rq & 7)) << 4)) =
+                        make_uint4(ov[4 * k], ov[4 * k + 1], ov[4 * k + 2], ov[4 * k + 3]);
+                ptx::fence_proxy_async_smem();
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                if (leader) {
+                    asm volatile(
+                        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2, %3}], "
+                        "[%4];" ::"l"(reinterpret_cast<uint64_t>(&tm_dq)),
+                        "r"(32 * c0), "r"(i * kTile), "r"(bh), "r"(ptx::smem_u32(stage))
+                        : "memory");
+                    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
                 }
             }
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(&bars->dq_free);
         }
+        if (leader) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -421,8 +453,13 @@ cudaError_t launch_bwd_tc_d(const KernelProblem& kp, const void* P1, const void*
             make_operand_map(maps[k], bases[k], kp.BH / kp.H, kp.H, kp.T, kp.d, kp.layout, 64, 128, true);
         if (e != cudaSuccess) return e;
     }
+    // dP1 accumulator: fp32 [BH, T, D], reduced in 32-column (128-byte) swizzled boxes.
+    CUtensorMap mq;
+    cudaError_t e = make_tensor_map_3d(&mq, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, kp.T, kp.BH, 32, 128,
+                                       CU_TENSOR_MAP_SWIZZLE_128B);
+    if (e != cudaSuccess) return e;
     dim3 grid((unsigned)kp.BH, (unsigned)((kp.T + kTile - 1) / kTile));
-    relation_bwd_tc_kernel<D><<<grid, kThreads, C::kSmemBytes, s>>>(m1, m2, mv, mg, kp, L, Dw, dq_acc,
+    relation_bwd_tc_kernel<D><<<grid, kThreads, C::kSmemBytes, s>>>(m1, m2, mv, mg, mq, kp, L, Dw,
                                                                      (__nv_bfloat16*)dP2, (__nv_bfloat16*)dV,
                                                                      tl.status);
     return cudaGetLastError();
