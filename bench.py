@@ -674,9 +674,9 @@ def main():
     fwd_k = f"relation_fwd_tc_kernel<{tile}, false>"
     fwd_src = ["fwd_tc.cu"] + srcs_common
     if tile == 64:
-        bwd_k, bwd_src = "relation_bwd_tc64_kernel<0>", ["bwd_tc64.cu"] + srcs_common
+        bwd_k, bwd_src = "relation_bwd_tc64_kernel<0>", ["bwd_tc64.cu", "bwd_elementwise.cuh"] + srcs_common
     else:
-        bwd_k, bwd_src = "relation_bwd_tc_kernel<128>", ["bwd_tc.cu"] + srcs_common
+        bwd_k, bwd_src = "relation_bwd_tc_kernel<128>", ["bwd_tc.cu", "bwd_elementwise.cuh"] + srcs_common
     if mean_main >= mean_fwd:
         dom, srcs, dom_ms, dom_flops = bwd_k, bwd_src, mean_main, f_bwd
     else:

@@ -28,12 +28,16 @@
 // and the dP1 partial reuses the S^T columns once dV has read P^T.
 #include <cuda_bf16.h>
 
+#include "bwd_elementwise.cuh"
 #include "kernels.h"
 #include "ptx_sm100.cuh"
 #include "tmap.h"
 
 namespace relation {
 namespace {
+
+using bwd_elem::ElemConst;
+using bwd_elem::elementwise16;
 
 constexpr int kTile = 128;
 constexpr int kElemWarps = 16;                     // warps 4 .. 19
@@ -100,9 +104,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sG = sQ + C::kStages * C::kTileBytes;   // dY_i per stage
     uint8_t* sDS = sG + C::kStages * C::kTileBytes;  // dS^T (bf16), [key row][query], MN-major for dS
     uint8_t* sDQ = sDS + C::kDsBytes;                 // dP1 staging panels (fp32, 128-byte swizzled rows)
-    float* sLt = reinterpret_cast<float*>(sDQ + kStagePanels * kStageBytes);  // per stage: 128 folded log2 normalisers
-    float* sDd = sLt + C::kStages * kTile;                      // per stage: 128 values of D
-    BwdBarriers* bars = reinterpret_cast<BwdBarriers*>(sDd + C::kStages * kTile);
+    // Per stage and query column pair (2c, 2c+1): -(L + lambda log c) log2(e) of both, then -D k_scale of both.
+    float4* sQC = reinterpret_cast<float4*>(sDQ + kStagePanels * kStageBytes);
+    BwdBarriers* bars = reinterpret_cast<BwdBarriers*>(sQC + C::kStages * (kTile / 2));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bh = blockIdx.x;
@@ -113,6 +117,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nq_all = (T + kTile - 1) / kTile;
     const int i_first = kp.causal ? jt : 0;
     const int n_q = nq_all - i_first;
+    const float k_scale = 0.5f * kp.inv_sqrt_d;  // dS^T = dR R'(U) / sqrt(d) with R'(U) carried as 2 R'(U)
 
     if (threadIdx.x == 0) {
         ptx::mbar_init(&bars->kv_full, 1);
@@ -162,16 +167,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 !ptx::mbar_wait_warp(&bars->q_empty[s], ((it / C::kStages) - 1) & 1, abort_flag, status,
                                      kDevTimeoutEmpty))
                 break;
+            float* qc = reinterpret_cast<float*>(sQC + s * (kTile / 2));
             for (int c = lane; c < kTile; c += 32) {
                 const int q = i * kTile + c;
-                float lt = 0.f, dd = 0.f;
+                float nlt = 0.f, ndk = 0.f;
                 if (q < T) {
                     const int count = kp.causal ? (q + 1) : T;
-                    lt = (L[(size_t)bh * T + q] + kp.lambda * logf((float)count)) * kLog2e;
-                    dd = Dw[(size_t)bh * T + q];
+                    nlt = -(L[(size_t)bh * T + q] + kp.lambda * __logf((float)count)) * kLog2e;
+                    ndk = -Dw[(size_t)bh * T + q] * k_scale;
                 }
-                sLt[s * kTile + c] = lt;
-                sDd[s * kTile + c] = dd;
+                qc[(c >> 1) * 4 + (c & 1)] = nlt;
+                qc[(c >> 1) * 4 + 2 + (c & 1)] = ndk;
             }
             if (lane == 0) {
                 ptx::mbar_arrive_expect_tx(&bars->q_full[s], 2 * C::kTileBytes);
@@ -267,10 +273,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kv = kv0 + r;
         const bool row_valid = kv < T;
         const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
-        const float c_half = 0.5f * kp.inv_sqrt_d;
-        const float c_diag = 0.5f * kp.inv_sqrt_d / kp.tau_S;
-        const float inv_tau = 1.f / kp.tau_S;
-        const float diag_corr = kp.lambda * logf((float)(kp.causal ? (kv + 1) : T));
+        ElemConst ec;
+        ec.c_nh = make_float2(-0.5f * kp.inv_sqrt_d, -0.5f * kp.inv_sqrt_d);
+        ec.c_hl = make_float2(0.5f * kp.inv_sqrt_d * kLog2e, 0.5f * kp.inv_sqrt_d * kLog2e);
+        ec.k2 = make_float2(k_scale, k_scale);
+        ec.one = make_float2(1.f, 1.f);
+        ec.mone = make_float2(-1.f, -1.f);
+        ec.c_diag = 0.5f * kp.inv_sqrt_d / kp.tau_S;
+        ec.half_inv_tau = 0.5f / kp.tau_S;
+        ec.log_count = __logf((float)(kp.causal ? (kv + 1) : T));
+        ec.diag_off = (0.5f + kp.lambda * ec.log_count) * kLog2e;  // (1/2 + lambda log c) log2(e)
+        ec.row_valid = row_valid;
+        ec.causal = kp.causal != 0;
         bool ok = true;
         for (int it = 0; ok && it < n_q; ++it) {
             const int s = it % C::kStages;
@@ -281,50 +295,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // q_full of this stage has completed (the MMA waited on it before S^T).
             ptx::tc_fence_after();
-            const float* lt = sLt + s * kTile;
-            const float* dd = sDd + s * kTile;
             const bool diag_tile = (i == jt);
             const int qlimit = T - i * kTile;  // query columns c < qlimit exist
-            const bool special = diag_tile || qlimit < kTile || !row_valid;
             uint8_t* ds_row = sDS + r * 128;
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 const int ks = 2 * blk + half;  // 16 queries 16ks .. 16ks+15
+                const int col0 = 16 * ks;
                 uint32_t sv[16], gv[16];
-                ptx::tmem_ld16(lane_addr + C::kColS + 16 * ks, sv);
-                ptx::tmem_ld16(lane_addr + C::kColDP + 16 * ks, gv);
+                ptx::tmem_ld16(lane_addr + C::kColS + col0, sv);
+                ptx::tmem_ld16(lane_addr + C::kColDP + col0, gv);
                 ptx::tmem_ld_wait();
                 ptx::pin_regs(sv);
                 ptx::pin_regs(gv);
+                const float4* qc = sQC + s * (kTile / 2) + col0 / 2;
+                // The masked variant is chosen per warp (uniformly) if any of its rows needs it.
+                const bool special = __any_sync(0xffffffffu, diag_tile || qlimit < col0 + 16 || !row_valid);
                 uint32_t pp[8], dp[8];
-#pragma unroll
-                for (int k2 = 0; k2 < 8; ++k2) {
-                    float pv[2], dv[2];
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int c = 16 * ks + 2 * k2 + h;
-                        const float a = as_f(sv[2 * k2 + h]);
-                        float x, slope;
-                        if (special && diag_tile && c == r) {
-                            const float sg = 0.5f + 0.5f * ptx::tanh_approx(a * c_diag);
-                            x = (sg + diag_corr) * kLog2e;
-                            slope = sg * (1.f - sg) * inv_tau;
-                        } else {
-                            const float hh = a * c_half;
-                            const float sg = 0.5f + 0.5f * ptx::tanh_approx(hh);
-                            const float u = 2.f * hh;
-                            x = u * sg * kLog2e;
-                            slope = fmaf(u * sg, 1.f - sg, sg);
-                        }
-                        float p = ptx::ex2_approx(x - lt[c]);
-                        if (special && (c >= qlimit || (kp.causal && diag_tile && c < r) || !row_valid)) p = 0.f;
-                        const float dR = p * (as_f(gv[2 * k2 + h]) - dd[c]);
-                        pv[h] = p;
-                        dv[h] = dR * slope * kp.inv_sqrt_d;
-                    }
-                    pp[k2] = ptx::pack_bf16x2(pv[0], pv[1]);
-                    dp[k2] = ptx::pack_bf16x2(dv[0], dv[1]);
-                }
+                if (!special)
+                    elementwise16<false>(sv, gv, qc, col0, r, ec, false, 0, pp, dp);
+                else
+                    (void)elementwise16<true>(sv, gv, qc, col0, r, ec, diag_tile, qlimit, pp, dp);
                 // P^T and dS^T pairs -> TMEM columns this warp has already read.
                 const uint32_t pc = packed_col(ks);
                 asm volatile(
