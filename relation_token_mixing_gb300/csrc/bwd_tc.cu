@@ -198,71 +198,71 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            const uint32_t id_nn = ptx::idesc_bf16(kTile, kTile, false, false);  // S^T, dP^T
-            const uint32_t id_tb = ptx::idesc_bf16(kTile, D, false, true);       // dV, dP2 (B MN-major)
-            const uint32_t id_dq = ptx::idesc_bf16(kTile, D, true, true);        // dP1 (A, B MN-major)
-            const uint32_t ka = ptx::smem_u32(sK), va = ptx::smem_u32(sV), dsa = ptx::smem_u32(sDS);
-            bool ok = ptx::mbar_wait(&bars->kv_full, 0, abort_flag, status, kDevTimeoutFull);
-            for (int it = 0; ok && it < n_q; ++it) {
-                const int s = it % C::kStages;
-                const uint32_t qa = ptx::smem_u32(sQ + s * C::kTileBytes);
-                const uint32_t ga = ptx::smem_u32(sG + s * C::kTileBytes);
-                if (!ptx::mbar_wait(&bars->q_full[s], (it / C::kStages) & 1, abort_flag, status, kDevTimeoutFull)) {
-                    ok = false;
-                    break;
-                }
-                ptx::tc_fence_after();
-                // dP^T first: its columns held the previous tile's dS^T, which dP2 has
-                // read (issued earlier), so it runs while the previous dP1 partial drains.
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks / 4) * kPanelBytes + (ks % 4) * 32;
-                    ptx::mma_ss(tmem + C::kColDP, ptx::smem_desc(va + off, 16, 1024, ptx::kSwizzle128B),
-                                ptx::smem_desc(ga + off, 16, 1024, ptx::kSwizzle128B), id_nn, ks > 0 ? 1u : 0u);
-                }
-                // S^T reuses the columns of the previous tile's dP1 partial.
-                if (it > 0 && !ptx::mbar_wait(&bars->dq_free, (it - 1) & 1, abort_flag, status, kDevTimeoutMma)) {
-                    ok = false;
-                    break;
-                }
-                ptx::tc_fence_after();
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks / 4) * kPanelBytes + (ks % 4) * 32;
-                    ptx::mma_ss(tmem + C::kColS, ptx::smem_desc(ka + off, 16, 1024, ptx::kSwizzle128B),
-                                ptx::smem_desc(qa + off, 16, 1024, ptx::kSwizzle128B), id_nn, ks > 0 ? 1u : 0u);
-                }
-                ptx::mma_commit(&bars->s_full);
-                if (!ptx::mbar_wait(&bars->p_full, it & 1, abort_flag, status, kDevTimeoutFull)) {
-                    ok = false;
-                    break;
-                }
-                ptx::tc_fence_after();
-#pragma unroll
-                for (int ks = 0; ks < kTile / 16; ++ks) {
-                    const uint64_t gdesc = ptx::smem_desc(ga + ks * 2048, kPanelBytes, 1024, ptx::kSwizzle128B);
-                    ptx::mma_ts(tmem + C::kColDV, tmem + C::kColS + packed_col(ks), gdesc, id_tb,
-                                (it > 0 || ks > 0) ? 1u : 0u);
-                }
-#pragma unroll
-                for (int ks = 0; ks < kTile / 16; ++ks) {
-                    const uint64_t qdesc = ptx::smem_desc(qa + ks * 2048, kPanelBytes, 1024, ptx::kSwizzle128B);
-                    ptx::mma_ts(tmem + C::kColDK, tmem + C::kColDP + packed_col(ks), qdesc, id_tb,
-                                (it > 0 || ks > 0) ? 1u : 0u);
-                }
-#pragma unroll
-                for (int ks = 0; ks < kTile / 16; ++ks) {
-                    const uint64_t adesc = ptx::smem_desc(dsa + ks * 2048, kPanelBytes, 1024, ptx::kSwizzle128B);
-                    const uint64_t bdesc = ptx::smem_desc(ka + ks * 2048, kPanelBytes, 1024, ptx::kSwizzle128B);
-                    ptx::mma_ss(tmem + C::kColDQ, adesc, bdesc, id_dq, ks > 0 ? 1u : 0u);
-                }
-                ptx::mma_commit(&bars->dq_full);
-                ptx::mma_commit(&bars->q_empty[s]);
+        // The whole warp runs the issue loop; one elected lane issues each MMA.
+        // Descriptors are built once; a byte offset is added as offset >> 4.
+        const uint32_t id_nn = ptx::idesc_bf16(kTile, kTile, false, false);  // S^T, dP^T
+        const uint32_t id_tb = ptx::idesc_bf16(kTile, D, false, true);       // dV, dP2 (B MN-major)
+        const uint32_t id_dq = ptx::idesc_bf16(kTile, D, true, true);        // dP1 (A, B MN-major)
+        const uint64_t dk = ptx::smem_desc(ptx::smem_u32(sK), 16, 1024, ptx::kSwizzle128B);    // K-major views
+        const uint64_t dv = ptx::smem_desc(ptx::smem_u32(sV), 16, 1024, ptx::kSwizzle128B);
+        const uint64_t dq = ptx::smem_desc(ptx::smem_u32(sQ), 16, 1024, ptx::kSwizzle128B);
+        const uint64_t dg = ptx::smem_desc(ptx::smem_u32(sG), 16, 1024, ptx::kSwizzle128B);
+        const uint64_t mg = ptx::smem_desc(ptx::smem_u32(sG), kPanelBytes, 1024, ptx::kSwizzle128B);  // MN-major
+        const uint64_t mq = ptx::smem_desc(ptx::smem_u32(sQ), kPanelBytes, 1024, ptx::kSwizzle128B);
+        const uint64_t mds = ptx::smem_desc(ptx::smem_u32(sDS), kPanelBytes, 1024, ptx::kSwizzle128B);
+        const uint64_t mk = ptx::smem_desc(ptx::smem_u32(sK), kPanelBytes, 1024, ptx::kSwizzle128B);
+        constexpr uint64_t kStageStep = C::kTileBytes >> 4;
+        bool ok = ptx::mbar_wait_warp(&bars->kv_full, 0, abort_flag, status, kDevTimeoutFull);
+        for (int it = 0; ok && it < n_q; ++it) {
+            const int s = it % C::kStages;
+            const uint64_t st = s * kStageStep;
+            if (!ptx::mbar_wait_warp(&bars->q_full[s], (it / C::kStages) & 1, abort_flag, status, kDevTimeoutFull)) {
+                ok = false;
+                break;
             }
-            ptx::mma_commit(&bars->mma_done);
-            drain_wait(&bars->mma_done, 0);
+            ptx::tc_fence_after();
+            // dP^T first: its columns held the previous tile's dS^T, which dP2 has
+            // read (issued earlier), so it runs while the previous dP1 partial drains.
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                const uint64_t off = (uint64_t)(((ks / 4) * kPanelBytes + (ks % 4) * 32) >> 4);
+                ptx::mma_ss_elect(tmem + C::kColDP, dv + off, dg + st + off, id_nn, ks > 0 ? 1u : 0u);
+            }
+            // S^T reuses the columns of the previous tile's dP1 partial.
+            if (it > 0 && !ptx::mbar_wait_warp(&bars->dq_free, (it - 1) & 1, abort_flag, status, kDevTimeoutMma)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                const uint64_t off = (uint64_t)(((ks / 4) * kPanelBytes + (ks % 4) * 32) >> 4);
+                ptx::mma_ss_elect(tmem + C::kColS, dk + off, dq + st + off, id_nn, ks > 0 ? 1u : 0u);
+            }
+            ptx::mma_commit_elect(&bars->s_full);
+            if (!ptx::mbar_wait_warp(&bars->p_full, it & 1, abort_flag, status, kDevTimeoutFull)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            // K-step ks covers queries 16ks..16ks+15: 16 rows (2048 bytes) of the MN-major tiles.
+#pragma unroll
+            for (int ks = 0; ks < kTile / 16; ++ks)
+                ptx::mma_ts_elect(tmem + C::kColDV, tmem + C::kColS + packed_col(ks), mg + st + ks * 128, id_tb,
+                                  (it > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
+            for (int ks = 0; ks < kTile / 16; ++ks)
+                ptx::mma_ts_elect(tmem + C::kColDK, tmem + C::kColDP + packed_col(ks), mq + st + ks * 128, id_tb,
+                                  (it > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
+            for (int ks = 0; ks < kTile / 16; ++ks)
+                ptx::mma_ss_elect(tmem + C::kColDQ, mds + ks * 128, mk + ks * 128, id_dq, ks > 0 ? 1u : 0u);
+            ptx::mma_commit_elect(&bars->dq_full);
+            ptx::mma_commit_elect(&bars->q_empty[s]);
         }
+        ptx::mma_commit_elect(&bars->mma_done);
+        if (lane == 0) drain_wait(&bars->mma_done, 0);
+        __syncwarp();
     } else if (warp < 4) {
         // warps 2-3: no role (they complete the first warpgroup)
     } else if (warp < kReduceWarp0) {
