@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_dy,
                            const __grid_constant__ CUtensorMap tm_dq, const KernelProblem kp,
                            const float* __restrict__ L, const float* __restrict__ Dw, __nv_bfloat16* __restrict__ dP2,
-                           __nv_bfloat16* __restrict__ dV, unsigned int* status) {
+                           __nv_bfloat16* __restrict__ dV, unsigned int* status, int head_group) {
     using C = BwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -109,10 +109,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     BwdBarriers* bars = reinterpret_cast<BwdBarriers*>(sQC + C::kStages * (kTile / 2));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.x;
-    const int batch = bh / kp.H, head = bh - batch * kp.H;
-    const int jt = blockIdx.y;  // key tile; low tiles see the most query tiles
     const int T = kp.T;
+    const int nt_all = (T + kTile - 1) / kTile;
+    int bh, jt;  // head and key tile; low tiles see the most query tiles and go first
+    grouped_tile_order(blockIdx.x, kp.BH, nt_all, head_group, bh, jt);
+    const int batch = bh / kp.H, head = bh - batch * kp.H;
     const int kv0 = jt * kTile;
     const int nq_all = (T + kTile - 1) / kTile;
     const int i_first = kp.causal ? jt : 0;
@@ -449,10 +450,21 @@ cudaError_t launch_bwd_tc_d(const KernelProblem& kp, const void* P1, const void*
     cudaError_t e = make_tensor_map_3d(&mq, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, kp.T, kp.BH, 32, 128,
                                        CU_TENSOR_MAP_SWIZZLE_128B);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)kp.BH, (unsigned)((kp.T + kTile - 1) / kTile));
-    relation_bwd_tc_kernel<D><<<grid, kThreads, C::kSmemBytes, s>>>(m1, m2, mv, mg, mq, kp, L, Dw,
-                                                                     (__nv_bfloat16*)dP2, (__nv_bfloat16*)dV,
-                                                                     tl.status);
+    const int64_t ctas = kp.BH * ((kp.T + kTile - 1) / kTile);
+    if (ctas > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    // Heads in flight: as many as fit in three quarters of L2 with P1, P2, V, dY
+    // (bf16) and the fp32 dP1 accumulator of each, i.e. 12 T D bytes per head.
+    static std::once_flag l2_once;
+    static int l2_bytes = 0;
+    std::call_once(l2_once, [] {
+        int dev = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&l2_bytes, cudaDevAttrL2CacheSize, dev);
+    });
+    const int64_t per_head = 12 * (int64_t)kp.T * D;
+    int64_t group = (l2_bytes > 0 ? (int64_t)l2_bytes * 3 / 4 : (int64_t)96 << 20) / per_head;
+    group = group < 1 ? 1 : (group > kp.BH ? kp.BH : group);
+    relation_bwd_tc_kernel<D><<<dim3((unsigned)ctas), kThreads, C::kSmemBytes, s>>>(
+        m1, m2, mv, mg, mq, kp, L, Dw, (__nv_bfloat16*)dP2, (__nv_bfloat16*)dV, tl.status, (int)group);
     return cudaGetLastError();
 }
 
