@@ -94,7 +94,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_dy,
                            const __grid_constant__ CUtensorMap tm_dq, const KernelProblem kp,
                            const float* __restrict__ L, const float* __restrict__ Dw, __nv_bfloat16* __restrict__ dP2,
-                           __nv_bfloat16* __restrict__ dV, unsigned int* status, int head_group) {
+                           __nv_bfloat16* __restrict__ dV, float* __restrict__ dlambda, unsigned int* status,
+                           int head_group) {
     using C = BwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -286,6 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ec.diag_off = (0.5f + kp.lambda * ec.log_count) * kLog2e;  // (1/2 + lambda log c) log2(e)
         ec.row_valid = row_valid;
         ec.causal = kp.causal != 0;
+        float dlam = 0.f;  // sum of log(c_i) dR_ii * k_scale over this warp's diagonal entries
         bool ok = true;
         for (int it = 0; ok && it < n_q; ++it) {
             const int s = it % C::kStages;
@@ -316,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!special)
                     elementwise16<false>(sv, gv, qc, col0, r, ec, false, 0, pp, dp);
                 else
-                    (void)elementwise16<true>(sv, gv, qc, col0, r, ec, diag_tile, qlimit, pp, dp);
+                    dlam += elementwise16<true>(sv, gv, qc, col0, r, ec, diag_tile, qlimit, pp, dp);
                 // P^T and dS^T pairs -> TMEM columns this warp has already read.
                 const uint32_t pc = packed_col(ks);
                 asm volatile(
@@ -344,6 +346,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&bars->p_full);
+        }
+        if (dlambda != nullptr) {
+            // dR_ii = p (g - D) = dr / k_scale; sum log(c_i) dR_ii.
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) dlam += __shfl_xor_sync(0xffffffffu, dlam, o);
+            if (lane == 0 && dlam != 0.f) atomicAdd(dlambda, dlam / k_scale);
         }
         // Epilogue: block b writes columns 32b .. 32b+31 of the dV and dP2 rows of this key tile.
         if (ok && ptx::mbar_wait_warp(&bars->mma_done, 0, abort_flag, status, kDevTimeoutMma) && 32 * blk < kp.d) {
@@ -424,8 +432,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D>
 cudaError_t launch_bwd_tc_d(const KernelProblem& kp, const void* P1, const void* P2, const void* V, const float* L,
-                            const float* Dw, const void* dY, float* dq_acc, void* dP2, void* dV, const TcLaunch& tl,
-                            cudaStream_t s) {
+                            const float* Dw, const void* dY, float* dq_acc, void* dP2, void* dV, float* dlambda,
+                            const TcLaunch& tl, cudaStream_t s) {
     using C = BwdCfg<D>;
     static_assert(C::kSmemBytes <= 232448, "shared memory budget");
     static std::once_flag attr_once;
@@ -464,7 +472,7 @@ cudaError_t launch_bwd_tc_d(const KernelProblem& kp, const void* P1, const void*
     int64_t group = (l2_bytes > 0 ? (int64_t)l2_bytes * 3 / 4 : (int64_t)96 << 20) / per_head;
     group = group < 1 ? 1 : (group > kp.BH ? kp.BH : group);
     relation_bwd_tc_kernel<D><<<dim3((unsigned)ctas), kThreads, C::kSmemBytes, s>>>(
-        m1, m2, mv, mg, mq, kp, L, Dw, (__nv_bfloat16*)dP2, (__nv_bfloat16*)dV, tl.status, (int)group);
+        m1, m2, mv, mg, mq, kp, L, Dw, (__nv_bfloat16*)dP2, (__nv_bfloat16*)dV, dlambda, tl.status, (int)group);
     return cudaGetLastError();
 }
 
@@ -475,7 +483,8 @@ cudaError_t launch_bwd_tc(const KernelProblem& kp, const void* P1, const void* P
                           const TcLaunch& tl, cudaStream_t s, bool padded64) {
     if (kp.d == 48 || kp.d == 60 || kp.d == 64)
         return launch_bwd_tc64(kp, P1, P2, V, L, Dw, dY, dq_acc, dP2, dV, dlambda, tl, s, padded64);
-    if (kp.d == 80 || kp.d == 128) return launch_bwd_tc_d<128>(kp, P1, P2, V, L, Dw, dY, dq_acc, dP2, dV, tl, s);
+    if (kp.d == 80 || kp.d == 128)
+        return launch_bwd_tc_d<128>(kp, P1, P2, V, L, Dw, dY, dq_acc, dP2, dV, dlambda, tl, s);
     return cudaErrorInvalidValue;
 }
 

@@ -77,7 +77,7 @@ struct TcLaunch {
 cudaError_t launch_fwd_tc(const KernelProblem& kp, const void* P1, const void* P2, const void* V, void* Y, float* L,
                           const TcLaunch& tl, cudaStream_t s, bool padded64 = false);
 // Whether the tensor-core backward kernel for this head width also sums dlambda.
-inline bool bwd_tc_sums_dlambda(int d) { return d <= 64; }  // the 64-wide kernel serves d = 48, 60, 64
+inline bool bwd_tc_sums_dlambda(int) { return true; }  // both tensor-core kernels sum it from the diagonal
 // padded64: P1, P2, V, dY point to zero-padded contiguous [BH, T, 64] copies
 // (made by launch_pad_operands) instead of the caller's tensors; dP2 and dV are
 // still written in the problem's layout and width.

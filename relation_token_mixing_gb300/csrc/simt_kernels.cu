@@ -139,8 +139,10 @@ __global__ void __launch_bounds__(256) bwd_prepare_kernel(KernelProblem kp, cons
         for (int c = lane; c < d; c += 32) {
             const float g = load_as_float(dY + off + c);
             dy_y = fmaf(g, load_as_float(Yf + off + c), dy_y);
-            dy_v = fmaf(g, load_as_float(V + off + c), dy_v);
-            p1p2 = fmaf(load_as_float(P1 + off + c), load_as_float(P2 + off + c), p1p2);
+            if (dlambda != nullptr) {  // the Self entry's terms, needed only for dlambda
+                dy_v = fmaf(g, load_as_float(V + off + c), dy_v);
+                p1p2 = fmaf(load_as_float(P1 + off + c), load_as_float(P2 + off + c), p1p2);
+            }
         }
         if (dq_acc != nullptr)
             for (int c = lane; c < dq_w; c += 32) dq_acc[(size_t)row * dq_w + c] = 0.f;
