@@ -415,6 +415,38 @@ __global__ void __launch_bounds__(256) convert_kernel(const float* __restrict__ 
     }
 }
 
+// Two floats as a bf16 pair (round to nearest even; the first in the low half).
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// The same for bf16 output, 8 values per thread and step (two 16-byte loads, one
+// 16-byte store), four steps' loads issued before their stores.
+__global__ void __launch_bounds__(256) convert8_bf16_kernel(const float4* __restrict__ src, uint4* __restrict__ dst,
+                                                            int64_t n8) {
+    constexpr int kUnroll = 4;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t k0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k0 < n8; k0 += kUnroll * stride) {
+        float4 a[kUnroll], b[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t k = k0 + u * stride;
+            if (k < n8) {
+                a[u] = src[2 * k];
+                b[u] = src[2 * k + 1];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t k = k0 + u * stride;
+            if (k < n8)
+                dst[k] = make_uint4(pack_bf16(a[u].x, a[u].y), pack_bf16(a[u].z, a[u].w), pack_bf16(b[u].x, b[u].y),
+                                    pack_bf16(b[u].z, b[u].w));
+        }
+    }
+}
+
 // dP1 accumulator [BH, T, dq_w] fp32 -> dP1 in the problem's layout and width;
 // one thread per 4 columns of a row.
 template <typename Tout>
@@ -589,9 +621,14 @@ cudaError_t launch_convert(const KernelProblem& kp, const float* src, int dq_w, 
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     if (kp.layout == 0 && kp.d == dq_w) {  // same layout on both sides: a flat conversion
-        if (bf16)
-            convert_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(src, (__nv_bfloat16*)dst, n4);
-        else
+        if (bf16) {  // d = dq_w is 64 or 128: whole groups of 8
+            const int64_t n8 = n4 / 2;
+            int64_t b8 = (n8 + 1023) / 1024;
+            const int64_t cap8 = (int64_t)num_sms * 16;
+            b8 = b8 > cap8 ? cap8 : (b8 < 1 ? 1 : b8);
+            convert8_bf16_kernel<<<(unsigned)b8, 256, 0, s>>>(reinterpret_cast<const float4*>(src),
+                                                              reinterpret_cast<uint4*>(dst), n8);
+        } else
             convert_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(src, (float*)dst, n4);
     } else if (bf16) {
         convert_rows_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(kp, src, dq_w, (__nv_bfloat16*)dst, n4);
