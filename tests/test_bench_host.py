@@ -1,0 +1,44 @@
+"""Host-side arithmetic of bench.py (no GPU): the visible-pair count and flop model the throughput is
+computed from, the Linear Relation byte model, and the DRAM-traffic record that the roofline reports only
+for the workload and kernel sources it was captured on."""
+import json
+import os
+import sys
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+from relation_token_mixing_gb300 import inputs as rin  # noqa: E402
+
+
+@pytest.mark.parametrize("T,causal", [(1, True), (7, True), (128, True), (7, False), (129, False)])
+def test_visible_pairs_by_brute_force(T, causal):
+    expect = sum(1 for i in range(T) for j in range(T) if (j <= i or not causal))
+    assert bench.pairs(T, causal) == expect
+
+
+def test_flops_count_every_head_and_pair():
+    w = rin.Workload("x", 2, 3, 10, 64, torch.bfloat16, 1.0, 0.5, True, 1.0)
+    assert bench.flops(w, 12) == 2 * 3 * (10 * 11 // 2) * 12 * 64
+
+
+def test_linear_bytes_per_head_token():
+    # forward: P1, P2, I~, Y in bf16 (2 bytes) and G in fp32: 4*2d + 4d = 12d
+    # backward: P1, P2, I~, dY, dP1, dP2, dI~ in bf16 and G, dG in fp32: 7*2d + 2*4d = 22d
+    for d in (48, 60, 64):
+        assert bench.linear_bytes_per_head_token(d) == 12 * d + 22 * d
+
+
+def test_recorded_traffic_is_keyed_by_workload_and_source():
+    with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+        rec = json.load(f)
+    for kernel, e in rec.items():
+        if kernel.startswith("_"):
+            continue
+        assert bench.recorded_traffic(kernel, e["source_hash"], e["workload"]) == e["bytes_per_launch"]
+        assert bench.recorded_traffic(kernel, e["source_hash"], e["workload"] + "_other") is None
+        assert bench.recorded_traffic(kernel, "0" * 16, e["workload"]) is None
+    assert bench.recorded_traffic("no_such_kernel", "0" * 16, "mhr_fwd_bwd_T4096") is None
