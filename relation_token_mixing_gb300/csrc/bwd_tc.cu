@@ -22,10 +22,12 @@
 //   elementwise: P^T, dS^T = dU^T / sqrt(d) -> TMEM (bf16) and dS^T -> smem
 //   dV  += P^T dY_i             (TS)      dP2 += dS^T P1_i     (TS)
 //   dP1_i (partial) = dS P2_j   (SS, dS read MN-major from smem)
-// TMEM: S^T [0,128) | dP^T [128,256) | dV [256,384) | dP2 [384,512); the packed
-// P^T and dS^T overwrite the S^T and dP^T columns their warp has already read
-// (block b stores its 32 queries' pairs in columns 32b..32b+15 of the region),
-// and the dP1 partial reuses the S^T columns once dV has read P^T.
+// TMEM: S^T [0,128) | dP^T [128,256) | dV [256,384) | dP2 [384,512).  Block b of
+// a lane quarter reads S^T and dP^T columns 32b..32b+31 of its rows and packs
+// its 32 queries' pairs into the dP^T columns it has read: dS^T into 32b..32b+15,
+// P^T into 32b+16..32b+31 (after both halves are in registers).  The S^T columns
+// are then free, so the dP1 partial goes there first and drains while dV and dP2
+// run.
 #include <cuda_bf16.h>
 
 #include "bwd_elementwise.cuh"
@@ -65,6 +67,8 @@ struct BwdCfg {
 // TMEM column (relative to the S^T or dP^T region) of the packed pairs of the
 // 16 queries 16ks..16ks+15: block ks/2 keeps its pairs in its own first 16 columns.
 __host__ __device__ constexpr uint32_t packed_col(int ks) { return 32u * (ks >> 1) + 8u * (ks & 1); }
+// The same queries' P^T pairs: the block's second 16 columns of the dP^T region.
+__host__ __device__ constexpr uint32_t packed_p_col(int ks) { return packed_col(ks) + 16u; }
 
 struct BwdBarriers {
     uint64_t kv_full;
@@ -247,19 +251,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             ptx::tc_fence_after();
+            // dP1 first, into the S^T columns (free now), so that it drains while dV and dP2 run.
+#pragma unroll
+            for (int ks = 0; ks < kTile / 16; ++ks)
+                ptx::mma_ss_elect(tmem + C::kColDQ, mds + ks * 128, mk + ks * 128, id_dq, ks > 0 ? 1u : 0u);
+            ptx::mma_commit_elect(&bars->dq_full);
             // K-step ks covers queries 16ks..16ks+15: 16 rows (2048 bytes) of the MN-major tiles.
 #pragma unroll
             for (int ks = 0; ks < kTile / 16; ++ks)
-                ptx::mma_ts_elect(tmem + C::kColDV, tmem + C::kColS + packed_col(ks), mg + st + ks * 128, id_tb,
+                ptx::mma_ts_elect(tmem + C::kColDV, tmem + C::kColDP + packed_p_col(ks), mg + st + ks * 128, id_tb,
                                   (it > 0 || ks > 0) ? 1u : 0u);
 #pragma unroll
             for (int ks = 0; ks < kTile / 16; ++ks)
                 ptx::mma_ts_elect(tmem + C::kColDK, tmem + C::kColDP + packed_col(ks), mq + st + ks * 128, id_tb,
                                   (it > 0 || ks > 0) ? 1u : 0u);
-#pragma unroll
-            for (int ks = 0; ks < kTile / 16; ++ks)
-                ptx::mma_ss_elect(tmem + C::kColDQ, mds + ks * 128, mk + ks * 128, id_dq, ks > 0 ? 1u : 0u);
-            ptx::mma_commit_elect(&bars->dq_full);
             ptx::mma_commit_elect(&bars->q_empty[s]);
         }
         ptx::mma_commit_elect(&bars->mma_done);
@@ -301,6 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool diag_tile = (i == jt);
             const int qlimit = T - i * kTile;  // query columns c < qlimit exist
             uint8_t* ds_row = sDS + r * 128;
+            uint32_t pp[2][8];  // P^T pairs of both halves: stored once both halves' dP^T columns are read
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 const int ks = 2 * blk + half;  // 16 queries 16ks .. 16ks+15
@@ -314,21 +320,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float4* qc = sQC + s * (kTile / 2) + col0 / 2;
                 // The masked variant is chosen per warp (uniformly) if any of its rows needs it.
                 const bool special = __any_sync(0xffffffffu, diag_tile || qlimit < col0 + 16 || !row_valid);
-                uint32_t pp[8], dp[8];
+                uint32_t dp[8];
                 if (!special)
-                    elementwise16<false>(sv, gv, qc, col0, r, ec, false, 0, pp, dp);
+                    elementwise16<false>(sv, gv, qc, col0, r, ec, false, 0, pp[half], dp);
                 else
-                    dlam += elementwise16<true>(sv, gv, qc, col0, r, ec, diag_tile, qlimit, pp, dp);
-                // P^T and dS^T pairs -> TMEM columns this warp has already read.
-                const uint32_t pc = packed_col(ks);
+                    dlam += elementwise16<true>(sv, gv, qc, col0, r, ec, diag_tile, qlimit, pp[half], dp);
+                // dS^T pairs -> dP^T columns this warp has already read.
                 asm volatile(
                     "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
-                        lane_addr + C::kColS + pc),
-                    "r"(pp[0]), "r"(pp[1]), "r"(pp[2]), "r"(pp[3]), "r"(pp[4]), "r"(pp[5]), "r"(pp[6]), "r"(pp[7])
-                    : "memory");
-                asm volatile(
-                    "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
-                        lane_addr + C::kColDP + pc),
+                        lane_addr + C::kColDP + packed_col(ks)),
                     "r"(dp[0]), "r"(dp[1]), "r"(dp[2]), "r"(dp[3]), "r"(dp[4]), "r"(dp[5]), "r"(dp[6]), "r"(dp[7])
                     : "memory");
                 // dS^T row r, queries 16ks..16ks+15: two 16-byte chunks of the
@@ -341,6 +341,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *dst = make_uint4(dp[4 * h], dp[4 * h + 1], dp[4 * h + 2], dp[4 * h + 3]);
                 }
             }
+            // Both halves' dP^T columns are read: P^T pairs -> the block's second 16 dP^T columns.
+#pragma unroll
+            for (int half = 0; half < 2; ++half)
+                asm volatile(
+                    "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
+                        lane_addr + C::kColDP + packed_p_col(2 * blk + half)),
+                    "r"(pp[half][0]), "r"(pp[half][1]), "r"(pp[half][2]), "r"(pp[half][3]), "r"(pp[half][4]),
+                    "r"(pp[half][5]), "r"(pp[half][6]), "r"(pp[half][7])
+                    : "memory");
             ptx::tmem_st_wait();
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
