@@ -33,7 +33,6 @@
 
 #include "bwd_elementwise.cuh"
 #include "kernels.h"
-#include "tile_copy.cuh"
 #include "ptx_sm100.cuh"
 #include "tmap.h"
 
@@ -107,10 +106,9 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
                  : "memory");
 }
 
-// Operand loads: TMA through 3-D maps ([B, H, T, d] layout), TMA through 4-D
-// maps ([B, T, H, d]), or cp.async from the raw pointers (head widths whose
-// rows TMA cannot address).
-enum LoadMode { kLoadTma3 = 0, kLoadTma4 = 1, kLoadCp = 2 };
+// Operand loads: TMA through 3-D maps ([B, H, T, d] layout and the zero-padded
+// copies of widths whose rows TMA cannot address) or 4-D maps ([B, T, H, d]).
+enum LoadMode { kLoadTma3 = 0, kLoadTma4 = 1 };
 template <int kLoad>
 __global__ void __launch_bounds__(kThreads, 1)
     relation_bwd_tc64_kernel(const __grid_constant__ CUtensorMap tm_p1, const __grid_constant__ CUtensorMap tm_p2,
@@ -118,9 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                              const __grid_constant__ CUtensorMap tm_dq, const KernelProblem kp,
                              const float* __restrict__ L, const float* __restrict__ Dw, __nv_bfloat16* __restrict__ dP2,
                              __nv_bfloat16* __restrict__ dV, float* __restrict__ dlambda, unsigned int* status,
-                             int head_group, const __nv_bfloat16* __restrict__ P1,
-                             const __nv_bfloat16* __restrict__ P2, const __nv_bfloat16* __restrict__ V,
-                             const __nv_bfloat16* __restrict__ dY) {
+                             int head_group) {
     constexpr bool kRank3 = kLoad == kLoadTma3;
     extern __shared__ uint8_t smem_raw[];
     Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -168,13 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // -------------------------------------------------------------- loader
         ptx::regs_dec<kRegsControl>();
-        if constexpr (kLoad == kLoadCp) {
-            cp_async_tile64(sm.k, P2, kp, bh, kv0, lane);
-            cp_async_tile64(sm.v, V, kp, bh, kv0, lane);
-            cp_async_commit();
-            cp_async_publish<0>();
-            if (lane == 0) ptx::mbar_arrive(&sm.kv_full);
-        } else if (lane == 0) {
+        if (lane == 0) {
             ptx::tma_prefetch_desc(&tm_p1);
             ptx::tma_prefetch_desc(&tm_p2);
             ptx::tma_prefetch_desc(&tm_v);
@@ -212,16 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 qc[(col >> 1) * 4 + (col & 1)] = nlt[k];
                 qc[(col >> 1) * 4 + 2 + (col & 1)] = ndk[k];
             }
-            if constexpr (kLoad == kLoadCp) {
-                // Tile i is issued, then tile i-1 (copies and constants) is published.
-                cp_async_tile64(sm.q[s], P1, kp, bh, i * kTile, lane);
-                cp_async_tile64(sm.g[s], dY, kp, bh, i * kTile, lane);
-                cp_async_commit();
-                if (it > 0) {
-                    cp_async_publish<1>();
-                    ptx::mbar_arrive(&sm.q_full[(it - 1) % kQStages]);
-                }
-            } else if (lane == 0) {
+            if (lane == 0) {
                 ptx::mbar_arrive_expect_tx(&sm.q_full[s], 2 * kTileBytes);
                 ptx::tma_load_operand(sm.q[s], &tm_p1, &sm.q_full[s], 0, i * kTile, bh, head, batch,
                                       kRank3);
@@ -231,11 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::mbar_arrive(&sm.q_full[s]);
             }
         }
-        if constexpr (kLoad == kLoadCp) {
-            cp_async_publish<0>();  // every copy has landed before the warp moves on
-            if (it == n_q && n_q > 0) ptx::mbar_arrive(&sm.q_full[(n_q - 1) % kQStages]);
-        }
-        if (kLoad != kLoadCp && lane == 0 && *abort_flag) {
+        if (lane == 0 && *abort_flag) {
             drain_wait(&sm.kv_full, 0);
             for (int jj = max(0, it - kQStages); jj < it; ++jj)
                 drain_wait(&sm.q_full[jj % kQStages], (jj / kQStages) & 1);
@@ -528,9 +505,8 @@ cudaError_t launch_bwd_tc64(const KernelProblem& kp, const void* P1, const void*
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        const void* fns[3] = {(const void*)relation_bwd_tc64_kernel<kLoadTma3>,
-                              (const void*)relation_bwd_tc64_kernel<kLoadTma4>,
-                              (const void*)relation_bwd_tc64_kernel<kLoadCp>};
+        const void* fns[2] = {(const void*)relation_bwd_tc64_kernel<kLoadTma3>,
+                              (const void*)relation_bwd_tc64_kernel<kLoadTma4>};
         for (const void* f : fns)
             if (attr_err == cudaSuccess)
                 attr_err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -538,14 +514,15 @@ cudaError_t launch_bwd_tc64(const KernelProblem& kp, const void* P1, const void*
     if (attr_err != cudaSuccess) return attr_err;
     // Operands in the problem's layout; heads narrower than 64 read as 64-wide
     // tiles whose extra columns are zero (so they add nothing to any product).
-    // Padded copies: contiguous rows of 64.  Else d * 2 bytes not a multiple of 16:
-    // TMA cannot step through the rows.
-    const int mode = padded64 ? kLoadTma3 : (kp.d * 2) % 16 != 0 ? kLoadCp : (kp.layout == 0 ? kLoadTma3 : kLoadTma4);
+    // Rows TMA cannot step through (d * 2 bytes not a multiple of 16) arrive as
+    // zero-padded contiguous copies of 64 columns (padded64).
+    if (!padded64 && (kp.d * 2) % 16 != 0) return cudaErrorInvalidValue;
+    const int mode = padded64 ? kLoadTma3 : (kp.layout == 0 ? kLoadTma3 : kLoadTma4);
     const int map_d = padded64 ? 64 : kp.d, map_layout = padded64 ? 0 : kp.layout;
     CUtensorMap m1{}, m2{}, mv{}, mg{}, mq{};
     const void* bases[4] = {P1, P2, V, dY};
     CUtensorMap* maps[4] = {&m1, &m2, &mv, &mg};
-    for (int k = 0; k < 4 && mode != kLoadCp; ++k) {
+    for (int k = 0; k < 4; ++k) {
         cudaError_t e =
             make_operand_map(maps[k], bases[k], kp.BH / kp.H, kp.H, kp.T, map_d, map_layout, 64, 128, true);
         if (e != cudaSuccess) return e;
@@ -569,18 +546,14 @@ cudaError_t launch_bwd_tc64(const KernelProblem& kp, const void* P1, const void*
     int64_t group = (l2_bytes > 0 ? (int64_t)l2_bytes * 3 / 4 : (int64_t)96 << 20) / per_head;
     group = group < 1 ? 1 : (group > kp.BH ? kp.BH : group);
     dim3 grid((unsigned)ctas);
-    const __nv_bfloat16 *p1 = (const __nv_bfloat16*)P1, *p2 = (const __nv_bfloat16*)P2,
-                        *v = (const __nv_bfloat16*)V, *g = (const __nv_bfloat16*)dY;
 #define RELATION_BWD64(M)                                                                                        \
     relation_bwd_tc64_kernel<M><<<grid, kThreads, kSmemBytes, s>>>(m1, m2, mv, mg, mq, kp, L, Dw,                 \
                                                                   (__nv_bfloat16*)dP2, (__nv_bfloat16*)dV, dlambda, \
-                                                                  tl.status, (int)group, p1, p2, v, g)
+                                                                  tl.status, (int)group)
     if (mode == kLoadTma3)
         RELATION_BWD64(kLoadTma3);
-    else if (mode == kLoadTma4)
-        RELATION_BWD64(kLoadTma4);
     else
-        RELATION_BWD64(kLoadCp);
+        RELATION_BWD64(kLoadTma4);
 #undef RELATION_BWD64
     return cudaGetLastError();
 }
