@@ -130,9 +130,11 @@ relation_status_t relation_bwd(const relation_problem_t* p, const void* P1, cons
 
 /*
  * The three stages relation_bwd runs in order, with the same arguments, for
- * callers that time or schedule them separately.  prepare: D_i, dlambda and
- * the dP1 accumulator reset.  main: the tensor-core (or fp32) pass producing
- * dP2, dV and the dP1 partial sums.  finish: dP1 accumulator to dtype.
+ * callers that time or schedule them separately.  prepare: D_i, dlambda set to
+ * zero (and, on the fp32 path, summed), the dP1 accumulator reset and, for bf16
+ * d_h = 60, the zero-padded operand copies in the workspace.  main: the
+ * tensor-core (or fp32) pass producing dP2, dV, the dP1 partial sums and, for
+ * bf16, dlambda.  finish: dP1 accumulator to dtype.
  */
 relation_status_t relation_bwd_prepare(const relation_problem_t* p, const void* P1, const void* P2,
                                        const void* V, const void* Y, const float* L,
