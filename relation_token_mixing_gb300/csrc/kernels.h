@@ -38,8 +38,8 @@ cudaError_t launch_givens(const KernelProblem& kp, bool bf16, const void* x, con
                           const float* theta, int pairing, bool transpose, float* dtheta, int num_sms,
                           cudaStream_t s);
 // Relation Cache decode: kp.T is the cache capacity (rows per head of the caches,
-// stored in kp.layout); part holds decode_chunks(kp) x (d + 2) floats per head.
-int decode_chunks(const KernelProblem& kp);
+// stored in kp.layout); part holds decode_chunks(kp, bf16) x (d + 2) floats per head.
+int decode_chunks(const KernelProblem& kp, bool bf16);
 cudaError_t launch_decode(const KernelProblem& kp, bool bf16, const void* P1n, const void* P2n, const void* Vn,
                           void* P2c, void* Vc, const int* pos, int append, void* Y, float* L, float* part,
                           unsigned int* status, cudaStream_t s);

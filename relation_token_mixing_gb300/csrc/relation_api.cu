@@ -583,7 +583,7 @@ relation_status_t relation_linear_bwd(const relation_problem_t* p, const void* P
 size_t relation_decode_workspace_bytes(const relation_problem_t* p) {
     if (check_problem(p) != RELATION_OK) return 0;
     const KernelProblem kp = kernel_problem(p);
-    return (size_t)kp.BH * (size_t)decode_chunks(kp) * (size_t)(p->d_h + 2) * sizeof(float);
+    return (size_t)kp.BH * (size_t)decode_chunks(kp, p->dtype == RELATION_BF16) * (size_t)(p->d_h + 2) * sizeof(float);
 }
 
 relation_status_t relation_decode(const relation_problem_t* p, const void* P1_new, const void* P2_new,
