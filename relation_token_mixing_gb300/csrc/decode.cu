@@ -8,8 +8,10 @@
 // The cache update appends p2_{t+1} and I~_{t+1} (Appendix A.5.3).
 //
 // The pass is HBM-bound (it reads 2 t d values per head), so it runs on CUDA
-// cores in fp32: split over key chunks (each CTA streams its chunk once with a
-// running softmax per group of lanes), then one CTA per head merges the chunks.
+// cores in fp32, split over key chunks: each CTA reads its chunk's cached rows
+// once (by two bulk copies into shared memory where the rows allow it, else by
+// direct 16- or 8-byte loads), computes the chunk's scores, maximum, weights and
+// weighted sum, and one CTA per head then merges the chunks.
 #include <math.h>
 
 #include <mutex>

@@ -143,6 +143,19 @@ def test_forward_workspace_size_and_checks(lib):
     assert call(_prob(d_h=50)) == 2
 
 
+@pytest.mark.parametrize("d,dtype,layout,chunk", [
+    (64, "bf16", "bhtd", 256), (48, "bf16", "bhtd", 256), (80, "bf16", "bhtd", 128), (128, "bf16", "bhtd", 128),
+    (60, "bf16", "bhtd", 512), (64, "bf16", "bthd", 512), (64, "f32", "bhtd", 128), (60, "f32", "bhtd", 128),
+    (128, "f32", "bhtd", 64), (128, "f32", "bthd", 512)])
+def test_decode_workspace_follows_the_chunk_of_its_path(d, dtype, layout, chunk):
+    """Chunk partials (m, l, o[d]) per head and chunk: chunks of 256/128/64 keys (both tensors' rows within
+    64 KB) on the bulk-copy path ([B, H, T, d], rows a multiple of 16 bytes), 512 keys otherwise."""
+    B, H, T = 2, 3, 1000
+    p = _prob(B=B, H=H, T=T, d_h=d, dtype=rb.RELATION_BF16 if dtype == "bf16" else rb.RELATION_F32,
+              layout=rb.RELATION_LAYOUT_BHTD if layout == "bhtd" else rb.RELATION_LAYOUT_BTHD)
+    assert rb.relation_decode_workspace_bytes(p) == B * H * ((T + chunk - 1) // chunk) * (d + 2) * 4
+
+
 def test_wait_selftest_limit_is_checked(lib):
     """Limits outside 1..10000 ms are rejected before any device call."""
     for ms in (0, 10001, 2 ** 31):
