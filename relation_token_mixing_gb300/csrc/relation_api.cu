@@ -93,8 +93,10 @@ KernelProblem kernel_problem(const relation_problem_t* p) {
     return kp;
 }
 
-// Every bf16 problem runs on the tensor cores (d_h = 60, whose 120-byte rows TMA
-// cannot step through, loads its tiles with cp.async instead).
+// Every bf16 problem runs on the tensor cores.  d_h = 60, whose 120-byte rows TMA
+// cannot step through, reads zero-padded copies of its operands (relation_fwd_ws
+// and the backward), or copies its tiles with cp.async (relation_fwd without a
+// workspace).
 bool use_tensor_cores(const relation_problem_t* p) { return p->dtype == RELATION_BF16; }
 
 // Width of the fp32 dP1 accumulator rows: the tensor-core tile width that the
