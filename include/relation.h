@@ -56,7 +56,7 @@ extern "C" {
 typedef enum {
     RELATION_OK = 0,
     RELATION_ERR_INVALID_ARGUMENT = 1, /* bad size, NULL pointer, tau_S <= 0, aliasing */
-    RELATION_ERR_UNSUPPORTED = 2,      /* d_h or dtype this build has no kernel for */
+    RELATION_ERR_UNSUPPORTED = 2,      /* d_h or dtype the library has no kernel for */
     RELATION_ERR_MISALIGNED = 3,       /* a tensor pointer is not 16-byte aligned */
     RELATION_ERR_WORKSPACE_TOO_SMALL = 4,
     RELATION_ERR_CUDA = 5,             /* a CUDA runtime call or launch failed */
