@@ -38,6 +38,13 @@
  *    64- / 128-wide tiles) or RELATION_F32 (fp32 CUDA-core path); any T >= 1;
  *    causal or not; either layout.  Other widths return
  *    RELATION_ERR_UNSUPPORTED.
+ *  - Sizes: B, H, T >= 1; B, H, T and B*H at most 2^31 - 1; B*H*T at most
+ *    2^33 rows and B*H*T*d_h at most 10^12 elements (beyond:
+ *    RELATION_ERR_INVALID_ARGUMENT).  Two paths have tighter launch-grid
+ *    limits and return RELATION_ERR_UNSUPPORTED before enqueuing anything:
+ *    the bf16 forward takes T <= 16,776,960 and the fp32 forward and backward
+ *    B*H <= 65535; decoding's limit is stated with relation_decode.  The
+ *    workspace queries return 0 for such problems.
  *  - No entry point throws, aborts, or falls back to the CPU.
  */
 #ifndef RELATION_GB300_RELATION_H_
@@ -56,7 +63,7 @@ extern "C" {
 typedef enum {
     RELATION_OK = 0,
     RELATION_ERR_INVALID_ARGUMENT = 1, /* bad size, NULL pointer, tau_S <= 0, aliasing */
-    RELATION_ERR_UNSUPPORTED = 2,      /* d_h or dtype the library has no kernel for */
+    RELATION_ERR_UNSUPPORTED = 2,      /* d_h, dtype or size the library has no kernel for */
     RELATION_ERR_MISALIGNED = 3,       /* a tensor pointer is not 16-byte aligned */
     RELATION_ERR_WORKSPACE_TOO_SMALL = 4,
     RELATION_ERR_CUDA = 5,             /* a CUDA runtime call or launch failed */
@@ -187,6 +194,11 @@ relation_status_t relation_bwd_noalloc(const relation_problem_t* p, const void* 
  *
  * p: B, H, d_h, dtype, tau_S, lambda, layout as for relation_fwd; p->T is the
  *    cache capacity (rows per head); p->causal is ignored (decoding is causal).
+ *    The capacity is read in at most 8192 chunks: T <= 2,097,152 for bf16
+ *    d_h 48 or 64 in the [B, H, T, d_h] layout; 1,048,576 for bf16 d_h 80 or
+ *    128 and fp32 d_h 48, 60 or 64 in that layout; 524,288 for fp32 d_h 80 or
+ *    128 in that layout; 4,194,304 for [B, T, H, d_h] caches and bf16 d_h 60.
+ *    A larger capacity returns RELATION_ERR_UNSUPPORTED.
  * P1_new, P2_new, V_new: [B, H, d_h] (dtype), the new token's states.
  * P2_cache, V_cache: [B, H, T, d_h] or [B, T, H, d_h] per p->layout (dtype);
  *    rows 0 .. positions[b]-1 of batch b hold the history.

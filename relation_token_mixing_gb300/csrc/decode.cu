@@ -359,7 +359,7 @@ template <typename Tin>
 __global__ void __launch_bounds__(128) decode_combine_kernel(KernelProblem kp, const float* __restrict__ part,
                                                               int n_chunks, Tin* __restrict__ Y,
                                                               float* __restrict__ L) {
-    extern __shared__ float w[];  // per chunk: e^{m_c - M}, then the denominator at w[n_chunks]
+    extern __shared__ float w[];  // per chunk: its maximum m_c, then its weight e^{m_c - M}
     __shared__ float red[4];
     const int64_t bh = blockIdx.x;
     const int d = kp.d;
@@ -463,15 +463,18 @@ cudaError_t launch_decode_t(const KernelProblem& kp, const void* P1n, const void
 
 int decode_chunks(const KernelProblem& kp, bool bf16) {
     const int c = decode_chunk_rows(kp, bf16);
-    return (kp.T + c - 1) / c;
+    return (int)(((int64_t)kp.T + c - 1) / c);
+}
+
+bool decode_grid_fits(const KernelProblem& kp, bool bf16) {
+    return kp.BH >= 1 && kp.BH <= 2147483647LL && decode_chunks(kp, bf16) <= kDecodeMaxChunks;
 }
 
 cudaError_t launch_decode(const KernelProblem& kp, bool bf16, const void* P1n, const void* P2n, const void* Vn,
                           void* P2c, void* Vc, const int* pos, int append, void* Y, float* L, float* part,
                           unsigned int* status, cudaStream_t s) {
     const int n_chunks = decode_chunks(kp, bf16);
-    // Chunk statistics of a head fit in 32 KB of shared memory in the merge.
-    if (kp.BH > 2147483647LL || n_chunks > 8192) return cudaErrorInvalidValue;
+    if (!decode_grid_fits(kp, bf16)) return cudaErrorInvalidValue;
     const bool bulk = decode_bulk(kp, bf16);
     const int chunk = decode_chunk_rows(kp, bf16);
     // Vector width and lanes per key row by (dtype, d): rows are read 16 bytes per

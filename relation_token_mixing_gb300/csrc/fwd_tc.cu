@@ -579,6 +579,11 @@ cudaError_t launch_fwd_tc_d(const KernelProblem& kp, const void* P1, const void*
 
 }  // namespace
 
+bool fwd_tc_grid_fits(const KernelProblem& kp) {
+    // Heads in gridDim.x, pairs of kBM-row query tiles in gridDim.y (at most 65535).
+    return kp.BH >= 1 && kp.BH <= 2147483647LL && ((int64_t)kp.T + 2 * kBM - 1) / (2 * kBM) <= 65535;
+}
+
 cudaError_t launch_fwd_tc(const KernelProblem& kp, const void* P1, const void* P2, const void* V, void* Y, float* L,
                           const TcLaunch& tl, cudaStream_t s, bool padded64) {
     if (kp.BH > 2147483647LL) return cudaErrorInvalidValue;

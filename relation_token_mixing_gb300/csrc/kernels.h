@@ -8,7 +8,9 @@
 
 namespace relation {
 
-// float32 CUDA-core path (also instantiated for bf16 storage).
+// float32 CUDA-core path (also instantiated for bf16 storage).  Its grids hold
+// the heads in gridDim.y: simt_grid_fits() says whether a problem fits.
+bool simt_grid_fits(const KernelProblem& kp);
 cudaError_t launch_fwd_simt(const KernelProblem& kp, bool bf16, const void* P1, const void* P2, const void* V,
                             void* Y, float* L, cudaStream_t s);
 cudaError_t launch_bwd_simt(const KernelProblem& kp, bool bf16, const void* P1, const void* P2, const void* V,
@@ -40,6 +42,9 @@ cudaError_t launch_givens(const KernelProblem& kp, bool bf16, const void* x, con
 // Relation Cache decode: kp.T is the cache capacity (rows per head of the caches,
 // stored in kp.layout); part holds decode_chunks(kp, bf16) x (d + 2) floats per head.
 int decode_chunks(const KernelProblem& kp, bool bf16);
+// The merge keeps one float per chunk of a head in shared memory (32 KB at most).
+constexpr int kDecodeMaxChunks = 8192;
+bool decode_grid_fits(const KernelProblem& kp, bool bf16);
 cudaError_t launch_decode(const KernelProblem& kp, bool bf16, const void* P1n, const void* P2n, const void* Vn,
                           void* P2c, void* Vc, const int* pos, int append, void* Y, float* L, float* part,
                           unsigned int* status, cudaStream_t s);
@@ -76,6 +81,8 @@ struct TcLaunch {
 // Y and L are written in the problem's layout and width.
 cudaError_t launch_fwd_tc(const KernelProblem& kp, const void* P1, const void* P2, const void* V, void* Y, float* L,
                           const TcLaunch& tl, cudaStream_t s, bool padded64 = false);
+// Whether the forward's grid (heads x query-tile pairs) fits the launch limits.
+bool fwd_tc_grid_fits(const KernelProblem& kp);
 // Whether the tensor-core backward kernel for this head width also sums dlambda.
 inline bool bwd_tc_sums_dlambda(int) { return true; }  // both tensor-core kernels sum it from the diagonal
 // padded64: P1, P2, V, dY point to zero-padded contiguous [BH, T, 64] copies

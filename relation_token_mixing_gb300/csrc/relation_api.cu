@@ -70,6 +70,10 @@ relation_status_t check_problem(const relation_problem_t* p) {
     if (p->B < 1 || p->H < 1 || p->T < 1 || p->d_h < 1) return RELATION_ERR_INVALID_ARGUMENT;
     if (p->T > (int64_t)INT32_MAX || p->B > (int64_t)INT32_MAX || p->H > (int64_t)INT32_MAX)
         return RELATION_ERR_INVALID_ARGUMENT;
+    // Heads index gridDim.x (at most 2^31 - 1); 2^33 rows keep every one-dimensional
+    // grid over rows or row tiles in range.  Both allow tensors far beyond one GPU.
+    if (p->B * p->H > (int64_t)INT32_MAX || p->B * p->H * p->T > ((int64_t)1 << 33))
+        return RELATION_ERR_INVALID_ARGUMENT;
     const double elems = (double)p->B * (double)p->H * (double)p->T * (double)p->d_h;
     if (elems > 1.0e12) return RELATION_ERR_INVALID_ARGUMENT;
     if (p->dtype != RELATION_F32 && p->dtype != RELATION_BF16) return RELATION_ERR_INVALID_ARGUMENT;
@@ -98,6 +102,18 @@ KernelProblem kernel_problem(const relation_problem_t* p) {
 // and the backward), or copies its tiles with cp.async (relation_fwd without a
 // workspace).
 bool use_tensor_cores(const relation_problem_t* p) { return p->dtype == RELATION_BF16; }
+
+// Launch-grid limits tighter than the generic ones, per path, checked before any
+// work is enqueued: the tensor-core forward holds query-tile pairs in gridDim.y,
+// the CUDA-core path the heads, and decoding keeps its chunk count bounded.
+// (The backward's tensor-core grid is one-dimensional and within the generic limits.)
+bool fwd_fits(const relation_problem_t* p) {
+    return use_tensor_cores(p) ? fwd_tc_grid_fits(kernel_problem(p)) : simt_grid_fits(kernel_problem(p));
+}
+bool bwd_fits(const relation_problem_t* p) { return use_tensor_cores(p) || simt_grid_fits(kernel_problem(p)); }
+bool decode_fits(const relation_problem_t* p) {
+    return decode_grid_fits(kernel_problem(p), p->dtype == RELATION_BF16);
+}
 
 // Width of the fp32 dP1 accumulator rows: the tensor-core tile width that the
 // head width is padded to.
@@ -142,6 +158,7 @@ struct BwdArgs {
 relation_status_t check_bwd(const BwdArgs& a) {
     relation_status_t st = check_problem(a.p);
     if (st != RELATION_OK) return st;
+    if (!bwd_fits(a.p)) return RELATION_ERR_UNSUPPORTED;
     const void* ins[] = {a.P1, a.P2, a.V, a.Y, a.L, a.dY};
     void* outs[] = {a.dP1, a.dP2, a.dV};
     for (const void* x : ins)
@@ -238,6 +255,7 @@ relation_status_t run_fwd(const relation_problem_t* p, const void* P1, const voi
                           float* L, void* workspace, size_t workspace_bytes, bool with_ws, cudaStream_t s) {
     relation_status_t st = check_problem(p);
     if (st != RELATION_OK) return st;
+    if (!fwd_fits(p)) return RELATION_ERR_UNSUPPORTED;
     if (!P1 || !P2 || !V || !Y) return RELATION_ERR_INVALID_ARGUMENT;
     if (!aligned16(P1) || !aligned16(P2) || !aligned16(V) || !aligned16(Y) || (L && !aligned16(L)))
         return RELATION_ERR_MISALIGNED;
@@ -310,7 +328,7 @@ relation_status_t relation_fwd(const relation_problem_t* p, const void* P1, cons
 }
 
 size_t relation_fwd_workspace_bytes(const relation_problem_t* p) {
-    if (check_problem(p) != RELATION_OK) return 0;
+    if (check_problem(p) != RELATION_OK || !fwd_fits(p)) return 0;
     return fwd_workspace_bytes(p);
 }
 
@@ -320,7 +338,7 @@ relation_status_t relation_fwd_ws(const relation_problem_t* p, const void* P1, c
 }
 
 size_t relation_bwd_workspace_bytes(const relation_problem_t* p) {
-    if (check_problem(p) != RELATION_OK) return 0;
+    if (check_problem(p) != RELATION_OK || !bwd_fits(p)) return 0;
     return workspace_layout(p, nullptr);
 }
 
@@ -583,7 +601,7 @@ relation_status_t relation_linear_bwd(const relation_problem_t* p, const void* P
 }
 
 size_t relation_decode_workspace_bytes(const relation_problem_t* p) {
-    if (check_problem(p) != RELATION_OK) return 0;
+    if (check_problem(p) != RELATION_OK || !decode_fits(p)) return 0;
     const KernelProblem kp = kernel_problem(p);
     return (size_t)kp.BH * (size_t)decode_chunks(kp, p->dtype == RELATION_BF16) * (size_t)(p->d_h + 2) * sizeof(float);
 }
@@ -594,6 +612,7 @@ relation_status_t relation_decode(const relation_problem_t* p, const void* P1_ne
                                   void* stream) {
     relation_status_t st = check_problem(p);
     if (st != RELATION_OK) return st;
+    if (!decode_fits(p)) return RELATION_ERR_UNSUPPORTED;
     const void* ptrs[] = {P1_new, P2_new, V_new, P2_cache, V_cache, positions, Y, workspace};
     for (const void* x : ptrs)
         if (x == nullptr) return RELATION_ERR_INVALID_ARGUMENT;
@@ -630,7 +649,7 @@ const char* relation_status_string(relation_status_t s) {
     switch (s) {
         case RELATION_OK: return "ok";
         case RELATION_ERR_INVALID_ARGUMENT: return "invalid argument";
-        case RELATION_ERR_UNSUPPORTED: return "unsupported problem (no kernel for this head width or dtype)";
+        case RELATION_ERR_UNSUPPORTED: return "unsupported problem (no kernel for this head width, dtype or size)";
         case RELATION_ERR_MISALIGNED: return "tensor pointer not 16-byte aligned";
         case RELATION_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than relation_bwd_workspace_bytes()";
         case RELATION_ERR_CUDA: return "CUDA runtime error";

@@ -534,6 +534,11 @@ cudaError_t launch_bwd_simt_t(const KernelProblem& kp, const void* P1, const voi
 
 }  // namespace
 
+bool simt_grid_fits(const KernelProblem& kp) {
+    // Row blocks in gridDim.x, heads in gridDim.y (at most 65535).
+    return kp.BH >= 1 && kp.BH <= 65535 && ((int64_t)kp.T + kRows - 1) / kRows <= 2147483647LL;
+}
+
 cudaError_t launch_fwd_simt(const KernelProblem& kp, bool bf16, const void* P1, const void* P2, const void* V,
                             void* Y, float* L, cudaStream_t s) {
     return bf16 ? launch_fwd_simt_t<__nv_bfloat16>(kp, P1, P2, V, Y, L, s)

@@ -156,6 +156,56 @@ def test_decode_workspace_follows_the_chunk_of_its_path(d, dtype, layout, chunk)
     assert rb.relation_decode_workspace_bytes(p) == B * H * ((T + chunk - 1) // chunk) * (d + 2) * 4
 
 
+def test_size_bounds_of_every_entry_point():
+    """B*H at most 2^31 - 1 (heads index gridDim.x) and B*H*T at most 2^33 rows (one-dimensional
+    grids over rows stay in range); both far beyond what one GPU holds."""
+    ws = rb.relation_bwd_workspace_bytes
+    assert ws(_prob(B=2 ** 16, H=2 ** 15, T=1, d_h=48)) == 0          # B*H = 2^31
+    assert ws(_prob(B=2 ** 16, H=2 ** 15 - 1, T=1, d_h=48)) > 0
+    assert ws(_prob(B=2 ** 6, H=2 ** 10, T=2 ** 17 + 1, d_h=48)) == 0   # 2^33 + 2^16 rows
+    assert ws(_prob(B=2 ** 6, H=2 ** 10, T=2 ** 17, d_h=48)) > 0        # exactly 2^33 rows
+    assert rb.relation_decode_workspace_bytes(_prob(B=2 ** 16, H=2 ** 15, T=1, d_h=48)) == 0
+
+
+def test_launch_grid_limits_are_refused_before_any_launch(lib):
+    """The tensor-core forward holds pairs of 128-row query tiles in gridDim.y (at most 65535), so
+    T <= 16,776,960; the CUDA-core (fp32) path holds the heads there, so B*H <= 65535.  Beyond:
+    RELATION_ERR_UNSUPPORTED and a workspace size of 0.  At the limit the calls go on to pointer
+    validation, which the fake, overlapping addresses here fail (status 1)."""
+    t_max = 65535 * 256
+    assert _fwd(lib, _prob(B=1, H=1, T=t_max + 1)) == 2
+    assert _fwd(lib, _prob(B=1, H=1, T=t_max)) == 1
+    assert rb.relation_fwd_workspace_bytes(_prob(B=1, H=1, T=t_max + 1, d_h=60)) == 0
+    assert rb.relation_fwd_workspace_bytes(_prob(B=1, H=1, T=t_max, d_h=60)) > 0
+    # the backward's tensor-core grid is one-dimensional: the same length is fine there
+    assert rb.relation_bwd_workspace_bytes(_prob(B=1, H=1, T=t_max + 1)) > 0
+    f32 = rb.RELATION_F32
+    for B, H in ((65536, 1), (256, 257)):
+        assert _fwd(lib, _prob(B=B, H=H, T=1, dtype=f32)) == 2
+        assert rb.relation_bwd_workspace_bytes(_prob(B=B, H=H, T=1, dtype=f32)) == 0
+        assert rb.relation_bwd_workspace_bytes(_prob(B=B, H=H, T=1)) > 0   # bf16: tensor-core path
+    assert _fwd(lib, _prob(B=65535, H=1, T=1, dtype=f32)) == 1
+    assert rb.relation_bwd_workspace_bytes(_prob(B=65535, H=1, T=1, dtype=f32)) > 0
+
+
+@pytest.mark.parametrize("d,dtype,layout,chunk", [
+    (64, "bf16", "bhtd", 256), (48, "bf16", "bhtd", 256), (80, "bf16", "bhtd", 128), (128, "bf16", "bhtd", 128),
+    (60, "bf16", "bhtd", 512), (64, "bf16", "bthd", 512), (64, "f32", "bhtd", 128), (48, "f32", "bhtd", 128),
+    (60, "f32", "bhtd", 128), (80, "f32", "bhtd", 64), (128, "f32", "bhtd", 64), (128, "f32", "bthd", 512)])
+def test_decode_capacity_limit(lib, d, dtype, layout, chunk):
+    """Decoding reads a cache of capacity T in at most 8192 chunks (the merge keeps one float per
+    chunk in shared memory); a larger capacity is refused with RELATION_ERR_UNSUPPORTED before
+    anything is enqueued, and its workspace size is 0."""
+    kw = dict(B=1, H=2, d_h=d, dtype=rb.RELATION_BF16 if dtype == "bf16" else rb.RELATION_F32,
+              layout=rb.RELATION_LAYOUT_BHTD if layout == "bhtd" else rb.RELATION_LAYOUT_BTHD)
+    cap = 8192 * chunk
+    assert rb.relation_decode_workspace_bytes(_prob(T=cap, **kw)) == 2 * 8192 * (d + 2) * 4
+    assert rb.relation_decode_workspace_bytes(_prob(T=cap + 1, **kw)) == 0
+    p = _prob(T=cap + 1, **kw)
+    assert lib.relation_decode(ctypes.byref(p), A, 2 * A, 3 * A, 4 * A, 5 * A, 6 * A, 0, 7 * A, None, 8 * A,
+                               1 << 30, None) == 2
+
+
 def test_wait_selftest_limit_is_checked(lib):
     """Limits outside 1..10000 ms are rejected before any device call."""
     for ms in (0, 10001, 2 ** 31):
