@@ -59,8 +59,8 @@ __device__ __forceinline__ void store_bf16x8(__nv_bfloat16* row, int c, int d, u
 // those heads, then tile 1, and so on (heaviest first for causal masks), so the
 // causal tail stays short while the heads in flight at any time stay few enough
 // for their inputs and fp32 accumulators to remain in L2.
-__device__ __forceinline__ void grouped_tile_order(unsigned idx, int64_t BH, int n_tiles, int group, int& bh,
-                                                   int& tile) {
+__host__ __device__ __forceinline__ void grouped_tile_order(unsigned idx, int64_t BH, int n_tiles, int group,
+                                                            int& bh, int& tile) {
     const unsigned per_group = (unsigned)group * (unsigned)n_tiles;
     const int64_t g = idx / per_group;
     const int r = (int)(idx - g * per_group);
