@@ -42,3 +42,38 @@ def test_recorded_traffic_is_keyed_by_workload_and_source():
         assert bench.recorded_traffic(kernel, e["source_hash"], e["workload"] + "_other") is None
         assert bench.recorded_traffic(kernel, "0" * 16, e["workload"]) is None
     assert bench.recorded_traffic("no_such_kernel", "0" * 16, "mhr_fwd_bwd_T4096") is None
+
+
+@pytest.mark.parametrize("B,H,per_head_s,expect_heads,expect_shape", [
+    (4, 16, 0.125, 64, (4, 16)),     # first pass 0.5 s: grows to the whole workload (8 s)
+    (64, 16, 0.125, 96, (6, 16)),    # grows by 24 (12 s / 0.5 s), six whole batches
+    (4, 16, 10.0, 4, (1, 4)),        # first pass 40 s: no second pass
+    (1, 3, 0.1, 3, (1, 3)),          # fewer heads than threads: one pass over all of them
+])
+def test_cpu_baseline_sample_grows_toward_its_target(monkeypatch, B, H, per_head_s, expect_heads, expect_shape):
+    """The oracle pass is sized in whole multiples of the oracle's thread count toward the target
+    time, at most the whole workload; the reported value is from the last pass.  The oracle and
+    the clock are stand-ins here, so only the sizing rule runs."""
+    import oracle
+
+    now = [0.0]
+    passes = []
+
+    def fake_fwd(P1, *a, **k):
+        heads = P1.shape[0] * P1.shape[1]
+        passes.append((P1.shape[0], P1.shape[1]))
+        now[0] += per_head_s * heads
+
+    monkeypatch.setattr(oracle, "threads", lambda: 4)
+    monkeypatch.setattr(oracle, "fwd", fake_fwd)
+    monkeypatch.setattr(oracle, "bwd", lambda *a, **k: None)
+    monkeypatch.setattr(bench.time, "perf_counter", lambda: now[0])
+    w = rin.Workload("x", B, H, 8, 64, torch.bfloat16, 1.0, 0.5, True, 1.0, backward=True)
+    out = bench.cpu_baseline(w, target_s=12.0)
+    assert passes[-1] == expect_shape and passes[-1][0] * passes[-1][1] == expect_heads
+    assert len(passes) == (2 if expect_heads > min(4, B * H) else 1)
+    dt = per_head_s * expect_heads
+    sample = rin.Workload("x", *expect_shape, 8, 64, torch.bfloat16, 1.0, 0.5, True, 1.0)
+    assert out["value"] == pytest.approx(bench.flops(sample, 12) / dt / 1e12)
+    assert out["cores"] == 4 and out["kind"] == "oracle"
+    assert ("the whole workload" in out["sample"]) == (expect_heads == B * H)
