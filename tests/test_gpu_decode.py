@@ -59,6 +59,14 @@ CASES = [
     ("bf16_d128", 1, 4, 2100, 128, torch.bfloat16, [2047], BHTD),
     ("f32_d64", 2, 2, 600, 64, torch.float32, [0, 599], BHTD),
     ("f32_d60_bthd", 2, 2, 300, 60, torch.float32, [17, 290], BTHD),
+    # the remaining bulk-copy instantiations ([B, H, T, d], 16-byte rows), with the new token
+    # first in its chunk (that chunk copies no cached row) and last in its chunk
+    ("bf16_d80", 2, 2, 700, 80, torch.bfloat16, [128, 699], BHTD),
+    ("f32_d48", 2, 2, 600, 48, torch.float32, [127, 599], BHTD),
+    ("f32_d60", 2, 2, 300, 60, torch.float32, [128, 299], BHTD),
+    ("f32_d80", 2, 2, 400, 80, torch.float32, [64, 399], BHTD),
+    ("f32_d128", 2, 2, 300, 128, torch.float32, [63, 299], BHTD),
+    ("f32_d128_bthd", 2, 2, 300, 128, torch.float32, [100, 299], BTHD),
 ]
 
 
