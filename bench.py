@@ -161,6 +161,52 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def decode_bytes_per_step(w, t: int) -> int:
+    """Algorithmic HBM bytes of one decoding step (bf16): both caches' t rows, the new token's
+    three rows, Y and L, for every head."""
+    e = 2
+    return w.B * w.H * (2 * t * w.d * e + 3 * w.d * e + w.d * e + 4)
+
+
+def decode_kernels(w) -> str:
+    """The decoding kernels the bench's [B, H, T, d] bf16 caches run on."""
+    part = "decode_partial_bulk_kernel" if (w.d * 2) % 16 == 0 else "decode_partial_kernel"
+    return f"{part} + decode_combine_kernel"
+
+
+def decode_config(w, t: int) -> dict:
+    return {"workload": f"decode_{w.name}", "B": w.B, "H": w.H, "cache_tokens": t, "d_h": w.d,
+            "tau_S": w.tau_S, "lambda": w.lam, "l2": L2_NOTE}
+
+
+PROLOGUE_PAIRING, PROLOGUE_BASE = 1, 1e4
+
+
+def prologue_bytes_per_step(w) -> int:
+    """Algorithmic HBM bytes of the prologue forward (P1, P2, V in; three out) and backward
+    (three gradients and the mixed states in; three out), bf16."""
+    tb = w.B * w.H * w.T * w.d * 2
+    return (3 + 3) * tb + (4 + 3) * tb
+
+
+def prologue_config(w) -> dict:
+    return {"workload": f"prologue_{w.name}", "B": w.B, "H": w.H, "T": w.T, "d_h": w.d, "pairing": "B",
+            "rope_base": PROLOGUE_BASE, "l2": L2_NOTE}
+
+
+def relation_config(w, world: int) -> dict:
+    """The `config` of every Relation fwd+bwd line (both arms): the workload, not the sample."""
+    return {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d_h": w.d, "causal": w.causal,
+            "tau_S": w.tau_S, "lambda": w.lam, "p_scale": round(w.p_scale, 6),
+            "parallelism": f"independent heads, {world} replica(s)", "l2": L2_NOTE}
+
+
+def linear_config(w, world: int) -> dict:
+    """The `config` of every Linear Relation line (both arms)."""
+    return {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d_h": w.d, "tau_S": w.tau_S,
+            "g_scale": w.g_scale, "parallelism": f"independent heads, {world} replica(s)", "l2": L2_NOTE}
+
+
 def cpu_baseline(w, target_s: float = 12.0):
     """The float64 oracle (as it stands) on a bounded sample of the workload: whole heads at the
     workload's T and d.  A first pass runs one head per oracle thread; when it ends well inside
@@ -214,8 +260,7 @@ def run_decode(args, w):
     Y = torch.empty_like(P1n)
     L = torch.empty(w.B, w.H, dtype=torch.float32, device=dev)
     flush = L2Flush(dev)
-    e = 2  # bf16
-    bytes_step = w.B * w.H * (2 * t * w.d * e + 3 * w.d * e + w.d * e + 4)  # caches, new rows, Y, L
+    bytes_step = decode_bytes_per_step(w, t)
     times = []
     with ClockSampler(0) as clk:
         for k in range(args.warmup + args.steps):
@@ -235,10 +280,9 @@ def run_decode(args, w):
         "value": bytes_step / (ms * 1e-3) / 1e9, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32 arithmetic on bf16", "data": "synthetic (seeded Gaussian caches, resident in HBM)",
-        "config": {"workload": f"decode_{w.name}", "B": w.B, "H": w.H, "cache_tokens": t, "d_h": w.d,
-                   "tau_S": w.tau_S, "lambda": w.lam, "l2": L2_NOTE},
+        "config": decode_config(w, t),
         "tokens_per_s": w.B / (ms * 1e-3),
-        "roofline": {"kernel": "decode_partial_kernel + decode_combine_kernel", "bound": "hbm",
+        "roofline": {"kernel": decode_kernels(w), "bound": "hbm",
                      "achieved": bytes_step / (ms * 1e-3) / 1e9, "peak": hbm[0], "unit": "GB/s",
                      "frac": bytes_step / (ms * 1e-3) / 1e9 / hbm[0], "peak_source": hbm[1], "traffic": None},
         "gpu_launches": 2 * args.steps,
@@ -275,17 +319,18 @@ def run_prologue(args, w):
     grads = [torch.empty_like(x["P1"]) for _ in range(3)]
     dth = torch.empty(w.H // 2, device=dev)
     flush = L2Flush(dev)
-    tb = x["P1"].numel() * x["P1"].element_size()
-    bytes_step = (3 + 3) * tb + (4 + 3) * tb  # fwd: 3 in, 3 out; bwd: 4 in, 3 out
+    bytes_step = prologue_bytes_per_step(w)
     tf, tbw = [], []
     with ClockSampler(0) as clk:
         for k in range(args.warmup + args.steps):
             flush()
             ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
             ev[0].record()
-            rb.relation_prologue_fwd(prob, x["P1"], x["P2"], x["V"], theta, 1, 1e4, None, *outs)
+            rb.relation_prologue_fwd(prob, x["P1"], x["P2"], x["V"], theta, PROLOGUE_PAIRING, PROLOGUE_BASE, None,
+                                     *outs)
             ev[1].record()
-            rb.relation_prologue_bwd(prob, x["dY"], x["dY"], x["dY"], outs[2], theta, 1, 1e4, None, *grads, dth)
+            rb.relation_prologue_bwd(prob, x["dY"], x["dY"], x["dY"], outs[2], theta, PROLOGUE_PAIRING,
+                                     PROLOGUE_BASE, None, *grads, dth)
             ev[2].record()
             torch.cuda.synchronize()
             if k >= args.warmup:
@@ -299,8 +344,7 @@ def run_prologue(args, w):
         "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32 arithmetic on bf16",
         "data": "synthetic (seeded Gaussian tensors, resident in HBM)",
-        "config": {"workload": f"prologue_{w.name}", "B": w.B, "H": w.H, "T": w.T, "d_h": w.d, "pairing": "B",
-                   "rope_base": 1e4, "l2": L2_NOTE},
+        "config": prologue_config(w),
         "breakdown_ms": {"fwd": statistics.mean(tf), "bwd": statistics.mean(tbw)},
         "roofline": {"kernel": "rope_kernel + givens_kernel", "bound": "hbm", "achieved": gbs, "peak": hbm[0],
                      "unit": "GB/s", "frac": gbs / hbm[0], "peak_source": hbm[1], "traffic": None},
@@ -440,9 +484,7 @@ def run_linear(args, w):
         "dtype": "bf16 operands, f32 state and accumulation",
         "data": "synthetic (seeded Gaussian P1, P2, I~, dY; log-retention G with the statistics of its "
                 "initialisation), resident in HBM",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d_h": w.d, "tau_S": w.tau_S,
-                   "g_scale": w.g_scale, "parallelism": f"independent heads, {ranks.world} replica(s)",
-                   "l2": L2_NOTE},
+        "config": linear_config(w, ranks.world),
         "breakdown_ms": {"fwd": statistics.mean(tf), "bwd": statistics.mean(tb)},
         "roofline": {"kernel": "relation_linear_fwd + relation_linear_bwd (all launches)", "bound": "hbm",
                      "achieved": gbs, "peak": hbm[0], "unit": "GB/s", "frac": gbs / hbm[0],
@@ -485,7 +527,7 @@ def run_linear_reference(args, w):
         "value": value, "unit": "tok/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": w.T / w.H / value * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic (seeded, bf16-rounded then upcast)",
-        "config": {"workload": w.name, "B": 1, "H": 1, "T": w.T, "d_h": w.d, "tau_S": w.tau_S},
+        "config": linear_config(w, int(os.environ.get("WORLD_SIZE", "1"))),
         "cpu_baseline": {"value": value, "unit": "tok/s", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
@@ -529,11 +571,83 @@ def run_reference(args, w):
         "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded Gaussian, bf16-rounded then upcast)",
-        "config": {"workload": w.name, "B": 1, "H": heads, "T": w.T, "d_h": w.d, "causal": w.causal,
-                   "tau_S": w.tau_S, "lambda": w.lam},
+        "config": relation_config(w, int(os.environ.get("WORLD_SIZE", "1"))),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
+    return 0
+
+
+def _reference_line(metric, unit, value, args, ms, config, sample, cores):
+    return {"impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded Gaussian, bf16-rounded then upcast)", "config": config,
+            "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def run_decode_reference(args, w):
+    """The float64 oracle's selected-row forward on row T-1 of every head: the whole decoding
+    step of the workload, timed on the host cores."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return 0
+    import oracle
+    from relation_token_mixing_gb300 import inputs as rin
+
+    x = rin.make(w)
+    t = w.T - 1
+    heads = list(range(w.B * w.H))
+    rows = [t] * len(heads)
+
+    def step():
+        oracle.fwd_rows(x["P1"], x["P2"], x["V"], w.tau_S, w.lam, True, heads, rows)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = decode_bytes_per_step(w, t) / dt / 1e9
+    sample = f"each step: row {t} of all {len(heads)} heads (the whole workload), float64"
+    print(json.dumps(_reference_line("Relation Cache decode: cache bytes read per second (bf16)", "GB/s", value,
+                                     args, dt * 1e3, decode_config(w, t), sample, oracle.threads())))
+    return 0
+
+
+def run_prologue_reference(args, w):
+    """The float64 prologue oracle (RoPE of P1 and P2, Givens mixing of V, and their backward
+    with d theta) over the whole workload, timed on the host."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return 0
+    import numpy as np
+
+    from oracle import prologue as po
+    from relation_token_mixing_gb300 import inputs as rin
+
+    # One whole batch (Givens mixing pairs heads inside a batch): a bounded sample.
+    x = {k: v[:1].double().numpy() for k, v in rin.make(w, with_dy=True).items()}
+    theta = np.linspace(-1.0, 1.0, w.H // 2)
+
+    def step():
+        po.rope(x["P1"], PROLOGUE_BASE)
+        po.rope(x["P2"], PROLOGUE_BASE)
+        mixed = po.givens(x["V"], theta, PROLOGUE_PAIRING)
+        po.rope_bwd(x["dY"], PROLOGUE_BASE)
+        po.rope_bwd(x["dY"], PROLOGUE_BASE)
+        po.givens_bwd(x["dY"], mixed, theta, PROLOGUE_PAIRING)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = prologue_bytes_per_step(w) / w.B / dt / 1e9
+    sample = f"each step: forward and backward of batch 1 of {w.B} ({w.H} heads, T={w.T}), float64 (numpy)"
+    print(json.dumps(_reference_line("Relation input prologue (RoPE + Givens) fwd+bwd bytes per second (bf16)",
+                                     "GB/s", value, args, dt * 1e3, prologue_config(w), sample, 1)))
     return 0
 
 
@@ -546,12 +660,12 @@ def main():
         lw = rin.LINEAR_WORKLOADS[name]
         return run_linear_reference(args, lw) if args.impl == "reference" else run_linear(args, lw)
     w = rin.WORKLOADS[args.workload]
+    if args.decode:
+        return run_decode_reference(args, w) if args.impl == "reference" else run_decode(args, w)
+    if args.prologue:
+        return run_prologue_reference(args, w) if args.impl == "reference" else run_prologue(args, w)
     if args.impl == "reference":
         return run_reference(args, w)
-    if args.decode:
-        return run_decode(args, w)
-    if args.prologue:
-        return run_prologue(args, w)
 
     import torch
 
@@ -709,9 +823,7 @@ def main():
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded Gaussian inputs, resident in HBM)",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d_h": w.d, "causal": w.causal,
-                   "tau_S": w.tau_S, "lambda": w.lam, "p_scale": round(w.p_scale, 6),
-                   "parallelism": f"independent heads, {world} replica(s)", "l2": L2_NOTE},
+        "config": relation_config(w, world),
         "frac_of_peak": {"value": value / peak_burst, "peak_tflops": peak_burst, "source": peak_src,
                          "sustained_frac": value / peak_sust},
         "executed_tflops": executed,

@@ -77,3 +77,29 @@ def test_cpu_baseline_sample_grows_toward_its_target(monkeypatch, B, H, per_head
     assert out["value"] == pytest.approx(bench.flops(sample, 12) / dt / 1e12)
     assert out["cores"] == 4 and out["kind"] == "oracle"
     assert ("the whole workload" in out["sample"]) == (expect_heads == B * H)
+
+
+@pytest.mark.parametrize("arm", ["relation", "decode", "prologue", "linear"])
+def test_reference_lines_carry_the_workload_config(capsys, arm):
+    """`--impl reference` times the float64 oracle on a bounded sample, but its line names the
+    same workload `config` as the GPU arm's (the sample is described in cpu_baseline.sample);
+    value, cpu_baseline and e2e agree.  Small shapes and the real oracle."""
+    import argparse
+
+    args = argparse.Namespace(gpus=1, steps=1, warmup=0)
+    if arm == "linear":
+        w = rin.LinearWorkload("small_linear", 1, 2, 64, 60, backward=True)
+        bench.run_linear_reference(args, w)
+        expect = bench.linear_config(w, 1)
+    else:
+        w = rin.Workload("small", 2, 4, 64, 64, torch.bfloat16, 1.0, 0.5, True, 1.0, backward=True)
+        fn, expect = {"relation": (bench.run_reference, bench.relation_config(w, 1)),
+                      "decode": (bench.run_decode_reference, bench.decode_config(w, w.T - 1)),
+                      "prologue": (bench.run_prologue_reference, bench.prologue_config(w))}[arm]
+        fn(args, w)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["config"] == expect
+    assert line["value"] > 0 and line["higher_is_better"] is True
+    assert line["cpu_baseline"]["value"] == line["value"] and line["cpu_baseline"]["kind"] == "oracle"
+    assert line["e2e"]["value"] == line["value"] and line["e2e"]["unit"] == line["unit"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
