@@ -67,7 +67,10 @@ typedef enum {
     RELATION_ERR_MISALIGNED = 3,       /* a tensor pointer is not 16-byte aligned */
     RELATION_ERR_WORKSPACE_TOO_SMALL = 4,
     RELATION_ERR_CUDA = 5,             /* a CUDA runtime call or launch failed */
-    RELATION_ERR_DEVICE_TIMEOUT = 6    /* a bounded device-side wait expired */
+    RELATION_ERR_DEVICE_TIMEOUT = 6,   /* a bounded device-side wait expired */
+    RELATION_ERR_DEVICE_UNSAFE = 7     /* as 6, and a kernel then also gave up draining its own
+                                          copies or products: some may have been in flight when
+                                          it returned, so the context should be recreated */
 } relation_status_t;
 
 typedef enum { RELATION_F32 = 0, RELATION_BF16 = 1 } relation_dtype_t;
@@ -171,10 +174,13 @@ relation_status_t relation_bwd_finish(const relation_problem_t* p, const void* P
  * relation_bwd_workspace_bytes() exceeds it return
  * RELATION_ERR_WORKSPACE_TOO_SMALL before any work is enqueued.  The function
  * calls no allocator.  The first call on each device looks up the array's
- * device address (cudaGetSymbolAddress, with that device current): make it
- * before any stream capture.  All calls share the array and overwrite what
- * they need, so calls whose work overlaps on the GPU race and must not run
- * concurrently.
+ * device address (cudaGetSymbolAddress, with that device current).  CUDA loads
+ * a library's device code lazily by default, so that first call can also be
+ * when the array is reserved on the device, which may allocate and synchronise
+ * inside the driver: make the first call at start-up, before any stream
+ * capture or latency-bound loop; later calls reserve nothing.  All calls share
+ * the array and overwrite what they need, so calls whose work overlaps on the
+ * GPU race and must not run concurrently.
  */
 #define RELATION_NOALLOC_SCRATCH_BYTES (32u << 20)
 relation_status_t relation_bwd_noalloc(const relation_problem_t* p, const void* P1, const void* P2,
@@ -298,8 +304,12 @@ relation_status_t relation_linear_bwd(const relation_problem_t* p, const void* P
  * Reads and clears the device status word of the current device.  Call after
  * synchronising the streams used.  Returns RELATION_OK,
  * RELATION_ERR_DEVICE_TIMEOUT (a bounded wait expired; outputs of the calls
- * since the last check are invalid), RELATION_ERR_INVALID_ARGUMENT (a decode
- * position outside its cache) or RELATION_ERR_CUDA.
+ * since the last check are invalid), RELATION_ERR_DEVICE_UNSAFE (a wait expired
+ * and the kernel's second, also bounded, wait for its own copies or products in
+ * flight expired too, so it returned while they may still have been writing
+ * shared memory: discard the outputs and recreate the context),
+ * RELATION_ERR_INVALID_ARGUMENT (a decode position outside its cache) or
+ * RELATION_ERR_CUDA.
  */
 relation_status_t relation_check_device_status(void);
 

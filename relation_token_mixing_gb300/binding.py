@@ -30,6 +30,7 @@ STATUS = {
     4: "RELATION_ERR_WORKSPACE_TOO_SMALL",
     5: "RELATION_ERR_CUDA",
     6: "RELATION_ERR_DEVICE_TIMEOUT",
+    7: "RELATION_ERR_DEVICE_UNSAFE",
 }
 
 

@@ -85,13 +85,6 @@ struct BwdBarriers {
 
 __device__ __forceinline__ float as_f(uint32_t u) { return __uint_as_float(u); }
 
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
-    const uint64_t t0 = global_ns();
-    while (!ptx::mbar_try_wait(bar, parity)) {
-        if (global_ns() - t0 > RELATION_WAIT_LIMIT_NS) return;
-    }
-}
-
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     relation_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_p1, const __grid_constant__ CUtensorMap tm_p2,
@@ -198,9 +191,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         if (lane == 0 && *abort_flag) {
-            drain_wait(&bars->kv_full, 0);
+            ptx::mbar_drain(&bars->kv_full, 0, status);
             for (int jj = max(0, it - C::kStages); jj < it; ++jj)
-                drain_wait(&bars->q_full[jj % C::kStages], (jj / C::kStages) & 1);
+                ptx::mbar_drain(&bars->q_full[jj % C::kStages], (jj / C::kStages) & 1, status);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
@@ -268,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mma_commit_elect(&bars->q_empty[s]);
         }
         ptx::mma_commit_elect(&bars->mma_done);
-        if (lane == 0) drain_wait(&bars->mma_done, 0);
+        if (lane == 0) ptx::mbar_drain(&bars->mma_done, 0, status);
         __syncwarp();
     } else if (warp < 4) {
         // warps 2-3: no role (they complete the first warpgroup)
@@ -395,7 +388,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool leader = (warp == kReduceWarp0) && lane == 0;
         for (int it = 0; it < n_q; ++it) {
             const int i = i_first + it;
-            if (!ptx::mbar_wait_warp(&bars->dq_full, it & 1, abort_flag, status, kDevTimeoutMma)) break;
+            // The four warps take one decision per tile (a 128-thread vote on named
+            // barrier 1): if any warp's bounded wait gave up, all four leave together,
+            // so none is left at the bar.sync below waiting for a warp that left.
+            const bool got = ptx::mbar_wait_warp(&bars->dq_full, it & 1, abort_flag, status, kDevTimeoutMma);
+            if (!ptx::bar_vote_all<1, 128>(got)) break;
             ptx::tc_fence_after();
 #pragma unroll 1
             for (int c0 = 0; c0 < D / 32; ++c0) {

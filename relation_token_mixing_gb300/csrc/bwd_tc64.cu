@@ -86,13 +86,6 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 __device__ __forceinline__ float as_f(uint32_t u) { return __uint_as_float(u); }
 
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
-    const uint64_t t0 = global_ns();
-    while (!ptx::mbar_try_wait(bar, parity)) {
-        if (global_ns() - t0 > RELATION_WAIT_LIMIT_NS) return;
-    }
-}
-
 __device__ __forceinline__ uint64_t kdesc(uint32_t addr) {  // K-major, 128-byte swizzle
     return ptx::smem_desc(addr, 16, 1024, ptx::kSwizzle128B);
 }
@@ -213,9 +206,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         if (lane == 0 && *abort_flag) {
-            drain_wait(&sm.kv_full, 0);
+            ptx::mbar_drain(&sm.kv_full, 0, status);
             for (int jj = max(0, it - kQStages); jj < it; ++jj)
-                drain_wait(&sm.q_full[jj % kQStages], (jj / kQStages) & 1);
+                ptx::mbar_drain(&sm.q_full[jj % kQStages], (jj / kQStages) & 1, status);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
@@ -322,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (it + 1 == n_q && !issue_dq(it)) break;
             }
             ptx::mma_commit_elect(&sm.mma_done);
-            drain_wait(&sm.mma_done, 0);
+            ptx::mbar_drain(&sm.mma_done, 0, status);
         }
     } else if (warp < 4) {
         ptx::regs_dec<kRegsControl>();
@@ -455,7 +448,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool leader = (warp == 4 + kElemWarps) && lane == 0;
         for (int it = 0; it < n_q; ++it) {
             const int i = i_first + it;
-            if (!ptx::mbar_wait_warp(&sm.dq_full, it & 1, abort_flag, status, kDevTimeoutMma)) break;
+            // The four warps take one decision per tile (a 128-thread vote on named
+            // barrier 1): if any warp's bounded wait gave up, all four leave together,
+            // so none is left at the bar.sync below waiting for a warp that left.
+            const bool got = ptx::mbar_wait_warp(&sm.dq_full, it & 1, abort_flag, status, kDevTimeoutMma);
+            if (!ptx::bar_vote_all<1, 128>(got)) break;
             ptx::tc_fence_after();
 #pragma unroll
             for (int c0 = 0; c0 < 2; ++c0) {

@@ -17,6 +17,10 @@ enum DeviceStatus : unsigned int {
     kDevBadLaunch = 4,      // a kernel saw a launch shape it was not built for
     kDevBadPosition = 5,    // a decode position outside the cache (the head was skipped)
 };
+// Flag OR-ed into the status word (beside the first code) when a CTA that gave up
+// waiting also gave up draining its own asynchronous copies or tensor-core work
+// and returned with some of it possibly still in flight.
+constexpr unsigned int kDevDrainIncomplete = 0x100u;
 
 // Kernel-side view of one problem.  Operand tensors (P1, P2, V, Y, dY, dP1,
 // dP2, dV) are contiguous [B, H, T, d] (layout 0) or [B, T, H, d] (layout 1);

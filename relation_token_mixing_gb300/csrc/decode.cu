@@ -99,15 +99,6 @@ __device__ __forceinline__ void load_vec_shared(const Tin* p, float (&v)[VEC]) {
     }
 }
 
-// Bounded wait that ignores the abort flag; used only to let copies still in
-// flight land before a CTA that gave up returns.
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
-    const uint64_t t0 = global_ns();
-    while (!ptx::mbar_try_wait(bar, parity)) {
-        if (global_ns() - t0 > RELATION_WAIT_LIMIT_NS) return;
-    }
-}
-
 // One bulk copy global -> shared, completion counted on `bar` in bytes (both
 // addresses 16-byte aligned, bytes a multiple of 16).
 __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -297,7 +288,7 @@ __global__ void __launch_bounds__(kThreads) decode_partial_bulk_kernel(
     __syncthreads();
     if (abort_flag) {  // the copies did not land within the limit (recorded in the status word)
         if (threadIdx.x == 0) {
-            drain_wait(bar, 0);  // give the copies in flight a second bounded wait before leaving
+            ptx::mbar_drain(bar, 0, status);  // give the copies in flight a second bounded wait before leaving
             out[0] = -INFINITY;
             out[1] = 0.f;
         }

@@ -81,14 +81,6 @@ struct FwdBarriers {
 __device__ __forceinline__ float as_f(uint32_t u) { return __uint_as_float(u); }
 __device__ __forceinline__ uint32_t as_u(float f) { return __float_as_uint(f); }
 
-// Bounded wait that ignores the abort flag; used only to drain in-flight work.
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
-    const uint64_t t0 = global_ns();
-    while (!ptx::mbar_try_wait(bar, parity)) {
-        if (global_ns() - t0 > RELATION_WAIT_LIMIT_NS) return;
-    }
-}
-
 // Dot product of row r of two staged tiles (D/64 swizzled panels of 128 rows x
 // 128 bytes; 16-byte chunk k of row r sits at chunk k ^ (r % 8)).
 template <int kPanels>
@@ -245,11 +237,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Let the copies already issued land before the CTA exits.
                 for (int jj = max(0, j - C::kStages); jj < j; ++jj) {
                     const int s = jj % C::kStages;
-                    drain_wait(&bars->k_full[s], (jj / C::kStages) & 1);
-                    drain_wait(&bars->v_full[s], (jj / C::kStages) & 1);
+                    ptx::mbar_drain(&bars->k_full[s], (jj / C::kStages) & 1, status);
+                    ptx::mbar_drain(&bars->v_full[s], (jj / C::kStages) & 1, status);
                 }
                 for (int t = 0; t < 2; ++t)
-                    if (n_t[t] > 0) drain_wait(&bars->q_full[t], 0);
+                    if (n_t[t] > 0) ptx::mbar_drain(&bars->q_full[t], 0, status);
             }
         }
     } else if (warp == 1) {
@@ -371,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ok) ptx::mma_commit_elect(&bars->kv_empty[s]);
             }
             ptx::mma_commit_elect(&bars->drain);
-            drain_wait(&bars->drain, 0);
+            ptx::mbar_drain(&bars->drain, 0, status);
         }
     } else if (warp < 4) {
         ptx::regs_dec<kRegsControl>();

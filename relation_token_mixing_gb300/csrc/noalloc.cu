@@ -11,7 +11,11 @@
 // library holds RELATION_NOALLOC_SCRATCH_BYTES of it until the process exits.
 // Its host-side name is only a stand-in, so the first call on each device
 // looks up its device address with cudaGetSymbolAddress (with that device
-// current) and caches it; make that first call before any stream capture.
+// current) and caches it.  With CUDA's default lazy loading of device code,
+// that lookup can also be the moment the array is reserved on the device (an
+// allocation and possibly a synchronisation inside the driver), so callers
+// make the first call at start-up, before any stream capture; later calls
+// reserve nothing.
 // All calls share the array: relation_bwd's prepare stage rewrites the parts
 // that must start at zero on every call, and calls whose work overlaps on the
 // GPU (different streams, or different host threads) race on it.

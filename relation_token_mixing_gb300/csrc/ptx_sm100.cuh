@@ -87,6 +87,40 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, v
     return __all_sync(0xffffffffu, ok);
 }
 
+// Bounded wait used only on the abort path, to let work already in flight
+// (copies, MMAs) land before the CTA returns; ignores the abort flag.  If it
+// also runs out, the CTA may return with that work still in flight: the status
+// word gets kDevDrainIncomplete so the host treats the context as unreliable.
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity, unsigned int* status) {
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_ns() - t0 > RELATION_WAIT_LIMIT_NS) {
+            if (status != nullptr) atomicOr(status, kDevDrainIncomplete);
+            return false;
+        }
+    }
+    return true;
+}
+
+// Vote over named barrier `kId` shared by `kCount` threads (whole warps):
+// every participant passes its own flag and all of them receive the AND.  The
+// instruction is also the barrier, so a group of warps that decides by this
+// vote either all continue or all leave; none can be left waiting at a later
+// named barrier for a warp that already left.
+template <int kId, int kCount>
+__device__ __forceinline__ bool bar_vote_all(bool q) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 q, %1, 0;\n\t"
+        "barrier.cta.red.and.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)q), "n"(kId), "n"(kCount)
+        : "memory");
+    return r != 0;
+}
+
 // ----------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

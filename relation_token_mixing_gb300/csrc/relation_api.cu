@@ -411,6 +411,7 @@ relation_status_t relation_check_device_status(void) {
         const unsigned int zero = 0;
         if (cudaMemcpy(di.status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
             return RELATION_ERR_CUDA;
+        if (word & kDevDrainIncomplete) return RELATION_ERR_DEVICE_UNSAFE;
         return word == kDevBadPosition ? RELATION_ERR_INVALID_ARGUMENT : RELATION_ERR_DEVICE_TIMEOUT;
     }
     return RELATION_OK;
@@ -654,6 +655,9 @@ const char* relation_status_string(relation_status_t s) {
         case RELATION_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than relation_bwd_workspace_bytes()";
         case RELATION_ERR_CUDA: return "CUDA runtime error";
         case RELATION_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait expired";
+        case RELATION_ERR_DEVICE_UNSAFE:
+            return "a bounded device-side wait expired and a kernel returned with its own copies or products "
+                   "possibly still in flight; the CUDA context should not be trusted";
     }
     return "unknown status";
 }

@@ -64,6 +64,23 @@ def test_noalloc_matches_workspace_backward_on_two_calls_in_a_row():
         _compare(w, got, ref)
 
 
+def test_noalloc_reserves_nothing_after_the_first_call():
+    """After a first call (which may be when the driver reserves the array on
+    this device), further calls leave the device's free memory unchanged."""
+    w, x, Y, L = _case(1, 2, 260, 64, torch.bfloat16, seed=3)
+    prob = rb.problem_for(x["P1"], w.tau_S, w.lam, w.causal)
+    outs = [torch.empty_like(x["V"]) for _ in range(3)]
+    dlam = torch.empty((1,), device="cuda")
+    rb.relation_bwd_noalloc(prob, x["P1"], x["P2"], x["V"], Y, L, x["dY"], *outs, dlam)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(2):
+        rb.relation_bwd_noalloc(prob, x["P1"], x["P2"], x["V"], Y, L, x["dY"], *outs, dlam)
+        torch.cuda.synchronize()
+        assert torch.cuda.mem_get_info()[0] == free0
+    assert rb.relation_check_device_status() == 0
+
+
 def test_noalloc_fp32_path_twice():
     for seed in (1, 2):
         w, x, Y, L = _case(1, 2, 150, 64, torch.float32, causal=seed == 1, seed=seed)
