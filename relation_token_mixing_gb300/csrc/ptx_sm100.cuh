@@ -431,6 +431,36 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
     return d;
 }
 
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+    float2 d;
+    asm("{.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2,%3};\n\tmov.b64 rb, {%4,%5};\n\t"
+        "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0,%1}, rd;}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+// 2^x on the fp32 pipes (no special-function unit), for x in [-125, 64]:
+// Cody-Waite reduction x = n + f with n the nearest integer (adding and
+// subtracting 1.5 * 2^23 rounds exactly) and |f| <= 1/2 exact; 2^f by a cubic
+// fitted to 2^f on [-1/2, 1/2] (least squares on Chebyshev nodes, iteratively
+// reweighted toward equal relative error: at most 7.7e-5 relative); n is then
+// added to the exponent field.  Outside the range the result is wrong, so
+// callers keep x inside it.
+__device__ __forceinline__ float2 exp2_fma2(float2 x) {
+    const float2 shifter = make_float2(12582912.f, 12582912.f);
+    const float2 c3 = make_float2(0.05522262f, 0.05522262f), c2 = make_float2(0.24261527f, 0.24261527f);
+    const float2 c1 = make_float2(0.6932516f, 0.6932516f), c0 = make_float2(0.9999276f, 0.9999276f);
+    const float2 t = add2(x, shifter);
+    const float2 f = sub2(x, sub2(t, shifter));
+    float2 p = fma2(f, c3, c2);
+    p = fma2(p, f, c1);
+    p = fma2(p, f, c0);
+    return make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(t.x) << 23)),
+                       __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(t.y) << 23)));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);

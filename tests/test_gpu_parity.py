@@ -3,11 +3,13 @@
 Tolerances (from the arithmetic):
   Y  : fp32 path <= 1e-5 * max|V|;  bf16 path <= 1e-2 * max|V| (fp32 accumulation,
        flow weights rounded to bf16 before the second product, bf16 output).
-  L  : fp32 path <= 1e-6 * max(1, |L|); bf16 path <= 1e-3 * max(1, |L|).  The bf16
-       kernels use tanh.approx (relative error ~2^-11) for SiLU, so an Exchange logit
-       of size |U| carries up to ~|U| 2^-12 of error; averaged over a row it stays far
-       below 1e-3.  Above 1 the bound is relative: fp32 spaces numbers near |L| by
-       |L| 2^-23, so the fp32 bound is about eight spacings at any magnitude.
+  L  : fp32 path <= 1e-6 * max(1, |L|) + T 2^-24; bf16 path <= 1e-3 * max(1, |L|).
+       The bf16 kernels use tanh.approx (relative error ~2^-11) for SiLU, so an
+       Exchange logit of size |U| carries up to ~|U| 2^-12 of error; averaged over a
+       row it stays far below 1e-3.  Above 1 the bound is relative: fp32 spaces
+       numbers near |L| by |L| 2^-23, about eight spacings at any magnitude.  The
+       fp32 term T 2^-24 is the worst-case relative rounding of a float32 sum of up
+       to T terms, which becomes log l's error when a row's terms are all equal.
   dP1, dP2, dV : fp32 path <= 1e-4 * max|g_ref| per tensor; bf16 path <= 2e-2 * max|g_ref|.
 Inputs come from the seeded generator (relation_token_mixing_gb300.inputs); the
 oracle upcasts the same rounded tensors to float64.
@@ -65,10 +67,11 @@ def _maxerr(a, b):
     return float(np.max(np.abs(np.asarray(a, dtype=np.float64) - np.asarray(b, dtype=np.float64))))
 
 
-def _lerr(a, b):
-    """Largest L error, relative above 1 (see the module docstring)."""
+def _lerr(a, b, dtype, T):
+    """Largest L error as a fraction of its bound (see the module docstring)."""
     a, b = np.asarray(a, dtype=np.float64), np.asarray(b, dtype=np.float64)
-    return float(np.max(np.abs(a - b) / np.maximum(1.0, np.abs(b))))
+    bound = L_TOL[dtype] * np.maximum(1.0, np.abs(b)) + (T * 2.0 ** -24 if dtype == torch.float32 else 0.0)
+    return float(np.max(np.abs(a - b) / bound))
 
 
 def _np(t):
@@ -80,11 +83,11 @@ def _check_fwd_full(w, x_cpu):
     Y, L = _gpu_fwd(x, w)
     Yr, Lr = oracle.fwd(x_cpu["P1"], x_cpu["P2"], x_cpu["V"], w.tau_S, w.lam, w.causal)
     vmax = float(np.max(np.abs(_np(x_cpu["V"]))))
-    ey, el = _maxerr(_np(Y), Yr), _lerr(_np(L), Lr)
+    ey, el = _maxerr(_np(Y), Yr), _lerr(_np(L), Lr, w.dtype, w.T)
     _record("Y", ey, Y_TOL[w.dtype] * vmax)
-    _record("L", el, L_TOL[w.dtype])
+    _record("L/bound", el, 1.0)
     assert ey <= Y_TOL[w.dtype] * vmax, (ey, vmax)
-    assert el <= L_TOL[w.dtype], el
+    assert el <= 1.0, el
     return Y, L
 
 
@@ -257,9 +260,9 @@ def _check_fwd_sampled(w, x_cpu, Y, L, n=200, seed=0):
     Lg = _np(L).reshape(BH, w.T)[heads, rows]
     vmax = float(np.max(np.abs(_np(x_cpu["V"]))))
     _record("Y(sampled)", _maxerr(Yg, Yr), Y_TOL[w.dtype] * vmax)
-    _record("L(sampled)", _lerr(Lg, Lr), L_TOL[w.dtype])
+    _record("L/bound(sampled)", _lerr(Lg, Lr, w.dtype, w.T), 1.0)
     assert _maxerr(Yg, Yr) <= Y_TOL[w.dtype] * vmax
-    assert _lerr(Lg, Lr) <= L_TOL[w.dtype]
+    assert _lerr(Lg, Lr, w.dtype, w.T) <= 1.0
 
 
 def _check_bwd_sampled(w, x_cpu, grads, heads=(0,), ncols=24, seed=1):

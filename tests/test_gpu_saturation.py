@@ -5,8 +5,12 @@ configuration at d = 64), so they never reach the regimes where the bf16
 kernels' tanh-based sigmoid/SiLU and the lazily raised softmax maximum could
 break.  These cases build the evidence directly:
 
-* Row-constant evidence: every row of P2 is b = (2, 0, ..., 0) and row i of P1
-  is (c_i sqrt(d) / 2, 0, ..., 0), so U_ij = c_i for every visible j.  Then
+* Row-constant evidence: row i of P1 is (c_i sqrt(d) / 2, 0, ..., 0) and row j
+  of P2 is (2, 0, w_j) with w_j seeded Gaussian coordinates 2..d-1, so
+  U_ij = c_i for every visible j.  (The w_j leave U unchanged but give dP1 a
+  scale: without them dP1_i = (2/sqrt(d)) sum_j dU_ij e_0, and since
+  sum_j dR_ij = 0 that is a cancellation residue whose size is set by the
+  rounding of D_i = dY_i . Y_i, not by the method.)  Then
   ("Ask Self, Ask Others", Sec. 3.1 eq.(1)-(3); Appendix A.1.2-A.1.3) the Self
   weight is F_ii = e^S / (e^S + n c^-lambda e^E) with S = sigmoid(c/tau_S),
   E = SiLU(c), n visible history entries and count c (i causal, T otherwise),
@@ -18,9 +22,12 @@ break.  These cases build the evidence directly:
 
 Every case is compared element by element with the float64 oracle and, where
 the closed form applies, with the closed form.  Tolerances: Y <= 1e-2 max|V|
-(bf16) / 1e-5 max|V| (fp32); L <= 1e-3 max(1, |L|) (bf16) / 1e-6 max(1, |L|)
-(fp32) -- relative above 1 because L reaches ~60 here and fp32 spaces numbers
-near 64 by 7.6e-6; gradients <= 2e-2 / 1e-4 of the largest reference entry.
+(bf16) / 1e-5 max|V| (fp32); L <= 1e-3 max(1, |L|) (bf16) /
+1e-6 max(1, |L|) + T 2^-24 (fp32) -- relative above 1 because L reaches ~60
+here and fp32 spaces numbers near 64 by 7.6e-6, plus the worst-case rounding
+of a float32 sum of up to T terms (relative error below T 2^-24), which sets
+log l when all of a row's terms are equal; gradients <= 2e-2 / 1e-4 of the
+largest reference entry.
 """
 import math
 
@@ -38,6 +45,11 @@ Y_TOL = {torch.float32: 1e-5, torch.bfloat16: 1e-2}
 L_TOL = {torch.float32: 1e-6, torch.bfloat16: 1e-3}
 G_TOL = {torch.float32: 1e-4, torch.bfloat16: 2e-2}
 
+
+def _l_bound(dtype, T, L_ref):
+    """Per-row L bound: relative above |L| = 1, plus float32 summation of T terms."""
+    return L_TOL[dtype] * np.maximum(1.0, np.abs(L_ref)) + (T * 2.0 ** -24 if dtype == torch.float32 else 0.0)
+
 EDGE_C = [8.0, -8.0, 20.0, -20.0, 60.0, -60.0, 0.3, -1.27846]
 
 
@@ -46,13 +58,16 @@ def _np(t):
 
 
 def _row_constant(T, d, dtype, cs, H=2):
-    """P1, P2 with U_ij = c_i (head h takes the list rotated by h), V, dY seeded."""
+    """P1, P2 with U_ij = c_i (head h takes the list rotated by h), V, dY seeded.
+
+    Coordinate 1 of P1 and P2 stays zero, free for a test to place one entry."""
     P1 = torch.zeros(1, H, T, d, dtype=torch.float64)
     for h in range(H):
         c = np.array([cs[(k + h) % len(cs)] for k in range(T)])
         P1[0, h, :, 0] = torch.from_numpy(c * math.sqrt(d) / 2.0)
     P2 = torch.zeros(1, H, T, d, dtype=torch.float64)
     P2[..., 0] = 2.0
+    P2[..., 2:] = rin.gaussian((1, H, T, d - 2), 43).double()
     x = {
         "P1": P1.to(dtype),
         "P2": P2.to(dtype),
@@ -97,9 +112,9 @@ def _run_fwd(x, tau, lam, causal):
 
 def _check_y_l(Yg, Lg, Yr, Lr, vmax, dtype, what):
     ey = float(np.max(np.abs(Yg - Yr)))
-    el = float(np.max(np.abs(Lg - Lr) / np.maximum(1.0, np.abs(Lr))))
+    el = float(np.max(np.abs(Lg - Lr) / _l_bound(dtype, Lr.shape[-1], Lr)))
     assert ey <= Y_TOL[dtype] * vmax, (what, "Y", ey, Y_TOL[dtype] * vmax)
-    assert el <= L_TOL[dtype], (what, "L", el, L_TOL[dtype])
+    assert el <= 1.0, (what, "L error / bound", el)
 
 
 CASES = [(dt, d, causal) for dt in (torch.bfloat16, torch.float32) for d in (64, 128) for causal in (True, False)]
@@ -166,6 +181,6 @@ def test_late_maximum_jump_rescales(dtype):
     E_neg = -60.0 / (1.0 + math.exp(60.0))
     hist = [math.log(i - 2) - lam * math.log(i) + E_neg, -lam * math.log(i) + 60.0]
     L_row = float(np.logaddexp.reduce([S] + hist))
-    assert abs(Lg[0, 0, i0] - L_row) <= L_TOL[dtype] * max(1.0, abs(L_row))
+    assert abs(Lg[0, 0, i0] - L_row) <= _l_bound(dtype, T, L_row)
     # Nearly all of the row's weight sits on key j*.
     assert float(np.max(np.abs(Yg[0, 0, i0] - _np(x["V"])[0, 0, j_star]))) <= Y_TOL[dtype] * vmax + 1e-20

@@ -18,7 +18,7 @@ from relation_token_mixing_gb300 import inputs as rin
 pytestmark = pytest.mark.gpu
 
 Y_TOL = {torch.float32: 1e-5, torch.bfloat16: 1e-2}
-L_TOL = {torch.float32: 1e-6, torch.bfloat16: 1e-3}  # relative above |L| = 1
+L_TOL = {torch.float32: 1e-6, torch.bfloat16: 1e-3}  # relative above |L| = 1; fp32 adds T 2^-24
 G_TOL = {torch.float32: 1e-4, torch.bfloat16: 2e-2}
 BHTD, BTHD = rb.RELATION_LAYOUT_BHTD, rb.RELATION_LAYOUT_BTHD
 
@@ -78,7 +78,8 @@ def test_widths_and_layouts_match_oracle(w, layout):
     Yr, Lr = oracle.fwd(x_cpu["P1"], x_cpu["P2"], x_cpu["V"], w.tau_S, w.lam, w.causal)
     vmax = float(np.max(np.abs(_np(x_cpu["V"]))))
     assert _maxerr(_np(_from_layout(Y, layout)), Yr) <= Y_TOL[w.dtype] * vmax
-    assert float(np.max(np.abs(_np(L) - Lr) / np.maximum(1.0, np.abs(Lr)))) <= L_TOL[w.dtype]
+    l_bound = L_TOL[w.dtype] * np.maximum(1.0, np.abs(Lr)) + (w.T * 2.0 ** -24 if w.dtype == torch.float32 else 0.0)
+    assert float(np.max(np.abs(_np(L) - Lr) / l_bound)) <= 1.0
 
     ref = oracle.bwd(x_cpu["P1"], x_cpu["P2"], x_cpu["V"], x_cpu["dY"], w.tau_S, w.lam, w.causal)
     for got, exp, name in zip((dP1, dP2, dV), ref[:3], ("dP1", "dP2", "dV")):
