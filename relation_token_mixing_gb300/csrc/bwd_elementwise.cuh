@@ -39,7 +39,13 @@ __device__ __forceinline__ float elementwise16(const uint32_t* sv, const uint32_
     for (int e = 0; e < 8; ++e) {
         const float2 a = make_float2(as_f(sv[2 * e]), as_f(sv[2 * e + 1]));
         const float2 g = make_float2(as_f(gv[2 * e]), as_f(gv[2 * e + 1]));
-        const float4 c4 = qc[e];  // one broadcast 16-byte load per column pair
+        // One 16-byte shared-memory load per column pair, the same address in every
+        // lane (a broadcast); the shared state space is explicit so the load does not
+        // go through the generic path.
+        float4 c4;
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(c4.x), "=f"(c4.y), "=f"(c4.z), "=f"(c4.w)
+                     : "r"((uint32_t)__cvta_generic_to_shared(qc + e)));
         const float2 nlt2 = make_float2(c4.x, c4.y), ndk2 = make_float2(c4.z, c4.w);
         const float2 nh = ptx::mul2(a, ec.c_nh);
         const float2 nt = make_float2(ptx::tanh_approx(nh.x), ptx::tanh_approx(nh.y));

@@ -21,13 +21,14 @@
 //                       to an fp32 accumulator in global memory by TMA bulk reduce
 // S^T and dP^T are produced and consumed in two halves of 64 queries with their
 // own full/free barriers.  Every elementwise warp copies its part of a half to
-// registers before working on it, so the MMA warp issues that half of tile i+1
-// right away: the products of tile i+1 run while tile i is still being worked
-// on, and the accumulations of tile i run while tile i+1 is.
-// Warps: 0 loader (TMA + per-query constants), 1 MMA issuer / TMEM owner,
-// 2-3 idle (complete the first warpgroup), 4-19 elementwise: four warpgroups,
-// one per 16 query columns of each half, 20-23 dP1 reduction (TMEM -> swizzled
-// shared staging -> TMA reduce-add).
+// registers before working on it, so the first MMA warp issues that half of tile
+// i+1 right away: the products of tile i+1 run while tile i is still being
+// worked on, and the accumulations of tile i (issued by the second MMA warp as
+// soon as its P^T and dS^T are stored) run while tile i+1 is.
+// Warps: 0 loader (TMA + per-query constants), 1-2 MMA issuers (1: S^T/dP^T,
+// also TMEM owner; 2: dV, dP2, dP1), 3 idle (completes the first warpgroup),
+// 4-19 elementwise: four warpgroups, one per 16 query columns of each half,
+// 20-23 dP1 reduction (TMEM -> swizzled shared staging -> TMA reduce-add).
 // TMEM: S^T [0,128) | dP^T [128,256) | P^T [256,320) | dV [320,384) | dP2 [384,448) | dP1 part [448,512).
 #include <cuda_bf16.h>
 
@@ -76,7 +77,7 @@ struct Smem {
     uint64_t ds_free[2];
     uint64_t dq_full;
     uint64_t dq_free;
-    uint64_t mma_done;
+    uint64_t mma_done[2];  // per MMA issuer: all of its products complete
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -129,7 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(&sm.kv_full, 1);
         for (int s = 0; s < kQStages; ++s) {
             ptx::mbar_init(&sm.q_full[s], 32);
-            ptx::mbar_init(&sm.q_empty[s], 1);
+            ptx::mbar_init(&sm.q_empty[s], 2);  // released by both MMA issuers
         }
         for (int s = 0; s < 2; ++s) ptx::mbar_init(&sm.ds_free[s], 1);
         for (int h = 0; h < 2; ++h) {
@@ -140,7 +141,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(&sm.pv_done, 1);
         ptx::mbar_init(&sm.dq_full, 1);
         ptx::mbar_init(&sm.dq_free, 128);
-        ptx::mbar_init(&sm.mma_done, 1);
+        ptx::mbar_init(&sm.mma_done[0], 1);
+        ptx::mbar_init(&sm.mma_done[1], 1);
         sm.abort_flag = 0;
         ptx::fence_barrier_init();
     }
@@ -210,30 +212,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int jj = max(0, it - kQStages); jj < it; ++jj)
                 ptx::mbar_drain(&sm.q_full[jj % kQStages], (jj / kQStages) & 1, status);
         }
-    } else if (warp == 1) {
-        // ---------------------------------------------------------- MMA issuer
-        // The whole warp runs the issue loop; one elected lane issues each MMA.
+    } else if (warp == 1 || warp == 2) {
+        // --------------------------------------------------------- MMA issuers
+        // Two instruction streams, each a converged warp with an elected lane:
+        //   warp 1: S^T and dP^T of the next query tile, per half, as soon as the
+        //           elementwise warps hold that half of the current tile;
+        //   warp 2: dV and dP2 of the current tile once its P^T and dS^T are
+        //           stored, then its dP1 partial.
+        // They write disjoint TMEM columns; the tensor core runs each stream's
+        // products in issue order, and every hand-off between them goes through
+        // the elementwise warps' barriers.
         ptx::regs_dec<kRegsControl>();
-        {
+        const uint32_t hi_k = ptx::desc_hi(kdesc(ptx::smem_u32(sm.k)));
+        const uint32_t hi_m = ptx::desc_hi(mdesc(ptx::smem_u32(sm.k)));
+        constexpr uint32_t kStageQ = kTileBytes >> 4, kStageS = (2 * kTileBytes) >> 4, kHalfQ = (kTileBytes / 2) >> 4;
+        bool ok = true;
+        if (warp == 1) {
             const uint32_t id_s = ptx::idesc_bf16(kTile, kTile / 2, false, false);  // S^T, dP^T halves (N = 64)
-            const uint32_t id_dv = ptx::idesc_bf16(kTile, kD, false, true);     // dV (B MN-major)
-            const uint32_t id_dk = ptx::idesc_bf16(kTile, kD, false, true);     // dP2 (A K-major, B MN-major)
-            const uint32_t id_dq = ptx::idesc_bf16(kTile, kD, true, true);      // dP1 (A, B MN-major)
-            // Descriptor words: the high word depends only on the layout (K-major or
-            // MN-major); the low word is the start address >> 4 plus the leading byte
-            // offset field, advanced by (byte offset >> 4) per K-step.
-            const uint32_t hi_k = ptx::desc_hi(kdesc(ptx::smem_u32(sm.k)));
-            const uint32_t hi_m = ptx::desc_hi(mdesc(ptx::smem_u32(sm.k)));
+            // Descriptor low words: start address >> 4 (plus the leading byte offset
+            // field), advanced by (byte offset >> 4) per K-step.
             const uint32_t k_lo = ptx::desc_lo(kdesc(ptx::smem_u32(sm.k)));
             const uint32_t v_lo = ptx::desc_lo(kdesc(ptx::smem_u32(sm.v)));
-            const uint32_t km_lo = ptx::desc_lo(mdesc(ptx::smem_u32(sm.k)));
             const uint32_t q_lo0 = ptx::desc_lo(kdesc(ptx::smem_u32(sm.q[0])));
             const uint32_t g_lo0 = ptx::desc_lo(kdesc(ptx::smem_u32(sm.g[0])));
-            const uint32_t qm_lo0 = ptx::desc_lo(mdesc(ptx::smem_u32(sm.q[0])));
-            const uint32_t gm_lo0 = ptx::desc_lo(mdesc(ptx::smem_u32(sm.g[0])));
-            const uint32_t sk_lo0 = ptx::desc_lo(kdesc(ptx::smem_u32(sm.ds[0])));
-            const uint32_t sm_lo0 = ptx::desc_lo(mdesc(ptx::smem_u32(sm.ds[0])));
-            constexpr uint32_t kStageQ = kTileBytes >> 4, kStageS = (2 * kTileBytes) >> 4, kHalfQ = (kTileBytes / 2) >> 4;
             // S^T and dP^T of query half h (64 queries): N = 64 products into columns
             // 64h..64h+63 of their regions; B starts 64 rows (8 KB) into the tile.
             auto issue_s_dp = [&](int qs, int h) {
@@ -249,51 +250,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       ks > 0 ? 1u : 0u);
                 ptx::mma_commit_elect(&sm.s_full[h]);
             };
-            bool ok = ptx::mbar_wait_warp(&sm.kv_full, 0, abort_flag, status, kDevTimeoutFull);
-            if (ok && n_q > 0) ok = ptx::mbar_wait_warp(&sm.q_full[0], 0, abort_flag, status, kDevTimeoutFull);
-            if (ok && n_q > 0) {
-                ptx::tc_fence_after();
-                issue_s_dp(0, 0);
-                issue_s_dp(0, 1);
+            ok = ptx::mbar_wait_warp(&sm.kv_full, 0, abort_flag, status, kDevTimeoutFull);
+            for (int it = 0; ok && it < n_q; ++it) {
+                // Products of tile it: half h once every elementwise warp holds half h
+                // of tile it-1 (the columns are then free).
+                const int qs = it % kQStages;
+                if (!ptx::mbar_wait_warp(&sm.q_full[qs], (it / kQStages) & 1, abort_flag, status, kDevTimeoutFull))
+                    break;
+                for (int h = 0; ok && h < 2; ++h) {
+                    if (it > 0 && !ptx::mbar_wait_warp(&sm.s_free[h], (it - 1) & 1, abort_flag, status,
+                                                       kDevTimeoutFull)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    issue_s_dp(qs, h);
+                }
+                if (ok) ptx::mma_commit_elect(&sm.q_empty[qs]);  // this stream no longer reads P1_i, dY_i
             }
-            // dP1_t = dS_t P2_j: A = dS_t (MN-major view of dS^T buffer t&1), K over key
-            // rows.  Issued one tile late, early in tile t+1: dS_t is complete and the
-            // reduce warps have had a whole tile to drain dP1_{t-1} from TMEM, so the
-            // products of the next tiles never queue behind the reduction.
-            auto issue_dq = [&](int t) -> bool {
-                if (t > 0 && !ptx::mbar_wait_warp(&sm.dq_free, (t - 1) & 1, abort_flag, status, kDevTimeoutMma))
-                    return false;
-                ptx::tc_fence_after();
-                const uint32_t sm_lo = sm_lo0 + ((t & 1) ? kStageS : 0u);
-#pragma unroll
-                for (int ks = 0; ks < kTile / 16; ++ks)
-                    ptx::mma_ss_elect(tmem + kColDQ, sm_lo + 128 * ks, hi_m, km_lo + 128 * ks, hi_m, id_dq,
-                                      ks > 0 ? 1u : 0u);
-                ptx::mma_commit_elect(&sm.dq_full);
-                ptx::mma_commit_elect(&sm.ds_free[t & 1]);
-                return true;
-            };
+            ptx::mma_commit_elect(&sm.mma_done[0]);
+            ptx::mbar_drain(&sm.mma_done[0], 0, status);
+        } else {
+            const uint32_t id_dv = ptx::idesc_bf16(kTile, kD, false, true);  // dV (B MN-major)
+            const uint32_t id_dk = ptx::idesc_bf16(kTile, kD, false, true);  // dP2 (A K-major, B MN-major)
+            const uint32_t id_dq = ptx::idesc_bf16(kTile, kD, true, true);   // dP1 (A, B MN-major)
+            const uint32_t km_lo = ptx::desc_lo(mdesc(ptx::smem_u32(sm.k)));
+            const uint32_t qm_lo0 = ptx::desc_lo(mdesc(ptx::smem_u32(sm.q[0])));
+            const uint32_t gm_lo0 = ptx::desc_lo(mdesc(ptx::smem_u32(sm.g[0])));
+            const uint32_t sk_lo0 = ptx::desc_lo(kdesc(ptx::smem_u32(sm.ds[0])));
+            const uint32_t sm_lo0 = ptx::desc_lo(mdesc(ptx::smem_u32(sm.ds[0])));
             for (int it = 0; ok && it < n_q; ++it) {
                 const int s = it & 1;          // dS buffer
                 const int qs = it % kQStages;  // P1/dY stage
-                if (it + 1 < n_q) {
-                    // First half of S^T(i+1), dP^T(i+1) as soon as every elementwise warp
-                    // has that half of tile i in registers.
-                    const int qn = (it + 1) % kQStages;
-                    if (!ptx::mbar_wait_warp(&sm.s_free[0], it & 1, abort_flag, status, kDevTimeoutFull) ||
-                        !ptx::mbar_wait_warp(&sm.q_full[qn], ((it + 1) / kQStages) & 1, abort_flag, status,
-                                             kDevTimeoutFull))
-                        break;
-                    ptx::tc_fence_after();
-                    issue_s_dp(qn, 0);
-                }
-                if (it > 0 && !issue_dq(it - 1)) break;
-                if (it + 1 < n_q) {
-                    const int qn = (it + 1) % kQStages;
-                    if (!ptx::mbar_wait_warp(&sm.s_free[1], it & 1, abort_flag, status, kDevTimeoutFull)) break;
-                    ptx::tc_fence_after();
-                    issue_s_dp(qn, 1);
-                }
                 if (!ptx::mbar_wait_warp(&sm.p_full, it & 1, abort_flag, status, kDevTimeoutFull)) break;
                 ptx::tc_fence_after();
                 // dV += P^T dY_i: K-step ks covers queries 16ks..16ks+15 (8 packed TMEM
@@ -311,11 +299,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int ks = 0; ks < kTile / 16; ++ks)
                     ptx::mma_ss_elect(tmem + kColDK, sk_lo + (ks >> 2) * kStageQ + 2 * (ks & 3), hi_k,
                                       qm_lo + 128 * ks, hi_m, id_dk, ks > 0 ? 1u : acc0);
-                ptx::mma_commit_elect(&sm.q_empty[qs]);  // P1_i and dY_i are no longer read
-                if (it + 1 == n_q && !issue_dq(it)) break;
+                ptx::mma_commit_elect(&sm.q_empty[qs]);  // this stream no longer reads P1_i, dY_i
+                // dP1_i = dS P2_j: A = dS (MN-major view of dS^T buffer s), K over key
+                // rows, into the partial's columns once the reduce warps drained the
+                // previous tile's.
+                if (it > 0 && !ptx::mbar_wait_warp(&sm.dq_free, (it - 1) & 1, abort_flag, status, kDevTimeoutMma))
+                    break;
+                ptx::tc_fence_after();
+                const uint32_t sm_lo = sm_lo0 + (s ? kStageS : 0u);
+#pragma unroll
+                for (int ks = 0; ks < kTile / 16; ++ks)
+                    ptx::mma_ss_elect(tmem + kColDQ, sm_lo + 128 * ks, hi_m, km_lo + 128 * ks, hi_m, id_dq,
+                                      ks > 0 ? 1u : 0u);
+                ptx::mma_commit_elect(&sm.dq_full);
+                ptx::mma_commit_elect(&sm.ds_free[s]);
             }
-            ptx::mma_commit_elect(&sm.mma_done);
-            ptx::mbar_drain(&sm.mma_done, 0, status);
+            ptx::mma_commit_elect(&sm.mma_done[1]);
+            ptx::mbar_drain(&sm.mma_done[1], 0, status);
         }
     } else if (warp < 4) {
         ptx::regs_dec<kRegsControl>();
@@ -418,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0 && dlam != 0.f) atomicAdd(dlambda, dlam / k_scale);
         }
         // Epilogue: blocks 0-1 write dV, blocks 2-3 write dP2, 32 columns each.
-        if (ok && ptx::mbar_wait_warp(&sm.mma_done, 0, abort_flag, status, kDevTimeoutMma)) {
+        if (ok && ptx::mbar_wait_warp(&sm.mma_done[1], 0, abort_flag, status, kDevTimeoutMma)) {
             ptx::tc_fence_after();
             const int c0 = blk & 1;
             __nv_bfloat16* dst_row = (blk < 2 ? dV : dP2) + row_offset(kp, bh, row_valid ? kv : 0);
