@@ -93,6 +93,12 @@ typedef struct {
  * when L is not NULL, L [B,H,T] float32 with L_i = log sum_j exp(R_ij) in the
  * paper's convention (correction included).  The backward needs L.
  * Y and L must not overlap any input.
+ * bf16 d_h = 60 without a workspace takes the slow route: its 120-byte rows
+ * cannot be read by the tensor memory accelerator, so the forward's producer
+ * warp copies every tile with 8-byte cp.async (about 4x slower at B16 H8
+ * T2048).  Callers that can spare a workspace use relation_fwd_ws below,
+ * which pads the operands once and runs the fast kernel; results are
+ * identical.
  */
 relation_status_t relation_fwd(const relation_problem_t* p, const void* P1, const void* P2,
                                const void* V, void* Y, float* L, void* stream);
