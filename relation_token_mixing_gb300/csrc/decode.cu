@@ -8,10 +8,12 @@
 // The cache update appends p2_{t+1} and I~_{t+1} (Appendix A.5.3).
 //
 // The pass is HBM-bound (it reads 2 t d values per head), so it runs on CUDA
-// cores in fp32, split over key chunks: each CTA reads its chunk's cached rows
-// once (by two bulk copies into shared memory where the rows allow it, else by
-// direct 16- or 8-byte loads), computes the chunk's scores, maximum, weights and
-// weighted sum, and one CTA per head then merges the chunks.
+// cores in fp32.  Caches whose rows bulk copies can move (contiguous
+// [B, H, T, d], rows a multiple of 16 bytes) are streamed: about two CTAs per
+// SM, each taking a share of a head's cached rows through a ring of shared-memory
+// stages with an online softmax per lane group.  Other caches are split into
+// chunks read directly (16- or 8-byte loads).  One CTA per head then merges the
+// shares, launched as a programmatic dependent of the partial pass.
 #include <math.h>
 
 #include <mutex>
@@ -77,26 +79,43 @@ __device__ __forceinline__ void load_vec(const Tin* p, float (&v)[VEC]) {
     }
 }
 
-// The same from shared memory (rows staged by the bulk-copy pass).
-template <typename Tin, int VEC>
-__device__ __forceinline__ void load_vec_shared(const Tin* p, float (&v)[VEC]) {
-    if constexpr (sizeof(Tin) == 2 && VEC == 8) {
-        const uint4 u = *reinterpret_cast<const uint4*>(p);
+// VEC consecutive elements as fp32 from 16-byte pieces (bf16 VEC = 8 or 16,
+// fp32 VEC = 4 or 8); `Shared`: p points into shared memory, else global (read
+// through the non-coherent path).
+template <typename Tin, int VEC, bool Shared>
+__device__ __forceinline__ void load_vec16(const Tin* p, float (&v)[VEC]) {
+    constexpr int kPer = 16 / (int)sizeof(Tin);  // elements per 16-byte piece
+    static_assert(VEC % kPer == 0, "whole 16-byte pieces");
+#pragma unroll
+    for (int piece = 0; piece < VEC / kPer; ++piece) {
+        const uint4 u = Shared ? *reinterpret_cast<const uint4*>(p + piece * kPer)
+                               : __ldg(reinterpret_cast<const uint4*>(p + piece * kPer));
         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
-            v[2 * k] = f.x;
-            v[2 * k + 1] = f.y;
+            if constexpr (sizeof(Tin) == 2) {
+                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+                v[piece * kPer + 2 * k] = f.x;
+                v[piece * kPer + 2 * k + 1] = f.y;
+            } else {
+                v[piece * kPer + k] = __uint_as_float(w[k]);
+            }
         }
-    } else {
-        static_assert(sizeof(Tin) == 4 && VEC == 4, "the bulk-copy pass reads 16-byte vectors");
-        const float4 u = *reinterpret_cast<const float4*>(p);
-        v[0] = u.x;
-        v[1] = u.y;
-        v[2] = u.z;
-        v[3] = u.w;
     }
+}
+
+// sigmoid and exp for the bf16-cache streaming pass on the special-function unit
+// (ex2.approx, rcp.approx: relative errors near 2^-22, far below the bf16 inputs'
+// 2^-9); the fp32 path keeps expf.
+template <bool kFast>
+__device__ __forceinline__ float exp_f(float x) {
+    if constexpr (kFast) return ptx::ex2_approx(x * 1.4426950408889634f);
+    return expf(x);
+}
+template <bool kFast>
+__device__ __forceinline__ float sigmoid_f(float x) {
+    if constexpr (kFast) return __frcp_rn(1.f + exp_f<true>(-x));
+    return sigmoid_exact(x);
 }
 
 // One bulk copy global -> shared, completion counted on `bar` in bytes (both
@@ -106,6 +125,20 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
                      ptx::smem_u32(dst)),
                  "l"(src), "r"(bytes), "r"(ptx::smem_u32(bar))
                  : "memory");
+}
+
+// Cluster-wide barrier (every thread of every CTA of the cluster): shared-memory
+// writes before it are visible to the cluster's reads after it.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Reads the float at the same shared-memory offset as `p` in CTA `rank` of the cluster.
+__device__ __forceinline__ float ld_cluster_f32(const float* p, int rank) {
+    uint32_t remote;
+    float v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(ptx::smem_u32(p)), "r"(rank));
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
 }
 
 // Partial pass: CTA (bh, chunk) handles keys [chunk*C, min(chunk*C + C, t+1));
@@ -214,144 +247,206 @@ __global__ void __launch_bounds__(kThreads) decode_partial_kernel(
     }
 }
 
-// Partial pass for contiguous [B, H, T, d] caches whose rows are a multiple of 16
-// bytes: the chunk's cached P2 and I~ rows arrive in shared memory by two bulk
-// copies (one instruction each, completion on one mbarrier); the new token's row
-// is stored next to them; the scores and the weighted sum then read shared memory.
-// Same outputs as decode_partial_kernel.
+// Streaming pass for contiguous [B, H, T, d] caches whose rows are a multiple of
+// 16 bytes.  The S CTAs of a head form one thread-block cluster; CTA s takes an
+// equal share of whole chunks of the cached rows 0..t-1 (CH rows per chunk) and
+// streams them through a ring of kStreamStages shared-memory stages, each filled
+// by two bulk copies (P2 rows, I~ rows) completing on the stage's mbarrier, so
+// the copies of the next chunks are in flight while the current one is scored.
+// Every group of G lanes keeps an online softmax over its rows (running max m,
+// sum l and weighted sum o of the I~ rows: the scan of Sec. 5.1 eq.(12)); the
+// groups merge into the CTA's (m, l, o), and CTA 0 of the cluster merges the S
+// results through distributed shared memory and writes Y and L.  CTA 0 also
+// scores the new token's row (the Self entry, from the new-row tensors) and
+// appends it to the cache row t, which no CTA reads.
+constexpr int kStreamStages = 3;
 template <typename Tin, int VEC, int G>
-__global__ void __launch_bounds__(kThreads) decode_partial_bulk_kernel(
+__global__ void __launch_bounds__(kThreads, 2) decode_cluster_kernel(
     KernelProblem kp, const Tin* __restrict__ P1n, const Tin* __restrict__ P2n, const Tin* __restrict__ Vn,
-    Tin* __restrict__ P2c, Tin* __restrict__ Vc, const int* __restrict__ pos, int append, int chunk,
-    float* __restrict__ part, unsigned int* status) {
+    Tin* __restrict__ P2c, Tin* __restrict__ Vc, const int* __restrict__ pos, int append, int ch,
+    Tin* __restrict__ Y, float* __restrict__ L, unsigned int* status) {
     constexpr int kGroups = kThreads / G;
+    constexpr bool kFast = sizeof(Tin) == 2;
     extern __shared__ __align__(128) uint8_t smb[];
+    __shared__ __align__(8) uint64_t full[kStreamStages];
     __shared__ int abort_flag;
     const int d = kp.d;
     const size_t row_bytes = (size_t)d * sizeof(Tin);
-    Tin* sK = reinterpret_cast<Tin*>(smb);
-    Tin* sV = reinterpret_cast<Tin*>(smb + (size_t)chunk * row_bytes);
-    float* sr = reinterpret_cast<float*>(smb + 2 * (size_t)chunk * row_bytes);  // chunk scores
-    float* red = sr + chunk;                                                     // per-warp reductions (8)
-    float* oacc = red + 8;                                                       // kGroups x d partial outputs
-    uint64_t* bar = reinterpret_cast<uint64_t*>(oacc + (size_t)kGroups * d);
+    const size_t stage_bytes = 2 * (size_t)ch * row_bytes;
+    // After the stream the stage area holds the merge: per group o (kGroups x d),
+    // m and l, then the CTA's result (m, l, o[d]).
+    float* og = reinterpret_cast<float*>(smb);
+    float* gm = og + (size_t)kGroups * d;
+    float* gl = gm + kGroups;
+    float* res = gl + kGroups;
     const int64_t bh = blockIdx.x;
     const int b = (int)(bh / kp.H);
     const int t = pos[b];
-    float* out = part + ((size_t)bh * gridDim.y + blockIdx.y) * (size_t)(d + 2);
-    if (t < 0 || t >= kp.T) {  // position outside the cache: reported, head skipped
-        if (threadIdx.x == 0) {
-            record_status(status, kDevBadPosition);
-            out[0] = -INFINITY;
-            out[1] = 0.f;
-        }
+    const int S = (int)gridDim.y, sidx = (int)blockIdx.y;  // cluster = the S CTAs of head bh
+    if (t < 0 || t >= kp.T) {  // position outside the cache (the whole cluster returns): reported, not written
+        if (threadIdx.x == 0 && sidx == 0) record_status(status, kDevBadPosition);
         return;
     }
-    const int n = t + 1;  // keys visible to the new row
-    const int j0 = blockIdx.y * chunk, j1 = min(n, j0 + chunk);
     const size_t new_off = (size_t)bh * d;  // [B, H, d] new-row tensors
-    if (append && blockIdx.y == 0)          // the new row goes to cache row t, which no CTA reads
+    if (append && sidx == 0)                // cache row t: no CTA reads it
         for (int c = threadIdx.x; c < d; c += kThreads) {
             P2c[row_offset(kp, bh, t) + c] = P2n[new_off + c];
             Vc[row_offset(kp, bh, t) + c] = Vn[new_off + c];
         }
-    if (j0 >= j1) {
-        if (threadIdx.x == 0) {
-            out[0] = -INFINITY;
-            out[1] = 0.f;
-        }
-        return;
-    }
-    const int rc = max(0, min(j1, t) - j0);  // cached rows of this chunk (row t is the new token)
+    const int n_all = (t + ch - 1) / ch;  // chunks of cached rows
+    const int per = (n_all + S - 1) / S;
+    const int k0 = sidx * per;
+    const int nck = max(0, min(n_all, k0 + per) - k0);
     if (threadIdx.x == 0) {
-        ptx::mbar_init(bar, 1);
+        for (int k = 0; k < kStreamStages; ++k) ptx::mbar_init(&full[k], 1);
         abort_flag = 0;
         ptx::fence_barrier_init();
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        if (rc > 0) {
-            const uint32_t bytes = (uint32_t)(rc * row_bytes);
-            ptx::mbar_arrive_expect_tx(bar, 2 * bytes);
-            bulk_copy_g2s(sK, P2c + row_offset(kp, bh, j0), bytes, bar);
-            bulk_copy_g2s(sV, Vc + row_offset(kp, bh, j0), bytes, bar);
-        } else {
-            ptx::mbar_arrive(bar);
-        }
-    }
-    if (t >= j0 && t < j1)  // the new token's row, next to the copied rows (disjoint from them)
-        for (int c = threadIdx.x; c < d; c += kThreads) {
-            sK[(size_t)(t - j0) * d + c] = P2n[new_off + c];
-            sV[(size_t)(t - j0) * d + c] = Vn[new_off + c];
-        }
-    (void)ptx::mbar_wait(bar, 0, &abort_flag, status, kDevTimeoutFull);
-    __syncthreads();
-    if (abort_flag) {  // the copies did not land within the limit (recorded in the status word)
-        if (threadIdx.x == 0) {
-            ptx::mbar_drain(bar, 0, status);  // give the copies in flight a second bounded wait before leaving
-            out[0] = -INFINITY;
-            out[1] = 0.f;
-        }
-        return;
-    }
+    // Thread 0 fills stage k % kStreamStages with chunk k0 + k.
+    auto issue = [&](int k) {
+        const int j0 = (k0 + k) * ch;
+        const int rc = min(t, j0 + ch) - j0;
+        uint8_t* st = smb + (size_t)(k % kStreamStages) * stage_bytes;
+        const uint32_t bytes = (uint32_t)(rc * row_bytes);
+        uint64_t* bar = &full[k % kStreamStages];
+        ptx::mbar_arrive_expect_tx(bar, 2 * bytes);
+        bulk_copy_g2s(st, P2c + row_offset(kp, bh, j0), bytes, bar);
+        bulk_copy_g2s(st + (size_t)ch * row_bytes, Vc + row_offset(kp, bh, j0), bytes, bar);
+    };
+    int issued = 0;  // chunks whose copies thread 0 has issued
+    if (threadIdx.x == 0)
+        for (; issued < kStreamStages && issued < nck; ++issued) issue(issued);
     const int grp = threadIdx.x / G, li = threadIdx.x % G;
     const int col = li * VEC;
     const bool active = col < d;
     float q[VEC];
 #pragma unroll
     for (int k = 0; k < VEC; ++k) q[k] = 0.f;
-    if (active) load_vec<Tin, VEC>(P1n + new_off + col, q);
-    const float corr = kp.lambda * logf((float)n);  // lambda log c, c = t+1
-    float mloc = -INFINITY;
-    for (int base = j0; base < j1; base += kGroups) {
-        const int j = base + grp;
-        float dot = 0.f;
-        if (j < j1 && active) {
-            float kv[VEC];
-            load_vec_shared<Tin, VEC>(sK + (size_t)(j - j0) * d + col, kv);
-#pragma unroll
-            for (int k = 0; k < VEC; ++k) dot = fmaf(q[k], kv[k], dot);
-        }
-#pragma unroll
-        for (int o = G / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-        if (j < j1) {
-            const float u = dot * kp.inv_sqrt_d;
-            const float r = (j == t) ? sigmoid_exact(u / kp.tau_S) : u * sigmoid_exact(u) - corr;
-            if (li == 0) sr[j - j0] = r;
-            mloc = fmaxf(mloc, r);
-        }
-    }
-    const float m = block_reduce(mloc, red, true);  // also orders the score stores
-    float o[VEC];
+    if (active) load_vec16<Tin, VEC, false>(P1n + new_off + col, q);
+    const float corr = kp.lambda * logf((float)(t + 1));  // lambda log c, c = t+1
+    float m = -INFINITY, l = 0.f, o[VEC];
 #pragma unroll
     for (int k = 0; k < VEC; ++k) o[k] = 0.f;
-    float lloc = 0.f;
-    for (int j = j0 + grp; j < j1; j += kGroups) {
-        const float p = expf(sr[j - j0] - m);
-        if (li == 0) lloc += p;
-        if (active) {
-            float vv[VEC];
-            load_vec_shared<Tin, VEC>(sV + (size_t)(j - j0) * d + col, vv);
+    // One row (its P2 and I~ values kv, vv) into the group's running state.  Every
+    // lane of the warp calls this together (the shuffles span the warp); lanes of a
+    // group without a row this round pass valid = false and keep their state.
+    auto take = [&](const float (&kv)[VEC], const float (&vv)[VEC], bool self, bool valid) {
+        float dot = 0.f;
+#pragma unroll
+        for (int k = 0; k < VEC; ++k) dot = fmaf(q[k], kv[k], dot);
+#pragma unroll
+        for (int w = G / 2; w > 0; w >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, w);
+        if (!valid) return;
+        const float u = dot * kp.inv_sqrt_d;
+        const float r = self ? sigmoid_f<kFast>(u / kp.tau_S) : u * sigmoid_f<kFast>(u) - corr;
+        // The running maximum is raised only when a row exceeds it (then the state is
+        // rescaled); otherwise the row adds exp(r - m).
+        if (r > m) {
+            const float s1 = (m == -INFINITY) ? 0.f : exp_f<kFast>(m - r);
+            l = fmaf(l, s1, 1.f);
+#pragma unroll
+            for (int k = 0; k < VEC; ++k) o[k] = fmaf(o[k], s1, vv[k]);
+            m = r;
+        } else {
+            const float p = exp_f<kFast>(r - m);
+            l += p;
 #pragma unroll
             for (int k = 0; k < VEC; ++k) o[k] = fmaf(p, vv[k], o[k]);
         }
-    }
-    const float l = block_reduce(lloc, red, false);
-    if (active) {
-        float* dst = oacc + (size_t)grp * d + col;
+    };
+    bool ok = true;
+    for (int k = 0; k < nck; ++k) {
+        if (!ptx::mbar_wait(&full[k % kStreamStages], (k / kStreamStages) & 1, &abort_flag, status,
+                            kDevTimeoutFull))
+            ok = false;
+        if (!__syncthreads_and(ok)) {  // every thread leaves together
+            ok = false;
+            break;
+        }
+        const Tin* sK = reinterpret_cast<const Tin*>(smb + (size_t)(k % kStreamStages) * stage_bytes);
+        const Tin* sV = sK + (size_t)ch * d;
+        const int rc = min(t, (k0 + k) * ch + ch) - (k0 + k) * ch;
+        for (int base = 0; base < rc; base += kGroups) {  // same trip count in every lane
+            const int r = base + grp;
+            float kv[VEC], vv[VEC];
 #pragma unroll
-        for (int k = 0; k < VEC; ++k) dst[k] = o[k];
+            for (int e = 0; e < VEC; ++e) kv[e] = vv[e] = 0.f;
+            if (active && r < rc) {
+                load_vec16<Tin, VEC, true>(sK + (size_t)r * d + col, kv);
+                load_vec16<Tin, VEC, true>(sV + (size_t)r * d + col, vv);
+            }
+            take(kv, vv, false, r < rc);
+        }
+        __syncthreads();  // the stage is consumed: refill it with the chunk kStreamStages ahead
+        if (threadIdx.x == 0 && issued < nck) issue(issued++);
+    }
+    if (!ok && threadIdx.x == 0)
+        // Give the copies in flight (the last one issued into each stage) a second
+        // bounded wait before the stage area is reused.
+        for (int k = max(0, issued - kStreamStages); k < issued; ++k)
+            ptx::mbar_drain(&full[k % kStreamStages], (k / kStreamStages) & 1, status);
+    if (sidx == 0 && threadIdx.x < 32) {  // the new token's Self entry, by group 0 (warp 0 shuffles together)
+        float kv[VEC], vv[VEC];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) kv[e] = vv[e] = 0.f;
+        if (active && grp == 0) {
+            load_vec16<Tin, VEC, false>(P2n + new_off + col, kv);
+            load_vec16<Tin, VEC, false>(Vn + new_off + col, vv);
+        }
+        take(kv, vv, true, grp == 0);
+    }
+    if (!ok) m = -INFINITY;  // a share whose rows did not arrive is left out (the timeout is reported)
+    // Merge of the groups into this CTA's (m, l, o) (the stages are no longer read).
+    __syncthreads();
+    if (active) {
+#pragma unroll
+        for (int k = 0; k < VEC; ++k) og[(size_t)grp * d + col + k] = o[k];
+    }
+    if (li == 0) {
+        gm[grp] = m;
+        gl[grp] = l;
     }
     __syncthreads();
+    float M = -INFINITY;
+    for (int g = 0; g < kGroups; ++g) M = fmaxf(M, gm[g]);
     for (int c = threadIdx.x; c < d; c += kThreads) {
         float acc = 0.f;
-        for (int g = 0; g < kGroups; ++g) acc += oacc[(size_t)g * d + c];
-        out[2 + c] = acc;
+        for (int g = 0; g < kGroups; ++g)
+            if (gm[g] != -INFINITY) acc = fmaf(exp_f<kFast>(gm[g] - M), og[(size_t)g * d + c], acc);
+        res[2 + c] = acc;
     }
     if (threadIdx.x == 0) {
-        out[0] = m;
-        out[1] = l;
+        float Lc = 0.f;
+        for (int g = 0; g < kGroups; ++g)
+            if (gm[g] != -INFINITY) Lc = fmaf(exp_f<kFast>(gm[g] - M), gl[g], Lc);
+        res[0] = M;
+        res[1] = Lc;
     }
+    // Every CTA of the cluster has its result in shared memory; CTA 0 merges them
+    // (Y = sum_s e^{m_s - M} o_s / sum_s e^{m_s - M} l_s, L = M + log of the
+    // denominator, the paper's convention with the correction included), then the
+    // cluster leaves together so no result is read after its CTA has exited.
+    cluster_sync();
+    if (sidx == 0) {
+        float Mc = -INFINITY;
+        for (int r = 0; r < S; ++r) Mc = fmaxf(Mc, ld_cluster_f32(res, r));
+        float den = 0.f;
+        for (int r = 0; r < S; ++r) {
+            const float mr = ld_cluster_f32(res, r);
+            if (mr != -INFINITY) den = fmaf(exp_f<kFast>(mr - Mc), ld_cluster_f32(res + 1, r), den);
+        }
+        for (int c = threadIdx.x; c < d; c += kThreads) {
+            float num = 0.f;
+            for (int r = 0; r < S; ++r) {
+                const float mr = ld_cluster_f32(res, r);
+                if (mr != -INFINITY) num = fmaf(exp_f<kFast>(mr - Mc), ld_cluster_f32(res + 2 + c, r), num);
+            }
+            store_from_float(Y + new_off + c, num / den);
+        }
+        if (L != nullptr && threadIdx.x == 0) L[bh] = Mc + logf(den);
+    }
+    cluster_sync();
 }
 
 // Merge of the chunks of one head: Y = sum_c e^{m_c - M} o_c / sum_c e^{m_c - M} l_c,
@@ -362,6 +457,9 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(KernelProblem kp, c
                                                               float* __restrict__ L) {
     extern __shared__ float w[];  // per chunk: its maximum m_c, then its weight e^{m_c - M}
     __shared__ float red[4];
+    // Launched as a programmatic dependent of the partial pass: wait until that
+    // grid has completed and its writes are visible (a no-op for a plain launch).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t bh = blockIdx.x;
     const int d = kp.d;
     const float* ph = part + (size_t)bh * n_chunks * (d + 2);
@@ -407,10 +505,6 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(KernelProblem kp, c
     if (L != nullptr && threadIdx.x == 0) L[bh] = M + logf(den);
 }
 
-// Shared memory the bulk-copy pass may ask for (two tensors' rows, at most 64 KB,
-// plus scores, reductions, partial outputs and the barrier).
-constexpr int kBulkSmemMax = 96 * 1024;
-
 // The bulk-copy pass serves contiguous [B, H, T, d] caches whose rows are a
 // multiple of 16 bytes; its chunk keeps both tensors' rows within 64 KB.
 bool decode_bulk(const KernelProblem& kp, bool bf16) {
@@ -423,41 +517,92 @@ int decode_chunk_rows(const KernelProblem& kp, bool bf16) {
     return (2 * 256 * row_bytes <= 65536) ? 256 : (2 * 128 * row_bytes <= 65536) ? 128 : 64;
 }
 
+// Rows per chunk of the streaming pass: at most 16 KB of each tensor per stage.
+int stream_chunk_rows(const KernelProblem& kp, bool bf16) {
+    const int rows = 16384 / (kp.d * (bf16 ? 2 : 4));
+    return rows < 128 ? rows : 128;
+}
+constexpr int kStreamSmemMax = 120 * 1024;
+constexpr int kMaxCluster = 8;  // portable cluster size
+
+// The merge, launched as a programmatic dependent of the partial pass (it may be
+// scheduled while that pass finishes and waits for its writes in-kernel).
+template <typename Tin>
+cudaError_t launch_combine(const KernelProblem& kp, const float* part, int n_chunks, Tin* Y, float* L,
+                           cudaStream_t s) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)kp.BH);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = sizeof(float) * (size_t)n_chunks;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_combine_kernel<Tin>, kp, part, n_chunks, Y, L);
+}
+
+// Streaming pass (bulk-copy caches): one cluster of S CTAs per head, S chosen so
+// that the grid fills the GPU once at the occupancy the kernel's shared memory
+// allows (at most the portable cluster size of 8).  One launch: the merge
+// happens inside each cluster.
 template <typename Tin, int VEC, int G>
-cudaError_t launch_decode_t(const KernelProblem& kp, const void* P1n, const void* P2n, const void* Vn, void* P2c,
-                            void* Vc, const int* pos, int append, void* Y, float* L, float* part, bool bulk,
-                            int chunk, int n_chunks, unsigned int* status, cudaStream_t s) {
+cudaError_t launch_stream(const KernelProblem& kp, const void* P1n, const void* P2n, const void* Vn, void* P2c,
+                          void* Vc, const int* pos, int append, void* Y, float* L, unsigned int* status,
+                          int num_sms, cudaStream_t s) {
+    constexpr int kGroups = kThreads / G;
+    auto kern = decode_cluster_kernel<Tin, VEC, G>;
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [&] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kStreamSmemMax);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    const int ch = stream_chunk_rows(kp, sizeof(Tin) == 2);
+    const size_t stages = (size_t)kStreamStages * 2 * ch * kp.d * sizeof(Tin);
+    const size_t merge = sizeof(float) * ((size_t)kGroups * kp.d + 2 * kGroups + kp.d + 2);
+    const size_t smem = stages > merge ? stages : merge;
+    if (smem > (size_t)kStreamSmemMax) return cudaErrorInvalidValue;
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+    if (e != cudaSuccess) return e;
+    const int64_t chunks_max = ((int64_t)kp.T + ch - 1) / ch;
+    int64_t S = ((int64_t)(per_sm > 0 ? per_sm : 1) * (num_sms > 0 ? num_sms : 148)) / kp.BH;
+    S = S < 1 ? 1 : S;
+    S = S > kMaxCluster ? kMaxCluster : S;
+    S = S > chunks_max ? chunks_max : S;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)kp.BH, (unsigned)S);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = (unsigned)S;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, kp, (const Tin*)P1n, (const Tin*)P2n, (const Tin*)Vn, (Tin*)P2c, (Tin*)Vc,
+                              pos, append, ch, (Tin*)Y, L, status);
+}
+
+// Direct pass (other caches): CTA (bh, chunk) over `chunk` keys read from HBM,
+// then the merge.
+template <typename Tin, int VEC, int G>
+cudaError_t launch_direct(const KernelProblem& kp, const void* P1n, const void* P2n, const void* Vn, void* P2c,
+                          void* Vc, const int* pos, int append, void* Y, float* L, float* part, int chunk,
+                          int n_chunks, unsigned int* status, cudaStream_t s) {
     constexpr int kGroups = kThreads / G;
     dim3 grid((unsigned)kp.BH, (unsigned)n_chunks);
-    bool launched = false;
-    if constexpr (!(sizeof(Tin) == 2 && VEC == 4)) {  // 16-byte rows vectors only
-        if (bulk) {
-            static std::once_flag attr_once;
-            static cudaError_t attr_err = cudaSuccess;
-            std::call_once(attr_once, [] {
-                attr_err = cudaFuncSetAttribute(decode_partial_bulk_kernel<Tin, VEC, G>,
-                                                cudaFuncAttributeMaxDynamicSharedMemorySize, kBulkSmemMax);
-            });
-            if (attr_err != cudaSuccess) return attr_err;
-            const size_t smem = 2 * (size_t)chunk * kp.d * sizeof(Tin) +
-                                sizeof(float) * ((size_t)chunk + 8 + (size_t)kGroups * kp.d) + 16;
-            if (smem > (size_t)kBulkSmemMax) return cudaErrorInvalidValue;
-            decode_partial_bulk_kernel<Tin, VEC, G><<<grid, kThreads, smem, s>>>(
-                kp, (const Tin*)P1n, (const Tin*)P2n, (const Tin*)Vn, (Tin*)P2c, (Tin*)Vc, pos, append, chunk, part,
-                status);
-            launched = true;
-        }
-    }
-    if (!launched) {
-        const size_t smem = sizeof(float) * ((size_t)chunk + 8 + (size_t)kGroups * kp.d);
-        decode_partial_kernel<Tin, VEC, G><<<grid, kThreads, smem, s>>>(kp, (const Tin*)P1n, (const Tin*)P2n,
-                                                                        (const Tin*)Vn, (Tin*)P2c, (Tin*)Vc, pos,
-                                                                        append, chunk, part, status);
-    }
+    const size_t smem = sizeof(float) * ((size_t)chunk + 8 + (size_t)kGroups * kp.d);
+    decode_partial_kernel<Tin, VEC, G><<<grid, kThreads, smem, s>>>(kp, (const Tin*)P1n, (const Tin*)P2n,
+                                                                    (const Tin*)Vn, (Tin*)P2c, (Tin*)Vc, pos, append,
+                                                                    chunk, part, status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    decode_combine_kernel<Tin><<<(unsigned)kp.BH, 128, sizeof(float) * n_chunks, s>>>(kp, part, n_chunks, (Tin*)Y, L);
-    return cudaGetLastError();
+    return launch_combine<Tin>(kp, part, n_chunks, (Tin*)Y, L, s);
 }
 
 }  // namespace
@@ -473,16 +618,39 @@ bool decode_grid_fits(const KernelProblem& kp, bool bf16) {
 
 cudaError_t launch_decode(const KernelProblem& kp, bool bf16, const void* P1n, const void* P2n, const void* Vn,
                           void* P2c, void* Vc, const int* pos, int append, void* Y, float* L, float* part,
-                          unsigned int* status, cudaStream_t s) {
+                          unsigned int* status, int num_sms, cudaStream_t s) {
     const int n_chunks = decode_chunks(kp, bf16);
     if (!decode_grid_fits(kp, bf16)) return cudaErrorInvalidValue;
-    const bool bulk = decode_bulk(kp, bf16);
     const int chunk = decode_chunk_rows(kp, bf16);
-    // Vector width and lanes per key row by (dtype, d): rows are read 16 bytes per
-    // lane where the row pitch allows it (8 bytes for bf16 d = 60).
-#define RELATION_DECODE(T_, VEC, G)                                                                           \
-    return launch_decode_t<T_, VEC, G>(kp, P1n, P2n, Vn, P2c, Vc, pos, append, Y, L, part, bulk, chunk, n_chunks, \
-                                       status, s)
+    if (decode_bulk(kp, bf16)) {
+        // Streaming pass: 16 bf16 or 8 fp32 elements per lane (two 16-byte pieces),
+        // G lanes per key row (a power of two covering d; fp32 d = 60 in 4-element
+        // pieces, its rows being 240 bytes).
+#define RELATION_STREAM(T_, VEC, G)                                                                              \
+    return launch_stream<T_, VEC, G>(kp, P1n, P2n, Vn, P2c, Vc, pos, append, Y, L, status, num_sms, s)
+        if (bf16) {
+            switch (kp.d) {
+                case 48: RELATION_STREAM(__nv_bfloat16, 16, 4);
+                case 64: RELATION_STREAM(__nv_bfloat16, 16, 4);
+                case 80: RELATION_STREAM(__nv_bfloat16, 16, 8);
+                case 128: RELATION_STREAM(__nv_bfloat16, 16, 8);
+                default: return cudaErrorInvalidValue;
+            }
+        }
+        switch (kp.d) {
+            case 48: RELATION_STREAM(float, 8, 8);
+            case 60: RELATION_STREAM(float, 4, 16);
+            case 64: RELATION_STREAM(float, 8, 8);
+            case 80: RELATION_STREAM(float, 8, 16);
+            case 128: RELATION_STREAM(float, 8, 16);
+            default: return cudaErrorInvalidValue;
+        }
+#undef RELATION_STREAM
+    }
+    // Direct pass: rows read 16 bytes per lane where the row pitch allows it (8
+    // bytes for bf16 d = 60).
+#define RELATION_DECODE(T_, VEC, G) \
+    return launch_direct<T_, VEC, G>(kp, P1n, P2n, Vn, P2c, Vc, pos, append, Y, L, part, chunk, n_chunks, status, s)
     if (bf16) {
         switch (kp.d) {
             case 48: RELATION_DECODE(__nv_bfloat16, 8, 8);

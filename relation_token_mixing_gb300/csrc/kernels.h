@@ -47,7 +47,7 @@ constexpr int kDecodeMaxChunks = 8192;
 bool decode_grid_fits(const KernelProblem& kp, bool bf16);
 cudaError_t launch_decode(const KernelProblem& kp, bool bf16, const void* P1n, const void* P2n, const void* Vn,
                           void* P2c, void* Vc, const int* pos, int append, void* Y, float* L, float* part,
-                          unsigned int* status, cudaStream_t s);
+                          unsigned int* status, int num_sms, cudaStream_t s);
 // n (<= 4) bf16 operand tensors of width kp.d <= 64 (any layout) -> zero-padded
 // contiguous [BH, T, 64] copies.
 cudaError_t launch_pad_operands(const KernelProblem& kp, const void* const* src, void* const* dst, int n,
