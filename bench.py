@@ -170,8 +170,9 @@ def decode_bytes_per_step(w, t: int) -> int:
 
 def decode_kernels(w) -> str:
     """The decoding kernels the bench's [B, H, T, d] bf16 caches run on."""
-    part = "decode_partial_bulk_kernel" if (w.d * 2) % 16 == 0 else "decode_partial_kernel"
-    return f"{part} + decode_combine_kernel"
+    if (w.d * 2) % 16 == 0:
+        return "decode_cluster_kernel"  # streaming pass and in-cluster merge, one launch
+    return "decode_partial_kernel + decode_combine_kernel"
 
 
 def decode_config(w, t: int) -> dict:
@@ -285,7 +286,7 @@ def run_decode(args, w):
         "roofline": {"kernel": decode_kernels(w), "bound": "hbm",
                      "achieved": bytes_step / (ms * 1e-3) / 1e9, "peak": hbm[0], "unit": "GB/s",
                      "frac": bytes_step / (ms * 1e-3) / 1e9 / hbm[0], "peak_source": hbm[1], "traffic": None},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": (1 if (w.d * 2) % 16 == 0 else 2) * args.steps,
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline:

@@ -223,8 +223,14 @@ relation_status_t relation_bwd_noalloc(const relation_problem_t* p, const void* 
  *    step's position; the library does not change `positions`.
  * Y: [B, H, d_h] (dtype).  L: optional [B, H] float32 log-normaliser of the row.
  * workspace: at least relation_decode_workspace_bytes(p) bytes, float32
- *    partial results.  Outputs must not overlap inputs or caches.
- * Two kernel launches (per-chunk partials, then one merge per head).
+ *    partial results (used by direct-read caches; streamed caches merge in
+ *    shared memory and leave it untouched).  Outputs must not overlap inputs
+ *    or caches.
+ * Caches in the [B, H, T, d_h] layout whose rows are a multiple of 16 bytes
+ * are streamed: one launch, a thread-block cluster of up to 8 CTAs per head
+ * whose CTAs each read a share of the history and merge in distributed shared
+ * memory.  Other caches take two launches (per-chunk partials, then one merge
+ * per head).
  */
 size_t relation_decode_workspace_bytes(const relation_problem_t* p);
 relation_status_t relation_decode(const relation_problem_t* p, const void* P1_new, const void* P2_new,

@@ -612,6 +612,8 @@ int decode_chunks(const KernelProblem& kp, bool bf16) {
     return (int)(((int64_t)kp.T + c - 1) / c);
 }
 
+int decode_launches(const KernelProblem& kp, bool bf16) { return decode_bulk(kp, bf16) ? 1 : 2; }
+
 bool decode_grid_fits(const KernelProblem& kp, bool bf16) {
     return kp.BH >= 1 && kp.BH <= 2147483647LL && decode_chunks(kp, bf16) <= kDecodeMaxChunks;
 }

@@ -45,6 +45,9 @@ int decode_chunks(const KernelProblem& kp, bool bf16);
 // The merge keeps one float per chunk of a head in shared memory (32 KB at most).
 constexpr int kDecodeMaxChunks = 8192;
 bool decode_grid_fits(const KernelProblem& kp, bool bf16);
+// Kernel launches of one decoding step: 1 for streamed caches (partial pass and
+// merge in one cluster launch), 2 for direct-read caches (partial pass, merge).
+int decode_launches(const KernelProblem& kp, bool bf16);
 cudaError_t launch_decode(const KernelProblem& kp, bool bf16, const void* P1n, const void* P2n, const void* Vn,
                           void* P2c, void* Vc, const int* pos, int append, void* Y, float* L, float* part,
                           unsigned int* status, int num_sms, cudaStream_t s);

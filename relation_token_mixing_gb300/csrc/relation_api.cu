@@ -640,7 +640,7 @@ relation_status_t relation_decode(const relation_problem_t* p, const void* P1_ne
     st = from_cuda(launch_decode(kernel_problem(p), p->dtype == RELATION_BF16, P1_new, P2_new, V_new, P2_cache,
                                  V_cache, positions, append, Y, L, static_cast<float*>(workspace), di.status,
                                  di.num_sms, static_cast<cudaStream_t>(stream)));
-    if (st == RELATION_OK) t_last_launches = 2;
+    if (st == RELATION_OK) t_last_launches = decode_launches(kernel_problem(p), p->dtype == RELATION_BF16);
     return st;
 }
 

@@ -76,7 +76,10 @@ def test_decode_row_matches_oracle(name, B, H, T, d, dtype, positions, layout):
     x, g = _setup(B, H, T, d, dtype, positions, tau, lam, layout)
     Y, L = rb.decode(g["P1n"], g["P2n"], g["Vn"], g["P2c"], g["Vc"], g["pos"], tau, lam, append=False,
                      layout=layout)
-    assert rb.relation_last_launch_count() == 2
+    # One cluster launch for caches the streaming pass reads ([B, H, T, d], rows a
+    # multiple of 16 bytes); a partial pass and a merge otherwise.
+    streamed = layout == BHTD and (d * (2 if dtype == torch.bfloat16 else 4)) % 16 == 0
+    assert rb.relation_last_launch_count() == (1 if streamed else 2)
     torch.cuda.synchronize()
     assert rb.relation_check_device_status() == 0
     Yr, Lr = _reference(x, positions, H, tau, lam)
