@@ -10,6 +10,10 @@ projection that produces g from the token is outside the operator):
     E_t  = S_t (C-_t)^T p^1_t,  Y_t = I~_t + E_t,  C_t = C-_t + S_t p^2_t I~_t^T   (17)
 The backward is the chain rule of this recurrence, run backwards in time with
 the states kept from the forward.  Plain numpy, one token at a time.
+
+gate()/gate_bwd() are the optional KDA-style retention of eq.(16) that produces
+g from a per-token projection r_t: g = -exp(A_log) * softplus(r + dt_bias) per
+head and channel, and its chain rule.
 """
 from __future__ import annotations
 
@@ -105,3 +109,25 @@ def bwd(P1, P2, I, G, tau: float, dY):
                 dP1[b, h, t] = dz * p2 + ((dq - q * float(q @ dq)) / n1 if n1 > 0 else 0.0)
                 dP2[b, h, t] = dz * p1 + ((dk - k * float(k @ dk)) / n2 if n2 > 0 else 0.0)
     return dP1, dP2, dI, dG
+
+
+def gate(R, A_log, dt_bias):
+    """KDA-style retention of Sec. 5.2 eq.(16) (Appendix A.4.1), per head h and channel c:
+    g = -exp(A_log[h, c]) * softplus(r + dt_bias[h, c]), alpha = exp(g) in (0, 1].
+    R: [B, H, T, d] (the projection output r_t); A_log, dt_bias: [H, d].  Returns G [B, H, T, d]."""
+    R = np.asarray(R, dtype=np.float64)
+    A_log = np.asarray(A_log, dtype=np.float64)[None, :, None, :]
+    dt_bias = np.asarray(dt_bias, dtype=np.float64)[None, :, None, :]
+    return -np.exp(A_log) * np.logaddexp(0.0, R + dt_bias)
+
+
+def gate_bwd(R, A_log, dt_bias, dG):
+    """Chain rule of gate(): from dG = d loss / d g, returns dR [B, H, T, d] and dA_log, d_dt_bias
+    [H, d] (summed over batches and tokens).  d softplus(x)/dx = sigmoid(x); d g / d A_log = g."""
+    R, dG = np.asarray(R, dtype=np.float64), np.asarray(dG, dtype=np.float64)
+    A = np.asarray(A_log, dtype=np.float64)[None, :, None, :]
+    x = R + np.asarray(dt_bias, dtype=np.float64)[None, :, None, :]
+    g = -np.exp(A) * np.logaddexp(0.0, x)
+    sig = 1.0 / (1.0 + np.exp(-x))
+    dR = dG * (-np.exp(A)) * sig
+    return dR, np.sum(dG * g, axis=(0, 2)), np.sum(dR, axis=(0, 2))

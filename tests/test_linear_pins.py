@@ -171,3 +171,93 @@ def test_retention_gradient_of_the_last_token():
     a = np.exp(G[0, 0, 4])
     expect = a * S * q * (C4[0, 0] @ W[0, 0, 4])
     assert np.allclose(dG[0, 0, 4], expect, rtol=1e-12, atol=1e-14)
+
+
+# ------------------------------------------------------------- retention gate
+# Sec. 5.2 eq.(16) / Appendix A.4.1: g = -exp(A_log) * softplus(r + dt_bias), per
+# head and channel, alpha = exp(g) in (0, 1].
+
+
+def _gate_inputs(B=2, H=3, T=5, d=4, seed=3):
+    r = np.random.default_rng(seed)
+    R = 2.0 * r.standard_normal((B, H, T, d))
+    A_log = 0.5 * r.standard_normal((H, d))
+    dt_bias = r.standard_normal((H, d))
+    return R, A_log, dt_bias
+
+
+def test_gate_special_values():
+    """softplus(0) = log 2; A_log = 0 gives exp(A_log) = 1; large arguments tend to -x e^A,
+    very negative ones to -e^A e^x; alpha stays in (0, 1]."""
+    R, A_log, dt_bias = _gate_inputs()
+    zero = np.zeros((1, 2, 1, 3))
+    G0 = lo.gate(zero, np.zeros((2, 3)), np.zeros((2, 3)))
+    assert np.allclose(G0, -np.log(2.0), rtol=0, atol=1e-15)
+    Gs = lo.gate(zero, np.log(np.array([[2.0, 3.0, 5.0]] * 2)), np.zeros((2, 3)))
+    assert np.allclose(Gs[0, 0, 0], -np.array([2.0, 3.0, 5.0]) * np.log(2.0), atol=1e-14)
+    big = lo.gate(np.full((1, 1, 1, 1), 40.0), np.array([[0.3]]), np.array([[1.0]]))
+    assert abs(big[0, 0, 0, 0] + np.exp(0.3) * 41.0) < 1e-12
+    small = lo.gate(np.full((1, 1, 1, 1), -40.0), np.array([[0.3]]), np.array([[1.0]]))
+    assert abs(small[0, 0, 0, 0] / (-np.exp(0.3) * np.exp(-39.0)) - 1.0) < 1e-12
+    G = lo.gate(R, A_log, dt_bias)
+    assert np.all(G < 0.0) and np.all(np.exp(G) <= 1.0) and np.all(np.exp(G) > 0.0)
+    # per-(head, channel) parameters: head h, channel c use A_log[h, c] and dt_bias[h, c]
+    h, c = 2, 1
+    x = R[1, h, 3, c] + dt_bias[h, c]
+    assert abs(G[1, h, 3, c] + np.exp(A_log[h, c]) * np.log1p(np.exp(x))) < 1e-12
+
+
+def test_gate_backward_by_finite_differences():
+    R, A_log, dt_bias = _gate_inputs()
+    dG = np.random.default_rng(9).standard_normal(R.shape)
+    dR, dA, dB = lo.gate_bwd(R, A_log, dt_bias, dG)
+    f = lambda R_, A_, b_: float(np.sum(lo.gate(R_, A_, b_) * dG))
+    h = 1e-6
+    for idx in [(0, 0, 0, 0), (1, 2, 4, 3), (0, 1, 2, 1)]:
+        Rp, Rm = R.copy(), R.copy()
+        Rp[idx] += h
+        Rm[idx] -= h
+        assert abs((f(Rp, A_log, dt_bias) - f(Rm, A_log, dt_bias)) / (2 * h) - dR[idx]) < 1e-6
+    for idx in [(0, 0), (2, 3), (1, 2)]:
+        Ap, Am = A_log.copy(), A_log.copy()
+        Ap[idx] += h
+        Am[idx] -= h
+        assert abs((f(R, Ap, dt_bias) - f(R, Am, dt_bias)) / (2 * h) - dA[idx]) < 1e-6
+        bp, bm = dt_bias.copy(), dt_bias.copy()
+        bp[idx] += h
+        bm[idx] -= h
+        assert abs((f(R, A_log, bp) - f(R, A_log, bm)) / (2 * h) - dB[idx]) < 1e-6
+
+
+def test_gated_linear_relation_chain_by_finite_differences():
+    """The gated operator: Y = Linear(P1, P2, I~, gate(R)); its gradients w.r.t. R, A_log and
+    dt_bias are the oracle's dG pushed through gate_bwd."""
+    B, H, T, d, tau = 1, 2, 6, 3, 1.5
+    P1, P2, I, _ = _inputs(B, H, T, d, seed=5)
+    R, A_log, dt_bias = _gate_inputs(B, H, T, d, seed=6)
+    dY = np.random.default_rng(7).standard_normal((B, H, T, d))
+    _, _, _, dG = lo.bwd(P1, P2, I, lo.gate(R, A_log, dt_bias), tau, dY)
+    dR, dA, dB = lo.gate_bwd(R, A_log, dt_bias, dG)
+    f = lambda R_, A_, b_: float(np.sum(lo.fwd(P1, P2, I, lo.gate(R_, A_, b_), tau)[0] * dY))
+    h = 1e-6
+    for idx in [(0, 0, 3, 1), (0, 1, 5, 2)]:
+        Rp, Rm = R.copy(), R.copy()
+        Rp[idx] += h
+        Rm[idx] -= h
+        assert abs((f(Rp, A_log, dt_bias) - f(Rm, A_log, dt_bias)) / (2 * h) - dR[idx]) < 1e-6
+    for idx in [(0, 0), (1, 2)]:
+        Ap, Am = A_log.copy(), A_log.copy()
+        Ap[idx] += h
+        Am[idx] -= h
+        assert abs((f(R, Ap, dt_bias) - f(R, Am, dt_bias)) / (2 * h) - dA[idx]) < 1e-6
+        bp, bm = dt_bias.copy(), dt_bias.copy()
+        bp[idx] += h
+        bm[idx] -= h
+        assert abs((f(R, A_log, bp) - f(R, A_log, bm)) / (2 * h) - dB[idx]) < 1e-6
+
+
+def test_gate_pins_catch_a_dropped_exponential():
+    """Planted mistake: -A_log instead of -exp(A_log) fails the special values."""
+    zero = np.zeros((1, 1, 1, 1))
+    wrong = -np.log(2.0) * np.log(np.array([[2.0]]))[None, :, None, :] * np.ones_like(zero)
+    assert abs(lo.gate(zero, np.log(np.array([[2.0]])), np.zeros((1, 1)))[0, 0, 0, 0] - wrong[0, 0, 0, 0]) > 0.5
