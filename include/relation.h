@@ -146,9 +146,11 @@ relation_status_t relation_bwd(const relation_problem_t* p, const void* P1, cons
 
 /*
  * The three stages relation_bwd runs in order, with the same arguments, for
- * callers that time or schedule them separately.  prepare: D_i, dlambda set to
- * zero (and, on the fp32 path, summed), the dP1 accumulator reset and, for bf16
- * d_h = 60, the zero-padded operand copies in the workspace.  main: the
+ * callers that time or schedule them separately.  prepare: D_i (on the bf16
+ * path folded with L_i and the count correction into the per-query constants
+ * the main pass reads, -(L_i + lambda log c_i) log2(e) and -D_i / (2 sqrt(d_h))),
+ * dlambda set to zero (and, on the fp32 path, summed), the dP1 accumulator
+ * reset and, for bf16 d_h = 60, the zero-padded operand copies in the workspace.  main: the
  * tensor-core (or fp32) pass producing dP2, dV, the dP1 partial sums and, for
  * bf16, dlambda.  finish: dP1 accumulator to dtype.
  */

@@ -42,6 +42,7 @@ using bwd_elem::ElemConst;
 using bwd_elem::elementwise16;
 
 constexpr int kTile = 128;
+constexpr uint32_t kQConstBytes = kTile / 2 * 16;  // per-query constants of one query tile
 constexpr int kElemWarps = 16;                     // warps 4 .. 19
 constexpr int kReduceWarp0 = 4 + kElemWarps;       // warps 20 .. 23
 constexpr int kThreads = 32 * (kReduceWarp0 + 4);  // 768
@@ -90,7 +91,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     relation_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_p1, const __grid_constant__ CUtensorMap tm_p2,
                            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_dy,
                            const __grid_constant__ CUtensorMap tm_dq, const KernelProblem kp,
-                           const float* __restrict__ L, const float* __restrict__ Dw, __nv_bfloat16* __restrict__ dP2,
+                           const float4* __restrict__ qconst, __nv_bfloat16* __restrict__ dP2,
                            __nv_bfloat16* __restrict__ dV, float* __restrict__ dlambda, unsigned int* status,
                            int head_group) {
     using C = BwdCfg<D>;
@@ -121,7 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         ptx::mbar_init(&bars->kv_full, 1);
         for (int s = 0; s < 2; ++s) {
-            ptx::mbar_init(&bars->q_full[s], 32);
+            ptx::mbar_init(&bars->q_full[s], 1);
             ptx::mbar_init(&bars->q_empty[s], 1);
         }
         ptx::mbar_init(&bars->s_full, 1);
@@ -158,6 +159,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       kp.layout == 0);
             }
         }
+        // Per-query constants of this head, 64 float4 (1 KB) per query tile.
+        const float4* qsrc = qconst + (size_t)bh * (size_t)(qconst_rows(T) / 2);
         int it = 0;
         for (; it < n_q; ++it) {
             const int s = it % C::kStages;
@@ -166,28 +169,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 !ptx::mbar_wait_warp(&bars->q_empty[s], ((it / C::kStages) - 1) & 1, abort_flag, status,
                                      kDevTimeoutEmpty))
                 break;
-            float* qc = reinterpret_cast<float*>(sQC + s * (kTile / 2));
-            for (int c = lane; c < kTile; c += 32) {
-                const int q = i * kTile + c;
-                float nlt = 0.f, ndk = 0.f;
-                if (q < T) {
-                    const int count = kp.causal ? (q + 1) : T;
-                    nlt = -(L[(size_t)bh * T + q] + kp.lambda * __logf((float)count)) * kLog2e;
-                    ndk = -Dw[(size_t)bh * T + q] * k_scale;
-                }
-                qc[(c >> 1) * 4 + (c & 1)] = nlt;
-                qc[(c >> 1) * 4 + 2 + (c & 1)] = ndk;
-            }
             if (lane == 0) {
-                ptx::mbar_arrive_expect_tx(&bars->q_full[s], 2 * C::kTileBytes);
+                ptx::mbar_arrive_expect_tx(&bars->q_full[s], 2 * C::kTileBytes + kQConstBytes);
+                ptx::bulk_load(sQC + s * (kTile / 2), qsrc + i * (kTile / 2), kQConstBytes, &bars->q_full[s]);
                 for (int p = 0; p < C::kPanels; ++p) {
                     ptx::tma_load_operand(sQ + s * C::kTileBytes + p * kPanelBytes, &tm_p1, &bars->q_full[s], p * 64,
                                      i * kTile, bh, head, batch, kp.layout == 0);
                     ptx::tma_load_operand(sG + s * C::kTileBytes + p * kPanelBytes, &tm_dy, &bars->q_full[s], p * 64,
                                      i * kTile, bh, head, batch, kp.layout == 0);
                 }
-            } else {
-                ptx::mbar_arrive(&bars->q_full[s]);
             }
         }
         if (lane == 0 && *abort_flag) {
@@ -437,8 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int D>
-cudaError_t launch_bwd_tc_d(const KernelProblem& kp, const void* P1, const void* P2, const void* V, const float* L,
-                            const float* Dw, const void* dY, float* dq_acc, void* dP2, void* dV, float* dlambda,
+cudaError_t launch_bwd_tc_d(const KernelProblem& kp, const void* P1, const void* P2, const void* V,
+                            const float4* qconst, const void* dY, float* dq_acc, void* dP2, void* dV, float* dlambda,
                             const TcLaunch& tl, cudaStream_t s) {
     using C = BwdCfg<D>;
     static_assert(C::kSmemBytes <= 232448, "shared memory budget");
@@ -478,19 +468,19 @@ cudaError_t launch_bwd_tc_d(const KernelProblem& kp, const void* P1, const void*
     int64_t group = (l2_bytes > 0 ? (int64_t)l2_bytes * 3 / 4 : (int64_t)96 << 20) / per_head;
     group = group < 1 ? 1 : (group > kp.BH ? kp.BH : group);
     relation_bwd_tc_kernel<D><<<dim3((unsigned)ctas), kThreads, C::kSmemBytes, s>>>(
-        m1, m2, mv, mg, mq, kp, L, Dw, (__nv_bfloat16*)dP2, (__nv_bfloat16*)dV, dlambda, tl.status, (int)group);
+        m1, m2, mv, mg, mq, kp, qconst, (__nv_bfloat16*)dP2, (__nv_bfloat16*)dV, dlambda, tl.status, (int)group);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_bwd_tc(const KernelProblem& kp, const void* P1, const void* P2, const void* V, const float* L,
-                          const float* Dw, const void* dY, float* dq_acc, void* dP2, void* dV, float* dlambda,
+cudaError_t launch_bwd_tc(const KernelProblem& kp, const void* P1, const void* P2, const void* V,
+                          const float4* qconst, const void* dY, float* dq_acc, void* dP2, void* dV, float* dlambda,
                           const TcLaunch& tl, cudaStream_t s, bool padded64) {
     if (kp.d == 48 || kp.d == 60 || kp.d == 64)
-        return launch_bwd_tc64(kp, P1, P2, V, L, Dw, dY, dq_acc, dP2, dV, dlambda, tl, s, padded64);
+        return launch_bwd_tc64(kp, P1, P2, V, qconst, dY, dq_acc, dP2, dV, dlambda, tl, s, padded64);
     if (kp.d == 80 || kp.d == 128)
-        return launch_bwd_tc_d<128>(kp, P1, P2, V, L, Dw, dY, dq_acc, dP2, dV, dlambda, tl, s);
+        return launch_bwd_tc_d<128>(kp, P1, P2, V, qconst, dY, dq_acc, dP2, dV, dlambda, tl, s);
     return cudaErrorInvalidValue;
 }
 

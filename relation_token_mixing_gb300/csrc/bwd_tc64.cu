@@ -52,6 +52,7 @@ constexpr int kElemWarps = 16;
 // warpgroup 56:  128*56 + 512*88 + 128*56 = 59392 <= 768*80.
 constexpr uint32_t kRegsControl = 56, kRegsElementwise = 88, kRegsReduce = 56;
 constexpr int kTileBytes = kTile * kD * 2;  // 16 KB: one 128-row x 128-byte swizzled panel
+constexpr uint32_t kQConstBytes = kTile / 2 * 16;  // per-query constants of one query tile
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kColS = 0, kColDP = 128, kColP = 256, kColDV = 320, kColDK = 384, kColDQ = 448;
 // Depth of the P1/dY ring: loads for tile i+2 are in flight while tile i is processed.
@@ -65,7 +66,8 @@ struct Smem {
     uint8_t ds[2][2 * kTileBytes];    // dS^T, two buffers of two 64-query panels
     uint8_t dq_stage[kTileBytes];     // one 32-column panel of the dP1 partial, fp32 [128][32], swizzled
     // Per-query constants, interleaved per column pair (2c, 2c+1):
-    // { -(L + lambda log c) log2(e) [2c], [2c+1],  -D (1/2)/sqrt(d) [2c], [2c+1] }
+    // { -(L + lambda log c) log2(e) [2c], [2c+1],  -D (1/2)/sqrt(d) [2c], [2c+1] },
+    // brought in with P1_i and dY_i (written by the preparation stage).
     float4 qconst[kQStages][kTile / 2];
     uint64_t kv_full;
     uint64_t q_full[kQStages];
@@ -108,7 +110,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     relation_bwd_tc64_kernel(const __grid_constant__ CUtensorMap tm_p1, const __grid_constant__ CUtensorMap tm_p2,
                              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_dy,
                              const __grid_constant__ CUtensorMap tm_dq, const KernelProblem kp,
-                             const float* __restrict__ L, const float* __restrict__ Dw, __nv_bfloat16* __restrict__ dP2,
+                             const float4* __restrict__ qconst, __nv_bfloat16* __restrict__ dP2,
                              __nv_bfloat16* __restrict__ dV, float* __restrict__ dlambda, unsigned int* status,
                              int head_group) {
     constexpr bool kRank3 = kLoad == kLoadTma3;
@@ -129,7 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         ptx::mbar_init(&sm.kv_full, 1);
         for (int s = 0; s < kQStages; ++s) {
-            ptx::mbar_init(&sm.q_full[s], 32);
+            ptx::mbar_init(&sm.q_full[s], 1);
             ptx::mbar_init(&sm.q_empty[s], 2);  // released by both MMA issuers
         }
         for (int s = 0; s < 2; ++s) ptx::mbar_init(&sm.ds_free[s], 1);
@@ -169,42 +171,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tma_load_operand(sm.k, &tm_p2, &sm.kv_full, 0, kv0, bh, head, batch, kRank3);
             ptx::tma_load_operand(sm.v, &tm_v, &sm.kv_full, 0, kv0, bh, head, batch, kRank3);
         }
+        // Per-query constants of this head, 64 float4 (1 KB) per query tile.
+        const float4* qsrc = qconst + (size_t)bh * (size_t)(qconst_rows(T) / 2);
         int it = 0;
         for (; it < n_q; ++it) {
             const int s = it % kQStages;
             const int i = i_first + it;
-            // Global loads first: they do not depend on the stage being free.
-            float nlt[4], ndk[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int q = i * kTile + lane + 32 * k;
-                nlt[k] = 0.f;
-                ndk[k] = 0.f;
-                if (q < T) {
-                    const int count = kp.causal ? (q + 1) : T;
-                    nlt[k] = -(L[(size_t)bh * T + q] + kp.lambda * __logf((float)count)) * kLog2e;
-                    ndk[k] = -Dw[(size_t)bh * T + q] * k_scale;
-                }
-            }
             if (it >= kQStages &&
                 !ptx::mbar_wait_warp(&sm.q_empty[s], ((it / kQStages) - 1) & 1, abort_flag, status, kDevTimeoutEmpty))
                 break;
-            // Lane pairs (2c, 2c+1) of each 32-column group build one float4.
-            float* qc = reinterpret_cast<float*>(sm.qconst[s]);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int col = lane + 32 * k;
-                qc[(col >> 1) * 4 + (col & 1)] = nlt[k];
-                qc[(col >> 1) * 4 + 2 + (col & 1)] = ndk[k];
-            }
             if (lane == 0) {
-                ptx::mbar_arrive_expect_tx(&sm.q_full[s], 2 * kTileBytes);
+                ptx::mbar_arrive_expect_tx(&sm.q_full[s], 2 * kTileBytes + kQConstBytes);
+                ptx::bulk_load(sm.qconst[s], qsrc + i * (kTile / 2), kQConstBytes, &sm.q_full[s]);
                 ptx::tma_load_operand(sm.q[s], &tm_p1, &sm.q_full[s], 0, i * kTile, bh, head, batch,
                                       kRank3);
                 ptx::tma_load_operand(sm.g[s], &tm_dy, &sm.q_full[s], 0, i * kTile, bh, head, batch,
                                       kRank3);
-            } else {
-                ptx::mbar_arrive(&sm.q_full[s]);
             }
         }
         if (lane == 0 && *abort_flag) {
@@ -496,8 +478,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_bwd_tc64(const KernelProblem& kp, const void* P1, const void* P2, const void* V, const float* L,
-                            const float* Dw, const void* dY, float* dq_acc, void* dP2, void* dV, float* dlambda,
+cudaError_t launch_bwd_tc64(const KernelProblem& kp, const void* P1, const void* P2, const void* V,
+                            const float4* qconst, const void* dY, float* dq_acc, void* dP2, void* dV, float* dlambda,
                             const TcLaunch& tl, cudaStream_t s, bool padded64) {
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
@@ -544,7 +526,7 @@ cudaError_t launch_bwd_tc64(const KernelProblem& kp, const void* P1, const void*
     group = group < 1 ? 1 : (group > kp.BH ? kp.BH : group);
     dim3 grid((unsigned)ctas);
 #define RELATION_BWD64(M)                                                                                        \
-    relation_bwd_tc64_kernel<M><<<grid, kThreads, kSmemBytes, s>>>(m1, m2, mv, mg, mq, kp, L, Dw,                 \
+    relation_bwd_tc64_kernel<M><<<grid, kThreads, kSmemBytes, s>>>(m1, m2, mv, mg, mq, kp, qconst,                 \
                                                                   (__nv_bfloat16*)dP2, (__nv_bfloat16*)dV, dlambda, \
                                                                   tl.status, (int)group)
     if (mode == kLoadTma3)

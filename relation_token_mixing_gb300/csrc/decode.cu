@@ -118,13 +118,9 @@ __device__ __forceinline__ float sigmoid_f(float x) {
     return sigmoid_exact(x);
 }
 
-// One bulk copy global -> shared, completion counted on `bar` in bytes (both
-// addresses 16-byte aligned, bytes a multiple of 16).
+// One bulk copy global -> shared, completion counted on `bar` in bytes.
 __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     ptx::smem_u32(dst)),
-                 "l"(src), "r"(bytes), "r"(ptx::smem_u32(bar))
-                 : "memory");
+    ptx::bulk_load(dst, src, bytes, bar);
 }
 
 // Cluster-wide barrier (every thread of every CTA of the cluster): shared-memory

@@ -17,13 +17,25 @@ cudaError_t launch_bwd_simt(const KernelProblem& kp, bool bf16, const void* P1, 
                             const float* L, const float* Dw, const void* dY, void* dP1, void* dP2, void* dV,
                             cudaStream_t s);
 
+// Per-query constants of the tensor-core backward kernels, written by the
+// preparation stage: for query t of head bh, nlt = -(L_t + lambda log c_t) log2(e)
+// and ndk = -D_t / (2 sqrt(d)) with D_t = dY_t . Y_t.  They are stored per query
+// pair (2p, 2p+1) as one float4 {nlt(2p), nlt(2p+1), ndk(2p), ndk(2p+1)}, each
+// head's rows padded with zeros to a multiple of 128 queries, so that the
+// constants of one 128-query tile are a single 1 KB bulk copy.
+constexpr int kQConstTile = 128;
+__host__ __device__ inline int64_t qconst_rows(int64_t T) { return (T + kQConstTile - 1) / kQConstTile * kQConstTile; }
+
 // Shared backward stages.
 // dq_acc (optional) is the fp32 dP1 accumulator [BH, T, dq_w]; it is zeroed.
 // pad_dst (bf16, d_h <= 64, dlambda summed elsewhere): also write zero-padded
 // contiguous [BH, T, 64] copies of P1, P2, V, dY to pad_dst[0..3] in the same pass.
+// qconst == nullptr: D_t is written to Dw [BH, T]; otherwise the per-query
+// constants [BH, qconst_rows(T), 2] are written to qconst and Dw is unused.
 cudaError_t launch_bwd_prepare(const KernelProblem& kp, bool bf16, const void* P1, const void* P2, const void* V,
                                const void* Y, const float* L, const void* dY, float* Dw, float* dq_acc, int dq_w,
-                               float* dlambda, cudaStream_t s, void* const* pad_dst = nullptr, int num_sms = 0);
+                               float* dlambda, cudaStream_t s, void* const* pad_dst = nullptr, int num_sms = 0,
+                               float* qconst = nullptr);
 // Input prologue.  RoPE frequencies base^(-2c/d) / (2 pi), c < d/2, as float
 // pairs hi + lo (enabled = 0: no rotation, a copy).
 struct RopeTable {
@@ -91,11 +103,11 @@ inline bool bwd_tc_sums_dlambda(int) { return true; }  // both tensor-core kerne
 // padded64: P1, P2, V, dY point to zero-padded contiguous [BH, T, 64] copies
 // (made by launch_pad_operands) instead of the caller's tensors; dP2 and dV are
 // still written in the problem's layout and width.
-cudaError_t launch_bwd_tc(const KernelProblem& kp, const void* P1, const void* P2, const void* V, const float* L,
-                          const float* Dw, const void* dY, float* dq_acc, void* dP2, void* dV, float* dlambda,
+cudaError_t launch_bwd_tc(const KernelProblem& kp, const void* P1, const void* P2, const void* V,
+                          const float4* qconst, const void* dY, float* dq_acc, void* dP2, void* dV, float* dlambda,
                           const TcLaunch& tl, cudaStream_t s, bool padded64 = false);
-cudaError_t launch_bwd_tc64(const KernelProblem& kp, const void* P1, const void* P2, const void* V, const float* L,
-                            const float* Dw, const void* dY, float* dq_acc, void* dP2, void* dV, float* dlambda,
+cudaError_t launch_bwd_tc64(const KernelProblem& kp, const void* P1, const void* P2, const void* V,
+                            const float4* qconst, const void* dY, float* dq_acc, void* dP2, void* dV, float* dlambda,
                             const TcLaunch& tl, cudaStream_t s, bool padded64 = false);
 
 }  // namespace relation

@@ -157,6 +157,15 @@ __device__ __forceinline__ void tma_load_operand(void* smem_dst, const CUtensorM
         tma_load_4d(smem_dst, map, bar, x, row, head, batch);
 }
 
+// One bulk copy global -> shared, completion counted on `bar` in bytes (both
+// addresses 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
 // ------------------------------------------------------------------- tcgen05
 // TMEM allocation; executed by one full warp.  Writes the base address to smem.
 __device__ __forceinline__ void tmem_alloc(uint32_t* smem_dst, uint32_t ncols) {

@@ -123,10 +123,15 @@ int dq_width(const relation_problem_t* p) { return p->d_h <= 64 ? 64 : 128; }
 // zero-padded to 64 columns, into the workspace by the preparation stage.
 bool pads_operands(const relation_problem_t* p) { return use_tensor_cores(p) && (p->d_h * 2) % 16 != 0; }
 
-// Workspace: D [rows] fp32 | dP1 accumulator [rows, dq_width] fp32 | (d_h = 60)
-// padded copies of P1, P2, V, dY [rows, 64] bf16; each part 256-byte aligned.
+// Workspace: D [rows] fp32 (CUDA-core path) or the tensor-core kernels' per-query
+// constants [B*H, T rounded up to 128, 2] fp32 | dP1 accumulator [rows, dq_width]
+// fp32 | (d_h = 60) padded copies of P1, P2, V, dY [rows, 64] bf16; each part
+// 256-byte aligned.
 size_t workspace_layout(const relation_problem_t* p, size_t* dq_offset, size_t* pad_offset = nullptr) {
-    const size_t d_bytes = round_up(rows_of(p) * sizeof(float), 256);
+    const size_t d_bytes =
+        use_tensor_cores(p)
+            ? round_up((size_t)p->B * (size_t)p->H * (size_t)qconst_rows(p->T) * 2 * sizeof(float), 256)
+            : round_up(rows_of(p) * sizeof(float), 256);
     const size_t dq_bytes = use_tensor_cores(p) ? round_up(rows_of(p) * (size_t)dq_width(p) * sizeof(float), 256) : 0;
     const size_t pad_bytes = pads_operands(p) ? 4 * round_up(rows_of(p) * 64 * 2, 256) : 0;
     if (dq_offset) *dq_offset = d_bytes;
@@ -210,7 +215,7 @@ relation_status_t run_prepare(const BwdArgs& a, int* launches) {
     if (pads_operands(a.p)) padded_operands(a.p, a.workspace, pad);
     st = from_cuda(launch_bwd_prepare(kp, a.p->dtype == RELATION_BF16, a.P1, a.P2, a.V, a.Y, a.L, a.dY, Dw, dq,
                                       dq_width(a.p), dlam_here, a.stream, pads_operands(a.p) ? pad : nullptr,
-                                      di.num_sms));
+                                      di.num_sms, use_tensor_cores(a.p) ? Dw : nullptr));
     if (st == RELATION_OK) *launches += 1;
     return st;
 }
@@ -219,6 +224,7 @@ relation_status_t run_main(const BwdArgs& a, int* launches) {
     size_t dq_off = 0;
     workspace_layout(a.p, &dq_off);
     const float* Dw = static_cast<const float*>(a.workspace);
+    const float4* qconst = static_cast<const float4*>(a.workspace);  // tensor-core layout of the same region
     const KernelProblem kp = kernel_problem(a.p);
     if (use_tensor_cores(a.p)) {
         DeviceInfo di;
@@ -230,10 +236,10 @@ relation_status_t run_main(const BwdArgs& a, int* launches) {
         if (pads_operands(a.p)) {
             void* pad[4];
             padded_operands(a.p, a.workspace, pad);
-            st = from_cuda(launch_bwd_tc(kp, pad[0], pad[1], pad[2], a.L, Dw, pad[3], dq, a.dP2, a.dV, dlam_main, tl,
+            st = from_cuda(launch_bwd_tc(kp, pad[0], pad[1], pad[2], qconst, pad[3], dq, a.dP2, a.dV, dlam_main, tl,
                                          a.stream, true));
         } else {
-            st = from_cuda(launch_bwd_tc(kp, a.P1, a.P2, a.V, a.L, Dw, a.dY, dq, a.dP2, a.dV, dlam_main, tl,
+            st = from_cuda(launch_bwd_tc(kp, a.P1, a.P2, a.V, qconst, a.dY, dq, a.dP2, a.dV, dlam_main, tl,
                                          a.stream));
         }
         if (st == RELATION_OK) *launches += 1;

@@ -113,6 +113,33 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(KernelProblem kp, co
     }
 }
 
+// Where the preparation stage puts D_t of row (bh, t): D [BH, T] for the
+// CUDA-core backward, or the tensor-core kernels' per-query constants (layout
+// in kernels.h), including the zero rows that pad each head to a multiple of 128.
+struct PrepOut {
+    float* D;       // used when qc == nullptr
+    float* qc;      // per-query constants
+    const float* L; // log-normaliser of the forward [BH, T]
+};
+__device__ __forceinline__ void put_row_result(const KernelProblem& kp, const PrepOut& po, int64_t row, float D) {
+    if (po.qc == nullptr) {
+        po.D[row] = D;
+        return;
+    }
+    constexpr float kLog2e = 1.4426950408889634f;
+    const int64_t bh = row / kp.T;
+    const int t = (int)(row - bh * kp.T);
+    const int count = kp.causal ? (t + 1) : kp.T;
+    const int64_t tp = qconst_rows(kp.T);
+    float* base = po.qc + (size_t)bh * (size_t)tp * 2;
+    base[(t >> 1) * 4 + (t & 1)] = -(po.L[row] + kp.lambda * __logf((float)count)) * kLog2e;
+    base[(t >> 1) * 4 + 2 + (t & 1)] = -D * (0.5f * kp.inv_sqrt_d);
+    for (int64_t u = (int64_t)kp.T + t; u < tp; u += kp.T) {
+        base[(u >> 1) * 4 + (u & 1)] = 0.f;
+        base[(u >> 1) * 4 + 2 + (u & 1)] = 0.f;
+    }
+}
+
 // ------------------------------------------------- backward: D_i and dlambda
 // One warp per row.  D_i = dY_i . Y_i.  dlambda = sum_i log(c_i) dR_ii, which
 // equals -sum_i log(c_i) sum_{j!=i} dR_ij because every row of dR sums to 0.
@@ -124,7 +151,7 @@ __global__ void __launch_bounds__(256) bwd_prepare_kernel(KernelProblem kp, cons
                                                           const Tin* __restrict__ Yf,
                                                           const float* __restrict__ L,
                                                           const Tin* __restrict__ dY,
-                                                          float* __restrict__ Dout, float* __restrict__ dq_acc,
+                                                          PrepOut po, float* __restrict__ dq_acc,
                                                           int dq_w, float* __restrict__ dlambda) {
     __shared__ float s_part[8];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -153,7 +180,7 @@ __global__ void __launch_bounds__(256) bwd_prepare_kernel(KernelProblem kp, cons
             p1p2 += __shfl_xor_sync(0xffffffffu, p1p2, o);
         }
         if (lane == 0) {
-            Dout[row] = dy_y;
+            put_row_result(kp, po, row, dy_y);
             const float u = p1p2 * kp.inv_sqrt_d;
             const float S = sigmoid_exact(u / kp.tau_S);
             const float Fii = expf(S - L[row]);
@@ -178,9 +205,10 @@ __global__ void __launch_bounds__(256) bwd_prepare_kernel(KernelProblem kp, cons
 // threads per row, each owning 16 bytes of dY and Y and D/(D/8)*4 bytes of the
 // accumulator.
 template <int D>
-__global__ void __launch_bounds__(256) bwd_prepare_bf16_kernel(int64_t rows, const uint4* __restrict__ Yv,
-                                                               const uint4* __restrict__ dYv,
-                                                               float* __restrict__ Dout, float4* __restrict__ dq4) {
+__global__ void __launch_bounds__(256) bwd_prepare_bf16_kernel(KernelProblem kp, int64_t rows,
+                                                               const uint4* __restrict__ Yv,
+                                                               const uint4* __restrict__ dYv, PrepOut po,
+                                                               float4* __restrict__ dq4) {
     constexpr int kTpr = D / 8;  // threads per row
     const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t row = t / kTpr;
@@ -201,7 +229,7 @@ __global__ void __launch_bounds__(256) bwd_prepare_bf16_kernel(int64_t rows, con
     }
 #pragma unroll
     for (int o = kTpr / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (row < rows && part == 0) Dout[row] = acc;
+    if (row < rows && part == 0) put_row_result(kp, po, row, acc);
 }
 
 // bf16 rows of width d <= 64 (d % 4 == 0), either layout, dlambda summed
@@ -216,9 +244,8 @@ struct PrepPad {
 };
 __global__ void __launch_bounds__(256) bwd_prepare_narrow_kernel(KernelProblem kp, int64_t rows,
                                                                  const uint2* __restrict__ Y,
-                                                                 const uint2* __restrict__ dY,
-                                                                 float* __restrict__ Dout, float4* __restrict__ dq4,
-                                                                 PrepPad pad) {
+                                                                 const uint2* __restrict__ dY, PrepOut po,
+                                                                 float4* __restrict__ dq4, PrepPad pad) {
     const int u = threadIdx.x & 15;
     const unsigned half = 0xffffu << (threadIdx.x & 16);
     const int units = kp.d >> 2;
@@ -248,7 +275,7 @@ __global__ void __launch_bounds__(256) bwd_prepare_narrow_kernel(KernelProblem k
         }
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(half, acc, o);
-        if (u == 0) Dout[row] = acc;
+        if (u == 0) put_row_result(kp, po, row, acc);
     }
 }
 
@@ -554,8 +581,9 @@ cudaError_t launch_bwd_simt(const KernelProblem& kp, bool bf16, const void* P1, 
 
 cudaError_t launch_bwd_prepare(const KernelProblem& kp, bool bf16, const void* P1, const void* P2, const void* V,
                                const void* Y, const float* L, const void* dY, float* Dw, float* dq_acc, int dq_w,
-                               float* dlambda, cudaStream_t s, void* const* pad_dst, int num_sms) {
+                               float* dlambda, cudaStream_t s, void* const* pad_dst, int num_sms, float* qconst) {
     const int64_t rows = kp.BH * kp.T;
+    const PrepOut po{Dw, qconst, L};
     // Narrow bf16 rows (and the padded copies, when asked for) in one pass.
     const bool narrow = bf16 && dlambda == nullptr && dq_acc != nullptr && dq_w == 64 && kp.d <= 64 &&
                         (kp.d & 3) == 0 && !(kp.layout == 0 && kp.d == 64);
@@ -572,7 +600,7 @@ cudaError_t launch_bwd_prepare(const KernelProblem& kp, bool bf16, const void* P
         const int64_t cap = (int64_t)(num_sms > 0 ? num_sms : 1) * 16;
         if (blocks > cap) blocks = cap;
         if (blocks < 1) blocks = 1;
-        bwd_prepare_narrow_kernel<<<(unsigned)blocks, 256, 0, s>>>(kp, rows, (const uint2*)Y, (const uint2*)dY, Dw,
+        bwd_prepare_narrow_kernel<<<(unsigned)blocks, 256, 0, s>>>(kp, rows, (const uint2*)Y, (const uint2*)dY, po,
                                                                      (float4*)dq_acc, pad);
         return cudaGetLastError();
     }
@@ -582,10 +610,10 @@ cudaError_t launch_bwd_prepare(const KernelProblem& kp, bool bf16, const void* P
         const int64_t threads = rows * (kp.d / 8);
         const unsigned blocks = (unsigned)((threads + 255) / 256);
         if (kp.d == 64)
-            bwd_prepare_bf16_kernel<64><<<blocks, 256, 0, s>>>(rows, (const uint4*)Y, (const uint4*)dY, Dw,
+            bwd_prepare_bf16_kernel<64><<<blocks, 256, 0, s>>>(kp, rows, (const uint4*)Y, (const uint4*)dY, po,
                                                                (float4*)dq_acc);
         else
-            bwd_prepare_bf16_kernel<128><<<blocks, 256, 0, s>>>(rows, (const uint4*)Y, (const uint4*)dY, Dw,
+            bwd_prepare_bf16_kernel<128><<<blocks, 256, 0, s>>>(kp, rows, (const uint4*)Y, (const uint4*)dY, po,
                                                                 (float4*)dq_acc);
         return cudaGetLastError();
     }
@@ -593,10 +621,10 @@ cudaError_t launch_bwd_prepare(const KernelProblem& kp, bool bf16, const void* P
     if (bf16)
         bwd_prepare_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
             kp, (const __nv_bfloat16*)P1, (const __nv_bfloat16*)P2, (const __nv_bfloat16*)V,
-            (const __nv_bfloat16*)Y, L, (const __nv_bfloat16*)dY, Dw, dq_acc, dq_w, dlambda);
+            (const __nv_bfloat16*)Y, L, (const __nv_bfloat16*)dY, po, dq_acc, dq_w, dlambda);
     else
         bwd_prepare_kernel<float><<<blocks, 256, 0, s>>>(kp, (const float*)P1, (const float*)P2, (const float*)V,
-                                                         (const float*)Y, L, (const float*)dY, Dw, dq_acc, dq_w,
+                                                         (const float*)Y, L, (const float*)dY, po, dq_acc, dq_w,
                                                          dlambda);
     return cudaGetLastError();
 }

@@ -63,13 +63,16 @@ def test_unsupported_head_width(lib, d):
 @pytest.mark.parametrize("layout", [rb.RELATION_LAYOUT_BHTD, rb.RELATION_LAYOUT_BTHD])
 @pytest.mark.parametrize("d,acc", [(48, 64), (60, 64), (64, 64), (80, 128), (128, 128)])
 def test_workspace_for_every_width(lib, d, acc, layout):
-    """bf16 workspace: D_i, the fp32 dP1 accumulator padded to the tensor-core tile width and, for
+    """bf16 workspace: the per-query constants of the tensor-core kernels, the fp32 dP1 accumulator
+    padded to the tensor-core tile width and, for
     d_h = 60 (rows TMA cannot step through), zero-padded bf16 copies of P1, P2, V, dY."""
     rows = 2 * 3 * 100
     need = rb.relation_bwd_workspace_bytes(_prob(d_h=d, layout=layout))
     pads = 4 * rows * 64 * 2 if d == 60 else 0
-    assert need >= rows * 4 + rows * acc * 4 + pads
-    assert need <= rows * 4 + rows * acc * 4 + pads + 6 * 256
+    # per-query constants: two floats per query, each head padded to a multiple of 128 queries
+    consts = 2 * 3 * 128 * 2 * 4
+    assert need >= consts + rows * acc * 4 + pads
+    assert need <= consts + rows * acc * 4 + pads + 6 * 256
 
 
 def test_problem_struct_matches_header():
@@ -97,7 +100,7 @@ def test_workspace_size_and_backward_checks(lib):
     p = _prob(B=2, H=3, T=100, d_h=64)
     need = rb.relation_bwd_workspace_bytes(p)
     rows = 2 * 3 * 100
-    assert need >= rows * 4 + rows * 64 * 4  # D_i plus the fp32 dP1 accumulator
+    assert need >= 2 * 3 * 128 * 8 + rows * 64 * 4  # per-query constants plus the fp32 dP1 accumulator
     pf = _prob(B=2, H=3, T=100, d_h=64, dtype=rb.RELATION_F32)
     assert rb.relation_bwd_workspace_bytes(pf) >= rows * 4
     args = [A * k for k in range(1, 11)]  # P1 P2 V Y L dY dP1 dP2 dV dlambda
