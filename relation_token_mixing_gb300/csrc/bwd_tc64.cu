@@ -76,7 +76,6 @@ struct Smem {
     uint64_t s_free[2];  // ... and read by every elementwise warp
     uint64_t p_full;
     uint64_t pv_done;
-    uint64_t ds_free[2];
     uint64_t dq_full;
     uint64_t dq_free;
     uint64_t mma_done[2];  // per MMA issuer: all of its products complete
@@ -134,7 +133,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(&sm.q_full[s], 1);
             ptx::mbar_init(&sm.q_empty[s], 2);  // released by both MMA issuers
         }
-        for (int s = 0; s < 2; ++s) ptx::mbar_init(&sm.ds_free[s], 1);
         for (int h = 0; h < 2; ++h) {
             ptx::mbar_init(&sm.s_full[h], 1);
             ptx::mbar_init(&sm.s_free[h], kElemWarps);
@@ -294,7 +292,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mma_ss_elect(tmem + kColDQ, sm_lo + 128 * ks, hi_m, km_lo + 128 * ks, hi_m, id_dq,
                                       ks > 0 ? 1u : 0u);
                 ptx::mma_commit_elect(&sm.dq_full);
-                ptx::mma_commit_elect(&sm.ds_free[s]);
             }
             ptx::mma_commit_elect(&sm.mma_done[1]);
             ptx::mbar_drain(&sm.mma_done[1], 0, status);
@@ -365,11 +362,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     dlam += elementwise16<true>(sv, gv, qc, col0, r, ec, diag_tile, qlimit, pp, dd);
                 if (h == 0) {
                     // Before the first store: P^T(i-1) must have been read by dV(i-1), and
-                    // dS buffer s by the products of tile i-2 (normally long done).
-                    if ((it > 0 &&
-                         !ptx::mbar_wait_warp(&sm.pv_done, (it - 1) & 1, abort_flag, status, kDevTimeoutMma)) ||
-                        (it >= 2 && !ptx::mbar_wait_warp(&sm.ds_free[s], ((it >> 1) - 1) & 1, abort_flag, status,
-                                                         kDevTimeoutMma))) {
+                    // dS buffer s by the dP2 and dP1 products of tile i-2.  One wait covers
+                    // both: the second MMA warp issues dP2(i-2), dP1(i-2) before dV(i-1), and
+                    // a commit completes only when every earlier product of its thread has.
+                    if (it > 0 &&
+                        !ptx::mbar_wait_warp(&sm.pv_done, (it - 1) & 1, abort_flag, status, kDevTimeoutMma)) {
                         ok = false;
                         break;
                     }
