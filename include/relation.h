@@ -271,6 +271,23 @@ relation_status_t relation_prologue_bwd(const relation_problem_t* p, const void*
                                         float* dtheta, void* stream);
 
 /*
+ * The operator with its input prologue fused into the tensor-core forward's
+ * operand loads (same passages as above): the results of relation_prologue_fwd
+ * followed by relation_fwd, without storing P1, P2 or I_mixed.  The kernel
+ * loads tiles of X1, X2 and of I for the head and its Givens partner; two of its
+ * warps rotate the X1 / X2 tiles (RoPE, rope_base and pos0 as above) and mix the
+ * I tiles in shared memory before the tensor core reads them, each rotated or
+ * mixed value rounded once to bf16 as the standalone prologue rounds it.
+ * X1, X2, I: [B,H,T,d_h] per p->layout.  Y, L as in relation_fwd.  theta,
+ * pairing, rope_base, pos0 as in relation_prologue_fwd.  Supported: dtype
+ * RELATION_BF16, d_h = 64, H even (else RELATION_ERR_UNSUPPORTED or
+ * RELATION_ERR_INVALID_ARGUMENT); one kernel launch.
+ */
+relation_status_t relation_fwd_prologue(const relation_problem_t* p, const void* X1, const void* X2, const void* I,
+                                        const float* theta, int pairing, float rope_base, const int32_t* pos0,
+                                        void* Y, float* L, void* stream);
+
+/*
  * Linear Relation ("Ask Self, Ask Others", Sec. 5.2 eq.(15)-(17); Appendix
  * A.4): per head a d_h x d_h relational state C with C_0 = 0 and channel-wise
  * retention alpha_t = exp(G_t) (Sec. 5.2 eq.(16); the projection producing G

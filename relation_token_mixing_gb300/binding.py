@@ -98,6 +98,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.relation_prologue_bwd.argtypes = [ctypes.POINTER(Problem), _VP, _VP, _VP, _VP, _VP, ctypes.c_int,
                                               ctypes.c_float, _VP, _VP, _VP, _VP, _VP, _VP]
         lib.relation_prologue_bwd.restype = ctypes.c_int
+        lib.relation_fwd_prologue.argtypes = [ctypes.POINTER(Problem), _VP, _VP, _VP, _VP, ctypes.c_int,
+                                              ctypes.c_float, _VP, _VP, _VP, _VP]
+        lib.relation_fwd_prologue.restype = ctypes.c_int
         lib.relation_decode_workspace_bytes.argtypes = [ctypes.POINTER(Problem)]
         lib.relation_decode_workspace_bytes.restype = ctypes.c_size_t
         lib.relation_decode.argtypes = [ctypes.POINTER(Problem), _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_int, _VP, _VP,
@@ -255,6 +258,12 @@ def relation_prologue_bwd(prob, dP1, dP2, dI_mixed, I_mixed, theta, pairing, rop
                                         _ptr(theta), int(pairing), float(rope_base), _ptr(pos0), _ptr(dX1),
                                         _ptr(dX2), _ptr(dI), _ptr(dtheta), _stream_ptr(stream)),
            "relation_prologue_bwd")
+
+
+def relation_fwd_prologue(prob, X1, X2, I, theta, pairing, rope_base, pos0, Y, L=None, stream=None) -> None:
+    _check(load().relation_fwd_prologue(ctypes.byref(prob), _ptr(X1), _ptr(X2), _ptr(I), _ptr(theta), int(pairing),
+                                        float(rope_base), _ptr(pos0), _ptr(Y), _ptr(L), _stream_ptr(stream)),
+           "relation_fwd_prologue")
 
 
 def relation_linear_workspace_bytes(prob: Problem) -> int:

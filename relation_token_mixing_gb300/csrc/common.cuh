@@ -37,6 +37,36 @@ struct KernelProblem {
     int layout;
 };
 
+// RoPE angle: sin and cos of 2 pi pos f_c, with f_c = base^(-2c/d) / (2 pi) given
+// as the float pair (hi, lo): pos * f_c is split into its integer and fractional
+// turns in float-float arithmetic, so large positions keep the angle accurate.
+__device__ __forceinline__ void rope_sincos(float pos, float hi, float lo, float* s, float* c) {
+    const float p_hi = pos * hi;
+    const float p_err = fmaf(pos, hi, -p_hi);  // exact rounding error of the product
+    const float p_lo = fmaf(pos, lo, p_err);
+    const float frac = (p_hi - rintf(p_hi)) + p_lo;
+    sincospif(2.f * frac, s, c);
+}
+
+// Givens mixing of head h's information states with its pair partner (pairing
+// 0: (0,1), (2,3), ...; pairing 1: (1,2), ..., (H-1,0), zero-based heads):
+// I~_h = cs I_h + sn I_partner.  Returns the partner and the pair index k.
+__device__ __forceinline__ int givens_partner(int h, int H, int pairing, int* k, bool* is_first) {
+    if (pairing == 0) {
+        *k = h >> 1;
+        *is_first = (h & 1) == 0;
+        return h ^ 1;
+    }
+    if (h & 1) {  // first of pair (h, h+1 mod H)
+        *k = (h - 1) >> 1;
+        *is_first = true;
+        return (h + 1) % H;
+    }
+    *k = (h == 0 ? H : h) / 2 - 1;  // second of pair (h-1 mod H, h)
+    *is_first = false;
+    return (h == 0 ? H : h) - 1;
+}
+
 // Element offset of row t of head bh (= b*H + h) in an operand tensor.
 __host__ __device__ __forceinline__ size_t row_offset(const KernelProblem& kp, int64_t bh, int64_t t) {
     if (kp.layout == 0) return ((size_t)bh * (size_t)kp.T + (size_t)t) * (size_t)kp.d;

@@ -48,7 +48,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 // denominator share whatever max is used.
 constexpr float kRescaleThreshold = 8.0f * 0.6931471805599453f;
 
-template <int D>
+template <int D, bool kPro = false>
 struct FwdCfg {
     // d = 64 leaves 128 TMEM columns free: P gets its own region per tile, so the
     // next S can be issued while the softmax still works on the current one.
@@ -57,11 +57,14 @@ struct FwdCfg {
     static constexpr uint32_t kColP = 384;
     static constexpr int kPanels = D / 64;
     static constexpr int kTileBytes = kBM * D * 2;
-    static constexpr int kStages = (D == 64) ? 4 : 2;
+    // With the fused prologue each stage also holds the pair partner's information
+    // tile (kVb), and the ring is one stage shorter to make room for it.
+    static constexpr int kStages = (D == 64) ? (kPro ? 3 : 4) : 2;
+    static constexpr int kVb = kPro ? 1 : 0;
     // 1 KB for 1024-byte alignment of the swizzled tiles, the tiles, the
     // barriers, and a 16 KB guard band that keeps any descriptor walk past a
     // tile's end inside the CTA's allocation.
-    static constexpr int kSmemBytes = 1024 + (2 + 2 * kStages) * kTileBytes + 256 + 16384;
+    static constexpr int kSmemBytes = 1024 + (2 + (2 + kVb) * kStages) * kTileBytes + 512 + 16384;
 };
 
 struct FwdBarriers {
@@ -74,6 +77,10 @@ struct FwdBarriers {
     uint64_t p_full[2];
     uint64_t o_done[2];
     uint64_t drain;
+    // Fused prologue: Q / K tiles rotated and V tiles mixed in shared memory.
+    uint64_t q_rot[2];
+    uint64_t k_rot[4];
+    uint64_t v_mix[4];
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -106,27 +113,107 @@ __device__ __forceinline__ float row_dot(const uint8_t* a_tile, const uint8_t* b
     return acc;
 }
 
+// Fused input prologue ("Ask Self, Ask Others: Relation Is All You Need",
+// Sec. 3.1 below eq.(1) and Appendix B.3: RoPE on the relation coordinates;
+// Sec. 3.2 eq.(4) and Appendix A.2.2-A.2.3: Givens mixing of head pairs' states),
+// applied to the 64-column tiles in shared memory after TMA lands them.
+struct ProArgs {
+    RopeTable tab;         // RoPE frequencies (tab.enabled == 0: no rotation)
+    const float* theta;    // Givens angles [H/2]
+    const int32_t* pos0;   // first position of each batch, or NULL
+    int pairing;
+};
+
+// RoPE of one 128-row x 64-column bf16 tile in place (128-byte rows, 16-byte
+// chunk k of row r stored at chunk k ^ (r % 8)): coordinate c < 32 turns with
+// c + 32 by the angle 2 pi f_c (pos_first + r).  Thread tr of 64 takes the four
+// coordinates 4 (tr % 8) .. +3 of rows tr / 8 + 8m: the angle of its first row
+// from rope_sincos, each next row's by turning it through the angle of 8 rows.
+__device__ __forceinline__ void rope_tile64(uint8_t* tile, int tr, float pos_first, const RopeTable& tab) {
+    const int q4 = tr & 7, g = tr >> 3;
+    float cs[4], sn[4], cd[4], sd[4];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        const int c = 4 * q4 + v;
+        rope_sincos(pos_first + (float)g, tab.hi[c], tab.lo[c], &sn[v], &cs[v]);
+        rope_sincos(8.f, tab.hi[c], tab.lo[c], &sd[v], &cd[v]);
+    }
+    const int chunk = q4 >> 1, sub = (q4 & 1) * 8;  // byte offset inside the 16-byte chunk
+#pragma unroll 4
+    for (int m = 0; m < 16; ++m) {
+        const int r = g + 8 * m;
+        uint8_t* row = tile + r * 128;
+        uint2* pa = reinterpret_cast<uint2*>(row + ((chunk ^ (r & 7)) << 4) + sub);
+        uint2* pb = reinterpret_cast<uint2*>(row + (((chunk + 4) ^ (r & 7)) << 4) + sub);
+        const uint2 a = *pa, b = *pb;
+        const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a.x));
+        const float2 a1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a.y));
+        const float2 b0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&b.x));
+        const float2 b1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&b.y));
+        const float av[4] = {a0.x, a0.y, a1.x, a1.y}, bv[4] = {b0.x, b0.y, b1.x, b1.y};
+        float ra[4], rb[4];
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            ra[v] = fmaf(cs[v], av[v], -sn[v] * bv[v]);
+            rb[v] = fmaf(sn[v], av[v], cs[v] * bv[v]);
+            const float c2 = fmaf(cs[v], cd[v], -sn[v] * sd[v]);
+            sn[v] = fmaf(sn[v], cd[v], cs[v] * sd[v]);
+            cs[v] = c2;
+        }
+        *pa = make_uint2(ptx::pack_bf16x2(ra[0], ra[1]), ptx::pack_bf16x2(ra[2], ra[3]));
+        *pb = make_uint2(ptx::pack_bf16x2(rb[0], rb[1]), ptx::pack_bf16x2(rb[2], rb[3]));
+    }
+}
+
+// Givens mixing of one 128 x 64 bf16 tile in place: v <- cs v + sn w, w the pair
+// partner's tile in the same layout (the map is elementwise, so chunks are
+// taken in storage order).  64 threads, 16 chunks of 8 values each.
+__device__ __forceinline__ void mix_tile64(uint8_t* v, const uint8_t* w, int tr, float cs, float sn) {
+#pragma unroll 4
+    for (int m = 0; m < 16; ++m) {
+        uint4* pv = reinterpret_cast<uint4*>(v) + tr + 64 * m;
+        const uint4 a = *pv, b = *(reinterpret_cast<const uint4*>(w) + tr + 64 * m);
+        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&aw[k]));
+            const float2 fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bw[k]));
+            o[k] = ptx::pack_bf16x2(fmaf(cs, fa.x, sn * fb.x), fmaf(cs, fa.y, sn * fb.y));
+        }
+        *pv = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
 // kCp: operand tiles copied by the producer warp with cp.async from the raw
 // pointers (head widths whose rows TMA cannot address; D = 64 only), else TMA.
-template <int D, bool kCp>
+// kPro: the operands are the prologue's inputs X1, X2, I (D = 64, TMA): warps
+// 2-3 rotate the Q and K tiles and mix each V tile with the pair partner's
+// before the tensor core reads them.
+template <int D, bool kCp, bool kPro = false>
 __global__ void __launch_bounds__(kThreads, 1)
     relation_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_p1, const __grid_constant__ CUtensorMap tm_p2,
                            const __grid_constant__ CUtensorMap tm_v, const KernelProblem kp,
                            const __nv_bfloat16* __restrict__ P1, const __nv_bfloat16* __restrict__ P2,
                            const __nv_bfloat16* __restrict__ V, __nv_bfloat16* __restrict__ Y,
-                           float* __restrict__ L, unsigned int* status) {
+                           float* __restrict__ L, unsigned int* status, const ProArgs pro) {
     static_assert(!kCp || D == 64, "cp.async tiles are 64 columns wide");
-    using C = FwdCfg<D>;
+    static_assert(!kPro || (D == 64 && !kCp), "the fused prologue works on 64-column TMA tiles");
+    using C = FwdCfg<D, kPro>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = smem;
     uint8_t* sK = sQ + 2 * C::kTileBytes;
     uint8_t* sV = sK + C::kStages * C::kTileBytes;
-    FwdBarriers* bars = reinterpret_cast<FwdBarriers*>(sV + C::kStages * C::kTileBytes);
+    uint8_t* sVb = sV + C::kStages * C::kTileBytes;  // pair partner's information tiles (kPro)
+    FwdBarriers* bars = reinterpret_cast<FwdBarriers*>(sVb + C::kVb * C::kStages * C::kTileBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bh = blockIdx.x;
     const int batch = bh / kp.H, head = bh - batch * kp.H;
+    int pro_pair = 0, partner = head;
+    bool pro_first = true;
+    if constexpr (kPro) partner = givens_partner(head, kp.H, pro.pairing, &pro_pair, &pro_first);
     const int pair = (int)gridDim.y - 1 - (int)blockIdx.y;  // heaviest (latest) query rows first
     const int T = kp.T;
     const int q_base = pair * 2 * kBM;
@@ -153,6 +240,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(&bars->kv_empty[s], 1);
         }
         ptx::mbar_init(&bars->drain, 1);
+        for (int t = 0; t < 2; ++t) ptx::mbar_init(&bars->q_rot[t], 2);
+        for (int s = 0; s < C::kStages; ++s) {
+            ptx::mbar_init(&bars->k_rot[s], 2);
+            ptx::mbar_init(&bars->v_mix[s], 2);
+        }
         bars->abort_flag = 0;
         ptx::fence_barrier_init();
     }
@@ -228,10 +320,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int p = 0; p < C::kPanels; ++p)
                     ptx::tma_load_4d(sK + s * C::kTileBytes + p * kPanelBytes, &tm_p2, &bars->k_full[s], p * 64,
                                      j * kBN, head, batch);
-                ptx::mbar_arrive_expect_tx(&bars->v_full[s], C::kTileBytes);
+                ptx::mbar_arrive_expect_tx(&bars->v_full[s], (1 + C::kVb) * C::kTileBytes);
                 for (int p = 0; p < C::kPanels; ++p)
                     ptx::tma_load_4d(sV + s * C::kTileBytes + p * kPanelBytes, &tm_v, &bars->v_full[s], p * 64,
                                      j * kBN, head, batch);
+                if constexpr (kPro)
+                    ptx::tma_load_4d(sVb + s * C::kTileBytes, &tm_v, &bars->v_full[s], 0, j * kBN, partner, batch);
             }
             if (*abort_flag) {
                 // Let the copies already issued land before the CTA exits.
@@ -249,6 +343,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The whole warp runs the issue loop; one elected lane issues each MMA.
         ptx::regs_dec<kRegsControl>();
         {
+            // With the fused prologue the tensor core waits for the rotated / mixed tiles.
+            uint64_t* q_ready = kPro ? bars->q_rot : bars->q_full;
+            uint64_t* k_ready = kPro ? bars->k_rot : bars->k_full;
+            uint64_t* v_ready_bar = kPro ? bars->v_mix : bars->v_full;
             const uint32_t id_s = ptx::idesc_bf16(kBM, kBN, false, false);
             const uint32_t id_o = ptx::idesc_bf16(kBM, D, false, true);
             // Descriptors are built once; a byte offset is added as offset >> 4.
@@ -275,8 +373,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             bool ok = true;
             for (int t = 0; t < 2 && ok; ++t)
-                if (n_t[t] > 0) ok = ptx::mbar_wait_warp(&bars->q_full[t], 0, abort_flag, status, kDevTimeoutFull);
-            if (ok && n_max > 0) ok = ptx::mbar_wait_warp(&bars->k_full[0], 0, abort_flag, status, kDevTimeoutFull);
+                if (n_t[t] > 0) ok = ptx::mbar_wait_warp(&q_ready[t], 0, abort_flag, status, kDevTimeoutFull);
+            if (ok && n_max > 0) ok = ptx::mbar_wait_warp(&k_ready[0], 0, abort_flag, status, kDevTimeoutFull);
             if (ok) {
                 ptx::tc_fence_after();
                 for (int t = 0; t < 2; ++t) {
@@ -298,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         if (!k_next_ready) {
-                            if (!ptx::mbar_wait_warp(&bars->k_full[s1], ((j + 1) / C::kStages) & 1, abort_flag, status,
+                            if (!ptx::mbar_wait_warp(&k_ready[s1], ((j + 1) / C::kStages) & 1, abort_flag, status,
                                                 kDevTimeoutFull)) {
                                 ok = false;
                                 break;
@@ -316,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         if (!v_ready) {
-                            if (!ptx::mbar_wait_warp(&bars->v_full[s], (j / C::kStages) & 1, abort_flag, status,
+                            if (!ptx::mbar_wait_warp(&v_ready_bar[s], (j / C::kStages) & 1, abort_flag, status,
                                                 kDevTimeoutFull)) {
                                 ok = false;
                                 break;
@@ -335,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         if (!v_ready) {
-                            if (!ptx::mbar_wait_warp(&bars->v_full[s], (j / C::kStages) & 1, abort_flag, status,
+                            if (!ptx::mbar_wait_warp(&v_ready_bar[s], (j / C::kStages) & 1, abort_flag, status,
                                                 kDevTimeoutFull)) {
                                 ok = false;
                                 break;
@@ -347,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::mma_commit_elect(&bars->o_done[t]);
                         if (j + 1 < n_t[t]) {
                             if (!k_next_ready) {
-                                if (!ptx::mbar_wait_warp(&bars->k_full[s1], ((j + 1) / C::kStages) & 1, abort_flag,
+                                if (!ptx::mbar_wait_warp(&k_ready[s1], ((j + 1) / C::kStages) & 1, abort_flag,
                                                     status, kDevTimeoutFull)) {
                                     ok = false;
                                     break;
@@ -367,6 +465,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp < 4) {
         ptx::regs_dec<kRegsControl>();
+        if constexpr (kPro) {
+            // ------------------------------------------------- fused prologue
+            const int tr = threadIdx.x - 64;
+            float g_sn, g_cs;
+            sincosf(pro.theta[pro_pair], &g_sn, &g_cs);
+            if (pro_first) g_sn = -g_sn;  // first of the pair: cos I_a - sin I_b
+            const float pos_base = pro.pos0 != nullptr ? (float)pro.pos0[batch] : 0.f;
+            bool ok = true;
+            for (int t = 0; t < 2 && ok; ++t) {
+                if (n_t[t] == 0) continue;
+                if (!(ok = ptx::mbar_wait_warp(&bars->q_full[t], 0, abort_flag, status, kDevTimeoutFull))) break;
+                if (pro.tab.enabled) rope_tile64(sQ + t * C::kTileBytes, tr, pos_base + (float)(q_base + t * kBM), pro.tab);
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&bars->q_rot[t]);
+            }
+            for (int j = 0; ok && j < n_max; ++j) {
+                const int s = j % C::kStages;
+                if (!ptx::mbar_wait_warp(&bars->k_full[s], (j / C::kStages) & 1, abort_flag, status, kDevTimeoutFull))
+                    break;
+                if (pro.tab.enabled) rope_tile64(sK + s * C::kTileBytes, tr, pos_base + (float)(j * kBN), pro.tab);
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&bars->k_rot[s]);
+                if (!ptx::mbar_wait_warp(&bars->v_full[s], (j / C::kStages) & 1, abort_flag, status, kDevTimeoutFull))
+                    break;
+                mix_tile64(sV + s * C::kTileBytes, sVb + s * C::kTileBytes, tr, g_cs, g_sn);
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&bars->v_mix[s]);
+            }
+        }
     } else {
         // ------------------------------------------------------------- softmax
         ptx::regs_inc<kRegsSoftmax>();
@@ -537,15 +667,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D, bool kCp>
+template <int D, bool kCp, bool kPro = false>
 cudaError_t launch_fwd_tc_d(const KernelProblem& kp, const void* P1, const void* P2, const void* V, void* Y,
-                            float* L, const TcLaunch& tl, cudaStream_t s, bool padded64 = false) {
-    using C = FwdCfg<D>;
+                            float* L, const TcLaunch& tl, cudaStream_t s, bool padded64 = false,
+                            const ProArgs& pro = ProArgs{}) {
+    using C = FwdCfg<D, kPro>;
+    static_assert(C::kSmemBytes <= 232448, "shared memory budget");
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(relation_fwd_tc_kernel<D, kCp>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        C::kSmemBytes);
+        attr_err = cudaFuncSetAttribute(relation_fwd_tc_kernel<D, kCp, kPro>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     });
     if (attr_err != cudaSuccess) return attr_err;
     // Heads narrower than D read as D-wide tiles whose extra columns are zero.
@@ -563,9 +695,9 @@ cudaError_t launch_fwd_tc_d(const KernelProblem& kp, const void* P1, const void*
     }
     const unsigned pairs = (unsigned)((kp.T + 2 * kBM - 1) / (2 * kBM));
     dim3 grid((unsigned)kp.BH, pairs);
-    relation_fwd_tc_kernel<D, kCp><<<grid, kThreads, C::kSmemBytes, s>>>(
+    relation_fwd_tc_kernel<D, kCp, kPro><<<grid, kThreads, C::kSmemBytes, s>>>(
         m1, m2, mv, kp, (const __nv_bfloat16*)P1, (const __nv_bfloat16*)P2, (const __nv_bfloat16*)V, (__nv_bfloat16*)Y,
-        L, tl.status);
+        L, tl.status, pro);
     return cudaGetLastError();
 }
 
@@ -587,6 +719,18 @@ cudaError_t launch_fwd_tc(const KernelProblem& kp, const void* P1, const void* P
     if (kp.d == 60) return launch_fwd_tc_d<64, true>(kp, P1, P2, V, Y, L, tl, s);  // 120-byte rows: no TMA
     if (kp.d == 80 || kp.d == 128) return launch_fwd_tc_d<128, false>(kp, P1, P2, V, Y, L, tl, s);
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_fwd_tc_prologue(const KernelProblem& kp, const void* X1, const void* X2, const void* I, void* Y,
+                                   float* L, const TcLaunch& tl, cudaStream_t s, const RopeTable& tab,
+                                   const float* theta, const int32_t* pos0, int pairing) {
+    if (kp.BH > 2147483647LL || kp.d != 64 || kp.H % 2 != 0) return cudaErrorInvalidValue;
+    ProArgs pro{};
+    pro.tab = tab;
+    pro.theta = theta;
+    pro.pos0 = pos0;
+    pro.pairing = pairing;
+    return launch_fwd_tc_d<64, false, true>(kp, X1, X2, I, Y, L, tl, s, false, pro);
 }
 
 }  // namespace relation

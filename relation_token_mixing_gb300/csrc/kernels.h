@@ -43,6 +43,13 @@ struct RopeTable {
     float hi[64];
     float lo[64];
 };
+// The tensor-core forward with the input prologue fused into its operand
+// loads (bf16, d_h = 64): X1, X2 are rotated and I mixed with the pair partner's
+// states in shared memory, so P1, P2 and the mixed states are never stored.
+struct TcLaunch;
+cudaError_t launch_fwd_tc_prologue(const KernelProblem& kp, const void* X1, const void* X2, const void* I, void* Y,
+                                   float* L, const TcLaunch& tl, cudaStream_t s, const RopeTable& tab,
+                                   const float* theta, const int32_t* pos0, int pairing);
 // RoPE of two operand tensors (x0 -> y0, x1 -> y1); transpose: the backward.
 cudaError_t launch_rope(const KernelProblem& kp, bool bf16, const void* x0, const void* x1, void* y0, void* y1,
                         const int* pos0, const RopeTable& tab, bool transpose, int num_sms, cudaStream_t s);

@@ -20,17 +20,6 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// sin and cos of 2 pi pos f_c, with f_c = base^(-2c/d) / (2 pi) given as the
-// float pair (hi, lo): pos * f_c is split into its integer and fractional
-// turns in float-float arithmetic, so large positions keep the angle accurate.
-__device__ __forceinline__ void rope_sincos(float pos, float hi, float lo, float* s, float* c) {
-    const float p_hi = pos * hi;
-    const float p_err = fmaf(pos, hi, -p_hi);  // exact rounding error of the product
-    const float p_lo = fmaf(pos, lo, p_err);
-    const float frac = (p_hi - rintf(p_hi)) + p_lo;
-    sincospif(2.f * frac, s, c);
-}
-
 // VC consecutive elements as fp32 (16-, 8- or 4-byte loads for bf16 VC = 8, 4, 2;
 // 16- / 8-byte for fp32).
 template <typename T, int VC>

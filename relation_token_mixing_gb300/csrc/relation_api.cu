@@ -507,6 +507,29 @@ relation_status_t relation_prologue_bwd(const relation_problem_t* p, const void*
     return st;
 }
 
+relation_status_t relation_fwd_prologue(const relation_problem_t* p, const void* X1, const void* X2, const void* I,
+                                        const float* theta, int pairing, float rope_base, const int32_t* pos0,
+                                        void* Y, float* L, void* stream) {
+    const void* in[] = {X1, X2, I};
+    const void* out[] = {Y};
+    relation_status_t st = check_prologue(p, in, 3, out, 1, theta, pairing, rope_base);
+    if (st != RELATION_OK) return st;
+    if (p->dtype != RELATION_BF16 || p->d_h != 64 || !fwd_fits(p)) return RELATION_ERR_UNSUPPORTED;
+    if (L != nullptr) {
+        if (!aligned16(L)) return RELATION_ERR_MISALIGNED;
+        const size_t tb = tensor_bytes(p), lb = rows_of(p) * sizeof(float);
+        for (const void* x : {X1, X2, I, (const void*)Y})
+            if (overlaps(L, lb, x, tb)) return RELATION_ERR_INVALID_ARGUMENT;
+    }
+    DeviceInfo di;
+    if ((st = device_info(&di)) != RELATION_OK) return st;
+    TcLaunch tl{di.num_sms, di.status};
+    st = from_cuda(launch_fwd_tc_prologue(kernel_problem(p), X1, X2, I, Y, L, tl, static_cast<cudaStream_t>(stream),
+                                          rope_table((int)p->d_h, rope_base), theta, pos0, pairing));
+    if (st == RELATION_OK) t_last_launches = 1;
+    return st;
+}
+
 namespace relation {
 namespace {
 relation_status_t check_linear(const relation_problem_t* p) {
