@@ -286,6 +286,26 @@ relation_status_t relation_prologue_bwd(const relation_problem_t* p, const void*
 relation_status_t relation_fwd_prologue(const relation_problem_t* p, const void* X1, const void* X2, const void* I,
                                         const float* theta, int pairing, float rope_base, const int32_t* pos0,
                                         void* Y, float* L, void* stream);
+/*
+ * The matching backward: the results of relation_bwd followed by
+ * relation_prologue_bwd (dX1, dX2, dI, and dtheta when not NULL; dlambda as in
+ * relation_bwd), from X1, X2, I and the forward's Y, L.  The main pass loads X1,
+ * X2, I like the fused forward and rotates / mixes them in shared memory; dX2
+ * leaves it un-rotated, dX1 is un-rotated while the dP1 accumulator is converted,
+ * and a last pass takes the gradient of the mixed states to dI and dtheta (the
+ * mixed states for dtheta recomputed from I).  dX1, dX2, dI: bf16 [B,H,T,d_h]
+ * per p->layout, fully overwritten; dtheta [H/2] float32, overwritten.
+ * workspace: at least relation_bwd_prologue_workspace_bytes(p) bytes (relation_bwd's
+ * workspace followed by a bf16 tensor for the mixed states' gradient), 16-byte
+ * aligned, not overlapping any argument.  Supported as relation_fwd_prologue;
+ * four kernel launches.
+ */
+size_t relation_bwd_prologue_workspace_bytes(const relation_problem_t* p);
+relation_status_t relation_bwd_prologue(const relation_problem_t* p, const void* X1, const void* X2, const void* I,
+                                        const float* theta, int pairing, float rope_base, const int32_t* pos0,
+                                        const void* Y, const float* L, const void* dY, void* dX1, void* dX2, void* dI,
+                                        float* dtheta, float* dlambda, void* workspace, size_t workspace_bytes,
+                                        void* stream);
 
 /*
  * Linear Relation ("Ask Self, Ask Others", Sec. 5.2 eq.(15)-(17); Appendix

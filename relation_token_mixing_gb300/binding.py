@@ -101,6 +101,12 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.relation_fwd_prologue.argtypes = [ctypes.POINTER(Problem), _VP, _VP, _VP, _VP, ctypes.c_int,
                                               ctypes.c_float, _VP, _VP, _VP, _VP]
         lib.relation_fwd_prologue.restype = ctypes.c_int
+        lib.relation_bwd_prologue_workspace_bytes.argtypes = [ctypes.POINTER(Problem)]
+        lib.relation_bwd_prologue_workspace_bytes.restype = ctypes.c_size_t
+        lib.relation_bwd_prologue.argtypes = [ctypes.POINTER(Problem), _VP, _VP, _VP, _VP, ctypes.c_int,
+                                              ctypes.c_float, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                              ctypes.c_size_t, _VP]
+        lib.relation_bwd_prologue.restype = ctypes.c_int
         lib.relation_decode_workspace_bytes.argtypes = [ctypes.POINTER(Problem)]
         lib.relation_decode_workspace_bytes.restype = ctypes.c_size_t
         lib.relation_decode.argtypes = [ctypes.POINTER(Problem), _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_int, _VP, _VP,
@@ -264,6 +270,40 @@ def relation_fwd_prologue(prob, X1, X2, I, theta, pairing, rope_base, pos0, Y, L
     _check(load().relation_fwd_prologue(ctypes.byref(prob), _ptr(X1), _ptr(X2), _ptr(I), _ptr(theta), int(pairing),
                                         float(rope_base), _ptr(pos0), _ptr(Y), _ptr(L), _stream_ptr(stream)),
            "relation_fwd_prologue")
+
+
+def relation_bwd_prologue_workspace_bytes(prob: Problem) -> int:
+    return int(load().relation_bwd_prologue_workspace_bytes(ctypes.byref(prob)))
+
+
+def relation_bwd_prologue(prob, X1, X2, I, theta, pairing, rope_base, pos0, Y, L, dY, dX1, dX2, dI, dtheta, dlambda,
+                          workspace, stream=None) -> None:
+    nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load().relation_bwd_prologue(ctypes.byref(prob), _ptr(X1), _ptr(X2), _ptr(I), _ptr(theta), int(pairing),
+                                        float(rope_base), _ptr(pos0), _ptr(Y), _ptr(L), _ptr(dY), _ptr(dX1),
+                                        _ptr(dX2), _ptr(dI), _ptr(dtheta), _ptr(dlambda), _ptr(workspace), nbytes,
+                                        _stream_ptr(stream)), "relation_bwd_prologue")
+
+
+def fused_prologue_step(X1, X2, I, theta, pairing: int, rope_base: float, tau_S: float, lam: float, dY,
+                        causal: bool = True, pos0=None, layout: int = RELATION_LAYOUT_BHTD, workspace=None,
+                        stream=None):
+    """Forward and backward of the operator with its input prologue fused into the kernels'
+    loads; allocates the outputs (and the workspace unless given) and returns
+    (Y, L, dX1, dX2, dI, dtheta, dlambda)."""
+    prob = problem_for(X1, tau_S, lam, causal, layout)
+    Y = torch.empty_like(I)
+    L = torch.empty((prob.B, prob.H, prob.T), dtype=torch.float32, device=X1.device)
+    relation_fwd_prologue(prob, X1, X2, I, theta, pairing, rope_base, pos0, Y, L, stream)
+    dX1, dX2, dI = torch.empty_like(X1), torch.empty_like(X2), torch.empty_like(I)
+    dtheta = torch.empty(prob.H // 2, dtype=torch.float32, device=X1.device)
+    dlam = torch.empty(1, dtype=torch.float32, device=X1.device)
+    if workspace is None:
+        n = relation_bwd_prologue_workspace_bytes(prob)
+        workspace = torch.empty((n + 3) // 4, dtype=torch.float32, device=X1.device)
+    relation_bwd_prologue(prob, X1, X2, I, theta, pairing, rope_base, pos0, Y, L, dY, dX1, dX2, dI, dtheta, dlam,
+                          workspace, stream)
+    return Y, L, dX1, dX2, dI, dtheta, dlam
 
 
 def relation_linear_workspace_bytes(prob: Problem) -> int:

@@ -34,6 +34,7 @@
 
 #include "bwd_elementwise.cuh"
 #include "kernels.h"
+#include "prologue_tiles.cuh"
 #include "ptx_sm100.cuh"
 #include "tmap.h"
 
@@ -70,6 +71,8 @@ struct Smem {
     // brought in with P1_i and dY_i (written by the preparation stage).
     float4 qconst[kQStages][kTile / 2];
     uint64_t kv_full;
+    uint64_t kv_rot;              // fused prologue: P2_j rotated and V_j mixed
+    uint64_t q_rot[kQStages];     // fused prologue: P1_i rotated
     uint64_t q_full[kQStages];
     uint64_t q_empty[kQStages];
     uint64_t s_full[2];  // S^T / dP^T of query half h (columns 64h..64h+63) computed
@@ -104,14 +107,20 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
 // Operand loads: TMA through 3-D maps ([B, H, T, d] layout and the zero-padded
 // copies of widths whose rows TMA cannot address) or 4-D maps ([B, T, H, d]).
 enum LoadMode { kLoadTma3 = 0, kLoadTma4 = 1 };
-template <int kLoad>
+// kPro: the operands are the prologue's inputs X1, X2, I (d_h = 64): warp 3 rotates
+// the key tile and mixes the V tile with the pair partner's (loaded into the dP1
+// staging panel, which is free until the first dP1 drain); the four dP1-reduce
+// warps rotate each query tile two tiles ahead.  dP2 leaves the epilogue
+// un-rotated (dX2); dV is the gradient of the mixed states, and the dP1
+// accumulator stays in rotated coordinates (both finished by later passes).
+template <int kLoad, bool kPro = false>
 __global__ void __launch_bounds__(kThreads, 1)
     relation_bwd_tc64_kernel(const __grid_constant__ CUtensorMap tm_p1, const __grid_constant__ CUtensorMap tm_p2,
                              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_dy,
                              const __grid_constant__ CUtensorMap tm_dq, const KernelProblem kp,
                              const float4* __restrict__ qconst, __nv_bfloat16* __restrict__ dP2,
                              __nv_bfloat16* __restrict__ dV, float* __restrict__ dlambda, unsigned int* status,
-                             int head_group) {
+                             int head_group, const __grid_constant__ ProArgs pro) {
     constexpr bool kRank3 = kLoad == kLoadTma3;
     extern __shared__ uint8_t smem_raw[];
     Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -126,9 +135,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int i_first = kp.causal ? jt : 0;
     const int n_q = nt_all - i_first;
     const float k_scale = 0.5f * kp.inv_sqrt_d;
+    int partner = head;
+    float g_cs = 1.f, g_sn = 0.f;  // Givens coefficients of this head (fused prologue)
+    if constexpr (kPro) partner = givens_coeffs(head, kp.H, pro, &g_cs, &g_sn);
+    const float pos_base = (kPro && pro.pos0 != nullptr) ? (float)pro.pos0[batch] : 0.f;
 
     if (threadIdx.x == 0) {
         ptx::mbar_init(&sm.kv_full, 1);
+        ptx::mbar_init(&sm.kv_rot, 1);
+        for (int s = 0; s < kQStages; ++s) ptx::mbar_init(&sm.q_rot[s], 4);
         for (int s = 0; s < kQStages; ++s) {
             ptx::mbar_init(&sm.q_full[s], 1);
             ptx::mbar_init(&sm.q_empty[s], 2);  // released by both MMA issuers
@@ -165,9 +180,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tma_prefetch_desc(&tm_v);
             ptx::tma_prefetch_desc(&tm_dy);
             ptx::tma_prefetch_desc(&tm_dq);
-            ptx::mbar_arrive_expect_tx(&sm.kv_full, 2 * kTileBytes);
+            ptx::mbar_arrive_expect_tx(&sm.kv_full, (kPro ? 3 : 2) * kTileBytes);
             ptx::tma_load_operand(sm.k, &tm_p2, &sm.kv_full, 0, kv0, bh, head, batch, kRank3);
             ptx::tma_load_operand(sm.v, &tm_v, &sm.kv_full, 0, kv0, bh, head, batch, kRank3);
+            if constexpr (kPro)  // the Givens partner's states, into the (still unused) dP1 staging panel
+                ptx::tma_load_operand(sm.dq_stage, &tm_v, &sm.kv_full, 0, kv0, bh - head + partner, partner, batch,
+                                      kRank3);
         }
         // Per-query constants of this head, 64 float4 (1 KB) per query tile.
         const float4* qsrc = qconst + (size_t)bh * (size_t)(qconst_rows(T) / 2);
@@ -230,12 +248,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       ks > 0 ? 1u : 0u);
                 ptx::mma_commit_elect(&sm.s_full[h]);
             };
-            ok = ptx::mbar_wait_warp(&sm.kv_full, 0, abort_flag, status, kDevTimeoutFull);
+            ok = ptx::mbar_wait_warp(kPro ? &sm.kv_rot : &sm.kv_full, 0, abort_flag, status, kDevTimeoutFull);
             for (int it = 0; ok && it < n_q; ++it) {
                 // Products of tile it: half h once every elementwise warp holds half h
                 // of tile it-1 (the columns are then free).
                 const int qs = it % kQStages;
-                if (!ptx::mbar_wait_warp(&sm.q_full[qs], (it / kQStages) & 1, abort_flag, status, kDevTimeoutFull))
+                if (!ptx::mbar_wait_warp(kPro ? &sm.q_rot[qs] : &sm.q_full[qs], (it / kQStages) & 1, abort_flag, status,
+                                         kDevTimeoutFull))
                     break;
                 for (int h = 0; ok && h < 2; ++h) {
                     if (it > 0 && !ptx::mbar_wait_warp(&sm.s_free[h], (it - 1) & 1, abort_flag, status,
@@ -298,6 +317,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp < 4) {
         ptx::regs_dec<kRegsControl>();
+        if constexpr (kPro) {
+            // Fused prologue of the key tile: rotate P2_j, mix V_j with the partner's states.
+            if (ptx::mbar_wait_warp(&sm.kv_full, 0, abort_flag, status, kDevTimeoutFull)) {
+                if (pro.tab.enabled) rope_tile64<32>(sm.k, lane, pos_base + (float)kv0, pro.tab);
+                mix_tile64<32>(sm.v, sm.dq_stage, lane, g_cs, g_sn);
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&sm.kv_rot);
+            }
+        }
     } else if (warp < 4 + kElemWarps) {
         // ------------------------------------------------- elementwise blocks
         ptx::regs_inc<kRegsElementwise>();
@@ -406,6 +435,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tmem_ld32(lane_addr + col, ov);
             ptx::tmem_ld_wait();
             ptx::pin_regs(ov);
+            if constexpr (kPro) {
+                if (blk >= 2 && pro.tab.enabled) {
+                    // dX2 = R^T dP2: coordinate c (< 32) of this row pairs with c + 32, the
+                    // other block's column; each block writes its half.
+                    uint32_t ow[32];
+                    ptx::tmem_ld32(lane_addr + kColDK + 32 * (1 - c0), ow);
+                    ptx::tmem_ld_wait();
+                    ptx::pin_regs(ow);
+                    const float pos = pos_base + (float)kv;
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        float sn, cs;
+                        rope_sincos(pos, pro.tab.hi[c], pro.tab.lo[c], &sn, &cs);
+                        const float g1 = as_f(c0 == 0 ? ov[c] : ow[c]), g2 = as_f(c0 == 0 ? ow[c] : ov[c]);
+                        ov[c] = __float_as_uint(c0 == 0 ? fmaf(cs, g1, sn * g2) : fmaf(cs, g2, -sn * g1));
+                    }
+                }
+            }
             if (row_valid) {
                 // Columns past the head width (zero padding of the tiles) are not written.
 #pragma unroll
@@ -425,12 +472,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int rq = quarter * 32 + lane;
         const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
         const bool leader = (warp == 4 + kElemWarps) && lane == 0;
+        // Fused prologue: rotate P1 of query tile it2 once it has landed (a no-op past
+        // the last tile); tiles 0 and 1 first, then tile it + 2 in iteration it.
+        auto rotate_q = [&](int it2) -> bool {
+            if constexpr (kPro) {
+                if (it2 >= n_q) return true;
+                const int s2 = it2 % kQStages;
+                if (!ptx::mbar_wait_warp(&sm.q_full[s2], (it2 / kQStages) & 1, abort_flag, status, kDevTimeoutFull))
+                    return false;
+                if (pro.tab.enabled)
+                    rope_tile64<128>(sm.q[s2], rq, pos_base + (float)((i_first + it2) * kTile), pro.tab);
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&sm.q_rot[s2]);
+            }
+            return true;
+        };
+        bool rot_ok = rotate_q(0) && rotate_q(1);
         for (int it = 0; it < n_q; ++it) {
             const int i = i_first + it;
+            rot_ok = rot_ok && rotate_q(it + 2);
             // The four warps take one decision per tile (a 128-thread vote on named
             // barrier 1): if any warp's bounded wait gave up, all four leave together,
             // so none is left at the bar.sync below waiting for a warp that left.
-            const bool got = ptx::mbar_wait_warp(&sm.dq_full, it & 1, abort_flag, status, kDevTimeoutMma);
+            const bool got = rot_ok && ptx::mbar_wait_warp(&sm.dq_full, it & 1, abort_flag, status, kDevTimeoutMma);
             if (!ptx::bar_vote_all<1, 128>(got)) break;
             ptx::tc_fence_after();
 #pragma unroll
@@ -475,14 +540,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_bwd_tc64(const KernelProblem& kp, const void* P1, const void* P2, const void* V,
-                            const float4* qconst, const void* dY, float* dq_acc, void* dP2, void* dV, float* dlambda,
-                            const TcLaunch& tl, cudaStream_t s, bool padded64) {
+namespace {
+template <bool kPro>
+cudaError_t launch_bwd_tc64_t(const KernelProblem& kp, const void* P1, const void* P2, const void* V,
+                              const float4* qconst, const void* dY, float* dq_acc, void* dP2, void* dV,
+                              float* dlambda, const TcLaunch& tl, cudaStream_t s, bool padded64, const ProArgs& pro) {
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        const void* fns[2] = {(const void*)relation_bwd_tc64_kernel<kLoadTma3>,
-                              (const void*)relation_bwd_tc64_kernel<kLoadTma4>};
+        const void* fns[2] = {(const void*)relation_bwd_tc64_kernel<kLoadTma3, kPro>,
+                              (const void*)relation_bwd_tc64_kernel<kLoadTma4, kPro>};
         for (const void* f : fns)
             if (attr_err == cudaSuccess)
                 attr_err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -523,15 +590,35 @@ cudaError_t launch_bwd_tc64(const KernelProblem& kp, const void* P1, const void*
     group = group < 1 ? 1 : (group > kp.BH ? kp.BH : group);
     dim3 grid((unsigned)ctas);
 #define RELATION_BWD64(M)                                                                                        \
-    relation_bwd_tc64_kernel<M><<<grid, kThreads, kSmemBytes, s>>>(m1, m2, mv, mg, mq, kp, qconst,                 \
-                                                                  (__nv_bfloat16*)dP2, (__nv_bfloat16*)dV, dlambda, \
-                                                                  tl.status, (int)group)
+    relation_bwd_tc64_kernel<M, kPro><<<grid, kThreads, kSmemBytes, s>>>(                                        \
+        m1, m2, mv, mg, mq, kp, qconst, (__nv_bfloat16*)dP2, (__nv_bfloat16*)dV, dlambda, tl.status, (int)group, pro)
     if (mode == kLoadTma3)
         RELATION_BWD64(kLoadTma3);
     else
         RELATION_BWD64(kLoadTma4);
 #undef RELATION_BWD64
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_tc64(const KernelProblem& kp, const void* P1, const void* P2, const void* V,
+                            const float4* qconst, const void* dY, float* dq_acc, void* dP2, void* dV, float* dlambda,
+                            const TcLaunch& tl, cudaStream_t s, bool padded64) {
+    return launch_bwd_tc64_t<false>(kp, P1, P2, V, qconst, dY, dq_acc, dP2, dV, dlambda, tl, s, padded64, ProArgs{});
+}
+
+cudaError_t launch_bwd_tc64_prologue(const KernelProblem& kp, const void* X1, const void* X2, const void* I,
+                                     const float4* qconst, const void* dY, float* dq_acc, void* dX2, void* dImix,
+                                     float* dlambda, const TcLaunch& tl, cudaStream_t s, const RopeTable& tab,
+                                     const float* theta, const int32_t* pos0, int pairing) {
+    if (kp.d != 64 || kp.H % 2 != 0) return cudaErrorInvalidValue;
+    ProArgs pro{};
+    pro.tab = tab;
+    pro.theta = theta;
+    pro.pos0 = pos0;
+    pro.pairing = pairing;
+    return launch_bwd_tc64_t<true>(kp, X1, X2, I, qconst, dY, dq_acc, dX2, dImix, dlambda, tl, s, false, pro);
 }
 
 }  // namespace relation

@@ -27,6 +27,7 @@
 #include <cuda_bf16.h>
 
 #include "kernels.h"
+#include "prologue_tiles.cuh"
 #include "tile_copy.cuh"
 #include "ptx_sm100.cuh"
 #include "tmap.h"
@@ -113,78 +114,6 @@ __device__ __forceinline__ float row_dot(const uint8_t* a_tile, const uint8_t* b
     return acc;
 }
 
-// Fused input prologue ("Ask Self, Ask Others: Relation Is All You Need",
-// Sec. 3.1 below eq.(1) and Appendix B.3: RoPE on the relation coordinates;
-// Sec. 3.2 eq.(4) and Appendix A.2.2-A.2.3: Givens mixing of head pairs' states),
-// applied to the 64-column tiles in shared memory after TMA lands them.
-struct ProArgs {
-    RopeTable tab;         // RoPE frequencies (tab.enabled == 0: no rotation)
-    const float* theta;    // Givens angles [H/2]
-    const int32_t* pos0;   // first position of each batch, or NULL
-    int pairing;
-};
-
-// RoPE of one 128-row x 64-column bf16 tile in place (128-byte rows, 16-byte
-// chunk k of row r stored at chunk k ^ (r % 8)): coordinate c < 32 turns with
-// c + 32 by the angle 2 pi f_c (pos_first + r).  Thread tr of 64 takes the four
-// coordinates 4 (tr % 8) .. +3 of rows tr / 8 + 8m: the angle of its first row
-// from rope_sincos, each next row's by turning it through the angle of 8 rows.
-__device__ __forceinline__ void rope_tile64(uint8_t* tile, int tr, float pos_first, const RopeTable& tab) {
-    const int q4 = tr & 7, g = tr >> 3;
-    float cs[4], sn[4], cd[4], sd[4];
-#pragma unroll
-    for (int v = 0; v < 4; ++v) {
-        const int c = 4 * q4 + v;
-        rope_sincos(pos_first + (float)g, tab.hi[c], tab.lo[c], &sn[v], &cs[v]);
-        rope_sincos(8.f, tab.hi[c], tab.lo[c], &sd[v], &cd[v]);
-    }
-    const int chunk = q4 >> 1, sub = (q4 & 1) * 8;  // byte offset inside the 16-byte chunk
-#pragma unroll 4
-    for (int m = 0; m < 16; ++m) {
-        const int r = g + 8 * m;
-        uint8_t* row = tile + r * 128;
-        uint2* pa = reinterpret_cast<uint2*>(row + ((chunk ^ (r & 7)) << 4) + sub);
-        uint2* pb = reinterpret_cast<uint2*>(row + (((chunk + 4) ^ (r & 7)) << 4) + sub);
-        const uint2 a = *pa, b = *pb;
-        const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a.x));
-        const float2 a1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a.y));
-        const float2 b0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&b.x));
-        const float2 b1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&b.y));
-        const float av[4] = {a0.x, a0.y, a1.x, a1.y}, bv[4] = {b0.x, b0.y, b1.x, b1.y};
-        float ra[4], rb[4];
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-            ra[v] = fmaf(cs[v], av[v], -sn[v] * bv[v]);
-            rb[v] = fmaf(sn[v], av[v], cs[v] * bv[v]);
-            const float c2 = fmaf(cs[v], cd[v], -sn[v] * sd[v]);
-            sn[v] = fmaf(sn[v], cd[v], cs[v] * sd[v]);
-            cs[v] = c2;
-        }
-        *pa = make_uint2(ptx::pack_bf16x2(ra[0], ra[1]), ptx::pack_bf16x2(ra[2], ra[3]));
-        *pb = make_uint2(ptx::pack_bf16x2(rb[0], rb[1]), ptx::pack_bf16x2(rb[2], rb[3]));
-    }
-}
-
-// Givens mixing of one 128 x 64 bf16 tile in place: v <- cs v + sn w, w the pair
-// partner's tile in the same layout (the map is elementwise, so chunks are
-// taken in storage order).  64 threads, 16 chunks of 8 values each.
-__device__ __forceinline__ void mix_tile64(uint8_t* v, const uint8_t* w, int tr, float cs, float sn) {
-#pragma unroll 4
-    for (int m = 0; m < 16; ++m) {
-        uint4* pv = reinterpret_cast<uint4*>(v) + tr + 64 * m;
-        const uint4 a = *pv, b = *(reinterpret_cast<const uint4*>(w) + tr + 64 * m);
-        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
-        uint32_t o[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&aw[k]));
-            const float2 fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bw[k]));
-            o[k] = ptx::pack_bf16x2(fmaf(cs, fa.x, sn * fb.x), fmaf(cs, fa.y, sn * fb.y));
-        }
-        *pv = make_uint4(o[0], o[1], o[2], o[3]);
-    }
-}
-
 // kCp: operand tiles copied by the producer warp with cp.async from the raw
 // pointers (head widths whose rows TMA cannot address; D = 64 only), else TMA.
 // kPro: the operands are the prologue's inputs X1, X2, I (D = 64, TMA): warps
@@ -196,7 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                            const __grid_constant__ CUtensorMap tm_v, const KernelProblem kp,
                            const __nv_bfloat16* __restrict__ P1, const __nv_bfloat16* __restrict__ P2,
                            const __nv_bfloat16* __restrict__ V, __nv_bfloat16* __restrict__ Y,
-                           float* __restrict__ L, unsigned int* status, const ProArgs pro) {
+                           float* __restrict__ L, unsigned int* status, const __grid_constant__ ProArgs pro) {
     static_assert(!kCp || D == 64, "cp.async tiles are 64 columns wide");
     static_assert(!kPro || (D == 64 && !kCp), "the fused prologue works on 64-column TMA tiles");
     using C = FwdCfg<D, kPro>;
@@ -211,9 +140,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bh = blockIdx.x;
     const int batch = bh / kp.H, head = bh - batch * kp.H;
-    int pro_pair = 0, partner = head;
-    bool pro_first = true;
-    if constexpr (kPro) partner = givens_partner(head, kp.H, pro.pairing, &pro_pair, &pro_first);
+    int partner = head;
+    float g_cs = 1.f, g_sn = 0.f;  // Givens coefficients of this head (fused prologue)
+    if constexpr (kPro) partner = givens_coeffs(head, kp.H, pro, &g_cs, &g_sn);
     const int pair = (int)gridDim.y - 1 - (int)blockIdx.y;  // heaviest (latest) query rows first
     const int T = kp.T;
     const int q_base = pair * 2 * kBM;
@@ -468,15 +397,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (kPro) {
             // ------------------------------------------------- fused prologue
             const int tr = threadIdx.x - 64;
-            float g_sn, g_cs;
-            sincosf(pro.theta[pro_pair], &g_sn, &g_cs);
-            if (pro_first) g_sn = -g_sn;  // first of the pair: cos I_a - sin I_b
             const float pos_base = pro.pos0 != nullptr ? (float)pro.pos0[batch] : 0.f;
             bool ok = true;
             for (int t = 0; t < 2 && ok; ++t) {
                 if (n_t[t] == 0) continue;
                 if (!(ok = ptx::mbar_wait_warp(&bars->q_full[t], 0, abort_flag, status, kDevTimeoutFull))) break;
-                if (pro.tab.enabled) rope_tile64(sQ + t * C::kTileBytes, tr, pos_base + (float)(q_base + t * kBM), pro.tab);
+                if (pro.tab.enabled) rope_tile64<64>(sQ + t * C::kTileBytes, tr, pos_base + (float)(q_base + t * kBM), pro.tab);
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(&bars->q_rot[t]);
@@ -485,13 +411,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int s = j % C::kStages;
                 if (!ptx::mbar_wait_warp(&bars->k_full[s], (j / C::kStages) & 1, abort_flag, status, kDevTimeoutFull))
                     break;
-                if (pro.tab.enabled) rope_tile64(sK + s * C::kTileBytes, tr, pos_base + (float)(j * kBN), pro.tab);
+                if (pro.tab.enabled) rope_tile64<64>(sK + s * C::kTileBytes, tr, pos_base + (float)(j * kBN), pro.tab);
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(&bars->k_rot[s]);
                 if (!ptx::mbar_wait_warp(&bars->v_full[s], (j / C::kStages) & 1, abort_flag, status, kDevTimeoutFull))
                     break;
-                mix_tile64(sV + s * C::kTileBytes, sVb + s * C::kTileBytes, tr, g_cs, g_sn);
+                mix_tile64<64>(sV + s * C::kTileBytes, sVb + s * C::kTileBytes, tr, g_cs, g_sn);
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(&bars->v_mix[s]);

@@ -50,14 +50,26 @@ struct TcLaunch;
 cudaError_t launch_fwd_tc_prologue(const KernelProblem& kp, const void* X1, const void* X2, const void* I, void* Y,
                                    float* L, const TcLaunch& tl, cudaStream_t s, const RopeTable& tab,
                                    const float* theta, const int32_t* pos0, int pairing);
+// The d_h = 64 tensor-core backward main pass with the prologue fused into its
+// loads: dX2 (un-rotated) and the gradient of the mixed states dImix (bf16, the
+// problem's layout); the dP1 accumulator holds dP1 in rotated coordinates.
+cudaError_t launch_bwd_tc64_prologue(const KernelProblem& kp, const void* X1, const void* X2, const void* I,
+                                     const float4* qconst, const void* dY, float* dq_acc, void* dX2, void* dImix,
+                                     float* dlambda, const TcLaunch& tl, cudaStream_t s, const RopeTable& tab,
+                                     const float* theta, const int32_t* pos0, int pairing);
+// dX1 = R^T dP1 from the fp32 dP1 accumulator [BH, T, 64] (d_h = 64, bf16 out, the
+// problem's layout).
+cudaError_t launch_rope_convert(const KernelProblem& kp, const float* dq_acc, void* dX1, const int32_t* pos0,
+                                const RopeTable& tab, int num_sms, cudaStream_t s);
 // RoPE of two operand tensors (x0 -> y0, x1 -> y1); transpose: the backward.
 cudaError_t launch_rope(const KernelProblem& kp, bool bf16, const void* x0, const void* x1, void* y0, void* y1,
                         const int* pos0, const RopeTable& tab, bool transpose, int num_sms, cudaStream_t s);
 // Givens head-pair mixing x -> y; transpose: the backward, with d theta (+=)
-// accumulated from the mixed states Im when dtheta is not NULL.
+// accumulated from the mixed states Im when dtheta is not NULL (im_unmixed: Im
+// holds the unmixed states, mixed in the kernel).
 cudaError_t launch_givens(const KernelProblem& kp, bool bf16, const void* x, const void* Im, void* y,
                           const float* theta, int pairing, bool transpose, float* dtheta, int num_sms,
-                          cudaStream_t s);
+                          cudaStream_t s, bool im_unmixed = false);
 // Relation Cache decode: kp.T is the cache capacity (rows per head of the caches,
 // stored in kp.layout); part holds decode_chunks(kp, bf16) x (d + 2) floats per head.
 int decode_chunks(const KernelProblem& kp, bool bf16);

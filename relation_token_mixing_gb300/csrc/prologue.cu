@@ -133,7 +133,8 @@ __global__ void __launch_bounds__(kThreads) rope_kernel(KernelProblem kp, const 
 }
 
 // Givens mixing of the information states, forward (I -> I~) or backward
-// (dI~ -> dI, plus d theta from the mixed states Im = I~ when dtheta != NULL).
+// (dI~ -> dI, plus d theta from the mixed states Im = I~ when dtheta != NULL;
+// im_unmixed: Im holds the unmixed states I, mixed here for the d theta products).
 // A group of LPR lanes takes one (batch, token, head pair), VC columns per lane
 // (LPR * VC >= d), so a warp covers 32 / LPR pairs per step with 16-byte
 // accesses where the rows allow them.
@@ -141,7 +142,7 @@ template <typename T, int VC, int LPR, typename Idx>
 __global__ void __launch_bounds__(kThreads) givens_kernel(KernelProblem kp, const T* __restrict__ x,
                                                           const T* __restrict__ Im, T* __restrict__ y,
                                                           const float* __restrict__ theta, int pairing, float sign,
-                                                          float* __restrict__ dtheta, Idx rows) {
+                                                          float* __restrict__ dtheta, Idx rows, bool im_unmixed) {
     constexpr int kRowsPerWarp = 32 / LPR;
     extern __shared__ float sh[];  // cos, sin, partial d theta: 3 x H/2
     const int P = kp.H / 2;
@@ -194,6 +195,14 @@ __global__ void __launch_bounds__(kThreads) givens_kernel(KernelProblem kp, cons
                     float ma[VC], mb[VC];
                     loadv<T, VC>(Im + oa, ma);
                     loadv<T, VC>(Im + ob, mb);
+                    if (im_unmixed) {  // sn = -sin here: I~a = cos Ia - sin Ib, I~b = sin Ia + cos Ib
+#pragma unroll
+                        for (int v = 0; v < VC; ++v) {
+                            const float ta = fmaf(cs, ma[v], sn * mb[v]), tb = fmaf(cs, mb[v], -sn * ma[v]);
+                            ma[v] = ta;
+                            mb[v] = tb;
+                        }
+                    }
 #pragma unroll
                     for (int v = 0; v < VC; ++v) part += q[v] * ma[v] - a[v] * mb[v];
                 }
@@ -209,6 +218,37 @@ __global__ void __launch_bounds__(kThreads) givens_kernel(KernelProblem kp, cons
     __syncthreads();
     for (int k = threadIdx.x; k < P; k += blockDim.x)
         if (acc[k] != 0.f) atomicAdd(&dtheta[k], acc[k]);
+}
+
+// dX1 = R^T dP1 from the fp32 dP1 accumulator [BH, T, 64] (rotated coordinates)
+// to bf16 in the problem's layout (d_h = 64): one thread per (row, four
+// coordinate pairs c, c + 32).
+__global__ void __launch_bounds__(kThreads) rope_convert_kernel(KernelProblem kp, const float* __restrict__ dq,
+                                                                __nv_bfloat16* __restrict__ dst,
+                                                                const int* __restrict__ pos0, RopeTable tab,
+                                                                int64_t units) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < units; k += stride) {
+        const int64_t row = k >> 3;
+        const int c = 4 * (int)(k & 7);
+        const int64_t bh = row / kp.T;
+        const int t = (int)(row - bh * kp.T);
+        const float4 g1 = *reinterpret_cast<const float4*>(dq + (size_t)row * 64 + c);
+        const float4 g2 = *reinterpret_cast<const float4*>(dq + (size_t)row * 64 + 32 + c);
+        const float a[4] = {g1.x, g1.y, g1.z, g1.w}, b[4] = {g2.x, g2.y, g2.z, g2.w};
+        float o1[4], o2[4];
+        const float pos = (float)((pos0 != nullptr ? pos0[bh / kp.H] : 0) + t);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            float sn = 0.f, cs = 1.f;
+            if (tab.enabled) rope_sincos(pos, tab.hi[c + v], tab.lo[c + v], &sn, &cs);
+            o1[v] = fmaf(cs, a[v], sn * b[v]);
+            o2[v] = fmaf(cs, b[v], -sn * a[v]);
+        }
+        __nv_bfloat16* o = dst + row_offset(kp, bh, t);
+        storev<__nv_bfloat16, 4>(o + c, o1);
+        storev<__nv_bfloat16, 4>(o + 32 + c, o2);
+    }
 }
 
 int64_t blocks_for(int64_t units, int num_sms) {
@@ -234,16 +274,16 @@ cudaError_t launch_rope_t(const KernelProblem& kp, const void* x0, const void* x
 
 template <typename T, int VC, int LPR>
 cudaError_t launch_givens_t(const KernelProblem& kp, const void* x, const void* Im, void* y, const float* theta,
-                            int pairing, float sign, float* dtheta, int num_sms, cudaStream_t s) {
+                            int pairing, float sign, float* dtheta, int num_sms, cudaStream_t s, bool im_unmixed) {
     const int64_t rows = (kp.BH / 2) * (int64_t)kp.T;  // (batch, token, head pair)
     const size_t smem = sizeof(float) * 3 * (size_t)(kp.H / 2);
     const unsigned blocks = (unsigned)blocks_for(rows * LPR, num_sms);
     if (rows + (int64_t)blocks * kThreads < (int64_t)UINT32_MAX)
         givens_kernel<T, VC, LPR, uint32_t><<<blocks, kThreads, smem, s>>>(
-            kp, (const T*)x, (const T*)Im, (T*)y, theta, pairing, sign, dtheta, (uint32_t)rows);
+            kp, (const T*)x, (const T*)Im, (T*)y, theta, pairing, sign, dtheta, (uint32_t)rows, im_unmixed);
     else
         givens_kernel<T, VC, LPR, uint64_t><<<blocks, kThreads, smem, s>>>(
-            kp, (const T*)x, (const T*)Im, (T*)y, theta, pairing, sign, dtheta, (uint64_t)rows);
+            kp, (const T*)x, (const T*)Im, (T*)y, theta, pairing, sign, dtheta, (uint64_t)rows, im_unmixed);
     return cudaGetLastError();
 }
 
@@ -266,7 +306,7 @@ cudaError_t launch_rope(const KernelProblem& kp, bool bf16, const void* x0, cons
 
 cudaError_t launch_givens(const KernelProblem& kp, bool bf16, const void* x, const void* Im, void* y,
                           const float* theta, int pairing, bool transpose, float* dtheta, int num_sms,
-                          cudaStream_t s) {
+                          cudaStream_t s, bool im_unmixed) {
     const float sign = transpose ? -1.f : 1.f;
     // Widest access the row pitch allows (16 bytes when d * elem is a multiple of 16),
     // and the fewest lanes (a power of two) that cover a row with it.
@@ -275,7 +315,7 @@ cudaError_t launch_givens(const KernelProblem& kp, bool bf16, const void* x, con
     int lpr = 1;
     while (lpr * vc < kp.d) lpr <<= 1;
 #define RELATION_GIVENS(T_, VC_, LPR_) \
-    return launch_givens_t<T_, VC_, LPR_>(kp, x, Im, y, theta, pairing, sign, dtheta, num_sms, s)
+    return launch_givens_t<T_, VC_, LPR_>(kp, x, Im, y, theta, pairing, sign, dtheta, num_sms, s, im_unmixed)
     if (bf16) {
         if (vc == 8) {
             if (lpr <= 8) RELATION_GIVENS(__nv_bfloat16, 8, 8);
@@ -293,6 +333,15 @@ cudaError_t launch_givens(const KernelProblem& kp, bool bf16, const void* x, con
     }
     RELATION_GIVENS(float, 2, 32);
 #undef RELATION_GIVENS
+}
+
+cudaError_t launch_rope_convert(const KernelProblem& kp, const float* dq_acc, void* dX1, const int32_t* pos0,
+                                const RopeTable& tab, int num_sms, cudaStream_t s) {
+    if (kp.d != 64) return cudaErrorInvalidValue;
+    const int64_t units = kp.BH * (int64_t)kp.T * 8;
+    rope_convert_kernel<<<(unsigned)blocks_for(units, num_sms), kThreads, 0, s>>>(
+        kp, dq_acc, static_cast<__nv_bfloat16*>(dX1), pos0, tab, units);
+    return cudaGetLastError();
 }
 
 }  // namespace relation

@@ -530,6 +530,68 @@ relation_status_t relation_fwd_prologue(const relation_problem_t* p, const void*
     return st;
 }
 
+size_t relation_bwd_prologue_workspace_bytes(const relation_problem_t* p) {
+    if (check_problem(p) != RELATION_OK || p->dtype != RELATION_BF16 || p->d_h != 64 || p->H % 2 != 0) return 0;
+    // relation_bwd's workspace, then the gradient of the mixed states (bf16, the problem's layout).
+    return round_up(workspace_layout(p, nullptr), 256) + round_up(tensor_bytes(p), 256);
+}
+
+relation_status_t relation_bwd_prologue(const relation_problem_t* p, const void* X1, const void* X2, const void* I,
+                                        const float* theta, int pairing, float rope_base, const int32_t* pos0,
+                                        const void* Y, const float* L, const void* dY, void* dX1, void* dX2, void* dI,
+                                        float* dtheta, float* dlambda, void* workspace, size_t workspace_bytes,
+                                        void* stream) {
+    const void* in[] = {X1, X2, I, Y, dY};
+    const void* out[] = {dX1, dX2, dI};
+    relation_status_t st = check_prologue(p, in, 5, out, 3, theta, pairing, rope_base);
+    if (st != RELATION_OK) return st;
+    if (p->dtype != RELATION_BF16 || p->d_h != 64) return RELATION_ERR_UNSUPPORTED;
+    if (L == nullptr || workspace == nullptr) return RELATION_ERR_INVALID_ARGUMENT;
+    if (!aligned16(L) || !aligned16(workspace) || (dtheta && (reinterpret_cast<uintptr_t>(dtheta) & 3u)) ||
+        (dlambda && (reinterpret_cast<uintptr_t>(dlambda) & 3u)))
+        return RELATION_ERR_MISALIGNED;
+    const size_t need = relation_bwd_prologue_workspace_bytes(p);
+    if (workspace_bytes < need) return RELATION_ERR_WORKSPACE_TOO_SMALL;
+    const size_t tb = tensor_bytes(p), lb = rows_of(p) * sizeof(float);
+    for (const void* x : {X1, X2, I, Y, dY, (const void*)L, (const void*)dX1, (const void*)dX2, (const void*)dI})
+        if (overlaps(workspace, need, x, x == (const void*)L ? lb : tb)) return RELATION_ERR_INVALID_ARGUMENT;
+    for (const void* o : {(const void*)dX1, (const void*)dX2, (const void*)dI})
+        if (overlaps(L, lb, o, tb)) return RELATION_ERR_INVALID_ARGUMENT;
+    const size_t small = sizeof(float) * (size_t)(p->H / 2);
+    for (const void* o : {(const void*)dtheta, (const void*)dlambda}) {
+        if (o == nullptr) continue;
+        for (const void* x : {X1, X2, I, Y, dY, (const void*)dX1, (const void*)dX2, (const void*)dI})
+            if (overlaps(o, small, x, tb)) return RELATION_ERR_INVALID_ARGUMENT;
+        if (overlaps(o, small, workspace, need) || overlaps(o, small, L, lb)) return RELATION_ERR_INVALID_ARGUMENT;
+    }
+    if (dtheta != nullptr && dlambda != nullptr && overlaps(dtheta, small, dlambda, sizeof(float)))
+        return RELATION_ERR_INVALID_ARGUMENT;
+    DeviceInfo di;
+    if ((st = device_info(&di)) != RELATION_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const KernelProblem kp = kernel_problem(p);
+    const RopeTable tab = rope_table((int)p->d_h, rope_base);
+    void* dImix = static_cast<char*>(workspace) + round_up(workspace_layout(p, nullptr), 256);
+    size_t dq_off = 0;
+    workspace_layout(p, &dq_off);
+    float* dq = reinterpret_cast<float*>(static_cast<char*>(workspace) + dq_off);
+    // Preparation as in relation_bwd (per-query constants from Y, dY, L; the dP1
+    // accumulator reset; dlambda zeroed): it reads none of X1, X2, I.
+    BwdArgs a{p, X1, X2, I, Y, L, dY, dX1, dX2, dImix, dlambda, workspace, workspace_bytes, s};
+    int launches = 0;
+    if ((st = run_prepare(a, &launches)) != RELATION_OK) return st;
+    TcLaunch tl{di.num_sms, di.status};
+    st = from_cuda(launch_bwd_tc64_prologue(kp, X1, X2, I, static_cast<const float4*>(workspace), dY, dq, dX2, dImix,
+                                            dlambda, tl, s, tab, theta, pos0, pairing));
+    if (st != RELATION_OK) return st;
+    st = from_cuda(launch_rope_convert(kp, dq, dX1, pos0, tab, di.num_sms, s));
+    if (st != RELATION_OK) return st;
+    if (dtheta != nullptr && cudaMemsetAsync(dtheta, 0, small, s) != cudaSuccess) return RELATION_ERR_CUDA;
+    st = from_cuda(launch_givens(kp, true, dImix, I, dI, theta, pairing, true, dtheta, di.num_sms, s, true));
+    if (st == RELATION_OK) t_last_launches = launches + 3;
+    return st;
+}
+
 namespace relation {
 namespace {
 relation_status_t check_linear(const relation_problem_t* p) {

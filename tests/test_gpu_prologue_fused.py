@@ -124,3 +124,65 @@ def test_fused_forward_rejects_unsupported_problems():
     with pytest.raises(rb.RelationError) as e:
         rb.relation_fwd_prologue(prob, dev["P1"], dev["P2"], dev["V"], th, 0, 1e4, None, Y)
     assert e.value.code == 2  # d_h 48: unsupported by the fused kernel
+
+
+BWD_CASES = [
+    # name, B, H, T, pairing, layout, pos0, causal, tau
+    ("A_bhtd", 2, 4, 300, 0, BHTD, None, True, 2.0),
+    ("B_bthd_pos0", 1, 6, 259, 1, BTHD, [1000], True, 1.0),
+    ("B_bhtd_noncausal", 1, 4, 200, 1, BHTD, [5], False, 1.0),
+]
+
+
+@pytest.mark.parametrize("name,B,H,T,pairing,layout,pos0,causal,tau", BWD_CASES, ids=[c[0] for c in BWD_CASES])
+def test_fused_backward_matches_composed_oracles(name, B, H, T, pairing, layout, pos0, causal, tau):
+    """relation_fwd_prologue + relation_bwd_prologue against the composed float64 oracles
+    (prologue outputs rounded to bf16, operator backward, prologue backward): dX1, dX2, dI at
+    the operator's bf16 gradient tolerance 2e-2 * max|g|, d theta and d lambda likewise."""
+    lam, base, d = 0.5, 1e4, 64
+    w = rin.Workload("fusedb", B, H, T, d, torch.bfloat16, tau, lam, causal, 1.0, backward=True)
+    x = rin.make(w)
+    g = torch.Generator().manual_seed(12)
+    theta = (torch.rand(H // 2, generator=g, dtype=torch.float64) * 6.0 - 3.0).float()
+    dev = {k: _to(v, layout).cuda() for k, v in x.items()}
+    th = theta.cuda()
+    p0 = torch.tensor(pos0, dtype=torch.int32).cuda() if pos0 is not None else None
+    Y, L, dX1, dX2, dI, dth, dlam = rb.fused_prologue_step(dev["P1"], dev["P2"], dev["V"], th, pairing, base, tau, lam,
+                                                           dev["dY"], causal, p0, layout)
+    assert rb.relation_last_launch_count() == 4
+    torch.cuda.synchronize()
+    assert rb.relation_check_device_status() == 0
+
+    xs = {k: _np(v) for k, v in x.items()}
+    rP1, rP2 = _bf16(po.rope(xs["P1"], base, pos0)), _bf16(po.rope(xs["P2"], base, pos0))
+    rIt = _bf16(po.givens(xs["V"], theta.double().numpy(), pairing))
+    gP1, gP2, gV, rdlam = oracle.bwd(rP1, rP2, rIt, xs["dY"], tau, lam, causal)
+    rdX1, rdX2 = po.rope_bwd(gP1, base, pos0), po.rope_bwd(gP2, base, pos0)
+    rdI, rdth = po.givens_bwd(gV, rIt, theta.double().numpy(), pairing)
+    for got, ref in ((dX1, rdX1), (dX2, rdX2), (dI, rdI)):
+        assert _err(_np(_back(got, layout)), ref) <= 2e-2 * float(np.max(np.abs(ref)))
+    assert _err(dth.cpu().numpy(), rdth) <= 2e-2 * max(1.0, float(np.max(np.abs(rdth))))
+    assert abs(float(dlam.item()) - float(rdlam)) <= 2e-2 * max(1.0, abs(float(rdlam)))
+
+
+def test_fused_backward_matches_the_two_call_chain():
+    """Against the standalone chain on the GPU (prologue, operator forward and backward,
+    prologue backward) at the headline head width and a ragged length."""
+    B, H, T, tau, lam, base, pairing = 1, 4, 333, 0.5, 0.5, 1e4, 0
+    w = rin.Workload("chainb", B, H, T, 64, torch.bfloat16, tau, lam, True, 1.0, backward=True)
+    dev = {k: v.cuda() for k, v in rin.make(w).items()}
+    prob = rb.problem_for(dev["P1"], tau, lam, True)
+    th = torch.tensor([0.7, -0.4], device="cuda")
+    Y, L, dX1, dX2, dI, dth, dlam = rb.fused_prologue_step(dev["P1"], dev["P2"], dev["V"], th, pairing, base, tau, lam,
+                                                           dev["dY"])
+    P1, P2, It = (torch.empty_like(dev["P1"]) for _ in range(3))
+    rb.relation_prologue_fwd(prob, dev["P1"], dev["P2"], dev["V"], th, pairing, base, None, P1, P2, It)
+    Yc, Lc = rb.fwd(P1, P2, It, tau, lam, True)
+    gP1, gP2, gV, dlc = rb.bwd(P1, P2, It, Yc, Lc, dev["dY"], tau, lam, True)
+    cX1, cX2, cI = (torch.empty_like(gP1) for _ in range(3))
+    cth = torch.empty(H // 2, device="cuda")
+    rb.relation_prologue_bwd(prob, gP1, gP2, gV, It, th, pairing, base, None, cX1, cX2, cI, cth)
+    torch.cuda.synchronize()
+    for a, b in ((dX1, cX1), (dX2, cX2), (dI, cI)):
+        assert float((a.float() - b.float()).abs().max()) <= 1e-2 * float(b.float().abs().max())
+    assert float((dth - cth).abs().max()) <= 1e-2 * max(1.0, float(cth.abs().max()))
