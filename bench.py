@@ -59,6 +59,9 @@ def parse():
                     help="time one Relation Cache decode step (full caches of the workload's T) instead")
     ap.add_argument("--prologue", action="store_true",
                     help="time the input prologue (RoPE + Givens) forward and backward of the workload instead")
+    ap.add_argument("--prologue-fused", action="store_true",
+                    help="time the operator step with the input prologue fused into its kernels' loads, beside "
+                         "the plain operator step and the two-call chain (prologue passes + operator)")
     ap.add_argument("--linear", action="store_true",
                     help="time Linear Relation forward + backward (workload from the linear set, default "
                          "linear_d60_T2048) instead")
@@ -352,6 +355,88 @@ def run_prologue(args, w):
         "roofline": {"kernel": "rope_kernel + givens_kernel", "bound": "hbm", "achieved": gbs, "peak": hbm[0],
                      "unit": "GB/s", "frac": gbs / hbm[0], "peak_source": hbm[1], "traffic": None},
         "gpu_launches": 4 * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_prologue_fused(args, w):
+    """One step = relation_fwd_prologue + relation_bwd_prologue (X1 = P1, X2 = P2, I = V of the
+    workload; RoPE base 1e4, pairing B, theta = linspace(-1, 1, H/2)).  Timed beside the plain
+    operator step (relation_fwd + relation_bwd on the same tensors) and the two-call chain
+    (relation_prologue_fwd, the operator step, relation_prologue_bwd), each with the L2 flushed
+    before every step.  value = the operator's algorithmic TFLOP/s over the fused step."""
+    import torch
+
+    from relation_token_mixing_gb300 import binding as rb
+    from relation_token_mixing_gb300 import inputs as rin
+
+    rb.load()
+    dev = torch.device("cuda", 0)
+    x = {k: v.to(dev) for k, v in rin.make(w, with_dy=True).items()}
+    prob = rb.problem_for(x["P1"], w.tau_S, w.lam, w.causal)
+    theta = torch.linspace(-1.0, 1.0, w.H // 2, device=dev)
+    Y = torch.empty_like(x["V"])
+    L = torch.empty((w.B, w.H, w.T), dtype=torch.float32, device=dev)
+    g = [torch.empty_like(x["P1"]) for _ in range(3)]
+    dth = torch.empty(w.H // 2, device=dev)
+    dlam = torch.empty(1, device=dev)
+    wsp = torch.empty((rb.relation_bwd_prologue_workspace_bytes(prob) + 3) // 4, dtype=torch.float32, device=dev)
+    ws = torch.empty((rb.relation_bwd_workspace_bytes(prob) + 3) // 4, dtype=torch.float32, device=dev)
+    pro = [torch.empty_like(x["P1"]) for _ in range(3)]
+    flush = L2Flush(dev)
+
+    def fused():
+        rb.relation_fwd_prologue(prob, x["P1"], x["P2"], x["V"], theta, PROLOGUE_PAIRING, PROLOGUE_BASE, None, Y, L)
+        rb.relation_bwd_prologue(prob, x["P1"], x["P2"], x["V"], theta, PROLOGUE_PAIRING, PROLOGUE_BASE, None, Y, L,
+                                 x["dY"], *g, dth, dlam, wsp)
+
+    def operator(P1, P2, V):
+        rb.relation_fwd(prob, P1, P2, V, Y, L)
+        rb.relation_bwd(prob, P1, P2, V, Y, L, x["dY"], *g, dlam, ws)
+
+    def chain():
+        rb.relation_prologue_fwd(prob, x["P1"], x["P2"], x["V"], theta, PROLOGUE_PAIRING, PROLOGUE_BASE, None, *pro)
+        operator(*pro)
+        rb.relation_prologue_bwd(prob, g[0], g[1], g[2], pro[2], theta, PROLOGUE_PAIRING, PROLOGUE_BASE, None,
+                                 *g_chain, dth)
+
+    g_chain = [torch.empty_like(x["P1"]) for _ in range(3)]
+    arms = {"fused": fused, "operator": lambda: operator(x["P1"], x["P2"], x["V"]), "chain": chain}
+    times = {k: [] for k in arms}
+    with ClockSampler(0) as clk:
+        for k in range(args.warmup + args.steps):
+            for name, fn in arms.items():
+                flush()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                fn()
+                e1.record()
+                torch.cuda.synchronize()
+                if k >= args.warmup:
+                    times[name].append(e0.elapsed_time(e1))
+    if rb.relation_check_device_status() != 0:
+        raise RuntimeError("device-side wait expired")
+    ms = {k: statistics.mean(v) for k, v in times.items()}
+    value = flops(w, 12) / (ms["fused"] * 1e-3) / 1e12
+    peak_burst, _, peak_src = load_peaks()
+    peak = (peak_burst, f"{peak_src} bf16 burst")
+    line = {
+        "metric": "Relation fwd+bwd with the input prologue fused into its loads, TFLOP/s (bf16, causal)",
+        "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms["fused"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded Gaussian inputs, resident in HBM)",
+        "config": {"workload": f"prologue_fused_{w.name}", "B": w.B, "H": w.H, "T": w.T, "d_h": w.d,
+                   "causal": w.causal, "tau_S": w.tau_S, "lambda": w.lam, "pairing": "B", "rope_base": PROLOGUE_BASE,
+                   "l2": L2_NOTE},
+        "breakdown_ms": {"fused_step": ms["fused"], "operator_step": ms["operator"], "two_call_chain": ms["chain"]},
+        "fused_over_operator": ms["fused"] / ms["operator"],
+        "fused_over_chain": ms["fused"] / ms["chain"],
+        "roofline": {"kernel": "fused step (relation_fwd_tc_kernel + relation_bwd_tc64_kernel with the prologue)",
+                     "bound": "tensor", "achieved": value, "peak": peak[0], "unit": "TFLOP/s",
+                     "frac": value / peak[0], "peak_source": peak[1], "traffic": None},
+        "gpu_launches": 5 * args.steps,
         "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)
@@ -667,6 +752,10 @@ def main():
         return run_decode_reference(args, w) if args.impl == "reference" else run_decode(args, w)
     if args.prologue:
         return run_prologue_reference(args, w) if args.impl == "reference" else run_prologue(args, w)
+    if args.prologue_fused:
+        if args.impl == "reference":
+            return run_reference(args, w)
+        return run_prologue_fused(args, w)
     if args.impl == "reference":
         return run_reference(args, w)
 

@@ -320,7 +320,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (kPro) {
             // Fused prologue of the key tile: rotate P2_j, mix V_j with the partner's states.
             if (ptx::mbar_wait_warp(&sm.kv_full, 0, abort_flag, status, kDevTimeoutFull)) {
-                if (pro.tab.enabled) rope_tile64<32>(sm.k, lane, pos_base + (float)kv0, pro.tab);
+                if (pro.tab.enabled) {
+                    RopeAngles<32> ang;
+                    ang.init(lane, pos_base + (float)kv0, pro.tab, 1.f);
+                    rope_tile64<32>(sm.k, lane, ang);
+                }
                 mix_tile64<32>(sm.v, sm.dq_stage, lane, g_cs, g_sn);
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
@@ -474,14 +478,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool leader = (warp == 4 + kElemWarps) && lane == 0;
         // Fused prologue: rotate P1 of query tile it2 once it has landed (a no-op past
         // the last tile); tiles 0 and 1 first, then tile it + 2 in iteration it.
+        // Query tiles come in order, so the angles carry from one tile to the next.
+        RopeAngles<128> ang;
+        if (kPro && pro.tab.enabled) ang.init(rq, pos_base + (float)(i_first * kTile), pro.tab, 1.f);
         auto rotate_q = [&](int it2) -> bool {
             if constexpr (kPro) {
                 if (it2 >= n_q) return true;
                 const int s2 = it2 % kQStages;
                 if (!ptx::mbar_wait_warp(&sm.q_full[s2], (it2 / kQStages) & 1, abort_flag, status, kDevTimeoutFull))
                     return false;
-                if (pro.tab.enabled)
-                    rope_tile64<128>(sm.q[s2], rq, pos_base + (float)((i_first + it2) * kTile), pro.tab);
+                if (pro.tab.enabled) rope_tile64<128>(sm.q[s2], rq, ang);
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(&sm.q_rot[s2]);

@@ -399,19 +399,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int tr = threadIdx.x - 64;
             const float pos_base = pro.pos0 != nullptr ? (float)pro.pos0[batch] : 0.f;
             bool ok = true;
+            RopeAngles<64> ang;  // the query tiles (consecutive), then the key tiles from row 0
+            if (pro.tab.enabled) ang.init(tr, pos_base + (float)q_base, pro.tab, 1.f);
             for (int t = 0; t < 2 && ok; ++t) {
                 if (n_t[t] == 0) continue;
                 if (!(ok = ptx::mbar_wait_warp(&bars->q_full[t], 0, abort_flag, status, kDevTimeoutFull))) break;
-                if (pro.tab.enabled) rope_tile64<64>(sQ + t * C::kTileBytes, tr, pos_base + (float)(q_base + t * kBM), pro.tab);
+                if (pro.tab.enabled) rope_tile64<64>(sQ + t * C::kTileBytes, tr, ang);
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(&bars->q_rot[t]);
             }
+            if (pro.tab.enabled) ang.init(tr, pos_base, pro.tab, 1.f);
             for (int j = 0; ok && j < n_max; ++j) {
                 const int s = j % C::kStages;
                 if (!ptx::mbar_wait_warp(&bars->k_full[s], (j / C::kStages) & 1, abort_flag, status, kDevTimeoutFull))
                     break;
-                if (pro.tab.enabled) rope_tile64<64>(sK + s * C::kTileBytes, tr, pos_base + (float)(j * kBN), pro.tab);
+                if (pro.tab.enabled) rope_tile64<64>(sK + s * C::kTileBytes, tr, ang);
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(&bars->k_rot[s]);
