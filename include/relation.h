@@ -352,6 +352,31 @@ relation_status_t relation_linear_bwd(const relation_problem_t* p, const void* P
                                       void* stream);
 
 /*
+ * Linear Relation with the KDA-style retention gate fused into its kernels
+ * ("Ask Self, Ask Others", Sec. 5.2 eq.(16); Appendix A.4.1): instead of G the
+ * gate's input R (the per-token projection output r_t; float32, laid out as G)
+ * and per-head, per-channel parameters A_log, dt_bias (float32 [H, d_h]):
+ *   g = -exp(A_log) * softplus(r + dt_bias),   alpha = exp(g) in (0, 1].
+ * relation_linear_fwd_gate: relation_linear_fwd with G = g (computed as each
+ *   chunk is read; g is never stored).
+ * relation_linear_bwd_gate: relation_linear_bwd with dR (float32, laid out as R,
+ *   fully overwritten) in place of dG, plus dA_log and d_dt_bias [H, d_h]
+ *   (float32, overwritten: sums over batches and tokens).  states_from_forward
+ *   refers to relation_linear_fwd_gate with the same arguments.
+ * Same support, workspace, launches and errors as the ungated calls; A_log and
+ * dt_bias must not be NULL and must not overlap any tensor argument.
+ */
+relation_status_t relation_linear_fwd_gate(const relation_problem_t* p, const void* P1, const void* P2,
+                                           const void* I, const float* R, const float* A_log, const float* dt_bias,
+                                           void* Y, float* state, void* workspace, size_t workspace_bytes,
+                                           void* stream);
+relation_status_t relation_linear_bwd_gate(const relation_problem_t* p, const void* P1, const void* P2,
+                                           const void* I, const float* R, const float* A_log, const float* dt_bias,
+                                           const void* dY, void* dP1, void* dP2, void* dI, float* dR, float* dA_log,
+                                           float* d_dt_bias, int states_from_forward, void* workspace,
+                                           size_t workspace_bytes, void* stream);
+
+/*
  * Reads and clears the device status word of the current device.  Call after
  * synchronising the streams used.  Returns RELATION_OK,
  * RELATION_ERR_DEVICE_TIMEOUT (a bounded wait expired; outputs of the calls

@@ -107,6 +107,12 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                               ctypes.c_float, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                               ctypes.c_size_t, _VP]
         lib.relation_bwd_prologue.restype = ctypes.c_int
+        lib.relation_linear_fwd_gate.argtypes = [ctypes.POINTER(Problem), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                                 _VP, ctypes.c_size_t, _VP]
+        lib.relation_linear_fwd_gate.restype = ctypes.c_int
+        lib.relation_linear_bwd_gate.argtypes = [ctypes.POINTER(Problem), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                                 _VP, _VP, _VP, _VP, _VP, ctypes.c_int, _VP, ctypes.c_size_t, _VP]
+        lib.relation_linear_bwd_gate.restype = ctypes.c_int
         lib.relation_decode_workspace_bytes.argtypes = [ctypes.POINTER(Problem)]
         lib.relation_decode_workspace_bytes.restype = ctypes.c_size_t
         lib.relation_decode.argtypes = [ctypes.POINTER(Problem), _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_int, _VP, _VP,
@@ -322,6 +328,36 @@ def relation_linear_bwd(prob, P1, P2, I, G, dY, dP1, dP2, dI, dG, states_from_fo
                                       _ptr(dP2), _ptr(dI), _ptr(dG), int(states_from_forward), _ptr(workspace),
                                       workspace.numel() * workspace.element_size(), _stream_ptr(stream)),
            "relation_linear_bwd")
+
+
+def relation_linear_fwd_gate(prob, P1, P2, I, R, A_log, dt_bias, Y, state, workspace, stream=None) -> None:
+    _check(load().relation_linear_fwd_gate(ctypes.byref(prob), _ptr(P1), _ptr(P2), _ptr(I), _ptr(R), _ptr(A_log),
+                                           _ptr(dt_bias), _ptr(Y), _ptr(state), _ptr(workspace),
+                                           workspace.numel() * workspace.element_size(), _stream_ptr(stream)),
+           "relation_linear_fwd_gate")
+
+
+def relation_linear_bwd_gate(prob, P1, P2, I, R, A_log, dt_bias, dY, dP1, dP2, dI, dR, dA_log, d_dt_bias,
+                             states_from_forward, workspace, stream=None) -> None:
+    _check(load().relation_linear_bwd_gate(ctypes.byref(prob), _ptr(P1), _ptr(P2), _ptr(I), _ptr(R), _ptr(A_log),
+                                           _ptr(dt_bias), _ptr(dY), _ptr(dP1), _ptr(dP2), _ptr(dI), _ptr(dR),
+                                           _ptr(dA_log), _ptr(d_dt_bias), int(states_from_forward), _ptr(workspace),
+                                           workspace.numel() * workspace.element_size(), _stream_ptr(stream)),
+           "relation_linear_bwd_gate")
+
+
+def linear_gate_fwd_bwd(P1, P2, I, R, A_log, dt_bias, dY, tau_S: float, layout: int = RELATION_LAYOUT_BHTD,
+                        stream=None):
+    """Gated Linear Relation forward and backward (states reused); returns
+    (Y, dP1, dP2, dI, dR, dA_log, d_dt_bias)."""
+    prob = problem_for(P1, tau_S, 0.0, True, layout)
+    ws = linear_workspace(prob, P1.device)
+    Y = torch.empty_like(I)
+    relation_linear_fwd_gate(prob, P1, P2, I, R, A_log, dt_bias, Y, None, ws, stream)
+    dP1, dP2, dI, dR = torch.empty_like(P1), torch.empty_like(P2), torch.empty_like(I), torch.empty_like(R)
+    dA, dB = torch.empty_like(A_log), torch.empty_like(dt_bias)
+    relation_linear_bwd_gate(prob, P1, P2, I, R, A_log, dt_bias, dY, dP1, dP2, dI, dR, dA, dB, True, ws, stream)
+    return Y, dP1, dP2, dI, dR, dA, dB
 
 
 def relation_check_device_status() -> int:

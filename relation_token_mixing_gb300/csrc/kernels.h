@@ -93,14 +93,21 @@ cudaError_t launch_convert(const KernelProblem& kp, const float* src, int dq_w, 
 // Linear Relation (bf16 operands, fp32 log-retention G, d <= 64).  The forward's
 // workspace holds BH * nseg * (64 * 64 + 64) floats for the segment states.
 int linear_segments(const KernelProblem& kp, int num_sms, int* seg_len);
+// gate_alog != nullptr: G holds the KDA gate's input r, and g = -exp(A_log) softplus(r + dt_bias)
+// per head and channel ([H, d] parameters).
 cudaError_t launch_linear_fwd(const KernelProblem& kp, const void* P1, const void* P2, const void* V, const float* G,
-                              void* Y, float* state_out, float* ws, int num_sms, cudaStream_t s);
+                              void* Y, float* state_out, float* ws, int num_sms, cudaStream_t s,
+                              const float* gate_alog = nullptr, const float* gate_dtb = nullptr);
 // The backward's workspace adds BH * nseg * 64 * 64 floats (reverse segment states)
 // and BH * T floats (p^1 . dq per token).
 // reuse_fwd_states: the workspace already holds the forward's segment states.
+// With the gate, dG receives dR and gate_dalog / gate_ddtb ([H, d], zeroed by the
+// caller) accumulate the parameters' gradients.
 cudaError_t launch_linear_bwd(const KernelProblem& kp, const void* P1, const void* P2, const void* V, const float* G,
                               const void* dY, void* dP1, void* dP2, void* dV, float* dG, bool reuse_fwd_states,
-                              float* ws, int num_sms, cudaStream_t s);
+                              float* ws, int num_sms, cudaStream_t s, const float* gate_alog = nullptr,
+                              const float* gate_dtb = nullptr, float* gate_dalog = nullptr,
+                              float* gate_ddtb = nullptr);
 
 // One warp waits on an mbarrier nothing arrives on, through the kernels' bounded
 // wait with a limit of limit_ns; the timeout is recorded in *status.

@@ -142,7 +142,9 @@ struct Args {
     const __nv_bfloat16* P1;
     const __nv_bfloat16* P2;
     const __nv_bfloat16* V;
-    const float* G;
+    const float* G;         // log-retention g, or the gate's input r (gate_alog != nullptr)
+    const float* gate_alog;  // KDA gate [H, d]: A_log, or nullptr (G holds g itself)
+    const float* gate_dtb;   // KDA gate [H, d]: dt_bias
     __nv_bfloat16* Y;
     float* state_out;  // [BH, d, d] or null
     float* hseg;       // [BH, nseg, 64, 64]: segment contributions, then entering states
@@ -263,14 +265,41 @@ struct Quarter {
     float2 al[4], f[4], b[4];
 };
 
+// KDA-style retention gate ("Ask Self, Ask Others", Sec. 5.2 eq.(16); Appendix
+// A.4.1) of one thread's channels c = 2 lane, 2 lane + 1 of head h:
+// g = -exp(A_log[h, c]) softplus(r + dt_bias[h, c]).  on == false: the loaded
+// values are g itself.
+struct GateCh {
+    float2 na, db;  // -exp(A_log), dt_bias
+    bool on;
+};
+template <class A>
+__device__ __forceinline__ GateCh gate_channels(const A& a, int64_t bh, int lane) {
+    GateCh gc{make_float2(0.f, 0.f), make_float2(0.f, 0.f), a.gate_alog != nullptr};
+    const int c = 2 * lane, d = a.kp.d;
+    if (gc.on && c < d) {
+        const size_t o = (size_t)(bh % a.kp.H) * d + c;
+        gc.na = make_float2(-expf(a.gate_alog[o]), -expf(a.gate_alog[o + 1]));
+        gc.db = make_float2(a.gate_dtb[o], a.gate_dtb[o + 1]);
+    }
+    return gc;
+}
+// softplus(x) = log(1 + e^x), written so that neither branch overflows.
+__device__ __forceinline__ float softplus_f(float x) { return fmaxf(x, 0.f) + log1pf(__expf(-fabsf(x))); }
+__device__ __forceinline__ float2 gate_g(float2 r, const GateCh& gc) {
+    return make_float2(gc.na.x * softplus_f(r.x + gc.db.x), gc.na.y * softplus_f(r.y + gc.db.y));
+}
+
 template <class GS, class ST>
-__device__ __forceinline__ void channel_phase_a(Quarter& Q, GS& gs, const ST& s, int d, int warp, int lane) {
+__device__ __forceinline__ void channel_phase_a(Quarter& Q, GS& gs, const ST& s, int d, int warp, int lane,
+                                                const GateCh& gc) {
     const int c = 2 * lane;
     const bool valid = c < d;
     float2 prod = make_float2(1.f, 1.f);
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-        const float2 g = *reinterpret_cast<const float2*>(s.g + (4 * warp + r) * kDp + c);
+        float2 g = *reinterpret_cast<const float2*>(s.g + (4 * warp + r) * kDp + c);
+        if (gc.on) g = gate_g(g, gc);
         Q.al[r] = valid ? make_float2(__expf(g.x), __expf(g.y)) : make_float2(1.f, 1.f);
         prod = mul2(prod, Q.al[r]);
         Q.f[r] = prod;
@@ -506,6 +535,7 @@ __device__ __forceinline__ void segment_pass(const Args& a) {
     float2 aseg = make_float2(1.f, 1.f);
     const int g = lane >> 2, t = lane & 3;
     const RowMap rm = row_map(kp, bh);
+    const GateCh gc = gate_channels(a, bh, lane);
     load_chunk<kVec16>(gs.st[0], a, rm, t_begin, warp, lane);
     for (int n = 0; n < nchunks; ++n) {
         Stage& s = gs.st[n & 1];
@@ -515,7 +545,7 @@ __device__ __forceinline__ void segment_pass(const Args& a) {
         if (n + 1 < nchunks) load_chunk<kVec16>(gs.st[(n + 1) & 1], a, rm, t0 + kC, warp, lane);
         row_scalars(gs, s, a.zscale, warp, lane);
         Quarter Q;
-        channel_phase_a(Q, gs, s, kp.d, warp, lane);
+        channel_phase_a(Q, gs, s, kp.d, warp, lane, gc);
         if (kOut && warp == 0) {
             uint4* A = reinterpret_cast<uint4*>(gs.amat);
             for (int k = lane; k < (int)(sizeof(gs.amat) / 16); k += 32) A[k] = make_uint4(0, 0, 0, 0);
@@ -643,7 +673,11 @@ struct BArgs {
     const __nv_bfloat16* P1;
     const __nv_bfloat16* P2;
     const __nv_bfloat16* V;
-    const float* G;
+    const float* G;         // log-retention g, or the gate's input r (gate_alog != nullptr)
+    const float* gate_alog;  // KDA gate [H, d]: A_log, or nullptr
+    const float* gate_dtb;   // KDA gate [H, d]: dt_bias
+    float* gate_dalog;       // gate: d A_log [H, d] (+=), or nullptr
+    float* gate_ddtb;        // gate: d dt_bias [H, d] (+=)
     const __nv_bfloat16* dY;
     __nv_bfloat16* dP1;
     __nv_bfloat16* dP2;
@@ -790,6 +824,7 @@ __global__ void __launch_bounds__(kThreads, 3) linear_bstate_kernel(BArgs a) {
     State D;  // dC rows c = 16w + g (+8), columns v
     state_zero(D);
     const RowMap rm = row_map(kp, bh);
+    const GateCh gc = gate_channels(a, bh, lane);
     load_chunk_b<kVec16>(gs.st[(nchunks - 1) & 1], a, rm, t_begin + (nchunks - 1) * kC, warp, lane, false);
     for (int n = nchunks - 1; n >= 0; --n) {
         BStage& s = gs.st[n & 1];
@@ -798,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, 3) linear_bstate_kernel(BArgs a) {
         if (n > 0) load_chunk_b<kVec16>(gs.st[(n - 1) & 1], a, rm, t_begin + (n - 1) * kC, warp, lane, false);
         row_scalars(gs, s, a.zscale, warp, lane);
         Quarter Q;
-        channel_phase_a(Q, gs, s, kp.d, warp, lane);
+        channel_phase_a(Q, gs, s, kp.d, warp, lane, gc);
         __syncthreads();
         {
             const QuarterTotals T = quarter_totals(gs, warp, lane);
@@ -888,6 +923,7 @@ __global__ void __launch_bounds__(kThreads, 3) linear_bwd_a_kernel(BArgs a) {
         state_zero(H);
     }
     const RowMap rm = row_map(kp, bh);
+    const GateCh gc = gate_channels(a, bh, lane);
     load_chunk_b<kVec16>(gs.st[0], a, rm, t_begin, warp, lane, true);
     for (int n = 0; n < nchunks; ++n) {
         BStage& s = gs.st[n & 1];
@@ -897,7 +933,7 @@ __global__ void __launch_bounds__(kThreads, 3) linear_bwd_a_kernel(BArgs a) {
         if (n + 1 < nchunks) load_chunk_b<kVec16>(gs.st[(n + 1) & 1], a, rm, t0 + kC, warp, lane, true);
         row_scalars(gs, s, a.zscale, warp, lane);
         Quarter Q;
-        channel_phase_a(Q, gs, s, kp.d, warp, lane);
+        channel_phase_a(Q, gs, s, kp.d, warp, lane, gc);
         __syncthreads();  // B2
         const QuarterTotals T = quarter_totals(gs, warp, lane);
         channel_phase_b<false, true, false, true>(Q, T, gs, s, warp, lane);
@@ -1037,6 +1073,8 @@ __global__ void __launch_bounds__(kThreads, 3) linear_bwd_b_kernel(BArgs a) {
     __syncthreads();
     float2 carry = *reinterpret_cast<const float2*>(gs.bnd + c);  // sum of z over the later tokens (+ boundary)
     const RowMap rm = row_map(kp, bh);
+    const GateCh gc = gate_channels(a, bh, lane);
+    float2 acc_dalog = make_float2(0.f, 0.f), acc_ddtb = make_float2(0.f, 0.f);  // gate: this thread's token sums
     load_chunk_b<kVec16>(gs.st[(nchunks - 1) & 1], a, rm, t_begin + (nchunks - 1) * kC, warp, lane, true);
     for (int n = nchunks - 1; n >= 0; --n) {
         BStage& s = gs.st[n & 1];
@@ -1046,7 +1084,7 @@ __global__ void __launch_bounds__(kThreads, 3) linear_bwd_b_kernel(BArgs a) {
         if (n > 0) load_chunk_b<kVec16>(gs.st[(n - 1) & 1], a, rm, t0 - kC, warp, lane, true);
         row_scalars(gs, s, a.zscale, warp, lane);
         Quarter Q;
-        channel_phase_a(Q, gs, s, kp.d, warp, lane);
+        channel_phase_a(Q, gs, s, kp.d, warp, lane, gc);
         if (warp == 0) {
             uint4* A = reinterpret_cast<uint4*>(gs.amat);
             for (int k = lane; k < (int)(sizeof(gs.amat) / 16); k += 32) A[k] = make_uint4(0, 0, 0, 0);
@@ -1226,7 +1264,18 @@ __global__ void __launch_bounds__(kThreads, 3) linear_bwd_b_kernel(BArgs a) {
                 const float S = rn.z;
                 const float dz = (pq[r] + pd) * S * (1.f - S) * a.zscale;
                 if (c < kp.d) {
-                    *reinterpret_cast<float2*>(a.dG + off + c) = later;
+                    float2 dg = later;
+                    if (gc.on) {
+                        // Chain rule through the gate: dg/dA_log = g, dg/dr = -exp(A_log) sigmoid(r + dt_bias).
+                        const float2 rr = *reinterpret_cast<const float2*>(s.g + i * kDp + c);
+                        const float2 gg = gate_g(rr, gc);
+                        const float2 sg = make_float2(1.f / (1.f + __expf(-(rr.x + gc.db.x))),
+                                                      1.f / (1.f + __expf(-(rr.y + gc.db.y))));
+                        acc_dalog = make_float2(fmaf(later.x, gg.x, acc_dalog.x), fmaf(later.y, gg.y, acc_dalog.y));
+                        dg = make_float2(later.x * gc.na.x * sg.x, later.y * gc.na.y * sg.y);
+                        acc_ddtb = make_float2(acc_ddtb.x + dg.x, acc_ddtb.y + dg.y);
+                    }
+                    *reinterpret_cast<float2*>(a.dG + off + c) = dg;
                     *reinterpret_cast<uint32_t*>(a.dP1 + off + c) =
                         pack2(lo_f(p1w[r]) + dz * p2.x, hi_f(p1w[r]) + dz * p2.y);
                     *reinterpret_cast<uint32_t*>(a.dP2 + off + c) =
@@ -1234,6 +1283,13 @@ __global__ void __launch_bounds__(kThreads, 3) linear_bwd_b_kernel(BArgs a) {
                 }
             }
         }
+    }
+    if (gc.on && c < kp.d) {
+        const size_t o = (size_t)(bh % kp.H) * kp.d + c;
+        atomicAdd(a.gate_dalog + o, acc_dalog.x);
+        atomicAdd(a.gate_dalog + o + 1, acc_dalog.y);
+        atomicAdd(a.gate_ddtb + o, acc_ddtb.x);
+        atomicAdd(a.gate_ddtb + o + 1, acc_ddtb.y);
     }
 }
 
@@ -1266,8 +1322,11 @@ int linear_segments(const KernelProblem& kp, int num_sms, int* seg_len) {
 }
 
 cudaError_t launch_linear_fwd(const KernelProblem& kp, const void* P1, const void* P2, const void* V, const float* G,
-                              void* Y, float* state_out, float* ws, int num_sms, cudaStream_t s) {
+                              void* Y, float* state_out, float* ws, int num_sms, cudaStream_t s, const float* gate_alog,
+                              const float* gate_dtb) {
     lin::Args a;
+    a.gate_alog = gate_alog;
+    a.gate_dtb = gate_dtb;
     a.P1 = static_cast<const __nv_bfloat16*>(P1);
     a.P2 = static_cast<const __nv_bfloat16*>(P2);
     a.V = static_cast<const __nv_bfloat16*>(V);
@@ -1308,8 +1367,11 @@ cudaError_t launch_linear_fwd(const KernelProblem& kp, const void* P1, const voi
 
 cudaError_t launch_linear_bwd(const KernelProblem& kp, const void* P1, const void* P2, const void* V, const float* G,
                               const void* dY, void* dP1, void* dP2, void* dV, float* dG, bool reuse_fwd_states,
-                              float* ws, int num_sms, cudaStream_t s) {
+                              float* ws, int num_sms, cudaStream_t s, const float* gate_alog, const float* gate_dtb,
+                              float* gate_dalog, float* gate_ddtb) {
     lin::Args fa;
+    fa.gate_alog = gate_alog;
+    fa.gate_dtb = gate_dtb;
     fa.P1 = static_cast<const __nv_bfloat16*>(P1);
     fa.P2 = static_cast<const __nv_bfloat16*>(P2);
     fa.V = static_cast<const __nv_bfloat16*>(V);
@@ -1323,6 +1385,10 @@ cudaError_t launch_linear_bwd(const KernelProblem& kp, const void* P1, const voi
     fa.hseg = ws;
     fa.aseg = ws + per_seg * lin::kDp * lin::kDp;
     lin::BArgs b;
+    b.gate_alog = gate_alog;
+    b.gate_dtb = gate_dtb;
+    b.gate_dalog = gate_dalog;
+    b.gate_ddtb = gate_ddtb;
     b.P1 = fa.P1;
     b.P2 = fa.P2;
     b.V = fa.V;

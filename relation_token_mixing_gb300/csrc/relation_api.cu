@@ -621,9 +621,24 @@ size_t relation_linear_workspace_bytes(const relation_problem_t* p) {
     return linear_ws_floats(p, di.num_sms, true) * sizeof(float);
 }
 
-relation_status_t relation_linear_fwd(const relation_problem_t* p, const void* P1, const void* P2, const void* I,
-                                      const float* G, void* Y, float* state, void* workspace,
-                                      size_t workspace_bytes, void* stream) {
+namespace relation {
+namespace {
+// Gate parameters [H, d_h] float32: both given or both absent; 4-byte aligned.
+// tensors[k] spans bytes[k] (bf16 operands, fp32 gate inputs / outputs).
+relation_status_t check_gate(const relation_problem_t* p, const float* a, const float* b, const void* const* tensors,
+                             const size_t* bytes, int n) {
+    if (a == nullptr || b == nullptr) return RELATION_ERR_INVALID_ARGUMENT;
+    if ((reinterpret_cast<uintptr_t>(a) & 3u) || (reinterpret_cast<uintptr_t>(b) & 3u)) return RELATION_ERR_MISALIGNED;
+    const size_t pb = (size_t)p->H * (size_t)p->d_h * sizeof(float);
+    for (int k = 0; k < n; ++k)
+        if (overlaps(a, pb, tensors[k], bytes[k]) || overlaps(b, pb, tensors[k], bytes[k]))
+            return RELATION_ERR_INVALID_ARGUMENT;
+    return RELATION_OK;
+}
+
+relation_status_t run_linear_fwd(const relation_problem_t* p, const void* P1, const void* P2, const void* I,
+                                 const float* G, const float* gate_alog, const float* gate_dtb, void* Y, float* state,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
     relation_status_t st = check_linear(p);
     if (st != RELATION_OK) return st;
     if (!P1 || !P2 || !I || !G || !Y || !workspace) return RELATION_ERR_INVALID_ARGUMENT;
@@ -647,15 +662,15 @@ relation_status_t relation_linear_fwd(const relation_problem_t* p, const void* P
     int len = 0;
     const int nseg = linear_segments(kp, di.num_sms, &len);
     st = from_cuda(launch_linear_fwd(kp, P1, P2, I, G, Y, state, static_cast<float*>(workspace), di.num_sms,
-                                     static_cast<cudaStream_t>(stream)));
+                                     static_cast<cudaStream_t>(stream), gate_alog, gate_dtb));
     if (st == RELATION_OK) t_last_launches = nseg > 1 ? 3 : 1;
     return st;
 }
 
-relation_status_t relation_linear_bwd(const relation_problem_t* p, const void* P1, const void* P2, const void* I,
-                                      const float* G, const void* dY, void* dP1, void* dP2, void* dI, float* dG,
-                                      int states_from_forward, void* workspace, size_t workspace_bytes,
-                                      void* stream) {
+relation_status_t run_linear_bwd(const relation_problem_t* p, const void* P1, const void* P2, const void* I,
+                                 const float* G, const float* gate_alog, const float* gate_dtb, const void* dY,
+                                 void* dP1, void* dP2, void* dI, float* dG, float* gate_dalog, float* gate_ddtb,
+                                 int states_from_forward, void* workspace, size_t workspace_bytes, void* stream) {
     relation_status_t st = check_linear(p);
     if (st != RELATION_OK) return st;
     const void* ins[] = {P1, P2, I, G, dY};
@@ -686,10 +701,70 @@ relation_status_t relation_linear_bwd(const relation_problem_t* p, const void* P
     int len = 0;
     const int nseg = linear_segments(kp, di.num_sms, &len);
     const bool reuse = states_from_forward != 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (gate_dalog != nullptr) {
+        const size_t pb = (size_t)p->H * (size_t)p->d_h * sizeof(float);
+        if (cudaMemsetAsync(gate_dalog, 0, pb, s) != cudaSuccess || cudaMemsetAsync(gate_ddtb, 0, pb, s) != cudaSuccess)
+            return RELATION_ERR_CUDA;
+    }
     st = from_cuda(launch_linear_bwd(kp, P1, P2, I, G, dY, dP1, dP2, dI, dG, reuse, static_cast<float*>(workspace),
-                                     di.num_sms, static_cast<cudaStream_t>(stream)));
+                                     di.num_sms, s, gate_alog, gate_dtb, gate_dalog, gate_ddtb));
     if (st == RELATION_OK) t_last_launches = nseg > 1 ? (reuse ? 4 : 6) : 2;
     return st;
+}
+}  // namespace
+}  // namespace relation
+
+relation_status_t relation_linear_fwd(const relation_problem_t* p, const void* P1, const void* P2, const void* I,
+                                      const float* G, void* Y, float* state, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+    return run_linear_fwd(p, P1, P2, I, G, nullptr, nullptr, Y, state, workspace, workspace_bytes, stream);
+}
+
+relation_status_t relation_linear_bwd(const relation_problem_t* p, const void* P1, const void* P2, const void* I,
+                                      const float* G, const void* dY, void* dP1, void* dP2, void* dI, float* dG,
+                                      int states_from_forward, void* workspace, size_t workspace_bytes,
+                                      void* stream) {
+    return run_linear_bwd(p, P1, P2, I, G, nullptr, nullptr, dY, dP1, dP2, dI, dG, nullptr, nullptr,
+                          states_from_forward, workspace, workspace_bytes, stream);
+}
+
+relation_status_t relation_linear_fwd_gate(const relation_problem_t* p, const void* P1, const void* P2,
+                                           const void* I, const float* R, const float* A_log, const float* dt_bias,
+                                           void* Y, float* state, void* workspace, size_t workspace_bytes,
+                                           void* stream) {
+    relation_status_t st = check_linear(p);
+    if (st != RELATION_OK) return st;
+    const size_t tb = tensor_bytes(p), sb = (size_t)p->B * p->H * p->d_h * p->d_h * sizeof(float);
+    const void* ts[] = {P1, P2, I, R, Y, state};
+    const size_t bs[] = {tb, tb, tb, 2 * tb, tb, sb};
+    if ((st = check_gate(p, A_log, dt_bias, ts, bs, state ? 6 : 5)) != RELATION_OK) return st;
+    return run_linear_fwd(p, P1, P2, I, R, A_log, dt_bias, Y, state, workspace, workspace_bytes, stream);
+}
+
+relation_status_t relation_linear_bwd_gate(const relation_problem_t* p, const void* P1, const void* P2,
+                                           const void* I, const float* R, const float* A_log, const float* dt_bias,
+                                           const void* dY, void* dP1, void* dP2, void* dI, float* dR, float* dA_log,
+                                           float* d_dt_bias, int states_from_forward, void* workspace,
+                                           size_t workspace_bytes, void* stream) {
+    relation_status_t st = check_linear(p);
+    if (st != RELATION_OK) return st;
+    const size_t tb = tensor_bytes(p);
+    const void* ts[] = {P1, P2, I, R, dY, dP1, dP2, dI, dR};
+    const size_t bs[] = {tb, tb, tb, 2 * tb, tb, tb, tb, tb, 2 * tb};
+    if ((st = check_gate(p, A_log, dt_bias, ts, bs, 9)) != RELATION_OK) return st;
+    float* outs[] = {dA_log, d_dt_bias};
+    const size_t pb = (size_t)p->H * (size_t)p->d_h * sizeof(float);
+    for (float* o : outs) {
+        if (o == nullptr) return RELATION_ERR_INVALID_ARGUMENT;
+        if (reinterpret_cast<uintptr_t>(o) & 3u) return RELATION_ERR_MISALIGNED;
+        for (int k = 0; k < 9; ++k)
+            if (overlaps(o, pb, ts[k], bs[k])) return RELATION_ERR_INVALID_ARGUMENT;
+        if (overlaps(o, pb, A_log, pb) || overlaps(o, pb, dt_bias, pb)) return RELATION_ERR_INVALID_ARGUMENT;
+    }
+    if (overlaps(dA_log, pb, d_dt_bias, pb)) return RELATION_ERR_INVALID_ARGUMENT;
+    return run_linear_bwd(p, P1, P2, I, R, A_log, dt_bias, dY, dP1, dP2, dI, dR, dA_log, d_dt_bias,
+                          states_from_forward, workspace, workspace_bytes, stream);
 }
 
 size_t relation_decode_workspace_bytes(const relation_problem_t* p) {

@@ -115,6 +115,21 @@ def linear_retention(B: int, H: int, T: int, d: int, seed: int = LINEAR_G_SEED, 
     return (-g_scale * a * torch.nn.functional.softplus(0.5 * z + b)).to(torch.float32)
 
 
+def linear_gate_inputs(B: int, H: int, T: int, d: int, seed: int = LINEAR_G_SEED, g_scale: float = 1.0):
+    """The draws behind linear_retention() as the inputs of the KDA-style gate: the per-token
+    projection output R = z / 2 [B, H, T, d] and the per-head channel parameters
+    A_log = log(g_scale * a), dt_bias = b [H, d] (float32), so that
+    -exp(A_log) * softplus(R + dt_bias) reproduces linear_retention() with the same seed."""
+    g = torch.Generator().manual_seed(int(seed))
+    a = 1.0 + 15.0 * torch.rand(1, H, 1, d, generator=g)
+    sp_b = torch.exp(torch.empty(1, H, 1, d).uniform_(float(torch.log(torch.tensor(1e-3))),
+                                                     float(torch.log(torch.tensor(1e-1))), generator=g))
+    b = torch.log(torch.expm1(sp_b))
+    z = torch.randn(B, H, T, d, generator=g)
+    return ((0.5 * z).to(torch.float32), torch.log(g_scale * a).reshape(H, d).to(torch.float32),
+            b.reshape(H, d).to(torch.float32))
+
+
 def make_linear(w: LinearWorkload) -> dict:
     """CPU tensors P1, P2, I (bf16), G (float32) and, when backward, dY (bf16); [B, H, T, d]."""
     shape = (w.B, w.H, w.T, w.d)

@@ -198,3 +198,65 @@ def test_linear_benchmark_workloads_sampled_heads(wname, heads):
         refs = lo.bwd(xs["P1"], xs["P2"], xs["I"], xs["G"], w.tau_S, xs["dY"])
         for got, ref in zip(grads, refs):
             assert _err(_np(got[b:b + 1, h:h + 1]), ref) <= GTOL * float(np.max(np.abs(ref)))
+
+
+# The KDA-style retention gate fused into the kernels (Sec. 5.2 eq.(16); Appendix A.4.1):
+# R, A_log, dt_bias in, g = -exp(A_log) softplus(R + dt_bias) computed as each chunk is read;
+# the backward returns dR, dA_log, d dt_bias.  Reference: oracle.linear.gate / gate_bwd composed
+# with the recurrent oracle.  Tolerances as above for Y and the per-token gradients; the
+# parameter gradients get the bound that the per-token one propagates to through their sums.
+GATE_CASES = [
+    ("d64_ragged", 2, 3, 100, 64, BHTD, 1.0, 2.0),
+    ("d60_bthd_segments", 1, 4, 333, 60, BTHD, 1.0, 2.0),
+    ("d48_strong_decay", 2, 2, 150, 48, BHTD, 8.0, 0.5),
+]
+
+
+@pytest.mark.parametrize("name,B,H,T,d,layout,gs,tau", GATE_CASES, ids=[c[0] for c in GATE_CASES])
+def test_linear_gate_matches_oracle(name, B, H, T, d, layout, gs, tau):
+    x = rin.make_linear(rin.LinearWorkload(name, B, H, T, d, tau, gs, backward=True))
+    R, A_log, dtb = rin.linear_gate_inputs(B, H, T, d, g_scale=gs)
+    dev = {k: _to(v, layout).cuda() for k, v in x.items()}
+    Rd = _to(R, layout).cuda()
+    Y, dP1, dP2, dI, dR, dA, dB = rb.linear_gate_fwd_bwd(dev["P1"], dev["P2"], dev["I"], Rd, A_log.cuda(),
+                                                          dtb.cuda(), dev["dY"], tau, layout=layout)
+    torch.cuda.synchronize()
+    assert rb.relation_check_device_status() == 0
+    xs = {k: _np(v) for k, v in x.items()}
+    Gr = lo.gate(R.double().numpy(), A_log.double().numpy(), dtb.double().numpy())
+    Yr, _ = lo.fwd(xs["P1"], xs["P2"], xs["I"], Gr, tau)
+    assert _err(_np(_back(Y, layout)), Yr) <= TOL * float(np.max(np.abs(Yr))), name
+    g1, g2, gI, gG = lo.bwd(xs["P1"], xs["P2"], xs["I"], Gr, tau, xs["dY"])
+    gR, gA, gB = lo.gate_bwd(R.double().numpy(), A_log.double().numpy(), dtb.double().numpy(), gG)
+    for got, ref, label in ((dP1, g1, "dP1"), (dP2, g2, "dP2"), (dI, gI, "dI")):
+        err = _err(_np(_back(got, layout)), ref)
+        assert err <= GTOL * max(float(np.max(np.abs(ref))), 1e-6), (name, label, err)
+    # The gate's gradients are dG times d g / d (input), so the per-token bound on dG
+    # (GTOL * max|dG|) propagates elementwise to dR (d g / d R = -exp(A_log) sigmoid(R + dt_bias),
+    # up to 16 g_scale here) and, through the sums over all B*T tokens, to dA_log (d g / d A_log
+    # = g) and d dt_bias (the same slope as R): GTOL * max|dG| * sum_t |d g / d parameter| per channel.
+    x_in = R.double().numpy() + dtb.double().numpy()[None, :, None, :]
+    slope_b = np.exp(A_log.double().numpy())[None, :, None, :] / (1.0 + np.exp(-x_in))
+    gmax = float(np.max(np.abs(gG)))
+    dR_err = np.abs(_np(_back(dR, layout)) - gR)
+    assert np.all(dR_err <= GTOL * gmax * slope_b + 1e-6), (name, "dR", float(np.max(dR_err / (GTOL * gmax * slope_b))))
+    for got, ref, w, label in ((dA, gA, np.abs(Gr), "dA_log"), (dB, gB, slope_b, "d_dt_bias")):
+        bound = GTOL * gmax * w.sum(axis=(0, 2))
+        assert np.all(np.abs(_np(got) - ref) <= bound), (name, label, float(np.max(np.abs(_np(got) - ref) / bound)))
+
+
+def test_linear_gate_equals_ungated_with_its_retention():
+    """The gated forward on (R, A_log, dt_bias) and the plain forward on G = gate(...) computed
+    in float32 on the host agree to within the bf16 operand rounding."""
+    B, H, T, d, tau = 1, 2, 200, 64, 2.0
+    x = rin.make_linear(rin.LinearWorkload("eq", B, H, T, d, tau))
+    R, A_log, dtb = rin.linear_gate_inputs(B, H, T, d)
+    dev = {k: v.cuda() for k, v in x.items()}
+    G32 = torch.from_numpy(lo.gate(R.double().numpy(), A_log.double().numpy(), dtb.double().numpy())).float().cuda()
+    Y0, _ = rb.linear_fwd(dev["P1"], dev["P2"], dev["I"], G32, tau)
+    prob = rb.problem_for(dev["P1"], tau, 0.0, True)
+    ws = rb.linear_workspace(prob, "cuda")
+    Y1 = torch.empty_like(dev["I"])
+    rb.relation_linear_fwd_gate(prob, dev["P1"], dev["P2"], dev["I"], R.cuda(), A_log.cuda(), dtb.cuda(), Y1, None, ws)
+    torch.cuda.synchronize()
+    assert float((Y0.float() - Y1.float()).abs().max()) <= 1e-2 * float(Y0.float().abs().max())
