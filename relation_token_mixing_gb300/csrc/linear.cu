@@ -284,8 +284,10 @@ __device__ __forceinline__ GateCh gate_channels(const A& a, int64_t bh, int lane
     }
     return gc;
 }
-// softplus(x) = log(1 + e^x), written so that neither branch overflows.
-__device__ __forceinline__ float softplus_f(float x) { return fmaxf(x, 0.f) + log1pf(__expf(-fabsf(x))); }
+// softplus(x) = max(x, 0) + log(1 + e^-|x|), which overflows for no x; the
+// logarithm's argument is rounded to fp32, an absolute error below 1e-7 in g,
+// i.e. in the retention alpha = exp(g) a relative error below 1e-7 x alpha.
+__device__ __forceinline__ float softplus_f(float x) { return fmaxf(x, 0.f) + __logf(1.f + __expf(-fabsf(x))); }
 __device__ __forceinline__ float2 gate_g(float2 r, const GateCh& gc) {
     return make_float2(gc.na.x * softplus_f(r.x + gc.db.x), gc.na.y * softplus_f(r.y + gc.db.y));
 }
