@@ -890,7 +890,7 @@ def main():
     # 128 the 128-wide ones (zero-padded tiles); 60 reads zero-padded copies of its
     # operands (made by one extra launch in the forward and one in the backward).
     tile = 64 if w.d <= 64 else 128
-    srcs_common = ["ptx_sm100.cuh", "common.cuh", "tile_copy.cuh"]
+    srcs_common = ["ptx_sm100.cuh", "common.cuh", "tile_copy.cuh", "prologue_tiles.cuh", "kernels.h"]
     fwd_k = f"relation_fwd_tc_kernel<{tile}, false>"
     fwd_src = ["fwd_tc.cu"] + srcs_common
     if tile == 64:
