@@ -351,6 +351,40 @@ __global__ void __launch_bounds__(kThreads, 2) decode_cluster_kernel(
             for (int k = 0; k < VEC; ++k) o[k] = fmaf(p, vv[k], o[k]);
         }
     };
+    // Two Exchange rows into the group's running state at once (independent dot
+    // products, split accumulators, one rescale at most); as take() otherwise.
+    auto take2 = [&](const float (&k1)[VEC], const float (&v1)[VEC], bool ok1, const float (&k2)[VEC],
+                     const float (&v2)[VEC], bool ok2) {
+        float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+#pragma unroll
+        for (int k = 0; k < VEC; k += 2) {
+            a0 = fmaf(q[k], k1[k], a0);
+            a1 = fmaf(q[k + 1], k1[k + 1], a1);
+            b0 = fmaf(q[k], k2[k], b0);
+            b1 = fmaf(q[k + 1], k2[k + 1], b1);
+        }
+        float d1 = a0 + a1, d2 = b0 + b1;
+#pragma unroll
+        for (int w = G / 2; w > 0; w >>= 1) {
+            d1 += __shfl_xor_sync(0xffffffffu, d1, w);
+            d2 += __shfl_xor_sync(0xffffffffu, d2, w);
+        }
+        const float u1 = d1 * kp.inv_sqrt_d, u2 = d2 * kp.inv_sqrt_d;
+        const float r1 = ok1 ? u1 * sigmoid_f<kFast>(u1) - corr : -INFINITY;
+        const float r2 = ok2 ? u2 * sigmoid_f<kFast>(u2) - corr : -INFINITY;
+        const float mx = fmaxf(r1, r2);
+        if (mx > m) {  // raise the running maximum (rescale the state)
+            const float s1 = (m == -INFINITY) ? 0.f : exp_f<kFast>(m - mx);
+            l *= s1;
+#pragma unroll
+            for (int k = 0; k < VEC; ++k) o[k] *= s1;
+            m = mx;
+        }
+        const float p1 = ok1 ? exp_f<kFast>(r1 - m) : 0.f, p2 = ok2 ? exp_f<kFast>(r2 - m) : 0.f;
+        l += p1 + p2;
+#pragma unroll
+        for (int k = 0; k < VEC; ++k) o[k] = fmaf(p1, v1[k], fmaf(p2, v2[k], o[k]));
+    };
     bool ok = true;
     for (int k = 0; k < nck; ++k) {
         if (!ptx::mbar_wait(&full[k % kStreamStages], (k / kStreamStages) & 1, &abort_flag, status,
@@ -363,16 +397,20 @@ __global__ void __launch_bounds__(kThreads, 2) decode_cluster_kernel(
         const Tin* sK = reinterpret_cast<const Tin*>(smb + (size_t)(k % kStreamStages) * stage_bytes);
         const Tin* sV = sK + (size_t)ch * d;
         const int rc = min(t, (k0 + k) * ch + ch) - (k0 + k) * ch;
-        for (int base = 0; base < rc; base += kGroups) {  // same trip count in every lane
-            const int r = base + grp;
-            float kv[VEC], vv[VEC];
+        for (int base = 0; base < rc; base += 2 * kGroups) {  // same trip count in every lane
+            const int r1 = base + grp, r2 = r1 + kGroups;
+            float kv1[VEC], vv1[VEC], kv2[VEC], vv2[VEC];
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) kv[e] = vv[e] = 0.f;
-            if (active && r < rc) {
-                load_vec16<Tin, VEC, true>(sK + (size_t)r * d + col, kv);
-                load_vec16<Tin, VEC, true>(sV + (size_t)r * d + col, vv);
+            for (int e = 0; e < VEC; ++e) kv1[e] = vv1[e] = kv2[e] = vv2[e] = 0.f;
+            if (active && r1 < rc) {
+                load_vec16<Tin, VEC, true>(sK + (size_t)r1 * d + col, kv1);
+                load_vec16<Tin, VEC, true>(sV + (size_t)r1 * d + col, vv1);
             }
-            take(kv, vv, false, r < rc);
+            if (active && r2 < rc) {
+                load_vec16<Tin, VEC, true>(sK + (size_t)r2 * d + col, kv2);
+                load_vec16<Tin, VEC, true>(sV + (size_t)r2 * d + col, vv2);
+            }
+            take2(kv1, vv1, r1 < rc, kv2, vv2, r2 < rc);
         }
         __syncthreads();  // the stage is consumed: refill it with the chunk kStreamStages ahead
         if (threadIdx.x == 0 && issued < nck) issue(issued++);
@@ -393,28 +431,48 @@ __global__ void __launch_bounds__(kThreads, 2) decode_cluster_kernel(
         take(kv, vv, true, grp == 0);
     }
     if (!ok) m = -INFINITY;  // a share whose rows did not arrive is left out (the timeout is reported)
-    // Merge of the groups into this CTA's (m, l, o) (the stages are no longer read).
-    __syncthreads();
-    if (active) {
+    // Merge of the groups into this CTA's (m, l, o): first the warp's groups by
+    // shuffles (lanes li of the groups pair up), then the warps through shared
+    // memory (the stages are no longer read).
 #pragma unroll
-        for (int k = 0; k < VEC; ++k) og[(size_t)grp * d + col + k] = o[k];
+    for (int w = G; w < 32; w <<= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, w), l2 = __shfl_xor_sync(0xffffffffu, l, w);
+        const float M = fmaxf(m, m2);
+        const float s1 = (m == -INFINITY) ? 0.f : exp_f<kFast>(m - M);
+        const float s2 = (m2 == -INFINITY) ? 0.f : exp_f<kFast>(m2 - M);
+        l = l * s1 + l2 * s2;
+#pragma unroll
+        for (int k = 0; k < VEC; ++k) o[k] = o[k] * s1 + __shfl_xor_sync(0xffffffffu, o[k], w) * s2;
+        m = M;
     }
-    if (li == 0) {
-        gm[grp] = m;
-        gl[grp] = l;
+    constexpr int kWarps = kThreads / 32;
+    __syncthreads();
+    const int wid = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) < G) {  // the first group of each warp now holds the warp's state
+        if (active) {
+#pragma unroll
+            for (int k = 0; k < VEC; ++k) og[(size_t)wid * d + col + k] = o[k];
+        }
+        if (li == 0) {
+            gm[wid] = m;
+            gl[wid] = l;
+        }
     }
     __syncthreads();
     float M = -INFINITY;
-    for (int g = 0; g < kGroups; ++g) M = fmaxf(M, gm[g]);
+#pragma unroll
+    for (int g = 0; g < kWarps; ++g) M = fmaxf(M, gm[g]);
     for (int c = threadIdx.x; c < d; c += kThreads) {
         float acc = 0.f;
-        for (int g = 0; g < kGroups; ++g)
+#pragma unroll
+        for (int g = 0; g < kWarps; ++g)
             if (gm[g] != -INFINITY) acc = fmaf(exp_f<kFast>(gm[g] - M), og[(size_t)g * d + c], acc);
         res[2 + c] = acc;
     }
     if (threadIdx.x == 0) {
         float Lc = 0.f;
-        for (int g = 0; g < kGroups; ++g)
+#pragma unroll
+        for (int g = 0; g < kWarps; ++g)
             if (gm[g] != -INFINITY) Lc = fmaf(exp_f<kFast>(gm[g] - M), gl[g], Lc);
         res[0] = M;
         res[1] = Lc;
