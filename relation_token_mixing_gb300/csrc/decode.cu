@@ -123,18 +123,22 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
     ptx::bulk_load(dst, src, bytes, bar);
 }
 
-// Cluster-wide barrier (every thread of every CTA of the cluster): shared-memory
-// writes before it are visible to the cluster's reads after it.
+// Cluster barrier halves (every thread of every CTA of the cluster takes part).
+// The relaxed arrive only marks that the CTA has started (so that its shared
+// memory may be written by the cluster once the phase completes); the release /
+// acquire pair makes shared-memory writes before it visible to reads after it.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// Reads the float at the same shared-memory offset as `p` in CTA `rank` of the cluster.
-__device__ __forceinline__ float ld_cluster_f32(const float* p, int rank) {
+// Writes v to the float at the same shared-memory offset as `p` in CTA `rank` of the cluster.
+__device__ __forceinline__ void st_cluster_f32(float* p, int rank, float v) {
     uint32_t remote;
-    float v;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(ptx::smem_u32(p)), "r"(rank));
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-    return v;
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
 }
 
 // Partial pass: CTA (bh, chunk) handles keys [chunk*C, min(chunk*C + C, t+1));
@@ -248,82 +252,101 @@ __global__ void __launch_bounds__(kThreads) decode_partial_kernel(
 // equal share of whole chunks of the cached rows 0..t-1 (CH rows per chunk) and
 // streams them through a ring of kStreamStages shared-memory stages, each filled
 // by two bulk copies (P2 rows, I~ rows) completing on the stage's mbarrier, so
-// the copies of the next chunks are in flight while the current one is scored.
-// Every group of G lanes keeps an online softmax over its rows (running max m,
-// sum l and weighted sum o of the I~ rows: the scan of Sec. 5.1 eq.(12)); the
-// groups merge into the CTA's (m, l, o), and CTA 0 of the cluster merges the S
-// results through distributed shared memory and writes Y and L.  CTA 0 also
-// scores the new token's row (the Self entry, from the new-row tensors) and
-// appends it to the cache row t, which no CTA reads.
+// the copies of the next chunks are in flight while the current one is scored
+// (a stage left without a chunk gets a plain arrive, which ends the loop).  Every
+// group of G lanes keeps an online softmax over its rows (running max m, sum l
+// and weighted sum o of the I~ rows: the scan of Sec. 5.1 eq.(12)); the groups
+// merge into the CTA's (m, l, o), which every CTA writes into CTA 0's shared
+// memory; after one cluster barrier CTA 0 merges the S results and writes Y and
+// L.  The new token's rows come by bulk copies issued before anything else: its
+// P1 row to every CTA, its P2 and I~ rows to CTA 0, which scores the Self entry
+// and appends the row to the cache row t (which no CTA reads).
 constexpr int kStreamStages = 3;
+constexpr int kMaxCluster = 8;    // portable cluster size
+constexpr int kStreamMaxD = 128;  // widest head the streaming pass takes
+
 template <typename Tin, int VEC, int G>
 __global__ void __launch_bounds__(kThreads, 2) decode_cluster_kernel(
     KernelProblem kp, const Tin* __restrict__ P1n, const Tin* __restrict__ P2n, const Tin* __restrict__ Vn,
     Tin* __restrict__ P2c, Tin* __restrict__ Vc, const int* __restrict__ pos, int append, int ch,
     Tin* __restrict__ Y, float* __restrict__ L, unsigned int* status) {
     constexpr int kGroups = kThreads / G;
+    constexpr int kWarps = kThreads / 32;
     constexpr bool kFast = sizeof(Tin) == 2;
     extern __shared__ __align__(128) uint8_t smb[];
     __shared__ __align__(8) uint64_t full[kStreamStages];
+    __shared__ __align__(8) uint64_t new_full;
+    __shared__ int stage_chunk[kStreamStages];  // the chunk in each stage; -1: none (the loop ends)
     __shared__ int abort_flag;
+    __shared__ __align__(16) Tin new_rows[3 * kStreamMaxD];  // the new token's P1, P2 and I~ rows
+    // CTA 0's copy receives every CTA's (m, l, o); the same offsets in the other
+    // CTAs stay unused.
+    __shared__ float cl_m[kMaxCluster], cl_l[kMaxCluster];
+    __shared__ __align__(16) float cl_o[kMaxCluster * kStreamMaxD];
     const int d = kp.d;
     const size_t row_bytes = (size_t)d * sizeof(Tin);
     const size_t stage_bytes = 2 * (size_t)ch * row_bytes;
-    // After the stream the stage area holds the merge: per group o (kGroups x d),
-    // m and l, then the CTA's result (m, l, o[d]).
+    // After the stream the stage area holds the merge of the warps: per warp o
+    // (kWarps x d), m and l.
     float* og = reinterpret_cast<float*>(smb);
-    float* gm = og + (size_t)kGroups * d;
-    float* gl = gm + kGroups;
-    float* res = gl + kGroups;
+    float* gm = og + (size_t)kWarps * d;
+    float* gl = gm + kWarps;
     const int64_t bh = blockIdx.x;
     const int b = (int)(bh / kp.H);
-    const int t = pos[b];
     const int S = (int)gridDim.y, sidx = (int)blockIdx.y;  // cluster = the S CTAs of head bh
+    const size_t new_off = (size_t)bh * d;                 // [B, H, d] new-row tensors
+    if (threadIdx.x == 0) {
+        for (int k = 0; k < kStreamStages; ++k) ptx::mbar_init(&full[k], 1);
+        ptx::mbar_init(&new_full, 1);
+        abort_flag = 0;
+        ptx::fence_barrier_init();
+        ptx::mbar_arrive_expect_tx(&new_full, (uint32_t)row_bytes * (sidx == 0 ? 3u : 1u));
+        bulk_copy_g2s(new_rows, P1n + new_off, (uint32_t)row_bytes, &new_full);
+        if (sidx == 0) {
+            bulk_copy_g2s(new_rows + kStreamMaxD, P2n + new_off, (uint32_t)row_bytes, &new_full);
+            bulk_copy_g2s(new_rows + 2 * kStreamMaxD, Vn + new_off, (uint32_t)row_bytes, &new_full);
+        }
+    }
+    const int t = pos[b];
+    __syncthreads();  // the barriers are initialised
     if (t < 0 || t >= kp.T) {  // position outside the cache (the whole cluster returns): reported, not written
-        if (threadIdx.x == 0 && sidx == 0) record_status(status, kDevBadPosition);
+        if (threadIdx.x == 0) {
+            if (sidx == 0) record_status(status, kDevBadPosition);
+            ptx::mbar_drain(&new_full, 0, status);  // the new rows land before the CTA's memory is released
+        }
         return;
     }
-    const size_t new_off = (size_t)bh * d;  // [B, H, d] new-row tensors
-    if (append && sidx == 0)                // cache row t: no CTA reads it
-        for (int c = threadIdx.x; c < d; c += kThreads) {
-            P2c[row_offset(kp, bh, t) + c] = P2n[new_off + c];
-            Vc[row_offset(kp, bh, t) + c] = Vn[new_off + c];
-        }
+    cluster_arrive_relaxed();  // this CTA has started; waited on before the first remote write
     const int n_all = (t + ch - 1) / ch;  // chunks of cached rows
     const int per = (n_all + S - 1) / S;
     const int k0 = sidx * per;
     const int nck = max(0, min(n_all, k0 + per) - k0);
-    if (threadIdx.x == 0) {
-        for (int k = 0; k < kStreamStages; ++k) ptx::mbar_init(&full[k], 1);
-        abort_flag = 0;
-        ptx::fence_barrier_init();
-    }
-    __syncthreads();
-    // Thread 0 fills stage k % kStreamStages with chunk k0 + k.
-    auto issue = [&](int k) {
-        const int j0 = (k0 + k) * ch;
-        const int rc = min(t, j0 + ch) - j0;
-        uint8_t* st = smb + (size_t)(k % kStreamStages) * stage_bytes;
-        const uint32_t bytes = (uint32_t)(rc * row_bytes);
-        uint64_t* bar = &full[k % kStreamStages];
+    // Thread 0 fills stage f % kStreamStages for the f-th time: chunk c, or none (c < 0).
+    auto fill = [&](int f, int c) {
+        const int st = f % kStreamStages;
+        uint64_t* bar = &full[st];
+        stage_chunk[st] = c;
+        if (c < 0) {
+            ptx::mbar_arrive(bar);
+            return;
+        }
+        const int j0 = c * ch;
+        const uint32_t bytes = (uint32_t)((min(t, j0 + ch) - j0) * row_bytes);
+        uint8_t* dst = smb + (size_t)st * stage_bytes;
         ptx::mbar_arrive_expect_tx(bar, 2 * bytes);
-        bulk_copy_g2s(st, P2c + row_offset(kp, bh, j0), bytes, bar);
-        bulk_copy_g2s(st + (size_t)ch * row_bytes, Vc + row_offset(kp, bh, j0), bytes, bar);
+        bulk_copy_g2s(dst, P2c + row_offset(kp, bh, j0), bytes, bar);
+        bulk_copy_g2s(dst + (size_t)ch * row_bytes, Vc + row_offset(kp, bh, j0), bytes, bar);
     };
-    int issued = 0;  // chunks whose copies thread 0 has issued
+    int fills = 0;  // thread 0: stage fills issued (fill f carries chunk k0 + f while f < nck)
     if (threadIdx.x == 0)
-        for (; issued < kStreamStages && issued < nck; ++issued) issue(issued);
+        for (; fills < kStreamStages; ++fills) fill(fills, fills < nck ? k0 + fills : -1);
     const int grp = threadIdx.x / G, li = threadIdx.x % G;
     const int col = li * VEC;
     const bool active = col < d;
-    float q[VEC];
-#pragma unroll
-    for (int k = 0; k < VEC; ++k) q[k] = 0.f;
-    if (active) load_vec16<Tin, VEC, false>(P1n + new_off + col, q);
     const float corr = kp.lambda * logf((float)(t + 1));  // lambda log c, c = t+1
-    float m = -INFINITY, l = 0.f, o[VEC];
+    float m = -INFINITY, l = 0.f, o[VEC], q[VEC];
 #pragma unroll
-    for (int k = 0; k < VEC; ++k) o[k] = 0.f;
+    for (int k = 0; k < VEC; ++k) o[k] = q[k] = 0.f;
     // One row (its P2 and I~ values kv, vv) into the group's running state.  Every
     // lane of the warp calls this together (the shuffles span the warp); lanes of a
     // group without a row this round pass valid = false and keep their state.
@@ -385,18 +408,40 @@ __global__ void __launch_bounds__(kThreads, 2) decode_cluster_kernel(
 #pragma unroll
         for (int k = 0; k < VEC; ++k) o[k] = fmaf(p1, v1[k], fmaf(p2, v2[k], o[k]));
     };
-    bool ok = true;
-    for (int k = 0; k < nck; ++k) {
-        if (!ptx::mbar_wait(&full[k % kStreamStages], (k / kStreamStages) & 1, &abort_flag, status,
-                            kDevTimeoutFull))
-            ok = false;
+    // The new token's rows: q for every lane; the Self entry (group 0 of warp 0,
+    // the warp shuffling together) and the append in CTA 0.
+    bool ok = ptx::mbar_wait(&new_full, 0, &abort_flag, status, kDevTimeoutFull);
+    if (ok) {
+        if (active) load_vec16<Tin, VEC, true>(new_rows + col, q);
+        if (append && sidx == 0)
+            for (int c = threadIdx.x; c < d; c += kThreads) {
+                P2c[row_offset(kp, bh, t) + c] = new_rows[kStreamMaxD + c];
+                Vc[row_offset(kp, bh, t) + c] = new_rows[2 * kStreamMaxD + c];
+            }
+    }
+    if (sidx == 0 && threadIdx.x < 32) {
+        float kv[VEC], vv[VEC];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) kv[e] = vv[e] = 0.f;
+        const bool mine = ok && active && grp == 0;
+        if (mine) {
+            load_vec16<Tin, VEC, true>(new_rows + kStreamMaxD + col, kv);
+            load_vec16<Tin, VEC, true>(new_rows + 2 * kStreamMaxD + col, vv);
+        }
+        take(kv, vv, true, grp == 0);
+    }
+    for (int k = 0;; ++k) {
+        const int st = k % kStreamStages;
+        if (!ptx::mbar_wait(&full[st], (k / kStreamStages) & 1, &abort_flag, status, kDevTimeoutFull)) ok = false;
         if (!__syncthreads_and(ok)) {  // every thread leaves together
             ok = false;
             break;
         }
-        const Tin* sK = reinterpret_cast<const Tin*>(smb + (size_t)(k % kStreamStages) * stage_bytes);
+        const int c = stage_chunk[st];
+        if (c < 0) break;  // the same in every thread
+        const Tin* sK = reinterpret_cast<const Tin*>(smb + (size_t)st * stage_bytes);
         const Tin* sV = sK + (size_t)ch * d;
-        const int rc = min(t, (k0 + k) * ch + ch) - (k0 + k) * ch;
+        const int rc = min(t, c * ch + ch) - c * ch;
         for (int base = 0; base < rc; base += 2 * kGroups) {  // same trip count in every lane
             const int r1 = base + grp, r2 = r1 + kGroups;
             float kv1[VEC], vv1[VEC], kv2[VEC], vv2[VEC];
@@ -412,24 +457,17 @@ __global__ void __launch_bounds__(kThreads, 2) decode_cluster_kernel(
             }
             take2(kv1, vv1, r1 < rc, kv2, vv2, r2 < rc);
         }
-        __syncthreads();  // the stage is consumed: refill it with the chunk kStreamStages ahead
-        if (threadIdx.x == 0 && issued < nck) issue(issued++);
+        __syncthreads();  // the stage is consumed: refill it
+        if (threadIdx.x == 0) {
+            fill(fills, fills < nck ? k0 + fills : -1);
+            ++fills;
+        }
     }
     if (!ok && threadIdx.x == 0)
-        // Give the copies in flight (the last one issued into each stage) a second
-        // bounded wait before the stage area is reused.
-        for (int k = max(0, issued - kStreamStages); k < issued; ++k)
-            ptx::mbar_drain(&full[k % kStreamStages], (k / kStreamStages) & 1, status);
-    if (sidx == 0 && threadIdx.x < 32) {  // the new token's Self entry, by group 0 (warp 0 shuffles together)
-        float kv[VEC], vv[VEC];
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) kv[e] = vv[e] = 0.f;
-        if (active && grp == 0) {
-            load_vec16<Tin, VEC, false>(P2n + new_off + col, kv);
-            load_vec16<Tin, VEC, false>(Vn + new_off + col, vv);
-        }
-        take(kv, vv, true, grp == 0);
-    }
+        // Give the copies in flight (the last fill of each stage) a second bounded
+        // wait before the stage area is reused.
+        for (int f = max(0, fills - kStreamStages); f < fills; ++f)
+            ptx::mbar_drain(&full[f % kStreamStages], (f / kStreamStages) & 1, status);
     if (!ok) m = -INFINITY;  // a share whose rows did not arrive is left out (the timeout is reported)
     // Merge of the groups into this CTA's (m, l, o): first the warp's groups by
     // shuffles (lanes li of the groups pair up), then the warps through shared
@@ -445,8 +483,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_cluster_kernel(
         for (int k = 0; k < VEC; ++k) o[k] = o[k] * s1 + __shfl_xor_sync(0xffffffffu, o[k], w) * s2;
         m = M;
     }
-    constexpr int kWarps = kThreads / 32;
-    __syncthreads();
+    __syncthreads();  // the stage area is free (copies in flight drained above)
     const int wid = threadIdx.x >> 5;
     if ((threadIdx.x & 31) < G) {  // the first group of each warp now holds the warp's state
         if (active) {
@@ -459,6 +496,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_cluster_kernel(
         }
     }
     __syncthreads();
+    cluster_wait();  // every CTA of the cluster has started: CTA 0's shared memory may be written
     float M = -INFINITY;
 #pragma unroll
     for (int g = 0; g < kWarps; ++g) M = fmaxf(M, gm[g]);
@@ -467,40 +505,36 @@ __global__ void __launch_bounds__(kThreads, 2) decode_cluster_kernel(
 #pragma unroll
         for (int g = 0; g < kWarps; ++g)
             if (gm[g] != -INFINITY) acc = fmaf(exp_f<kFast>(gm[g] - M), og[(size_t)g * d + c], acc);
-        res[2 + c] = acc;
+        st_cluster_f32(cl_o + (size_t)sidx * kStreamMaxD + c, 0, acc);
     }
     if (threadIdx.x == 0) {
         float Lc = 0.f;
 #pragma unroll
         for (int g = 0; g < kWarps; ++g)
             if (gm[g] != -INFINITY) Lc = fmaf(exp_f<kFast>(gm[g] - M), gl[g], Lc);
-        res[0] = M;
-        res[1] = Lc;
+        st_cluster_f32(cl_m + sidx, 0, M);
+        st_cluster_f32(cl_l + sidx, 0, Lc);
     }
-    // Every CTA of the cluster has its result in shared memory; CTA 0 merges them
-    // (Y = sum_s e^{m_s - M} o_s / sum_s e^{m_s - M} l_s, L = M + log of the
-    // denominator, the paper's convention with the correction included), then the
-    // cluster leaves together so no result is read after its CTA has exited.
+    // After the barrier CTA 0 holds the S results in its own shared memory and
+    // merges them (Y = sum_s e^{m_s - M} o_s / sum_s e^{m_s - M} l_s, L = M + log
+    // of the denominator, the paper's convention with the correction included);
+    // no CTA's shared memory is accessed by another after it.
     cluster_sync();
     if (sidx == 0) {
         float Mc = -INFINITY;
-        for (int r = 0; r < S; ++r) Mc = fmaxf(Mc, ld_cluster_f32(res, r));
+        for (int r = 0; r < S; ++r) Mc = fmaxf(Mc, cl_m[r]);
         float den = 0.f;
-        for (int r = 0; r < S; ++r) {
-            const float mr = ld_cluster_f32(res, r);
-            if (mr != -INFINITY) den = fmaf(exp_f<kFast>(mr - Mc), ld_cluster_f32(res + 1, r), den);
-        }
+        for (int r = 0; r < S; ++r)
+            if (cl_m[r] != -INFINITY) den = fmaf(exp_f<kFast>(cl_m[r] - Mc), cl_l[r], den);
         for (int c = threadIdx.x; c < d; c += kThreads) {
             float num = 0.f;
-            for (int r = 0; r < S; ++r) {
-                const float mr = ld_cluster_f32(res, r);
-                if (mr != -INFINITY) num = fmaf(exp_f<kFast>(mr - Mc), ld_cluster_f32(res + 2 + c, r), num);
-            }
+            for (int r = 0; r < S; ++r)
+                if (cl_m[r] != -INFINITY)
+                    num = fmaf(exp_f<kFast>(cl_m[r] - Mc), cl_o[(size_t)r * kStreamMaxD + c], num);
             store_from_float(Y + new_off + c, num / den);
         }
         if (L != nullptr && threadIdx.x == 0) L[bh] = Mc + logf(den);
     }
-    cluster_sync();
 }
 
 // Merge of the chunks of one head: Y = sum_c e^{m_c - M} o_c / sum_c e^{m_c - M} l_c,
@@ -577,7 +611,6 @@ int stream_chunk_rows(const KernelProblem& kp, bool bf16) {
     return rows < 128 ? rows : 128;
 }
 constexpr int kStreamSmemMax = 120 * 1024;
-constexpr int kMaxCluster = 8;  // portable cluster size
 
 // The merge, launched as a programmatic dependent of the partial pass (it may be
 // scheduled while that pass finishes and waits for its writes in-kernel).
@@ -605,7 +638,6 @@ template <typename Tin, int VEC, int G>
 cudaError_t launch_stream(const KernelProblem& kp, const void* P1n, const void* P2n, const void* Vn, void* P2c,
                           void* Vc, const int* pos, int append, void* Y, float* L, unsigned int* status,
                           int num_sms, cudaStream_t s) {
-    constexpr int kGroups = kThreads / G;
     auto kern = decode_cluster_kernel<Tin, VEC, G>;
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
@@ -615,7 +647,7 @@ cudaError_t launch_stream(const KernelProblem& kp, const void* P1n, const void* 
     if (attr_err != cudaSuccess) return attr_err;
     const int ch = stream_chunk_rows(kp, sizeof(Tin) == 2);
     const size_t stages = (size_t)kStreamStages * 2 * ch * kp.d * sizeof(Tin);
-    const size_t merge = sizeof(float) * ((size_t)kGroups * kp.d + 2 * kGroups + kp.d + 2);
+    const size_t merge = sizeof(float) * ((size_t)(kThreads / 32) * (kp.d + 2));
     const size_t smem = stages > merge ? stages : merge;
     if (smem > (size_t)kStreamSmemMax) return cudaErrorInvalidValue;
     int per_sm = 0;
