@@ -465,8 +465,8 @@ cudaError_t launch_bwd_tc_d(const KernelProblem& kp, const void* P1, const void*
         if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&l2_bytes, cudaDevAttrL2CacheSize, dev);
     });
     const int64_t per_head = 12 * (int64_t)kp.T * D;
-    int64_t group = (l2_bytes > 0 ? (int64_t)l2_bytes * 3 / 4 : (int64_t)96 << 20) / per_head;
-    group = group < 1 ? 1 : (group > kp.BH ? kp.BH : group);
+    const int64_t group =
+        balanced_head_group(kp.BH, (l2_bytes > 0 ? (int64_t)l2_bytes * 3 / 4 : (int64_t)96 << 20) / per_head);
     relation_bwd_tc_kernel<D><<<dim3((unsigned)ctas), kThreads, C::kSmemBytes, s>>>(
         m1, m2, mv, mg, mq, kp, qconst, (__nv_bfloat16*)dP2, (__nv_bfloat16*)dV, dlambda, tl.status, (int)group);
     return cudaGetLastError();

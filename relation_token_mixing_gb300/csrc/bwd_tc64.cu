@@ -82,6 +82,7 @@ struct Smem {
     uint64_t dq_full;
     uint64_t dq_free;
     uint64_t mma_done[2];  // per MMA issuer: all of its products complete
+    uint64_t acc_done;     // dV and dP2 final (the last tile's accumulations complete)
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -140,7 +141,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (kPro) partner = givens_coeffs(head, kp.H, pro, &g_cs, &g_sn);
     const float pos_base = (kPro && pro.pos0 != nullptr) ? (float)pro.pos0[batch] : 0.f;
 
+    // Loads of the key tile and of query tile it (P1_i, dY_i and the per-query
+    // constants of this head, 64 float4 = 1 KB per query tile) into ring stage it % kQStages.
+    const float4* qsrc = qconst + (size_t)bh * (size_t)(qconst_rows(T) / 2);
+    auto issue_kv = [&] {
+        ptx::mbar_arrive_expect_tx(&sm.kv_full, (kPro ? 3 : 2) * kTileBytes);
+        ptx::tma_load_operand(sm.k, &tm_p2, &sm.kv_full, 0, kv0, bh, head, batch, kRank3);
+        ptx::tma_load_operand(sm.v, &tm_v, &sm.kv_full, 0, kv0, bh, head, batch, kRank3);
+        if constexpr (kPro)  // the Givens partner's states, into the (still unused) dP1 staging panel
+            ptx::tma_load_operand(sm.dq_stage, &tm_v, &sm.kv_full, 0, kv0, bh - head + partner, partner, batch,
+                                  kRank3);
+    };
+    auto issue_q = [&](int it) {
+        const int s = it % kQStages;
+        const int i = i_first + it;
+        ptx::mbar_arrive_expect_tx(&sm.q_full[s], 2 * kTileBytes + kQConstBytes);
+        ptx::bulk_load(sm.qconst[s], qsrc + i * (kTile / 2), kQConstBytes, &sm.q_full[s]);
+        ptx::tma_load_operand(sm.q[s], &tm_p1, &sm.q_full[s], 0, i * kTile, bh, head, batch, kRank3);
+        ptx::tma_load_operand(sm.g[s], &tm_dy, &sm.q_full[s], 0, i * kTile, bh, head, batch, kRank3);
+    };
     if (threadIdx.x == 0) {
+        ptx::tma_prefetch_desc(&tm_p1);
+        ptx::tma_prefetch_desc(&tm_p2);
+        ptx::tma_prefetch_desc(&tm_v);
+        ptx::tma_prefetch_desc(&tm_dy);
+        ptx::tma_prefetch_desc(&tm_dq);
         ptx::mbar_init(&sm.kv_full, 1);
         ptx::mbar_init(&sm.kv_rot, 1);
         for (int s = 0; s < kQStages; ++s) ptx::mbar_init(&sm.q_rot[s], 4);
@@ -158,8 +183,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(&sm.dq_free, 128);
         ptx::mbar_init(&sm.mma_done[0], 1);
         ptx::mbar_init(&sm.mma_done[1], 1);
+        ptx::mbar_init(&sm.acc_done, 1);
         sm.abort_flag = 0;
         ptx::fence_barrier_init();
+        // The loads that need no free stage leave before the block-wide barrier (and
+        // the TMEM allocation behind it): the key tile and the first query tiles.
+        issue_kv();
+        for (int it = 0; it < n_q && it < kQStages; ++it) issue_q(it);
     }
     if (warp == 1) {
         ptx::tmem_alloc(&sm.tmem_base, 512);
@@ -174,36 +204,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // -------------------------------------------------------------- loader
         ptx::regs_dec<kRegsControl>();
-        if (lane == 0) {
-            ptx::tma_prefetch_desc(&tm_p1);
-            ptx::tma_prefetch_desc(&tm_p2);
-            ptx::tma_prefetch_desc(&tm_v);
-            ptx::tma_prefetch_desc(&tm_dy);
-            ptx::tma_prefetch_desc(&tm_dq);
-            ptx::mbar_arrive_expect_tx(&sm.kv_full, (kPro ? 3 : 2) * kTileBytes);
-            ptx::tma_load_operand(sm.k, &tm_p2, &sm.kv_full, 0, kv0, bh, head, batch, kRank3);
-            ptx::tma_load_operand(sm.v, &tm_v, &sm.kv_full, 0, kv0, bh, head, batch, kRank3);
-            if constexpr (kPro)  // the Givens partner's states, into the (still unused) dP1 staging panel
-                ptx::tma_load_operand(sm.dq_stage, &tm_v, &sm.kv_full, 0, kv0, bh - head + partner, partner, batch,
-                                      kRank3);
-        }
-        // Per-query constants of this head, 64 float4 (1 KB) per query tile.
-        const float4* qsrc = qconst + (size_t)bh * (size_t)(qconst_rows(T) / 2);
-        int it = 0;
+        // The key tile and the first kQStages query tiles were issued at the start.
+        int it = n_q < kQStages ? n_q : kQStages;
         for (; it < n_q; ++it) {
-            const int s = it % kQStages;
-            const int i = i_first + it;
-            if (it >= kQStages &&
-                !ptx::mbar_wait_warp(&sm.q_empty[s], ((it / kQStages) - 1) & 1, abort_flag, status, kDevTimeoutEmpty))
+            if (!ptx::mbar_wait_warp(&sm.q_empty[it % kQStages], ((it / kQStages) - 1) & 1, abort_flag, status,
+                                     kDevTimeoutEmpty))
                 break;
-            if (lane == 0) {
-                ptx::mbar_arrive_expect_tx(&sm.q_full[s], 2 * kTileBytes + kQConstBytes);
-                ptx::bulk_load(sm.qconst[s], qsrc + i * (kTile / 2), kQConstBytes, &sm.q_full[s]);
-                ptx::tma_load_operand(sm.q[s], &tm_p1, &sm.q_full[s], 0, i * kTile, bh, head, batch,
-                                      kRank3);
-                ptx::tma_load_operand(sm.g[s], &tm_dy, &sm.q_full[s], 0, i * kTile, bh, head, batch,
-                                      kRank3);
-            }
+            if (lane == 0) issue_q(it);
         }
         if (lane == 0 && *abort_flag) {
             ptx::mbar_drain(&sm.kv_full, 0, status);
@@ -278,6 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t gm_lo0 = ptx::desc_lo(mdesc(ptx::smem_u32(sm.g[0])));
             const uint32_t sk_lo0 = ptx::desc_lo(kdesc(ptx::smem_u32(sm.ds[0])));
             const uint32_t sm_lo0 = ptx::desc_lo(mdesc(ptx::smem_u32(sm.ds[0])));
+            bool acc_committed = false;
             for (int it = 0; ok && it < n_q; ++it) {
                 const int s = it & 1;          // dS buffer
                 const int qs = it % kQStages;  // P1/dY stage
@@ -299,6 +307,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mma_ss_elect(tmem + kColDK, sk_lo + (ks >> 2) * kStageQ + 2 * (ks & 3), hi_k,
                                       qm_lo + 128 * ks, hi_m, id_dk, ks > 0 ? 1u : acc0);
                 ptx::mma_commit_elect(&sm.q_empty[qs]);  // this stream no longer reads P1_i, dY_i
+                if (it == n_q - 1) {
+                    ptx::mma_commit_elect(&sm.acc_done);  // dV and dP2 are final: the epilogue may start
+                    acc_committed = true;
+                }
                 // dP1_i = dS P2_j: A = dS (MN-major view of dS^T buffer s), K over key
                 // rows, into the partial's columns once the reduce warps drained the
                 // previous tile's.
@@ -312,6 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       ks > 0 ? 1u : 0u);
                 ptx::mma_commit_elect(&sm.dq_full);
             }
+            if (!acc_committed) ptx::mma_commit_elect(&sm.acc_done);  // left early: the epilogue's wait still ends
             ptx::mma_commit_elect(&sm.mma_done[1]);
             ptx::mbar_drain(&sm.mma_done[1], 0, status);
         }
@@ -430,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0 && dlam != 0.f) atomicAdd(dlambda, dlam / k_scale);
         }
         // Epilogue: blocks 0-1 write dV, blocks 2-3 write dP2, 32 columns each.
-        if (ok && ptx::mbar_wait_warp(&sm.mma_done[1], 0, abort_flag, status, kDevTimeoutMma)) {
+        if (ok && ptx::mbar_wait_warp(&sm.acc_done, 0, abort_flag, status, kDevTimeoutMma)) {
             ptx::tc_fence_after();
             const int c0 = blk & 1;
             __nv_bfloat16* dst_row = (blk < 2 ? dV : dP2) + row_offset(kp, bh, row_valid ? kv : 0);
@@ -534,7 +547,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        if (leader) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        // The staging panel must be read before the CTA's shared memory goes; the
+        // reduce-adds complete in global memory before the grid does.
+        if (leader) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -592,8 +607,8 @@ cudaError_t launch_bwd_tc64_t(const KernelProblem& kp, const void* P1, const voi
         if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&l2_bytes, cudaDevAttrL2CacheSize, dev);
     });
     const int64_t per_head = 12 * (int64_t)kp.T * kD;
-    int64_t group = (l2_bytes > 0 ? (int64_t)l2_bytes * 3 / 4 : (int64_t)96 << 20) / per_head;
-    group = group < 1 ? 1 : (group > kp.BH ? kp.BH : group);
+    const int64_t group =
+        balanced_head_group(kp.BH, (l2_bytes > 0 ? (int64_t)l2_bytes * 3 / 4 : (int64_t)96 << 20) / per_head);
     dim3 grid((unsigned)ctas);
 #define RELATION_BWD64(M)                                                                                        \
     relation_bwd_tc64_kernel<M, kPro><<<grid, kThreads, kSmemBytes, s>>>(                                        \

@@ -103,6 +103,16 @@ __host__ __device__ __forceinline__ void grouped_tile_order(unsigned idx, int64_
     bh = (int)(g * group) + (r - tile * heads);
 }
 
+// Heads per group for grouped_tile_order: at most `most` (what fits in L2), with
+// the groups as equal in size as possible.  A small last group would start its
+// longest key tiles only when the other groups' CTAs are nearly done, leaving the
+// rest of the GPU idle while they finish.
+inline int64_t balanced_head_group(int64_t BH, int64_t most) {
+    most = most < 1 ? 1 : (most > BH ? BH : most);
+    const int64_t groups = (BH + most - 1) / most;
+    return (BH + groups - 1) / groups;
+}
+
 // Records the first failure in the status word; never traps.
 __device__ __forceinline__ void record_status(unsigned int* status, unsigned int code) {
     if (status != nullptr) atomicCAS(status, 0u, code);
