@@ -309,6 +309,34 @@ __device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {
         "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
         : "memory");
 }
+// ------------------------------------------------------------- launch control
+// Asks the scheduler to cancel the launch of a CTA of this grid that has not
+// started yet, so that the caller can do its work instead.  The 16-byte answer
+// lands at `resp` (16-byte aligned shared memory) and completes `bar`, on which
+// the caller has announced 16 bytes of transaction.  Once an answer has
+// cancelled nothing, no further request may be made.
+__device__ __forceinline__ void clc_try_cancel(void* resp, uint64_t* bar) {
+    asm volatile("clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(
+                     smem_u32(resp)),
+                 "r"(smem_u32(bar))
+                 : "memory");
+}
+// Decodes an answer: the x index of the CTA it cancelled, or -1 if it cancelled none.
+__device__ __forceinline__ int clc_cancelled_x(const void* resp) {
+    uint64_t lo, hi;
+    asm volatile("ld.shared.v2.u64 {%0, %1}, [%2];" : "=l"(lo), "=l"(hi) : "r"(smem_u32(resp)) : "memory");
+    uint32_t x = 0, ok = 0;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b128 r;\n\t"
+        "mov.b128 r, {%2, %3};\n\t"
+        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+        "selp.u32 %1, 1, 0, p;\n\t"
+        "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %0, r;\n\t}"
+        : "+r"(x), "=r"(ok)
+        : "l"(lo), "l"(hi));
+    return ok ? (int)x : -1;
+}
+
 __device__ __forceinline__ uint32_t desc_lo(uint64_t d) { return (uint32_t)d; }
 __device__ __forceinline__ uint32_t desc_hi(uint64_t d) { return (uint32_t)(d >> 32); }
 
