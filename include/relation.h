@@ -196,6 +196,39 @@ relation_status_t relation_bwd_noalloc(const relation_problem_t* p, const void* 
                                        void* dP1, void* dP2, void* dV, float* dlambda, void* stream);
 
 /*
+ * One training step of the operator from and to HOST memory: relation_fwd
+ * then relation_bwd (eq.(1)-(3) and their chain rule) on inputs P1, P2, V and
+ * upstream dY held in host memory, with Y, dP1, dP2, dV (and L when not NULL)
+ * written to host memory and dlambda (a host float, may be NULL) set to the
+ * gradient summed over all heads.  The paper has no counterpart: this is the
+ * library's entry point for callers whose tensors live on the host.
+ * Heads are independent, so the batch is processed in `chunks` slices of
+ * B / chunks whole sequences (chunks must divide B).  Slice c+1 is copied in,
+ * and slice c-1 copied out, on two streams of the library's own while slice c
+ * is computed on `stream`.  So with page-locked (pinned) host buffers most of
+ * the host <-> device traffic overlaps the kernels; pageable buffers give the
+ * same results with the copies serialised.  Results equal relation_fwd's and
+ * relation_bwd's on the whole batch up to the order of floating-point
+ * accumulation (dP1's partial sums; dlambda's slice sums are added in slice
+ * order).
+ * Host tensors: the problem's layout and dtype, whole [B, ...] tensors, any
+ * alignment; inputs must not overlap outputs.  device_buffer: device memory
+ * of at least relation_step_host_device_bytes(p, chunks) bytes (0 = p or
+ * chunks unsupported), 16-byte aligned, owned by the caller, contents ignored.
+ * The call returns once the work is queued; `stream` (NULL: the legacy default
+ * stream) completes after all of it, so the host results are ready once that
+ * stream has been synchronised.  Enqueueing holds a per-device lock: calls from
+ * several threads are queued one after another.  On an error return, part of
+ * the work may already be queued: synchronise the device before reusing the
+ * buffers.
+ */
+size_t relation_step_host_device_bytes(const relation_problem_t* p, int chunks);
+relation_status_t relation_step_host(const relation_problem_t* p, const void* P1, const void* P2,
+                                     const void* V, const void* dY, void* Y, float* L, void* dP1,
+                                     void* dP2, void* dV, float* dlambda, int chunks,
+                                     void* device_buffer, size_t device_bytes, void* stream);
+
+/*
  * Relation Cache decoding (Sec. 5.3 eq.(18); Appendix A.5): one autoregressive
  * step for B*H heads.  The cache of a head holds the P2 rows and information
  * states I~ of the tokens already processed; only the new Relation row is

@@ -90,6 +90,11 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.relation_bwd_noalloc.argtypes = [ctypes.POINTER(Problem), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                              _VP]
         lib.relation_bwd_noalloc.restype = ctypes.c_int
+        lib.relation_step_host_device_bytes.argtypes = [ctypes.POINTER(Problem), ctypes.c_int]
+        lib.relation_step_host_device_bytes.restype = ctypes.c_size_t
+        lib.relation_step_host.argtypes = [ctypes.POINTER(Problem), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                           ctypes.c_int, _VP, ctypes.c_size_t, _VP]
+        lib.relation_step_host.restype = ctypes.c_int
         lib.relation_bwd_workspace_bytes.argtypes = [ctypes.POINTER(Problem)]
         lib.relation_bwd_workspace_bytes.restype = ctypes.c_size_t
         lib.relation_prologue_fwd.argtypes = [ctypes.POINTER(Problem), _VP, _VP, _VP, _VP, ctypes.c_int,
@@ -158,6 +163,16 @@ def _ptr(t) -> int | None:
         raise ValueError("Relation tensors must be CUDA tensors")
     if not t.is_contiguous():
         raise ValueError("Relation tensors must be contiguous [B, H, T, d_h]")
+    return t.data_ptr()
+
+
+def _host_ptr(t) -> int | None:
+    if t is None:
+        return None
+    if t.is_cuda:
+        raise ValueError("relation_step_host takes host tensors")
+    if not t.is_contiguous():
+        raise ValueError("Relation tensors must be contiguous")
     return t.data_ptr()
 
 
@@ -244,6 +259,20 @@ def relation_bwd_noalloc(prob, P1, P2, V, Y, L, dY, dP1, dP2, dV, dlambda, strea
     _check(load().relation_bwd_noalloc(ctypes.byref(prob), _ptr(P1), _ptr(P2), _ptr(V), _ptr(Y), _ptr(L), _ptr(dY),
                                        _ptr(dP1), _ptr(dP2), _ptr(dV), _ptr(dlambda), _stream_ptr(stream)),
            "relation_bwd_noalloc")
+
+
+def relation_step_host_device_bytes(prob: Problem, chunks: int) -> int:
+    return int(load().relation_step_host_device_bytes(ctypes.byref(prob), int(chunks)))
+
+
+def relation_step_host(prob, P1, P2, V, dY, Y, L, dP1, dP2, dV, dlambda, chunks, device_buffer, stream=None) -> None:
+    """Host tensors in and out (pinned for overlap); device_buffer a CUDA tensor of
+    relation_step_host_device_bytes(prob, chunks) bytes."""
+    _check(load().relation_step_host(ctypes.byref(prob), _host_ptr(P1), _host_ptr(P2), _host_ptr(V), _host_ptr(dY),
+                                     _host_ptr(Y), _host_ptr(L), _host_ptr(dP1), _host_ptr(dP2), _host_ptr(dV),
+                                     _host_ptr(dlambda), int(chunks), _ptr(device_buffer),
+                                     device_buffer.numel() * device_buffer.element_size(), _stream_ptr(stream)),
+           "relation_step_host")
 
 
 def relation_decode_workspace_bytes(prob: Problem) -> int:
@@ -447,6 +476,23 @@ def decode(P1_new, P2_new, V_new, P2_cache, V_cache, positions, tau_S: float, la
                                 device=P1_new.device)
     relation_decode(prob, P1_new, P2_new, V_new, P2_cache, V_cache, positions, append, Y, L, workspace, stream)
     return Y, L
+
+
+def step_host(P1, P2, V, dY, tau_S: float, lam: float, causal: bool = True, chunks: int = 1, out=None,
+              device_buffer=None, want_L: bool = False, stream=None, layout: int = RELATION_LAYOUT_BHTD):
+    """relation_step_host on host tensors; allocates what is not given (pinned host outputs,
+    the device buffer).  Returns (Y, L or None, dP1, dP2, dV, dlambda) as host tensors."""
+    prob = problem_for(P1, tau_S, lam, causal, layout)
+    if out is None:
+        out = tuple(torch.empty(P1.shape, dtype=P1.dtype).pin_memory() for _ in range(4))
+    Y, dP1, dP2, dV = out
+    L = torch.empty((prob.B, prob.H, prob.T), dtype=torch.float32).pin_memory() if want_L else None
+    dlam = torch.empty(1, dtype=torch.float32).pin_memory()
+    if device_buffer is None:
+        nbytes = relation_step_host_device_bytes(prob, chunks)
+        device_buffer = torch.empty((nbytes + 3) // 4, dtype=torch.float32, device="cuda")
+    relation_step_host(prob, P1, P2, V, dY, Y, L, dP1, dP2, dV, dlam, chunks, device_buffer, stream)
+    return Y, L, dP1, dP2, dV, dlam
 
 
 def bwd(P1, P2, V, Y, L, dY, tau_S: float, lam: float, causal: bool = True, stream=None, workspace=None,

@@ -87,6 +87,8 @@ cudaError_t launch_decode(const KernelProblem& kp, bool bf16, const void* P1n, c
 cudaError_t launch_pad_operands(const KernelProblem& kp, const void* const* src, void* const* dst, int n,
                                 int num_sms, cudaStream_t s);
 // dP1 accumulator [BH, T, dq_w] -> dP1 in the problem's layout and width.
+// *out = x[0] + ... + x[n-1] (one thread, index order).
+cudaError_t launch_sum_in_order(const float* x, int n, float* out, cudaStream_t s);
 cudaError_t launch_convert(const KernelProblem& kp, const float* src, int dq_w, void* dst, bool bf16, int num_sms,
                            cudaStream_t s);
 

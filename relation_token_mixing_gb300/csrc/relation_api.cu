@@ -321,12 +321,153 @@ relation_status_t run_finish(const BwdArgs& a, int* launches) {
     return st;
 }
 
+// ------------------------------------------------------------------ host step
+// relation_step_host: one training step from and to host memory, in slices of
+// whole sequences.  Per device it keeps two non-blocking streams (copies in,
+// copies out) and the events that order them against the compute stream; the
+// enqueueing of one call holds the device's lock.
+struct HostStepRes {
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t ev_in[2], ev_comp[2], ev_out[2], ev_start, ev_sum, ev_done;
+    bool ready = false;
+};
+constexpr int kHostStepDevices = 64;
+HostStepRes g_host_step[kHostStepDevices];
+std::mutex g_host_step_mu[kHostStepDevices];
+
+relation_status_t host_step_resources(int dev, HostStepRes** out) {
+    HostStepRes& h = g_host_step[dev];
+    if (!h.ready) {
+        if (cudaStreamCreateWithFlags(&h.in, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&h.out, cudaStreamNonBlocking) != cudaSuccess)
+            return RELATION_ERR_CUDA;
+        cudaEvent_t* evs[] = {&h.ev_in[0], &h.ev_in[1], &h.ev_comp[0], &h.ev_comp[1], &h.ev_out[0],
+                              &h.ev_out[1], &h.ev_start, &h.ev_sum, &h.ev_done};
+        for (cudaEvent_t* e : evs)
+            if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return RELATION_ERR_CUDA;
+        h.ready = true;
+    }
+    *out = &h;
+    return RELATION_OK;
+}
+
+// Device buffer of relation_step_host: two slots, each [P1 P2 V dY Y dP1 dP2 dV | L | backward
+// workspace | forward workspace] for one slice, then the slices' dlambda and their sum.
+struct HostStepLayout {
+    relation_problem_t ps;  // one slice: B / chunks sequences
+    size_t tb, lb, bws, fws, slot, total;
+};
+
+bool host_step_layout(const relation_problem_t* p, int chunks, HostStepLayout* l) {
+    if (check_problem(p) != RELATION_OK || chunks < 1 || p->B % chunks != 0) return false;
+    l->ps = *p;
+    l->ps.B = p->B / chunks;
+    if (!fwd_fits(&l->ps) || !bwd_fits(&l->ps)) return false;
+    l->tb = round_up(tensor_bytes(&l->ps), 256);
+    l->lb = round_up(rows_of(&l->ps) * sizeof(float), 256);
+    l->bws = round_up(workspace_layout(&l->ps, nullptr), 256);
+    l->fws = round_up(fwd_workspace_bytes(&l->ps), 256);
+    l->slot = 8 * l->tb + l->lb + l->bws + l->fws;
+    l->total = 2 * l->slot + round_up((size_t)(chunks + 1) * sizeof(float), 256);
+    return true;
+}
+
 }  // namespace
 }  // namespace relation
 
 using namespace relation;
 
 extern "C" {
+
+size_t relation_step_host_device_bytes(const relation_problem_t* p, int chunks) {
+    HostStepLayout l;
+    return host_step_layout(p, chunks, &l) ? l.total : 0;
+}
+
+relation_status_t relation_step_host(const relation_problem_t* p, const void* P1, const void* P2, const void* V,
+                                     const void* dY, void* Y, float* L, void* dP1, void* dP2, void* dV,
+                                     float* dlambda, int chunks, void* device_buffer, size_t device_bytes,
+                                     void* stream) {
+    relation_status_t st = check_problem(p);
+    if (st != RELATION_OK) return st;
+    if (chunks < 1 || p->B % chunks != 0) return RELATION_ERR_INVALID_ARGUMENT;
+    HostStepLayout l;
+    if (!host_step_layout(p, chunks, &l)) return RELATION_ERR_UNSUPPORTED;
+    const void* h_in[4] = {P1, P2, V, dY};
+    void* h_out[4] = {Y, dP1, dP2, dV};
+    for (const void* x : h_in)
+        if (x == nullptr) return RELATION_ERR_INVALID_ARGUMENT;
+    for (void* x : h_out)
+        if (x == nullptr) return RELATION_ERR_INVALID_ARGUMENT;
+    if (device_buffer == nullptr) return RELATION_ERR_INVALID_ARGUMENT;
+    if (!aligned16(device_buffer)) return RELATION_ERR_MISALIGNED;
+    if (device_bytes < l.total) return RELATION_ERR_WORKSPACE_TOO_SMALL;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kHostStepDevices) return RELATION_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_host_step_mu[dev]);
+    HostStepRes* r = nullptr;
+    if ((st = host_step_resources(dev, &r)) != RELATION_OK) return st;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t tbc = tensor_bytes(&l.ps), lbc = rows_of(&l.ps) * sizeof(float);  // one slice's bytes
+    char* base = static_cast<char*>(device_buffer);
+    // Slot k's tensors: 0 P1, 1 P2, 2 V, 3 dY, 4 Y, 5 dP1, 6 dP2, 7 dV; then L and the workspaces.
+    auto dt = [&](int slot, int k) -> void* { return base + slot * l.slot + k * l.tb; };
+    auto dl = [&](int slot) { return reinterpret_cast<float*>(base + slot * l.slot + 8 * l.tb); };
+    auto dbw = [&](int slot) -> void* { return base + slot * l.slot + 8 * l.tb + l.lb; };
+    auto dfw = [&](int slot) -> void* { return base + slot * l.slot + 8 * l.tb + l.lb + l.bws; };
+    float* dlam = reinterpret_cast<float*>(base + 2 * l.slot);  // per slice, then their sum
+#define RELATION_CK(x)                                      do {                                                        if ((x) != cudaSuccess) return RELATION_ERR_CUDA;     } while (0)
+    // Nothing starts before the work already queued on the caller's stream.
+    RELATION_CK(cudaEventRecord(r->ev_start, s));
+    RELATION_CK(cudaStreamWaitEvent(r->in, r->ev_start, 0));
+    RELATION_CK(cudaStreamWaitEvent(r->out, r->ev_start, 0));
+    int launches = 0;
+    for (int c = 0; c < chunks; ++c) {
+        const int slot = c & 1;
+        // In: slice c into its slot once slice c-2 has left it.
+        if (c >= 2) RELATION_CK(cudaStreamWaitEvent(r->in, r->ev_out[slot], 0));
+        for (int k = 0; k < 4; ++k)
+            RELATION_CK(cudaMemcpyAsync(dt(slot, k), static_cast<const char*>(h_in[k]) + (size_t)c * tbc, tbc,
+                                        cudaMemcpyHostToDevice, r->in));
+        RELATION_CK(cudaEventRecord(r->ev_in[slot], r->in));
+        // Compute on the caller's stream.
+        RELATION_CK(cudaStreamWaitEvent(s, r->ev_in[slot], 0));
+        if (c >= 2) RELATION_CK(cudaStreamWaitEvent(s, r->ev_out[slot], 0));
+        st = run_fwd(&l.ps, dt(slot, 0), dt(slot, 1), dt(slot, 2), dt(slot, 4), dl(slot), dfw(slot), l.fws, true, s);
+        if (st != RELATION_OK) return st;
+        launches += t_last_launches;
+        const BwdArgs a{&l.ps,       dt(slot, 0), dt(slot, 1), dt(slot, 2), dt(slot, 4), dl(slot),
+                        dt(slot, 3), dt(slot, 5), dt(slot, 6), dt(slot, 7), dlambda ? dlam + c : nullptr,
+                        dbw(slot),   l.bws,       s};
+        if ((st = check_bwd(a)) != RELATION_OK) return st;
+        if ((st = run_prepare(a, &launches)) != RELATION_OK) return st;
+        if ((st = run_main(a, &launches)) != RELATION_OK) return st;
+        if ((st = run_finish(a, &launches)) != RELATION_OK) return st;
+        RELATION_CK(cudaEventRecord(r->ev_comp[slot], s));
+        // Out: slice c's results while the next slice is computed.
+        RELATION_CK(cudaStreamWaitEvent(r->out, r->ev_comp[slot], 0));
+        for (int k = 0; k < 4; ++k)
+            RELATION_CK(cudaMemcpyAsync(static_cast<char*>(h_out[k]) + (size_t)c * tbc, dt(slot, 4 + k), tbc,
+                                        cudaMemcpyDeviceToHost, r->out));
+        if (L != nullptr)
+            RELATION_CK(cudaMemcpyAsync(reinterpret_cast<char*>(L) + (size_t)c * lbc, dl(slot), lbc,
+                                        cudaMemcpyDeviceToHost, r->out));
+        RELATION_CK(cudaEventRecord(r->ev_out[slot], r->out));
+    }
+    if (dlambda != nullptr) {
+        RELATION_CK(launch_sum_in_order(dlam, chunks, dlam + chunks, s));
+        ++launches;
+        RELATION_CK(cudaEventRecord(r->ev_sum, s));
+        RELATION_CK(cudaStreamWaitEvent(r->out, r->ev_sum, 0));
+        RELATION_CK(cudaMemcpyAsync(dlambda, dlam + chunks, sizeof(float), cudaMemcpyDeviceToHost, r->out));
+    }
+    // The caller's stream completes after every copy out.
+    RELATION_CK(cudaEventRecord(r->ev_done, r->out));
+    RELATION_CK(cudaStreamWaitEvent(s, r->ev_done, 0));
+#undef RELATION_CK
+    t_last_launches = launches;
+    return RELATION_OK;
+}
 
 relation_status_t relation_fwd(const relation_problem_t* p, const void* P1, const void* P2, const void* V, void* Y,
                                float* L, void* stream) {

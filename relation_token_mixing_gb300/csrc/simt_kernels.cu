@@ -646,6 +646,19 @@ cudaError_t launch_pad_operands(const KernelProblem& kp, const void* const* src,
     return cudaGetLastError();
 }
 
+// out = x[0] + ... + x[n-1], added in index order by one thread (n is a handful of
+// per-slice partial sums).
+__global__ void sum_in_order_kernel(const float* __restrict__ x, int n, float* __restrict__ out) {
+    float acc = 0.f;
+    for (int k = 0; k < n; ++k) acc += x[k];
+    *out = acc;
+}
+
+cudaError_t launch_sum_in_order(const float* x, int n, float* out, cudaStream_t s) {
+    sum_in_order_kernel<<<1, 1, 0, s>>>(x, n, out);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_convert(const KernelProblem& kp, const float* src, int dq_w, void* dst, bool bf16, int num_sms,
                            cudaStream_t s) {
     const int64_t n4 = kp.BH * (int64_t)kp.T * (kp.d / 4);  // d is a multiple of 4

@@ -256,3 +256,26 @@ def test_prologue_argument_checks(lib):
     assert f(ctypes.byref(p), A, 2 * A, 3 * A, None, 0, 1e4, None, 8 * A, 9 * A, 10 * A, None) == 1  # no theta
     assert f(ctypes.byref(p), A, 2 * A, 3 * A + 8, 4 * A, 0, 1e4, None, 8 * A, 9 * A, 10 * A, None) == 3
     assert f(ctypes.byref(p), A, 2 * A, 3 * A, 4 * A, 0, 1e4, None, A + 32, 9 * A, 10 * A, None) == 1  # P1 out over X1
+
+
+def test_step_host_sizes_and_checks(lib):
+    """relation_step_host: two slots of one slice's tensors (8 of them), L and backward workspace,
+    so the device buffer shrinks with more slices; chunks that do not divide B are refused, and
+    every call below fails its argument checks before any device call."""
+    p = _prob(B=4, H=2, T=100, d_h=64)
+    need = {c: rb.relation_step_host_device_bytes(p, c) for c in (1, 2, 4)}
+    for c, n in need.items():
+        ps = _prob(B=4 // c, H=2, T=100, d_h=64)
+        tb = (4 // c) * 2 * 100 * 64 * 2
+        assert n >= 2 * (8 * tb + (4 // c) * 2 * 100 * 4 + rb.relation_bwd_workspace_bytes(ps))
+    assert need[4] < need[2] < need[1]
+    assert rb.relation_step_host_device_bytes(p, 3) == 0
+    assert rb.relation_step_host_device_bytes(p, 0) == 0
+    host = [A * k for k in range(1, 11)]  # P1 P2 V dY Y L dP1 dP2 dV dlambda
+    buf = 64 * A
+    fn = lib.relation_step_host
+    assert fn(ctypes.byref(p), *host, 3, buf, need[1], None) == 1  # 3 does not divide B
+    assert fn(ctypes.byref(p), None, *host[1:], 1, buf, need[1], None) == 1
+    assert fn(ctypes.byref(p), *host, 1, None, need[1], None) == 1
+    assert fn(ctypes.byref(p), *host, 1, buf + 4, need[1], None) == 3
+    assert fn(ctypes.byref(p), *host, 2, buf, need[2] - 1, None) == 4
