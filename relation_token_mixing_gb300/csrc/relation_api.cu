@@ -328,7 +328,7 @@ relation_status_t run_finish(const BwdArgs& a, int* launches) {
 // enqueueing of one call holds the device's lock.
 struct HostStepRes {
     cudaStream_t in = nullptr, out = nullptr;
-    cudaEvent_t ev_in[2], ev_comp[2], ev_out[2], ev_start, ev_sum, ev_done;
+    cudaEvent_t ev_in[2], ev_dy[2], ev_fwd[2], ev_comp[2], ev_out[2], ev_start, ev_sum, ev_done;
     bool ready = false;
 };
 constexpr int kHostStepDevices = 64;
@@ -341,8 +341,9 @@ relation_status_t host_step_resources(int dev, HostStepRes** out) {
         if (cudaStreamCreateWithFlags(&h.in, cudaStreamNonBlocking) != cudaSuccess ||
             cudaStreamCreateWithFlags(&h.out, cudaStreamNonBlocking) != cudaSuccess)
             return RELATION_ERR_CUDA;
-        cudaEvent_t* evs[] = {&h.ev_in[0], &h.ev_in[1], &h.ev_comp[0], &h.ev_comp[1], &h.ev_out[0],
-                              &h.ev_out[1], &h.ev_start, &h.ev_sum, &h.ev_done};
+        cudaEvent_t* evs[] = {&h.ev_in[0],  &h.ev_in[1],   &h.ev_dy[0],   &h.ev_dy[1], &h.ev_fwd[0],
+                              &h.ev_fwd[1], &h.ev_comp[0], &h.ev_comp[1], &h.ev_out[0], &h.ev_out[1],
+                              &h.ev_start,  &h.ev_sum,     &h.ev_done};
         for (cudaEvent_t* e : evs)
             if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return RELATION_ERR_CUDA;
         h.ready = true;
@@ -424,18 +425,23 @@ relation_status_t relation_step_host(const relation_problem_t* p, const void* P1
     int launches = 0;
     for (int c = 0; c < chunks; ++c) {
         const int slot = c & 1;
-        // In: slice c into its slot once slice c-2 has left it.
+        // In: slice c into its slot once slice c-2 has left it; the forward's operands
+        // first, dY (needed by the backward only) after them.
         if (c >= 2) RELATION_CK(cudaStreamWaitEvent(r->in, r->ev_out[slot], 0));
-        for (int k = 0; k < 4; ++k)
+        for (int k = 0; k < 4; ++k) {
             RELATION_CK(cudaMemcpyAsync(dt(slot, k), static_cast<const char*>(h_in[k]) + (size_t)c * tbc, tbc,
                                         cudaMemcpyHostToDevice, r->in));
-        RELATION_CK(cudaEventRecord(r->ev_in[slot], r->in));
+            if (k == 2) RELATION_CK(cudaEventRecord(r->ev_in[slot], r->in));
+        }
+        RELATION_CK(cudaEventRecord(r->ev_dy[slot], r->in));
         // Compute on the caller's stream.
         RELATION_CK(cudaStreamWaitEvent(s, r->ev_in[slot], 0));
         if (c >= 2) RELATION_CK(cudaStreamWaitEvent(s, r->ev_out[slot], 0));
         st = run_fwd(&l.ps, dt(slot, 0), dt(slot, 1), dt(slot, 2), dt(slot, 4), dl(slot), dfw(slot), l.fws, true, s);
         if (st != RELATION_OK) return st;
         launches += t_last_launches;
+        RELATION_CK(cudaEventRecord(r->ev_fwd[slot], s));
+        RELATION_CK(cudaStreamWaitEvent(s, r->ev_dy[slot], 0));
         const BwdArgs a{&l.ps,       dt(slot, 0), dt(slot, 1), dt(slot, 2), dt(slot, 4), dl(slot),
                         dt(slot, 3), dt(slot, 5), dt(slot, 6), dt(slot, 7), dlambda ? dlam + c : nullptr,
                         dbw(slot),   l.bws,       s};
@@ -444,13 +450,17 @@ relation_status_t relation_step_host(const relation_problem_t* p, const void* P1
         if ((st = run_main(a, &launches)) != RELATION_OK) return st;
         if ((st = run_finish(a, &launches)) != RELATION_OK) return st;
         RELATION_CK(cudaEventRecord(r->ev_comp[slot], s));
-        // Out: slice c's results while the next slice is computed.
-        RELATION_CK(cudaStreamWaitEvent(r->out, r->ev_comp[slot], 0));
-        for (int k = 0; k < 4; ++k)
-            RELATION_CK(cudaMemcpyAsync(static_cast<char*>(h_out[k]) + (size_t)c * tbc, dt(slot, 4 + k), tbc,
-                                        cudaMemcpyDeviceToHost, r->out));
+        // Out: slice c's Y (and L) once its forward is done, its gradients once its
+        // backward is, while the next slice is computed.
+        RELATION_CK(cudaStreamWaitEvent(r->out, r->ev_fwd[slot], 0));
+        RELATION_CK(cudaMemcpyAsync(static_cast<char*>(h_out[0]) + (size_t)c * tbc, dt(slot, 4), tbc,
+                                    cudaMemcpyDeviceToHost, r->out));
         if (L != nullptr)
             RELATION_CK(cudaMemcpyAsync(reinterpret_cast<char*>(L) + (size_t)c * lbc, dl(slot), lbc,
+                                        cudaMemcpyDeviceToHost, r->out));
+        RELATION_CK(cudaStreamWaitEvent(r->out, r->ev_comp[slot], 0));
+        for (int k = 1; k < 4; ++k)
+            RELATION_CK(cudaMemcpyAsync(static_cast<char*>(h_out[k]) + (size_t)c * tbc, dt(slot, 4 + k), tbc,
                                         cudaMemcpyDeviceToHost, r->out));
         RELATION_CK(cudaEventRecord(r->ev_out[slot], r->out));
     }
