@@ -262,6 +262,7 @@ __global__ void __launch_bounds__(kThreads) decode_partial_kernel(
 // P1 row to every CTA, its P2 and I~ rows to CTA 0, which scores the Self entry
 // and appends the row to the cache row t (which no CTA reads).
 constexpr int kStreamStages = 3;
+constexpr int kEmptyStage = -2;    // a stage filled with a wrongly guessed chunk (scored as nothing)
 constexpr int kMaxCluster = 8;    // portable cluster size
 constexpr int kStreamMaxD = 128;  // widest head the streaming pass takes
 
@@ -295,11 +296,25 @@ __global__ void __launch_bounds__(kThreads, 2) decode_cluster_kernel(
     const int b = (int)(bh / kp.H);
     const int S = (int)gridDim.y, sidx = (int)blockIdx.y;  // cluster = the S CTAs of head bh
     const size_t new_off = (size_t)bh * d;                 // [B, H, d] new-row tensors
+    // The first stage is filled before the position is known, with the first chunk
+    // this CTA would take were the cache full (t = T-1, rows of the allocation only);
+    // once t is known, a wrong guess is consumed as an empty stage.
+    const int spec_n = (kp.T - 1 + ch - 1) / ch;  // chunks of a full cache
+    const int spec_c = sidx * ((spec_n + S - 1) / S);
+    const bool spec = spec_c < spec_n;
     if (threadIdx.x == 0) {
         for (int k = 0; k < kStreamStages; ++k) ptx::mbar_init(&full[k], 1);
         ptx::mbar_init(&new_full, 1);
         abort_flag = 0;
         ptx::fence_barrier_init();
+        if (spec) {
+            const int j0 = spec_c * ch;
+            const uint32_t bytes = (uint32_t)((min(kp.T - 1, j0 + ch) - j0) * row_bytes);
+            stage_chunk[0] = spec_c;
+            ptx::mbar_arrive_expect_tx(&full[0], 2 * bytes);
+            bulk_copy_g2s(smb, P2c + row_offset(kp, bh, j0), bytes, &full[0]);
+            bulk_copy_g2s(smb + (size_t)ch * row_bytes, Vc + row_offset(kp, bh, j0), bytes, &full[0]);
+        }
         ptx::mbar_arrive_expect_tx(&new_full, (uint32_t)row_bytes * (sidx == 0 ? 3u : 1u));
         bulk_copy_g2s(new_rows, P1n + new_off, (uint32_t)row_bytes, &new_full);
         if (sidx == 0) {
@@ -308,19 +323,28 @@ __global__ void __launch_bounds__(kThreads, 2) decode_cluster_kernel(
         }
     }
     const int t = pos[b];
-    __syncthreads();  // the barriers are initialised
-    if (t < 0 || t >= kp.T) {  // position outside the cache (the whole cluster returns): reported, not written
+    const bool t_ok = t >= 0 && t < kp.T;
+    const int n_all = t_ok ? (t + ch - 1) / ch : 0;  // chunks of cached rows
+    const int per = (n_all + S - 1) / S;
+    const int k0 = sidx * per;
+    const int nck = max(0, min(n_all, k0 + per) - k0);
+    // The guess is right when this CTA's first chunk is the one guessed (then the copy
+    // holds at least its rows); otherwise stage 0 is marked empty before anyone reads it.
+    const bool spec_ok = spec && nck > 0 && k0 == spec_c;
+    if (threadIdx.x == 0 && spec && !spec_ok) stage_chunk[0] = kEmptyStage;
+    __syncthreads();  // the barriers are initialised, stage 0's chunk is settled
+    if (!t_ok) {  // position outside the cache (the whole cluster returns): reported, not written
         if (threadIdx.x == 0) {
             if (sidx == 0) record_status(status, kDevBadPosition);
-            ptx::mbar_drain(&new_full, 0, status);  // the new rows land before the CTA's memory is released
+            // The copies land before the CTA's memory is released.
+            ptx::mbar_drain(&new_full, 0, status);
+            if (spec) ptx::mbar_drain(&full[0], 0, status);
         }
         return;
     }
     cluster_arrive_relaxed();  // this CTA has started; waited on before the first remote write
-    const int n_all = (t + ch - 1) / ch;  // chunks of cached rows
-    const int per = (n_all + S - 1) / S;
-    const int k0 = sidx * per;
-    const int nck = max(0, min(n_all, k0 + per) - k0);
+    // Fill f carries chunk k0 + f - lag (lag 1 after an empty stage 0), none past the share.
+    const int lag = (spec && !spec_ok) ? 1 : 0;
     // Thread 0 fills stage f % kStreamStages for the f-th time: chunk c, or none (c < 0).
     auto fill = [&](int f, int c) {
         const int st = f % kStreamStages;
@@ -337,9 +361,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_cluster_kernel(
         bulk_copy_g2s(dst, P2c + row_offset(kp, bh, j0), bytes, bar);
         bulk_copy_g2s(dst + (size_t)ch * row_bytes, Vc + row_offset(kp, bh, j0), bytes, bar);
     };
-    int fills = 0;  // thread 0: stage fills issued (fill f carries chunk k0 + f while f < nck)
+    auto chunk_of_fill = [&](int f) { return (f - lag >= 0 && f - lag < nck) ? k0 + f - lag : -1; };
+    int fills = spec ? 1 : 0;  // thread 0: stage fills issued (the guessed one included)
     if (threadIdx.x == 0)
-        for (; fills < kStreamStages; ++fills) fill(fills, fills < nck ? k0 + fills : -1);
+        for (; fills < kStreamStages; ++fills) fill(fills, chunk_of_fill(fills));
     const int grp = threadIdx.x / G, li = threadIdx.x % G;
     const int col = li * VEC;
     const bool active = col < d;
@@ -438,6 +463,14 @@ __global__ void __launch_bounds__(kThreads, 2) decode_cluster_kernel(
             break;
         }
         const int c = stage_chunk[st];
+        if (c == kEmptyStage) {  // a wrong guess: nothing to score, refill the stage
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                fill(fills, chunk_of_fill(fills));
+                ++fills;
+            }
+            continue;
+        }
         if (c < 0) break;  // the same in every thread
         const Tin* sK = reinterpret_cast<const Tin*>(smb + (size_t)st * stage_bytes);
         const Tin* sV = sK + (size_t)ch * d;
@@ -459,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_cluster_kernel(
         }
         __syncthreads();  // the stage is consumed: refill it
         if (threadIdx.x == 0) {
-            fill(fills, fills < nck ? k0 + fills : -1);
+            fill(fills, chunk_of_fill(fills));
             ++fills;
         }
     }
