@@ -217,8 +217,10 @@ relation_status_t relation_bwd_noalloc(const relation_problem_t* p, const void* 
  * chunks unsupported), 16-byte aligned, owned by the caller, contents ignored.
  * The call returns once the work is queued; `stream` (NULL: the legacy default
  * stream) completes after all of it, so the host results are ready once that
- * stream has been synchronised.  Enqueueing holds a per-device lock: calls from
- * several threads are queued one after another.  On an error return, part of
+ * stream has been synchronised.  Calls on one stream may reuse one device buffer
+ * back to back; a buffer passed to calls on different streams must be ordered by
+ * the caller (the second call's stream waiting for the first's).  Enqueueing holds
+ * a per-device lock: calls from several threads are queued one after another.  On an error return, part of
  * the work may already be queued: synchronise the device before reusing the
  * buffers.
  */
