@@ -11,8 +11,10 @@
 // With t = tanh(U/2):  s = (1 + t)/2 and SiLU'(U) = (1 + t + (U/2)(1 - t^2)) / 2,
 // so one MUFU tanh serves both SiLU (forward value) and its slope.
 //
-// One CTA = one head x one 128-row key tile; it walks the query tiles i that
-// see it.  Per query tile (everything transposed so key rows sit on TMEM lanes):
+// Work unit = one head x one 128-row key tile, walking the query tiles i that
+// see it; the grid has one CTA per unit, and a CTA goes on with the units of
+// CTAs not launched yet (launch control, below), so at most one CTA per SM runs
+// the grid.  Per query tile (everything transposed so key rows sit on TMEM lanes):
 //   S^T = P2_j P1_i^T, dP^T = V_j dY_i^T        (SS, two N = 64 halves each)
 //   elementwise: P^T -> TMEM (bf16), dS^T = dU^T/8 -> shared memory (bf16)
 //   dV  += P^T dY_i     (TS)
