@@ -50,6 +50,10 @@ constexpr int kPanelBytes = 128 * 128;
 constexpr int kStageBytes = kTile * 128;  // one dP1 staging panel: 128 rows x 32 fp32 columns
 constexpr int kStagePanels = 2;           // staging panels in flight
 constexpr float kLog2e = 1.4426950408889634f;
+// Register split after launch at 80 per thread (six warps per SM sub-partition):
+// load/MMA warpgroup 56, the four elementwise warpgroups 88, the dP1-reduce
+// warpgroup 56:  128*56 + 512*88 + 128*56 = 59392 <= 768*80.
+constexpr uint32_t kRegsControl = 56, kRegsElementwise = 88, kRegsReduce = 56;
 
 template <int D>
 struct BwdCfg {
@@ -145,6 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // -------------------------------------------------------------- loader
+        ptx::regs_dec<kRegsControl>();
         if (lane == 0) {
             ptx::tma_prefetch_desc(&tm_p1);
             ptx::tma_prefetch_desc(&tm_p2);
@@ -189,6 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------- MMA issuer
         // The whole warp runs the issue loop; one elected lane issues each MMA.
         // Descriptors are built once; a byte offset is added as offset >> 4.
+        ptx::regs_dec<kRegsControl>();
         const uint32_t id_nn = ptx::idesc_bf16(kTile, kTile, false, false);  // S^T, dP^T
         const uint32_t id_tb = ptx::idesc_bf16(kTile, D, false, true);       // dV, dP2 (B MN-major)
         const uint32_t id_dq = ptx::idesc_bf16(kTile, D, true, true);        // dP1 (A, B MN-major)
@@ -255,8 +261,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp < 4) {
         // warps 2-3: no role (they complete the first warpgroup)
+        ptx::regs_dec<kRegsControl>();
     } else if (warp < kReduceWarp0) {
         // --------------------------------------------------- elementwise stage
+        ptx::regs_inc<kRegsElementwise>();
         const int quarter = warp & 3;
         const int blk = (warp - 4) >> 2;    // query columns 32blk .. 32blk+31
         const int r = quarter * 32 + lane;  // key row within the tile
@@ -372,6 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Per query tile, four 32-column panels: TMEM -> swizzled shared staging
         // -> one TMA bulk reduce-add (fp32) into the accumulator; rows past T are
         // dropped by TMA.  TMEM is released once the last panel is in registers.
+        ptx::regs_dec<kRegsReduce>();
         const int quarter = warp & 3;
         const int rq = quarter * 32 + lane;  // query row within the tile
         const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
