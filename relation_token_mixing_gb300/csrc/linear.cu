@@ -268,16 +268,17 @@ struct Quarter {
 // KDA-style retention gate ("Ask Self, Ask Others", Sec. 5.2 eq.(16); Appendix
 // A.4.1) of one thread's channels c = 2 lane, 2 lane + 1 of head h:
 // g = -exp(A_log[h, c]) softplus(r + dt_bias[h, c]).  on == false: the loaded
-// values are g itself.
+// values are g itself.  The kernels take the gate as a template parameter, so
+// `on` is a compile-time constant and the ungated kernels carry none of it.
 struct GateCh {
     float2 na, db;  // -exp(A_log), dt_bias
     bool on;
 };
-template <class A>
+template <bool kGate, class A>
 __device__ __forceinline__ GateCh gate_channels(const A& a, int64_t bh, int lane) {
-    GateCh gc{make_float2(0.f, 0.f), make_float2(0.f, 0.f), a.gate_alog != nullptr};
+    GateCh gc{make_float2(0.f, 0.f), make_float2(0.f, 0.f), kGate};
     const int c = 2 * lane, d = a.kp.d;
-    if (gc.on && c < d) {
+    if (kGate && c < d) {
         const size_t o = (size_t)(bh % a.kp.H) * d + c;
         gc.na = make_float2(-expf(a.gate_alog[o]), -expf(a.gate_alog[o + 1]));
         gc.db = make_float2(a.gate_dtb[o], a.gate_dtb[o + 1]);
@@ -516,7 +517,7 @@ __device__ __forceinline__ void zero_group_smem(GroupSmem& gs) {
 
 // ------------------------------------------------------------------- kernels
 // One CTA (4 warps) per work item bh * nseg + segment.
-template <bool kVec16, bool kOut>
+template <bool kVec16, bool kOut, bool kGate>
 __device__ __forceinline__ void segment_pass(const Args& a) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     GroupSmem& gs = *reinterpret_cast<GroupSmem*>(smem_raw);
@@ -537,7 +538,7 @@ __device__ __forceinline__ void segment_pass(const Args& a) {
     float2 aseg = make_float2(1.f, 1.f);
     const int g = lane >> 2, t = lane & 3;
     const RowMap rm = row_map(kp, bh);
-    const GateCh gc = gate_channels(a, bh, lane);
+    const GateCh gc = gate_channels<kGate>(a, bh, lane);
     load_chunk<kVec16>(gs.st[0], a, rm, t_begin, warp, lane);
     for (int n = 0; n < nchunks; ++n) {
         Stage& s = gs.st[n & 1];
@@ -594,13 +595,13 @@ __device__ __forceinline__ void segment_pass(const Args& a) {
     }
 }
 
-template <bool kVec16>
+template <bool kVec16, bool kGate>
 __global__ void __launch_bounds__(kThreads, 4) linear_state_kernel(Args a) {
-    segment_pass<kVec16, false>(a);
+    segment_pass<kVec16, false, kGate>(a);
 }
-template <bool kVec16>
+template <bool kVec16, bool kGate>
 __global__ void __launch_bounds__(kThreads, 4) linear_fwd_kernel(Args a) {
-    segment_pass<kVec16, true>(a);
+    segment_pass<kVec16, true, kGate>(a);
 }
 
 // Entering state of every segment (in place of its own contribution) and the
@@ -808,7 +809,7 @@ __device__ __forceinline__ void level_dA(BwdSmem& gs, const BStage& s, int warp,
 }
 
 // ---- state passes of the backward (segment contributions of the reverse state)
-template <bool kVec16>
+template <bool kVec16, bool kGate>
 __global__ void __launch_bounds__(kThreads, 3) linear_bstate_kernel(BArgs a) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     BwdSmem& gs = *reinterpret_cast<BwdSmem*>(smem_raw);
@@ -826,7 +827,7 @@ __global__ void __launch_bounds__(kThreads, 3) linear_bstate_kernel(BArgs a) {
     State D;  // dC rows c = 16w + g (+8), columns v
     state_zero(D);
     const RowMap rm = row_map(kp, bh);
-    const GateCh gc = gate_channels(a, bh, lane);
+    const GateCh gc = gate_channels<kGate>(a, bh, lane);
     load_chunk_b<kVec16>(gs.st[(nchunks - 1) & 1], a, rm, t_begin + (nchunks - 1) * kC, warp, lane, false);
     for (int n = nchunks - 1; n >= 0; --n) {
         BStage& s = gs.st[n & 1];
@@ -896,7 +897,7 @@ __global__ void __launch_bounds__(256) linear_bscan_kernel(float* dcseg, const f
 }
 
 // ---- sweep A: forward in time, dq
-template <bool kVec16>
+template <bool kVec16, bool kGate>
 __global__ void __launch_bounds__(kThreads, 3) linear_bwd_a_kernel(BArgs a) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     BwdSmem& gs = *reinterpret_cast<BwdSmem*>(smem_raw);
@@ -925,7 +926,7 @@ __global__ void __launch_bounds__(kThreads, 3) linear_bwd_a_kernel(BArgs a) {
         state_zero(H);
     }
     const RowMap rm = row_map(kp, bh);
-    const GateCh gc = gate_channels(a, bh, lane);
+    const GateCh gc = gate_channels<kGate>(a, bh, lane);
     load_chunk_b<kVec16>(gs.st[0], a, rm, t_begin, warp, lane, true);
     for (int n = 0; n < nchunks; ++n) {
         BStage& s = gs.st[n & 1];
@@ -1031,7 +1032,7 @@ __global__ void __launch_bounds__(kThreads, 3) linear_bwd_a_kernel(BArgs a) {
 }
 
 // ---- sweep B: backward in time, dk, dv and the outputs
-template <bool kVec16>
+template <bool kVec16, bool kGate>
 __global__ void __launch_bounds__(kThreads, 3) linear_bwd_b_kernel(BArgs a) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     BwdSmem& gs = *reinterpret_cast<BwdSmem*>(smem_raw);
@@ -1075,7 +1076,7 @@ __global__ void __launch_bounds__(kThreads, 3) linear_bwd_b_kernel(BArgs a) {
     __syncthreads();
     float2 carry = *reinterpret_cast<const float2*>(gs.bnd + c);  // sum of z over the later tokens (+ boundary)
     const RowMap rm = row_map(kp, bh);
-    const GateCh gc = gate_channels(a, bh, lane);
+    const GateCh gc = gate_channels<kGate>(a, bh, lane);
     float2 acc_dalog = make_float2(0.f, 0.f), acc_ddtb = make_float2(0.f, 0.f);  // gate: this thread's token sums
     load_chunk_b<kVec16>(gs.st[(nchunks - 1) & 1], a, rm, t_begin + (nchunks - 1) * kC, warp, lane, true);
     for (int n = nchunks - 1; n >= 0; --n) {
@@ -1323,6 +1324,60 @@ int linear_segments(const KernelProblem& kp, int num_sms, int* seg_len) {
     return (kp.T + len - 1) / len;
 }
 
+namespace lin {
+// The launches of one direction for one (row width, gate) instantiation; each sets
+// its kernels' shared-memory limit once.
+template <bool kVec16, bool kGate>
+cudaError_t fwd_passes(const Args& a, float* state_out, cudaStream_t s) {
+    const size_t smem = sizeof(GroupSmem);
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaFuncSetAttribute(linear_fwd_kernel<kVec16, kGate>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(linear_state_kernel<kVec16, kGate>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+        attr_done = true;
+    }
+    const unsigned grid = (unsigned)(a.kp.BH * a.nseg);
+    const dim3 block(kThreads);
+    if (a.nseg > 1) {
+        linear_state_kernel<kVec16, kGate><<<grid, block, smem, s>>>(a);
+        linear_scan_kernel<<<(unsigned)a.kp.BH * 16, 256, 0, s>>>(a.hseg, a.aseg, a.nseg, state_out, a.kp.d);
+    }
+    linear_fwd_kernel<kVec16, kGate><<<grid, block, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <bool kVec16, bool kGate>
+cudaError_t bwd_passes(const Args& fa, const BArgs& b, bool reuse_fwd_states, cudaStream_t s) {
+    const size_t fsmem = sizeof(GroupSmem), bsmem = sizeof(BwdSmem);
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaFuncSetAttribute(linear_state_kernel<kVec16, kGate>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)fsmem);
+        cudaFuncSetAttribute(linear_bstate_kernel<kVec16, kGate>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)bsmem);
+        cudaFuncSetAttribute(linear_bwd_a_kernel<kVec16, kGate>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)bsmem);
+        cudaFuncSetAttribute(linear_bwd_b_kernel<kVec16, kGate>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)bsmem);
+        attr_done = true;
+    }
+    const unsigned grid = (unsigned)(b.kp.BH * b.nseg);
+    const dim3 block(kThreads);
+    if (fa.nseg > 1) {
+        if (!reuse_fwd_states) {
+            linear_state_kernel<kVec16, kGate><<<grid, block, fsmem, s>>>(fa);
+            linear_scan_kernel<<<(unsigned)fa.kp.BH * 16, 256, 0, s>>>(fa.hseg, fa.aseg, fa.nseg, nullptr, fa.kp.d);
+        }
+        linear_bstate_kernel<kVec16, kGate><<<grid, block, bsmem, s>>>(b);
+        linear_bscan_kernel<<<(unsigned)b.kp.BH * 16, 256, 0, s>>>(b.dcseg, b.aseg, b.nseg);
+    }
+    linear_bwd_a_kernel<kVec16, kGate><<<grid, block, bsmem, s>>>(b);
+    linear_bwd_b_kernel<kVec16, kGate><<<grid, block, bsmem, s>>>(b);
+    return cudaGetLastError();
+}
+}  // namespace lin
+
 cudaError_t launch_linear_fwd(const KernelProblem& kp, const void* P1, const void* P2, const void* V, const float* G,
                               void* Y, float* state_out, float* ws, int num_sms, cudaStream_t s, const float* gate_alog,
                               const float* gate_dtb) {
@@ -1340,31 +1395,10 @@ cudaError_t launch_linear_fwd(const KernelProblem& kp, const void* P1, const voi
     a.nseg = linear_segments(kp, num_sms, &a.seg_len);
     a.hseg = ws;
     a.aseg = ws + (size_t)kp.BH * a.nseg * lin::kDp * lin::kDp;
-    const size_t smem = sizeof(lin::GroupSmem);
-    const bool vec16 = (kp.d % 8) == 0;
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaFuncSetAttribute(lin::linear_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        cudaFuncSetAttribute(lin::linear_fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        cudaFuncSetAttribute(lin::linear_state_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        cudaFuncSetAttribute(lin::linear_state_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
-        attr_done = true;
-    }
-    const unsigned grid = (unsigned)(kp.BH * a.nseg);
-    const dim3 block(lin::kThreads);
-    if (a.nseg > 1) {
-        if (vec16)
-            lin::linear_state_kernel<true><<<grid, block, smem, s>>>(a);
-        else
-            lin::linear_state_kernel<false><<<grid, block, smem, s>>>(a);
-        lin::linear_scan_kernel<<<(unsigned)kp.BH * 16, 256, 0, s>>>(a.hseg, a.aseg, a.nseg, state_out, kp.d);
-    }
+    const bool vec16 = (kp.d % 8) == 0, gate = gate_alog != nullptr;
     if (vec16)
-        lin::linear_fwd_kernel<true><<<grid, block, smem, s>>>(a);
-    else
-        lin::linear_fwd_kernel<false><<<grid, block, smem, s>>>(a);
-    return cudaGetLastError();
+        return gate ? lin::fwd_passes<true, true>(a, state_out, s) : lin::fwd_passes<true, false>(a, state_out, s);
+    return gate ? lin::fwd_passes<false, true>(a, state_out, s) : lin::fwd_passes<false, false>(a, state_out, s);
 }
 
 cudaError_t launch_linear_bwd(const KernelProblem& kp, const void* P1, const void* P2, const void* V, const float* G,
@@ -1408,46 +1442,12 @@ cudaError_t launch_linear_bwd(const KernelProblem& kp, const void* P1, const voi
     b.zscale = fa.zscale;
     b.nseg = fa.nseg;
     b.seg_len = fa.seg_len;
-    const size_t fsmem = sizeof(lin::GroupSmem), bsmem = sizeof(lin::BwdSmem);
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaFuncSetAttribute(lin::linear_state_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsmem);
-        cudaFuncSetAttribute(lin::linear_state_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)fsmem);
-        cudaFuncSetAttribute(lin::linear_bstate_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bsmem);
-        cudaFuncSetAttribute(lin::linear_bstate_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)bsmem);
-        cudaFuncSetAttribute(lin::linear_bwd_a_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bsmem);
-        cudaFuncSetAttribute(lin::linear_bwd_a_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bsmem);
-        cudaFuncSetAttribute(lin::linear_bwd_b_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bsmem);
-        cudaFuncSetAttribute(lin::linear_bwd_b_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bsmem);
-        attr_done = true;
-    }
-    const unsigned grid = (unsigned)per_seg;
-    const dim3 block(lin::kThreads);
-    const bool vec16 = (kp.d % 8) == 0;
-    if (fa.nseg > 1) {
-        if (!reuse_fwd_states) {
-            if (vec16)
-                lin::linear_state_kernel<true><<<grid, block, fsmem, s>>>(fa);
-            else
-                lin::linear_state_kernel<false><<<grid, block, fsmem, s>>>(fa);
-            lin::linear_scan_kernel<<<(unsigned)kp.BH * 16, 256, 0, s>>>(fa.hseg, fa.aseg, fa.nseg, nullptr, kp.d);
-        }
-        if (vec16)
-            lin::linear_bstate_kernel<true><<<grid, block, bsmem, s>>>(b);
-        else
-            lin::linear_bstate_kernel<false><<<grid, block, bsmem, s>>>(b);
-        lin::linear_bscan_kernel<<<(unsigned)kp.BH * 16, 256, 0, s>>>(b.dcseg, b.aseg, b.nseg);
-    }
-    if (vec16) {
-        lin::linear_bwd_a_kernel<true><<<grid, block, bsmem, s>>>(b);
-        lin::linear_bwd_b_kernel<true><<<grid, block, bsmem, s>>>(b);
-    } else {
-        lin::linear_bwd_a_kernel<false><<<grid, block, bsmem, s>>>(b);
-        lin::linear_bwd_b_kernel<false><<<grid, block, bsmem, s>>>(b);
-    }
-    return cudaGetLastError();
+    const bool vec16 = (kp.d % 8) == 0, gate = gate_alog != nullptr;
+    if (vec16)
+        return gate ? lin::bwd_passes<true, true>(fa, b, reuse_fwd_states, s)
+                    : lin::bwd_passes<true, false>(fa, b, reuse_fwd_states, s);
+    return gate ? lin::bwd_passes<false, true>(fa, b, reuse_fwd_states, s)
+                : lin::bwd_passes<false, false>(fa, b, reuse_fwd_states, s);
 }
 
 }  // namespace relation
