@@ -24,6 +24,9 @@
 // Per key tile j, per query tile t:  S_t = Q_t K_j^T (SS MMA) -> softmax ->
 // P_t -> O_t += P_t V_j (TS MMA, P read from TMEM).  The two query tiles
 // alternate so the tensor core works on one while the other is in softmax.
+// At D = 128 their softmax warps also take turns on the special-function unit
+// (one mbarrier pair per sub-partition), so that one tile's tanh / ex2 loops
+// run while the other tile waits for its next S or stores P.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -82,9 +85,13 @@ struct FwdBarriers {
     uint64_t q_rot[2];
     uint64_t k_rot[4];
     uint64_t v_mix[4];
+    // Turns of the two query tiles' softmax warps on each sub-partition's
+    // special-function unit (one barrier per tile and warp quarter).
+    uint64_t turn[2][4];
     uint32_t tmem_base;
     int abort_flag;
 };
+static_assert(sizeof(FwdBarriers) <= 512, "the barriers' 512-byte region");
 
 __device__ __forceinline__ float as_f(uint32_t u) { return __uint_as_float(u); }
 __device__ __forceinline__ uint32_t as_u(float f) { return __float_as_uint(f); }
@@ -170,6 +177,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::mbar_init(&bars->drain, 1);
         for (int t = 0; t < 2; ++t) ptx::mbar_init(&bars->q_rot[t], 2);
+        if constexpr (!C::kSepP)
+            for (int t = 0; t < 2; ++t)
+                for (int q = 0; q < 4; ++q) ptx::mbar_init(&bars->turn[t][q], 1);
         for (int s = 0; s < C::kStages; ++s) {
             ptx::mbar_init(&bars->k_rot[s], 2);
             ptx::mbar_init(&bars->v_mix[s], 2);
@@ -442,6 +452,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float corr = kp.lambda * logf((float)count);    // lambda log c_i
         const int diag_tile = (q_base + t * kBM) / kBN;
         const int tail_cols = T - (n_kv_all - 1) * kBN;
+        // When P overwrites S (D = 128), a tile's next S is computed only after its
+        // transport product, so each step spends long stretches in TMEM traffic and
+        // waits.  There the warps of the two tiles that share a sub-partition take
+        // turns on its special-function unit for the first min(n_0, n_1) steps: tile
+        // 0's step j, then tile 1's step j, each running its tanh / ex2 loops while the
+        // other waits for S or stores P.  Tile 1's remaining steps run without turns.
+        // At D = 64 the next S is ready early and that stretch is short: one warp alone
+        // drives the unit at about three quarters of its rate, so the tiles share it.
+        const int n_pair = C::kSepP ? 0 : min(n_t[0], n_t[1]);
+        uint64_t* turn_mine = &bars->turn[t][quarter];
+        uint64_t* turn_next = &bars->turn[t ^ 1][quarter];
         float m = -INFINITY, l = 0.f;
         bool ok = nt > 0;
         for (int j = 0; ok && j < nt; ++j) {
@@ -460,6 +481,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // S(j) is in registers: the next S of this tile may overwrite it.
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(&bars->s_free[t]);
+            }
+            if constexpr (!C::kSepP) {
+                if (j < n_pair && j + t > 0 &&
+                    !ptx::mbar_wait_warp(turn_mine, (j + t - 1) & 1, abort_flag, status, kDevTimeoutMma)) {
+                    ok = false;
+                    break;
+                }
+                ptx::pin_regs(sv);  // the loops below start after the turn is taken
             }
             // sv[c] becomes R'_ic (natural units) in place, R' = R + lambda log c_i.
             const bool is_diag = (j == diag_tile);
@@ -519,6 +548,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float2 s01 = ptx::add2(ls[0], ls[1]), s23 = ptx::add2(ls[2], ls[3]);
                 const float2 st = ptx::add2(s01, s23);
                 l += st.x + st.y;
+            }
+            if constexpr (!C::kSepP) {
+                ptx::pin_regs(pk[0]);  // and end before it is passed on
+                ptx::pin_regs(pk[1]);
+                __syncwarp();
+                if (j < n_pair && lane == 0) ptx::mbar_arrive(turn_next);
             }
             if constexpr (C::kSepP) {
                 // P(j) replaces P(j-1) once the transport of block j-1 has read it (that
