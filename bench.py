@@ -98,13 +98,14 @@ def kernel_source_hash(names) -> str:
 
 def recorded_traffic(kernel: str, source_hash: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on this workload and
-    matches the current source."""
+    matches the current source.  A kernel captured on several workloads has one entry per extra
+    workload, keyed "<kernel> @ <workload>"."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         rec = json.load(f)
-    e = rec.get(kernel)
+    e = rec.get(f"{kernel} @ {workload}") or rec.get(kernel)
     if not e or e.get("source_hash") != source_hash or e.get("workload") != workload:
         return None
     return e.get("bytes_per_launch")

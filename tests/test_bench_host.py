@@ -35,9 +35,12 @@ def test_linear_bytes_per_head_token():
 def test_recorded_traffic_is_keyed_by_workload_and_source():
     with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
         rec = json.load(f)
-    for kernel, e in rec.items():
-        if kernel.startswith("_"):
+    for key, e in rec.items():
+        if key.startswith("_"):
             continue
+        kernel = key.split(" @ ")[0]
+        if " @ " in key:
+            assert key.split(" @ ")[1] == e["workload"]
         assert bench.recorded_traffic(kernel, e["source_hash"], e["workload"]) == e["bytes_per_launch"]
         assert bench.recorded_traffic(kernel, e["source_hash"], e["workload"] + "_other") is None
         assert bench.recorded_traffic(kernel, "0" * 16, e["workload"]) is None
