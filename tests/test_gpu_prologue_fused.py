@@ -4,7 +4,7 @@ B.3: RoPE on P1, P2; Sec. 3.2 eq.(4) and Appendix A.2.2-A.2.3: Givens head-pair
 mixing of the information states), against the float64 oracles composed in the same
 order: oracle.prologue (RoPE, Givens) then the Full Relation oracle.
 
-Tolerances are the operator's bf16 ones: Y <= 1e-2 * max|I~| (the benchmark spec's bf16 bound),
+Tolerances are the operator's bf16 ones: Y <= 1e-2 * max|I~| (the bf16 output bound),
 L <= 1e-3 * max(1, |L|).  The fused kernel rounds the rotated and mixed values to bf16
 once, as the standalone prologue does before the operator reads them, so it is also
 compared with that two-call chain on the GPU.
