@@ -279,3 +279,51 @@ def test_step_host_sizes_and_checks(lib):
     assert fn(ctypes.byref(p), *host, 1, None, need[1], None) == 1
     assert fn(ctypes.byref(p), *host, 1, buf + 4, need[1], None) == 3
     assert fn(ctypes.byref(p), *host, 2, buf, need[2] - 1, None) == 4
+
+
+def _declarations():
+    """(name, return type, parameter types) of every prototype in include/relation.h."""
+    import os
+    import re
+    path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "relation.h")
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    out = []
+    for m in re.finditer(r"^\s*((?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?)\s*(relation_[a-z0-9_]+)\s*\(([^)]*)\)\s*;",
+                         text, re.M):
+        body = m.group(3).strip()
+        params = [] if body in ("", "void") else [p.strip() for p in body.split(",")]
+        # drop the parameter name (the last identifier after the type), keep the type
+        types = [re.sub(r"\s*\b[A-Za-z_][A-Za-z0-9_]*$", "", p) if re.search(r"[\s*]\w+$", p) else p
+                 for p in params]
+        out.append((m.group(2), m.group(1).replace(" ", ""), types))
+    return out
+
+
+def _ctype_matches(c_type: str, ct) -> bool:
+    if "*" in c_type:
+        return ct is ctypes.c_void_p or ct is ctypes.c_char_p or hasattr(ct, "_type_") and issubclass(ct, ctypes._Pointer)
+    scalar = {"size_t": ctypes.c_size_t, "int": ctypes.c_int, "uint32_t": ctypes.c_uint32, "float": ctypes.c_float,
+              "double": ctypes.c_double, "relation_status_t": ctypes.c_int}
+    want = scalar.get(c_type.replace("const", "").strip())
+    return want is not None and ctypes.sizeof(ct) == ctypes.sizeof(want) and (
+        issubclass(ct, (ctypes.c_float, ctypes.c_double)) == issubclass(want, (ctypes.c_float, ctypes.c_double)))
+
+
+def test_binding_signatures_match_the_header(lib):
+    """Every entry point's ctypes argument list matches its prototype, position by position (a pointer where
+    the header has a pointer, an integer or float of the header's width elsewhere), and the return type's width
+    matches: a slip in the marshalling would otherwise pass wrong arguments silently."""
+    decls = _declarations()
+    assert len(decls) == len(rb.declared_symbols())
+    for name, ret, types in decls:
+        f = getattr(lib, name)
+        assert f.argtypes is not None, name
+        assert len(f.argtypes) == len(types), (name, len(f.argtypes), len(types))
+        for k, (c_type, ct) in enumerate(zip(types, f.argtypes)):
+            assert _ctype_matches(c_type, ct), (name, k, c_type, ct)
+        if ret == "constchar*":
+            assert f.restype is ctypes.c_char_p, name
+        else:
+            assert _ctype_matches(ret, f.restype), (name, ret, f.restype)
