@@ -327,3 +327,18 @@ def test_binding_signatures_match_the_header(lib):
             assert f.restype is ctypes.c_char_p, name
         else:
             assert _ctype_matches(ret, f.restype), (name, ret, f.restype)
+
+
+def test_binding_constants_match_the_header():
+    """Status codes, dtype and layout values and the ABI version in binding.py are the header's."""
+    import os
+    import re
+    path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "relation.h")
+    text = re.sub(r"/\*.*?\*/", "", open(path).read(), flags=re.S)
+    enum = {n: int(v) for n, v in re.findall(r"\b(RELATION_[A-Z0-9_]+)\s*=\s*(\d+)", text)}
+    status = {v: n for n, v in enum.items() if n == "RELATION_OK" or n.startswith("RELATION_ERR_")}
+    assert rb.STATUS == status
+    for name in ("RELATION_F32", "RELATION_BF16", "RELATION_LAYOUT_BHTD", "RELATION_LAYOUT_BTHD"):
+        assert getattr(rb, name) == enum[name], name
+    version = int(re.search(r"#define RELATION_ABI_VERSION (\d+)", text).group(1))
+    assert rb.relation_abi_version() == version
